@@ -1,0 +1,464 @@
+"""Benchmark of one DFlash draft-and-verify cycle on GB300.
+
+A step is one cycle over the batched workload (B = 32 sequences, cached
+context uniform in [1024, 8192], block 8, five draft layers, V = 262144, bf16,
+T = 1): context fusion of the cycle's bs new rows per sequence into every
+layer's cache, the five layers' block attention, and verification.  Inputs
+are seeded synthetic tensors resident in HBM; each step streams ~3.3 GB
+(more than the 129 MB L2).
+
+Prints one JSON line.  Arms:
+  (default)         the CUDA path (libdflash.so) on N GPUs, one process each,
+                    each rank its own batch (weak scaling, no collective on the
+                    data path); value = cycles/s of the whole job.
+  --impl reference  the CPU oracle timed on the host cores on a bounded sample
+                    of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "draft-verify cycles/sec at B=32 (tokens/sec and HBM GB/s as % of peak reported beside it)"
+UNIT = "cycles/s"
+ATTN_SRC = os.path.join(ROOT, "block_speculative_decoding_gb300", "csrc", "attn.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_main_batched.md")
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d["hbm_gbs"], d["bf16_tflops"], "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def env_rank():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def reduce_max_sum(elapsed_s: float, tokens: float, device):
+    """Max of the elapsed time and sum of the tokens over ranks (1 rank: identity)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return elapsed_s, tokens
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=device)
+    s = torch.tensor([tokens], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(s, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(s.item())
+
+
+def rank_config(rank: int, batch: int | None = None) -> workloads.CycleConfig:
+    """Each rank runs its own batch: same shapes, seed offset by the rank.
+    `batch` shrinks B (profiling runs of a smaller case only)."""
+    from dataclasses import replace
+    c = workloads.BATCHED
+    if batch is not None and batch != c.B:
+        c = replace(c, B=batch)
+    return replace(c, seed=c.seed + 100 * rank) if rank else c
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling in the background."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "--query-gpu=" + self.Q, "--format=csv,noheader,nounits",
+                                       "-i", str(gpu_index), "-lms", "100"], stdout=self.f,
+                                      stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return None
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+        self.f.flush()
+        self.f.seek(0)
+        rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.count(",") >= 8]
+        os.unlink(self.f.name)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def measured_traffic():
+    """Per-launch DRAM bytes of the attention kernel from the committed ncu
+    summary, or None if absent or taken on a different kernel source."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    text = open(TRAFFIC_FILE).read()
+    m = re.search(r"traffic_bytes_per_launch_full_size:\s*([0-9.eE+]+)", text)
+    h = re.search(r"attn\.cu sha256:\s*([0-9a-f]{64})", text)
+    if not m or not h:
+        return None
+    cur = hashlib.sha256(open(ATTN_SRC, "rb").read()).hexdigest()
+    return float(m.group(1)) if h.group(1) == cur else None
+
+
+# ----------------------------------------------------------------- inputs ---
+
+class Cycle:
+    """Device-resident inputs and preallocated outputs/workspaces of one rank."""
+
+    def __init__(self, cfg, device, temperature):
+        import block_speculative_decoding_gb300 as dfl
+        self.dfl = dfl
+        self.cfg, self.dev, self.T = cfg, device, temperature
+        self.seq = workloads.seq_lens(cfg, device)
+        self.k, self.v = workloads.cache(cfg, device)
+        self.w = workloads.weights(cfg, device)
+        self.M = cfg.B * cfg.bs
+        self.taps = workloads.taps(cfg, self.M, device)
+        self.cu = workloads.cu_rows([cfg.bs] * cfg.B, device)
+        self.blocks = [workloads.block(cfg, device, layer=l) for l in range(cfg.L)]
+        self.lt, self.ld = workloads.logits(cfg, device)
+        self.x = workloads.draft_tokens(self.ld, temperature, seed=cfg.seed + 7)
+        self.cache = dfl.KVCache(self.k, self.v, self.seq)
+        self.outs = [torch.empty_like(b[0]) for b in self.blocks]
+        self.acc = torch.empty(cfg.B, dtype=torch.int32, device=device)
+        self.tok = torch.empty(cfg.B, cfg.bs, dtype=torch.int32, device=device)
+        dt = dfl.BF16
+        self.ws_f = torch.empty(dfl.fuse_context_workspace_size(self.M, cfg.J, cfg.d_target, cfg.D, cfg.L, cfg.Hkv, dt),
+                                dtype=torch.uint8, device=device)
+        self.ws_a = torch.empty(dfl.block_attn_workspace_size(cfg.B, cfg.bs, cfg.Hq, cfg.Hkv, cfg.capacity, 0, dt),
+                                dtype=torch.uint8, device=device)
+        self.ws_v = torch.empty(dfl.verify_workspace_size(cfg.B, cfg.bs, cfg.V, dt), dtype=torch.uint8, device=device)
+        self.cycle = 0
+        s = self.seq.cpu().numpy().astype(np.int64)
+        self.attn_bytes_per_call = int(s.sum()) * cfg.Hkv * cfg.d * 2 * 2
+        self.verify_bytes = cfg.B * (2 * cfg.bs - 1) * cfg.V * 2
+        self.fuse_bytes = (self.w.w_fuse.numel() + self.w.w_kv.numel()) * 2 + self.M * cfg.J * cfg.d_target * 2 \
+            + self.M * cfg.L * 2 * cfg.Hkv * cfg.d * 2
+        self.fuse_flops = 2 * self.M * (cfg.J * cfg.d_target * cfg.D + cfg.D * cfg.L * 2 * cfg.Hkv * cfg.d)
+
+    def step(self, stream, ev=None, only="all"):
+        dfl, c = self.dfl, self.cfg
+        if ev is not None:
+            ev[0].record(stream)
+        if only in ("all", "fuse"):
+            dfl.fuse_context(self.taps, self.cu, self.w.w_fuse, self.w.g_fuse, self.w.w_kv, self.w.k_gain,
+                             self.cache, workspace=self.ws_f, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        if only in ("all", "attn"):
+            for l in range(c.L):
+                q, kb, vb = self.blocks[l]
+                dfl.block_attn(l, q, kb, vb, self.w.q_gain[l], self.w.k_gain[l], self.cache, out=self.outs[l],
+                               workspace=self.ws_a, stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+        if only in ("all", "verify"):
+            dfl.verify(self.lt, self.ld, self.x, self.T, 1234, self.cycle, accepted_len=self.acc,
+                       out_tokens=self.tok, workspace=self.ws_v, stream=stream)
+        if ev is not None:
+            ev[3].record(stream)
+        self.cycle += 1
+
+
+LAUNCHES_PER_STEP = 4 + 5 * 3 + 4   # fusion 4, block attention 3 per layer, verify 4 (T > 0)
+
+
+def run_gpu(args):
+    rank, world, local = env_rank()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from __graft_entry__ import build
+    if rank == 0:
+        build()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    build()
+    cfg = rank_config(rank, args.batch)
+    cyc = Cycle(cfg, dev, args.temperature)
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            cyc.step(stream, only=args.only)
+    torch.cuda.synchronize()
+    # tokens per cycle from this rank's verification outputs
+    tokens_per_cycle = float((cyc.acc.cpu() + 1).sum())
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        cyc.step(stream, evs[i], only=args.only)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    clk = clocks.stop()
+    elapsed = t0.elapsed_time(t1) / 1e3
+    fuse_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    attn_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs) / cfg.L
+    ver_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    elapsed_max, tokens_all = reduce_max_sum(elapsed, tokens_per_cycle * args.steps, dev)
+
+    if args.only != "all" or args.batch is not None:
+        if rank == 0:
+            print(json.dumps({"profiling_run": True, "only": args.only, "B": cfg.B, "steps": args.steps,
+                              "ms_per_step": elapsed * 1e3 / args.steps, "fuse_ms": fuse_ms,
+                              "attn_ms_per_layer": attn_ms, "verify_ms": ver_ms}), flush=True)
+        return
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(cyc, stream, args, dev)
+
+    if rank != 0:
+        return
+    hbm, tfl, src = peaks()
+    cycles = world * args.steps
+    attn_gbs = cyc.attn_bytes_per_call / (attn_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": cycles / elapsed_max, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": elapsed_max * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "batched: B=32, cached context uniform in [1024, 8192] (ragged), 5 draft layers, "
+                               "GQA 32/8, head 128, D=2560, block 8, V=262144, T=%g; per step: fusion of 8 new rows "
+                               "per sequence, 5 x block attention, verification" % args.temperature,
+                   "B": cfg.B, "block_size": cfg.bs, "vocab": cfg.V, "layers": cfg.L,
+                   "mean_context": float(cyc.seq.float().mean()), "parallelism": "dp%d (independent batches)" % world,
+                   "l2": "inputs larger than L2: %.2f GB streamed per step" % (
+                       (cfg.L * cyc.attn_bytes_per_call + cyc.verify_bytes + cyc.fuse_bytes) / 1e9)},
+        "tokens_per_sec": tokens_all / elapsed_max,
+        "mean_tokens_per_cycle": tokens_per_cycle / cfg.B,
+        "roofline": {"kernel": "block attention (prologue + split-KV main + combine), per layer call",
+                     "bound": "hbm", "achieved": attn_gbs, "peak": hbm, "unit": "GB/s",
+                     "frac": attn_gbs / hbm, "peak_source": src,
+                     "algorithmic_bytes_per_launch": cyc.attn_bytes_per_call,
+                     "traffic": measured_traffic()},
+        "components_ms": {"fuse_context": fuse_ms, "block_attn_per_layer": attn_ms, "verify": ver_ms},
+        "rooflines": {
+            "verify": {"bound": "hbm", "achieved": cyc.verify_bytes / (ver_ms * 1e-3) / 1e9, "peak": hbm,
+                       "unit": "GB/s", "frac": cyc.verify_bytes / (ver_ms * 1e-3) / 1e9 / hbm},
+            "fuse_context": {"bound": "hbm (M=%d: weight-bound)" % cyc.M,
+                             "achieved": cyc.fuse_bytes / (fuse_ms * 1e-3) / 1e9, "peak": hbm, "unit": "GB/s",
+                             "frac": cyc.fuse_bytes / (fuse_ms * 1e-3) / 1e9 / hbm,
+                             "tflops": cyc.fuse_flops / (fuse_ms * 1e-3) / 1e12}},
+        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "clocks": clk,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, args.cpu_seconds, args.temperature)
+    print(json.dumps(line), flush=True)
+
+
+def run_e2e(cyc, stream, args, dev):
+    """Same cycle through the public API with the step's inputs in pinned host
+    memory: H2D copies of the new context rows, block projections, logits and
+    draft tokens, then the calls, then D2H of the accepted lengths and tokens."""
+    host = {
+        "taps": [t.cpu().pin_memory() for t in cyc.taps],
+        "blocks": [[t.cpu().pin_memory() for t in b] for b in cyc.blocks],
+        "lt": cyc.lt.cpu().pin_memory(), "ld": cyc.ld.cpu().pin_memory(), "x": cyc.x.cpu().pin_memory(),
+    }
+    acc_h = torch.empty(cyc.cfg.B, dtype=torch.int32).pin_memory()
+    tok_h = torch.empty(cyc.cfg.B, cyc.cfg.bs, dtype=torch.int32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host["taps"]) + \
+        sum(t.numel() * t.element_size() for b in host["blocks"] for t in b) + \
+        sum(host[k].numel() * host[k].element_size() for k in ("lt", "ld", "x"))
+    d2h = acc_h.numel() * 4 + tok_h.numel() * 4
+
+    def step():
+        for d, h in zip(cyc.taps, host["taps"]):
+            d.copy_(h, non_blocking=True)
+        for db, hb in zip(cyc.blocks, host["blocks"]):
+            for d, h in zip(db, hb):
+                d.copy_(h, non_blocking=True)
+        cyc.lt.copy_(host["lt"], non_blocking=True)
+        cyc.ld.copy_(host["ld"], non_blocking=True)
+        cyc.x.copy_(host["x"], non_blocking=True)
+        cyc.step(stream)
+        acc_h.copy_(cyc.acc, non_blocking=True)
+        tok_h.copy_(cyc.tok, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, args.warmup)):
+            step()
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        n = max(1, min(args.steps, 50))
+        t0.record(stream)
+        for _ in range(n):
+            step()
+        t1.record(stream)
+        torch.cuda.synchronize()
+    el = t0.elapsed_time(t1) / 1e3
+    el, _ = reduce_max_sum(el, 0.0, dev)
+    _, world, _ = env_rank()
+    return {"value": world * n / el, "unit": UNIT, "steps": n, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h)}
+
+
+# ------------------------------------------------------------ CPU oracle ----
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return max(n)
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+def oracle_cycle_for(cfg, inputs, seqs, T):
+    """The oracle's full cycle for the sequences `seqs` of the batch."""
+    import oracle
+    w, seq, taps, blocks, lt, ld, x, k, v = inputs
+    rows = np.concatenate([np.arange(b * cfg.bs, (b + 1) * cfg.bs) for b in seqs])
+    pos = np.concatenate([seq[b] + np.arange(cfg.bs) for b in seqs])
+    oracle.fuse_rows([t[rows] for t in taps], w["w_fuse"], w["g_fuse"], w["w_kv"], w["k_gain"], pos, cfg.L,
+                     cfg.Hkv, cfg.d, bf16=True)
+    for l in range(cfg.L):
+        q, kb, vb = blocks[l]
+        oracle.block_attn(q[seqs], kb[seqs], vb[seqs], w["q_gain"][l], w["k_gain"][l], k[l][seqs], v[l][seqs],
+                          seq[seqs], bf16=True)
+    oracle.verify(lt[seqs], ld[seqs], x[seqs], T, 1234, 0, seq_ids=np.asarray(seqs))
+
+
+def oracle_inputs(cfg, T, seqs_needed):
+    """Host copies (float64) of the workload, restricted to the sampled sequences' data."""
+    f = lambda t: t.detach().to("cpu", torch.float64).numpy()  # noqa: E731
+    w = workloads.weights(cfg, "cpu")
+    wd = {"w_fuse": f(w.w_fuse), "g_fuse": f(w.g_fuse), "w_kv": f(w.w_kv), "k_gain": f(w.k_gain),
+          "q_gain": f(w.q_gain)}
+    seq = workloads.seq_lens(cfg).numpy()
+    taps = [f(t) for t in workloads.taps(cfg, cfg.B * cfg.bs, "cpu")]
+    blocks = [[f(t) for t in workloads.block(cfg, "cpu", layer=l)] for l in range(cfg.L)]
+    lt, ld = workloads.logits(cfg, "cpu")
+    x = workloads.draft_tokens(ld, T, seed=cfg.seed + 7).numpy()
+    nmax = int(seq[seqs_needed].max())
+    g = workloads.generator(cfg.seed * 1000 + 3, "cpu")
+    # cached K/V for the sampled sequences only (synthetic N(0,1), same shapes)
+    k = np.zeros((cfg.L, cfg.B, cfg.Hkv, nmax, cfg.d))
+    v = np.zeros_like(k)
+    for b in seqs_needed:
+        k[:, b] = torch.randn(cfg.L, cfg.Hkv, nmax, cfg.d, generator=g).to(torch.bfloat16).double().numpy()
+        v[:, b] = torch.randn(cfg.L, cfg.Hkv, nmax, cfg.d, generator=g).to(torch.bfloat16).double().numpy()
+    return wd, seq, taps, blocks, f(lt), f(ld), x, k, v
+
+
+def cpu_baseline(cfg, seconds, T):
+    """Oracle cycles/s on the host: whole cycles of as many sequences as fit in
+    `seconds`, scaled to the B-sequence batch."""
+    sample_max = 8
+    seqs_all = list(range(sample_max))
+    inputs = oracle_inputs(cfg, T, seqs_all)
+    t0 = time.perf_counter()
+    done = 0
+    for b in seqs_all:
+        oracle_cycle_for(cfg, inputs, [b], T)
+        done += 1
+        if time.perf_counter() - t0 > seconds:
+            break
+    el = time.perf_counter() - t0
+    per_cycle = el * cfg.B / done
+    return {"value": 1.0 / per_cycle, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+            "sample": "%d of %d sequences, each a full cycle (fusion of its 8 rows, 5 layers of block attention, "
+                      "verification), %.1f s, scaled x%g to the batch" % (done, cfg.B, el, cfg.B / done)}
+
+
+def run_reference(args):
+    rank, world, _ = env_rank()
+    if rank != 0:
+        return
+    cfg = workloads.BATCHED
+    seqs = list(range(min(cfg.B, max(args.steps, 1))))
+    inputs = oracle_inputs(cfg, args.temperature, list(range(min(cfg.B, 8))))
+    for i in range(args.warmup):
+        oracle_cycle_for(cfg, inputs, [i % 8], args.temperature)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle_cycle_for(cfg, inputs, [i % 8], args.temperature)
+    el = time.perf_counter() - t0
+    value = args.steps / cfg.B / el        # each step is 1/B of a cycle
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el * 1e3 / max(args.steps, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "batched: B=32, ragged context [1024, 8192], 5 layers, block 8, V=262144, T=%g"
+                       % args.temperature},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+                             "sample": "one sequence's full cycle per step (1/32 of a batch cycle)"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="dflash", choices=["dflash", "reference"])
+    ap.add_argument("--temperature", type=float, default=1.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--only", default="all", choices=["all", "fuse", "attn", "verify"],
+                    help="profiling runs: time one component of the cycle only")
+    ap.add_argument("--batch", type=int, default=None, help="profiling runs: smaller batch")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "dflash":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+    try:
+        import torch.distributed as dist
+        if dist.is_available() and dist.is_initialized():
+            dist.destroy_process_group()
+    except Exception:
+        pass
+
+
+if __name__ == "__main__":
+    main()

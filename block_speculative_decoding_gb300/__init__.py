@@ -1,0 +1,222 @@
+"""DFlash draft-and-verify hot path on GB300: Python binding of libdflash.so.
+
+Argument marshalling only.  Every step of the path runs in the CUDA kernels of
+libdflash.so (sm_103a); torch supplies device memory and streams.  If the
+library is missing this module raises on first use: there is no CPU fallback.
+
+Functions (same names as the C ABI in include/dflash.h, without the prefix):
+    fuse_context(taps, cu_new, w_fuse, g_fuse, w_kv, k_gain, cache, ...)
+    block_attn(layer, q, kb, vb, q_gain, k_gain, cache, ...)
+    verify(target_logits, draft_logits, draft_tokens, temperature, seed, cycle, ...)
+plus the *_workspace_size queries, philox4x32_10 and read_device_status.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+__all__ = [
+    "KVCache", "DFlashError", "lib", "fuse_context", "block_attn", "verify",
+    "fuse_context_workspace_size", "block_attn_workspace_size", "verify_workspace_size",
+    "philox4x32_10", "read_device_status", "version", "LIB_PATH",
+    "DEV_CAPACITY", "DEV_BAD_TOKEN", "DEV_BAD_SEQLEN", "DEV_TIMEOUT",
+]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdflash.so")
+
+F32, BF16 = 0, 1
+DEV_CAPACITY, DEV_BAD_TOKEN, DEV_BAD_SEQLEN, DEV_TIMEOUT = 1, 2, 4, 8
+_STATUS = {0: "OK", 1: "INVALID_ARGUMENT", 2: "UNSUPPORTED", 3: "CAPACITY", 4: "CUDA", 5: "WORKSPACE"}
+
+
+class DFlashError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__("dflash status %d (%s): %s" % (code, _STATUS.get(code, "?"), msg))
+        self.code = code
+
+
+class _KVCacheDesc(ctypes.Structure):
+    _fields_ = [
+        ("num_layers", ctypes.c_int), ("batch", ctypes.c_int), ("num_kv_heads", ctypes.c_int),
+        ("head_dim", ctypes.c_int), ("capacity", ctypes.c_int), ("dtype", ctypes.c_int),
+        ("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("seq_len", ctypes.c_void_p),
+    ]
+
+
+_lib = None
+
+
+def lib():
+    """Load libdflash.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError("libdflash.so is not built (%s); run __graft_entry__.build() or "
+                           "python -m block_speculative_decoding_gb300._build" % LIB_PATH)
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i32, sz, f32, u32, u64 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float,
+                                  ctypes.c_uint32, ctypes.c_uint64)
+    P = ctypes.POINTER
+    L.dflash_fuse_context_workspace_size.argtypes = [i32] * 6 + [i32]
+    L.dflash_fuse_context_workspace_size.restype = sz
+    L.dflash_fuse_context.argtypes = [i32, P(vp), i32, vp, i32, i32, vp, vp, i32, vp, vp, f32, f32,
+                                      P(_KVCacheDesc), vp, vp, sz, vp]
+    L.dflash_fuse_context.restype = i32
+    L.dflash_block_attn_workspace_size.argtypes = [i32] * 7
+    L.dflash_block_attn_workspace_size.restype = sz
+    L.dflash_block_attn.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, f32, f32,
+                                    P(_KVCacheDesc), i32, vp, vp, sz, vp]
+    L.dflash_block_attn.restype = i32
+    L.dflash_verify_workspace_size.argtypes = [i32] * 4
+    L.dflash_verify_workspace_size.restype = sz
+    L.dflash_verify.argtypes = [vp, vp, i32, vp, i32, i32, i32, f32, u64, u64, vp, vp, vp, sz, vp]
+    L.dflash_verify.restype = i32
+    L.dflash_philox4x32_10.argtypes = [vp, u32, u32, vp, i32, vp]
+    L.dflash_philox4x32_10.restype = i32
+    L.dflash_read_device_status.argtypes = [P(u32), vp]
+    L.dflash_read_device_status.restype = i32
+    L.dflash_last_error_string.argtypes = []
+    L.dflash_last_error_string.restype = ctypes.c_char_p
+    L.dflash_version.argtypes = []
+    L.dflash_version.restype = i32
+    _lib = L
+    return L
+
+
+def _check(code):
+    if code != 0:
+        raise DFlashError(code, lib().dflash_last_error_string().decode())
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError("dflash tensors must be bfloat16 or float32, got %s" % t.dtype)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("dflash tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _workspace(nbytes, device, ws):
+    if ws is not None:
+        if ws.numel() * ws.element_size() < nbytes:
+            raise ValueError("workspace too small: need %d bytes" % nbytes)
+        return ws
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+@dataclass
+class KVCache:
+    """Caller-owned draft cache: k, v [L, B, Hkv, cap, 128], seq_len int32 [B]."""
+    k: torch.Tensor
+    v: torch.Tensor
+    seq_len: torch.Tensor
+
+    def desc(self) -> _KVCacheDesc:
+        L, B, H, cap, d = self.k.shape
+        if self.seq_len.dtype != torch.int32:
+            raise TypeError("seq_len must be int32")
+        return _KVCacheDesc(L, B, H, d, cap, _dt(self.k), self.k.data_ptr(), self.v.data_ptr(),
+                            self.seq_len.data_ptr())
+
+
+def version() -> int:
+    return lib().dflash_version()
+
+
+def fuse_context_workspace_size(total_new, num_taps, d_target, d_model, num_layers, num_kv_heads, dtype):
+    return lib().dflash_fuse_context_workspace_size(total_new, num_taps, d_target, d_model, num_layers,
+                                                    num_kv_heads, dtype)
+
+
+def block_attn_workspace_size(batch, block_size, num_q_heads, num_kv_heads, capacity, window, dtype):
+    return lib().dflash_block_attn_workspace_size(batch, block_size, num_q_heads, num_kv_heads, capacity,
+                                                  window, dtype)
+
+
+def verify_workspace_size(batch, block_size, vocab, dtype):
+    return lib().dflash_verify_workspace_size(batch, block_size, vocab, dtype)
+
+
+def fuse_context(taps, cu_new, w_fuse, g_fuse, w_kv, k_gain, cache: KVCache, rope_theta=1e6, eps=1e-6,
+                 h_t_out=None, workspace=None, stream=None):
+    """Fuse J tap tensors [M, d_t] and append K/V rows to every layer of `cache`."""
+    J = len(taps)
+    M, d_t = taps[0].shape
+    D = w_fuse.shape[0]
+    L, B, Hkv = cache.k.shape[:3]
+    dt = _dt(taps[0])
+    nbytes = fuse_context_workspace_size(M, J, d_t, D, L, Hkv, dt)
+    ws = _workspace(nbytes, taps[0].device, workspace)
+    arr = (ctypes.c_void_p * J)(*[t.data_ptr() for t in taps])
+    for t in taps:
+        _ptr(t)
+    desc = cache.desc()
+    _check(lib().dflash_fuse_context(J, arr, d_t, _ptr(cu_new), B, M, _ptr(w_fuse), _ptr(g_fuse), D,
+                                     _ptr(w_kv), _ptr(k_gain), rope_theta, eps, ctypes.byref(desc),
+                                     _ptr(h_t_out), _ptr(ws), nbytes, _stream(stream)))
+    return h_t_out
+
+
+def block_attn(layer, q, kb, vb, q_gain, k_gain, cache: KVCache, window=0, rope_theta=1e6, eps=1e-6,
+               out=None, workspace=None, stream=None):
+    """One layer's non-causal block attention; returns out [B, Hq, bs, 128]."""
+    B, Hq, bs, d = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    desc = cache.desc()
+    nbytes = block_attn_workspace_size(B, bs, Hq, desc.num_kv_heads, desc.capacity, window, desc.dtype)
+    ws = _workspace(nbytes, q.device, workspace)
+    _check(lib().dflash_block_attn(layer, B, bs, Hq, _ptr(q), _ptr(kb), _ptr(vb), _ptr(q_gain),
+                                   _ptr(k_gain), rope_theta, eps, ctypes.byref(desc), window, _ptr(out),
+                                   _ptr(ws), nbytes, _stream(stream)))
+    return out
+
+
+def verify(target_logits, draft_logits, draft_tokens, temperature, seed, cycle, accepted_len=None,
+           out_tokens=None, workspace=None, stream=None):
+    """Exact speculative verification; returns (accepted_len [B], out_tokens [B, bs])."""
+    B, bs, V = target_logits.shape
+    dev = target_logits.device
+    if accepted_len is None:
+        accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty(B, bs, dtype=torch.int32, device=dev)
+    dt = _dt(target_logits)
+    nbytes = verify_workspace_size(B, bs, V, dt)
+    ws = _workspace(nbytes, dev, workspace)
+    _check(lib().dflash_verify(_ptr(target_logits), _ptr(draft_logits), dt, _ptr(draft_tokens), B, bs, V,
+                               float(temperature), int(seed), int(cycle), _ptr(accepted_len),
+                               _ptr(out_tokens), _ptr(ws), nbytes, _stream(stream)))
+    return accepted_len, out_tokens
+
+
+def philox4x32_10(ctr: torch.Tensor, key0: int, key1: int, stream=None) -> torch.Tensor:
+    """Philox-4x32-10 of int32 counters ctr [n, 4] (bit patterns) on the GPU."""
+    out = torch.empty_like(ctr)
+    _check(lib().dflash_philox4x32_10(_ptr(ctr), key0 & 0xFFFFFFFF, key1 & 0xFFFFFFFF, _ptr(out),
+                                      ctr.shape[0], _stream(stream)))
+    return out
+
+
+def read_device_status(stream=None) -> int:
+    """Synchronise, return and clear the library's device status bits."""
+    v = ctypes.c_uint32(0)
+    _check(lib().dflash_read_device_status(ctypes.byref(v), _stream(stream)))
+    return int(v.value)

@@ -1,0 +1,76 @@
+// Host-side declarations shared by the translation units of libdflash.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include <string>
+
+#include "../../include/dflash.h"
+
+namespace dflash {
+
+// --- errors ----------------------------------------------------------------
+void set_error(const std::string& msg);
+dflash_status fail(dflash_status code, const std::string& msg);
+dflash_status cuda_fail(cudaError_t err, const char* what);
+
+// --- device facts, cached per device --------------------------------------
+struct DeviceInfo {
+  int device = -1;
+  int num_sms = 0;
+  size_t max_smem_optin = 0;
+  unsigned* status = nullptr;  // address of the library's device status word
+};
+dflash_status device_info(DeviceInfo* out);
+
+// --- TMA descriptors --------------------------------------------------------
+// 2D row-major bf16 tensor [rows][cols] with a (box_cols x box_rows) box and
+// the 128-byte swizzle (box_cols * 2 must be 128).  Out-of-range rows read 0.
+dflash_status make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                                uint32_t box_rows, uint32_t box_cols);
+
+// Workspace carving: 256-byte aligned sub-buffers.
+struct WsCarver {
+  uintptr_t base;
+  size_t used = 0;
+  explicit WsCarver(void* p) : base(reinterpret_cast<uintptr_t>(p)) {}
+  template <typename T>
+  T* take(size_t count) {
+    used = (used + 255) & ~size_t(255);
+    T* p = reinterpret_cast<T*>(base + used);
+    used += count * sizeof(T);
+    return p;
+  }
+};
+
+inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+// --- verify ------------------------------------------------------------------
+size_t verify_ws_bytes(int B, int bs, int V);
+dflash_status launch_verify(const void* lt, const void* ld, dflash_dtype dt, const int32_t* x, int B,
+                            int bs, int V, float T, uint64_t seed, uint64_t cycle, int32_t* acc,
+                            int32_t* out, void* ws, cudaStream_t st, const DeviceInfo& dev);
+
+// --- block attention ---------------------------------------------------------
+size_t attn_ws_bytes(int B, int bs, int Hq, int Hkv, int cap, int window, dflash_dtype dt);
+dflash_status launch_block_attn(int layer, int B, int bs, int Hq, const void* q, const void* kb,
+                                const void* vb, const void* qg, const void* kg, float theta,
+                                float eps, const dflash_kv_cache& c, int window, void* out, void* ws,
+                                cudaStream_t st, const DeviceInfo& dev);
+
+// --- context fusion ----------------------------------------------------------
+size_t fuse_ws_bytes(int M, int J, int dt_width, int D, int L, int Hkv, dflash_dtype dt);
+dflash_status launch_fuse_context(int J, const void* const* taps, int dt_width, const int32_t* cu_new,
+                                  int B, int M, const void* w_fuse, const void* g_fuse, int D,
+                                  const void* w_kv, const void* k_gain, float theta, float eps,
+                                  const dflash_kv_cache& c, void* h_t_out, void* ws,
+                                  cudaStream_t st, const DeviceInfo& dev);
+
+// --- diagnostics --------------------------------------------------------------
+dflash_status launch_philox(const uint32_t* ctr, uint32_t k0, uint32_t k1, uint32_t* out, int n,
+                            cudaStream_t st);
+
+}  // namespace dflash

@@ -1,0 +1,610 @@
+// Context fusion and K/V injection into the draft cache.
+//
+// Pages: "Nemotron 3.5 Bolt E4B: Block-Parallel Speculation with DFlash",
+// section "Five target states become persistent draft context" (concatenate
+// the five captured target states on the feature axis, project them back to
+// the draft width, project that into K/V entries inserted into every draft
+// layer's cache; the K/V projections of all layers may run as one matrix
+// multiplication); "DFlash & DFlash2: Block-Diffusion LLM-Speedup" 4.1
+// (H_t = RMSNorm(W_c [H^(l1); ...; H^(l5)]), K_i = W_i^K H_t, V_i = W_i^V H_t).
+//
+// bf16 path, three launches after a small row-map kernel:
+//   1. gemm_tc (fusion)  Y = [taps] W_c^T on tcgen05 tensor cores: TMA loads of
+//      128x64 A tiles (taken from the tap that owns the K block -- the concat is
+//      never materialised) and BNx64 W_c tiles into a 4-stage ring, one thread
+//      issues tcgen05.mma (M=128, N=BN, K=16) into a double-buffered TMEM
+//      accumulator, four epilogue warps drain it.  Small M uses split-K; the
+//      fp32 partial sums stay in the workspace.
+//   2. rmsnorm           H_t = bf16(sum_splits(Y) * rsqrt(mean(Y^2) + eps) * g)
+//   3. gemm_tc (K/V)     [K|V] = H_t W_kv^T with a fused epilogue: every
+//      128-column head of a K projection is RMS-normalised (gain k_gain[l]) and
+//      rotated at its cache position, V heads are copied, and both are stored
+//      as bf16 rows of the cache.
+// fp32 path: the same steps as plain SIMT kernels (parity path).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+
+#include "dflash_device.cuh"
+#include "dflash_internal.h"
+
+namespace dflash {
+namespace {
+
+constexpr int HD = 128;
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+constexpr int kGemmThreads = 192;  // warp 0: TMA producer, warp 1: MMA issuer, warps 2-5: epilogue
+constexpr int kMaxSeg = 8;
+constexpr double kTwoPi = 6.283185307179586476925286766559;
+constexpr int kSplitTarget = 148;  // work units aimed for when splitting K
+
+struct InvFreq {
+  double v[HD / 2];
+};
+
+struct TmapPack {
+  CUtensorMap a[kMaxSeg];
+};
+
+struct GemmArgs {
+  int M, N, num_kb, kb_per_seg, k_splits, m_tiles, n_tiles;
+  int epi;                 // 0: fp32 partial store, 1: K/V cache epilogue
+  float* out_f32;          // epi 0: [k_splits][M][N]
+  __nv_bfloat16* cache_k;  // epi 1
+  __nv_bfloat16* cache_v;
+  int L, Bc, Hkv, cap;
+  const int2* rowinfo;     // [M] (sequence, position) or (-1, -1)
+  const float2* rope_cs;   // [M][64] (cos, sin)
+  const __nv_bfloat16* k_gain;  // [L][128] or null
+  float eps;
+  unsigned* status;
+};
+
+template <int BN>
+__host__ __device__ constexpr int stage_bytes() {
+  return kBM * kBK * 2 + BN * kBK * 2;
+}
+
+template <int BN, int STAGES>
+constexpr size_t gemm_smem_bytes() {
+  return 1024 + static_cast<size_t>(STAGES) * stage_bytes<BN>() + 8 * (2 * STAGES + 4) + 16;
+}
+
+__device__ __forceinline__ void unit_coords(int u, const GemmArgs& p, int& m, int& n, int& kb0, int& kb1,
+                                            int& ks) {
+  n = u % p.n_tiles;
+  m = (u / p.n_tiles) % p.m_tiles;
+  ks = u / (p.n_tiles * p.m_tiles);
+  kb0 = static_cast<int>((static_cast<long>(ks) * p.num_kb) / p.k_splits);
+  kb1 = static_cast<int>((static_cast<long>(ks + 1) * p.num_kb) / p.k_splits);
+}
+
+// Epilogue of one 128-column head of the K/V projection for this thread's row.
+__device__ __forceinline__ void kv_head_epilogue(uint32_t taddr, int col0, int row, const GemmArgs& p) {
+  const int hidx = col0 / HD;
+  const int l = hidx / (2 * p.Hkv);
+  const int s = (hidx / p.Hkv) % 2;
+  const int h = hidx % p.Hkv;
+  int2 ri = make_int2(-1, -1);
+  if (row < p.M) ri = p.rowinfo[row];
+  const bool valid = ri.x >= 0;
+  __nv_bfloat16* dst = (s == 0 ? p.cache_k : p.cache_v) +
+                       ((((static_cast<size_t>(l) * p.Bc + (valid ? ri.x : 0)) * p.Hkv + h) * p.cap) +
+                        (valid ? ri.y : 0)) * HD;
+  uint32_t r[32];
+  if (s == 1) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      tmem_ld_32cols(taddr + c * 32, r);
+      tmem_ld_wait();
+      if (valid) {
+        uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          d4[i] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * i]), __uint_as_float(r[8 * i + 1])),
+                             pack_bf16x2(__uint_as_float(r[8 * i + 2]), __uint_as_float(r[8 * i + 3])),
+                             pack_bf16x2(__uint_as_float(r[8 * i + 4]), __uint_as_float(r[8 * i + 5])),
+                             pack_bf16x2(__uint_as_float(r[8 * i + 6]), __uint_as_float(r[8 * i + 7])));
+      }
+    }
+    return;
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    tmem_ld_32cols(taddr + c * 32, r);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float v = __uint_as_float(r[i]);
+      ss += v * v;
+    }
+  }
+  const float rinv = rsqrtf(ss * (1.0f / HD) + p.eps);
+  const __nv_bfloat16* kg = p.k_gain ? p.k_gain + l * HD : nullptr;
+  const float2* cs = p.rope_cs + static_cast<size_t>(valid ? row : 0) * (HD / 2);
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const int e0 = half * 32;
+    uint32_t r2[32];
+    tmem_ld_32cols(taddr + e0, r);
+    tmem_ld_32cols(taddr + 64 + e0, r2);
+    tmem_ld_wait();
+    uint32_t o1[16], o2[16];
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+      float a[2], b[2];
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int e = e0 + i + k;
+        const float g1 = kg ? __bfloat162float(kg[e]) : 1.f;
+        const float g2 = kg ? __bfloat162float(kg[e + 64]) : 1.f;
+        const float y1 = __uint_as_float(r[i + k]) * rinv * g1;
+        const float y2 = __uint_as_float(r2[i + k]) * rinv * g2;
+        const float2 c = valid ? cs[e] : make_float2(1.f, 0.f);
+        a[k] = y1 * c.x - y2 * c.y;
+        b[k] = y2 * c.x + y1 * c.y;
+      }
+      o1[i / 2] = pack_bf16x2(a[0], a[1]);
+      o2[i / 2] = pack_bf16x2(b[0], b[1]);
+    }
+    if (valid) {
+      uint4* d1 = reinterpret_cast<uint4*>(dst + e0);
+      uint4* d2 = reinterpret_cast<uint4*>(dst + 64 + e0);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        d1[i] = make_uint4(o1[4 * i], o1[4 * i + 1], o1[4 * i + 2], o1[4 * i + 3]);
+        d2[i] = make_uint4(o2[4 * i], o2[4 * i + 1], o2[4 * i + 2], o2[4 * i + 3]);
+      }
+    }
+  }
+}
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_constant__ TmapPack amaps,
+                                                                  const __grid_constant__ CUtensorMap bmap,
+                                                                  const GemmArgs p) {
+  constexpr int A_BYTES = kBM * kBK * 2;
+  constexpr int STAGE = stage_bytes<BN>();
+  constexpr uint32_t IDESC = umma_idesc_bf16(kBM, BN);
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + STAGES * STAGE);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 4);
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = full0 + 8 * STAGES;
+  const uint32_t tfull0 = empty0 + 8 * STAGES;
+  const uint32_t tempty0 = tfull0 + 16;
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull0 + 8 * a, 1);
+      mbar_init(tempty0 + 8 * a, 4);
+    }
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 2 * BN);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total = p.m_tiles * p.n_tiles * p.k_splits;
+
+  if (warp == 0) {
+    if (lane == 0) {  // ------------------------------ TMA producer
+      for (int s = 0; s < kMaxSeg; ++s)
+        if (s * p.kb_per_seg < p.num_kb) tma_prefetch_desc(&amaps.a[s]);
+      tma_prefetch_desc(&bmap);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+        int m, n, kb0, kb1, ks;
+        unit_coords(u, p, m, n, kb0, kb1, ks);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!(ok = mbar_wait(empty0 + 8 * stage, phase ^ 1u, p.status))) break;
+          const uint32_t fb = full0 + 8 * stage;
+          mbar_arrive_expect_tx(fb, STAGE);
+          const uint32_t sa = base + stage * STAGE;
+          const int seg = kb / p.kb_per_seg;
+          tma_load_2d(sa, &amaps.a[seg], fb, (kb - seg * p.kb_per_seg) * kBK, m * kBM);
+          tma_load_2d(sa + A_BYTES, &bmap, fb, kb * kBK, n * BN);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // ------------------------------ MMA issuer
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+        int m, n, kb0, kb1, ks;
+        unit_coords(u, p, m, n, kb0, kb1, ks);
+        if (!(ok = mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1u, p.status))) break;
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!(ok = mbar_wait(full0 + 8 * stage, phase, p.status))) break;
+          tc_fence_after_sync();
+          const uint32_t sa = base + stage * STAGE;
+          const uint64_t ad = umma_desc_kmajor_sw128(sa);
+          const uint64_t bd = umma_desc_kmajor_sw128(sa + A_BYTES);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)
+            umma_bf16(d_tmem, ad + 2 * k, bd + 2 * k, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
+          umma_commit(empty0 + 8 * stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        umma_commit(tfull0 + 8 * acc);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+    }
+  } else {  // -------------------------------------------- epilogue warps 2..5
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int u = blockIdx.x; u < total; u += gridDim.x) {
+      int m, n, kb0, kb1, ks;
+      unit_coords(u, p, m, n, kb0, kb1, ks);
+      if (!mbar_wait(tfull0 + 8 * acc, acc_phase, p.status)) break;
+      tc_fence_after_sync();
+      const int row = m * kBM + q * 32 + lane;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+      if (p.epi == 0) {
+        float* dst = p.out_f32 + (static_cast<size_t>(ks) * p.M + row) * p.N + n * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld_32cols(taddr + c * 32, r);
+          tmem_ld_wait();
+          if (row < p.M) {
+            float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              d4[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                  __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int hh = 0; hh < BN / HD; ++hh) kv_head_epilogue(taddr + hh * HD, n * BN + hh * HD, row, p);
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, 2 * BN);
+  }
+}
+
+// Row -> (sequence, cache position) and the RoPE (cos, sin) table of each row.
+__global__ void __launch_bounds__(64) fuse_rowmap_kernel(const int32_t* __restrict__ cu_new,
+                                                         const int32_t* __restrict__ seq_len, int B,
+                                                         int cap, InvFreq inv, int2* __restrict__ rowinfo,
+                                                         float2* __restrict__ rope_cs, unsigned* status) {
+  const int m = blockIdx.x;
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {  // largest b with cu_new[b] <= m
+    const int mid = (lo + hi + 1) >> 1;
+    if (cu_new[mid] <= m) lo = mid; else hi = mid - 1;
+  }
+  const int b = lo;
+  const int t = m - cu_new[b];
+  const int nnew = cu_new[b + 1] - cu_new[b];
+  const int n = seq_len[b];
+  const bool seq_ok = n >= 0 && n <= cap;
+  const bool valid = seq_ok && n + nnew <= cap && t >= 0 && t < nnew;
+  const int pos = valid ? n + t : 0;
+  if (threadIdx.x < HD / 2) {
+    double ang = static_cast<double>(pos) * inv.v[threadIdx.x];
+    ang -= kTwoPi * rint(ang / kTwoPi);
+    float sv, cv;
+    sincosf(static_cast<float>(ang), &sv, &cv);
+    rope_cs[static_cast<size_t>(m) * (HD / 2) + threadIdx.x] = make_float2(cv, sv);
+  }
+  if (threadIdx.x == 0) {
+    rowinfo[m] = valid ? make_int2(b, pos) : make_int2(-1, -1);
+    if (!valid) raise_status(status, seq_ok ? DFLASH_DEV_CAPACITY : DFLASH_DEV_BAD_SEQLEN);
+  }
+}
+
+// H_t = sum of split-K partials, RMS-normalised with gain g; stored as TH
+// (workspace copy for the next GEMM) and optionally as TO (caller's copy).
+template <typename TG, typename TH>
+__global__ void __launch_bounds__(256) fuse_rmsnorm_kernel(const float* __restrict__ part, int k_splits,
+                                                           int M, int D, const TG* __restrict__ g,
+                                                           float eps, TH* __restrict__ ht,
+                                                           TH* __restrict__ ht_out) {
+  const int m = blockIdx.x;
+  float ss = 0.f;
+  for (int e = threadIdx.x; e < D; e += 256) {
+    float y = 0.f;
+    for (int s = 0; s < k_splits; ++s) y += part[(static_cast<size_t>(s) * M + m) * D + e];
+    ss += y * y;
+  }
+  ss = warp_sum(ss);
+  __shared__ float red[8];
+  if (threadIdx.x % 32 == 0) red[threadIdx.x / 32] = ss;
+  __syncthreads();
+  float tot = 0.f;
+  for (int w = 0; w < 8; ++w) tot += red[w];
+  const float r = rsqrtf(tot / static_cast<float>(D) + eps);
+  for (int e = threadIdx.x; e < D; e += 256) {
+    float y = 0.f;
+    for (int s = 0; s < k_splits; ++s) y += part[(static_cast<size_t>(s) * M + m) * D + e];
+    const float gv = g ? to_f32<TG>(g[e]) : 1.f;
+    const TH h = from_f32<TH>(y * r * gv);
+    ht[static_cast<size_t>(m) * D + e] = h;
+    if (ht_out) ht_out[static_cast<size_t>(m) * D + e] = h;
+  }
+}
+
+// ------------------------------------------------------------- fp32 path ----
+
+struct F32Segs {
+  const float* a[kMaxSeg];
+};
+
+// C[M][N] = [A_0 | A_1 | ...] (each [M][kseg]) x W^T, W [N][K]; 64x64 tiles.
+__global__ void __launch_bounds__(256) simt_gemm_f32_kernel(F32Segs segs, int kseg, const float* __restrict__ W,
+                                                            int M, int N, int K, float* __restrict__ C) {
+  __shared__ float As[16][64 + 1];
+  __shared__ float Ws[16][64 + 1];
+  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+  const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
+  float acc[4][4] = {};
+  for (int k0 = 0; k0 < K; k0 += 16) {
+    for (int i = threadIdx.x; i < 16 * 64; i += 256) {
+      const int kk = i % 16, r = i / 16;
+      const int k = k0 + kk;
+      const int seg = k / kseg;
+      As[kk][r] = (m0 + r < M && k < K) ? segs.a[seg][static_cast<size_t>(m0 + r) * kseg + (k - seg * kseg)] : 0.f;
+      Ws[kk][r] = (n0 + r < N && k < K) ? W[static_cast<size_t>(n0 + r) * K + k] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk)
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] += As[kk][ty * 4 + i] * Ws[kk][tx * 4 + j];
+    __syncthreads();
+  }
+  for (int i = 0; i < 4; ++i)
+    for (int j = 0; j < 4; ++j) {
+      const int r = m0 + ty * 4 + i, c = n0 + tx * 4 + j;
+      if (r < M && c < N) C[static_cast<size_t>(r) * N + c] = acc[i][j];
+    }
+}
+
+// One warp per (row, head of the K/V projection): norm + RoPE for keys, store.
+__global__ void __launch_bounds__(256) kv_store_f32_kernel(const float* __restrict__ kv, int M, int L, int Hkv,
+                                                           int Bc, int cap, const int2* __restrict__ rowinfo,
+                                                           const float2* __restrict__ rope_cs,
+                                                           const float* __restrict__ k_gain, float eps,
+                                                           float* __restrict__ cache_k, float* __restrict__ cache_v) {
+  const int heads = L * 2 * Hkv;
+  const long wid = (static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
+  const int lane = threadIdx.x % 32;
+  if (wid >= static_cast<long>(M) * heads) return;
+  const int m = static_cast<int>(wid / heads), hidx = static_cast<int>(wid % heads);
+  const int2 ri = rowinfo[m];
+  if (ri.x < 0) return;
+  const int l = hidx / (2 * Hkv), s = (hidx / Hkv) % 2, h = hidx % Hkv;
+  const float* src = kv + static_cast<size_t>(m) * heads * HD + static_cast<size_t>(hidx) * HD;
+  float* dst = (s == 0 ? cache_k : cache_v) + (((static_cast<size_t>(l) * Bc + ri.x) * Hkv + h) * cap + ri.y) * HD;
+  const int e0 = 2 * lane;
+  float x0 = src[e0], x1 = src[e0 + 1], y0 = src[e0 + 64], y1 = src[e0 + 65];
+  if (s == 1) {
+    dst[e0] = x0;
+    dst[e0 + 1] = x1;
+    dst[e0 + 64] = y0;
+    dst[e0 + 65] = y1;
+    return;
+  }
+  const float ss = warp_sum(x0 * x0 + x1 * x1 + y0 * y0 + y1 * y1);
+  const float r = rsqrtf(ss * (1.0f / HD) + eps);
+  const float* kg = k_gain ? k_gain + l * HD : nullptr;
+  x0 *= r * (kg ? kg[e0] : 1.f);
+  x1 *= r * (kg ? kg[e0 + 1] : 1.f);
+  y0 *= r * (kg ? kg[e0 + 64] : 1.f);
+  y1 *= r * (kg ? kg[e0 + 65] : 1.f);
+  const float2 c0 = rope_cs[static_cast<size_t>(m) * 64 + e0], c1 = rope_cs[static_cast<size_t>(m) * 64 + e0 + 1];
+  dst[e0] = x0 * c0.x - y0 * c0.y;
+  dst[e0 + 1] = x1 * c1.x - y1 * c1.y;
+  dst[e0 + 64] = y0 * c0.x + x0 * c0.y;
+  dst[e0 + 65] = y1 * c1.x + x1 * c1.y;
+}
+
+// ------------------------------------------------------------- planning -----
+
+struct FusePlan {
+  int m_tiles, fuse_n_tiles, k_splits, kv_bn;
+};
+
+FusePlan plan(int M, int D, int Ntot) {
+  FusePlan f;
+  f.m_tiles = (M + kBM - 1) / kBM;
+  f.fuse_n_tiles = D / 256;
+  const int tiles = f.m_tiles * f.fuse_n_tiles;
+  f.k_splits = std::max(1, std::min(16, kSplitTarget / std::max(1, tiles)));
+  f.kv_bn = 256;  // two heads per tile; fewer, larger tiles beat a second wave at small M
+  return f;
+}
+
+constexpr int kStagesBN256 = 4;
+constexpr int kStagesBN128 = 6;
+
+template <int BN, int STAGES>
+dflash_status launch_gemm(const TmapPack& am, const CUtensorMap& bm, const GemmArgs& a, cudaStream_t st,
+                          const DeviceInfo& dev) {
+  const size_t smem = gemm_smem_bytes<BN, STAGES>();
+  if (smem > dev.max_smem_optin) return fail(DFLASH_ERR_UNSUPPORTED, "gemm_tc: shared memory");
+  static int configured = -1;
+  if (configured != dev.device) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(gemm_tc_kernel)");
+    configured = dev.device;
+  }
+  const int units = a.m_tiles * a.n_tiles * a.k_splits;
+  const int grid = std::min(units, dev.num_sms);
+  gemm_tc_kernel<BN, STAGES><<<grid, kGemmThreads, smem, st>>>(am, bm, a);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? DFLASH_OK : cuda_fail(e, "gemm_tc_kernel launch");
+}
+
+}  // namespace
+
+size_t fuse_ws_bytes(int M, int J, int dt_width, int D, int L, int Hkv, dflash_dtype dt) {
+  (void)J;
+  (void)dt_width;
+  const int Ntot = L * 2 * Hkv * HD;
+  size_t s = align256(static_cast<size_t>(M) * sizeof(int2)) +
+             align256(static_cast<size_t>(M) * (HD / 2) * sizeof(float2));
+  if (dt == DFLASH_BF16) {
+    const FusePlan f = plan(M, D, Ntot);
+    s += align256(static_cast<size_t>(f.k_splits) * M * D * sizeof(float)) +
+         align256(static_cast<size_t>(M) * D * sizeof(__nv_bfloat16));
+  } else {
+    s += align256(static_cast<size_t>(M) * D * sizeof(float)) * 2 +
+         align256(static_cast<size_t>(M) * Ntot * sizeof(float));
+  }
+  return s + 256;
+}
+
+dflash_status launch_fuse_context(int J, const void* const* taps, int dt_width, const int32_t* cu_new,
+                                  int B, int M, const void* w_fuse, const void* g_fuse, int D,
+                                  const void* w_kv, const void* k_gain, float theta, float eps,
+                                  const dflash_kv_cache& c, void* h_t_out, void* ws, cudaStream_t st,
+                                  const DeviceInfo& dev) {
+  const int L = c.num_layers, Hkv = c.num_kv_heads;
+  const int Ntot = L * 2 * Hkv * HD;
+  InvFreq inv;
+  for (int e = 0; e < HD / 2; ++e) inv.v[e] = std::pow(static_cast<double>(theta), -2.0 * e / HD);
+  WsCarver w(ws);
+  int2* rowinfo = w.take<int2>(M);
+  float2* rope_cs = w.take<float2>(static_cast<size_t>(M) * (HD / 2));
+  fuse_rowmap_kernel<<<M, 64, 0, st>>>(cu_new, c.seq_len, B, c.capacity, inv, rowinfo, rope_cs, dev.status);
+
+  if (c.dtype == DFLASH_F32) {
+    float* Y = w.take<float>(static_cast<size_t>(M) * D);
+    float* H = w.take<float>(static_cast<size_t>(M) * D);
+    float* KV = w.take<float>(static_cast<size_t>(M) * Ntot);
+    F32Segs segs{};
+    for (int j = 0; j < J; ++j) segs.a[j] = static_cast<const float*>(taps[j]);
+    simt_gemm_f32_kernel<<<dim3((D + 63) / 64, (M + 63) / 64), 256, 0, st>>>(
+        segs, dt_width, static_cast<const float*>(w_fuse), M, D, J * dt_width, Y);
+    fuse_rmsnorm_kernel<float, float><<<M, 256, 0, st>>>(Y, 1, M, D, static_cast<const float*>(g_fuse), eps, H,
+                                                         static_cast<float*>(h_t_out));
+    F32Segs hs{};
+    hs.a[0] = H;
+    simt_gemm_f32_kernel<<<dim3((Ntot + 63) / 64, (M + 63) / 64), 256, 0, st>>>(
+        hs, D, static_cast<const float*>(w_kv), M, Ntot, D, KV);
+    const long warps = static_cast<long>(M) * L * 2 * Hkv;
+    kv_store_f32_kernel<<<static_cast<unsigned>((warps * 32 + 255) / 256), 256, 0, st>>>(
+        KV, M, L, Hkv, c.batch, c.capacity, rowinfo, rope_cs, static_cast<const float*>(k_gain), eps,
+        static_cast<float*>(c.k), static_cast<float*>(c.v));
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? DFLASH_OK : cuda_fail(e, "fp32 fusion launch");
+  }
+
+  const FusePlan f = plan(M, D, Ntot);
+  float* Ypart = w.take<float>(static_cast<size_t>(f.k_splits) * M * D);
+  auto* H = w.take<__nv_bfloat16>(static_cast<size_t>(M) * D);
+
+  // 1. fusion GEMM: A = the J taps (one tensor map each), B = W_c [D][J*dt]
+  TmapPack am{};
+  for (int j = 0; j < J; ++j) {
+    dflash_status s = make_tmap_bf16_2d(&am.a[j], taps[j], static_cast<uint64_t>(M), dt_width, kBM, kBK);
+    if (s) return s;
+  }
+  CUtensorMap bm;
+  dflash_status s = make_tmap_bf16_2d(&bm, w_fuse, static_cast<uint64_t>(D), static_cast<uint64_t>(J) * dt_width, 256, kBK);
+  if (s) return s;
+  GemmArgs a{};
+  a.M = M;
+  a.N = D;
+  a.num_kb = J * dt_width / kBK;
+  a.kb_per_seg = dt_width / kBK;
+  a.k_splits = std::min(f.k_splits, a.num_kb);
+  a.m_tiles = f.m_tiles;
+  a.n_tiles = f.fuse_n_tiles;
+  a.epi = 0;
+  a.out_f32 = Ypart;
+  a.status = dev.status;
+  s = launch_gemm<256, kStagesBN256>(am, bm, a, st, dev);
+  if (s) return s;
+
+  // 2. RMSNorm -> H_t (bf16)
+  fuse_rmsnorm_kernel<__nv_bfloat16, __nv_bfloat16><<<M, 256, 0, st>>>(
+      Ypart, a.k_splits, M, D, static_cast<const __nv_bfloat16*>(g_fuse), eps, H,
+      static_cast<__nv_bfloat16*>(h_t_out));
+
+  // 3. K/V GEMM with the cache epilogue
+  TmapPack hm{};
+  s = make_tmap_bf16_2d(&hm.a[0], H, static_cast<uint64_t>(M), D, kBM, kBK);
+  if (s) return s;
+  CUtensorMap wm;
+  s = make_tmap_bf16_2d(&wm, w_kv, static_cast<uint64_t>(Ntot), D, f.kv_bn, kBK);
+  if (s) return s;
+  GemmArgs k{};
+  k.M = M;
+  k.N = Ntot;
+  k.num_kb = D / kBK;
+  k.kb_per_seg = k.num_kb;
+  k.k_splits = 1;
+  k.m_tiles = f.m_tiles;
+  k.n_tiles = Ntot / f.kv_bn;
+  k.epi = 1;
+  k.cache_k = static_cast<__nv_bfloat16*>(c.k);
+  k.cache_v = static_cast<__nv_bfloat16*>(c.v);
+  k.L = L;
+  k.Bc = c.batch;
+  k.Hkv = Hkv;
+  k.cap = c.capacity;
+  k.rowinfo = rowinfo;
+  k.rope_cs = rope_cs;
+  k.k_gain = static_cast<const __nv_bfloat16*>(k_gain);
+  k.eps = eps;
+  k.status = dev.status;
+  return f.kv_bn == 256 ? launch_gemm<256, kStagesBN256>(hm, wm, k, st, dev)
+                        : launch_gemm<128, kStagesBN128>(hm, wm, k, st, dev);
+}
+
+}  // namespace dflash

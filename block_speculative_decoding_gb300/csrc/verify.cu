@@ -1,0 +1,543 @@
+// Exact speculative verification over the full vocabulary.
+//
+// Pages: "Nemotron 3.5 Bolt E4B: Block-Parallel Speculation with DFlash",
+// section "Why exact verification preserves the target" (accept with
+// min(1, p/q), otherwise draw from the normalised positive residual; greedy:
+// accept while the draft equals the target argmax); "DFlash & DFlash2:
+// Block-Diffusion LLM-Speedup", 4.4 (same rules) and FAQ Q3 (temperature
+// applied to both rows before the ratio).
+//
+// Kernels (one stream, no inter-CTA waiting):
+//   1. stats    -- every logit row (bs target rows, bs-1 draft rows per
+//                  sequence) is cut into 16384-logit chunks; each CTA streams
+//                  one chunk with 16-byte loads and writes (max, sum 2^x) of
+//                  x = logit * log2(e)/T, or (max, first argmax) when T == 0.
+//   2. decide   -- one warp per sequence merges the chunk partials into
+//                  log-normalisers, evaluates alpha_k = min(1, p(x)/q(x)) from
+//                  two single-logit loads per row, draws the Philox uniforms and
+//                  finds the first rejection n.  Greedy ends here.
+//   3. residual -- for row n only (the correction row, or the bonus row):
+//                  per-chunk masses of max(0, p - q) and of p.
+//   4. select   -- one CTA per sequence: inverse-CDF search for the first
+//                  index whose cumulative mass exceeds v * S.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+
+#include "dflash_device.cuh"
+#include "dflash_internal.h"
+
+namespace dflash {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kChunk = 16384;                 // logits per CTA chunk
+constexpr int kPerThread = kChunk / kThreads;  // 64 logits per thread
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct Decision {
+  int n;            // accepted drafts; the correction/bonus comes from row n
+  uint32_t vbits;   // Philox word for the draw at row n
+  float lzp;        // log2 normaliser of p (row n), in units of logit*scale
+  float lzq;        // log2 normaliser of q (row n); unused for the bonus row
+};
+
+// 16-byte vector loaders: 8 bf16, 4 fp32, or one scalar.
+template <typename T, int VEC>
+struct Vec;
+template <>
+struct Vec<__nv_bfloat16, 8> {
+  using type = uint4;
+  static __device__ __forceinline__ void unpack(const type& v, float* f) {
+    f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x); f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+    f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z); f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+  }
+};
+template <>
+struct Vec<float, 4> {
+  using type = float4;
+  static __device__ __forceinline__ void unpack(const type& v, float* f) {
+    f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
+  }
+};
+template <typename T>
+struct Vec<T, 1> {
+  using type = T;
+  static __device__ __forceinline__ void unpack(const type& v, float* f) { f[0] = to_f32<T>(v); }
+};
+
+// Load this thread's 64 logits of chunk [e0, e1): vector i of thread t covers
+// elements e0 + (i*256 + t)*VEC ...  Out-of-range elements become -inf.
+template <typename T, int VEC>
+__device__ __forceinline__ void load_chunk(const T* __restrict__ row, int e0, int e1,
+                                           float (&f)[kPerThread]) {
+  using VT = typename Vec<T, VEC>::type;
+  constexpr int NV = kPerThread / VEC;
+  VT v[NV];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int e = e0 + (i * kThreads + threadIdx.x) * VEC;
+    if (e < e1) v[i] = __ldcs(reinterpret_cast<const VT*>(row + e));
+  }
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int e = e0 + (i * kThreads + threadIdx.x) * VEC;
+    if (e < e1) {
+      Vec<T, VEC>::unpack(v[i], f + i * VEC);
+    } else {
+#pragma unroll
+      for (int j = 0; j < VEC; ++j) f[i * VEC + j] = -INFINITY;
+    }
+  }
+}
+
+template <int VEC>
+__device__ __forceinline__ int elem_index(int e0, int slot) {
+  const int i = slot / VEC, j = slot % VEC;
+  return e0 + (i * kThreads + threadIdx.x) * VEC + j;
+}
+
+// (m, s) represents s * 2^m; merges tolerate empty (-inf) sides.
+__device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
+  if (m2 == -INFINITY) return;
+  if (m == -INFINITY) {
+    m = m2;
+    s = s2;
+    return;
+  }
+  const float mn = fmaxf(m, m2);
+  s = s * exp2f(m - mn) + s2 * exp2f(m2 - mn);
+  m = mn;
+}
+
+__device__ __forceinline__ void amax_merge(float& v, int& i, float v2, int i2) {
+  if (v2 > v || (v2 == v && i2 < i)) {
+    v = v2;
+    i = i2;
+  }
+}
+
+template <typename T, int VEC, bool GREEDY>
+__global__ void __launch_bounds__(kThreads) verify_stats_kernel(const T* __restrict__ lt,
+                                                                const T* __restrict__ ld, int B,
+                                                                int bs, int V, int nchunk,
+                                                                float scale,
+                                                                float2* __restrict__ part) {
+  const int c = blockIdx.x % nchunk;
+  const int r = blockIdx.x / nchunk;
+  const T* row = (r < B * bs) ? lt + static_cast<size_t>(r) * V
+                              : ld + static_cast<size_t>(r - B * bs) * V;
+  const int e0 = c * kChunk;
+  const int e1 = min(V, e0 + kChunk);
+  float f[kPerThread];
+  load_chunk<T, VEC>(row, e0, e1, f);
+
+  float a, b;  // GREEDY: (value, index-as-bits); else (max, sum)
+  if constexpr (GREEDY) {
+    float bv = -INFINITY;
+    int bi = INT_MAX;
+#pragma unroll
+    for (int s = 0; s < kPerThread; ++s) {  // slots visit this thread's logits in index order
+      const int e = elem_index<VEC>(e0, s);
+      if (e < e1 && (bi == INT_MAX || f[s] > bv)) {
+        bv = f[s];
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float v2 = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
+      amax_merge(bv, bi, v2, i2);
+    }
+    a = bv;
+    b = __int_as_float(bi);
+  } else {
+    float m = -INFINITY;
+#pragma unroll
+    for (int s = 0; s < kPerThread; ++s) {
+      f[s] *= scale;
+      m = fmaxf(m, f[s]);
+    }
+    float sum = 0.f;
+    if (m != -INFINITY) {
+#pragma unroll
+      for (int s = 0; s < kPerThread; ++s) sum += exp2f(f[s] - m);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+      const float s2 = __shfl_xor_sync(0xffffffffu, sum, o);
+      lse_merge(m, sum, m2, s2);
+    }
+    a = m;
+    b = sum;
+  }
+  __shared__ float2 red[kThreads / 32];
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (lane == 0) red[warp] = make_float2(a, b);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float2 acc = red[0];
+    for (int w = 1; w < kThreads / 32; ++w) {
+      if constexpr (GREEDY) {
+        int ai = __float_as_int(acc.y);
+        amax_merge(acc.x, ai, red[w].x, __float_as_int(red[w].y));
+        acc.y = __int_as_float(ai);
+      } else {
+        lse_merge(acc.x, acc.y, red[w].x, red[w].y);
+      }
+    }
+    part[static_cast<size_t>(r) * nchunk + c] = acc;
+  }
+}
+
+// Merge the chunk partials of one row across the warp; every lane gets the result.
+template <bool GREEDY>
+__device__ __forceinline__ float2 merge_row(const float2* __restrict__ part, int nchunk) {
+  float a = -INFINITY, b = GREEDY ? __int_as_float(INT_MAX) : 0.f;
+  for (int c = threadIdx.x % 32; c < nchunk; c += 32) {
+    const float2 p = part[c];
+    if constexpr (GREEDY) {
+      int bi = __float_as_int(b);
+      amax_merge(a, bi, p.x, __float_as_int(p.y));
+      b = __int_as_float(bi);
+    } else {
+      lse_merge(a, b, p.x, p.y);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float a2 = __shfl_xor_sync(0xffffffffu, a, o);
+    const float b2 = __shfl_xor_sync(0xffffffffu, b, o);
+    if constexpr (GREEDY) {
+      int bi = __float_as_int(b);
+      amax_merge(a, bi, a2, __float_as_int(b2));
+      b = __int_as_float(bi);
+    } else {
+      lse_merge(a, b, a2, b2);
+    }
+  }
+  return make_float2(a, b);
+}
+
+template <typename T, bool GREEDY>
+__global__ void __launch_bounds__(128) verify_decide_kernel(
+    const T* __restrict__ lt, const T* __restrict__ ld, const int32_t* __restrict__ x, int B, int bs,
+    int V, int nchunk, float scale, const float2* __restrict__ part, uint32_t k0, uint32_t k1,
+    uint32_t c_lo, uint32_t c_hi, int32_t* __restrict__ acc, int32_t* __restrict__ out,
+    Decision* __restrict__ dec, unsigned* status) {
+  const int lane = threadIdx.x % 32;
+  const int b = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  if (b >= B) return;
+  const int R_t = B * bs;
+  float lzp = 0.f, lzq = 0.f;
+  int amax = 0;
+  for (int k = 0; k < bs; ++k) {
+    const float2 pt = merge_row<GREEDY>(part + static_cast<size_t>(b * bs + k) * nchunk, nchunk);
+    if constexpr (GREEDY) {
+      int i = __float_as_int(pt.y);
+      if (lane == k) amax = (i == INT_MAX) ? 0 : i;
+    } else {
+      if (lane == k) lzp = pt.x + log2f(pt.y);
+      if (k < bs - 1) {
+        const float2 pq = merge_row<false>(
+            part + static_cast<size_t>(R_t + b * (bs - 1) + k) * nchunk, nchunk);
+        if (lane == k) lzq = pq.x + log2f(pq.y);
+      }
+    }
+  }
+  bool rejected = false;
+  uint32_t vbits = 0;
+  int xk = -1;
+  if (lane < bs - 1) xk = x[b * (bs - 1) + lane];
+  if (lane < bs) {
+    uint4 w = make_uint4(0u, 0u, 0u, 0u);
+    if constexpr (!GREEDY) w = philox4x32_10(make_uint4(lane, b, c_lo, c_hi), k0, k1);
+    vbits = w.y;
+    if (lane < bs - 1) {
+      if (xk < 0 || xk >= V) {
+        raise_status(status, DFLASH_DEV_BAD_TOKEN);
+        rejected = true;
+      } else if constexpr (GREEDY) {
+        rejected = (amax != xk);
+      } else {
+        const float lp = to_f32<T>(lt[static_cast<size_t>(b * bs + lane) * V + xk]) * scale - lzp;
+        const float lq = to_f32<T>(ld[static_cast<size_t>(b * (bs - 1) + lane) * V + xk]) * scale - lzq;
+        const float alpha = fminf(1.f, exp2f(lp - lq));
+        rejected = !(uniform24(w.x) < alpha);
+      }
+    }
+  }
+  const unsigned mask = __ballot_sync(0xffffffffu, rejected);
+  const int n = mask ? (__ffs(mask) - 1) : (bs - 1);
+  const int amax_n = __shfl_sync(0xffffffffu, amax, n);
+  const uint32_t vbits_n = __shfl_sync(0xffffffffu, vbits, n);
+  const float lzp_n = __shfl_sync(0xffffffffu, lzp, n);
+  const float lzq_n = __shfl_sync(0xffffffffu, lzq, n);
+  if (lane < bs) {
+    int v = -1;
+    if (lane < n) v = xk;
+    else if (lane == n && GREEDY) v = amax_n;
+    out[b * bs + lane] = v;
+  }
+  if (lane == 0) {
+    acc[b] = n;
+    if constexpr (!GREEDY) {
+      Decision d;
+      d.n = n;
+      d.vbits = vbits_n;
+      d.lzp = lzp_n;
+      d.lzq = lzq_n;
+      dec[b] = d;
+    }
+  }
+}
+
+// Residual weight of one logit pair (or of p alone for the bonus row).
+__device__ __forceinline__ float resid_weight(float xt, float xd, const Decision& d, bool has_q,
+                                              float& pw) {
+  pw = exp2f(xt - d.lzp);
+  if (!has_q) return pw;
+  const float qw = exp2f(xd - d.lzq);
+  return fmaxf(0.f, pw - qw);
+}
+
+template <typename T, int VEC>
+__global__ void __launch_bounds__(kThreads) verify_residual_kernel(
+    const T* __restrict__ lt, const T* __restrict__ ld, int B, int bs, int V, int nchunk,
+    float scale, const Decision* __restrict__ dec, float2* __restrict__ rpart) {
+  const int c = blockIdx.x % nchunk, b = blockIdx.x / nchunk;
+  const Decision d = dec[b];
+  const bool has_q = d.n < bs - 1;
+  const T* prow = lt + static_cast<size_t>(b * bs + d.n) * V;
+  const int e0 = c * kChunk, e1 = min(V, e0 + kChunk);
+  float ft[kPerThread], fd[kPerThread];
+  load_chunk<T, VEC>(prow, e0, e1, ft);
+  if (has_q) {
+    load_chunk<T, VEC>(ld + static_cast<size_t>(b * (bs - 1) + d.n) * V, e0, e1, fd);
+  }
+  float sr = 0.f, sp = 0.f;
+#pragma unroll
+  for (int s = 0; s < kPerThread; ++s) {
+    if (ft[s] == -INFINITY) continue;  // out of range (or a -inf logit: zero mass)
+    float pw;
+    const float r = resid_weight(ft[s] * scale, has_q ? fd[s] * scale : 0.f, d, has_q, pw);
+    sr += r;
+    sp += pw;
+  }
+  sr = warp_sum(sr);
+  sp = warp_sum(sp);
+  __shared__ float2 red[kThreads / 32];
+  if (threadIdx.x % 32 == 0) red[threadIdx.x / 32] = make_float2(sr, sp);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float2 a = red[0];
+    for (int w = 1; w < kThreads / 32; ++w) {
+      a.x += red[w].x;
+      a.y += red[w].y;
+    }
+    rpart[static_cast<size_t>(b) * nchunk + c] = a;
+  }
+}
+
+// This thread's contiguous segment [s0, s0 + 64) of a row, with 16-byte vector
+// loads where possible; elements at or beyond s1 become -inf.
+template <typename T, int VEC>
+__device__ __forceinline__ void load_segment(const T* __restrict__ row, int s0, int s1,
+                                             float (&f)[kPerThread]) {
+  using VT = typename Vec<T, VEC>::type;
+  constexpr int NV = kPerThread / VEC;
+  VT v[NV];
+#pragma unroll
+  for (int i = 0; i < NV; ++i)
+    if (s0 + i * VEC < s1) v[i] = *reinterpret_cast<const VT*>(row + s0 + i * VEC);
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    if (s0 + i * VEC < s1) {
+      Vec<T, VEC>::unpack(v[i], f + i * VEC);
+    } else {
+#pragma unroll
+      for (int j = 0; j < VEC; ++j) f[i * VEC + j] = -INFINITY;
+    }
+  }
+}
+
+template <typename T, int VEC>
+__global__ void __launch_bounds__(kThreads) verify_select_kernel(
+    const T* __restrict__ lt, const T* __restrict__ ld, int B, int bs, int V, int nchunk,
+    float scale, const Decision* __restrict__ dec, const float2* __restrict__ rpart,
+    int32_t* __restrict__ out) {
+  const int b = blockIdx.x;
+  const Decision d = dec[b];
+  const bool has_q = d.n < bs - 1;
+  __shared__ int s_chunk;
+  __shared__ int s_use_p;
+  __shared__ float s_target;
+  __shared__ float s_scan[kThreads];
+  __shared__ int s_pick;
+  __shared__ int s_last;
+  if (threadIdx.x == 0) {
+    const float2* rp = rpart + static_cast<size_t>(b) * nchunk;
+    float sr = 0.f;
+    for (int c = 0; c < nchunk; ++c) sr += rp[c].x;
+    const int use_p = !(sr > 0.f);
+    float S = 0.f;
+    for (int c = 0; c < nchunk; ++c) S += use_p ? rp[c].y : rp[c].x;
+    const float t = uniform24(d.vbits) * S;
+    float cum = 0.f;
+    int cs = -1;
+    float excl = 0.f;
+    int last_pos = 0;
+    for (int c = 0; c < nchunk; ++c) {
+      const float w = use_p ? rp[c].y : rp[c].x;
+      if (w > 0.f) last_pos = c;
+      if (cs < 0 && cum + w > t) {
+        cs = c;
+        excl = cum;
+      }
+      cum += w;
+    }
+    if (cs < 0) {  // rounding left the threshold at the very end
+      cs = last_pos;
+      excl = 0.f;
+      for (int c = 0; c < cs; ++c) excl += use_p ? rp[c].y : rp[c].x;
+    }
+    s_chunk = cs;
+    s_use_p = use_p;
+    s_target = fmaxf(0.f, t - excl);
+    s_pick = INT_MAX;
+    s_last = -1;
+  }
+  __syncthreads();
+  const int e0 = s_chunk * kChunk, e1 = min(V, e0 + kChunk);
+  const bool use_p = s_use_p != 0;
+  const float target = s_target;
+  const T* prow = lt + static_cast<size_t>(b * bs + d.n) * V;
+  const T* qrow = has_q ? ld + static_cast<size_t>(b * (bs - 1) + d.n) * V : nullptr;
+  // contiguous segment of 64 logits per thread, in vocabulary order
+  const int s0 = e0 + threadIdx.x * kPerThread;
+  const int s1 = min(e1, s0 + kPerThread);
+  float w[kPerThread];
+  load_segment<T, VEC>(prow, s0, s1, w);
+  if (has_q && !use_p) {
+    float fq[kPerThread];
+    load_segment<T, VEC>(qrow, s0, s1, fq);
+#pragma unroll
+    for (int i = 0; i < kPerThread; ++i) {
+      float pw;
+      w[i] = w[i] == -INFINITY ? 0.f : resid_weight(w[i] * scale, fq[i] * scale, d, true, pw);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < kPerThread; ++i) w[i] = w[i] == -INFINITY ? 0.f : exp2f(w[i] * scale - d.lzp);
+  }
+  float seg = 0.f;
+  int last_pos = -1;
+#pragma unroll
+  for (int i = 0; i < kPerThread; ++i) {
+    if (w[i] > 0.f) last_pos = s0 + i;
+    seg += w[i];
+  }
+  // inclusive scan of segment masses across the block (Hillis-Steele)
+  s_scan[threadIdx.x] = seg;
+  __syncthreads();
+  for (int o = 1; o < kThreads; o <<= 1) {
+    const float v = threadIdx.x >= o ? s_scan[threadIdx.x - o] : 0.f;
+    __syncthreads();
+    s_scan[threadIdx.x] += v;
+    __syncthreads();
+  }
+  const float incl = s_scan[threadIdx.x];
+  const float excl = incl - seg;
+  if (last_pos >= 0) atomicMax(&s_last, last_pos);
+  if (seg > 0.f && excl <= target && target < incl) {
+    float run = excl;
+    int pick = -1;
+#pragma unroll 1
+    for (int i = 0; i < kPerThread; ++i) {
+      if (w[i] > 0.f) {
+        pick = s0 + i;  // last positive so far: fallback if rounding runs out
+        run += w[i];
+        if (run > target) break;
+      }
+    }
+    if (pick >= 0) atomicMin(&s_pick, pick);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int y = s_pick;
+    if (y == INT_MAX) y = s_last >= 0 ? s_last : e0;
+    out[b * bs + d.n] = y;
+  }
+}
+
+int pick_vec(dflash_dtype dt, int V, const void* a, const void* b) {
+  const uintptr_t al = reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(b);
+  if (dt == DFLASH_BF16) return (V % 8 == 0 && (al & 15) == 0) ? 8 : 1;
+  return (V % 4 == 0 && (al & 15) == 0) ? 4 : 1;
+}
+
+template <typename T, int VEC>
+dflash_status run(const T* lt, const T* ld, const int32_t* x, int B, int bs, int V, float Temp,
+                  uint64_t seed, uint64_t cycle, int32_t* acc, int32_t* out, void* ws,
+                  cudaStream_t st, const DeviceInfo& dev) {
+  const int nchunk = (V + kChunk - 1) / kChunk;
+  const bool greedy = (Temp == 0.0f);
+  const int R = greedy ? B * bs : B * bs + B * (bs - 1);
+  WsCarver w(ws);
+  float2* part = w.take<float2>(static_cast<size_t>(2 * B * bs) * nchunk);
+  Decision* dec = w.take<Decision>(B);
+  float2* rpart = w.take<float2>(static_cast<size_t>(B) * nchunk);
+  const float scale = greedy ? 1.f : kLog2e / Temp;
+  const uint32_t k0 = static_cast<uint32_t>(seed), k1 = static_cast<uint32_t>(seed >> 32);
+  const uint32_t c0 = static_cast<uint32_t>(cycle), c1 = static_cast<uint32_t>(cycle >> 32);
+  const unsigned g1 = static_cast<unsigned>(nchunk) * static_cast<unsigned>(R);
+  if (greedy) {
+    verify_stats_kernel<T, VEC, true><<<g1, kThreads, 0, st>>>(lt, ld, B, bs, V, nchunk, scale, part);
+    verify_decide_kernel<T, true><<<(B + 3) / 4, 128, 0, st>>>(
+        lt, ld, x, B, bs, V, nchunk, scale, part, k0, k1, c0, c1, acc, out, dec, dev.status);
+  } else {
+    verify_stats_kernel<T, VEC, false><<<g1, kThreads, 0, st>>>(lt, ld, B, bs, V, nchunk, scale, part);
+    verify_decide_kernel<T, false><<<(B + 3) / 4, 128, 0, st>>>(
+        lt, ld, x, B, bs, V, nchunk, scale, part, k0, k1, c0, c1, acc, out, dec, dev.status);
+    verify_residual_kernel<T, VEC><<<static_cast<unsigned>(nchunk) * B, kThreads, 0, st>>>(lt, ld, B, bs, V, nchunk,
+                                                                          scale, dec, rpart);
+    verify_select_kernel<T, VEC><<<B, kThreads, 0, st>>>(lt, ld, B, bs, V, nchunk, scale, dec, rpart, out);
+  }
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? DFLASH_OK : cuda_fail(e, "verify kernel launch");
+}
+
+}  // namespace
+
+size_t verify_ws_bytes(int B, int bs, int V) {
+  const size_t nchunk = (static_cast<size_t>(V) + kChunk - 1) / kChunk;
+  return align256(2 * static_cast<size_t>(B) * bs * nchunk * sizeof(float2)) +
+         align256(static_cast<size_t>(B) * sizeof(Decision)) +
+         align256(static_cast<size_t>(B) * nchunk * sizeof(float2)) + 256;
+}
+
+dflash_status launch_verify(const void* lt, const void* ld, dflash_dtype dt, const int32_t* x, int B,
+                            int bs, int V, float T, uint64_t seed, uint64_t cycle, int32_t* acc,
+                            int32_t* out, void* ws, cudaStream_t st, const DeviceInfo& dev) {
+  const bool greedy = (T == 0.0f);
+  const double rows = greedy ? double(B) * bs : double(B) * (2 * bs - 1);
+  if (rows * ((V + kChunk - 1) / kChunk) >= 2147483647.0)
+    return fail(DFLASH_ERR_UNSUPPORTED, "verify: too many logit chunks for one launch");
+  if (greedy) ld = lt;  // draft rows are never read under greedy decoding
+  const int vec = pick_vec(dt, V, lt, ld);
+  if (dt == DFLASH_BF16) {
+    auto* a = static_cast<const __nv_bfloat16*>(lt);
+    auto* b = static_cast<const __nv_bfloat16*>(ld);
+    return vec == 8 ? run<__nv_bfloat16, 8>(a, b, x, B, bs, V, T, seed, cycle, acc, out, ws, st, dev)
+                    : run<__nv_bfloat16, 1>(a, b, x, B, bs, V, T, seed, cycle, acc, out, ws, st, dev);
+  }
+  auto* a = static_cast<const float*>(lt);
+  auto* b = static_cast<const float*>(ld);
+  return vec == 4 ? run<float, 4>(a, b, x, B, bs, V, T, seed, cycle, acc, out, ws, st, dev)
+                  : run<float, 1>(a, b, x, B, bs, V, T, seed, cycle, acc, out, ws, st, dev);
+}
+
+}  // namespace dflash

@@ -1,0 +1,221 @@
+/*
+ * dflash.h -- C ABI of the DFlash draft-and-verify hot path on GB300 (sm_103a).
+ *
+ * One DFlash cycle (page "Nemotron 3.5 Bolt E4B: Block-Parallel Speculation with
+ * DFlash", section "The released serving cycle") is, on the drafter side:
+ *   1. dflash_fuse_context  -- concatenate the captured target hidden states on
+ *      the feature axis, project them to the draft width (W_c) with RMSNorm, and
+ *      project that into K/V entries appended to every draft layer's cache
+ *      (same page, "Five target states become persistent draft context";
+ *      page "DFlash & DFlash2: Block-Diffusion LLM-Speedup", 4.1).
+ *   2. dflash_block_attn    -- one non-causal attention of the draft block
+ *      (anchor + mask positions) over the cached context plus the block, GQA,
+ *      per-head Q/K RMSNorm before RoPE (E4B page, same section).
+ *   3. dflash_verify        -- exact speculative verification: min(1, p/q)
+ *      acceptance, a correction drawn from the normalised max(0, p - q)
+ *      residual, or argmax matching under greedy decoding (E4B page, "Why exact
+ *      verification preserves the target"; DFlash2 page, 4.4).
+ *
+ * Conventions for every call
+ *  - All tensor pointers are DEVICE pointers (cudaMalloc'd, or any memory the
+ *    GPU can address), owned by the caller.  The library never allocates device
+ *    memory; scratch space is the caller's `workspace` of at least the size the
+ *    matching *_workspace_size() function returns (256-byte aligned).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Calls enqueue kernels on it and return without synchronising.
+ *  - Every argument is validated on the host before any launch; on a non-zero
+ *    status nothing has been enqueued and nothing is written.
+ *  - Conditions only the device can see (a sequence whose seq_len + n_new
+ *    exceeds the cache capacity, a draft token outside [0, V)) never fault:
+ *    the kernel skips the affected writes and raises a bit in the library's
+ *    device status word, read with dflash_read_device_status().
+ *  - Tensors are dense, row-major, in the stated shape.  One dtype per call:
+ *    DFLASH_BF16 (storage bf16, float32 arithmetic) or DFLASH_F32.
+ *  - Reading of positions (the pages do not fix them): cached context row t of
+ *    a sequence sits at cache position t; block row j sits at seq_len[b] + j.
+ *  - RoPE pairs element e with e + d/2 and turns it by pos * theta^(-2e/d).
+ */
+#ifndef DFLASH_H_
+#define DFLASH_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DFLASH_API __attribute__((visibility("default")))
+#else
+#define DFLASH_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int dflash_status;
+enum {
+  DFLASH_OK = 0,
+  DFLASH_ERR_INVALID_ARGUMENT = 1, /* null pointer, negative size, bad alignment  */
+  DFLASH_ERR_UNSUPPORTED = 2,      /* a shape or dtype this build does not handle */
+  DFLASH_ERR_CAPACITY = 3,         /* host-visible size exceeds the cache capacity */
+  DFLASH_ERR_CUDA = 4,             /* a CUDA call failed: dflash_last_error_string */
+  DFLASH_ERR_WORKSPACE = 5         /* workspace NULL, misaligned or too small     */
+};
+
+typedef int dflash_dtype;
+enum { DFLASH_F32 = 0, DFLASH_BF16 = 1 };
+
+/* Bits of the device status word (dflash_read_device_status). */
+enum {
+  DFLASH_DEV_CAPACITY = 1u << 0,   /* fuse_context: seq_len[b]+n_new[b] > capacity; rows skipped */
+  DFLASH_DEV_BAD_TOKEN = 1u << 1,  /* verify: draft token outside [0, V); treated as rejected   */
+  DFLASH_DEV_BAD_SEQLEN = 1u << 2, /* seq_len[b] < 0 or > capacity; sequence skipped          */
+  DFLASH_DEV_TIMEOUT = 1u << 3     /* a bounded wait inside a kernel gave up (never expected) */
+};
+
+/*
+ * Draft KV cache, one per draft model (all layers).  Caller-owned.
+ *   k, v    : [num_layers][batch][num_kv_heads][capacity][head_dim], dtype.
+ *             K rows hold keys already RMS-normalised and rotated.
+ *   seq_len : device int32 [batch], cached positions per sequence.  The calls
+ *             read it and never advance it: after dflash_fuse_context the
+ *             caller adds n_new[b] (rolling back a rejected proposal = not
+ *             advancing; block K/V are never written to the cache).
+ */
+typedef struct {
+  int num_layers;
+  int batch;
+  int num_kv_heads;
+  int head_dim;    /* must be 128 */
+  int capacity;    /* positions per (layer, sequence, head), >= 1 */
+  dflash_dtype dtype;
+  void* k;
+  void* v;
+  const int32_t* seq_len;
+} dflash_kv_cache;
+
+/* ---------------------------------------------------------------------------
+ * 1. Context fusion and K/V injection.
+ *    E4B page "Five target states become persistent draft context"; DFlash2
+ *    page 4.1:  H_t = RMSNorm(W_c [H^(l1); ...; H^(lJ)]),  K_l = W_l^K H_t,
+ *    V_l = W_l^V H_t.  Every key then gets the per-head RMSNorm (gain k_gain[l])
+ *    and RoPE at its cache position before it is stored.
+ *
+ *  num_taps, taps : J device pointers (host array of J pointers), each
+ *                   [total_new, d_target]; tap order = ascending target layer.
+ *                   Rows are packed by sequence: rows cu_new[b] .. cu_new[b+1]-1
+ *                   belong to sequence b.  16-byte aligned.
+ *  cu_new         : device int32 [batch+1], cu_new[0] = 0, non-decreasing,
+ *                   cu_new[batch] = total_new.
+ *  w_fuse         : [d_model, J*d_target]   (W_c in the pages' orientation)
+ *  g_fuse         : [d_model] RMSNorm gain (NULL = ones)
+ *  w_kv           : [L*2*Hkv*128, d_model]; output column
+ *                   ((l*2 + s)*Hkv + h)*128 + e, s = 0 key, 1 value
+ *  k_gain         : [L, 128] per-layer key-norm gain (NULL = ones)
+ *  rope_theta, eps: RoPE base (1e6 by default) and RMSNorm epsilon (1e-6)
+ *  cache          : host pointer to the cache descriptor; K/V rows
+ *                   seq_len[b] .. seq_len[b]+n_new[b]-1 of every layer are
+ *                   written.  dtype of cache, taps and weights must agree.
+ *  h_t_out        : optional [total_new, d_model] copy of H_t (may be NULL)
+ * Constraints (bf16): d_target % 64 == 0, d_model % 256 == 0, head_dim 128.
+ * Ownership: reads all inputs, writes cache rows, h_t_out and the workspace.
+ * ------------------------------------------------------------------------- */
+DFLASH_API size_t dflash_fuse_context_workspace_size(int total_new, int num_taps, int d_target, int d_model,
+                                          int num_layers, int num_kv_heads, dflash_dtype dtype);
+
+DFLASH_API dflash_status dflash_fuse_context(int num_taps, const void* const* taps, int d_target,
+                                  const int32_t* cu_new, int batch, int total_new,
+                                  const void* w_fuse, const void* g_fuse, int d_model,
+                                  const void* w_kv, const void* k_gain,
+                                  float rope_theta, float eps,
+                                  const dflash_kv_cache* cache, void* h_t_out,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * 2. Draft-block attention of one layer.
+ *    E4B page "The released serving cycle" (steps 2-3) and "Five target
+ *    states...": Q [B,Hq,bs,128] and K/V [B,Hkv,bs,128] of the block,
+ *    Hq/Hkv query heads per KV head, per-head Q/K RMSNorm before RoPE; the
+ *    block attends to the cached context plus itself, non-causally.
+ *
+ *  layer        : draft layer index into the cache (0 .. L-1)
+ *  batch, block_size, num_q_heads : B, bs (1..16), Hq (Hq % Hkv == 0,
+ *                 Hq/Hkv * bs <= 64)
+ *  q            : [B, Hq, bs, 128]    kb, vb : [B, Hkv, bs, 128]
+ *  q_gain, k_gain: [128] this layer's norm gains (NULL = ones)
+ *  window       : 0 = the whole cached context, else the latest `window`
+ *                 cached positions
+ *  out          : [B, Hq, bs, 128] = softmax(q^ K^T / sqrt(128)) V with
+ *                 q^ = RoPE(RMSNorm(q) * q_gain) at position seq_len[b]+j and
+ *                 keys = cache[layer][b][h/(Hq/Hkv)][lo..seq_len[b]) ++
+ *                 RoPE(RMSNorm(kb) * k_gain).
+ * bf16 rounding points: q^ and the block keys (before the products) and out.
+ * ------------------------------------------------------------------------- */
+DFLASH_API size_t dflash_block_attn_workspace_size(int batch, int block_size, int num_q_heads,
+                                        int num_kv_heads, int capacity, int window,
+                                        dflash_dtype dtype);
+
+DFLASH_API dflash_status dflash_block_attn(int layer, int batch, int block_size, int num_q_heads,
+                                const void* q, const void* kb, const void* vb,
+                                const void* q_gain, const void* k_gain,
+                                float rope_theta, float eps,
+                                const dflash_kv_cache* cache, int window,
+                                void* out, void* workspace, size_t workspace_bytes,
+                                void* stream);
+
+/* ---------------------------------------------------------------------------
+ * 3. Exact speculative verification.
+ *    E4B page "Why exact verification preserves the target"; DFlash2 page 4.4
+ *    (acceptance, residual, greedy rule) and FAQ Q3 (temperature).
+ *
+ *  target_logits : [B, bs, V]; row k scores draft token x_{k+1}; row bs-1
+ *                  scores the bonus position.
+ *  draft_logits  : [B, bs-1, V]; row k is the drafter's score for x_{k+1}.
+ *                  Unused (may be NULL) when temperature == 0.
+ *  draft_tokens  : device int32 [B, bs-1]
+ *  temperature   : > 0: p = softmax(l_t/T), q = softmax(l_d/T); accept x iff
+ *                  u < min(1, p(x)/q(x)); at the first rejection emit the
+ *                  inverse-CDF draw (vocabulary order) from max(0, p - q)
+ *                  (from p if that mass is 0); if all bs-1 are accepted emit a
+ *                  draw from p of row bs-1.  == 0: accept while x equals the
+ *                  target argmax (lowest index on ties); emit the argmax at the
+ *                  first mismatch, or of row bs-1.
+ *  seed, cycle   : Philox-4x32-10 key (seed) and counter
+ *                  (k, b, cycle_lo, cycle_hi); word 0 -> acceptance uniform,
+ *                  word 1 -> draw uniform, uniform(w) = (w >> 8) * 2^-24.
+ *  accepted_len  : device int32 [B], n in [0, bs-1]
+ *  out_tokens    : device int32 [B, bs]: x_1 .. x_n, then the correction or
+ *                  bonus token, then -1.
+ * ------------------------------------------------------------------------- */
+DFLASH_API size_t dflash_verify_workspace_size(int batch, int block_size, int vocab, dflash_dtype dtype);
+
+DFLASH_API dflash_status dflash_verify(const void* target_logits, const void* draft_logits,
+                            dflash_dtype dtype, const int32_t* draft_tokens,
+                            int batch, int block_size, int vocab,
+                            float temperature, uint64_t seed, uint64_t cycle,
+                            int32_t* accepted_len, int32_t* out_tokens,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Diagnostics.
+ * ------------------------------------------------------------------------- */
+
+/* Philox-4x32-10 (Salmon et al., SC'11) on n device counters: ctr [n][4],
+ * key [2] (host values), out [n][4].  The generator verification draws from. */
+DFLASH_API dflash_status dflash_philox4x32_10(const uint32_t* ctr, uint32_t key0, uint32_t key1,
+                                   uint32_t* out, int n, void* stream);
+
+/* Synchronises `stream`, returns the device status word (DFLASH_DEV_* bits)
+ * in *flags and clears it on the current device. */
+DFLASH_API dflash_status dflash_read_device_status(uint32_t* flags, void* stream);
+
+/* Text of the last host-side error of the calling thread ("" if none). */
+DFLASH_API const char* dflash_last_error_string(void);
+
+/* ABI version: (major << 16) | minor. */
+DFLASH_API int dflash_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DFLASH_H_ */

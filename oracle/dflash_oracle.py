@@ -348,13 +348,15 @@ def _categorical_draw(weights, v):
     return y, tie
 
 
-def verify(target_logits, draft_logits, draft_tokens, temperature, seed, cycle):
+def verify(target_logits, draft_logits, draft_tokens, temperature, seed, cycle, seq_ids=None):
     """Speculative verification of one drafted block per sequence.
 
     target_logits [B, bs, V]: row k is the target's scores for the position of
     draft token x_{k+1} (row bs-1 scores the bonus position);
     draft_logits [B, bs-1, V]: row k is the drafter's q for x_{k+1};
-    draft_tokens [B, bs-1].
+    draft_tokens [B, bs-1]; seq_ids [B] optional sequence indices used in the
+    random-number counter (default 0 .. B-1), so that a subset of a batch can
+    be checked on its own.
 
     T > 0, row k = 0 .. bs-2 in order ([DF2] 4.4, [E4B] "Why exact
     verification..."):  p = softmax(l_t / T), q = softmax(l_d / T);
@@ -375,6 +377,7 @@ def verify(target_logits, draft_logits, draft_tokens, temperature, seed, cycle):
     alive = np.ones(B, dtype=bool)
     near = np.zeros(B, dtype=bool)
     rows_b = np.arange(B)
+    ids = rows_b if seq_ids is None else np.asarray(seq_ids, dtype=np.int64)
     if T == 0.0:
         tmax = lt.argmax(axis=-1)                # [B, bs], lowest index on ties
         for k in range(bs - 1):
@@ -387,7 +390,7 @@ def verify(target_logits, draft_logits, draft_tokens, temperature, seed, cycle):
         u = np.empty((B, bs))
         v = np.empty((B, bs))
         for k in range(bs):
-            u[:, k], v[:, k] = verify_uniforms(seed, cycle, k, rows_b)
+            u[:, k], v[:, k] = verify_uniforms(seed, cycle, k, ids)
         for k in range(bs - 1):
             lp = _log_softmax(lt[:, k] / T)
             lq = _log_softmax(ld[:, k] / T)

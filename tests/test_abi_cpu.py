@@ -1,0 +1,92 @@
+"""The C ABI library loads, exports every declared symbol, and validates
+arguments on the host -- all without a GPU (no compute call is made)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dflash.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from block_speculative_decoding_gb300 import _build
+    path = _build.build()
+    import block_speculative_decoding_gb300 as dfl
+    return dfl.lib(), path
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"DFLASH_API\s+[\w\s\*]+?\b(dflash_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_three_calls():
+    syms = declared_symbols()
+    for s in ("dflash_fuse_context", "dflash_block_attn", "dflash_verify"):
+        assert s in syms
+    assert len(syms) == 10
+
+
+def test_library_exports_every_declared_symbol(L):
+    lib, path = L
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT\s+(dflash_\w+)", out))
+    for s in declared_symbols():
+        assert s in exported, s
+        assert hasattr(lib, s)
+    # nothing else leaks out of the library under the dflash_ prefix
+    assert exported == set(declared_symbols())
+
+
+def test_workspace_queries(L):
+    import block_speculative_decoding_gb300 as dfl
+    assert dfl.verify_workspace_size(32, 8, 262144, dfl.BF16) > 32 * 15 * 16 * 8
+    assert dfl.verify_workspace_size(0, 8, 262144, dfl.BF16) == 0
+    assert dfl.block_attn_workspace_size(32, 8, 32, 8, 8256, 0, dfl.BF16) > 0
+    assert dfl.block_attn_workspace_size(0, 8, 32, 8, 8256, 0, dfl.BF16) == 0
+    assert dfl.fuse_context_workspace_size(256, 5, 2560, 2560, 5, 8, dfl.BF16) >= 256 * 2560 * 2
+    assert dfl.version() == (1 << 16)
+
+
+def _cache(**kw):
+    import block_speculative_decoding_gb300 as dfl
+    d = dict(num_layers=5, batch=2, num_kv_heads=8, head_dim=128, capacity=64, dtype=dfl.BF16,
+             k=16, v=16, seq_len=16)
+    d.update(kw)
+    return dfl._KVCacheDesc(d["num_layers"], d["batch"], d["num_kv_heads"], d["head_dim"], d["capacity"],
+                            d["dtype"], d["k"], d["v"], d["seq_len"])
+
+
+def test_host_validation_rejects_bad_arguments_before_any_launch(L):
+    lib, _ = L
+    P = ctypes.c_void_p
+    # verify: block size out of range, negative temperature, NULL outputs
+    assert lib.dflash_verify(P(16), P(16), 1, P(16), 2, 0, 100, 1.0, 0, 0, P(16), P(16), P(256), 1 << 20, None) == 1
+    assert lib.dflash_verify(P(16), P(16), 1, P(16), 2, 8, 100, -1.0, 0, 0, P(16), P(16), P(256), 1 << 20, None) == 1
+    assert lib.dflash_verify(P(16), P(16), 1, P(16), 2, 8, 100, 1.0, 0, 0, None, P(16), P(256), 1 << 20, None) == 1
+    assert lib.dflash_verify(P(16), P(16), 7, P(16), 2, 8, 100, 1.0, 0, 0, P(16), P(16), P(256), 1 << 20, None) == 2
+    # verify: workspace too small / misaligned
+    assert lib.dflash_verify(P(16), P(16), 1, P(16), 2, 8, 100, 1.0, 0, 0, P(16), P(16), P(256), 8, None) == 5
+    assert lib.dflash_verify(P(16), P(16), 1, P(16), 2, 8, 100, 1.0, 0, 0, P(16), P(16), P(16), 1 << 20, None) == 5
+    assert b"workspace" in lib.dflash_last_error_string()
+    # an empty batch is a no-op
+    assert lib.dflash_verify(None, None, 1, None, 0, 8, 100, 1.0, 0, 0, None, None, None, 0, None) == 0
+    # block attention: head_dim, GQA divisibility, block size, cache NULL, layer range
+    c = _cache(head_dim=64)
+    assert lib.dflash_block_attn(0, 2, 8, 32, P(16), P(16), P(16), None, None, 1e6, 1e-6, ctypes.byref(c), 0, P(16), P(256), 1 << 30, None) == 2
+    c = _cache()
+    assert lib.dflash_block_attn(0, 2, 8, 30, P(16), P(16), P(16), None, None, 1e6, 1e-6, ctypes.byref(c), 0, P(16), P(256), 1 << 30, None) == 1
+    assert lib.dflash_block_attn(0, 2, 17, 32, P(16), P(16), P(16), None, None, 1e6, 1e-6, ctypes.byref(c), 0, P(16), P(256), 1 << 30, None) == 2
+    assert lib.dflash_block_attn(5, 2, 8, 32, P(16), P(16), P(16), None, None, 1e6, 1e-6, ctypes.byref(c), 0, P(16), P(256), 1 << 30, None) == 1
+    assert lib.dflash_block_attn(0, 2, 8, 32, P(16), P(16), P(16), None, None, 1e6, 1e-6, None, 0, P(16), P(256), 1 << 30, None) == 1
+    assert lib.dflash_block_attn(0, 2, 8, 32, P(17), P(16), P(16), None, None, 1e6, 1e-6, ctypes.byref(c), 0, P(16), P(256), 1 << 30, None) == 1
+    # fusion: tap count, widths, capacity visible on the host
+    taps = (ctypes.c_void_p * 5)(16, 16, 16, 16, 16)
+    assert lib.dflash_fuse_context(0, taps, 2560, P(16), 2, 8, P(16), None, 2560, P(16), None, 1e6, 1e-6, ctypes.byref(c), None, P(256), 1 << 30, None) == 2
+    assert lib.dflash_fuse_context(5, taps, 2500, P(16), 2, 8, P(16), None, 2560, P(16), None, 1e6, 1e-6, ctypes.byref(c), None, P(256), 1 << 30, None) == 2
+    assert lib.dflash_fuse_context(5, taps, 2560, P(16), 2, 1000, P(16), None, 2560, P(16), None, 1e6, 1e-6, ctypes.byref(c), None, P(256), 1 << 30, None) == 3
+    assert lib.dflash_fuse_context(5, taps, 2560, P(16), 2, 0, P(16), None, 2560, P(16), None, 1e6, 1e-6, ctypes.byref(c), None, P(256), 1 << 30, None) == 0

@@ -1,0 +1,118 @@
+"""GPU parity of dflash_block_attn against the oracle.
+
+Relative Frobenius error of the output <= 2e-3 (bf16) / 1e-5 (fp32), on small
+cases spanning several 64-key tiles, several key splits and a ragged tail, and
+on sampled sequences of the full-size workloads in the launch configuration
+the benchmark uses.
+"""
+import numpy as np
+import pytest
+import torch
+
+import block_speculative_decoding_gb300 as dfl
+import oracle
+import workloads
+from helpers import TOL, max_abs, np64, rel_fro
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _inputs(B, bs, cap, dtype, seed, Hq=32, Hkv=8, layers=2):
+    g = torch.Generator().manual_seed(seed)
+    k = torch.randn(layers, B, Hkv, cap, 128, generator=g).to(dtype)
+    v = torch.randn(layers, B, Hkv, cap, 128, generator=g).to(dtype)
+    q = torch.randn(B, Hq, bs, 128, generator=g).to(dtype)
+    kb = torch.randn(B, Hkv, bs, 128, generator=g).to(dtype)
+    vb = torch.randn(B, Hkv, bs, 128, generator=g).to(dtype)
+    qg = (1 + 0.1 * torch.randn(128, generator=g)).to(dtype)
+    kg = (1 + 0.1 * torch.randn(128, generator=g)).to(dtype)
+    return k, v, q, kb, vb, qg, kg
+
+
+def _oracle(q, kb, vb, qg, kg, k_layer, v_layer, seq, window, dtype):
+    return oracle.block_attn(np64(q), np64(kb), np64(vb), np64(qg), np64(kg), np64(k_layer), np64(v_layer),
+                             np.asarray(seq), window=window, bf16=(dtype == torch.bfloat16))
+
+
+@pytest.mark.parametrize("bs", [1, 4, 5, 8, 16])
+@pytest.mark.parametrize("window", [0, 100])
+def test_block_attn_bf16_small(bs, window):
+    seq = [0, 70, 700]
+    cap = 768
+    k, v, q, kb, vb, qg, kg = _inputs(3, bs, cap, torch.bfloat16, seed=bs * 10 + window)
+    cache = dfl.KVCache(k.to(DEV), v.to(DEV), torch.tensor(seq, dtype=torch.int32, device=DEV))
+    out = dfl.block_attn(1, q.to(DEV), kb.to(DEV), vb.to(DEV), qg.to(DEV), kg.to(DEV), cache, window=window)
+    ref = _oracle(q, kb, vb, qg, kg, k[1], v[1], seq, window, torch.bfloat16)
+    err = rel_fro(out, ref)
+    assert err <= TOL[torch.bfloat16], (err, max_abs(out, ref))
+
+
+def test_block_attn_fp32_tiny_case():
+    cfg = workloads.TINY_FP32
+    k, v, q, kb, vb, qg, kg = _inputs(2, cfg.bs, 128, torch.float32, seed=1, layers=1)
+    seq = [64, 5]
+    cache = dfl.KVCache(k.to(DEV), v.to(DEV), torch.tensor(seq, dtype=torch.int32, device=DEV))
+    out = dfl.block_attn(0, q.to(DEV), kb.to(DEV), vb.to(DEV), qg.to(DEV), kg.to(DEV), cache)
+    ref = _oracle(q, kb, vb, qg, kg, k[0], v[0], seq, 0, torch.float32)
+    assert rel_fro(out, ref) <= TOL[torch.float32]
+
+
+def test_block_attn_null_gains_mean_ones():
+    k, v, q, kb, vb, qg, kg = _inputs(2, 8, 320, torch.bfloat16, seed=5)
+    seq = [300, 17]
+    cache = dfl.KVCache(k.to(DEV), v.to(DEV), torch.tensor(seq, dtype=torch.int32, device=DEV))
+    out = dfl.block_attn(0, q.to(DEV), kb.to(DEV), vb.to(DEV), None, None, cache)
+    ref = _oracle(q, kb, vb, torch.ones(128), torch.ones(128), k[0], v[0], seq, 0, torch.bfloat16)
+    assert rel_fro(out, ref) <= TOL[torch.bfloat16]
+
+
+def _full_size(cfg, layer, sample):
+    """Run the whole batch on the GPU (benchmark launch), check `sample` sequences."""
+    seq = workloads.seq_lens(cfg, DEV)
+    k, v = workloads.cache(cfg, DEV, layers=1)
+    w = workloads.weights(cfg, DEV)
+    q, kb, vb = workloads.block(cfg, DEV, layer=layer)
+    cache = dfl.KVCache(k, v, seq)
+    out = dfl.block_attn(0, q, kb, vb, w.q_gain[layer], w.k_gain[layer], cache)
+    torch.cuda.synchronize()
+    sel = torch.tensor(sample)
+    seq_c = seq.cpu()[sel]
+    nmax = int(seq_c.max())
+    ref = _oracle(q[sel], kb[sel], vb[sel], w.q_gain[layer], w.k_gain[layer], k[0, sel, :, :nmax],
+                  v[0, sel, :, :nmax], seq_c.numpy(), 0, cfg.dtype)
+    err = rel_fro(out[sel], ref)
+    assert err <= TOL[cfg.dtype], (err, max_abs(out[sel], ref))
+    return err
+
+
+def test_block_attn_batched_full_size_sampled():
+    print("batched rel err %.2e" % _full_size(workloads.BATCHED, 2, [0, 5, 17, 31]))
+
+
+def test_block_attn_high_batch_bs16_sampled():
+    print("high_batch bs16 rel err %.2e" % _full_size(workloads.high_batch(16, 1.0), 0, [0, 63, 127]))
+
+
+def test_block_attn_high_batch_bs4_sampled():
+    print("high_batch bs4 rel err %.2e" % _full_size(workloads.high_batch(4, 1.0), 1, [3, 100]))
+
+
+def test_block_attn_long_context_sampled():
+    print("long_context rel err %.2e" % _full_size(workloads.LONG_CONTEXT, 0, [0, 3]))
+
+
+def test_block_attn_single_stream():
+    print("single_stream rel err %.2e" % _full_size(workloads.SINGLE_STREAM, 4, [0]))
+
+
+def test_block_attn_bad_seq_len_is_flagged_not_faulted():
+    k, v, q, kb, vb, qg, kg = _inputs(2, 8, 128, torch.bfloat16, seed=9)
+    seq = torch.tensor([100, 5000], dtype=torch.int32, device=DEV)   # 5000 > capacity 128
+    cache = dfl.KVCache(k.to(DEV), v.to(DEV), seq)
+    dfl.read_device_status()
+    out = dfl.block_attn(0, q.to(DEV), kb.to(DEV), vb.to(DEV), qg.to(DEV), kg.to(DEV), cache)
+    assert dfl.read_device_status() & dfl.DEV_BAD_SEQLEN
+    ref = _oracle(q[:1], kb[:1], vb[:1], qg, kg, k[0, :1], v[0, :1], [100], 0, torch.bfloat16)
+    assert rel_fro(out[:1], ref) <= TOL[torch.bfloat16]
+    assert torch.isfinite(out.float()).all()
