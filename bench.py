@@ -65,13 +65,15 @@ def reduce_max_sum(elapsed_s: float, tokens: float, device):
     return float(t.item()), float(s.item())
 
 
-def rank_config(rank: int, batch: int | None = None) -> workloads.CycleConfig:
+def rank_config(rank: int, batch: int | None = None, layers: int | None = None) -> workloads.CycleConfig:
     """Each rank runs its own batch: same shapes, seed offset by the rank.
-    `batch` shrinks B (profiling runs of a smaller case only)."""
+    `batch` / `layers` shrink the case (profiling runs only)."""
     from dataclasses import replace
     c = workloads.BATCHED
     if batch is not None and batch != c.B:
         c = replace(c, B=batch)
+    if layers is not None and layers != c.L:
+        c = replace(c, L=layers)
     return replace(c, seed=c.seed + 100 * rank) if rank else c
 
 
@@ -204,7 +206,7 @@ def run_gpu(args):
         import torch.distributed as dist
         dist.barrier()
     build()
-    cfg = rank_config(rank, args.batch)
+    cfg = rank_config(rank, args.batch, args.layers)
     cyc = Cycle(cfg, dev, args.temperature)
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
@@ -238,7 +240,7 @@ def run_gpu(args):
     ver_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
     elapsed_max, tokens_all = reduce_max_sum(elapsed, tokens_per_cycle * args.steps, dev)
 
-    if args.only != "all" or args.batch is not None:
+    if args.only != "all" or args.batch is not None or args.layers is not None:
         if rank == 0:
             print(json.dumps({"profiling_run": True, "only": args.only, "B": cfg.B, "steps": args.steps,
                               "ms_per_step": elapsed * 1e3 / args.steps, "fuse_ms": fuse_ms,
@@ -445,6 +447,7 @@ def main():
     ap.add_argument("--only", default="all", choices=["all", "fuse", "attn", "verify"],
                     help="profiling runs: time one component of the cycle only")
     ap.add_argument("--batch", type=int, default=None, help="profiling runs: smaller batch")
+    ap.add_argument("--layers", type=int, default=None, help="profiling runs: fewer draft layers")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "dflash":
         args.warmup = 3

@@ -10,16 +10,17 @@
 //
 // Kernels:
 //   prologue -- per (sequence, block row): RMSNorm * gain and RoPE of every
-//               query head and block key, rounded to the storage dtype.
+//               query head and block key, rounded to the storage dtype; also
+//               clears the split counters of the merge below.
 //   main     -- split-KV, memory-bound: a persistent grid walks work items
 //               (sequence, KV head, key split).  A producer warp streams 64-key
-//               K and V tiles of the cache with TMA (128-byte swizzle) through
-//               a ring of shared-memory stages; four consumer warps compute
-//               S = Q K^T and O += P V with mma.sync m16n8k16 (bf16 -> fp32) for
-//               all Hq/Hkv query heads x bs block rows of the KV head at once,
-//               with an online softmax reduced by warp shuffles.  The last split
-//               of each (sequence, KV head) also takes the bs block keys.
-//   combine  -- log-sum-exp merge of the per-split partial outputs.
+//               K/V tiles of the cache (and, for the last split, the block's
+//               own keys) with TMA (128-byte swizzle) through a 4-stage ring;
+//               one thread issues tcgen05.mma for S = Q K^T and O += P V into
+//               tensor memory; two softmax warps own one query row per thread
+//               (all Hq/Hkv heads x bs block rows of the KV head share every
+//               tile).  The last CTA to finish a (sequence, KV head) merges the
+//               splits' partial outputs (log-sum-exp).
 // fp32 storage uses a plain SIMT kernel (parity path for the tiny fp32 case).
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -36,12 +37,9 @@ namespace {
 
 constexpr int HD = 128;
 constexpr int kTile = 64;                       // keys per TMA stage
-constexpr int kConsumerWarps = 4;
-constexpr int kAttnThreads = (kConsumerWarps + 1) * 32;
 constexpr int kHalfTileBytes = kTile * 64 * 2;  // 64 keys x 64 dims bf16 = 8 KB (one TMA box)
 constexpr int kStageBytes = 4 * kHalfTileBytes; // K (2 boxes) + V (2 boxes) = 32 KB
-constexpr int kMergeSlotFloats = 16 * HD + 32;  // O[16][128], m[16], l[16]
-constexpr int kMaxBatch = 4096;
+constexpr int kMaxBatch = 2048;
 constexpr double kTwoPi = 6.283185307179586476925286766559;
 
 struct InvFreq {
@@ -49,7 +47,7 @@ struct InvFreq {
 };
 
 struct AttnParams {
-  int B, bs, G, Hkv, Hq, cap, layer, window, chunk, max_splits, rows, n_mt, n_wg;
+  int B, bs, G, Hkv, Hq, cap, layer, window, chunk, max_splits, rows;
   const int32_t* seq_len;
   const __nv_bfloat16* qh;   // [B, Hq, bs, 128]   prologue output
   const __nv_bfloat16* kbh;  // [B, Hkv, bs, 128]  prologue output
@@ -58,6 +56,7 @@ struct AttnParams {
   float* opart;              // [B, Hkv, max_splits, rows, 128] normalised partial outputs
   float2* mlpart;            // [B, Hkv, max_splits, rows]      (max, sum) in log2 units
   float scale_log2;          // log2(e) / sqrt(128)
+  int* counters;             // [B, Hkv] finished splits (cleared by the prologue)
   unsigned* status;
 };
 
@@ -81,7 +80,9 @@ __global__ void __launch_bounds__(256) attn_prologue_kernel(
     const T* __restrict__ q, const T* __restrict__ kb, const T* __restrict__ qg,
     const T* __restrict__ kg, const int32_t* __restrict__ seq_len, int B, int bs, int Hq, int Hkv,
     int cap, float eps, InvFreq inv_freq, T* __restrict__ qh, T* __restrict__ kbh,
-    unsigned* status) {
+    int* __restrict__ counters, int n_counters, unsigned* status) {
+  if (blockIdx.x == 0 && counters)
+    for (int i = threadIdx.x; i < n_counters; i += blockDim.x) counters[i] = 0;
   const int b = blockIdx.x / bs, j = blockIdx.x % bs;
   const int n = clamp_seq(seq_len[b], cap, status);
   const int pos = n + j;
@@ -123,11 +124,23 @@ __global__ void __launch_bounds__(256) attn_prologue_kernel(
 }
 
 // --------------------------------------------------------------------------
-// main split-KV kernel (bf16)
 // --------------------------------------------------------------------------
+// main split-KV kernel (bf16): tcgen05 tensor cores, TMA, TMEM accumulators
+// --------------------------------------------------------------------------
+//
+// Work item = (sequence b, KV head g, key split s).  Per 64-key tile:
+//   S   = Q K^T   tcgen05.mma M=128 (query rows; the Hq/Hkv*bs real rows sit in
+//                 TMEM lanes 0..rows-1), N=64 keys, K=128 -> TMEM (2 buffers)
+//   P   = 2^(S*scale - m)   one thread per query row (softmax warps 0, 1),
+//                 written to shared memory as bf16 hi + lo (K-major, swizzled)
+//   O  += P V     tcgen05.mma M=128, N=128 dims, K=64 keys, V read MN-major
+//                 straight from the TMA tile -> TMEM accumulator
+// The running max is only refreshed (and O rescaled) when it grows by more
+// than 2^8, so P stays within [0, 256].
+// Roles: warps 0-1 softmax/epilogue, warp 2 TMA producer, warp 3 MMA issuer.
 
 struct Item {
-  int b, g, s, nsplit, kstart, kend, ntiles;
+  int b, g, s, nsplit, kstart, kend, ntiles, nt;  // nt = ntiles + (last split ? 1 block tile : 0)
   bool last;
 };
 
@@ -150,177 +163,139 @@ __device__ __forceinline__ Item decode_item(int w, const int* s_prefix, const in
   it.kend = first + min(ncache, (it.s + 1) * p.chunk);
   it.ntiles = it.kend > it.kstart ? (it.kend - it.kstart + kTile - 1) / kTile : 0;
   it.last = it.s == it.nsplit - 1;
+  it.nt = it.ntiles + (it.last ? 1 : 0);
   return it;
 }
 
-// Swizzled byte offset of (key row, 16-byte chunk c in 0..15) inside a K or V
-// stage: two TMA boxes of 64 dims each, rows of 128 bytes, chunk ^= row & 7.
-__device__ __forceinline__ uint32_t tile_off(int key, int c) {
-  return static_cast<uint32_t>((c >> 3) * kHalfTileBytes + key * 128 + (((c & 7) ^ (key & 7)) << 4));
+constexpr int kStages = 4;
+constexpr int kTcThreads = 128;
+constexpr int kRowBytes = 128;                        // 64 bf16
+constexpr int kPHalf = 64 * kRowBytes;                // P hi or lo of one buffer: 64 rows
+constexpr int kQBox = 64 * kRowBytes;                 // one 64-dim half of Q: 64 rows
+constexpr int kOffP = 0;                              // P[buf][half]  at (2*buf + half) * kPHalf
+constexpr int kOffQ = 4 * kPHalf;                     // Q[buf][box]   at kOffQ + (2*buf + box) * kQBox
+constexpr int kOffKV = kOffQ + 4 * kQBox;             // stage s at kOffKV + s * kStageBytes
+constexpr int kOffBar = kOffKV + kStages * kStageBytes;
+constexpr int kNumBars = 2 * kStages + 13;
+constexpr int kTmemCols = 256;                        // S buffers at 0 and 64, O at 128
+constexpr uint32_t kIdescQK = umma_idesc_bf16(128, 64, false);
+constexpr uint32_t kIdescPV = umma_idesc_bf16(128, 128, true);
+constexpr float kRescaleLog2 = 8.0f;
+
+size_t attn_main_smem(int B) {
+  return 1024 + kOffBar + 8 * kNumBars + 16 + (2 * static_cast<size_t>(B) + 1) * sizeof(int);
 }
 
-struct SoftmaxState {
-  float m[2], l[2];
-  float o[16][4];
+// Thread `row` (< rows) owns one query row: write its final output, or its
+// normalised partial and (m, l); the last CTA to finish a (b, g) merges.
+__device__ __forceinline__ void finish_item(const Item& it, const AttnParams& p, int row, const float (&o)[HD],
+                                            float m, float l, int* s_flag) {
+  const bool real = row < p.rows;
+  const size_t out_row0 = (static_cast<size_t>(it.b) * p.Hq + it.g * p.G) * p.bs;
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+  if (it.nsplit == 1) {
+    if (real) {
+      uint4* dst = reinterpret_cast<uint4*>(p.out + (out_row0 + row) * HD);
+#pragma unroll
+      for (int i = 0; i < HD / 8; ++i)
+        dst[i] = make_uint4(pack_bf16x2(o[8 * i] * inv, o[8 * i + 1] * inv),
+                            pack_bf16x2(o[8 * i + 2] * inv, o[8 * i + 3] * inv),
+                            pack_bf16x2(o[8 * i + 4] * inv, o[8 * i + 5] * inv),
+                            pack_bf16x2(o[8 * i + 6] * inv, o[8 * i + 7] * inv));
+    }
+    return;
+  }
+  const size_t bg = static_cast<size_t>(it.b) * p.Hkv + it.g;
+  const size_t part0 = bg * p.max_splits * p.rows;
+  if (real) {
+    float4* dst = reinterpret_cast<float4*>(p.opart + (part0 + static_cast<size_t>(it.s) * p.rows + row) * HD);
+#pragma unroll
+    for (int i = 0; i < HD / 4; ++i)
+      dst[i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv, o[4 * i + 3] * inv);
+    p.mlpart[part0 + static_cast<size_t>(it.s) * p.rows + row] = make_float2(m, l);
+  }
+  __threadfence();
+  named_barrier_sync(1, 64);
+  if (threadIdx.x == 0) *s_flag = (atomicAdd(p.counters + bg, 1) == it.nsplit - 1);
+  named_barrier_sync(1, 64);
+  if (!*s_flag) return;
+  __threadfence();
+  if (!real) return;
+  // this CTA finished (b, g) last: log-sum-exp merge of all its splits
+  const float2* ml = p.mlpart + part0 + row;
+  float M = -INFINITY;
+  for (int s = 0; s < it.nsplit; ++s) M = fmaxf(M, __ldcg(ml + static_cast<size_t>(s) * p.rows).x);
+  const float Mu = M == -INFINITY ? 0.f : M;
+  float acc[HD];
+#pragma unroll
+  for (int i = 0; i < HD; ++i) acc[i] = 0.f;
+  float den = 0.f;
+  for (int s = 0; s < it.nsplit; ++s) {
+    const float2 v = __ldcg(ml + static_cast<size_t>(s) * p.rows);
+    const float f = v.y * exp2f(v.x - Mu);
+    den += f;
+    const float4* src = reinterpret_cast<const float4*>(p.opart + (part0 + static_cast<size_t>(s) * p.rows + row) * HD);
+#pragma unroll
+    for (int i = 0; i < HD / 4; ++i) {
+      const float4 x = __ldcg(src + i);
+      acc[4 * i] += f * x.x;
+      acc[4 * i + 1] += f * x.y;
+      acc[4 * i + 2] += f * x.z;
+      acc[4 * i + 3] += f * x.w;
+    }
+  }
+  const float dinv = den > 0.f ? 1.f / den : 0.f;
+  uint4* dst = reinterpret_cast<uint4*>(p.out + (out_row0 + row) * HD);
+#pragma unroll
+  for (int i = 0; i < HD / 8; ++i)
+    dst[i] = make_uint4(pack_bf16x2(acc[8 * i] * dinv, acc[8 * i + 1] * dinv),
+                        pack_bf16x2(acc[8 * i + 2] * dinv, acc[8 * i + 3] * dinv),
+                        pack_bf16x2(acc[8 * i + 4] * dinv, acc[8 * i + 5] * dinv),
+                        pack_bf16x2(acc[8 * i + 6] * dinv, acc[8 * i + 7] * dinv));
+}
+
+struct AttnMaps {
+  CUtensorMap k, v, q, kb, vb;
 };
 
-// Online-softmax update of one warp's 16 rows with an S tile of NT*8 keys.
-// s[j][0..1] belong to row lane/4, s[j][2..3] to row lane/4 + 8.  On return
-// s holds p = 2^(s - m) (fp32) and the running state is rescaled.
-template <int NT>
-__device__ __forceinline__ void softmax_update(SoftmaxState& st, float (&s)[NT][4]) {
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    float mx = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < NT; ++j) mx = fmaxf(mx, fmaxf(s[j][2 * h], s[j][2 * h + 1]));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    const float mnew = fmaxf(st.m[h], mx);
-    const float muse = mnew == -INFINITY ? 0.f : mnew;
-    const float corr = exp2f(st.m[h] - muse);
-    st.m[h] = mnew;
-    float rs = 0.f;
-#pragma unroll
-    for (int j = 0; j < NT; ++j) {
-      s[j][2 * h] = exp2f(s[j][2 * h] - muse);
-      s[j][2 * h + 1] = exp2f(s[j][2 * h + 1] - muse);
-      rs += s[j][2 * h] + s[j][2 * h + 1];
-    }
-    st.l[h] = st.l[h] * corr + rs;
-#pragma unroll
-    for (int n = 0; n < 16; ++n) {
-      st.o[n][2 * h] *= corr;
-      st.o[n][2 * h + 1] *= corr;
-    }
-  }
-}
-
-// A fragments (m16 x k16) of P for keys [16*kk, 16*kk+16): P = hi + lo, both
-// bf16, so the P V product keeps ~16 mantissa bits of each weight.
-__device__ __forceinline__ void p_fragments(const float (&e)[4], const float (&o)[4], uint32_t (&hi)[4],
-                                            uint32_t (&lo)[4]) {
-  const float* src[4] = {&e[0], &e[2], &o[0], &o[2]};
-#pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    const float a = src[r][0], b = src[r][1];
-    hi[r] = pack_bf16x2(a, b);
-    lo[r] = pack_bf16x2(a - bf16_lo(hi[r]), b - bf16_hi(hi[r]));
-  }
-}
-
-// One 64-key cache tile from shared memory.
-__device__ __forceinline__ void process_cache_tile(SoftmaxState& st, const uint32_t (&qa)[8][4],
-                                                   uint32_t kst, uint32_t vst, int nvalid,
-                                                   float scale_log2, int lane) {
-  float s[8][4];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
-  const int mi = lane >> 3;  // which 8x8 matrix this lane addresses
-#pragma unroll
-  for (int np = 0; np < 4; ++np) {
-    const int key = 16 * np + (mi >> 1) * 8 + (lane & 7);
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      uint32_t b0, b1, b2, b3;
-      ldmatrix_x4(kst + tile_off(key, 2 * kk + (mi & 1)), b0, b1, b2, b3);
-      mma_bf16_16816(s[2 * np], qa[kk], b0, b1);
-      mma_bf16_16816(s[2 * np + 1], qa[kk], b2, b3);
-    }
-  }
-  const int kc = 2 * (lane & 3);
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int key = 8 * j + kc + (e & 1);
-      s[j][e] = key < nvalid ? s[j][e] * scale_log2 : -INFINITY;
-    }
-  }
-  softmax_update<8>(st, s);
-#pragma unroll
-  for (int kk2 = 0; kk2 < 4; ++kk2) {
-    uint32_t ph[4], pl[4];
-    p_fragments(s[2 * kk2], s[2 * kk2 + 1], ph, pl);
-    const int key = 16 * kk2 + (mi & 1) * 8 + (lane & 7);
-#pragma unroll
-    for (int dp = 0; dp < 8; ++dp) {
-      uint32_t b0, b1, b2, b3;
-      ldmatrix_x4_trans(vst + tile_off(key, 2 * dp + (mi >> 1)), b0, b1, b2, b3);
-      mma_bf16_16816(st.o[2 * dp], ph, b0, b1);
-      mma_bf16_16816(st.o[2 * dp + 1], ph, b2, b3);
-      mma_bf16_16816(st.o[2 * dp], pl, b0, b1);
-      mma_bf16_16816(st.o[2 * dp + 1], pl, b2, b3);
-    }
-  }
-}
-
-// The bs (<= 16) block keys, read straight from global memory.
-__device__ __forceinline__ void process_block_keys(SoftmaxState& st, const uint32_t (&qa)[8][4],
-                                                   const __nv_bfloat16* __restrict__ kbh,
-                                                   const __nv_bfloat16* __restrict__ vb, int bs,
-                                                   float scale_log2, int lane) {
-  float s[2][4];
-#pragma unroll
-  for (int j = 0; j < 2; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
-  const int kc = 2 * (lane & 3);
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const int key = 8 * j + (lane >> 2);
-    const uint32_t* kr = reinterpret_cast<const uint32_t*>(kbh + static_cast<size_t>(key) * HD);
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      const uint32_t b0 = key < bs ? kr[(16 * kk + kc) / 2] : 0u;
-      const uint32_t b1 = key < bs ? kr[(16 * kk + 8 + kc) / 2] : 0u;
-      mma_bf16_16816(s[j], qa[kk], b0, b1);
-    }
-  }
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int key = 8 * j + kc + (e & 1);
-      s[j][e] = key < bs ? s[j][e] * scale_log2 : -INFINITY;
-    }
-  }
-  softmax_update<2>(st, s);
-  uint32_t ph[4], pl[4];
-  p_fragments(s[0], s[1], ph, pl);
-  const unsigned short* vr = reinterpret_cast<const unsigned short*>(vb);
-#pragma unroll
-  for (int dn = 0; dn < 16; ++dn) {
-    const int dim = 8 * dn + (lane >> 2);
-    const int k0 = kc, k1 = kc + 8;
-    auto ld = [&](int key) -> uint32_t { return key < bs ? vr[static_cast<size_t>(key) * HD + dim] : 0u; };
-    const uint32_t b0 = ld(k0) | (ld(k0 + 1) << 16);
-    const uint32_t b1 = ld(k1) | (ld(k1 + 1) << 16);
-    mma_bf16_16816(st.o[dn], ph, b0, b1);
-    mma_bf16_16816(st.o[dn], pl, b0, b1);
-  }
-}
-
-template <int STAGES>
-__global__ void __launch_bounds__(kAttnThreads) attn_main_kernel(const __grid_constant__ CUtensorMap kmap,
-                                                                 const __grid_constant__ CUtensorMap vmap,
-                                                                 const AttnParams p, int total_items) {
+__global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_constant__ AttnMaps maps,
+                                                                const AttnParams p, int total_items) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
-  // layout: [stages x 32 KB][merge slots][prefix B+1][n B][full STAGES][empty STAGES]
-  float* merge = reinterpret_cast<float*>(gbase + STAGES * kStageBytes);
-  int* s_prefix = reinterpret_cast<int*>(merge + 4 * kMergeSlotFloats);
+  const uint32_t bar0 = base + kOffBar;
+  // barrier addresses
+  const uint32_t kv_full = bar0, kv_empty = bar0 + 8 * kStages;
+  const uint32_t q_full = bar0 + 16 * kStages, q_empty = q_full + 16;
+  const uint32_t s_full = q_empty + 16, s_empty = s_full + 16;
+  const uint32_t p_full = s_empty + 16, p_empty = p_full + 16;
+  const uint32_t o_free = p_empty + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + kOffBar + 8 * kNumBars);
+  int* s_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  int* s_prefix = reinterpret_cast<int*>(tmem_slot + 4);
   int* s_n = s_prefix + (p.B + 1);
-  uint64_t* bars = reinterpret_cast<uint64_t*>((reinterpret_cast<uintptr_t>(s_n + p.B) + 7) & ~uintptr_t(7));
-  const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * STAGES;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, p.n_mt);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(kv_full + 8 * s, 1);
+      mbar_init(kv_empty + 8 * s, 1);
     }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(q_full + 8 * i, 1);
+      mbar_init(q_empty + 8 * i, 1);
+      mbar_init(s_full + 8 * i, 1);
+      mbar_init(s_empty + 8 * i, 2);
+      mbar_init(p_full + 8 * i, 2);
+      mbar_init(p_empty + 8 * i, 1);
+    }
+    mbar_init(o_free, 2);
     mbar_fence_init();
+  }
+  if (warp == 3) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
   }
   if (warp == 0) {  // per-sequence lengths and the work-item prefix
     for (int b = lane; b < p.B; b += 32) s_n[b] = clamp_seq(p.seq_len[b], p.cap, p.status);
@@ -335,177 +310,243 @@ __global__ void __launch_bounds__(kAttnThreads) attn_main_kernel(const __grid_co
       s_prefix[p.B] = acc;
     }
   }
+  tc_fence_before_sync();
   __syncthreads();
-  const int n_items = min(total_items, s_prefix[p.B]);  // items that exist for these lengths
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  const int n_items = min(total_items, s_prefix[p.B]);
+  const int rows_pad = p.rows > 32 ? 64 : 32;
 
-  if (warp == kConsumerWarps) {
-    // ---------------- producer: TMA K/V tiles into the stage ring ----------
+  if (warp == 2) {
+    // ------------------------------------------------------------ producer
     if (lane == 0) {
-      tma_prefetch_desc(&kmap);
-      tma_prefetch_desc(&vmap);
+      tma_prefetch_desc(&maps.k);
+      tma_prefetch_desc(&maps.v);
+      tma_prefetch_desc(&maps.q);
       const uint64_t pol = l2_policy_evict_first();
-      int stage = 0;
-      uint32_t phase = 0;
-      for (int w = blockIdx.x; w < n_items; w += gridDim.x) {
+      int stage = 0, qb = 0;
+      uint32_t kv_ph = 0, q_ph = 0;
+      bool ok = true;
+      for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
         const Item it = decode_item(w, s_prefix, s_n, p);
+        if (!(ok = mbar_wait(q_empty + 8 * qb, q_ph ^ 1u, p.status))) break;
+        mbar_arrive_expect_tx(q_full + 8 * qb, 2 * rows_pad * kRowBytes);
+        const int qrow = (it.b * p.Hq + it.g * p.G) * p.bs;
+        const uint32_t qdst = base + kOffQ + 2 * qb * kQBox;
+        tma_load_2d(qdst, &maps.q, q_full + 8 * qb, 0, qrow);
+        tma_load_2d(qdst + kQBox, &maps.q, q_full + 8 * qb, 64, qrow);
+        if (++qb == 2) {
+          qb = 0;
+          q_ph ^= 1u;
+        }
         const int rowbase = ((p.layer * p.B + it.b) * p.Hkv + it.g) * p.cap;
-        for (int t = 0; t < it.ntiles; ++t) {
-          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, p.status)) return;
-          const uint32_t fb = full0 + 8 * stage;
+        const int brow = (it.b * p.Hkv + it.g) * p.bs;
+        for (int t = 0; t < it.nt; ++t) {
+          if (!(ok = mbar_wait(kv_empty + 8 * stage, kv_ph ^ 1u, p.status))) break;
+          const uint32_t fb = kv_full + 8 * stage;
           mbar_arrive_expect_tx(fb, kStageBytes);
-          const uint32_t dst = base + stage * kStageBytes;
-          const int y = rowbase + it.kstart + t * kTile;
-          tma_load_2d_hint(dst, &kmap, fb, 0, y, pol);
-          tma_load_2d_hint(dst + kHalfTileBytes, &kmap, fb, 64, y, pol);
-          tma_load_2d_hint(dst + 2 * kHalfTileBytes, &vmap, fb, 0, y, pol);
-          tma_load_2d_hint(dst + 3 * kHalfTileBytes, &vmap, fb, 64, y, pol);
-          if (++stage == STAGES) {
+          const uint32_t dst = base + kOffKV + stage * kStageBytes;
+          if (t < it.ntiles) {
+            const int y = rowbase + it.kstart + t * kTile;
+            tma_load_2d_hint(dst, &maps.k, fb, 0, y, pol);
+            tma_load_2d_hint(dst + kHalfTileBytes, &maps.k, fb, 64, y, pol);
+            tma_load_2d_hint(dst + 2 * kHalfTileBytes, &maps.v, fb, 0, y, pol);
+            tma_load_2d_hint(dst + 3 * kHalfTileBytes, &maps.v, fb, 64, y, pol);
+          } else {  // the block's own keys and values
+            tma_load_2d(dst, &maps.kb, fb, 0, brow);
+            tma_load_2d(dst + kHalfTileBytes, &maps.kb, fb, 64, brow);
+            tma_load_2d(dst + 2 * kHalfTileBytes, &maps.vb, fb, 0, brow);
+            tma_load_2d(dst + 3 * kHalfTileBytes, &maps.vb, fb, 64, brow);
+          }
+          if (++stage == kStages) {
             stage = 0;
-            phase ^= 1u;
+            kv_ph ^= 1u;
           }
         }
       }
     }
-    return;  // the producer takes no part in the consumers' named barriers
-  }
-
-  // ---------------- consumers ------------------------------------------------
-  const int mt = warp % p.n_mt;
-  const int wg = warp / p.n_mt;
-  const bool active = warp < p.n_mt * p.n_wg;
-  int stage = 0;
-  uint32_t phase = 0;
-  bool ok = true;
-  for (int w = blockIdx.x; w < n_items; w += gridDim.x) {
-    const Item it = decode_item(w, s_prefix, s_n, p);
-    SoftmaxState st;
-    st.m[0] = st.m[1] = -INFINITY;
-    st.l[0] = st.l[1] = 0.f;
+  } else if (warp == 3) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0, qb = 0, sb = 0, pb = 0;
+      uint32_t kv_ph = 0, q_ph = 0, s_ph = 0, p_ph = 0, o_ph = 0;
+      bool ok = true;
+      auto pv = [&](int st, bool first) -> bool {
+        if (!mbar_wait(p_full + 8 * pb, p_ph, p.status)) return false;
+        if (first && !mbar_wait(o_free, o_ph ^ 1u, p.status)) return false;
+        tc_fence_after_sync();
+        const uint32_t vbase = base + kOffKV + st * kStageBytes + 2 * kHalfTileBytes;
+        const uint64_t vdesc = umma_desc_mnmajor_sw128(vbase, kHalfTileBytes, 1024);
 #pragma unroll
-    for (int n = 0; n < 16; ++n) st.o[n][0] = st.o[n][1] = st.o[n][2] = st.o[n][3] = 0.f;
-    uint32_t qa[8][4];
-    {
-      const size_t qrow0 = (static_cast<size_t>(it.b) * p.Hq + it.g * p.G) * p.bs;
-      const int r0 = mt * 16 + (lane >> 2), r1 = r0 + 8;
-      const uint32_t* q0 = reinterpret_cast<const uint32_t*>(p.qh + (qrow0 + r0) * HD);
-      const uint32_t* q1 = reinterpret_cast<const uint32_t*>(p.qh + (qrow0 + r1) * HD);
-      const int kc = 2 * (lane & 3);
+        for (int h = 0; h < 2; ++h) {
+          const uint64_t pdesc = umma_desc_kmajor_sw128(base + kOffP + (2 * pb + h) * kPHalf);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        qa[kk][0] = r0 < p.rows ? q0[(16 * kk + kc) / 2] : 0u;
-        qa[kk][1] = r1 < p.rows ? q1[(16 * kk + kc) / 2] : 0u;
-        qa[kk][2] = r0 < p.rows ? q0[(16 * kk + 8 + kc) / 2] : 0u;
-        qa[kk][3] = r1 < p.rows ? q1[(16 * kk + 8 + kc) / 2] : 0u;
-      }
-    }
-    for (int t = 0; t < it.ntiles; ++t) {
-      if (active && ok && (t % p.n_wg) == wg) {
-        ok = mbar_wait(full0 + 8 * stage, phase, p.status);
-        if (ok) {
-          const uint32_t kst = base + stage * kStageBytes;
-          const int nvalid = min(kTile, it.kend - (it.kstart + t * kTile));
-          process_cache_tile(st, qa, kst, kst + 2 * kHalfTileBytes, nvalid, p.scale_log2, lane);
+          for (int kk = 0; kk < 4; ++kk)
+            umma_bf16(tmem + 128, pdesc + 2 * kk, vdesc + 128 * kk, kIdescPV, (first && h == 0 && kk == 0) ? 0u : 1u);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(empty0 + 8 * stage);
-      }
-      if (++stage == STAGES) {
-        stage = 0;
-        phase ^= 1u;
-      }
-    }
-    if (it.last && active && wg == 0) {
-      const size_t kb0 = (static_cast<size_t>(it.b) * p.Hkv + it.g) * p.bs * HD;
-      process_block_keys(st, qa, p.kbh + kb0, p.vb + kb0, p.bs, p.scale_log2, lane);
-    }
-    // ---- merge the warp groups' partial softmax states through shared memory
-    named_barrier_sync(1, kConsumerWarps * 32);
-    if (active) {
-      float* slot = merge + (wg * p.n_mt + mt) * kMergeSlotFloats;
-      float l0 = st.l[0], l1 = st.l[1];
-      l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-      l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-      l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-      l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-      const int r0 = lane >> 2, kc = 2 * (lane & 3);
+        umma_commit(kv_empty + 8 * st);
+        umma_commit(p_empty + 8 * pb);
+        if (++pb == 2) {
+          pb = 0;
+          p_ph ^= 1u;
+        }
+        if (first) o_ph ^= 1u;
+        return true;
+      };
+      for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+        const Item it = decode_item(w, s_prefix, s_n, p);
+        if (!(ok = mbar_wait(q_full + 8 * qb, q_ph, p.status))) break;
+        tc_fence_after_sync();
+        const uint32_t qa = base + kOffQ + 2 * qb * kQBox;
+        int prev = -1;
+        for (int t = 0; t < it.nt && ok; ++t) {
+          if (!(ok = mbar_wait(kv_full + 8 * stage, kv_ph, p.status))) break;
+          if (!(ok = mbar_wait(s_empty + 8 * sb, s_ph ^ 1u, p.status))) break;
+          tc_fence_after_sync();
+          const uint32_t kb = base + kOffKV + stage * kStageBytes;
 #pragma unroll
-      for (int n = 0; n < 16; ++n) {
-        slot[r0 * HD + 8 * n + kc] = st.o[n][0];
-        slot[r0 * HD + 8 * n + kc + 1] = st.o[n][1];
-        slot[(r0 + 8) * HD + 8 * n + kc] = st.o[n][2];
-        slot[(r0 + 8) * HD + 8 * n + kc + 1] = st.o[n][3];
-      }
-      if ((lane & 3) == 0) {
-        slot[16 * HD + r0] = st.m[0];
-        slot[16 * HD + r0 + 8] = st.m[1];
-        slot[16 * HD + 16 + r0] = l0;
-        slot[16 * HD + 16 + r0 + 8] = l1;
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t ad = umma_desc_kmajor_sw128(qa + (kk >> 2) * kQBox) + 2 * (kk & 3);
+            const uint64_t bd = umma_desc_kmajor_sw128(kb + (kk >> 2) * kHalfTileBytes) + 2 * (kk & 3);
+            umma_bf16(tmem + 64 * sb, ad, bd, kIdescQK, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(s_full + 8 * sb);
+          if (++sb == 2) {
+            sb = 0;
+            s_ph ^= 1u;
+          }
+          if (prev >= 0) ok = pv(prev, t == 1);
+          prev = stage;
+          if (++stage == kStages) {
+            stage = 0;
+            kv_ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(q_empty + 8 * qb);
+        if (++qb == 2) {
+          qb = 0;
+          q_ph ^= 1u;
+        }
+        ok = pv(prev, it.nt == 1);
       }
     }
-    named_barrier_sync(1, kConsumerWarps * 32);
-    const bool single = it.nsplit == 1;
-    const size_t part_row0 = ((static_cast<size_t>(it.b) * p.Hkv + it.g) * p.max_splits + it.s) * p.rows;
-    const size_t out_row0 = (static_cast<size_t>(it.b) * p.Hq + it.g * p.G) * p.bs;
-    for (int idx = threadIdx.x; idx < p.rows * HD; idx += kConsumerWarps * 32) {
-      const int row = idx / HD, e = idx % HD;
-      const int rmt = row / 16, rr = row % 16;
-      float M = -INFINITY;
-      for (int g2 = 0; g2 < p.n_wg; ++g2)
-        M = fmaxf(M, merge[(g2 * p.n_mt + rmt) * kMergeSlotFloats + 16 * HD + rr]);
-      const float Mu = M == -INFINITY ? 0.f : M;
-      float L = 0.f, O = 0.f;
-      for (int g2 = 0; g2 < p.n_wg; ++g2) {
-        const float* sl = merge + (g2 * p.n_mt + rmt) * kMergeSlotFloats;
-        const float f = exp2f(sl[16 * HD + rr] - Mu);
-        L += sl[16 * HD + 16 + rr] * f;
-        O += sl[rr * HD + e] * f;
+  } else {
+    // ------------------------------------------------ softmax + epilogue
+    const int row = 32 * warp + lane;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(32 * warp) << 16);
+    int sb = 0, pb = 0;
+    uint32_t s_ph = 0;
+    int pcnt[2] = {0, 0};
+    bool ok = true;
+    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+      const Item it = decode_item(w, s_prefix, s_n, p);
+      float m_used = -INFINITY, l = 0.f;
+      for (int t = 0; t < it.nt; ++t) {
+        if (!(ok = mbar_wait(s_full + 8 * sb, s_ph, p.status))) break;
+        tc_fence_after_sync();
+        uint32_t sr[64];
+        tmem_ld_32cols(tl + 64 * sb, *reinterpret_cast<uint32_t(*)[32]>(sr));
+        tmem_ld_32cols(tl + 64 * sb + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+        tmem_ld_wait();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_empty + 8 * sb);
+        if (++sb == 2) {
+          sb = 0;
+          s_ph ^= 1u;
+        }
+        const int nvalid = t < it.ntiles ? min(kTile, it.kend - (it.kstart + t * kTile)) : p.bs;
+        float x[64];
+        float mt = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          x[i] = i < nvalid ? __uint_as_float(sr[i]) * p.scale_log2 : -INFINITY;
+          mt = fmaxf(mt, x[i]);
+        }
+        if (t == 0) {
+          m_used = mt;
+        } else {
+          const bool need = mt > m_used + kRescaleLog2;
+          if (__any_sync(0xffffffffu, need)) {
+            // O must be complete up to tile t-1 before it is rescaled
+            const int xb = pb ^ 1;
+            if (!(ok = mbar_wait(p_empty + 8 * xb, (pcnt[xb] - 1) & 1, p.status))) break;
+            tc_fence_after_sync();
+            const float f = need ? exp2f(m_used - mt) : 1.f;
+            if (need) {
+              l *= f;
+              m_used = mt;
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              uint32_t r[32];
+              tmem_ld_32cols(tl + 128 + 32 * c, r);
+              tmem_ld_wait();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * f);
+              tmem_st_32cols(tl + 128 + 32 * c, r);
+            }
+            tmem_st_wait();
+            tc_fence_before_sync();
+          }
+        }
+        const float mu = m_used == -INFINITY ? 0.f : m_used;
+        float ls = 0.f;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          x[i] = exp2f(x[i] - mu);
+          ls += x[i];
+        }
+        l += ls;
+        // P[pb] is free once the P V product that last read it has completed
+        if (pcnt[pb] > 0 && !(ok = mbar_wait(p_empty + 8 * pb, (pcnt[pb] - 1) & 1, p.status))) break;
+        uint8_t* ph = gbase + kOffP + (2 * pb) * kPHalf + row * kRowBytes;
+        uint8_t* pl = ph + kPHalf;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint32_t hv[4], lv[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float a = x[8 * c + 2 * j], bb = x[8 * c + 2 * j + 1];
+            hv[j] = pack_bf16x2(a, bb);
+            lv[j] = pack_bf16x2(a - bf16_lo(hv[j]), bb - bf16_hi(hv[j]));
+          }
+          const int off = ((c ^ (row & 7)) << 4);
+          *reinterpret_cast<uint4*>(ph + off) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+          *reinterpret_cast<uint4*>(pl + off) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full + 8 * pb);
+        ++pcnt[pb];
+        pb ^= 1;
       }
-      const float val = L > 0.f ? O / L : 0.f;
-      if (single) {
-        p.out[(out_row0 + row) * HD + e] = __float2bfloat16_rn(val);
-      } else {
-        p.opart[(part_row0 + row) * HD + e] = val;
-        if (e == 0) p.mlpart[part_row0 + row] = make_float2(M, L);
+      if (!ok) break;
+      // item end: the last P V product must have landed in O
+      const int xb = pb ^ 1;
+      if (!(ok = mbar_wait(p_empty + 8 * xb, (pcnt[xb] - 1) & 1, p.status))) break;
+      tc_fence_after_sync();
+      float o[HD];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tmem_ld_32cols(tl + 128 + 32 * c, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[32 * c + i] = __uint_as_float(r[i]);
       }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(o_free);
+      finish_item(it, p, row, o, m_used, l, s_flag);
     }
   }
-}
-
-constexpr int kCombineThreads = 256;
-
-// Log-sum-exp merge of the split partials of one (sequence, KV head): one warp
-// per output row, each lane owning 4 of the 128 dims.
-__global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(const AttnParams p) {
-  const int b = blockIdx.x / p.Hkv, g = blockIdx.x % p.Hkv;
-  const int n = min(max(p.seq_len[b], 0), p.cap);
-  const int first = p.window > 0 ? max(0, n - p.window) : 0;
-  const int ns = n_splits(n - first, p.chunk);
-  if (ns <= 1) return;
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const size_t part0 = (static_cast<size_t>(b) * p.Hkv + g) * p.max_splits * p.rows;
-  const size_t out_row0 = (static_cast<size_t>(b) * p.Hq + g * p.G) * p.bs;
-  for (int row = warp; row < p.rows; row += kCombineThreads / 32) {
-    float M = -INFINITY;
-    for (int s = lane; s < ns; s += 32) M = fmaxf(M, p.mlpart[part0 + static_cast<size_t>(s) * p.rows + row].x);
-    M = warp_max(M);
-    const float Mu = M == -INFINITY ? 0.f : M;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float den = 0.f;
-#pragma unroll 4
-    for (int s = 0; s < ns; ++s) {
-      const size_t r = part0 + static_cast<size_t>(s) * p.rows + row;
-      const float2 ml = p.mlpart[r];
-      const float4 o = reinterpret_cast<const float4*>(p.opart + r * HD)[lane];
-      const float f = ml.y * exp2f(ml.x - Mu);
-      den += f;
-      acc.x += f * o.x;
-      acc.y += f * o.y;
-      acc.z += f * o.z;
-      acc.w += f * o.w;
-    }
-    const float inv = den > 0.f ? 1.f / den : 0.f;
-    uint2 packed = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
-    reinterpret_cast<uint2*>(p.out + (out_row0 + row) * HD)[lane] = packed;
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 3) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kTmemCols);
   }
 }
 
@@ -594,18 +635,12 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const float* __restrict__
     out[((static_cast<size_t>(b) * Hq + h) * bs + j) * HD + tid] = o[j] / s_l[j];
 }
 
+
 int pick_chunk(int B, int Hkv, int cap, int window) {
   const long keys = window > 0 ? std::min(window, cap) : cap;
   long c = (static_cast<long>(B) * Hkv * keys) / 2400;
   c = (c + 63) / 64 * 64;
   return static_cast<int>(std::min<long>(4096, std::max<long>(256, c)));
-}
-
-constexpr int kStages = 4;
-
-size_t attn_main_smem(int B) {
-  return 1024 + static_cast<size_t>(kStages) * kStageBytes + 4 * kMergeSlotFloats * sizeof(float) +
-         (2 * static_cast<size_t>(B) + 1) * sizeof(int) + 8 + 16 * kStages;
 }
 
 }  // namespace
@@ -620,7 +655,8 @@ size_t attn_ws_bytes(int B, int bs, int Hq, int Hkv, int cap, int window, dflash
              align256(static_cast<size_t>(B) * Hkv * bs * HD * esz);
   if (dt == DFLASH_BF16)
     s += align256(static_cast<size_t>(B) * Hkv * max_splits * rows * HD * sizeof(float)) +
-         align256(static_cast<size_t>(B) * Hkv * max_splits * rows * sizeof(float2));
+         align256(static_cast<size_t>(B) * Hkv * max_splits * rows * sizeof(float2)) +
+         align256(static_cast<size_t>(B) * Hkv * sizeof(int));
   return s + 256;
 }
 
@@ -628,7 +664,6 @@ dflash_status launch_block_attn(int layer, int B, int bs, int Hq, const void* q,
                                 const void* vb, const void* qg, const void* kg, float theta,
                                 float eps, const dflash_kv_cache& c, int window, void* out, void* ws,
                                 cudaStream_t st, const DeviceInfo& dev) {
-  if (B > kMaxBatch) return fail(DFLASH_ERR_UNSUPPORTED, "block_attn: batch must be <= 4096");
   const int Hkv = c.num_kv_heads;
   const int G = Hq / Hkv;
   InvFreq inv;
@@ -640,7 +675,7 @@ dflash_status launch_block_attn(int layer, int B, int bs, int Hq, const void* q,
     float* kbh = w.take<float>(static_cast<size_t>(B) * Hkv * bs * HD);
     attn_prologue_kernel<float><<<B * bs, 256, 0, st>>>(
         static_cast<const float*>(q), static_cast<const float*>(kb), static_cast<const float*>(qg),
-        static_cast<const float*>(kg), c.seq_len, B, bs, Hq, Hkv, c.capacity, eps, inv, qh, kbh,
+        static_cast<const float*>(kg), c.seq_len, B, bs, Hq, Hkv, c.capacity, eps, inv, qh, kbh, nullptr, 0,
         dev.status);
     attn_f32_kernel<<<B * Hq, 128, 0, st>>>(qh, kbh, static_cast<const float*>(vb),
                                             static_cast<const float*>(c.k), static_cast<const float*>(c.v),
@@ -649,6 +684,7 @@ dflash_status launch_block_attn(int layer, int B, int bs, int Hq, const void* q,
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? DFLASH_OK : cuda_fail(e, "fp32 block attention launch");
   }
+  if (B > kMaxBatch) return fail(DFLASH_ERR_UNSUPPORTED, "block_attn: bf16 batch must be <= 2048");
   AttnParams p;
   p.B = B;
   p.bs = bs;
@@ -662,8 +698,6 @@ dflash_status launch_block_attn(int layer, int B, int bs, int Hq, const void* q,
   const int keys = window > 0 ? std::min(window, c.capacity) : c.capacity;
   p.max_splits = n_splits(keys, p.chunk);
   p.rows = G * bs;
-  p.n_mt = (p.rows + 15) / 16;
-  p.n_wg = p.n_mt == 3 ? 1 : 4 / p.n_mt;
   p.seq_len = c.seq_len;
   auto* qh = w.take<__nv_bfloat16>(static_cast<size_t>(B) * Hq * bs * HD);
   auto* kbh = w.take<__nv_bfloat16>(static_cast<size_t>(B) * Hkv * bs * HD);
@@ -673,35 +707,36 @@ dflash_status launch_block_attn(int layer, int B, int bs, int Hq, const void* q,
   p.out = static_cast<__nv_bfloat16*>(out);
   p.opart = w.take<float>(static_cast<size_t>(B) * Hkv * p.max_splits * p.rows * HD);
   p.mlpart = w.take<float2>(static_cast<size_t>(B) * Hkv * p.max_splits * p.rows);
+  p.counters = w.take<int>(static_cast<size_t>(B) * Hkv);
   p.scale_log2 = 1.4426950408889634f * scale;
   p.status = dev.status;
 
-  CUtensorMap kmap, vmap;
+  AttnMaps maps;
   const uint64_t rows = static_cast<uint64_t>(c.num_layers) * c.batch * Hkv * c.capacity;
-  dflash_status s = make_tmap_bf16_2d(&kmap, c.k, rows, HD, kTile, 64);
-  if (s) return s;
-  s = make_tmap_bf16_2d(&vmap, c.v, rows, HD, kTile, 64);
+  dflash_status s = make_tmap_bf16_2d(&maps.k, c.k, rows, HD, kTile, 64);
+  if (!s) s = make_tmap_bf16_2d(&maps.v, c.v, rows, HD, kTile, 64);
+  if (!s) s = make_tmap_bf16_2d(&maps.q, qh, static_cast<uint64_t>(B) * Hq * bs, HD, p.rows > 32 ? 64 : 32, 64);
+  if (!s) s = make_tmap_bf16_2d(&maps.kb, kbh, static_cast<uint64_t>(B) * Hkv * bs, HD, kTile, 64);
+  if (!s) s = make_tmap_bf16_2d(&maps.vb, vb, static_cast<uint64_t>(B) * Hkv * bs, HD, kTile, 64);
   if (s) return s;
 
   attn_prologue_kernel<__nv_bfloat16><<<B * bs, 256, 0, st>>>(
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(kb),
-      static_cast<const __nv_bfloat16*>(qg), static_cast<const __nv_bfloat16*>(kg), c.seq_len, B, bs,
-      Hq, Hkv, c.capacity, eps, inv, qh, kbh, dev.status);
+      static_cast<const __nv_bfloat16*>(qg), static_cast<const __nv_bfloat16*>(kg), c.seq_len, B, bs, Hq, Hkv,
+      c.capacity, eps, inv, qh, kbh, p.counters, B * Hkv, dev.status);
 
   const size_t smem = attn_main_smem(B);
   if (smem > dev.max_smem_optin) return fail(DFLASH_ERR_UNSUPPORTED, "block_attn: shared memory");
   static int configured_device = -1;
   if (configured_device != dev.device) {
-    cudaError_t e = cudaFuncSetAttribute(attn_main_kernel<kStages>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(dev.max_smem_optin));
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attn_main_kernel)");
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attn_tc_kernel)");
     configured_device = dev.device;
   }
   const long upper = static_cast<long>(B) * Hkv * p.max_splits;
   const int grid = static_cast<int>(std::min<long>(upper, dev.num_sms));
-  attn_main_kernel<kStages><<<grid, kAttnThreads, smem, st>>>(kmap, vmap, p, static_cast<int>(upper));
-  attn_combine_kernel<<<B * Hkv, kCombineThreads, 0, st>>>(p);
+  attn_tc_kernel<<<grid, kTcThreads, smem, st>>>(maps, p, static_cast<int>(upper));
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? DFLASH_OK : cuda_fail(e, "block attention launch");
 }
