@@ -81,6 +81,7 @@ __global__ void __launch_bounds__(256) attn_prologue_kernel(
     const T* __restrict__ kg, const int32_t* __restrict__ seq_len, int B, int bs, int Hq, int Hkv,
     int cap, float eps, InvFreq inv_freq, T* __restrict__ qh, T* __restrict__ kbh,
     int* __restrict__ counters, int n_counters, unsigned* status) {
+  pdl_launch_dependents();
   if (blockIdx.x == 0 && counters)
     for (int i = threadIdx.x; i < n_counters; i += blockDim.x) counters[i] = 0;
   const int b = blockIdx.x / bs, j = blockIdx.x % bs;
@@ -144,21 +145,37 @@ struct Item {
   bool last;
 };
 
-__device__ __forceinline__ Item decode_item(int w, const int* s_prefix, const int* s_n, const AttnParams& p) {
-  int lo = 0, hi = p.B - 1;
-  while (lo < hi) {  // largest b with prefix[b] <= w
-    const int mid = (lo + hi + 1) >> 1;
-    if (s_prefix[mid] <= w) lo = mid; else hi = mid - 1;
-  }
+// Work items in the order the queue hands them out: first every non-last
+// split (all `chunk` keys long), then the last split of every (b, g) (the
+// ragged remainder plus the block keys) -- largest first, so the dynamic queue
+// balances like longest-processing-time scheduling.
+__device__ __forceinline__ Item decode_item(int w, const int* s_full_prefix, const int* s_n, const AttnParams& p) {
   Item it;
-  it.b = lo;
-  const int n = s_n[lo];
+  const int F = s_full_prefix[p.B];
+  int b, g, s;
+  if (w < F) {
+    int lo = 0, hi = p.B - 1;
+    while (lo < hi) {  // largest b with prefix[b] <= w
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_full_prefix[mid] <= w) lo = mid; else hi = mid - 1;
+    }
+    b = lo;
+    const int nfull = (s_full_prefix[b + 1] - s_full_prefix[b]) / p.Hkv;
+    const int r = w - s_full_prefix[b];
+    g = r / nfull;
+    s = r % nfull;
+  } else {
+    b = (w - F) / p.Hkv;
+    g = (w - F) % p.Hkv;
+    s = -1;
+  }
+  const int n = s_n[b];
   const int first = p.window > 0 ? max(0, n - p.window) : 0;
   const int ncache = n - first;
+  it.b = b;
+  it.g = g;
   it.nsplit = n_splits(ncache, p.chunk);
-  const int r = w - s_prefix[lo];
-  it.g = r / it.nsplit;
-  it.s = r % it.nsplit;
+  it.s = s < 0 ? it.nsplit - 1 : s;
   it.kstart = first + it.s * p.chunk;
   it.kend = first + min(ncache, (it.s + 1) * p.chunk);
   it.ntiles = it.kend > it.kstart ? (it.kend - it.kstart + kTile - 1) / kTile : 0;
@@ -167,29 +184,52 @@ __device__ __forceinline__ Item decode_item(int w, const int* s_prefix, const in
   return it;
 }
 
-constexpr int kStages = 4;
-constexpr int kTcThreads = 128;
-constexpr int kRowBytes = 128;                        // 64 bf16
-constexpr int kPHalf = 64 * kRowBytes;                // P hi or lo of one buffer: 64 rows
-constexpr int kQBox = 64 * kRowBytes;                 // one 64-dim half of Q: 64 rows
-constexpr int kOffP = 0;                              // P[buf][half]  at (2*buf + half) * kPHalf
-constexpr int kOffQ = 4 * kPHalf;                     // Q[buf][box]   at kOffQ + (2*buf + box) * kQBox
-constexpr int kOffKV = kOffQ + 4 * kQBox;             // stage s at kOffKV + s * kStageBytes
-constexpr int kOffBar = kOffKV + kStages * kStageBytes;
-constexpr int kNumBars = 2 * kStages + 13;
-constexpr int kTmemCols = 256;                        // S buffers at 0 and 64, O at 128
+constexpr int kMaxStages = 6;
+constexpr int kTcThreads = 224;   // 7 warps, roles below
+constexpr int kRowBytes = 128;    // 64 bf16
+constexpr int kItemRing = 4;
+constexpr int kItemConsumers = 6; // QK issuer, PV issuer, 2 softmax warps, 2 epilogue warps
+constexpr int kNumBars = 2 * kMaxStages + 2 * 2 * 6 + 2 * kItemRing;
+constexpr int kTmemCols = 512;
+// tensor-memory columns: S[2] 64 each, O[2] 128 each, P[2] = {hi 32, lo 32}
+// (bf16 pairs packed per 32-bit column)
+constexpr uint32_t kColS = 0, kColO0 = 128, kColP = 256, kColO1 = 384;
 constexpr uint32_t kIdescQK = umma_idesc_bf16(128, 64, false);
 constexpr uint32_t kIdescPV = umma_idesc_bf16(128, 128, true);
 constexpr float kRescaleLog2 = 8.0f;
 
-size_t attn_main_smem(int B) {
-  return 1024 + kOffBar + 8 * kNumBars + 16 + (2 * static_cast<size_t>(B) + 1) * sizeof(int);
+__device__ __forceinline__ uint32_t col_o(int ob) { return ob ? kColO1 : kColO0; }
+
+// Shared-memory plan (byte offsets from the 1024-aligned base): Q double
+// buffer (the A operand of S = Q K^T; the M=128 MMA reads 128 rows, the rows
+// past rows_pad fall on the following buffers and only feed accumulator lanes
+// that are never read), then the K/V stage ring, barriers and small arrays.
+struct TcLayout {
+  int rows_pad, half;   // half = rows_pad * 128 bytes: one 64-dim half of Q
+  int off_q, off_kv, stages, off_bar, off_misc, bytes;
+};
+
+__host__ __device__ inline TcLayout tc_layout(int rows, int B, int smem_limit) {
+  TcLayout L;
+  L.rows_pad = rows > 32 ? 64 : 32;
+  L.half = L.rows_pad * kRowBytes;
+  L.off_q = 0;                      // Q[buf][box] at (2*buf + box) * half
+  L.off_kv = 4 * L.half;            // stage s at off_kv + s * kStageBytes
+  const int misc = 64 + 2 * 64 * 8 + (2 * B + 1) * 4;  // tmem slot, flags, items, (m, l)[2][64], prefix, n
+  const int fixed = 1024 + L.off_kv + 8 * kNumBars + misc;
+  int st = (smem_limit - fixed) / kStageBytes;
+  L.stages = st > kMaxStages ? kMaxStages : st;
+  L.off_bar = L.off_kv + L.stages * kStageBytes;
+  L.off_misc = L.off_bar + 8 * kNumBars;
+  L.bytes = 1024 + L.off_misc + misc;
+  return L;
 }
 
-// Thread `row` (< rows) owns one query row: write its final output, or its
-// normalised partial and (m, l); the last CTA to finish a (b, g) merges.
+// Thread `row` owns one query row: write its final output, or its normalised
+// partial and (m, l); the last CTA to finish a (b, g) merges the splits.
+// `bar_id` / `leader` name the named barrier and thread of the 64 epilogue threads.
 __device__ __forceinline__ void finish_item(const Item& it, const AttnParams& p, int row, const float (&o)[HD],
-                                            float m, float l, int* s_flag) {
+                                            float m, float l, int* s_flag, int bar_id, int leader) {
   const bool real = row < p.rows;
   const size_t out_row0 = (static_cast<size_t>(it.b) * p.Hq + it.g * p.G) * p.bs;
   const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -215,10 +255,12 @@ __device__ __forceinline__ void finish_item(const Item& it, const AttnParams& p,
     p.mlpart[part0 + static_cast<size_t>(it.s) * p.rows + row] = make_float2(m, l);
   }
   __threadfence();
-  named_barrier_sync(1, 64);
-  if (threadIdx.x == 0) *s_flag = (atomicAdd(p.counters + bg, 1) == it.nsplit - 1);
-  named_barrier_sync(1, 64);
-  if (!*s_flag) return;
+  named_barrier_sync(bar_id, 64);
+  if (threadIdx.x == leader) *s_flag = (atomicAdd(p.counters + bg, 1) == it.nsplit - 1);
+  named_barrier_sync(bar_id, 64);
+  const int last = *s_flag;
+  named_barrier_sync(bar_id, 64);  // s_flag is reused by the next item
+  if (!last) return;
   __threadfence();
   if (!real) return;
   // this CTA finished (b, g) last: log-sum-exp merge of all its splits
@@ -258,27 +300,58 @@ struct AttnMaps {
   CUtensorMap k, v, q, kb, vb;
 };
 
+// Ring of two-phase mbarriers shared by one producer role and one consumer role.
+struct Ring {
+  int idx = 0;
+  uint32_t phase = 0;
+  __device__ __forceinline__ void next(int n) {
+    if (++idx == n) {
+      idx = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
+// Reads the next work item from the shared item ring (-1 = no more work).
+__device__ __forceinline__ int next_item(uint32_t it_full, uint32_t it_empty, const int* s_item, Ring& r,
+                                         unsigned* status, bool warp_wide) {
+  if (!mbar_wait(it_full + 8 * r.idx, r.phase, status)) return -1;
+  const int w = s_item[r.idx];
+  if (warp_wide) __syncwarp();
+  if (!warp_wide || (threadIdx.x & 31) == 0) mbar_arrive(it_empty + 8 * r.idx);
+  r.next(kItemRing);
+  return w;
+}
+
+// Roles: warp 0/1 softmax of query rows 0-31 / 32-63 (tensor-memory lane
+// quarters 0/1), warp 2 TMA producer, warp 3 S = Q K^T issuer, warp 4/5
+// epilogue of rows 0-31 / 32-63, warp 6 O += P V issuer.
 __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_constant__ AttnMaps maps,
-                                                                const AttnParams p, int total_items) {
+                                                                const AttnParams p, const TcLayout lay) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
-  const uint32_t bar0 = base + kOffBar;
-  // barrier addresses
-  const uint32_t kv_full = bar0, kv_empty = bar0 + 8 * kStages;
-  const uint32_t q_full = bar0 + 16 * kStages, q_empty = q_full + 16;
+  const int S = lay.stages;
+  const int half = lay.half;
+  const uint32_t bar0 = base + lay.off_bar;
+  const uint32_t kv_full = bar0, kv_empty = bar0 + 8 * kMaxStages;
+  const uint32_t q_full = bar0 + 16 * kMaxStages, q_empty = q_full + 16;
   const uint32_t s_full = q_empty + 16, s_empty = s_full + 16;
   const uint32_t p_full = s_empty + 16, p_empty = p_full + 16;
-  const uint32_t o_free = p_empty + 16;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + kOffBar + 8 * kNumBars);
+  const uint32_t o_full = p_empty + 16, o_free = o_full + 16;
+  const uint32_t ml_full = o_free + 16, ml_empty = ml_full + 16;
+  const uint32_t it_full = ml_empty + 16, it_empty = it_full + 8 * kItemRing;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + lay.off_misc);
   int* s_flag = reinterpret_cast<int*>(tmem_slot + 1);
-  int* s_prefix = reinterpret_cast<int*>(tmem_slot + 4);
+  int* s_item = reinterpret_cast<int*>(tmem_slot + 8);            // kItemRing entries
+  float2* s_ml = reinterpret_cast<float2*>(gbase + lay.off_misc + 64);  // [2][64] (m, l) per row
+  int* s_prefix = reinterpret_cast<int*>(gbase + lay.off_misc + 64 + 2 * 64 * 8);
   int* s_n = s_prefix + (p.B + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(kv_full + 8 * s, 1);
       mbar_init(kv_empty + 8 * s, 1);
     }
@@ -289,15 +362,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       mbar_init(s_empty + 8 * i, 2);
       mbar_init(p_full + 8 * i, 2);
       mbar_init(p_empty + 8 * i, 1);
+      mbar_init(o_full + 8 * i, 1);
+      mbar_init(o_free + 8 * i, 2);
+      mbar_init(ml_full + 8 * i, 2);
+      mbar_init(ml_empty + 8 * i, 2);
     }
-    mbar_init(o_free, 2);
+    for (int i = 0; i < kItemRing; ++i) {
+      mbar_init(it_full + 8 * i, 1);
+      mbar_init(it_empty + 8 * i, kItemConsumers);
+    }
     mbar_fence_init();
   }
   if (warp == 3) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 0) {  // per-sequence lengths and the work-item prefix
+  if (warp == 0) {  // per-sequence lengths and the prefix of full (non-last) splits
     for (int b = lane; b < p.B; b += 32) s_n[b] = clamp_seq(p.seq_len[b], p.cap, p.status);
     __syncwarp();
     if (lane == 0) {
@@ -305,7 +385,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       for (int b = 0; b < p.B; ++b) {
         s_prefix[b] = acc;
         const int first = p.window > 0 ? max(0, s_n[b] - p.window) : 0;
-        acc += n_splits(s_n[b] - first, p.chunk) * p.Hkv;
+        acc += (n_splits(s_n[b] - first, p.chunk) - 1) * p.Hkv;
       }
       s_prefix[p.B] = acc;
     }
@@ -314,8 +394,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  const int n_items = min(total_items, s_prefix[p.B]);
-  const int rows_pad = p.rows > 32 ? 64 : 32;
+  const int n_items = s_prefix[p.B] + p.B * p.Hkv;
 
   if (warp == 2) {
     // ------------------------------------------------------------ producer
@@ -323,29 +402,32 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       tma_prefetch_desc(&maps.k);
       tma_prefetch_desc(&maps.v);
       tma_prefetch_desc(&maps.q);
+      pdl_wait_primary();  // the prologue's Q, block keys and cleared counters
       const uint64_t pol = l2_policy_evict_first();
-      int stage = 0, qb = 0;
-      uint32_t kv_ph = 0, q_ph = 0;
+      Ring kv, q, itr;
       bool ok = true;
-      for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+      while (ok) {
+        const int w = atomicAdd(p.counters + p.B * p.Hkv, 1);
+        if (!(ok = mbar_wait(it_empty + 8 * itr.idx, itr.phase ^ 1u, p.status))) break;
+        s_item[itr.idx] = w < n_items ? w : -1;
+        mbar_arrive(it_full + 8 * itr.idx);
+        itr.next(kItemRing);
+        if (w >= n_items) break;
         const Item it = decode_item(w, s_prefix, s_n, p);
-        if (!(ok = mbar_wait(q_empty + 8 * qb, q_ph ^ 1u, p.status))) break;
-        mbar_arrive_expect_tx(q_full + 8 * qb, 2 * rows_pad * kRowBytes);
+        if (!(ok = mbar_wait(q_empty + 8 * q.idx, q.phase ^ 1u, p.status))) break;
+        mbar_arrive_expect_tx(q_full + 8 * q.idx, 2 * half);
         const int qrow = (it.b * p.Hq + it.g * p.G) * p.bs;
-        const uint32_t qdst = base + kOffQ + 2 * qb * kQBox;
-        tma_load_2d(qdst, &maps.q, q_full + 8 * qb, 0, qrow);
-        tma_load_2d(qdst + kQBox, &maps.q, q_full + 8 * qb, 64, qrow);
-        if (++qb == 2) {
-          qb = 0;
-          q_ph ^= 1u;
-        }
+        const uint32_t qdst = base + lay.off_q + 2 * q.idx * half;
+        tma_load_2d(qdst, &maps.q, q_full + 8 * q.idx, 0, qrow);
+        tma_load_2d(qdst + half, &maps.q, q_full + 8 * q.idx, 64, qrow);
+        q.next(2);
         const int rowbase = ((p.layer * p.B + it.b) * p.Hkv + it.g) * p.cap;
         const int brow = (it.b * p.Hkv + it.g) * p.bs;
         for (int t = 0; t < it.nt; ++t) {
-          if (!(ok = mbar_wait(kv_empty + 8 * stage, kv_ph ^ 1u, p.status))) break;
-          const uint32_t fb = kv_full + 8 * stage;
+          if (!(ok = mbar_wait(kv_empty + 8 * kv.idx, kv.phase ^ 1u, p.status))) break;
+          const uint32_t fb = kv_full + 8 * kv.idx;
           mbar_arrive_expect_tx(fb, kStageBytes);
-          const uint32_t dst = base + kOffKV + stage * kStageBytes;
+          const uint32_t dst = base + lay.off_kv + kv.idx * kStageBytes;
           if (t < it.ntiles) {
             const int y = rowbase + it.kstart + t * kTile;
             tma_load_2d_hint(dst, &maps.k, fb, 0, y, pol);
@@ -358,188 +440,222 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
             tma_load_2d(dst + 2 * kHalfTileBytes, &maps.vb, fb, 0, brow);
             tma_load_2d(dst + 3 * kHalfTileBytes, &maps.vb, fb, 64, brow);
           }
-          if (++stage == kStages) {
-            stage = 0;
-            kv_ph ^= 1u;
-          }
+          kv.next(S);
         }
       }
     }
   } else if (warp == 3) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------ S = Q K^T issuer
     if (lane == 0) {
-      int stage = 0, qb = 0, sb = 0, pb = 0;
-      uint32_t kv_ph = 0, q_ph = 0, s_ph = 0, p_ph = 0, o_ph = 0;
+      Ring kv, q, sr, itr;
       bool ok = true;
-      auto pv = [&](int st, bool first) -> bool {
-        if (!mbar_wait(p_full + 8 * pb, p_ph, p.status)) return false;
-        if (first && !mbar_wait(o_free, o_ph ^ 1u, p.status)) return false;
-        tc_fence_after_sync();
-        const uint32_t vbase = base + kOffKV + st * kStageBytes + 2 * kHalfTileBytes;
-        const uint64_t vdesc = umma_desc_mnmajor_sw128(vbase, kHalfTileBytes, 1024);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint64_t pdesc = umma_desc_kmajor_sw128(base + kOffP + (2 * pb + h) * kPHalf);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(tmem + 128, pdesc + 2 * kk, vdesc + 128 * kk, kIdescPV, (first && h == 0 && kk == 0) ? 0u : 1u);
-        }
-        umma_commit(kv_empty + 8 * st);
-        umma_commit(p_empty + 8 * pb);
-        if (++pb == 2) {
-          pb = 0;
-          p_ph ^= 1u;
-        }
-        if (first) o_ph ^= 1u;
-        return true;
-      };
-      for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+      while (ok) {
+        const int w = next_item(it_full, it_empty, s_item, itr, p.status, false);
+        if (w < 0) break;
         const Item it = decode_item(w, s_prefix, s_n, p);
-        if (!(ok = mbar_wait(q_full + 8 * qb, q_ph, p.status))) break;
-        tc_fence_after_sync();
-        const uint32_t qa = base + kOffQ + 2 * qb * kQBox;
-        int prev = -1;
+        if (!(ok = mbar_wait(q_full + 8 * q.idx, q.phase, p.status))) break;
+        const uint32_t qa = base + lay.off_q + 2 * q.idx * half;
         for (int t = 0; t < it.nt && ok; ++t) {
-          if (!(ok = mbar_wait(kv_full + 8 * stage, kv_ph, p.status))) break;
-          if (!(ok = mbar_wait(s_empty + 8 * sb, s_ph ^ 1u, p.status))) break;
+          if (!(ok = mbar_wait(kv_full + 8 * kv.idx, kv.phase, p.status))) break;
+          if (!(ok = mbar_wait(s_empty + 8 * sr.idx, sr.phase ^ 1u, p.status))) break;
           tc_fence_after_sync();
-          const uint32_t kb = base + kOffKV + stage * kStageBytes;
+          const uint32_t kb = base + lay.off_kv + kv.idx * kStageBytes;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t ad = umma_desc_kmajor_sw128(qa + (kk >> 2) * kQBox) + 2 * (kk & 3);
+            const uint64_t ad = umma_desc_kmajor_sw128(qa + (kk >> 2) * half) + 2 * (kk & 3);
             const uint64_t bd = umma_desc_kmajor_sw128(kb + (kk >> 2) * kHalfTileBytes) + 2 * (kk & 3);
-            umma_bf16(tmem + 64 * sb, ad, bd, kIdescQK, kk > 0 ? 1u : 0u);
+            umma_bf16(tmem + kColS + 64 * sr.idx, ad, bd, kIdescQK, kk > 0 ? 1u : 0u);
           }
-          umma_commit(s_full + 8 * sb);
-          if (++sb == 2) {
-            sb = 0;
-            s_ph ^= 1u;
-          }
-          if (prev >= 0) ok = pv(prev, t == 1);
-          prev = stage;
-          if (++stage == kStages) {
-            stage = 0;
-            kv_ph ^= 1u;
-          }
+          umma_commit(s_full + 8 * sr.idx);
+          sr.next(2);
+          kv.next(S);
         }
         if (!ok) break;
-        umma_commit(q_empty + 8 * qb);
-        if (++qb == 2) {
-          qb = 0;
-          q_ph ^= 1u;
-        }
-        ok = pv(prev, it.nt == 1);
+        umma_commit(q_empty + 8 * q.idx);
+        q.next(2);
       }
     }
-  } else {
-    // ------------------------------------------------ softmax + epilogue
+  } else if (warp == 6) {
+    // ------------------------------------------------ O += P V issuer
+    if (lane == 0) {
+      Ring kv, pr, orr, itr;
+      bool ok = true;
+      while (ok) {
+        const int w = next_item(it_full, it_empty, s_item, itr, p.status, false);
+        if (w < 0) break;
+        const Item it = decode_item(w, s_prefix, s_n, p);
+        const uint32_t od = tmem + col_o(orr.idx);
+        for (int t = 0; t < it.nt && ok; ++t) {
+          if (!(ok = mbar_wait(p_full + 8 * pr.idx, pr.phase, p.status))) break;
+          if (t == 0 && !(ok = mbar_wait(o_free + 8 * orr.idx, orr.phase ^ 1u, p.status))) break;
+          tc_fence_after_sync();
+          const uint32_t vbase = base + lay.off_kv + kv.idx * kStageBytes + 2 * kHalfTileBytes;
+          const uint64_t vdesc = umma_desc_mnmajor_sw128(vbase, kHalfTileBytes, 1024);
+          const uint32_t pa = tmem + kColP + 64 * pr.idx;
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              umma_bf16_ts(od, pa + 32 * h + 8 * kk, vdesc + 128 * kk, kIdescPV, (t == 0 && h == 0 && kk == 0) ? 0u : 1u);
+          umma_commit(kv_empty + 8 * kv.idx);
+          umma_commit(p_empty + 8 * pr.idx);
+          pr.next(2);
+          kv.next(S);
+        }
+        if (!ok) break;
+        umma_commit(o_full + 8 * orr.idx);
+        orr.next(2);
+      }
+    }
+  } else if (warp <= 1) {
+    // ------------------------------------------------ softmax (one thread per query row)
     const int row = 32 * warp + lane;
     const uint32_t tl = tmem + (static_cast<uint32_t>(32 * warp) << 16);
-    int sb = 0, pb = 0;
-    uint32_t s_ph = 0;
+    // A warp whose 32 rows are all padding keeps every wait and arrive (so
+    // the barrier phases stay in step) but does no math.
+    const bool act = 32 * warp < lay.rows_pad;
+    const float scale = p.scale_log2;
+    Ring sr, pr, mlr, itr;
+    int ob = 0;
     int pcnt[2] = {0, 0};
     bool ok = true;
-    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+    while (ok) {
+      const int w = next_item(it_full, it_empty, s_item, itr, p.status, true);
+      if (w < 0) break;
       const Item it = decode_item(w, s_prefix, s_n, p);
       float m_used = -INFINITY, l = 0.f;
       for (int t = 0; t < it.nt; ++t) {
-        if (!(ok = mbar_wait(s_full + 8 * sb, s_ph, p.status))) break;
+        if (!(ok = mbar_wait(s_full + 8 * sr.idx, sr.phase, p.status))) break;
         tc_fence_after_sync();
-        uint32_t sr[64];
-        tmem_ld_32cols(tl + 64 * sb, *reinterpret_cast<uint32_t(*)[32]>(sr));
-        tmem_ld_32cols(tl + 64 * sb + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
-        tmem_ld_wait();
+        uint32_t sv[64];
+        if (act) {
+          tmem_ld_32cols(tl + kColS + 64 * sr.idx, *reinterpret_cast<uint32_t(*)[32]>(sv));
+          tmem_ld_32cols(tl + kColS + 64 * sr.idx + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+          tmem_ld_wait();
+        }
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(s_empty + 8 * sb);
-        if (++sb == 2) {
-          sb = 0;
-          s_ph ^= 1u;
-        }
-        const int nvalid = t < it.ntiles ? min(kTile, it.kend - (it.kstart + t * kTile)) : p.bs;
-        float x[64];
-        float mt = -INFINITY;
+        if (lane == 0) mbar_arrive(s_empty + 8 * sr.idx);
+        sr.next(2);
+        uint32_t hv[32], lv[32];
+        if (act) {
+          float x[64];
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          x[i] = i < nvalid ? __uint_as_float(sr[i]) * p.scale_log2 : -INFINITY;
-          mt = fmaxf(mt, x[i]);
-        }
-        if (t == 0) {
-          m_used = mt;
-        } else {
-          const bool need = mt > m_used + kRescaleLog2;
-          if (__any_sync(0xffffffffu, need)) {
-            // O must be complete up to tile t-1 before it is rescaled
-            const int xb = pb ^ 1;
-            if (!(ok = mbar_wait(p_empty + 8 * xb, (pcnt[xb] - 1) & 1, p.status))) break;
-            tc_fence_after_sync();
-            const float f = need ? exp2f(m_used - mt) : 1.f;
-            if (need) {
-              l *= f;
-              m_used = mt;
-            }
+          for (int i = 0; i < 64; ++i) x[i] = __uint_as_float(sv[i]);
+          const int nvalid = t < it.ntiles ? min(kTile, it.kend - (it.kstart + t * kTile)) : p.bs;
+          if (nvalid < kTile) {
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              uint32_t r[32];
-              tmem_ld_32cols(tl + 128 + 32 * c, r);
-              tmem_ld_wait();
-#pragma unroll
-              for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * f);
-              tmem_st_32cols(tl + 128 + 32 * c, r);
-            }
-            tmem_st_wait();
-            tc_fence_before_sync();
+            for (int i = 0; i < 64; ++i)
+              if (i >= nvalid) x[i] = -INFINITY;
           }
-        }
-        const float mu = m_used == -INFINITY ? 0.f : m_used;
-        float ls = 0.f;
+          // tile max of the raw scores (scale > 0), tree-reduced
+          float mx[16];
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          x[i] = exp2f(x[i] - mu);
-          ls += x[i];
+          for (int i = 0; i < 16; ++i) mx[i] = fmaxf(fmaxf(x[4 * i], x[4 * i + 1]), fmaxf(x[4 * i + 2], x[4 * i + 3]));
+#pragma unroll
+          for (int w2 = 8; w2 >= 1; w2 >>= 1)
+#pragma unroll
+            for (int i = 0; i < w2; ++i) mx[i] = fmaxf(mx[i], mx[i + w2]);
+          const float mt = mx[0] * scale;
+          if (t == 0) {
+            m_used = mt;
+          } else {
+            const bool need = mt > m_used + kRescaleLog2;
+            if (__any_sync(0xffffffffu, need)) {
+              // O must hold every P V product up to tile t-1 before it is rescaled
+              const int xb = pr.idx ^ 1;
+              if (!(ok = mbar_wait(p_empty + 8 * xb, (pcnt[xb] - 1) & 1, p.status))) break;
+              tc_fence_after_sync();
+              const float f = need ? exp2f(m_used - mt) : 1.f;
+              if (need) {
+                l *= f;
+                m_used = mt;
+              }
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                uint32_t r[32];
+                tmem_ld_32cols(tl + col_o(ob) + 32 * c, r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * f);
+                tmem_st_32cols(tl + col_o(ob) + 32 * c, r);
+              }
+              tmem_st_wait();
+              tc_fence_before_sync();
+            }
+          }
+          const float nm = -(m_used == -INFINITY ? 0.f : m_used);
+          float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float a = exp2f(fmaf(x[2 * i], scale, nm));
+            const float b = exp2f(fmaf(x[2 * i + 1], scale, nm));
+            ls[i & 3] += a + b;
+            hv[i] = pack_bf16x2(a, b);
+            lv[i] = pack_bf16x2(a - bf16_lo(hv[i]), b - bf16_hi(hv[i]));
+          }
+          l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
         }
-        l += ls;
         // P[pb] is free once the P V product that last read it has completed
-        if (pcnt[pb] > 0 && !(ok = mbar_wait(p_empty + 8 * pb, (pcnt[pb] - 1) & 1, p.status))) break;
-        uint8_t* ph = gbase + kOffP + (2 * pb) * kPHalf + row * kRowBytes;
-        uint8_t* pl = ph + kPHalf;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint32_t hv[4], lv[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float a = x[8 * c + 2 * j], bb = x[8 * c + 2 * j + 1];
-            hv[j] = pack_bf16x2(a, bb);
-            lv[j] = pack_bf16x2(a - bf16_lo(hv[j]), bb - bf16_hi(hv[j]));
-          }
-          const int off = ((c ^ (row & 7)) << 4);
-          *reinterpret_cast<uint4*>(ph + off) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-          *reinterpret_cast<uint4*>(pl + off) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+        if (pcnt[pr.idx] > 0 && !(ok = mbar_wait(p_empty + 8 * pr.idx, (pcnt[pr.idx] - 1) & 1, p.status))) break;
+        tc_fence_after_sync();
+        if (act) {
+          tmem_st_32cols(tl + kColP + 64 * pr.idx, hv);
+          tmem_st_32cols(tl + kColP + 64 * pr.idx + 32, lv);
+          tmem_st_wait();
         }
-        fence_proxy_async_smem();
+        tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(p_full + 8 * pb);
-        ++pcnt[pb];
-        pb ^= 1;
+        if (lane == 0) mbar_arrive(p_full + 8 * pr.idx);
+        ++pcnt[pr.idx];
+        pr.next(2);
       }
       if (!ok) break;
-      // item end: the last P V product must have landed in O
-      const int xb = pb ^ 1;
-      if (!(ok = mbar_wait(p_empty + 8 * xb, (pcnt[xb] - 1) & 1, p.status))) break;
+      // hand (m, l) of this item to the epilogue warps
+      if (!(ok = mbar_wait(ml_empty + 8 * mlr.idx, mlr.phase ^ 1u, p.status))) break;
+      s_ml[mlr.idx * 64 + row] = make_float2(m_used, l);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ml_full + 8 * mlr.idx);
+      mlr.next(2);
+      ob ^= 1;
+    }
+  } else {
+    // ------------------------------------------------ epilogue (warps 4, 5)
+    const int row = 32 * (warp - 4) + lane;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(32 * (warp - 4)) << 16);
+    const bool act = 32 * (warp - 4) < lay.rows_pad;
+    Ring orr, mlr, itr;
+    bool ok = true;
+    while (ok) {
+      const int w = next_item(it_full, it_empty, s_item, itr, p.status, true);
+      if (w < 0) break;
+      const Item it = decode_item(w, s_prefix, s_n, p);
+      if (!(ok = mbar_wait(o_full + 8 * orr.idx, orr.phase, p.status))) break;
       tc_fence_after_sync();
       float o[HD];
+      if (act) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld_32cols(tl + 128 + 32 * c, r);
-        tmem_ld_wait();
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tmem_ld_32cols(tl + col_o(orr.idx) + 32 * c, r);
+          tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o[32 * c + i] = __uint_as_float(r[i]);
+          for (int i = 0; i < 32; ++i) o[32 * c + i] = __uint_as_float(r[i]);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < HD; ++i) o[i] = 0.f;
       }
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(o_free);
-      finish_item(it, p, row, o, m_used, l, s_flag);
+      if (lane == 0) mbar_arrive(o_free + 8 * orr.idx);
+      orr.next(2);
+      if (!(ok = mbar_wait(ml_full + 8 * mlr.idx, mlr.phase, p.status))) break;
+      const float2 ml = s_ml[mlr.idx * 64 + row];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ml_empty + 8 * mlr.idx);
+      mlr.next(2);
+      finish_item(it, p, row, o, ml.x, ml.y, s_flag, 2, 128);
     }
   }
   tc_fence_before_sync();
@@ -656,7 +772,7 @@ size_t attn_ws_bytes(int B, int bs, int Hq, int Hkv, int cap, int window, dflash
   if (dt == DFLASH_BF16)
     s += align256(static_cast<size_t>(B) * Hkv * max_splits * rows * HD * sizeof(float)) +
          align256(static_cast<size_t>(B) * Hkv * max_splits * rows * sizeof(float2)) +
-         align256(static_cast<size_t>(B) * Hkv * sizeof(int));
+         align256((static_cast<size_t>(B) * Hkv + 1) * sizeof(int));
   return s + 256;
 }
 
@@ -707,7 +823,7 @@ dflash_status launch_block_attn(int layer, int B, int bs, int Hq, const void* q,
   p.out = static_cast<__nv_bfloat16*>(out);
   p.opart = w.take<float>(static_cast<size_t>(B) * Hkv * p.max_splits * p.rows * HD);
   p.mlpart = w.take<float2>(static_cast<size_t>(B) * Hkv * p.max_splits * p.rows);
-  p.counters = w.take<int>(static_cast<size_t>(B) * Hkv);
+  p.counters = w.take<int>(static_cast<size_t>(B) * Hkv + 1);  // + the work-queue counter
   p.scale_log2 = 1.4426950408889634f * scale;
   p.status = dev.status;
 
@@ -723,10 +839,10 @@ dflash_status launch_block_attn(int layer, int B, int bs, int Hq, const void* q,
   attn_prologue_kernel<__nv_bfloat16><<<B * bs, 256, 0, st>>>(
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(kb),
       static_cast<const __nv_bfloat16*>(qg), static_cast<const __nv_bfloat16*>(kg), c.seq_len, B, bs, Hq, Hkv,
-      c.capacity, eps, inv, qh, kbh, p.counters, B * Hkv, dev.status);
+      c.capacity, eps, inv, qh, kbh, p.counters, B * Hkv + 1, dev.status);
 
-  const size_t smem = attn_main_smem(B);
-  if (smem > dev.max_smem_optin) return fail(DFLASH_ERR_UNSUPPORTED, "block_attn: shared memory");
+  const TcLayout lay = tc_layout(p.rows, B, static_cast<int>(dev.max_smem_optin));
+  if (lay.stages < 2) return fail(DFLASH_ERR_UNSUPPORTED, "block_attn: shared memory");
   static int configured_device = -1;
   if (configured_device != dev.device) {
     cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -735,8 +851,18 @@ dflash_status launch_block_attn(int layer, int B, int bs, int Hq, const void* q,
     configured_device = dev.device;
   }
   const long upper = static_cast<long>(B) * Hkv * p.max_splits;
-  const int grid = static_cast<int>(std::min<long>(upper, dev.num_sms));
-  attn_tc_kernel<<<grid, kTcThreads, smem, st>>>(maps, p, static_cast<int>(upper));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(std::min<long>(upper, dev.num_sms)));
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(lay.bytes);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t le = cudaLaunchKernelEx(&cfg, attn_tc_kernel, maps, p, lay);
+  if (le != cudaSuccess) return cuda_fail(le, "attn_tc_kernel launch");
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? DFLASH_OK : cuda_fail(e, "block attention launch");
 }
