@@ -11,7 +11,7 @@
 // Kernels:
 //   prologue -- per (sequence, block row): RMSNorm * gain and RoPE of every
 //               query head and block key, rounded to the storage dtype; also
-//               clears the split counters of the merge below.
+//               clears the work-queue counter of the main kernel.
 //   main     -- split-KV, memory-bound: a persistent grid walks work items
 //               (sequence, KV head, key split).  A producer warp streams 64-key
 //               K/V tiles of the cache (and, for the last split, the block's
@@ -56,7 +56,7 @@ struct AttnParams {
   float* opart;              // [B, Hkv, max_splits, rows, 128] normalised partial outputs
   float2* mlpart;            // [B, Hkv, max_splits, rows]      (max, sum) in log2 units
   float scale_log2;          // log2(e) / sqrt(128)
-  int* counters;             // [B, Hkv] finished splits (cleared by the prologue)
+  int* counters;             // [1] work-queue counter (cleared by the prologue)
   unsigned* status;
 };
 
@@ -146,9 +146,9 @@ struct Item {
 };
 
 // Work items in the order the queue hands them out: first every non-last
-// split (all `chunk` keys long), then the last split of every (b, g) (the
-// ragged remainder plus the block keys) -- largest first, so the dynamic queue
-// balances like longest-processing-time scheduling.
+// split, then the last split of every (b, g), which also carries the block
+// keys.  The splits of a sequence are near-equal, so the dynamic queue keeps
+// the tail short.
 __device__ __forceinline__ Item decode_item(int w, const int* s_full_prefix, const int* s_n, const AttnParams& p) {
   Item it;
   const int F = s_full_prefix[p.B];
@@ -176,8 +176,9 @@ __device__ __forceinline__ Item decode_item(int w, const int* s_full_prefix, con
   it.g = g;
   it.nsplit = n_splits(ncache, p.chunk);
   it.s = s < 0 ? it.nsplit - 1 : s;
-  it.kstart = first + it.s * p.chunk;
-  it.kend = first + min(ncache, (it.s + 1) * p.chunk);
+  // the sequence's cached keys are cut into nsplit near-equal ranges
+  it.kstart = first + static_cast<int>((static_cast<long>(it.s) * ncache) / it.nsplit);
+  it.kend = first + static_cast<int>((static_cast<long>(it.s + 1) * ncache) / it.nsplit);
   it.ntiles = it.kend > it.kstart ? (it.kend - it.kstart + kTile - 1) / kTile : 0;
   it.last = it.s == it.nsplit - 1;
   it.nt = it.ntiles + (it.last ? 1 : 0);
@@ -185,37 +186,39 @@ __device__ __forceinline__ Item decode_item(int w, const int* s_full_prefix, con
 }
 
 constexpr int kMaxStages = 6;
-constexpr int kTcThreads = 224;   // 7 warps, roles below
+constexpr int kTcThreads = 352;   // 11 warps, roles below
 constexpr int kRowBytes = 128;    // 64 bf16
 constexpr int kItemRing = 4;
-constexpr int kItemConsumers = 6; // QK issuer, PV issuer, 2 softmax warps, 2 epilogue warps
-constexpr int kNumBars = 2 * kMaxStages + 2 * 2 * 6 + 2 * kItemRing;
+constexpr int kNumBars = 2 * kMaxStages + 6 * 2 * 2 + 2 * kItemRing;
 constexpr int kTmemCols = 512;
-// tensor-memory columns: S[2] 64 each, O[2] 128 each, P[2] = {hi 32, lo 32}
-// (bf16 pairs packed per 32-bit column)
-constexpr uint32_t kColS = 0, kColO0 = 128, kColP = 256, kColO1 = 384;
+// tensor-memory columns: S[2] (fp32, 64 keys), P[2] (bf16 pairs: hi 32, lo 32),
+// O[2] (fp32, 128 dims)
+constexpr uint32_t kColS = 0, kColP = 128, kColO = 256;
 constexpr uint32_t kIdescQK = umma_idesc_bf16(128, 64, false);
 constexpr uint32_t kIdescPV = umma_idesc_bf16(128, 128, true);
 constexpr float kRescaleLog2 = 8.0f;
 
-__device__ __forceinline__ uint32_t col_o(int ob) { return ob ? kColO1 : kColO0; }
-
-// Shared-memory plan (byte offsets from the 1024-aligned base): Q double
-// buffer (the A operand of S = Q K^T; the M=128 MMA reads 128 rows, the rows
-// past rows_pad fall on the following buffers and only feed accumulator lanes
-// that are never read), then the K/V stage ring, barriers and small arrays.
+// The Q tile is copied to MMA rows 0.. and 64.. (rows_pad = 32 or 64 query
+// rows each), so every query row owns two tensor-memory lanes: copy 0 keeps
+// keys 0-31 of each 64-key tile, copy 1 keys 32-63.  Each copy runs its own
+// online softmax and accumulates its own partial O; the epilogue merges the
+// two (log-sum-exp).  The softmax work of a tile is thus spread over two
+// (rows_pad 32) or four (rows_pad 64) SM sub-partitions.
 struct TcLayout {
-  int rows_pad, half;   // half = rows_pad * 128 bytes: one 64-dim half of Q
-  int off_q, off_kv, stages, off_bar, off_misc, bytes;
+  int rows_pad;
+  int off_q, off_x, off_kv, stages, off_bar, off_misc, bytes;
 };
 
 __host__ __device__ inline TcLayout tc_layout(int rows, int B, int smem_limit) {
   TcLayout L;
   L.rows_pad = rows > 32 ? 64 : 32;
-  L.half = L.rows_pad * kRowBytes;
-  L.off_q = 0;                      // Q[buf][box] at (2*buf + box) * half
-  L.off_kv = 4 * L.half;            // stage s at off_kv + s * kStageBytes
-  const int misc = 64 + 2 * 64 * 8 + (2 * B + 1) * 4;  // tmem slot, flags, items, (m, l)[2][64], prefix, n
+  // Q: two 64-dim boxes of 128 MMA rows; buffer q sits rows_pad rows in, so for
+  // rows_pad = 32 both buffers fit in one 32 KB region, for 64 in two.
+  const int qbytes = L.rows_pad == 32 ? 32768 : 65536;
+  L.off_q = 0;
+  L.off_x = qbytes;                                   // O exchange of copy 1 -> copy 0
+  L.off_kv = L.off_x + L.rows_pad * 128 * 4;
+  const int misc = 64 + 2 * 2 * 64 * 8 + (2 * B + 1) * 4;
   const int fixed = 1024 + L.off_kv + 8 * kNumBars + misc;
   int st = (smem_limit - fixed) / kStageBytes;
   L.stages = st > kMaxStages ? kMaxStages : st;
@@ -225,82 +228,81 @@ __host__ __device__ inline TcLayout tc_layout(int rows, int B, int smem_limit) {
   return L;
 }
 
-// Thread `row` owns one query row: write its final output, or its normalised
-// partial and (m, l); the last CTA to finish a (b, g) merges the splits.
-// `bar_id` / `leader` name the named barrier and thread of the 64 epilogue threads.
+// Byte offset of Q buffer `qb` copy `c` box `h` (64-dim half) in the Q region.
+__device__ __forceinline__ uint32_t q_off(const TcLayout& L, int qb, int c, int h) {
+  if (L.rows_pad == 32) return static_cast<uint32_t>(h * 16384 + c * 8192 + qb * 4096);
+  return static_cast<uint32_t>(qb * 32768 + h * 16384 + c * 8192);
+}
+
+// Thread `row` owns one query row: write its final output (single split) or
+// its normalised partial output and (m, l) for the combine kernel.
 __device__ __forceinline__ void finish_item(const Item& it, const AttnParams& p, int row, const float (&o)[HD],
-                                            float m, float l, int* s_flag, int bar_id, int leader) {
-  const bool real = row < p.rows;
-  const size_t out_row0 = (static_cast<size_t>(it.b) * p.Hq + it.g * p.G) * p.bs;
+                                            float m, float l) {
+  if (row >= p.rows) return;
   const float inv = l > 0.f ? 1.f / l : 0.f;
   if (it.nsplit == 1) {
-    if (real) {
-      uint4* dst = reinterpret_cast<uint4*>(p.out + (out_row0 + row) * HD);
+    const size_t out_row0 = (static_cast<size_t>(it.b) * p.Hq + it.g * p.G) * p.bs;
+    uint4* dst = reinterpret_cast<uint4*>(p.out + (out_row0 + row) * HD);
 #pragma unroll
-      for (int i = 0; i < HD / 8; ++i)
-        dst[i] = make_uint4(pack_bf16x2(o[8 * i] * inv, o[8 * i + 1] * inv),
-                            pack_bf16x2(o[8 * i + 2] * inv, o[8 * i + 3] * inv),
-                            pack_bf16x2(o[8 * i + 4] * inv, o[8 * i + 5] * inv),
-                            pack_bf16x2(o[8 * i + 6] * inv, o[8 * i + 7] * inv));
-    }
+    for (int i = 0; i < HD / 8; ++i)
+      dst[i] = make_uint4(pack_bf16x2(o[8 * i] * inv, o[8 * i + 1] * inv),
+                          pack_bf16x2(o[8 * i + 2] * inv, o[8 * i + 3] * inv),
+                          pack_bf16x2(o[8 * i + 4] * inv, o[8 * i + 5] * inv),
+                          pack_bf16x2(o[8 * i + 6] * inv, o[8 * i + 7] * inv));
     return;
   }
-  const size_t bg = static_cast<size_t>(it.b) * p.Hkv + it.g;
-  const size_t part0 = bg * p.max_splits * p.rows;
-  if (real) {
-    float4* dst = reinterpret_cast<float4*>(p.opart + (part0 + static_cast<size_t>(it.s) * p.rows + row) * HD);
+  const size_t r = ((static_cast<size_t>(it.b) * p.Hkv + it.g) * p.max_splits + it.s) * p.rows + row;
+  float4* dst = reinterpret_cast<float4*>(p.opart + r * HD);
 #pragma unroll
-    for (int i = 0; i < HD / 4; ++i)
-      dst[i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv, o[4 * i + 3] * inv);
-    p.mlpart[part0 + static_cast<size_t>(it.s) * p.rows + row] = make_float2(m, l);
-  }
-  __threadfence();
-  named_barrier_sync(bar_id, 64);
-  if (threadIdx.x == leader) *s_flag = (atomicAdd(p.counters + bg, 1) == it.nsplit - 1);
-  named_barrier_sync(bar_id, 64);
-  const int last = *s_flag;
-  named_barrier_sync(bar_id, 64);  // s_flag is reused by the next item
-  if (!last) return;
-  __threadfence();
-  if (!real) return;
-  // this CTA finished (b, g) last: log-sum-exp merge of all its splits
-  const float2* ml = p.mlpart + part0 + row;
+  for (int i = 0; i < HD / 4; ++i)
+    dst[i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv, o[4 * i + 3] * inv);
+  p.mlpart[r] = make_float2(m, l);
+}
+
+// Log-sum-exp merge of the split partials of every (sequence, KV head) that
+// has more than one split: one warp per output row, 4 dims per lane.
+__global__ void __launch_bounds__(256) attn_combine_kernel(const AttnParams p) {
+  pdl_wait_primary();
+  const int gw = blockIdx.x * 8 + threadIdx.x / 32;   // global warp = (b, g, row)
+  const int lane = threadIdx.x % 32;
+  const int row = gw % p.rows;
+  const int bg = gw / p.rows;
+  if (bg >= p.B * p.Hkv) return;
+  const int b = bg / p.Hkv, g = bg % p.Hkv;
+  const int n = min(max(p.seq_len[b], 0), p.cap);
+  const int first = p.window > 0 ? max(0, n - p.window) : 0;
+  const int ns = n_splits(n - first, p.chunk);
+  if (ns <= 1) return;
+  const size_t r0 = static_cast<size_t>(bg) * p.max_splits * p.rows + row;
   float M = -INFINITY;
-  for (int s = 0; s < it.nsplit; ++s) M = fmaxf(M, __ldcg(ml + static_cast<size_t>(s) * p.rows).x);
+  for (int s = lane; s < ns; s += 32) M = fmaxf(M, p.mlpart[r0 + static_cast<size_t>(s) * p.rows].x);
+  M = warp_max(M);
   const float Mu = M == -INFINITY ? 0.f : M;
-  float acc[HD];
-#pragma unroll
-  for (int i = 0; i < HD; ++i) acc[i] = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float den = 0.f;
-  for (int s = 0; s < it.nsplit; ++s) {
-    const float2 v = __ldcg(ml + static_cast<size_t>(s) * p.rows);
-    const float f = v.y * exp2f(v.x - Mu);
+#pragma unroll 8
+  for (int s = 0; s < ns; ++s) {
+    const size_t r = r0 + static_cast<size_t>(s) * p.rows;
+    const float2 ml = p.mlpart[r];
+    const float4 o = reinterpret_cast<const float4*>(p.opart + r * HD)[lane];
+    const float f = ml.y * exp2f(ml.x - Mu);
     den += f;
-    const float4* src = reinterpret_cast<const float4*>(p.opart + (part0 + static_cast<size_t>(s) * p.rows + row) * HD);
-#pragma unroll
-    for (int i = 0; i < HD / 4; ++i) {
-      const float4 x = __ldcg(src + i);
-      acc[4 * i] += f * x.x;
-      acc[4 * i + 1] += f * x.y;
-      acc[4 * i + 2] += f * x.z;
-      acc[4 * i + 3] += f * x.w;
-    }
+    acc.x += f * o.x;
+    acc.y += f * o.y;
+    acc.z += f * o.z;
+    acc.w += f * o.w;
   }
-  const float dinv = den > 0.f ? 1.f / den : 0.f;
-  uint4* dst = reinterpret_cast<uint4*>(p.out + (out_row0 + row) * HD);
-#pragma unroll
-  for (int i = 0; i < HD / 8; ++i)
-    dst[i] = make_uint4(pack_bf16x2(acc[8 * i] * dinv, acc[8 * i + 1] * dinv),
-                        pack_bf16x2(acc[8 * i + 2] * dinv, acc[8 * i + 3] * dinv),
-                        pack_bf16x2(acc[8 * i + 4] * dinv, acc[8 * i + 5] * dinv),
-                        pack_bf16x2(acc[8 * i + 6] * dinv, acc[8 * i + 7] * dinv));
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  const size_t out_row = (static_cast<size_t>(b) * p.Hq + g * p.G) * p.bs + row;
+  reinterpret_cast<uint2*>(p.out + out_row * HD)[lane] =
+      make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
 }
 
 struct AttnMaps {
   CUtensorMap k, v, q, kb, vb;
 };
 
-// Ring of two-phase mbarriers shared by one producer role and one consumer role.
+// Index and phase of a ring of two-phase mbarriers.
 struct Ring {
   int idx = 0;
   uint32_t phase = 0;
@@ -314,18 +316,19 @@ struct Ring {
 
 // Reads the next work item from the shared item ring (-1 = no more work).
 __device__ __forceinline__ int next_item(uint32_t it_full, uint32_t it_empty, const int* s_item, Ring& r,
-                                         unsigned* status, bool warp_wide) {
+                                         unsigned* status) {
   if (!mbar_wait(it_full + 8 * r.idx, r.phase, status)) return -1;
   const int w = s_item[r.idx];
-  if (warp_wide) __syncwarp();
-  if (!warp_wide || (threadIdx.x & 31) == 0) mbar_arrive(it_empty + 8 * r.idx);
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(it_empty + 8 * r.idx);
   r.next(kItemRing);
   return w;
 }
 
-// Roles: warp 0/1 softmax of query rows 0-31 / 32-63 (tensor-memory lane
-// quarters 0/1), warp 2 TMA producer, warp 3 S = Q K^T issuer, warp 4/5
-// epilogue of rows 0-31 / 32-63, warp 6 O += P V issuer.
+// Roles: warps 0-3 softmax of tensor-memory lane quarter = warp, warps 4-7
+// epilogue of lane quarter = warp - 4 (only the quarters holding query rows
+// are active), warp 8 TMA producer, warp 9 S = Q K^T issuer, warp 10
+// O += P V issuer.
 __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_constant__ AttnMaps maps,
                                                                 const AttnParams p, const TcLayout lay) {
   extern __shared__ uint8_t smem_raw[];
@@ -333,7 +336,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
   const int S = lay.stages;
-  const int half = lay.half;
   const uint32_t bar0 = base + lay.off_bar;
   const uint32_t kv_full = bar0, kv_empty = bar0 + 8 * kMaxStages;
   const uint32_t q_full = bar0 + 16 * kMaxStages, q_empty = q_full + 16;
@@ -343,13 +345,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   const uint32_t ml_full = o_free + 16, ml_empty = ml_full + 16;
   const uint32_t it_full = ml_empty + 16, it_empty = it_full + 8 * kItemRing;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + lay.off_misc);
-  int* s_flag = reinterpret_cast<int*>(tmem_slot + 1);
-  int* s_item = reinterpret_cast<int*>(tmem_slot + 8);            // kItemRing entries
-  float2* s_ml = reinterpret_cast<float2*>(gbase + lay.off_misc + 64);  // [2][64] (m, l) per row
-  int* s_prefix = reinterpret_cast<int*>(gbase + lay.off_misc + 64 + 2 * 64 * 8);
+  int* s_item = reinterpret_cast<int*>(tmem_slot + 8);                    // kItemRing entries
+  float2* s_ml = reinterpret_cast<float2*>(gbase + lay.off_misc + 64);    // [2 buf][2 copy][64 row]
+  int* s_prefix = reinterpret_cast<int*>(gbase + lay.off_misc + 64 + 2 * 2 * 64 * 8);
   int* s_n = s_prefix + (p.B + 1);
+  float* s_x = reinterpret_cast<float*>(gbase + lay.off_x);             // [rows_pad][128]
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int nq = lay.rows_pad / 32;   // lane quarters per copy: 1 or 2
+  const int n_sm = 2 * nq;            // active softmax warps (and epilogue warps)
+  // quarter q is active when its lanes hold a query row: q % 2 < nq
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(kv_full + 8 * s, 1);
@@ -359,25 +364,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       mbar_init(q_full + 8 * i, 1);
       mbar_init(q_empty + 8 * i, 1);
       mbar_init(s_full + 8 * i, 1);
-      mbar_init(s_empty + 8 * i, 2);
-      mbar_init(p_full + 8 * i, 2);
+      mbar_init(s_empty + 8 * i, n_sm);
+      mbar_init(p_full + 8 * i, n_sm);
       mbar_init(p_empty + 8 * i, 1);
       mbar_init(o_full + 8 * i, 1);
-      mbar_init(o_free + 8 * i, 2);
-      mbar_init(ml_full + 8 * i, 2);
-      mbar_init(ml_empty + 8 * i, 2);
+      mbar_init(o_free + 8 * i, n_sm);
+      mbar_init(ml_full + 8 * i, n_sm);
+      mbar_init(ml_empty + 8 * i, n_sm);
     }
     for (int i = 0; i < kItemRing; ++i) {
       mbar_init(it_full + 8 * i, 1);
-      mbar_init(it_empty + 8 * i, kItemConsumers);
+      mbar_init(it_empty + 8 * i, 2 + 2 * n_sm);
     }
     mbar_fence_init();
   }
-  if (warp == 3) {
+  if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 0) {  // per-sequence lengths and the prefix of full (non-last) splits
+  if (warp == 8) {  // per-sequence lengths and the prefix of full (non-last) splits
     for (int b = lane; b < p.B; b += 32) s_n[b] = clamp_seq(p.seq_len[b], p.cap, p.status);
     __syncwarp();
     if (lane == 0) {
@@ -393,10 +398,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
+  pdl_launch_dependents();  // the combine kernel may launch; it waits for this grid
   const uint32_t tmem = *tmem_slot;
   const int n_items = s_prefix[p.B] + p.B * p.Hkv;
 
-  if (warp == 2) {
+  if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&maps.k);
@@ -407,7 +413,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       Ring kv, q, itr;
       bool ok = true;
       while (ok) {
-        const int w = atomicAdd(p.counters + p.B * p.Hkv, 1);
+        const int w = atomicAdd(p.counters, 1);
         if (!(ok = mbar_wait(it_empty + 8 * itr.idx, itr.phase ^ 1u, p.status))) break;
         s_item[itr.idx] = w < n_items ? w : -1;
         mbar_arrive(it_full + 8 * itr.idx);
@@ -415,11 +421,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         if (w >= n_items) break;
         const Item it = decode_item(w, s_prefix, s_n, p);
         if (!(ok = mbar_wait(q_empty + 8 * q.idx, q.phase ^ 1u, p.status))) break;
-        mbar_arrive_expect_tx(q_full + 8 * q.idx, 2 * half);
+        mbar_arrive_expect_tx(q_full + 8 * q.idx, 4 * lay.rows_pad * kRowBytes);
         const int qrow = (it.b * p.Hq + it.g * p.G) * p.bs;
-        const uint32_t qdst = base + lay.off_q + 2 * q.idx * half;
-        tma_load_2d(qdst, &maps.q, q_full + 8 * q.idx, 0, qrow);
-        tma_load_2d(qdst + half, &maps.q, q_full + 8 * q.idx, 64, qrow);
+        for (int c = 0; c < 2; ++c)
+          for (int h = 0; h < 2; ++h)
+            tma_load_2d(base + lay.off_q + q_off(lay, q.idx, c, h), &maps.q, q_full + 8 * q.idx, 64 * h, qrow);
         q.next(2);
         const int rowbase = ((p.layer * p.B + it.b) * p.Hkv + it.g) * p.cap;
         const int brow = (it.b * p.Hkv + it.g) * p.bs;
@@ -444,30 +450,32 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         }
       }
     }
-  } else if (warp == 3) {
+  } else if (warp == 9) {
     // ------------------------------------------------ S = Q K^T issuer
     if (lane == 0) {
-      Ring kv, q, sr, itr;
+      Ring kv, q, sq, itr;
       bool ok = true;
       while (ok) {
-        const int w = next_item(it_full, it_empty, s_item, itr, p.status, false);
+        if (!(ok = mbar_wait(it_full + 8 * itr.idx, itr.phase, p.status))) break;
+        const int w = s_item[itr.idx];
+        mbar_arrive(it_empty + 8 * itr.idx);
+        itr.next(kItemRing);
         if (w < 0) break;
         const Item it = decode_item(w, s_prefix, s_n, p);
         if (!(ok = mbar_wait(q_full + 8 * q.idx, q.phase, p.status))) break;
-        const uint32_t qa = base + lay.off_q + 2 * q.idx * half;
         for (int t = 0; t < it.nt && ok; ++t) {
           if (!(ok = mbar_wait(kv_full + 8 * kv.idx, kv.phase, p.status))) break;
-          if (!(ok = mbar_wait(s_empty + 8 * sr.idx, sr.phase ^ 1u, p.status))) break;
+          if (!(ok = mbar_wait(s_empty + 8 * sq.idx, sq.phase ^ 1u, p.status))) break;
           tc_fence_after_sync();
           const uint32_t kb = base + lay.off_kv + kv.idx * kStageBytes;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t ad = umma_desc_kmajor_sw128(qa + (kk >> 2) * half) + 2 * (kk & 3);
+            const uint64_t ad = umma_desc_kmajor_sw128(base + lay.off_q + q_off(lay, q.idx, 0, kk >> 2)) + 2 * (kk & 3);
             const uint64_t bd = umma_desc_kmajor_sw128(kb + (kk >> 2) * kHalfTileBytes) + 2 * (kk & 3);
-            umma_bf16(tmem + kColS + 64 * sr.idx, ad, bd, kIdescQK, kk > 0 ? 1u : 0u);
+            umma_bf16(tmem + kColS + 64 * sq.idx, ad, bd, kIdescQK, kk > 0 ? 1u : 0u);
           }
-          umma_commit(s_full + 8 * sr.idx);
-          sr.next(2);
+          umma_commit(s_full + 8 * sq.idx);
+          sq.next(2);
           kv.next(S);
         }
         if (!ok) break;
@@ -475,19 +483,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         q.next(2);
       }
     }
-  } else if (warp == 6) {
+  } else if (warp == 10) {
     // ------------------------------------------------ O += P V issuer
     if (lane == 0) {
-      Ring kv, pr, orr, itr;
+      Ring kv, pr, o, itr;
       bool ok = true;
       while (ok) {
-        const int w = next_item(it_full, it_empty, s_item, itr, p.status, false);
+        if (!(ok = mbar_wait(it_full + 8 * itr.idx, itr.phase, p.status))) break;
+        const int w = s_item[itr.idx];
+        mbar_arrive(it_empty + 8 * itr.idx);
+        itr.next(kItemRing);
         if (w < 0) break;
         const Item it = decode_item(w, s_prefix, s_n, p);
-        const uint32_t od = tmem + col_o(orr.idx);
+        const uint32_t od = tmem + kColO + 128 * o.idx;
         for (int t = 0; t < it.nt && ok; ++t) {
           if (!(ok = mbar_wait(p_full + 8 * pr.idx, pr.phase, p.status))) break;
-          if (t == 0 && !(ok = mbar_wait(o_free + 8 * orr.idx, orr.phase ^ 1u, p.status))) break;
+          if (t == 0 && !(ok = mbar_wait(o_free + 8 * o.idx, o.phase ^ 1u, p.status))) break;
           tc_fence_after_sync();
           const uint32_t vbase = base + lay.off_kv + kv.idx * kStageBytes + 2 * kHalfTileBytes;
           const uint64_t vdesc = umma_desc_mnmajor_sw128(vbase, kHalfTileBytes, 1024);
@@ -497,170 +508,198 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               umma_bf16_ts(od, pa + 32 * h + 8 * kk, vdesc + 128 * kk, kIdescPV, (t == 0 && h == 0 && kk == 0) ? 0u : 1u);
-          umma_commit(kv_empty + 8 * kv.idx);
           umma_commit(p_empty + 8 * pr.idx);
+          umma_commit(kv_empty + 8 * kv.idx);
           pr.next(2);
           kv.next(S);
         }
         if (!ok) break;
-        umma_commit(o_full + 8 * orr.idx);
-        orr.next(2);
+        umma_commit(o_full + 8 * o.idx);
+        o.next(2);
       }
     }
-  } else if (warp <= 1) {
-    // ------------------------------------------------ softmax (one thread per query row)
-    const int row = 32 * warp + lane;
-    const uint32_t tl = tmem + (static_cast<uint32_t>(32 * warp) << 16);
-    // A warp whose 32 rows are all padding keeps every wait and arrive (so
-    // the barrier phases stay in step) but does no math.
-    const bool act = 32 * warp < lay.rows_pad;
-    const float scale = p.scale_log2;
-    Ring sr, pr, mlr, itr;
-    int ob = 0;
-    int pcnt[2] = {0, 0};
-    bool ok = true;
-    while (ok) {
-      const int w = next_item(it_full, it_empty, s_item, itr, p.status, true);
-      if (w < 0) break;
-      const Item it = decode_item(w, s_prefix, s_n, p);
-      float m_used = -INFINITY, l = 0.f;
-      for (int t = 0; t < it.nt; ++t) {
-        if (!(ok = mbar_wait(s_full + 8 * sr.idx, sr.phase, p.status))) break;
-        tc_fence_after_sync();
-        uint32_t sv[64];
-        if (act) {
-          tmem_ld_32cols(tl + kColS + 64 * sr.idx, *reinterpret_cast<uint32_t(*)[32]>(sv));
-          tmem_ld_32cols(tl + kColS + 64 * sr.idx + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
-          tmem_ld_wait();
+  } else if (warp <= 3) {
+    // ------------------------------------------------ softmax
+    if ((warp & 1) < nq) {
+      const int lg = 32 * warp + lane;         // tensor-memory lane
+      const int row = lg % 64;                 // query row (rows_pad = 32: quarters 0, 2)
+      const int copy = lg / 64;                // copy 0: keys 0-31, copy 1: keys 32-63
+      const int key0 = 32 * copy;
+      const uint32_t tl = tmem + (static_cast<uint32_t>(32 * warp) << 16);
+      const float scale = p.scale_log2;
+      {  // the other copy's key columns of both P buffers stay zero for the whole kernel
+        uint32_t z[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) z[i] = 0u;
+#pragma unroll
+        for (int pb = 0; pb < 2; ++pb) {
+          tmem_st_32cols(tl + kColP + 64 * pb, z);
+          tmem_st_32cols(tl + kColP + 64 * pb + 32, z);
         }
+        tmem_st_wait();
         tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(s_empty + 8 * sr.idx);
-        sr.next(2);
-        uint32_t hv[32], lv[32];
-        if (act) {
-          float x[64];
+      }
+      Ring sr, mlr, itr;
+      int ob = 0, pb = 0;
+      int pcnt[2] = {0, 0};
+      bool ok = true;
+      while (ok) {
+        const int w = next_item(it_full, it_empty, s_item, itr, p.status);
+        if (w < 0) break;
+        const Item it = decode_item(w, s_prefix, s_n, p);
+        float m_used = -INFINITY, l = 0.f;
+        for (int t = 0; t < it.nt; ++t) {
+          if (!(ok = mbar_wait(s_full + 8 * sr.idx, sr.phase, p.status))) break;
+          tc_fence_after_sync();
+          float x[32];
+          {
+            uint32_t r[32];
+            tmem_ld_32cols(tl + kColS + 64 * sr.idx + key0, r);
+            tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 64; ++i) x[i] = __uint_as_float(sv[i]);
-          const int nvalid = t < it.ntiles ? min(kTile, it.kend - (it.kstart + t * kTile)) : p.bs;
-          if (nvalid < kTile) {
+            for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(r[i]);
+          }
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(s_empty + 8 * sr.idx);
+          sr.next(2);
+          const int nvalid = (t < it.ntiles ? min(kTile, it.kend - (it.kstart + t * kTile)) : p.bs) - key0;
+          if (nvalid < 32) {
 #pragma unroll
-            for (int i = 0; i < 64; ++i)
+            for (int i = 0; i < 32; ++i)
               if (i >= nvalid) x[i] = -INFINITY;
           }
-          // tile max of the raw scores (scale > 0), tree-reduced
-          float mx[16];
+          float mx[8];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) mx[i] = fmaxf(fmaxf(x[4 * i], x[4 * i + 1]), fmaxf(x[4 * i + 2], x[4 * i + 3]));
+          for (int i = 0; i < 8; ++i) mx[i] = fmaxf(fmaxf(x[4 * i], x[4 * i + 1]), fmaxf(x[4 * i + 2], x[4 * i + 3]));
 #pragma unroll
-          for (int w2 = 8; w2 >= 1; w2 >>= 1)
+          for (int w2 = 4; w2 >= 1; w2 >>= 1)
 #pragma unroll
             for (int i = 0; i < w2; ++i) mx[i] = fmaxf(mx[i], mx[i + w2]);
           const float mt = mx[0] * scale;
-          if (t == 0) {
-            m_used = mt;
-          } else {
-            const bool need = mt > m_used + kRescaleLog2;
-            if (__any_sync(0xffffffffu, need)) {
-              // O must hold every P V product up to tile t-1 before it is rescaled
-              const int xb = pr.idx ^ 1;
-              if (!(ok = mbar_wait(p_empty + 8 * xb, (pcnt[xb] - 1) & 1, p.status))) break;
-              tc_fence_after_sync();
-              const float f = need ? exp2f(m_used - mt) : 1.f;
-              if (need) {
-                l *= f;
-                m_used = mt;
-              }
+          const bool need = m_used == -INFINITY ? (mt != -INFINITY) : (mt > m_used + kRescaleLog2);
+          if (__any_sync(0xffffffffu, need) && t > 0) {
+            // this copy's O must hold every P V product up to tile t-1 before it is rescaled
+            const int xb = pb ^ 1;
+            if (!(ok = mbar_wait(p_empty + 8 * xb, (pcnt[xb] - 1) & 1, p.status))) break;
+            tc_fence_after_sync();
+            const float f = need ? (m_used == -INFINITY ? 0.f : exp2f(m_used - mt)) : 1.f;
 #pragma unroll
-              for (int c = 0; c < 4; ++c) {
-                uint32_t r[32];
-                tmem_ld_32cols(tl + col_o(ob) + 32 * c, r);
-                tmem_ld_wait();
+            for (int c = 0; c < 4; ++c) {
+              uint32_t r[32];
+              tmem_ld_32cols(tl + kColO + 128 * ob + 32 * c, r);
+              tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * f);
-                tmem_st_32cols(tl + col_o(ob) + 32 * c, r);
-              }
-              tmem_st_wait();
-              tc_fence_before_sync();
+              for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * f);
+              tmem_st_32cols(tl + kColO + 128 * ob + 32 * c, r);
             }
+            tmem_st_wait();
+          }
+          if (need) {
+            l = (m_used == -INFINITY) ? 0.f : l * exp2f(m_used - mt);
+            m_used = mt;
           }
           const float nm = -(m_used == -INFINITY ? 0.f : m_used);
+          // P over this copy's 32 keys as bf16 hi + lo pairs
+          uint32_t hv[16], lv[16];
           float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
+          for (int i = 0; i < 16; ++i) {
             const float a = exp2f(fmaf(x[2 * i], scale, nm));
-            const float b = exp2f(fmaf(x[2 * i + 1], scale, nm));
-            ls[i & 3] += a + b;
-            hv[i] = pack_bf16x2(a, b);
-            lv[i] = pack_bf16x2(a - bf16_lo(hv[i]), b - bf16_hi(hv[i]));
+            const float c2 = exp2f(fmaf(x[2 * i + 1], scale, nm));
+            ls[i & 3] += a + c2;
+            hv[i] = pack_bf16x2(a, c2);
+            lv[i] = pack_bf16x2(a - bf16_lo(hv[i]), c2 - bf16_hi(hv[i]));
           }
           l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-        }
-        // P[pb] is free once the P V product that last read it has completed
-        if (pcnt[pr.idx] > 0 && !(ok = mbar_wait(p_empty + 8 * pr.idx, (pcnt[pr.idx] - 1) & 1, p.status))) break;
-        tc_fence_after_sync();
-        if (act) {
-          tmem_st_32cols(tl + kColP + 64 * pr.idx, hv);
-          tmem_st_32cols(tl + kColP + 64 * pr.idx + 32, lv);
+          // P[pb] is free once the P V product that last read it has completed
+          if (pcnt[pb] > 0 && !(ok = mbar_wait(p_empty + 8 * pb, (pcnt[pb] - 1) & 1, p.status))) break;
+          tc_fence_after_sync();
+          tmem_st_16cols(tl + kColP + 64 * pb + 16 * copy, hv);
+          tmem_st_16cols(tl + kColP + 64 * pb + 32 + 16 * copy, lv);
           tmem_st_wait();
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(p_full + 8 * pb);
+          ++pcnt[pb];
+          pb ^= 1;
         }
-        tc_fence_before_sync();
+        if (!ok) break;
+        // hand (m, l) of this copy to the epilogue warps
+        if (!(ok = mbar_wait(ml_empty + 8 * mlr.idx, mlr.phase ^ 1u, p.status))) break;
+        s_ml[(mlr.idx * 2 + copy) * 64 + row] = make_float2(m_used, l);
         __syncwarp();
-        if (lane == 0) mbar_arrive(p_full + 8 * pr.idx);
-        ++pcnt[pr.idx];
-        pr.next(2);
+        if (lane == 0) mbar_arrive(ml_full + 8 * mlr.idx);
+        mlr.next(2);
+        ob ^= 1;
       }
-      if (!ok) break;
-      // hand (m, l) of this item to the epilogue warps
-      if (!(ok = mbar_wait(ml_empty + 8 * mlr.idx, mlr.phase ^ 1u, p.status))) break;
-      s_ml[mlr.idx * 64 + row] = make_float2(m_used, l);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(ml_full + 8 * mlr.idx);
-      mlr.next(2);
-      ob ^= 1;
     }
   } else {
-    // ------------------------------------------------ epilogue (warps 4, 5)
-    const int row = 32 * (warp - 4) + lane;
-    const uint32_t tl = tmem + (static_cast<uint32_t>(32 * (warp - 4)) << 16);
-    const bool act = 32 * (warp - 4) < lay.rows_pad;
-    Ring orr, mlr, itr;
-    bool ok = true;
-    while (ok) {
-      const int w = next_item(it_full, it_empty, s_item, itr, p.status, true);
-      if (w < 0) break;
-      const Item it = decode_item(w, s_prefix, s_n, p);
-      if (!(ok = mbar_wait(o_full + 8 * orr.idx, orr.phase, p.status))) break;
-      tc_fence_after_sync();
-      float o[HD];
-      if (act) {
+    // ------------------------------------------------ epilogue (warps 4-7)
+    const int e = warp - 4;
+    if ((e & 1) < nq) {
+      const int lg = 32 * e + lane;
+      const int row = lg % 64;
+      const int copy = lg / 64;
+      const uint32_t tl = tmem + (static_cast<uint32_t>(32 * e) << 16);
+      Ring orr, mlr, itr;
+      bool ok = true;
+      while (ok) {
+        const int w = next_item(it_full, it_empty, s_item, itr, p.status);
+        if (w < 0) break;
+        const Item it = decode_item(w, s_prefix, s_n, p);
+        if (!(ok = mbar_wait(o_full + 8 * orr.idx, orr.phase, p.status))) break;
+        tc_fence_after_sync();
+        float o[HD];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t r[32];
-          tmem_ld_32cols(tl + col_o(orr.idx) + 32 * c, r);
+          tmem_ld_32cols(tl + kColO + 128 * orr.idx + 32 * c, r);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[32 * c + i] = __uint_as_float(r[i]);
         }
-      } else {
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(o_free + 8 * orr.idx);
+        orr.next(2);
+        if (!(ok = mbar_wait(ml_full + 8 * mlr.idx, mlr.phase, p.status))) break;
+        const float2 mine = s_ml[(mlr.idx * 2 + copy) * 64 + row];
+        const float2 other = s_ml[(mlr.idx * 2 + (copy ^ 1)) * 64 + row];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ml_empty + 8 * mlr.idx);
+        mlr.next(2);
+        // merge the two copies' partial softmax states (log-sum-exp)
+        const float M = fmaxf(mine.x, other.x);
+        const float Mu = M == -INFINITY ? 0.f : M;
+        const float fm = mine.x == -INFINITY ? 0.f : exp2f(mine.x - Mu);
+        const float fo = other.x == -INFINITY ? 0.f : exp2f(other.x - Mu);
+        if (copy == 1) {
+          float4* xr = reinterpret_cast<float4*>(s_x + row * HD);
 #pragma unroll
-        for (int i = 0; i < HD; ++i) o[i] = 0.f;
+          for (int i = 0; i < HD / 4; ++i)
+            xr[i] = make_float4(o[4 * i] * fm, o[4 * i + 1] * fm, o[4 * i + 2] * fm, o[4 * i + 3] * fm);
+        }
+        named_barrier_sync(1, 32 * n_sm);
+        if (copy == 0) {
+          const float4* xr = reinterpret_cast<const float4*>(s_x + row * HD);
+#pragma unroll
+          for (int i = 0; i < HD / 4; ++i) {
+            const float4 v = xr[i];
+            o[4 * i] = o[4 * i] * fm + v.x;
+            o[4 * i + 1] = o[4 * i + 1] * fm + v.y;
+            o[4 * i + 2] = o[4 * i + 2] * fm + v.z;
+            o[4 * i + 3] = o[4 * i + 3] * fm + v.w;
+          }
+        }
+        named_barrier_sync(1, 32 * n_sm);  // s_x is free for the next item
+        if (copy == 0) finish_item(it, p, row, o, M, mine.y * fm + other.y * fo);
       }
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(o_free + 8 * orr.idx);
-      orr.next(2);
-      if (!(ok = mbar_wait(ml_full + 8 * mlr.idx, mlr.phase, p.status))) break;
-      const float2 ml = s_ml[mlr.idx * 64 + row];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(ml_empty + 8 * mlr.idx);
-      mlr.next(2);
-      finish_item(it, p, row, o, ml.x, ml.y, s_flag, 2, 128);
     }
   }
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 3) {
+  if (warp == 9) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -754,7 +793,7 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const float* __restrict__
 
 int pick_chunk(int B, int Hkv, int cap, int window) {
   const long keys = window > 0 ? std::min(window, cap) : cap;
-  long c = (static_cast<long>(B) * Hkv * keys) / 2400;
+  long c = (static_cast<long>(B) * Hkv * keys) / 3600;
   c = (c + 63) / 64 * 64;
   return static_cast<int>(std::min<long>(4096, std::max<long>(256, c)));
 }
@@ -772,7 +811,7 @@ size_t attn_ws_bytes(int B, int bs, int Hq, int Hkv, int cap, int window, dflash
   if (dt == DFLASH_BF16)
     s += align256(static_cast<size_t>(B) * Hkv * max_splits * rows * HD * sizeof(float)) +
          align256(static_cast<size_t>(B) * Hkv * max_splits * rows * sizeof(float2)) +
-         align256((static_cast<size_t>(B) * Hkv + 1) * sizeof(int));
+         align256(sizeof(int));
   return s + 256;
 }
 
@@ -823,7 +862,7 @@ dflash_status launch_block_attn(int layer, int B, int bs, int Hq, const void* q,
   p.out = static_cast<__nv_bfloat16*>(out);
   p.opart = w.take<float>(static_cast<size_t>(B) * Hkv * p.max_splits * p.rows * HD);
   p.mlpart = w.take<float2>(static_cast<size_t>(B) * Hkv * p.max_splits * p.rows);
-  p.counters = w.take<int>(static_cast<size_t>(B) * Hkv + 1);  // + the work-queue counter
+  p.counters = w.take<int>(1);
   p.scale_log2 = 1.4426950408889634f * scale;
   p.status = dev.status;
 
@@ -839,7 +878,7 @@ dflash_status launch_block_attn(int layer, int B, int bs, int Hq, const void* q,
   attn_prologue_kernel<__nv_bfloat16><<<B * bs, 256, 0, st>>>(
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(kb),
       static_cast<const __nv_bfloat16*>(qg), static_cast<const __nv_bfloat16*>(kg), c.seq_len, B, bs, Hq, Hkv,
-      c.capacity, eps, inv, qh, kbh, p.counters, B * Hkv + 1, dev.status);
+      c.capacity, eps, inv, qh, kbh, p.counters, 1, dev.status);
 
   const TcLayout lay = tc_layout(p.rows, B, static_cast<int>(dev.max_smem_optin));
   if (lay.stages < 2) return fail(DFLASH_ERR_UNSUPPORTED, "block_attn: shared memory");
@@ -863,6 +902,15 @@ dflash_status launch_block_attn(int layer, int B, int bs, int Hq, const void* q,
   cfg.numAttrs = 1;
   cudaError_t le = cudaLaunchKernelEx(&cfg, attn_tc_kernel, maps, p, lay);
   if (le != cudaSuccess) return cuda_fail(le, "attn_tc_kernel launch");
+  if (p.max_splits > 1) {
+    cudaLaunchConfig_t cc = cfg;
+    const long warps = static_cast<long>(B) * Hkv * p.rows;
+    cc.gridDim = dim3(static_cast<unsigned>((warps + 7) / 8));
+    cc.blockDim = dim3(256);
+    cc.dynamicSmemBytes = 0;
+    le = cudaLaunchKernelEx(&cc, attn_combine_kernel, p);
+    if (le != cudaSuccess) return cuda_fail(le, "attn_combine_kernel launch");
+  }
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? DFLASH_OK : cuda_fail(e, "block attention launch");
 }
