@@ -75,6 +75,10 @@ def lib():
     L.dflash_verify_workspace_size.restype = sz
     L.dflash_verify.argtypes = [vp, vp, i32, vp, i32, i32, i32, f32, u64, u64, vp, vp, vp, sz, vp]
     L.dflash_verify.restype = i32
+    L.dflash_verify_noalloc_max_scratch.argtypes = []
+    L.dflash_verify_noalloc_max_scratch.restype = sz
+    L.dflash_verify_noalloc.argtypes = [vp, vp, i32, vp, i32, i32, i32, f32, u64, u64, vp, vp, vp]
+    L.dflash_verify_noalloc.restype = i32
     L.dflash_philox4x32_10.argtypes = [vp, u32, u32, vp, i32, vp]
     L.dflash_philox4x32_10.restype = i32
     L.dflash_read_device_status.argtypes = [P(u32), vp]

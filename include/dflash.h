@@ -196,6 +196,34 @@ DFLASH_API dflash_status dflash_verify(const void* target_logits, const void* dr
                             void* workspace, size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * 3b. Verification without a caller workspace.  The DFlash pages have no
+ *     counterpart to this entry point; it serves callers that cannot allocate
+ *     device memory when they verify -- code inside a CUDA graph being
+ *     captured (cudaMalloc would break the capture), allocators that forbid
+ *     late allocation, plain C hosts with no device allocator.
+ *
+ *  Same arguments and results as dflash_verify, minus the workspace.  Scratch
+ *  comes from a static device array of dflash_verify_noalloc_max_scratch()
+ *  bytes (4 MiB) that every GPU loading the library holds until exit; sizes
+ *  needing more (dflash_verify_workspace_size() larger than that) are
+ *  rejected with DFLASH_ERR_UNSUPPORTED and nothing is launched.  No call
+ *  allocates or frees memory.  The first call on each device looks up the
+ *  array's device address (cudaGetSymbolAddress) with that device current;
+ *  make that first call before any stream capture.  All calls on a device
+ *  share the array: calls that overlap on the GPU race, so order them on one
+ *  stream.  The array keeps the last call's contents; nothing in it needs
+ *  clearing because every entry is written before it is read.
+ * ------------------------------------------------------------------------- */
+DFLASH_API size_t dflash_verify_noalloc_max_scratch(void);
+
+DFLASH_API dflash_status dflash_verify_noalloc(const void* target_logits, const void* draft_logits,
+                                               dflash_dtype dtype, const int32_t* draft_tokens,
+                                               int batch, int block_size, int vocab,
+                                               float temperature, uint64_t seed, uint64_t cycle,
+                                               int32_t* accepted_len, int32_t* out_tokens,
+                                               void* stream);
+
+/* ---------------------------------------------------------------------------
  * Diagnostics.
  * ------------------------------------------------------------------------- */
 
