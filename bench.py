@@ -352,84 +352,149 @@ def blas_threads():
     return os.cpu_count()
 
 
-def oracle_cycle_for(cfg, inputs, seqs, T):
-    """The oracle's full cycle for the sequences `seqs` of the batch."""
-    import oracle
-    w, seq, taps, blocks, lt, ld, x, k, v = inputs
-    rows = np.concatenate([np.arange(b * cfg.bs, (b + 1) * cfg.bs) for b in seqs])
-    pos = np.concatenate([seq[b] + np.arange(cfg.bs) for b in seqs])
-    oracle.fuse_rows([t[rows] for t in taps], w["w_fuse"], w["g_fuse"], w["w_kv"], w["k_gain"], pos, cfg.L,
-                     cfg.Hkv, cfg.d, bf16=True)
-    for l in range(cfg.L):
-        q, kb, vb = blocks[l]
-        oracle.block_attn(q[seqs], kb[seqs], vb[seqs], w["q_gain"][l], w["k_gain"][l], k[l][seqs], v[l][seqs],
-                          seq[seqs], bf16=True)
-    oracle.verify(lt[seqs], ld[seqs], x[seqs], T, 1234, 0, seq_ids=np.asarray(seqs))
+class OracleSample:
+    """Host (float64) copies of the workload for a few sampled sequences.
 
+    Weights, taps, block projections, logits and draft tokens are the same
+    seeded tensors the GPU arm uses; each sampled sequence's cached K/V (its
+    own seq_len rows per layer and head, synthetic N(0,1) in bf16 values) is
+    drawn up front from a generator seeded by the sequence index."""
 
-def oracle_inputs(cfg, T, seqs_needed):
-    """Host copies (float64) of the workload, restricted to the sampled sequences' data."""
-    f = lambda t: t.detach().to("cpu", torch.float64).numpy()  # noqa: E731
-    w = workloads.weights(cfg, "cpu")
-    wd = {"w_fuse": f(w.w_fuse), "g_fuse": f(w.g_fuse), "w_kv": f(w.w_kv), "k_gain": f(w.k_gain),
-          "q_gain": f(w.q_gain)}
-    seq = workloads.seq_lens(cfg).numpy()
-    taps = [f(t) for t in workloads.taps(cfg, cfg.B * cfg.bs, "cpu")]
-    blocks = [[f(t) for t in workloads.block(cfg, "cpu", layer=l)] for l in range(cfg.L)]
-    lt, ld = workloads.logits(cfg, "cpu")
-    x = workloads.draft_tokens(ld, T, seed=cfg.seed + 7).numpy()
-    nmax = int(seq[seqs_needed].max())
-    g = workloads.generator(cfg.seed * 1000 + 3, "cpu")
-    # cached K/V for the sampled sequences only (synthetic N(0,1), same shapes)
-    k = np.zeros((cfg.L, cfg.B, cfg.Hkv, nmax, cfg.d))
-    v = np.zeros_like(k)
-    for b in seqs_needed:
-        k[:, b] = torch.randn(cfg.L, cfg.Hkv, nmax, cfg.d, generator=g).to(torch.bfloat16).double().numpy()
-        v[:, b] = torch.randn(cfg.L, cfg.Hkv, nmax, cfg.d, generator=g).to(torch.bfloat16).double().numpy()
-    return wd, seq, taps, blocks, f(lt), f(ld), x, k, v
+    def __init__(self, cfg, T, seqs):
+        f = lambda t: t.detach().to("cpu", torch.float64).numpy()  # noqa: E731
+        self.cfg, self.T, self.seqs = cfg, T, list(seqs)
+        w = workloads.weights(cfg, "cpu")
+        self.w = {"w_fuse": f(w.w_fuse), "g_fuse": f(w.g_fuse), "w_kv": f(w.w_kv), "k_gain": f(w.k_gain),
+                  "q_gain": f(w.q_gain)}
+        self.seq = workloads.seq_lens(cfg).numpy().astype(np.int64)
+        taps = workloads.taps(cfg, cfg.B * cfg.bs, "cpu")
+        self.taps = {b: [f(t[b * cfg.bs:(b + 1) * cfg.bs]) for t in taps] for b in self.seqs}
+        blocks = [workloads.block(cfg, "cpu", layer=l) for l in range(cfg.L)]
+        self.blocks = {b: [[f(t[b:b + 1]) for t in blocks[l]] for l in range(cfg.L)] for b in self.seqs}
+        lt, ld = workloads.logits(cfg, "cpu")
+        x = workloads.draft_tokens(ld, T, seed=cfg.seed + 7)
+        self.lt = {b: f(lt[b:b + 1]) for b in self.seqs}
+        self.ld = {b: f(ld[b:b + 1]) for b in self.seqs}
+        self.x = {b: x[b:b + 1].numpy() for b in self.seqs}
+        # cached K/V of the sampled sequences: float32 holding bf16 values (the oracle
+        # widens what it reads to float64)
+        self._kv = {}
+        for b in self.seqs:
+            g = workloads.generator(cfg.seed * 1000 + 3 + b, "cpu")
+            n = int(self.seq[b])
+            k = torch.randn(cfg.L, 1, cfg.Hkv, n, cfg.d, generator=g).to(torch.bfloat16).float().numpy()
+            v = torch.randn(cfg.L, 1, cfg.Hkv, n, cfg.d, generator=g).to(torch.bfloat16).float().numpy()
+            self._kv[b] = (k, v)
+
+    def kv(self, b):
+        return self._kv[b]
+
+    # the three parts of one sequence's cycle, as the oracle computes them
+    def fuse(self, b):
+        import oracle
+        c = self.cfg
+        pos = self.seq[b] + np.arange(c.bs)
+        oracle.fuse_rows(self.taps[b], self.w["w_fuse"], self.w["g_fuse"], self.w["w_kv"], self.w["k_gain"], pos,
+                         c.L, c.Hkv, c.d, bf16=True)
+
+    def attn(self, b, l, g=None):
+        """Layer l of sequence b; g = one KV head (with its query group) or all heads."""
+        import oracle
+        c = self.cfg
+        k, v = self.kv(b)
+        q, kb, vb = self.blocks[b][l]
+        ck, cv = k[l], v[l]
+        if g is not None:
+            G = c.Hq // c.Hkv
+            q, kb, vb = q[:, g * G:(g + 1) * G], kb[:, g:g + 1], vb[:, g:g + 1]
+            ck, cv = ck[:, g:g + 1], cv[:, g:g + 1]
+        oracle.block_attn(q, kb, vb, self.w["q_gain"][l], self.w["k_gain"][l], ck, cv, self.seq[b:b + 1],
+                          bf16=True)
+
+    def verify(self, b):
+        import oracle
+        oracle.verify(self.lt[b], self.ld[b], self.x[b], self.T, 1234, 0, seq_ids=np.asarray([b]))
+
+    def cycle(self, b):
+        self.fuse(b)
+        for l in range(self.cfg.L):
+            self.attn(b, l)
+        self.verify(b)
 
 
 def cpu_baseline(cfg, seconds, T):
-    """Oracle cycles/s on the host: whole cycles of as many sequences as fit in
-    `seconds`, scaled to the B-sequence batch."""
-    sample_max = 8
-    seqs_all = list(range(sample_max))
-    inputs = oracle_inputs(cfg, T, seqs_all)
+    """Oracle cycles/s on the host: whole cycles of sampled sequences, repeated
+    until `seconds` have passed, scaled to the B-sequence batch."""
+    sample = OracleSample(cfg, T, range(8))
     t0 = time.perf_counter()
     done = 0
-    for b in seqs_all:
-        oracle_cycle_for(cfg, inputs, [b], T)
+    while True:
+        sample.cycle(sample.seqs[done % len(sample.seqs)])
         done += 1
         if time.perf_counter() - t0 > seconds:
             break
     el = time.perf_counter() - t0
+    ctx = float(np.mean([sample.seq[sample.seqs[i % len(sample.seqs)]] for i in range(done)]))
     per_cycle = el * cfg.B / done
     return {"value": 1.0 / per_cycle, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
-            "sample": "%d of %d sequences, each a full cycle (fusion of its 8 rows, 5 layers of block attention, "
-                      "verification), %.1f s, scaled x%g to the batch" % (done, cfg.B, el, cfg.B / done)}
+            "sample": "%d full single-sequence cycles (fusion of its 8 rows, 5 layers of block attention, "
+                      "verification) over sequences 0-7 (mean context %.0f vs %.0f for the batch), %.1f s, "
+                      "scaled x%d to the batch" % (done, ctx, float(sample.seq.mean()), el, cfg.B)}
 
 
 def run_reference(args):
+    """The oracle as the reference arm.  Each step is one unit of a sampled
+    sequence's cycle, rotating over fusion (one sequence), block attention
+    (one layer, one KV head with its query group) and verification (one
+    sequence); the batch cycle time is estimated as
+    B * (t_fuse + L * Hkv * t_attn_head + t_verify) from the units' means."""
     rank, world, _ = env_rank()
     if rank != 0:
         return
     cfg = workloads.BATCHED
-    seqs = list(range(min(cfg.B, max(args.steps, 1))))
-    inputs = oracle_inputs(cfg, args.temperature, list(range(min(cfg.B, 8))))
+    sample = OracleSample(cfg, args.temperature, range(8))
+    kinds = ("fuse", "attn", "verify")
+
+    def unit(i):
+        b = sample.seqs[(i // 3) % len(sample.seqs)]
+        kind = kinds[i % 3]
+        if kind == "fuse":
+            sample.fuse(b)
+        elif kind == "attn":
+            j = i // 3
+            sample.attn(b, j % cfg.L, (j // cfg.L) % cfg.Hkv)
+        else:
+            sample.verify(b)
+        return kind
+
     for i in range(args.warmup):
-        oracle_cycle_for(cfg, inputs, [i % 8], args.temperature)
+        unit(i)
+    times = {k: [] for k in kinds}
     t0 = time.perf_counter()
     for i in range(args.steps):
-        oracle_cycle_for(cfg, inputs, [i % 8], args.temperature)
+        ts = time.perf_counter()
+        k = unit(i)
+        times[k].append(time.perf_counter() - ts)
+    i = args.steps
+    while any(not v for v in times.values()):     # fewer than 3 steps: finish one unit of each kind
+        ts = time.perf_counter()
+        k = unit(i)
+        times[k].append(time.perf_counter() - ts)
+        i += 1
     el = time.perf_counter() - t0
-    value = args.steps / cfg.B / el        # each step is 1/B of a cycle
+    m = {k: statistics.mean(v) for k, v in times.items()}
+    cycle_s = cfg.B * (m["fuse"] + cfg.L * cfg.Hkv * m["attn"] + m["verify"])
+    value = 1.0 / cycle_s
+    sample_txt = ("%d oracle units (rotating: one sequence's fusion, one layer x KV head of block attention, "
+                  "one sequence's verification) over sequences 0-7, %.1f s; batch cycle = B x (fuse + L x Hkv x "
+                  "attn + verify) = %.2f s" % (i, el, cycle_s))
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": el * 1e3 / max(args.steps, 1),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": "batched: B=32, ragged context [1024, 8192], 5 layers, block 8, V=262144, T=%g"
                        % args.temperature},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
-                             "sample": "one sequence's full cycle per step (1/32 of a batch cycle)"},
+                             "sample": sample_txt},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 

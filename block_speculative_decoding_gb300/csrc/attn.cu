@@ -12,15 +12,21 @@
 //   prologue -- per (sequence, block row): RMSNorm * gain and RoPE of every
 //               query head and block key, rounded to the storage dtype; also
 //               clears the work-queue counter of the main kernel.
-//   main     -- split-KV, memory-bound: a persistent grid walks work items
-//               (sequence, KV head, key split).  A producer warp streams 64-key
-//               K/V tiles of the cache (and, for the last split, the block's
-//               own keys) with TMA (128-byte swizzle) through a 4-stage ring;
-//               one thread issues tcgen05.mma for S = Q K^T and O += P V into
-//               tensor memory; two softmax warps own one query row per thread
-//               (all Hq/Hkv heads x bs block rows of the KV head share every
-//               tile).  The last CTA to finish a (sequence, KV head) merges the
-//               splits' partial outputs (log-sum-exp).
+//   main     -- split-KV, memory-bound: a persistent grid (one CTA per SM)
+//               takes work items (sequence, KV head, key split) from an atomic
+//               queue; splits of one (sequence, KV head) are near-equal.  A
+//               producer warp streams 64-key K/V tiles of the cache (and, for
+//               the last split, the block's own keys) with TMA (128-byte
+//               swizzle) through a ring of up to six stages.  Q is loaded twice,
+//               as MMA rows 0.. and 64.. (two lane quarters); one thread issues
+//               S = Q K^T and another O += P V with tcgen05.mma; softmax warps
+//               own one query row per thread and per copy, each copy taking
+//               one half of every tile's keys, and write P (bf16 hi + lo) to
+//               tensor memory.  Epilogue warps merge the two copies (log-sum-
+//               exp) and write the output row, or a normalised fp32 partial
+//               and its (max, sum) when the item is one of several splits.
+//   combine  -- one warp per output row merges the splits' partials
+//               (log-sum-exp); launched as a programmatic dependent of main.
 // fp32 storage uses a plain SIMT kernel (parity path for the tiny fp32 case).
 #include <cuda.h>
 #include <cuda_bf16.h>
