@@ -42,9 +42,9 @@ namespace dflash {
 namespace {
 
 constexpr int HD = 128;
-constexpr int kTile = 64;                       // keys per TMA stage
-constexpr int kHalfTileBytes = kTile * 64 * 2;  // 64 keys x 64 dims bf16 = 8 KB (one TMA box)
-constexpr int kStageBytes = 4 * kHalfTileBytes; // K (2 boxes) + V (2 boxes) = 32 KB
+constexpr int kKeys = 128;                      // keys per tile (the tensor core's M)
+constexpr int kBoxBytes = kKeys * 64 * 2;       // 128 keys x 64 dims bf16 = 16 KB (one TMA box)
+constexpr int kHalfBytes = 2 * kBoxBytes;       // K (or V) of one tile: 32 KB
 constexpr int kMaxBatch = 2048;
 constexpr double kTwoPi = 6.283185307179586476925286766559;
 
@@ -61,8 +61,11 @@ struct AttnParams {
   __nv_bfloat16* out;        // [B, Hq, bs, 128]
   float* opart;              // [B, Hkv, max_splits, rows, 128] normalised partial outputs
   float2* mlpart;            // [B, Hkv, max_splits, rows]      (max, sum) in log2 units
+  const __nv_bfloat16* ck;   // this cache's K and V, [L, B, Hkv, cap, 128]
+  const __nv_bfloat16* cv;
   float scale_log2;          // log2(e) / sqrt(128)
-  int* counters;             // [1] work-queue counter (cleared by the prologue)
+  int* counters;             // [1 + B * Hkv]: work-queue counter, then one flag per (b, g)
+                             // whose scores outgrew the running max (cleared by the prologue)
   unsigned* status;
 };
 
@@ -131,25 +134,41 @@ __global__ void __launch_bounds__(256) attn_prologue_kernel(
 }
 
 // --------------------------------------------------------------------------
-// --------------------------------------------------------------------------
 // main split-KV kernel (bf16): tcgen05 tensor cores, TMA, TMEM accumulators
 // --------------------------------------------------------------------------
 //
-// Work item = (sequence b, KV head g, key split s).  Per 64-key tile:
-//   S   = Q K^T   tcgen05.mma M=128 (query rows; the Hq/Hkv*bs real rows sit in
-//                 TMEM lanes 0..rows-1), N=64 keys, K=128 -> TMEM (2 buffers)
-//   P   = 2^(S*scale - m)   one thread per query row (softmax warps 0, 1),
-//                 written to shared memory as bf16 hi + lo (K-major, swizzled)
-//   O  += P V     tcgen05.mma M=128, N=128 dims, K=64 keys, V read MN-major
-//                 straight from the TMA tile -> TMEM accumulator
-// The running max is only refreshed (and O rescaled) when it grows by more
-// than 2^8, so P stays within [0, 256].
-// Roles: warps 0-1 softmax/epilogue, warp 2 TMA producer, warp 3 MMA issuer.
+// The products are taken transposed, so that the 128 keys of a tile fill the
+// tensor core's M dimension and the few query rows of a (sequence, KV head)
+// (G * bs <= 64, padded to NC = 32 or 64) its N dimension:
+//   S^T = K Q^T    M = 128 keys, N = NC query rows, K = 128 dims; A = the K
+//                  tile (K-major), B = Q (K-major) -> tensor memory, key k in
+//                  lane k
+//   P^T = 2^(S^T * scale - m)   one softmax thread per key (lane), NC/32
+//                  warps per lane quarter; written to shared memory as bf16
+//                  hi and lo parts side by side (MN-major: the 2 NC values of
+//                  one key contiguous)
+//   O^T += V^T [P_hi^T P_lo^T]   M = 128 dims, N = 2 NC, K = 128 keys; A = the
+//                  V tile read MN-major, B = P^T -> tensor memory, dim d in
+//                  lane d; the epilogue adds the hi and lo columns
+// The running max m of each query row is set once per work item, from its
+// first tile, and shared by all keys (threads).  A later score may exceed it
+// by up to 2^64 without loss: P, its sums and O stay finite in fp32 / bf16 and
+// bf16 hi + lo keeps ~16 bits relative to each value.  If any score exceeds it
+// by more than that, the (sequence, KV head) is flagged and the combine kernel
+// recomputes its rows exactly.  The row sums are kept per thread and reduced
+// over the keys once per work item.
 
 struct Item {
   int b, g, s, nsplit, kstart, kend, ntiles, nt;  // nt = ntiles + (last split ? 1 block tile : 0)
   bool last;
 };
+
+__host__ __device__ __forceinline__ int split_start(int s, int nsplit, int ncache) {
+  if (s <= 0) return 0;
+  if (s >= nsplit) return ncache;
+  // near-equal ranges, interior boundaries on whole tiles
+  return static_cast<int>((static_cast<long>(s) * ncache) / nsplit) & ~(kKeys - 1);
+}
 
 // Work items in the order the queue hands them out: first every non-last
 // split, then the last split of every (b, g), which also carries the block
@@ -182,91 +201,119 @@ __device__ __forceinline__ Item decode_item(int w, const int* s_full_prefix, con
   it.g = g;
   it.nsplit = n_splits(ncache, p.chunk);
   it.s = s < 0 ? it.nsplit - 1 : s;
-  // the sequence's cached keys are cut into nsplit near-equal ranges
-  it.kstart = first + static_cast<int>((static_cast<long>(it.s) * ncache) / it.nsplit);
-  it.kend = first + static_cast<int>((static_cast<long>(it.s + 1) * ncache) / it.nsplit);
-  it.ntiles = it.kend > it.kstart ? (it.kend - it.kstart + kTile - 1) / kTile : 0;
+  it.kstart = first + split_start(it.s, it.nsplit, ncache);
+  it.kend = first + split_start(it.s + 1, it.nsplit, ncache);
+  it.ntiles = it.kend > it.kstart ? (it.kend - it.kstart + kKeys - 1) / kKeys : 0;
   it.last = it.s == it.nsplit - 1;
   it.nt = it.ntiles + (it.last ? 1 : 0);
   return it;
 }
 
-constexpr int kMaxStages = 6;
-constexpr int kTcThreads = 352;   // 11 warps, roles below
-constexpr int kRowBytes = 128;    // 64 bf16
-constexpr int kItemRing = 4;
-constexpr int kNumBars = 2 * kMaxStages + 6 * 2 * 2 + 2 * kItemRing;
-constexpr int kTmemCols = 512;
-// tensor-memory columns: S[2] (fp32, 64 keys), P[2] (bf16 pairs: hi 32, lo 32),
-// O[2] (fp32, 128 dims)
-constexpr uint32_t kColS = 0, kColP = 128, kColO = 256;
-constexpr uint32_t kIdescQK = umma_idesc_bf16(128, 64, false);
-constexpr uint32_t kIdescPV = umma_idesc_bf16(128, 128, true);
-constexpr float kRescaleLog2 = 8.0f;
+// Keys of tile t of an item that hold data (the block tile holds bs keys).
+__device__ __forceinline__ int tile_keys(const Item& it, int t, int bs) {
+  return t < it.ntiles ? min(kKeys, it.kend - (it.kstart + t * kKeys)) : bs;
+}
 
-// The Q tile is copied to MMA rows 0.. and 64.. (rows_pad = 32 or 64 query
-// rows each), so every query row owns two tensor-memory lanes: copy 0 keeps
-// keys 0-31 of each 64-key tile, copy 1 keys 32-63.  Each copy runs its own
-// online softmax and accumulates its own partial O; the epilogue merges the
-// two (log-sum-exp).  The softmax work of a tile is thus spread over two
-// (rows_pad 32) or four (rows_pad 64) SM sub-partitions.
-struct TcLayout {
-  int rows_pad;
-  int off_q, off_x, off_kv, stages, off_bar, off_misc, bytes;
+constexpr int kMaxRing = 4;       // K and V ring stages (each)
+constexpr int kSBufs = 4;         // S^T buffers in tensor memory
+constexpr int kItemRing = 4;
+constexpr int kBlockBoxRows = 16; // block keys per TMA box (bs <= 16)
+constexpr int kNumBars = 4 * kMaxRing + 2 * 2 + 2 * kSBufs + 4 * 2 + 2 * 2 + 2 * kItemRing + 2;
+constexpr float kOverflowLog2 = 64.0f;  // largest score above the running max, in log2 units
+
+template <int NC>
+struct TcCfg {
+  static constexpr int kCPW = NC == 32 ? 16 : 32;    // query rows (columns) per softmax warp
+  static constexpr int kSoftWarps = 4 * (NC / kCPW);  // two softmax warps per lane quarter
+  static constexpr int kEpiWarp0 = kSoftWarps;      // 4 epilogue warps, one per lane quarter
+  static constexpr int kProdWarp = kSoftWarps + 4;
+  static constexpr int kSWarp = kSoftWarps + 5;     // S^T = K Q^T issuer (also allocates TMEM)
+  static constexpr int kOWarp = kSoftWarps + 6;     // O^T += V^T P^T issuer
+  static constexpr int kThreads = 32 * (kSoftWarps + 7);
+  // tensor memory: S^T [kSBufs] x NC columns, then O^T [2] x 2 NC columns (hi, lo)
+  static constexpr uint32_t kTmemCols = NC == 32 ? 256 : 512;
+  static constexpr uint32_t kColS = 0, kColO = kSBufs * NC;
+  static constexpr int kQBoxBytes = NC * 128;       // NC rows x 64 dims bf16
+  // P^T of one tile: 128 keys x (NC hi + NC lo) bf16, 128-byte swizzled rows of
+  // 64 values; NC = 32: one row per key (hi | lo); NC = 64: a hi block of 128
+  // rows, then a lo block
+  static constexpr int kPBytes = kKeys * 2 * NC * 2;
+  static constexpr uint32_t kPLoOffset = NC == 32 ? 64u : 16384u;   // lo part of a key's values
+  static constexpr uint32_t kIdescS = umma_idesc_bf16(128, NC, false, false);
+  static constexpr uint32_t kIdescO = umma_idesc_bf16(128, 2 * NC, true, true);
 };
 
-__host__ __device__ inline TcLayout tc_layout(int rows, int B, int smem_limit) {
+struct TcLayout {
+  int nk, nv;
+  int off_q, off_p, off_k, off_v, off_bar, off_misc, bytes;
+};
+
+__host__ __device__ inline int tc_misc_bytes(int B, int nc) {
+  // tmem slot + item ring (64) | s_m [2][NC] | s_l [2][4][NC] | s_red [2 halves][2][4][32] |
+  // prefix [B+1], n [B]
+  return 64 + 2 * nc * 4 + 2 * 4 * nc * 4 + 2 * 2 * 4 * 32 * 4 + (2 * B + 1) * 4;
+}
+
+__host__ __device__ inline TcLayout tc_layout(int nc, int B, int smem_limit) {
   TcLayout L;
-  L.rows_pad = rows > 32 ? 64 : 32;
-  // Q: two 64-dim boxes of 128 MMA rows; buffer q sits rows_pad rows in, so for
-  // rows_pad = 32 both buffers fit in one 32 KB region, for 64 in two.
-  const int qbytes = L.rows_pad == 32 ? 32768 : 65536;
-  L.off_q = 0;
-  L.off_x = qbytes;                                   // O exchange of copy 1 -> copy 0
-  L.off_kv = L.off_x + L.rows_pad * 128 * 4;
-  const int misc = 64 + 2 * 2 * 64 * 8 + (2 * B + 1) * 4;
-  const int fixed = 1024 + L.off_kv + 8 * kNumBars + misc;
-  int st = (smem_limit - fixed) / kStageBytes;
-  L.stages = st > kMaxStages ? kMaxStages : st;
-  L.off_bar = L.off_kv + L.stages * kStageBytes;
+  L.off_q = 0;                           // 2 buffers x 2 boxes of NC rows
+  L.off_p = 4 * nc * 128;                // 2 buffers of P^T (hi and lo)
+  L.off_k = L.off_p + 2 * kKeys * 2 * nc * 2;
+  const int fixed = 1024 + L.off_k + 8 * kNumBars + tc_misc_bytes(B, nc);
+  int total = (smem_limit - fixed) / kHalfBytes;
+  if (total > 2 * kMaxRing) total = 2 * kMaxRing;
+  L.nv = (total + 1) / 2;
+  L.nk = total - L.nv;
+  L.off_v = L.off_k + L.nk * kHalfBytes;
+  L.off_bar = L.off_v + L.nv * kHalfBytes;
   L.off_misc = L.off_bar + 8 * kNumBars;
-  L.bytes = 1024 + L.off_misc + misc;
+  L.bytes = 1024 + L.off_misc + tc_misc_bytes(B, nc);
   return L;
 }
 
-// Byte offset of Q buffer `qb` copy `c` box `h` (64-dim half) in the Q region.
-__device__ __forceinline__ uint32_t q_off(const TcLayout& L, int qb, int c, int h) {
-  if (L.rows_pad == 32) return static_cast<uint32_t>(h * 16384 + c * 8192 + qb * 4096);
-  return static_cast<uint32_t>(qb * 32768 + h * 16384 + c * 8192);
-}
-
-// Thread `row` owns one query row: write its final output (single split) or
-// its normalised partial output and (m, l) for the combine kernel.
-__device__ __forceinline__ void finish_item(const Item& it, const AttnParams& p, int row, const float (&o)[HD],
-                                            float m, float l) {
-  if (row >= p.rows) return;
-  const float inv = l > 0.f ? 1.f / l : 0.f;
-  if (it.nsplit == 1) {
-    const size_t out_row0 = (static_cast<size_t>(it.b) * p.Hq + it.g * p.G) * p.bs;
-    uint4* dst = reinterpret_cast<uint4*>(p.out + (out_row0 + row) * HD);
-#pragma unroll
-    for (int i = 0; i < HD / 8; ++i)
-      dst[i] = make_uint4(pack_bf16x2(o[8 * i] * inv, o[8 * i + 1] * inv),
-                          pack_bf16x2(o[8 * i + 2] * inv, o[8 * i + 3] * inv),
-                          pack_bf16x2(o[8 * i + 4] * inv, o[8 * i + 5] * inv),
-                          pack_bf16x2(o[8 * i + 6] * inv, o[8 * i + 7] * inv));
-    return;
+// One output row computed key by key (4 dims per lane, exact running max):
+// the fallback for a (sequence, KV head) whose scores outgrew the running max
+// of the tensor-core kernel.
+__device__ void attn_row_exact(const AttnParams& p, int b, int g, int row, int first, int n) {
+  const int lane = threadIdx.x % 32;
+  const int h = g * p.G + row / p.bs, j = row % p.bs;
+  const float4 q = bf16x4_to_f32(p.qh + ((static_cast<size_t>(b) * p.Hq + h) * p.bs + j) * HD + 4 * lane);
+  const size_t cbase = ((static_cast<size_t>(p.layer) * p.B + b) * p.Hkv + g) * p.cap;
+  const size_t bbase = (static_cast<size_t>(b) * p.Hkv + g) * p.bs;
+  float m = -INFINITY, l = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int t = first; t < n + p.bs; ++t) {
+    const bool blk = t >= n;
+    const __nv_bfloat16* kr = blk ? p.kbh + (bbase + (t - n)) * HD : p.ck + (cbase + t) * HD;
+    const __nv_bfloat16* vr = blk ? p.vb + (bbase + (t - n)) * HD : p.cv + (cbase + t) * HD;
+    const float4 k = bf16x4_to_f32(kr + 4 * lane);
+    const float s = warp_sum(q.x * k.x + q.y * k.y + q.z * k.z + q.w * k.w) * p.scale_log2;
+    const float4 v = bf16x4_to_f32(vr + 4 * lane);
+    if (s > m) {
+      const float f = exp2f(m - s);
+      l *= f;
+      acc.x *= f;
+      acc.y *= f;
+      acc.z *= f;
+      acc.w *= f;
+      m = s;
+    }
+    const float e = exp2f(s - m);
+    l += e;
+    acc.x += e * v.x;
+    acc.y += e * v.y;
+    acc.z += e * v.z;
+    acc.w += e * v.w;
   }
-  const size_t r = ((static_cast<size_t>(it.b) * p.Hkv + it.g) * p.max_splits + it.s) * p.rows + row;
-  float4* dst = reinterpret_cast<float4*>(p.opart + r * HD);
-#pragma unroll
-  for (int i = 0; i < HD / 4; ++i)
-    dst[i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv, o[4 * i + 3] * inv);
-  p.mlpart[r] = make_float2(m, l);
+  const float inv = 1.f / l;
+  const size_t out_row = (static_cast<size_t>(b) * p.Hq + g * p.G) * p.bs + row;
+  reinterpret_cast<uint2*>(p.out + out_row * HD)[lane] =
+      make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
 }
 
-// Log-sum-exp merge of the split partials of every (sequence, KV head) that
-// has more than one split: one warp per output row, 4 dims per lane.
+// Per output row (one warp, 4 dims per lane): the log-sum-exp merge of the
+// split partials of a (sequence, KV head) with more than one split, or the
+// exact recomputation of a (sequence, KV head) the main kernel flagged.
 __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnParams p) {
   pdl_wait_primary();
   const int gw = blockIdx.x * 8 + threadIdx.x / 32;   // global warp = (b, g, row)
@@ -277,6 +324,10 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnParams p) {
   const int b = bg / p.Hkv, g = bg % p.Hkv;
   const int n = min(max(p.seq_len[b], 0), p.cap);
   const int first = p.window > 0 ? max(0, n - p.window) : 0;
+  if (p.counters[1 + bg] != 0) {
+    attn_row_exact(p, b, g, row, first, n);
+    return;
+  }
   const int ns = n_splits(n - first, p.chunk);
   if (ns <= 1) return;
   const size_t r0 = static_cast<size_t>(bg) * p.max_splits * p.rows + row;
@@ -331,64 +382,120 @@ __device__ __forceinline__ int next_item(uint32_t it_full, uint32_t it_empty, co
   return w;
 }
 
-// Roles: warps 0-3 softmax of tensor-memory lane quarter = warp, warps 4-7
-// epilogue of lane quarter = warp - 4 (only the quarters holding query rows
-// are active), warp 8 TMA producer, warp 9 S = Q K^T issuer, warp 10
-// O += P V issuer.
-__global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_constant__ AttnMaps maps,
-                                                                const AttnParams p, const TcLayout lay) {
+// Sum over the warp's 32 lanes of each v[j] (N = 16 or 32 values); lane i
+// returns the sum of v[i % N].  Exchange rounds halve the values a lane keeps
+// (for N = 16 the two half-warps are added first).
+template <int N>
+__device__ __forceinline__ float warp_reduce_scatter_sum(float (&v)[N], int lane) {
+  if (N == 16) {
+#pragma unroll
+    for (int j = 0; j < N; ++j) v[j] += __shfl_xor_sync(0xffffffffu, v[j], 16);
+  }
+#pragma unroll
+  for (int w = N / 2; w >= 1; w >>= 1) {
+    const bool upper = (lane & w) != 0;
+#pragma unroll
+    for (int j = 0; j < w; ++j) {
+      const float send = upper ? v[j] : v[j + w];
+      const float keep = upper ? v[j + w] : v[j];
+      v[j] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+    }
+  }
+  return v[0];
+}
+
+// Maximum of N values by a tree of pairwise maxima.
+template <int N>
+__device__ __forceinline__ float array_max(const float (&v)[N]) {
+  float t[N / 2];
+#pragma unroll
+  for (int i = 0; i < N / 2; ++i) t[i] = fmaxf(v[2 * i], v[2 * i + 1]);
+#pragma unroll
+  for (int w = N / 4; w >= 1; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) t[i] = fmaxf(t[i], t[i + w]);
+  return t[0];
+}
+
+// N (16 or 32) columns of this warp's lane quarter as floats.
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&d)[N]) {
+  uint32_t r[N];
+  if constexpr (N == 16) tmem_ld_16cols(taddr, r);
+  else tmem_ld_32cols(taddr, r);
+  tmem_ld_wait();
+#pragma unroll
+  for (int j = 0; j < N; ++j) d[j] = __uint_as_float(r[j]);
+}
+
+// Roles (c = NC/2 query rows per softmax warp):
+//   warps 0 .. 7       softmax: warp w owns key (lane) 32*(w%4) + lane of every
+//                      tile and query rows c*(w/4) .. +c-1
+//   warps 8 .. 11      epilogue: O^T lanes (dims) of lane quarter w%4
+//   warp 12            TMA producer (work queue, Q, K ring, V ring)
+//   warp 13            S^T = K Q^T issuer; allocates tensor memory
+//   warp 14            O^T += V^T P^T issuer
+template <int NC>
+__global__ void __launch_bounds__(TcCfg<NC>::kThreads, 1) attn_tc_kernel(const __grid_constant__ AttnMaps maps,
+                                                                         const AttnParams p, const TcLayout lay) {
+  using C = TcCfg<NC>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
-  const int S = lay.stages;
+  const int NK = lay.nk, NV = lay.nv;
   const uint32_t bar0 = base + lay.off_bar;
-  const uint32_t kv_full = bar0, kv_empty = bar0 + 8 * kMaxStages;
-  const uint32_t q_full = bar0 + 16 * kMaxStages, q_empty = q_full + 16;
-  const uint32_t s_full = q_empty + 16, s_empty = s_full + 16;
-  const uint32_t p_full = s_empty + 16, p_empty = p_full + 16;
+  const uint32_t k_full = bar0, k_empty = k_full + 8 * kMaxRing;
+  const uint32_t v_full = k_empty + 8 * kMaxRing, v_empty = v_full + 8 * kMaxRing;
+  const uint32_t q_full = v_empty + 8 * kMaxRing, q_empty = q_full + 16;
+  const uint32_t s_full = q_empty + 16, s_empty = s_full + 8 * kSBufs;
+  const uint32_t p_full = s_empty + 8 * kSBufs, p_empty = p_full + 16;
   const uint32_t o_full = p_empty + 16, o_free = o_full + 16;
   const uint32_t ml_full = o_free + 16, ml_empty = ml_full + 16;
   const uint32_t it_full = ml_empty + 16, it_empty = it_full + 8 * kItemRing;
+  const uint32_t red_bar = it_empty + 8 * kItemRing;  // one per column half
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + lay.off_misc);
-  int* s_item = reinterpret_cast<int*>(tmem_slot + 8);                    // kItemRing entries
-  float2* s_ml = reinterpret_cast<float2*>(gbase + lay.off_misc + 64);    // [2 buf][2 copy][64 row]
-  int* s_prefix = reinterpret_cast<int*>(gbase + lay.off_misc + 64 + 2 * 2 * 64 * 8);
+  int* s_item = reinterpret_cast<int*>(tmem_slot + 8);                           // kItemRing entries
+  float* s_m = reinterpret_cast<float*>(gbase + lay.off_misc + 64);               // [2][NC]
+  float* s_l = s_m + 2 * NC;                                                       // [2][4][NC]
+  float* s_red = s_l + 2 * 4 * NC;                                                 // [2 halves][2][4][32]
+  int* s_prefix = reinterpret_cast<int*>(s_red + 2 * 2 * 4 * 32);
   int* s_n = s_prefix + (p.B + 1);
-  float* s_x = reinterpret_cast<float*>(gbase + lay.off_x);             // [rows_pad][128]
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int nq = lay.rows_pad / 32;   // lane quarters per copy: 1 or 2
-  const int n_sm = 2 * nq;            // active softmax warps (and epilogue warps)
-  // quarter q is active when its lanes hold a query row: q % 2 < nq
   if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(kv_full + 8 * s, 1);
-      mbar_init(kv_empty + 8 * s, 1);
+    for (int s = 0; s < kMaxRing; ++s) {
+      mbar_init(k_full + 8 * s, 1);
+      mbar_init(k_empty + 8 * s, 1);
+      mbar_init(v_full + 8 * s, 1);
+      mbar_init(v_empty + 8 * s, 1);
+    }
+    for (int s = 0; s < kSBufs; ++s) {
+      mbar_init(s_full + 8 * s, 1);
+      mbar_init(s_empty + 8 * s, C::kSoftWarps);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(q_full + 8 * i, 1);
       mbar_init(q_empty + 8 * i, 1);
-      mbar_init(s_full + 8 * i, 1);
-      mbar_init(s_empty + 8 * i, n_sm);
-      mbar_init(p_full + 8 * i, n_sm);
+      mbar_init(p_full + 8 * i, C::kSoftWarps);
       mbar_init(p_empty + 8 * i, 1);
       mbar_init(o_full + 8 * i, 1);
-      mbar_init(o_free + 8 * i, n_sm);
-      mbar_init(ml_full + 8 * i, n_sm);
-      mbar_init(ml_empty + 8 * i, n_sm);
+      mbar_init(o_free + 8 * i, 4);
+      mbar_init(ml_full + 8 * i, C::kSoftWarps);
+      mbar_init(ml_empty + 8 * i, 4);
     }
     for (int i = 0; i < kItemRing; ++i) {
       mbar_init(it_full + 8 * i, 1);
-      mbar_init(it_empty + 8 * i, 2 + 2 * n_sm);
+      mbar_init(it_empty + 8 * i, 2 + C::kSoftWarps + 4);
     }
+    for (int i = 0; i < 2; ++i) mbar_init(red_bar + 8 * i, 4);
     mbar_fence_init();
   }
-  if (warp == 9) {
-    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+  if (warp == C::kSWarp) {
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 8) {  // per-sequence lengths and the prefix of full (non-last) splits
+  if (warp == C::kProdWarp) {  // per-sequence lengths and the prefix of full (non-last) splits
     for (int b = lane; b < p.B; b += 32) s_n[b] = clamp_seq(p.seq_len[b], p.cap, p.status);
     __syncwarp();
     if (lane == 0) {
@@ -408,15 +515,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   const uint32_t tmem = *tmem_slot;
   const int n_items = s_prefix[p.B] + p.B * p.Hkv;
 
-  if (warp == 8) {
+  if (warp == C::kProdWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&maps.k);
       tma_prefetch_desc(&maps.v);
       tma_prefetch_desc(&maps.q);
-      pdl_wait_primary();  // the prologue's Q, block keys and cleared counters
+      pdl_wait_primary();  // the prologue's Q, block keys and cleared counter
       const uint64_t pol = l2_policy_evict_first();
-      Ring kv, q, itr;
+      Ring kr, vr, q, itr;
       bool ok = true;
       while (ok) {
         const int w = atomicAdd(p.counters, 1);
@@ -427,39 +534,47 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         if (w >= n_items) break;
         const Item it = decode_item(w, s_prefix, s_n, p);
         if (!(ok = mbar_wait(q_empty + 8 * q.idx, q.phase ^ 1u, p.status))) break;
-        mbar_arrive_expect_tx(q_full + 8 * q.idx, 4 * lay.rows_pad * kRowBytes);
+        mbar_arrive_expect_tx(q_full + 8 * q.idx, 2 * C::kQBoxBytes);
         const int qrow = (it.b * p.Hq + it.g * p.G) * p.bs;
-        for (int c = 0; c < 2; ++c)
-          for (int h = 0; h < 2; ++h)
-            tma_load_2d(base + lay.off_q + q_off(lay, q.idx, c, h), &maps.q, q_full + 8 * q.idx, 64 * h, qrow);
+        const uint32_t qdst = base + lay.off_q + q.idx * 2 * C::kQBoxBytes;
+        tma_load_2d(qdst, &maps.q, q_full + 8 * q.idx, 0, qrow);
+        tma_load_2d(qdst + C::kQBoxBytes, &maps.q, q_full + 8 * q.idx, 64, qrow);
         q.next(2);
         const int rowbase = ((p.layer * p.B + it.b) * p.Hkv + it.g) * p.cap;
         const int brow = (it.b * p.Hkv + it.g) * p.bs;
-        for (int t = 0; t < it.nt; ++t) {
-          if (!(ok = mbar_wait(kv_empty + 8 * kv.idx, kv.phase ^ 1u, p.status))) break;
-          const uint32_t fb = kv_full + 8 * kv.idx;
-          mbar_arrive_expect_tx(fb, kStageBytes);
-          const uint32_t dst = base + lay.off_kv + kv.idx * kStageBytes;
-          if (t < it.ntiles) {
-            const int y = rowbase + it.kstart + t * kTile;
-            tma_load_2d_hint(dst, &maps.k, fb, 0, y, pol);
-            tma_load_2d_hint(dst + kHalfTileBytes, &maps.k, fb, 64, y, pol);
-            tma_load_2d_hint(dst + 2 * kHalfTileBytes, &maps.v, fb, 0, y, pol);
-            tma_load_2d_hint(dst + 3 * kHalfTileBytes, &maps.v, fb, 64, y, pol);
-          } else {  // the block's own keys and values
-            tma_load_2d(dst, &maps.kb, fb, 0, brow);
-            tma_load_2d(dst + kHalfTileBytes, &maps.kb, fb, 64, brow);
-            tma_load_2d(dst + 2 * kHalfTileBytes, &maps.vb, fb, 0, brow);
-            tma_load_2d(dst + 3 * kHalfTileBytes, &maps.vb, fb, 64, brow);
+        for (int t = 0; t < it.nt && ok; ++t) {
+          const bool blk = t >= it.ntiles;
+          const uint32_t bytes = blk ? 2 * kBlockBoxRows * 128 : kHalfBytes;
+          const int y = rowbase + it.kstart + t * kKeys;
+          if (!(ok = mbar_wait(k_empty + 8 * kr.idx, kr.phase ^ 1u, p.status))) break;
+          const uint32_t kdst = base + lay.off_k + kr.idx * kHalfBytes;
+          mbar_arrive_expect_tx(k_full + 8 * kr.idx, bytes);
+          if (!blk) {
+            tma_load_2d_hint(kdst, &maps.k, k_full + 8 * kr.idx, 0, y, pol);
+            tma_load_2d_hint(kdst + kBoxBytes, &maps.k, k_full + 8 * kr.idx, 64, y, pol);
+          } else {
+            tma_load_2d(kdst, &maps.kb, k_full + 8 * kr.idx, 0, brow);
+            tma_load_2d(kdst + kBoxBytes, &maps.kb, k_full + 8 * kr.idx, 64, brow);
           }
-          kv.next(S);
+          kr.next(NK);
+          if (!(ok = mbar_wait(v_empty + 8 * vr.idx, vr.phase ^ 1u, p.status))) break;
+          const uint32_t vdst = base + lay.off_v + vr.idx * kHalfBytes;
+          mbar_arrive_expect_tx(v_full + 8 * vr.idx, bytes);
+          if (!blk) {
+            tma_load_2d_hint(vdst, &maps.v, v_full + 8 * vr.idx, 0, y, pol);
+            tma_load_2d_hint(vdst + kBoxBytes, &maps.v, v_full + 8 * vr.idx, 64, y, pol);
+          } else {
+            tma_load_2d(vdst, &maps.vb, v_full + 8 * vr.idx, 0, brow);
+            tma_load_2d(vdst + kBoxBytes, &maps.vb, v_full + 8 * vr.idx, 64, brow);
+          }
+          vr.next(NV);
         }
       }
     }
-  } else if (warp == 9) {
-    // ------------------------------------------------ S = Q K^T issuer
+  } else if (warp == C::kSWarp) {
+    // ------------------------------------------------ S^T = K Q^T issuer
     if (lane == 0) {
-      Ring kv, q, sq, itr;
+      Ring kr, q, sq, itr;
       bool ok = true;
       while (ok) {
         if (!(ok = mbar_wait(it_full + 8 * itr.idx, itr.phase, p.status))) break;
@@ -469,30 +584,32 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         if (w < 0) break;
         const Item it = decode_item(w, s_prefix, s_n, p);
         if (!(ok = mbar_wait(q_full + 8 * q.idx, q.phase, p.status))) break;
+        const uint32_t qb = base + lay.off_q + q.idx * 2 * C::kQBoxBytes;
         for (int t = 0; t < it.nt && ok; ++t) {
-          if (!(ok = mbar_wait(kv_full + 8 * kv.idx, kv.phase, p.status))) break;
+          if (!(ok = mbar_wait(k_full + 8 * kr.idx, kr.phase, p.status))) break;
           if (!(ok = mbar_wait(s_empty + 8 * sq.idx, sq.phase ^ 1u, p.status))) break;
           tc_fence_after_sync();
-          const uint32_t kb = base + lay.off_kv + kv.idx * kStageBytes;
+          const uint32_t kb = base + lay.off_k + kr.idx * kHalfBytes;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t ad = umma_desc_kmajor_sw128(base + lay.off_q + q_off(lay, q.idx, 0, kk >> 2)) + 2 * (kk & 3);
-            const uint64_t bd = umma_desc_kmajor_sw128(kb + (kk >> 2) * kHalfTileBytes) + 2 * (kk & 3);
-            umma_bf16(tmem + kColS + 64 * sq.idx, ad, bd, kIdescQK, kk > 0 ? 1u : 0u);
+            const uint64_t ad = umma_desc_kmajor_sw128(kb + (kk >> 2) * kBoxBytes) + 2 * (kk & 3);
+            const uint64_t bd = umma_desc_kmajor_sw128(qb + (kk >> 2) * C::kQBoxBytes) + 2 * (kk & 3);
+            umma_bf16(tmem + C::kColS + NC * sq.idx, ad, bd, C::kIdescS, kk > 0 ? 1u : 0u);
           }
           umma_commit(s_full + 8 * sq.idx);
-          sq.next(2);
-          kv.next(S);
+          umma_commit(k_empty + 8 * kr.idx);
+          sq.next(kSBufs);
+          kr.next(NK);
         }
         if (!ok) break;
         umma_commit(q_empty + 8 * q.idx);
         q.next(2);
       }
     }
-  } else if (warp == 10) {
-    // ------------------------------------------------ O += P V issuer
+  } else if (warp == C::kOWarp) {
+    // ------------------------------------------------ O^T += V^T P^T issuer
     if (lane == 0) {
-      Ring kv, pr, o, itr;
+      Ring vr, pr, o, itr;
       bool ok = true;
       while (ok) {
         if (!(ok = mbar_wait(it_full + 8 * itr.idx, itr.phase, p.status))) break;
@@ -501,213 +618,240 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         itr.next(kItemRing);
         if (w < 0) break;
         const Item it = decode_item(w, s_prefix, s_n, p);
-        const uint32_t od = tmem + kColO + 128 * o.idx;
+        const uint32_t od = tmem + C::kColO + 2 * NC * o.idx;
         for (int t = 0; t < it.nt && ok; ++t) {
           if (!(ok = mbar_wait(p_full + 8 * pr.idx, pr.phase, p.status))) break;
           if (t == 0 && !(ok = mbar_wait(o_free + 8 * o.idx, o.phase ^ 1u, p.status))) break;
+          if (!(ok = mbar_wait(v_full + 8 * vr.idx, vr.phase, p.status))) break;
           tc_fence_after_sync();
-          const uint32_t vbase = base + lay.off_kv + kv.idx * kStageBytes + 2 * kHalfTileBytes;
-          const uint64_t vdesc = umma_desc_mnmajor_sw128(vbase, kHalfTileBytes, 1024);
-          const uint32_t pa = tmem + kColP + 64 * pr.idx;
+          const int nsteps = (tile_keys(it, t, p.bs) + 15) / 16;
+          // A = V^T: two 64-dim blocks 16 KB apart, 8-key groups 1 KB apart;
+          // B = P^T: NC = 32 one 64-value block, NC = 64 two (hi, lo) 16 KB apart
+          const uint64_t vd = umma_desc_mnmajor(base + lay.off_v + vr.idx * kHalfBytes, kBoxBytes, 1024, 2u);
+          const uint64_t pd = umma_desc_mnmajor(base + lay.off_p + pr.idx * C::kPBytes, 16384, 1024, 2u);
 #pragma unroll
-          for (int h = 0; h < 2; ++h)
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              umma_bf16_ts(od, pa + 32 * h + 8 * kk, vdesc + 128 * kk, kIdescPV, (t == 0 && h == 0 && kk == 0) ? 0u : 1u);
+          for (int j = 0; j < 8; ++j)  // one step = 16 keys = 2 KB of V^T and of P^T
+            if (j < nsteps) umma_bf16(od, vd + 128 * j, pd + 128 * j, C::kIdescO, (t > 0 || j > 0) ? 1u : 0u);
           umma_commit(p_empty + 8 * pr.idx);
-          umma_commit(kv_empty + 8 * kv.idx);
+          umma_commit(v_empty + 8 * vr.idx);
           pr.next(2);
-          kv.next(S);
+          vr.next(NV);
         }
         if (!ok) break;
         umma_commit(o_full + 8 * o.idx);
         o.next(2);
       }
     }
-  } else if (warp <= 3) {
+  } else if (warp < C::kSoftWarps) {
     // ------------------------------------------------ softmax
-    if ((warp & 1) < nq) {
-      const int lg = 32 * warp + lane;         // tensor-memory lane
-      const int row = lg % 64;                 // query row (rows_pad = 32: quarters 0, 2)
-      const int copy = lg / 64;                // copy 0: keys 0-31, copy 1: keys 32-63
-      const int key0 = 32 * copy;
-      const uint32_t tl = tmem + (static_cast<uint32_t>(32 * warp) << 16);
-      const float scale = p.scale_log2;
-      {  // the other copy's key columns of both P buffers stay zero for the whole kernel
-        uint32_t z[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) z[i] = 0u;
-#pragma unroll
-        for (int pb = 0; pb < 2; ++pb) {
-          tmem_st_32cols(tl + kColP + 64 * pb, z);
-          tmem_st_32cols(tl + kColP + 64 * pb + 32, z);
-        }
-        tmem_st_wait();
+    constexpr int CW = C::kCPW;
+    const int qd = warp & 3;                 // lane quarter
+    const int hc = warp >> 2;                // column group: query rows CW*hc .. +CW-1
+    const int key = 32 * qd + lane;          // this thread's key of every tile
+    const uint32_t tl = tmem + (static_cast<uint32_t>(32 * qd) << 16);
+    const float scale = p.scale_log2;
+    // this key's P^T values in a P buffer: 128-byte rows, the 16-byte chunk c of
+    // a row stored at chunk c ^ (key & 7)
+    const uint32_t prow = key * 128;
+    // The four warps of a column group agree on the running max of a work item
+    // through one mbarrier (bounded waits) on its first tile; the exchange
+    // slots alternate by phase.
+    const uint32_t rbar = red_bar + 8 * hc;
+    uint32_t rph = 0;
+    Ring sr, vr, mlr, itr;
+    int pb = 0;
+    int pcnt[2] = {0, 0};
+    bool ok = true;
+    while (ok) {
+      const int w = next_item(it_full, it_empty, s_item, itr, p.status);
+      if (w < 0) break;
+      const Item it = decode_item(w, s_prefix, s_n, p);
+      float m[CW], l[CW];
+      float dmax = -INFINITY;  // largest score above m over the item's later tiles
+      for (int t = 0; t < it.nt; ++t) {
+        if (!(ok = mbar_wait(s_full + 8 * sr.idx, sr.phase, p.status))) break;
+        tc_fence_after_sync();
+        float d[CW];
+        tmem_ld_cols<CW>(tl + C::kColS + NC * sr.idx + CW * hc, d);
         tc_fence_before_sync();
-      }
-      Ring sr, mlr, itr;
-      int ob = 0, pb = 0;
-      int pcnt[2] = {0, 0};
-      bool ok = true;
-      while (ok) {
-        const int w = next_item(it_full, it_empty, s_item, itr, p.status);
-        if (w < 0) break;
-        const Item it = decode_item(w, s_prefix, s_n, p);
-        float m_used = -INFINITY, l = 0.f;
-        for (int t = 0; t < it.nt; ++t) {
-          if (!(ok = mbar_wait(s_full + 8 * sr.idx, sr.phase, p.status))) break;
-          tc_fence_after_sync();
-          float x[32];
-          {
-            uint32_t r[32];
-            tmem_ld_32cols(tl + kColS + 64 * sr.idx + key0, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(r[i]);
-          }
-          tc_fence_before_sync();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(s_empty + 8 * sr.idx);
-          sr.next(2);
-          const int nvalid = (t < it.ntiles ? min(kTile, it.kend - (it.kstart + t * kTile)) : p.bs) - key0;
-          if (nvalid < 32) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (i >= nvalid) x[i] = -INFINITY;
-          }
-          float mx[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) mx[i] = fmaxf(fmaxf(x[4 * i], x[4 * i + 1]), fmaxf(x[4 * i + 2], x[4 * i + 3]));
-#pragma unroll
-          for (int w2 = 4; w2 >= 1; w2 >>= 1)
-#pragma unroll
-            for (int i = 0; i < w2; ++i) mx[i] = fmaxf(mx[i], mx[i + w2]);
-          const float mt = mx[0] * scale;
-          const bool need = m_used == -INFINITY ? (mt != -INFINITY) : (mt > m_used + kRescaleLog2);
-          if (__any_sync(0xffffffffu, need) && t > 0) {
-            // this copy's O must hold every P V product up to tile t-1 before it is rescaled
-            const int xb = pb ^ 1;
-            if (!(ok = mbar_wait(p_empty + 8 * xb, (pcnt[xb] - 1) & 1, p.status))) break;
-            tc_fence_after_sync();
-            const float f = need ? (m_used == -INFINITY ? 0.f : exp2f(m_used - mt)) : 1.f;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              uint32_t r[32];
-              tmem_ld_32cols(tl + kColO + 128 * ob + 32 * c, r);
-              tmem_ld_wait();
-#pragma unroll
-              for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * f);
-              tmem_st_32cols(tl + kColO + 128 * ob + 32 * c, r);
-            }
-            tmem_st_wait();
-          }
-          if (need) {
-            l = (m_used == -INFINITY) ? 0.f : l * exp2f(m_used - mt);
-            m_used = mt;
-          }
-          const float nm = -(m_used == -INFINITY ? 0.f : m_used);
-          // P over this copy's 32 keys as bf16 hi + lo pairs
-          uint32_t hv[16], lv[16];
-          float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float a = exp2f(fmaf(x[2 * i], scale, nm));
-            const float c2 = exp2f(fmaf(x[2 * i + 1], scale, nm));
-            ls[i & 3] += a + c2;
-            hv[i] = pack_bf16x2(a, c2);
-            lv[i] = pack_bf16x2(a - bf16_lo(hv[i]), c2 - bf16_hi(hv[i]));
-          }
-          l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-          // P[pb] is free once the P V product that last read it has completed
-          if (pcnt[pb] > 0 && !(ok = mbar_wait(p_empty + 8 * pb, (pcnt[pb] - 1) & 1, p.status))) break;
-          tc_fence_after_sync();
-          tmem_st_16cols(tl + kColP + 64 * pb + 16 * copy, hv);
-          tmem_st_16cols(tl + kColP + 64 * pb + 32 + 16 * copy, lv);
-          tmem_st_wait();
-          tc_fence_before_sync();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(p_full + 8 * pb);
-          ++pcnt[pb];
-          pb ^= 1;
-        }
-        if (!ok) break;
-        // hand (m, l) of this copy to the epilogue warps
-        if (!(ok = mbar_wait(ml_empty + 8 * mlr.idx, mlr.phase ^ 1u, p.status))) break;
-        s_ml[(mlr.idx * 2 + copy) * 64 + row] = make_float2(m_used, l);
         __syncwarp();
-        if (lane == 0) mbar_arrive(ml_full + 8 * mlr.idx);
-        mlr.next(2);
-        ob ^= 1;
+        if (lane == 0) mbar_arrive(s_empty + 8 * sr.idx);
+        sr.next(kSBufs);
+        const int nvalid = tile_keys(it, t, p.bs);
+        const bool valid = key < nvalid;
+        const int live_cols = valid ? min(CW, p.rows - CW * hc) : 0;  // query rows this key scores
+        if (t == 0) {
+          // the running max of each row: the maximum over the item's first tile
+#pragma unroll
+          for (int j = 0; j < CW; ++j) d[j] = j < live_cols ? d[j] * scale : -INFINITY;
+          float* red = s_red + (hc * 2 + static_cast<int>(rph)) * 128;
+#pragma unroll
+          for (int j = 0; j < CW; ++j) m[j] = warp_max_redux(d[j]);
+          if (lane == 0) {
+#pragma unroll
+            for (int j4 = 0; j4 < CW / 4; ++j4)
+              reinterpret_cast<float4*>(red + 32 * qd)[j4] =
+                  make_float4(m[4 * j4], m[4 * j4 + 1], m[4 * j4 + 2], m[4 * j4 + 3]);
+            mbar_arrive(rbar);
+          }
+          if (!(ok = mbar_wait(rbar, rph, p.status))) break;
+          rph ^= 1u;
+#pragma unroll
+          for (int j4 = 0; j4 < CW / 4; ++j4) {
+            const float4 a0 = reinterpret_cast<const float4*>(red)[j4];
+            const float4 a1 = reinterpret_cast<const float4*>(red + 32)[j4];
+            const float4 a2 = reinterpret_cast<const float4*>(red + 64)[j4];
+            const float4 a3 = reinterpret_cast<const float4*>(red + 96)[j4];
+            m[4 * j4] = fmax3(fmax3(a0.x, a1.x, a2.x), a3.x, -INFINITY);
+            m[4 * j4 + 1] = fmax3(fmax3(a0.y, a1.y, a2.y), a3.y, -INFINITY);
+            m[4 * j4 + 2] = fmax3(fmax3(a0.z, a1.z, a2.z), a3.z, -INFINITY);
+            m[4 * j4 + 3] = fmax3(fmax3(a0.w, a1.w, a2.w), a3.w, -INFINITY);
+          }
+#pragma unroll
+          for (int j = 0; j < CW; ++j) {
+            d[j] = j < live_cols ? d[j] - m[j] : -INFINITY;
+            l[j] = 0.f;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < CW; ++j) d[j] = j < live_cols ? fmaf(d[j], scale, -m[j]) : -INFINITY;
+          dmax = fmaxf(dmax, array_max<CW>(d));
+        }
+        // P^T of this key: bf16 hi (truncated) and lo (the truncated rest);
+        // hi + lo is within 2^-14 of P, below it
+        uint32_t hv[CW / 2], lv[CW / 2];
+#pragma unroll
+        for (int i = 0; i < CW / 2; ++i) {
+          const float a = ex2_approx(d[2 * i]);
+          const float c2 = ex2_approx(d[2 * i + 1]);
+          l[2 * i] += a;
+          l[2 * i + 1] += c2;
+          const uint32_t ua = __float_as_uint(a), uc = __float_as_uint(c2);
+          hv[i] = __byte_perm(ua, uc, 0x7632);
+          lv[i] = __byte_perm(__float_as_uint(a - __uint_as_float(ua & 0xFFFF0000u)),
+                              __float_as_uint(c2 - __uint_as_float(uc & 0xFFFF0000u)), 0x7632);
+        }
+        // the O^T product reads V rows up to the next multiple of 16 keys: zero
+        // the rows past the end of the data, whatever the tile holds there
+        const bool zero_row = !valid && key < ((nvalid + 15) & ~15);
+        if (__any_sync(0xffffffffu, zero_row)) {
+          if (!(ok = mbar_wait(v_full + 8 * vr.idx, vr.phase, p.status))) break;
+          if (zero_row && hc == 0) {
+            const uint32_t vst = base + lay.off_v + vr.idx * kHalfBytes;
+            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              st_shared_v4(vst + key * 128 + 16 * c, z);
+              st_shared_v4(vst + kBoxBytes + key * 128 + 16 * c, z);
+            }
+          }
+        }
+        vr.next(NV);
+        if (pcnt[pb] > 0 && !(ok = mbar_wait(p_empty + 8 * pb, (pcnt[pb] - 1) & 1, p.status))) break;
+        const uint32_t ph = base + lay.off_p + pb * C::kPBytes + prow;
+#pragma unroll
+        for (int c = 0; c < CW / 8; ++c) {
+          const int chi = (CW / 8) * hc + c;            // chunk of the hi values in the row
+          const int clo = NC == 32 ? 4 + chi : chi;     // NC = 32: lo in the same row
+          const uint32_t lo_base = NC == 32 ? 0u : C::kPLoOffset;
+          st_shared_v4(ph + 16 * (chi ^ (key & 7)), make_uint4(hv[4 * c], hv[4 * c + 1], hv[4 * c + 2], hv[4 * c + 3]));
+          st_shared_v4(ph + lo_base + 16 * (clo ^ (key & 7)),
+                       make_uint4(lv[4 * c], lv[4 * c + 1], lv[4 * c + 2], lv[4 * c + 3]));
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full + 8 * pb);
+        ++pcnt[pb];
+        pb ^= 1;
       }
+      if (!ok) break;
+      // a score beyond 2^64 above the running max: the combine kernel redoes
+      // this (sequence, KV head) exactly
+      if (__any_sync(0xffffffffu, dmax > kOverflowLog2) && lane == 0) atomicOr(p.counters + 1 + it.b * p.Hkv + it.g, 1);
+      // row sums over this warp's keys -> the epilogue; the quarter-0 warps also
+      // hand over the running max
+      if (!(ok = mbar_wait(ml_empty + 8 * mlr.idx, mlr.phase ^ 1u, p.status))) break;
+      if (qd == 0 && lane == 0) {
+#pragma unroll
+        for (int j4 = 0; j4 < CW / 4; ++j4)
+          reinterpret_cast<float4*>(s_m + mlr.idx * NC + CW * hc)[j4] =
+              make_float4(m[4 * j4], m[4 * j4 + 1], m[4 * j4 + 2], m[4 * j4 + 3]);
+      }
+      const float lsum = warp_reduce_scatter_sum<CW>(l, lane);   // lane i: column i % CW
+      if (lane < CW) s_l[(mlr.idx * 4 + qd) * NC + CW * hc + lane] = lsum;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ml_full + 8 * mlr.idx);
+      mlr.next(2);
     }
   } else {
-    // ------------------------------------------------ epilogue (warps 4-7)
-    const int e = warp - 4;
-    if ((e & 1) < nq) {
-      const int lg = 32 * e + lane;
-      const int row = lg % 64;
-      const int copy = lg / 64;
-      const uint32_t tl = tmem + (static_cast<uint32_t>(32 * e) << 16);
-      Ring orr, mlr, itr;
-      bool ok = true;
-      while (ok) {
-        const int w = next_item(it_full, it_empty, s_item, itr, p.status);
-        if (w < 0) break;
-        const Item it = decode_item(w, s_prefix, s_n, p);
-        if (!(ok = mbar_wait(o_full + 8 * orr.idx, orr.phase, p.status))) break;
-        tc_fence_after_sync();
-        float o[HD];
+    // ------------------------------------------------ epilogue
+    const int qd = warp & 3;
+    const int dim = 32 * qd + lane;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(32 * qd) << 16);
+    Ring orr, mlr, itr;
+    bool ok = true;
+    while (ok) {
+      const int w = next_item(it_full, it_empty, s_item, itr, p.status);
+      if (w < 0) break;
+      const Item it = decode_item(w, s_prefix, s_n, p);
+      if (!(ok = mbar_wait(o_full + 8 * orr.idx, orr.phase, p.status))) break;
+      tc_fence_after_sync();
+      float o[NC];  // O^T lane `dim`: the hi and lo column blocks added
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          tmem_ld_32cols(tl + kColO + 128 * orr.idx + 32 * c, r);
-          tmem_ld_wait();
+      for (int c = 0; c < NC / 32; ++c) {
+        uint32_t rh[32], rl[32];
+        tmem_ld_32cols(tl + C::kColO + 2 * NC * orr.idx + 32 * c, rh);
+        tmem_ld_32cols(tl + C::kColO + 2 * NC * orr.idx + NC + 32 * c, rl);
+        tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[32 * c + i] = __uint_as_float(r[i]);
+        for (int j = 0; j < 32; ++j) o[32 * c + j] = __uint_as_float(rh[j]) + __uint_as_float(rl[j]);
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(o_free + 8 * orr.idx);
+      orr.next(2);
+      if (!(ok = mbar_wait(ml_full + 8 * mlr.idx, mlr.phase, p.status))) break;
+      // lane i: the sum and its reciprocal for rows i and 32 + i
+      const float* lrow = s_l + mlr.idx * 4 * NC;
+      float den[NC / 32], inv[NC / 32];
+#pragma unroll
+      for (int c = 0; c < NC / 32; ++c) {
+        const int r = 32 * c + lane;
+        den[c] = lrow[r] + lrow[NC + r] + lrow[2 * NC + r] + lrow[3 * NC + r];
+        inv[c] = r < p.rows ? 1.f / den[c] : 0.f;
+      }
+      if (it.nsplit == 1) {
+        const size_t row0 = (static_cast<size_t>(it.b) * p.Hq + it.g * p.G) * p.bs;
+#pragma unroll
+        for (int r = 0; r < NC; ++r) {
+          const float iv = __shfl_sync(0xffffffffu, inv[r / 32], r % 32);
+          if (r < p.rows) p.out[(row0 + r) * HD + dim] = __float2bfloat16_rn(o[r] * iv);
         }
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(o_free + 8 * orr.idx);
-        orr.next(2);
-        if (!(ok = mbar_wait(ml_full + 8 * mlr.idx, mlr.phase, p.status))) break;
-        const float2 mine = s_ml[(mlr.idx * 2 + copy) * 64 + row];
-        const float2 other = s_ml[(mlr.idx * 2 + (copy ^ 1)) * 64 + row];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(ml_empty + 8 * mlr.idx);
-        mlr.next(2);
-        // merge the two copies' partial softmax states (log-sum-exp)
-        const float M = fmaxf(mine.x, other.x);
-        const float Mu = M == -INFINITY ? 0.f : M;
-        const float fm = mine.x == -INFINITY ? 0.f : exp2f(mine.x - Mu);
-        const float fo = other.x == -INFINITY ? 0.f : exp2f(other.x - Mu);
-        if (copy == 1) {
-          float4* xr = reinterpret_cast<float4*>(s_x + row * HD);
+      } else {
+        const size_t r0 = ((static_cast<size_t>(it.b) * p.Hkv + it.g) * p.max_splits + it.s) * p.rows;
 #pragma unroll
-          for (int i = 0; i < HD / 4; ++i)
-            xr[i] = make_float4(o[4 * i] * fm, o[4 * i + 1] * fm, o[4 * i + 2] * fm, o[4 * i + 3] * fm);
+        for (int r = 0; r < NC; ++r) {
+          const float iv = __shfl_sync(0xffffffffu, inv[r / 32], r % 32);
+          if (r < p.rows) p.opart[(r0 + r) * HD + dim] = o[r] * iv;
         }
-        named_barrier_sync(1, 32 * n_sm);
-        if (copy == 0) {
-          const float4* xr = reinterpret_cast<const float4*>(s_x + row * HD);
+        if (qd == 0) {
 #pragma unroll
-          for (int i = 0; i < HD / 4; ++i) {
-            const float4 v = xr[i];
-            o[4 * i] = o[4 * i] * fm + v.x;
-            o[4 * i + 1] = o[4 * i + 1] * fm + v.y;
-            o[4 * i + 2] = o[4 * i + 2] * fm + v.z;
-            o[4 * i + 3] = o[4 * i + 3] * fm + v.w;
+          for (int c = 0; c < NC / 32; ++c) {
+            const int r = 32 * c + lane;
+            if (r < p.rows) p.mlpart[r0 + r] = make_float2(s_m[mlr.idx * NC + r], den[c]);
           }
         }
-        named_barrier_sync(1, 32 * n_sm);  // s_x is free for the next item
-        if (copy == 0) finish_item(it, p, row, o, M, mine.y * fm + other.y * fo);
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ml_empty + 8 * mlr.idx);
+      mlr.next(2);
     }
   }
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == C::kSWarp) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(tmem, C::kTmemCols);
   }
 }
 
@@ -800,7 +944,7 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const float* __restrict__
 int pick_chunk(int B, int Hkv, int cap, int window) {
   const long keys = window > 0 ? std::min(window, cap) : cap;
   long c = (static_cast<long>(B) * Hkv * keys) / 3600;
-  c = (c + 63) / 64 * 64;
+  c = (c + kKeys - 1) / kKeys * kKeys;
   return static_cast<int>(std::min<long>(4096, std::max<long>(256, c)));
 }
 
@@ -817,7 +961,7 @@ size_t attn_ws_bytes(int B, int bs, int Hq, int Hkv, int cap, int window, dflash
   if (dt == DFLASH_BF16)
     s += align256(static_cast<size_t>(B) * Hkv * max_splits * rows * HD * sizeof(float)) +
          align256(static_cast<size_t>(B) * Hkv * max_splits * rows * sizeof(float2)) +
-         align256(sizeof(int));
+         align256((1 + static_cast<size_t>(B) * Hkv) * sizeof(int));
   return s + 256;
 }
 
@@ -868,37 +1012,33 @@ dflash_status launch_block_attn(int layer, int B, int bs, int Hq, const void* q,
   p.out = static_cast<__nv_bfloat16*>(out);
   p.opart = w.take<float>(static_cast<size_t>(B) * Hkv * p.max_splits * p.rows * HD);
   p.mlpart = w.take<float2>(static_cast<size_t>(B) * Hkv * p.max_splits * p.rows);
-  p.counters = w.take<int>(1);
+  p.counters = w.take<int>(1 + static_cast<size_t>(B) * Hkv);
+  p.ck = static_cast<const __nv_bfloat16*>(c.k);
+  p.cv = static_cast<const __nv_bfloat16*>(c.v);
   p.scale_log2 = 1.4426950408889634f * scale;
   p.status = dev.status;
 
+  const int nc = p.rows > 32 ? 64 : 32;   // query rows padded to the MMA's N
   AttnMaps maps;
   const uint64_t rows = static_cast<uint64_t>(c.num_layers) * c.batch * Hkv * c.capacity;
-  dflash_status s = make_tmap_bf16_2d(&maps.k, c.k, rows, HD, kTile, 64);
-  if (!s) s = make_tmap_bf16_2d(&maps.v, c.v, rows, HD, kTile, 64);
-  if (!s) s = make_tmap_bf16_2d(&maps.q, qh, static_cast<uint64_t>(B) * Hq * bs, HD, p.rows > 32 ? 64 : 32, 64);
-  if (!s) s = make_tmap_bf16_2d(&maps.kb, kbh, static_cast<uint64_t>(B) * Hkv * bs, HD, kTile, 64);
-  if (!s) s = make_tmap_bf16_2d(&maps.vb, vb, static_cast<uint64_t>(B) * Hkv * bs, HD, kTile, 64);
+  dflash_status s = make_tmap_bf16_2d(&maps.k, c.k, rows, HD, kKeys, 64);
+  if (!s) s = make_tmap_bf16_2d(&maps.v, c.v, rows, HD, kKeys, 64);
+  if (!s) s = make_tmap_bf16_2d(&maps.q, qh, static_cast<uint64_t>(B) * Hq * bs, HD, nc, 64);
+  if (!s) s = make_tmap_bf16_2d(&maps.kb, kbh, static_cast<uint64_t>(B) * Hkv * bs, HD, kBlockBoxRows, 64);
+  if (!s) s = make_tmap_bf16_2d(&maps.vb, vb, static_cast<uint64_t>(B) * Hkv * bs, HD, kBlockBoxRows, 64);
   if (s) return s;
 
   attn_prologue_kernel<__nv_bfloat16><<<B * bs, 256, 0, st>>>(
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(kb),
       static_cast<const __nv_bfloat16*>(qg), static_cast<const __nv_bfloat16*>(kg), c.seq_len, B, bs, Hq, Hkv,
-      c.capacity, eps, inv, qh, kbh, p.counters, 1, dev.status);
+      c.capacity, eps, inv, qh, kbh, p.counters, 1 + B * Hkv, dev.status);
 
-  const TcLayout lay = tc_layout(p.rows, B, static_cast<int>(dev.max_smem_optin));
-  if (lay.stages < 2) return fail(DFLASH_ERR_UNSUPPORTED, "block_attn: shared memory");
-  static int configured_device = -1;
-  if (configured_device != dev.device) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(dev.max_smem_optin));
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attn_tc_kernel)");
-    configured_device = dev.device;
-  }
+  const TcLayout lay = tc_layout(nc, B, static_cast<int>(dev.max_smem_optin));
+  if (lay.nk < 1 || lay.nv < 1 || lay.bytes > static_cast<int>(dev.max_smem_optin))
+    return fail(DFLASH_ERR_UNSUPPORTED, "block_attn: shared memory");
   const long upper = static_cast<long>(B) * Hkv * p.max_splits;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(std::min<long>(upper, dev.num_sms)));
-  cfg.blockDim = dim3(kTcThreads);
   cfg.dynamicSmemBytes = static_cast<size_t>(lay.bytes);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -906,9 +1046,30 @@ dflash_status launch_block_attn(int layer, int B, int bs, int Hq, const void* q,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t le = cudaLaunchKernelEx(&cfg, attn_tc_kernel, maps, p, lay);
+  cudaError_t le;
+  if (nc == 32) {
+    static int configured = -1;
+    if (configured != dev.device) {
+      le = cudaFuncSetAttribute(attn_tc_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(dev.max_smem_optin));
+      if (le != cudaSuccess) return cuda_fail(le, "cudaFuncSetAttribute(attn_tc_kernel)");
+      configured = dev.device;
+    }
+    cfg.blockDim = dim3(TcCfg<32>::kThreads);
+    le = cudaLaunchKernelEx(&cfg, attn_tc_kernel<32>, maps, p, lay);
+  } else {
+    static int configured = -1;
+    if (configured != dev.device) {
+      le = cudaFuncSetAttribute(attn_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(dev.max_smem_optin));
+      if (le != cudaSuccess) return cuda_fail(le, "cudaFuncSetAttribute(attn_tc_kernel)");
+      configured = dev.device;
+    }
+    cfg.blockDim = dim3(TcCfg<64>::kThreads);
+    le = cudaLaunchKernelEx(&cfg, attn_tc_kernel<64>, maps, p, lay);
+  }
   if (le != cudaSuccess) return cuda_fail(le, "attn_tc_kernel launch");
-  if (p.max_splits > 1) {
+  {  // always: it also redoes flagged (sequence, KV head) pairs
     cudaLaunchConfig_t cc = cfg;
     const long warps = static_cast<long>(B) * Hkv * p.rows;
     cc.gridDim = dim3(static_cast<unsigned>((warps + 7) / 8));

@@ -243,11 +243,28 @@ __device__ __forceinline__ uint64_t umma_desc_mnmajor_sw128(uint32_t addr, uint3
   return d;
 }
 
-// Instruction descriptor: kind::f16, A = B = bf16, D = fp32; A K-major, B
-// K-major (b_mn_major = false) or MN-major (true).
-__host__ __device__ constexpr uint32_t umma_idesc_bf16(int m, int n, bool b_mn_major = false) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn_major ? (1u << 16) : 0u) |
-         (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+// Shared-memory matrix descriptor for an MN-major bf16 operand with swizzle
+// `mode` (2: 128-byte, 4: 64-byte, 6: 32-byte): each K row holds the swizzle
+// width of contiguous MN elements, 8-row K groups are `sbo` bytes apart and
+// MN blocks of the swizzle width `lbo` bytes apart.  `addr` must be aligned to
+// the 8-row group.
+__device__ __forceinline__ uint64_t umma_desc_mnmajor(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t mode) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(mode & 7u) << 61;
+  return d;
+}
+
+// Instruction descriptor: kind::f16, A = B = bf16, D = fp32; B K-major
+// (b_mn_major = false) or MN-major (true), A likewise.
+__host__ __device__ constexpr uint32_t umma_idesc_bf16(int m, int n, bool b_mn_major = false,
+                                                       bool a_mn_major = false) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (a_mn_major ? (1u << 15) : 0u) |
+         (b_mn_major ? (1u << 16) : 0u) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(m >> 4) << 24);
 }
 
 // 32 lanes x 16 columns of 32-bit accumulators (thread i: lane_base + i).
@@ -330,6 +347,18 @@ __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t& r0, u
                : "r"(addr));
 }
 
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// 2^x by the hardware approximation (ex2.approx.ftz.f32); 2^-inf = 0.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
@@ -360,6 +389,26 @@ __device__ __forceinline__ float from_f32<float>(float v) { return v; }
 template <>
 __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
   return __float2bfloat16_rn(v);
+}
+
+// Four consecutive bf16 values (8-byte aligned) as floats.
+__device__ __forceinline__ float4 bf16x4_to_f32(const __nv_bfloat16* src) {
+  const uint2 u = *reinterpret_cast<const uint2*>(src);
+  return make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
+}
+
+// Maximum over the 32 lanes of the warp (all lanes active).
+__device__ __forceinline__ float warp_max_redux(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
 }
 
 __device__ __forceinline__ float warp_sum(float v) {

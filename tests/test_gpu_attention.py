@@ -1,7 +1,7 @@
 """GPU parity of dflash_block_attn against the oracle.
 
 Relative Frobenius error of the output <= 2e-3 (bf16) / 1e-5 (fp32), on small
-cases spanning several 64-key tiles, several key splits and a ragged tail, and
+cases spanning several 128-key tiles, several key splits and a ragged tail, and
 on sampled sequences of the full-size workloads in the launch configuration
 the benchmark uses.
 """
@@ -44,6 +44,45 @@ def test_block_attn_bf16_small(bs, window):
     cache = dfl.KVCache(k.to(DEV), v.to(DEV), torch.tensor(seq, dtype=torch.int32, device=DEV))
     out = dfl.block_attn(1, q.to(DEV), kb.to(DEV), vb.to(DEV), qg.to(DEV), kg.to(DEV), cache, window=window)
     ref = _oracle(q, kb, vb, qg, kg, k[1], v[1], seq, window, torch.bfloat16)
+    err = rel_fro(out, ref)
+    assert err <= TOL[torch.bfloat16], (err, max_abs(out, ref))
+
+
+@pytest.mark.parametrize("bs", [8, 16])
+def test_block_attn_never_reads_past_seq_len(bs):
+    """Cache rows at and past seq_len (and the other layer) hold NaN: the output
+    must not see them, for lengths on, just before and just after tile edges."""
+    seq = [0, 1, 127, 128, 129, 255, 256, 700, 1000]
+    cap = 1024
+    k, v, q, kb, vb, qg, kg = _inputs(len(seq), bs, cap, torch.bfloat16, seed=40 + bs)
+    kn, vn = k.clone(), v.clone()
+    for b, n in enumerate(seq):
+        kn[:, b, :, n:] = float("nan")
+        vn[:, b, :, n:] = float("nan")
+    kn[0] = float("nan")
+    vn[0] = float("nan")
+    cache = dfl.KVCache(kn.to(DEV), vn.to(DEV), torch.tensor(seq, dtype=torch.int32, device=DEV))
+    out = dfl.block_attn(1, q.to(DEV), kb.to(DEV), vb.to(DEV), qg.to(DEV), kg.to(DEV), cache)
+    assert torch.isfinite(out.float()).all()
+    ref = _oracle(q, kb, vb, qg, kg, k[1], v[1], seq, 0, torch.bfloat16)
+    err = rel_fro(out, ref)
+    assert err <= TOL[torch.bfloat16], (err, max_abs(out, ref))
+
+
+def test_block_attn_scores_far_above_the_first_tile_stay_exact():
+    """A key scoring ~2^290 above the first tile's maximum, late in a
+    three-split sequence, in a single-split sequence and (not flagged) in a
+    first tile: the outputs still match the oracle."""
+    seq = [700, 200, 300]
+    cap = 1024
+    k, v, q, kb, vb, qg, kg = _inputs(3, 8, cap, torch.bfloat16, seed=77, layers=1)
+    g = torch.Generator().manual_seed(78)
+    for b, pos, head in [(0, 650, 3), (1, 150, 5), (2, 10, 1)]:
+        k[0, b, head, pos] = (200.0 * torch.randn(128, generator=g)).to(torch.bfloat16)
+    cache = dfl.KVCache(k.to(DEV), v.to(DEV), torch.tensor(seq, dtype=torch.int32, device=DEV))
+    out = dfl.block_attn(0, q.to(DEV), kb.to(DEV), vb.to(DEV), qg.to(DEV), kg.to(DEV), cache)
+    assert torch.isfinite(out.float()).all()
+    ref = _oracle(q, kb, vb, qg, kg, k[0], v[0], seq, 0, torch.bfloat16)
     err = rel_fro(out, ref)
     assert err <= TOL[torch.bfloat16], (err, max_abs(out, ref))
 
