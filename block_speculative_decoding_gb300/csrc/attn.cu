@@ -941,9 +941,13 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const float* __restrict__
 }
 
 
+// Keys per split: aims at ~1200 work items for a full cache (about eight per
+// SM).  Longer splits amortise each split's partial output (written, then
+// merged by the combine kernel) and its pipeline ramp; enough items remain for
+// the dynamic queue to balance the SMs.
 int pick_chunk(int B, int Hkv, int cap, int window) {
   const long keys = window > 0 ? std::min(window, cap) : cap;
-  long c = (static_cast<long>(B) * Hkv * keys) / 3600;
+  long c = (static_cast<long>(B) * Hkv * keys) / 1200;
   c = (c + kKeys - 1) / kKeys * kKeys;
   return static_cast<int>(std::min<long>(4096, std::max<long>(256, c)));
 }
