@@ -12,14 +12,18 @@
 //                  sequence) is cut into 16384-logit chunks; each CTA streams
 //                  one chunk with 16-byte loads and writes (max, sum 2^x) of
 //                  x = logit * log2(e)/T, or (max, first argmax) when T == 0.
-//   2. decide   -- one warp per sequence merges the chunk partials into
-//                  log-normalisers, evaluates alpha_k = min(1, p(x)/q(x)) from
-//                  two single-logit loads per row, draws the Philox uniforms and
-//                  finds the first rejection n.  Greedy ends here.
-//   3. residual -- for row n only (the correction row, or the bonus row):
-//                  per-chunk masses of max(0, p - q) and of p.
-//   4. select   -- one CTA per sequence: inverse-CDF search for the first
-//                  index whose cumulative mass exceeds v * S.
+//   2. decide   -- (T == 0) one warp per sequence: the target argmax of every
+//                  row against the draft tokens.
+//   2. finish   -- (T > 0) one CTA per (sequence, chunk), launched as a
+//                  programmatic dependent of the stats pass.  Its first warp
+//                  merges the sequence's chunk partials into log-normalisers,
+//                  evaluates alpha_k = min(1, p(x)/q(x)) from two single-logit
+//                  loads per row, draws the Philox uniforms and finds the first
+//                  rejection n (every CTA of the sequence takes the same
+//                  decision).  The CTA then sums max(0, p - q) (the bonus row:
+//                  p) over its chunk of row n; the last CTA of the sequence to
+//                  finish (an atomic count) runs the inverse-CDF search for the
+//                  first index whose cumulative mass exceeds v * S.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -67,37 +71,6 @@ struct Vec<T, 1> {
   static __device__ __forceinline__ void unpack(const type& v, float* f) { f[0] = to_f32<T>(v); }
 };
 
-// Load this thread's 64 logits of chunk [e0, e1): vector i of thread t covers
-// elements e0 + (i*256 + t)*VEC ...  Out-of-range elements become -inf.
-template <typename T, int VEC>
-__device__ __forceinline__ void load_chunk(const T* __restrict__ row, int e0, int e1,
-                                           float (&f)[kPerThread]) {
-  using VT = typename Vec<T, VEC>::type;
-  constexpr int NV = kPerThread / VEC;
-  VT v[NV];
-#pragma unroll
-  for (int i = 0; i < NV; ++i) {
-    const int e = e0 + (i * kThreads + threadIdx.x) * VEC;
-    if (e < e1) v[i] = __ldcs(reinterpret_cast<const VT*>(row + e));
-  }
-#pragma unroll
-  for (int i = 0; i < NV; ++i) {
-    const int e = e0 + (i * kThreads + threadIdx.x) * VEC;
-    if (e < e1) {
-      Vec<T, VEC>::unpack(v[i], f + i * VEC);
-    } else {
-#pragma unroll
-      for (int j = 0; j < VEC; ++j) f[i * VEC + j] = -INFINITY;
-    }
-  }
-}
-
-template <int VEC>
-__device__ __forceinline__ int elem_index(int e0, int slot) {
-  const int i = slot / VEC, j = slot % VEC;
-  return e0 + (i * kThreads + threadIdx.x) * VEC + j;
-}
-
 // (m, s) represents s * 2^m; merges tolerate empty (-inf) sides.
 __device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
   if (m2 == -INFINITY) return;
@@ -118,31 +91,58 @@ __device__ __forceinline__ void amax_merge(float& v, int& i, float v2, int i2) {
   }
 }
 
+// Raw 16-byte vectors of this thread's 64 logits of chunk [e0, e1): vector i
+// covers elements e0 + (i*256 + t)*VEC ...; `live` marks in-range vectors.
+template <typename T, int VEC>
+__device__ __forceinline__ void load_raw(const T* __restrict__ row, int e0, int e1,
+                                         typename Vec<T, VEC>::type (&v)[kPerThread / VEC], bool (&live)[kPerThread / VEC]) {
+  using VT = typename Vec<T, VEC>::type;
+#pragma unroll
+  for (int i = 0; i < kPerThread / VEC; ++i) {
+    const int e = e0 + (i * kThreads + threadIdx.x) * VEC;
+    live[i] = e < e1;
+    if (live[i]) v[i] = __ldcs(reinterpret_cast<const VT*>(row + e));
+  }
+}
+
+// The stats pass zeroes the per-sequence counters of the finish kernel.
 template <typename T, int VEC, bool GREEDY>
-__global__ void __launch_bounds__(kThreads) verify_stats_kernel(const T* __restrict__ lt,
-                                                                const T* __restrict__ ld, int B,
-                                                                int bs, int V, int nchunk,
-                                                                float scale,
-                                                                float2* __restrict__ part) {
+__global__ void __launch_bounds__(kThreads, 4) verify_stats_kernel(const T* __restrict__ lt,
+                                                                   const T* __restrict__ ld, int B,
+                                                                   int bs, int V, int nchunk,
+                                                                   float scale,
+                                                                   float2* __restrict__ part,
+                                                                   int* __restrict__ counters) {
+  pdl_launch_dependents();
+  if (blockIdx.x == 0 && counters)
+    for (int i = threadIdx.x; i < B; i += kThreads) counters[i] = 0;
   const int c = blockIdx.x % nchunk;
   const int r = blockIdx.x / nchunk;
   const T* row = (r < B * bs) ? lt + static_cast<size_t>(r) * V
                               : ld + static_cast<size_t>(r - B * bs) * V;
   const int e0 = c * kChunk;
   const int e1 = min(V, e0 + kChunk);
-  float f[kPerThread];
-  load_chunk<T, VEC>(row, e0, e1, f);
+  constexpr int NV = kPerThread / VEC;
+  typename Vec<T, VEC>::type v[NV];
+  bool live[NV];
+  load_raw<T, VEC>(row, e0, e1, v, live);
 
   float a, b;  // GREEDY: (value, index-as-bits); else (max, sum)
   if constexpr (GREEDY) {
     float bv = -INFINITY;
     int bi = INT_MAX;
 #pragma unroll
-    for (int s = 0; s < kPerThread; ++s) {  // slots visit this thread's logits in index order
-      const int e = elem_index<VEC>(e0, s);
-      if (e < e1 && (bi == INT_MAX || f[s] > bv)) {
-        bv = f[s];
-        bi = e;
+    for (int i = 0; i < NV; ++i) {  // slots visit this thread's logits in index order
+      if (!live[i]) continue;
+      float f[VEC];
+      Vec<T, VEC>::unpack(v[i], f);
+#pragma unroll
+      for (int j = 0; j < VEC; ++j) {
+        const int e = e0 + (i * kThreads + threadIdx.x) * VEC + j;
+        if (bi == INT_MAX || f[j] > bv) {
+          bv = f[j];
+          bi = e;
+        }
       }
     }
 #pragma unroll
@@ -154,16 +154,26 @@ __global__ void __launch_bounds__(kThreads) verify_stats_kernel(const T* __restr
     a = bv;
     b = __int_as_float(bi);
   } else {
-    float m = -INFINITY;
+    float mx = -INFINITY;
 #pragma unroll
-    for (int s = 0; s < kPerThread; ++s) {
-      f[s] *= scale;
-      m = fmaxf(m, f[s]);
+    for (int i = 0; i < NV; ++i) {
+      if (!live[i]) continue;
+      float f[VEC];
+      Vec<T, VEC>::unpack(v[i], f);
+#pragma unroll
+      for (int j = 0; j < VEC; ++j) mx = fmaxf(mx, f[j]);
     }
+    float m = mx * scale;  // scale > 0
     float sum = 0.f;
-    if (m != -INFINITY) {
+    if (mx != -INFINITY) {
 #pragma unroll
-      for (int s = 0; s < kPerThread; ++s) sum += exp2f(f[s] - m);
+      for (int i = 0; i < NV; ++i) {
+        if (!live[i]) continue;
+        float f[VEC];
+        Vec<T, VEC>::unpack(v[i], f);
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) sum += ex2_approx(fmaf(f[j], scale, -m));
+      }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -222,15 +232,20 @@ __device__ __forceinline__ float2 merge_row(const float2* __restrict__ part, int
   return make_float2(a, b);
 }
 
+// The decision for sequence b, taken by one warp (lane k: block position k):
+// log-normalisers of the rows, the acceptance test of every draft, the first
+// rejection n.  Every lane returns the same Decision.  With `acc` / `out` it
+// also writes the accepted length and the tokens: the accepted drafts, -1 after
+// row n, and at row n the target argmax (greedy) or nothing (the correction is
+// drawn later).
 template <typename T, bool GREEDY>
-__global__ void __launch_bounds__(128) verify_decide_kernel(
-    const T* __restrict__ lt, const T* __restrict__ ld, const int32_t* __restrict__ x, int B, int bs,
-    int V, int nchunk, float scale, const float2* __restrict__ part, uint32_t k0, uint32_t k1,
-    uint32_t c_lo, uint32_t c_hi, int32_t* __restrict__ acc, int32_t* __restrict__ out,
-    Decision* __restrict__ dec, unsigned* status) {
+__device__ __forceinline__ Decision decide_seq(const T* __restrict__ lt, const T* __restrict__ ld,
+                                               const int32_t* __restrict__ x, int b, int B, int bs, int V,
+                                               int nchunk, float scale, const float2* __restrict__ part,
+                                               uint32_t k0, uint32_t k1, uint32_t c_lo, uint32_t c_hi,
+                                               int32_t* __restrict__ acc, int32_t* __restrict__ out,
+                                               unsigned* status) {
   const int lane = threadIdx.x % 32;
-  const int b = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
-  if (b >= B) return;
   const int R_t = B * bs;
   float lzp = 0.f, lzq = 0.f;
   int amax = 0;
@@ -258,7 +273,7 @@ __global__ void __launch_bounds__(128) verify_decide_kernel(
     vbits = w.y;
     if (lane < bs - 1) {
       if (xk < 0 || xk >= V) {
-        raise_status(status, DFLASH_DEV_BAD_TOKEN);
+        if (out) raise_status(status, DFLASH_DEV_BAD_TOKEN);
         rejected = true;
       } else if constexpr (GREEDY) {
         rejected = (amax != xk);
@@ -273,26 +288,24 @@ __global__ void __launch_bounds__(128) verify_decide_kernel(
   const unsigned mask = __ballot_sync(0xffffffffu, rejected);
   const int n = mask ? (__ffs(mask) - 1) : (bs - 1);
   const int amax_n = __shfl_sync(0xffffffffu, amax, n);
-  const uint32_t vbits_n = __shfl_sync(0xffffffffu, vbits, n);
-  const float lzp_n = __shfl_sync(0xffffffffu, lzp, n);
-  const float lzq_n = __shfl_sync(0xffffffffu, lzq, n);
-  if (lane < bs) {
-    int v = -1;
-    if (lane < n) v = xk;
-    else if (lane == n && GREEDY) v = amax_n;
-    out[b * bs + lane] = v;
-  }
-  if (lane == 0) {
-    acc[b] = n;
-    if constexpr (!GREEDY) {
-      Decision d;
-      d.n = n;
-      d.vbits = vbits_n;
-      d.lzp = lzp_n;
-      d.lzq = lzq_n;
-      dec[b] = d;
-    }
-  }
+  Decision d;
+  d.n = n;
+  d.vbits = __shfl_sync(0xffffffffu, vbits, n);
+  d.lzp = __shfl_sync(0xffffffffu, lzp, n);
+  d.lzq = __shfl_sync(0xffffffffu, lzq, n);
+  if (out && lane < bs && (GREEDY || lane != n)) out[b * bs + lane] = lane < n ? xk : (lane == n ? amax_n : -1);
+  if (acc && lane == 0) acc[b] = n;
+  return d;
+}
+
+// Greedy decoding: one warp per sequence.
+template <typename T>
+__global__ void __launch_bounds__(128) verify_decide_kernel(
+    const T* __restrict__ lt, const int32_t* __restrict__ x, int B, int bs, int V, int nchunk,
+    const float2* __restrict__ part, int32_t* __restrict__ acc, int32_t* __restrict__ out, unsigned* status) {
+  const int b = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  if (b >= B) return;
+  decide_seq<T, true>(lt, lt, x, b, B, bs, V, nchunk, 1.f, part, 0u, 0u, 0u, 0u, acc, out, status);
 }
 
 // Residual weight of one logit pair (or of p alone for the bonus row).
@@ -304,74 +317,70 @@ __device__ __forceinline__ float resid_weight(float xt, float xd, const Decision
   return fmaxf(0.f, pw - qw);
 }
 
+// Non-greedy verification after the stats pass; see the file comment.
 template <typename T, int VEC>
-__global__ void __launch_bounds__(kThreads) verify_residual_kernel(
-    const T* __restrict__ lt, const T* __restrict__ ld, int B, int bs, int V, int nchunk,
-    float scale, const Decision* __restrict__ dec, float2* __restrict__ rpart) {
-  const int c = blockIdx.x % nchunk, b = blockIdx.x / nchunk;
-  const Decision d = dec[b];
-  const bool has_q = d.n < bs - 1;
-  const T* prow = lt + static_cast<size_t>(b * bs + d.n) * V;
-  const int e0 = c * kChunk, e1 = min(V, e0 + kChunk);
-  float ft[kPerThread], fd[kPerThread];
-  load_chunk<T, VEC>(prow, e0, e1, ft);
-  if (has_q) {
-    load_chunk<T, VEC>(ld + static_cast<size_t>(b * (bs - 1) + d.n) * V, e0, e1, fd);
+__global__ void __launch_bounds__(kThreads) verify_finish_kernel(
+    const T* __restrict__ lt, const T* __restrict__ ld, const int32_t* __restrict__ x, int B, int bs, int V,
+    int nchunk, float scale, const float2* __restrict__ part, uint32_t k0, uint32_t k1, uint32_t c_lo,
+    uint32_t c_hi, int32_t* __restrict__ acc, int32_t* __restrict__ out, float2* __restrict__ rpart,
+    int* __restrict__ counters, unsigned* status) {
+  pdl_wait_primary();  // the stats pass's partials and cleared counters
+  const int b = blockIdx.x / nchunk, c = blockIdx.x % nchunk;
+  __shared__ Decision s_dec;
+  __shared__ int s_is_last;
+  if (threadIdx.x < 32) {
+    const Decision dw = decide_seq<T, false>(lt, ld, x, b, B, bs, V, nchunk, scale, part, k0, k1, c_lo, c_hi,
+                                             c == 0 ? acc : nullptr, c == 0 ? out : nullptr, status);
+    if (threadIdx.x == 0) s_dec = dw;
   }
-  float sr = 0.f, sp = 0.f;
-#pragma unroll
-  for (int s = 0; s < kPerThread; ++s) {
-    if (ft[s] == -INFINITY) continue;  // out of range (or a -inf logit: zero mass)
-    float pw;
-    const float r = resid_weight(ft[s] * scale, has_q ? fd[s] * scale : 0.f, d, has_q, pw);
-    sr += r;
-    sp += pw;
-  }
-  sr = warp_sum(sr);
-  sp = warp_sum(sp);
-  __shared__ float2 red[kThreads / 32];
-  if (threadIdx.x % 32 == 0) red[threadIdx.x / 32] = make_float2(sr, sp);
   __syncthreads();
-  if (threadIdx.x == 0) {
-    float2 a = red[0];
-    for (int w = 1; w < kThreads / 32; ++w) {
-      a.x += red[w].x;
-      a.y += red[w].y;
-    }
-    rpart[static_cast<size_t>(b) * nchunk + c] = a;
-  }
-}
-
-// This thread's contiguous segment [s0, s0 + 64) of a row, with 16-byte vector
-// loads where possible; elements at or beyond s1 become -inf.
-template <typename T, int VEC>
-__device__ __forceinline__ void load_segment(const T* __restrict__ row, int s0, int s1,
-                                             float (&f)[kPerThread]) {
-  using VT = typename Vec<T, VEC>::type;
-  constexpr int NV = kPerThread / VEC;
-  VT v[NV];
-#pragma unroll
-  for (int i = 0; i < NV; ++i)
-    if (s0 + i * VEC < s1) v[i] = *reinterpret_cast<const VT*>(row + s0 + i * VEC);
-#pragma unroll
-  for (int i = 0; i < NV; ++i) {
-    if (s0 + i * VEC < s1) {
-      Vec<T, VEC>::unpack(v[i], f + i * VEC);
-    } else {
-#pragma unroll
-      for (int j = 0; j < VEC; ++j) f[i * VEC + j] = -INFINITY;
-    }
-  }
-}
-
-template <typename T, int VEC>
-__global__ void __launch_bounds__(kThreads) verify_select_kernel(
-    const T* __restrict__ lt, const T* __restrict__ ld, int B, int bs, int V, int nchunk,
-    float scale, const Decision* __restrict__ dec, const float2* __restrict__ rpart,
-    int32_t* __restrict__ out) {
-  const int b = blockIdx.x;
-  const Decision d = dec[b];
+  const Decision d = s_dec;
   const bool has_q = d.n < bs - 1;
+  {
+    // masses of max(0, p - q) and of p over this chunk of row n
+    constexpr int NV = kPerThread / VEC;
+    const T* prow = lt + static_cast<size_t>(b * bs + d.n) * V;
+    const int e0 = c * kChunk, e1 = min(V, e0 + kChunk);
+    typename Vec<T, VEC>::type vt[NV], vq[NV];
+    bool live[NV];
+    load_raw<T, VEC>(prow, e0, e1, vt, live);
+    if (has_q) load_raw<T, VEC>(ld + static_cast<size_t>(b * (bs - 1) + d.n) * V, e0, e1, vq, live);
+    float sr = 0.f, sp = 0.f;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      if (!live[i]) continue;
+      float ft[VEC], fq[VEC];
+      Vec<T, VEC>::unpack(vt[i], ft);
+      if (has_q) Vec<T, VEC>::unpack(vq[i], fq);
+#pragma unroll
+      for (int j = 0; j < VEC; ++j) {
+        if (ft[j] == -INFINITY) continue;  // a -inf logit: zero mass
+        float pw;
+        const float r = resid_weight(ft[j] * scale, has_q ? fq[j] * scale : 0.f, d, has_q, pw);
+        sr += r;
+        sp += pw;
+      }
+    }
+    sr = warp_sum(sr);
+    sp = warp_sum(sp);
+    __shared__ float2 red[kThreads / 32];
+    if (threadIdx.x % 32 == 0) red[threadIdx.x / 32] = make_float2(sr, sp);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float2 a = red[0];
+      for (int w = 1; w < kThreads / 32; ++w) {
+        a.x += red[w].x;
+        a.y += red[w].y;
+      }
+      rpart[static_cast<size_t>(b) * nchunk + c] = a;
+      __threadfence();
+      s_is_last = atomicAdd(counters + b, 1) == nchunk - 1;
+    }
+    __syncthreads();
+  }
+  if (!s_is_last) return;
+  __threadfence();
+  // the last CTA of the sequence: inverse-CDF search over row n
   __shared__ int s_chunk;
   __shared__ int s_use_p;
   __shared__ float s_target;
@@ -381,17 +390,18 @@ __global__ void __launch_bounds__(kThreads) verify_select_kernel(
   if (threadIdx.x == 0) {
     const float2* rp = rpart + static_cast<size_t>(b) * nchunk;
     float sr = 0.f;
-    for (int c = 0; c < nchunk; ++c) sr += rp[c].x;
+    for (int c = 0; c < nchunk; ++c) sr += __ldcg(&rp[c]).x;
     const int use_p = !(sr > 0.f);
     float S = 0.f;
-    for (int c = 0; c < nchunk; ++c) S += use_p ? rp[c].y : rp[c].x;
+    for (int c = 0; c < nchunk; ++c) S += use_p ? __ldcg(&rp[c]).y : __ldcg(&rp[c]).x;
     const float t = uniform24(d.vbits) * S;
     float cum = 0.f;
     int cs = -1;
     float excl = 0.f;
     int last_pos = 0;
     for (int c = 0; c < nchunk; ++c) {
-      const float w = use_p ? rp[c].y : rp[c].x;
+      const float2 rc = __ldcg(&rp[c]);
+      const float w = use_p ? rc.y : rc.x;
       if (w > 0.f) last_pos = c;
       if (cs < 0 && cum + w > t) {
         cs = c;
@@ -402,7 +412,7 @@ __global__ void __launch_bounds__(kThreads) verify_select_kernel(
     if (cs < 0) {  // rounding left the threshold at the very end
       cs = last_pos;
       excl = 0.f;
-      for (int c = 0; c < cs; ++c) excl += use_p ? rp[c].y : rp[c].x;
+      for (int c = 0; c < cs; ++c) excl += use_p ? __ldcg(&rp[c]).y : __ldcg(&rp[c]).x;
     }
     s_chunk = cs;
     s_use_p = use_p;
@@ -420,18 +430,34 @@ __global__ void __launch_bounds__(kThreads) verify_select_kernel(
   const int s0 = e0 + threadIdx.x * kPerThread;
   const int s1 = min(e1, s0 + kPerThread);
   float w[kPerThread];
-  load_segment<T, VEC>(prow, s0, s1, w);
-  if (has_q && !use_p) {
-    float fq[kPerThread];
-    load_segment<T, VEC>(qrow, s0, s1, fq);
+  {
+    constexpr int NV = kPerThread / VEC;
+    using VT = typename Vec<T, VEC>::type;
+    VT vp[NV], vq[NV];
+    const bool with_q = has_q && !use_p;
 #pragma unroll
-    for (int i = 0; i < kPerThread; ++i) {
-      float pw;
-      w[i] = w[i] == -INFINITY ? 0.f : resid_weight(w[i] * scale, fq[i] * scale, d, true, pw);
+    for (int i = 0; i < NV; ++i) {
+      if (s0 + i * VEC < s1) {
+        vp[i] = *reinterpret_cast<const VT*>(prow + s0 + i * VEC);
+        if (with_q) vq[i] = *reinterpret_cast<const VT*>(qrow + s0 + i * VEC);
+      }
     }
-  } else {
 #pragma unroll
-    for (int i = 0; i < kPerThread; ++i) w[i] = w[i] == -INFINITY ? 0.f : exp2f(w[i] * scale - d.lzp);
+    for (int i = 0; i < NV; ++i) {
+      float fp[VEC], fq[VEC];
+      const bool in = s0 + i * VEC < s1;
+      if (in) {
+        Vec<T, VEC>::unpack(vp[i], fp);
+        if (with_q) Vec<T, VEC>::unpack(vq[i], fq);
+      }
+#pragma unroll
+      for (int j = 0; j < VEC; ++j) {
+        float pw;
+        w[i * VEC + j] = (!in || fp[j] == -INFINITY) ? 0.f
+                         : with_q ? resid_weight(fp[j] * scale, fq[j] * scale, d, true, pw)
+                                  : exp2f(fp[j] * scale - d.lzp);
+      }
+    }
   }
   float seg = 0.f;
   int last_pos = -1;
@@ -488,23 +514,30 @@ dflash_status run(const T* lt, const T* ld, const int32_t* x, int B, int bs, int
   const int R = greedy ? B * bs : B * bs + B * (bs - 1);
   WsCarver w(ws);
   float2* part = w.take<float2>(static_cast<size_t>(2 * B * bs) * nchunk);
-  Decision* dec = w.take<Decision>(B);
   float2* rpart = w.take<float2>(static_cast<size_t>(B) * nchunk);
+  int* counters = w.take<int>(B);
   const float scale = greedy ? 1.f : kLog2e / Temp;
   const uint32_t k0 = static_cast<uint32_t>(seed), k1 = static_cast<uint32_t>(seed >> 32);
   const uint32_t c0 = static_cast<uint32_t>(cycle), c1 = static_cast<uint32_t>(cycle >> 32);
   const unsigned g1 = static_cast<unsigned>(nchunk) * static_cast<unsigned>(R);
   if (greedy) {
-    verify_stats_kernel<T, VEC, true><<<g1, kThreads, 0, st>>>(lt, ld, B, bs, V, nchunk, scale, part);
-    verify_decide_kernel<T, true><<<(B + 3) / 4, 128, 0, st>>>(
-        lt, ld, x, B, bs, V, nchunk, scale, part, k0, k1, c0, c1, acc, out, dec, dev.status);
+    verify_stats_kernel<T, VEC, true><<<g1, kThreads, 0, st>>>(lt, ld, B, bs, V, nchunk, scale, part, nullptr);
+    verify_decide_kernel<T><<<(B + 3) / 4, 128, 0, st>>>(lt, x, B, bs, V, nchunk, part, acc, out, dev.status);
   } else {
-    verify_stats_kernel<T, VEC, false><<<g1, kThreads, 0, st>>>(lt, ld, B, bs, V, nchunk, scale, part);
-    verify_decide_kernel<T, false><<<(B + 3) / 4, 128, 0, st>>>(
-        lt, ld, x, B, bs, V, nchunk, scale, part, k0, k1, c0, c1, acc, out, dec, dev.status);
-    verify_residual_kernel<T, VEC><<<static_cast<unsigned>(nchunk) * B, kThreads, 0, st>>>(lt, ld, B, bs, V, nchunk,
-                                                                          scale, dec, rpart);
-    verify_select_kernel<T, VEC><<<B, kThreads, 0, st>>>(lt, ld, B, bs, V, nchunk, scale, dec, rpart, out);
+    verify_stats_kernel<T, VEC, false><<<g1, kThreads, 0, st>>>(lt, ld, B, bs, V, nchunk, scale, part, counters);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(nchunk) * static_cast<unsigned>(B));
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t le = cudaLaunchKernelEx(&cfg, verify_finish_kernel<T, VEC>, lt, ld, x, B, bs, V, nchunk, scale,
+                                        static_cast<const float2*>(part), k0, k1, c0, c1, acc, out, rpart, counters,
+                                        dev.status);
+    if (le != cudaSuccess) return cuda_fail(le, "verify_finish_kernel launch");
   }
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? DFLASH_OK : cuda_fail(e, "verify kernel launch");
@@ -515,8 +548,8 @@ dflash_status run(const T* lt, const T* ld, const int32_t* x, int B, int bs, int
 size_t verify_ws_bytes(int B, int bs, int V) {
   const size_t nchunk = (static_cast<size_t>(V) + kChunk - 1) / kChunk;
   return align256(2 * static_cast<size_t>(B) * bs * nchunk * sizeof(float2)) +
-         align256(static_cast<size_t>(B) * sizeof(Decision)) +
-         align256(static_cast<size_t>(B) * nchunk * sizeof(float2)) + 256;
+         align256(static_cast<size_t>(B) * nchunk * sizeof(float2)) +
+         align256(static_cast<size_t>(B) * sizeof(int)) + 256;
 }
 
 dflash_status launch_verify(const void* lt, const void* ld, dflash_dtype dt, const int32_t* x, int B,
