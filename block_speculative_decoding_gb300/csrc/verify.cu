@@ -244,29 +244,25 @@ __device__ __forceinline__ Decision decide_seq(const T* __restrict__ lt, const T
                                                int nchunk, float scale, const float2* __restrict__ part,
                                                uint32_t k0, uint32_t k1, uint32_t c_lo, uint32_t c_hi,
                                                int32_t* __restrict__ acc, int32_t* __restrict__ out,
-                                               unsigned* status) {
+                                               unsigned* status, const float* s_lz = nullptr) {
   const int lane = threadIdx.x % 32;
-  const int R_t = B * bs;
+  int xk = -1;
+  if (lane < bs - 1) xk = x[b * (bs - 1) + lane];
   float lzp = 0.f, lzq = 0.f;
   int amax = 0;
-  for (int k = 0; k < bs; ++k) {
-    const float2 pt = merge_row<GREEDY>(part + static_cast<size_t>(b * bs + k) * nchunk, nchunk);
-    if constexpr (GREEDY) {
-      int i = __float_as_int(pt.y);
+  if constexpr (GREEDY) {
+    for (int k = 0; k < bs; ++k) {
+      const float2 pt = merge_row<true>(part + static_cast<size_t>(b * bs + k) * nchunk, nchunk);
+      const int i = __float_as_int(pt.y);
       if (lane == k) amax = (i == INT_MAX) ? 0 : i;
-    } else {
-      if (lane == k) lzp = pt.x + log2f(pt.y);
-      if (k < bs - 1) {
-        const float2 pq = merge_row<false>(
-            part + static_cast<size_t>(R_t + b * (bs - 1) + k) * nchunk, nchunk);
-        if (lane == k) lzq = pq.x + log2f(pq.y);
-      }
     }
+  } else {
+    // normalisers precomputed by the block (row_normalisers)
+    if (lane < bs) lzp = s_lz[lane];
+    if (lane < bs - 1) lzq = s_lz[bs + lane];
   }
   bool rejected = false;
   uint32_t vbits = 0;
-  int xk = -1;
-  if (lane < bs - 1) xk = x[b * (bs - 1) + lane];
   if (lane < bs) {
     uint4 w = make_uint4(0u, 0u, 0u, 0u);
     if constexpr (!GREEDY) w = philox4x32_10(make_uint4(lane, b, c_lo, c_hi), k0, k1);
@@ -317,6 +313,20 @@ __device__ __forceinline__ float resid_weight(float xt, float xd, const Decision
   return fmaxf(0.f, pw - qw);
 }
 
+// log2 normaliser of every row of sequence b (target rows 0..bs-1, then the
+// draft rows), from the chunk partials: the warps of the block take the rows in
+// turn, each loading all its partials before merging them.
+__device__ __forceinline__ void row_normalisers(const float2* __restrict__ part, int b, int B, int bs, int nchunk,
+                                                float* s_lz) {
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int nrows = 2 * bs - 1;
+  for (int r = warp; r < nrows; r += kThreads / 32) {
+    const size_t prow = r < bs ? static_cast<size_t>(b * bs + r) : static_cast<size_t>(B * bs + b * (bs - 1) + r - bs);
+    const float2 st = merge_row<false>(part + prow * nchunk, nchunk);
+    if (lane == 0) s_lz[r] = st.x + log2f(st.y);
+  }
+}
+
 // Non-greedy verification after the stats pass; see the file comment.
 template <typename T, int VEC>
 __global__ void __launch_bounds__(kThreads) verify_finish_kernel(
@@ -328,9 +338,12 @@ __global__ void __launch_bounds__(kThreads) verify_finish_kernel(
   const int b = blockIdx.x / nchunk, c = blockIdx.x % nchunk;
   __shared__ Decision s_dec;
   __shared__ int s_is_last;
+  __shared__ float s_lz[32];
+  row_normalisers(part, b, B, bs, nchunk, s_lz);
+  __syncthreads();
   if (threadIdx.x < 32) {
     const Decision dw = decide_seq<T, false>(lt, ld, x, b, B, bs, V, nchunk, scale, part, k0, k1, c_lo, c_hi,
-                                             c == 0 ? acc : nullptr, c == 0 ? out : nullptr, status);
+                                             c == 0 ? acc : nullptr, c == 0 ? out : nullptr, status, s_lz);
     if (threadIdx.x == 0) s_dec = dw;
   }
   __syncthreads();
