@@ -8,18 +8,22 @@
 // multiplication); "DFlash & DFlash2: Block-Diffusion LLM-Speedup" 4.1
 // (H_t = RMSNorm(W_c [H^(l1); ...; H^(l5)]), K_i = W_i^K H_t, V_i = W_i^V H_t).
 //
-// bf16 path, three launches after a small row-map kernel:
-//   1. gemm_tc (fusion)  Y = [taps] W_c^T on tcgen05 tensor cores: TMA loads of
+// bf16 path, three launches chained as programmatic dependents:
+//   1. gemm_tc (fusion)  Y = [taps] W_c^T on tcgen05 tensor cores: a unit is
+//      MT x 128 rows by 128 columns of Y over a range of K blocks; TMA loads
 //      128x64 A tiles (taken from the tap that owns the K block -- the concat is
-//      never materialised) and BNx64 W_c tiles into a 4-stage ring, one thread
-//      issues tcgen05.mma (M=128, N=BN, K=16) into a double-buffered TMEM
-//      accumulator, four epilogue warps drain it.  Small M uses split-K; the
-//      fp32 partial sums stay in the workspace.
-//   2. rmsnorm           H_t = bf16(sum_splits(Y) * rsqrt(mean(Y^2) + eps) * g)
-//   3. gemm_tc (K/V)     [K|V] = H_t W_kv^T with a fused epilogue: every
-//      128-column head of a K projection is RMS-normalised (gain k_gain[l]) and
-//      rotated at its cache position, V heads are copied, and both are stored
-//      as bf16 rows of the cache.
+//      never materialised) and the 128x64 W_c tile into a ring, one thread
+//      issues tcgen05.mma (M=128, N=128, K=16) into MT accumulators in tensor
+//      memory, four epilogue warps drain them.  A few new rows (M <= 256) take
+//      MT = 2, so each W_c tile is read once, and split K over ~one unit per
+//      SM; the fp32 partial sums stay in the workspace.
+//   2. rownorm           row -> (sequence, cache position) and its RoPE table
+//      (before waiting for the GEMM), then H_t = bf16(sum_splits(Y) *
+//      rsqrt(mean(Y^2) + eps) * g)
+//   3. gemm_tc (K/V)     [K|V] = H_t W_kv^T, one head (128 columns) per unit, with
+//      a fused epilogue: a K head is RMS-normalised (gain k_gain[l]) and rotated
+//      at its cache position, a V head copied, both stored as bf16 cache rows.
+//      Its producer loads the first W_kv tiles before waiting for H_t.
 // fp32 path: the same steps as plain SIMT kernels (parity path).
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -40,7 +44,7 @@ constexpr int kBK = 64;
 constexpr int kGemmThreads = 192;  // warp 0: TMA producer, warp 1: MMA issuer, warps 2-5: epilogue
 constexpr int kMaxSeg = 8;
 constexpr double kTwoPi = 6.283185307179586476925286766559;
-constexpr int kSplitTarget = 148;  // work units aimed for when splitting K
+constexpr int kSplitTarget = 152;  // work units aimed for when splitting K (one per SM)
 
 struct InvFreq {
   double v[HD / 2];
@@ -53,6 +57,7 @@ struct TmapPack {
 struct GemmArgs {
   int M, N, num_kb, kb_per_seg, k_splits, m_tiles, n_tiles;
   int epi;                 // 0: fp32 partial store, 1: K/V cache epilogue
+  int pdl;                 // launched as a programmatic dependent: A comes from the previous kernel
   float* out_f32;          // epi 0: [k_splits][M][N]
   __nv_bfloat16* cache_k;  // epi 1
   __nv_bfloat16* cache_v;
@@ -64,14 +69,22 @@ struct GemmArgs {
   unsigned* status;
 };
 
-template <int BN>
+// A unit is MT x 128 rows by BN columns (over a range of K blocks); its MT
+// accumulators of BN fp32 columns sit side by side in tensor memory, twice
+// over (double-buffered) when that fits the 512 columns.
+template <int BN, int MT>
 __host__ __device__ constexpr int stage_bytes() {
-  return kBM * kBK * 2 + BN * kBK * 2;
+  return MT * kBM * kBK * 2 + BN * kBK * 2;
 }
 
-template <int BN, int STAGES>
+template <int BN, int MT>
+__host__ __device__ constexpr int num_acc() {
+  return 2 * MT * BN <= 512 ? 2 : 1;
+}
+
+template <int BN, int STAGES, int MT>
 constexpr size_t gemm_smem_bytes() {
-  return 1024 + static_cast<size_t>(STAGES) * stage_bytes<BN>() + 8 * (2 * STAGES + 4) + 16;
+  return 1024 + static_cast<size_t>(STAGES) * stage_bytes<BN, MT>() + 8 * (2 * STAGES + 4) + 16;
 }
 
 __device__ __forceinline__ void unit_coords(int u, const GemmArgs& p, int& m, int& n, int& kb0, int& kb1,
@@ -164,12 +177,14 @@ __device__ __forceinline__ void kv_head_epilogue(uint32_t taddr, int col0, int r
   }
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int MT>
 __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_constant__ TmapPack amaps,
                                                                   const __grid_constant__ CUtensorMap bmap,
                                                                   const GemmArgs p) {
-  constexpr int A_BYTES = kBM * kBK * 2;
-  constexpr int STAGE = stage_bytes<BN>();
+  constexpr int A_BYTES = kBM * kBK * 2;   // one 128-row A box
+  constexpr int STAGE = stage_bytes<BN, MT>();
+  constexpr int NACC = num_acc<BN, MT>();
+  constexpr int ACC_COLS = MT * BN;
   constexpr uint32_t IDESC = umma_idesc_bf16(kBM, BN);
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -195,12 +210,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
     mbar_fence_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), 2 * BN);
+    tmem_alloc(smem_u32(tmem_slot), NACC * ACC_COLS);
     tmem_relinquish();
   }
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
+  pdl_launch_dependents();
   const uint32_t tmem_base = *tmem_slot;
   const int total = p.m_tiles * p.n_tiles * p.k_splits;
 
@@ -209,6 +225,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
       for (int s = 0; s < kMaxSeg; ++s)
         if (s * p.kb_per_seg < p.num_kb) tma_prefetch_desc(&amaps.a[s]);
       tma_prefetch_desc(&bmap);
+      // The B operand (weights) does not depend on the previous kernel: as a
+      // programmatic dependent, fill the ring's B halves first, then wait.
+      int pre = 0;
+      if (p.pdl && blockIdx.x < total) {
+        int m, n, kb0, kb1, ks;
+        unit_coords(blockIdx.x, p, m, n, kb0, kb1, ks);
+        for (; pre < STAGES && kb0 + pre < kb1; ++pre) {
+          const uint32_t fb = full0 + 8 * pre;
+          mbar_arrive_expect_tx(fb, STAGE);
+          tma_load_2d(base + pre * STAGE + MT * A_BYTES, &bmap, fb, (kb0 + pre) * kBK, n * BN);
+        }
+      }
+      pdl_wait_primary();
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -216,13 +245,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
         int m, n, kb0, kb1, ks;
         unit_coords(u, p, m, n, kb0, kb1, ks);
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!(ok = mbar_wait(empty0 + 8 * stage, phase ^ 1u, p.status))) break;
+          const bool b_done = u == static_cast<int>(blockIdx.x) && kb - kb0 < pre;
+          if (!b_done && !(ok = mbar_wait(empty0 + 8 * stage, phase ^ 1u, p.status))) break;
           const uint32_t fb = full0 + 8 * stage;
-          mbar_arrive_expect_tx(fb, STAGE);
+          if (!b_done) mbar_arrive_expect_tx(fb, STAGE);
           const uint32_t sa = base + stage * STAGE;
           const int seg = kb / p.kb_per_seg;
-          tma_load_2d(sa, &amaps.a[seg], fb, (kb - seg * p.kb_per_seg) * kBK, m * kBM);
-          tma_load_2d(sa + A_BYTES, &bmap, fb, kb * kBK, n * BN);
+#pragma unroll
+          for (int i = 0; i < MT; ++i)
+            tma_load_2d(sa + i * A_BYTES, &amaps.a[seg], fb, (kb - seg * p.kb_per_seg) * kBK, (m * MT + i) * kBM);
+          if (!b_done) tma_load_2d(sa + MT * A_BYTES, &bmap, fb, kb * kBK, n * BN);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -242,16 +274,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
         unit_coords(u, p, m, n, kb0, kb1, ks);
         if (!(ok = mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1u, p.status))) break;
         tc_fence_after_sync();
-        const uint32_t d_tmem = tmem_base + acc * BN;
+        const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!(ok = mbar_wait(full0 + 8 * stage, phase, p.status))) break;
           tc_fence_after_sync();
           const uint32_t sa = base + stage * STAGE;
-          const uint64_t ad = umma_desc_kmajor_sw128(sa);
-          const uint64_t bd = umma_desc_kmajor_sw128(sa + A_BYTES);
+          const uint64_t bd = umma_desc_kmajor_sw128(sa + MT * A_BYTES);
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k)
-            umma_bf16(d_tmem, ad + 2 * k, bd + 2 * k, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
+          for (int i = 0; i < MT; ++i) {
+            const uint64_t ad = umma_desc_kmajor_sw128(sa + i * A_BYTES);
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k)
+              umma_bf16(d_tmem + i * BN, ad + 2 * k, bd + 2 * k, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
+          }
           umma_commit(empty0 + 8 * stage);
           if (++stage == STAGES) {
             stage = 0;
@@ -259,7 +294,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
           }
         }
         umma_commit(tfull0 + 8 * acc);
-        if (++acc == 2) {
+        if (++acc == NACC) {
           acc = 0;
           acc_phase ^= 1u;
         }
@@ -274,31 +309,34 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
       unit_coords(u, p, m, n, kb0, kb1, ks);
       if (!mbar_wait(tfull0 + 8 * acc, acc_phase, p.status)) break;
       tc_fence_after_sync();
-      const int row = m * kBM + q * 32 + lane;
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-      if (p.epi == 0) {
-        float* dst = p.out_f32 + (static_cast<size_t>(ks) * p.M + row) * p.N + n * BN;
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld_32cols(taddr + c * 32, r);
-          tmem_ld_wait();
-          if (row < p.M) {
-            float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+      for (int i = 0; i < MT; ++i) {
+        const int row = (m * MT + i) * kBM + q * 32 + lane;
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * ACC_COLS + i * BN;
+        if (p.epi == 0) {
+          float* dst = p.out_f32 + (static_cast<size_t>(ks) * p.M + row) * p.N + n * BN;
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld_32cols(taddr + c * 32, r);
+            tmem_ld_wait();
+            if (row < p.M) {
+              float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              d4[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
-                                  __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+              for (int j = 0; j < 8; ++j)
+                d4[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                    __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+            }
           }
-        }
-      } else {
+        } else {
 #pragma unroll 1
-        for (int hh = 0; hh < BN / HD; ++hh) kv_head_epilogue(taddr + hh * HD, n * BN + hh * HD, row, p);
+          for (int hh = 0; hh < BN / HD; ++hh) kv_head_epilogue(taddr + hh * HD, n * BN + hh * HD, row, p);
+        }
       }
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
-      if (++acc == 2) {
+      if (++acc == NACC) {
         acc = 0;
         acc_phase ^= 1u;
       }
@@ -308,69 +346,118 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
   __syncthreads();
   if (warp == 1) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem_base, 2 * BN);
+    tmem_dealloc(tmem_base, NACC * ACC_COLS);
   }
 }
 
-// Row -> (sequence, cache position) and the RoPE (cos, sin) table of each row.
-__global__ void __launch_bounds__(64) fuse_rowmap_kernel(const int32_t* __restrict__ cu_new,
-                                                         const int32_t* __restrict__ seq_len, int B,
-                                                         int cap, InvFreq inv, int2* __restrict__ rowinfo,
-                                                         float2* __restrict__ rope_cs, unsigned* status) {
-  const int m = blockIdx.x;
-  int lo = 0, hi = B - 1;
-  while (lo < hi) {  // largest b with cu_new[b] <= m
-    const int mid = (lo + hi + 1) >> 1;
-    if (cu_new[mid] <= m) lo = mid; else hi = mid - 1;
-  }
-  const int b = lo;
-  const int t = m - cu_new[b];
-  const int nnew = cu_new[b + 1] - cu_new[b];
-  const int n = seq_len[b];
-  const bool seq_ok = n >= 0 && n <= cap;
-  const bool valid = seq_ok && n + nnew <= cap && t >= 0 && t < nnew;
-  const int pos = valid ? n + t : 0;
-  if (threadIdx.x < HD / 2) {
-    double ang = static_cast<double>(pos) * inv.v[threadIdx.x];
-    ang -= kTwoPi * rint(ang / kTwoPi);
-    float sv, cv;
-    sincosf(static_cast<float>(ang), &sv, &cv);
-    rope_cs[static_cast<size_t>(m) * (HD / 2) + threadIdx.x] = make_float2(cv, sv);
-  }
-  if (threadIdx.x == 0) {
-    rowinfo[m] = valid ? make_int2(b, pos) : make_int2(-1, -1);
-    if (!valid) raise_status(status, seq_ok ? DFLASH_DEV_CAPACITY : DFLASH_DEV_BAD_SEQLEN);
-  }
-}
+// One CTA per new row m:
+//   * row -> (sequence, cache position) and the RoPE (cos, sin) table of the row
+//     (used by the K/V epilogue);
+//   * H_t[m] = the sum of the split-K partials of Y[m], RMS-normalised with
+//     gain g, stored as TH (workspace copy for the K/V GEMM) and optionally as
+//     the caller's copy.  Each thread keeps its float4 slots of the row in
+//     registers (rows up to 4096 wide), so the partials are read once.
+constexpr int kNormThreads = 256;
+constexpr int kNormSlots = 4;  // float4 slots per thread
 
-// H_t = sum of split-K partials, RMS-normalised with gain g; stored as TH
-// (workspace copy for the next GEMM) and optionally as TO (caller's copy).
 template <typename TG, typename TH>
-__global__ void __launch_bounds__(256) fuse_rmsnorm_kernel(const float* __restrict__ part, int k_splits,
-                                                           int M, int D, const TG* __restrict__ g,
-                                                           float eps, TH* __restrict__ ht,
-                                                           TH* __restrict__ ht_out) {
+__global__ void __launch_bounds__(kNormThreads) fuse_rownorm_kernel(
+    const float* __restrict__ part, int k_splits, int M, int D, const TG* __restrict__ g, float eps,
+    TH* __restrict__ ht, TH* __restrict__ ht_out, const int32_t* __restrict__ cu_new,
+    const int32_t* __restrict__ seq_len, int B, int cap, InvFreq inv, int2* __restrict__ rowinfo,
+    float2* __restrict__ rope_cs, unsigned* status) {
   const int m = blockIdx.x;
+  if (threadIdx.x <= HD / 2) {
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {  // largest b with cu_new[b] <= m
+      const int mid = (lo + hi + 1) >> 1;
+      if (cu_new[mid] <= m) lo = mid; else hi = mid - 1;
+    }
+    const int b = lo;
+    const int t = m - cu_new[b];
+    const int nnew = cu_new[b + 1] - cu_new[b];
+    const int n = seq_len[b];
+    const bool seq_ok = n >= 0 && n <= cap;
+    const bool valid = seq_ok && n + nnew <= cap && t >= 0 && t < nnew;
+    const int pos = valid ? n + t : 0;
+    if (threadIdx.x < HD / 2) {
+      double ang = static_cast<double>(pos) * inv.v[threadIdx.x];
+      ang -= kTwoPi * rint(ang / kTwoPi);
+      float sv, cv;
+      sincosf(static_cast<float>(ang), &sv, &cv);
+      rope_cs[static_cast<size_t>(m) * (HD / 2) + threadIdx.x] = make_float2(cv, sv);
+    } else {
+      rowinfo[m] = valid ? make_int2(b, pos) : make_int2(-1, -1);
+      if (!valid) raise_status(status, seq_ok ? DFLASH_DEV_CAPACITY : DFLASH_DEV_BAD_SEQLEN);
+    }
+  }
+  pdl_launch_dependents();
+  pdl_wait_primary();  // the partials of the fusion GEMM
+  const int nv = D / 4;  // float4 slots of the row
+  const float4* prow = reinterpret_cast<const float4*>(part + static_cast<size_t>(m) * D);
+  const size_t split_stride = static_cast<size_t>(M) * D / 4;
+  auto row_sum = [&](int v) {
+    float4 t4 = prow[v];
+    for (int s = 1; s < k_splits; ++s) {
+      const float4 t = prow[s * split_stride + v];
+      t4.x += t.x;
+      t4.y += t.y;
+      t4.z += t.z;
+      t4.w += t.w;
+    }
+    return t4;
+  };
+  const bool in_regs = nv <= kNormThreads * kNormSlots;
+  float4 y[kNormSlots];
   float ss = 0.f;
-  for (int e = threadIdx.x; e < D; e += 256) {
-    float y = 0.f;
-    for (int s = 0; s < k_splits; ++s) y += part[(static_cast<size_t>(s) * M + m) * D + e];
-    ss += y * y;
+#pragma unroll
+  for (int i = 0; i < kNormSlots; ++i) {
+    const int v = threadIdx.x + i * kNormThreads;
+    y[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (in_regs && v < nv) y[i] = row_sum(v);
+    ss += y[i].x * y[i].x + y[i].y * y[i].y + y[i].z * y[i].z + y[i].w * y[i].w;
+  }
+  if (!in_regs) {
+    for (int v = threadIdx.x; v < nv; v += kNormThreads) {
+      const float4 t4 = row_sum(v);
+      ss += t4.x * t4.x + t4.y * t4.y + t4.z * t4.z + t4.w * t4.w;
+    }
   }
   ss = warp_sum(ss);
-  __shared__ float red[8];
+  __shared__ float red[kNormThreads / 32];
   if (threadIdx.x % 32 == 0) red[threadIdx.x / 32] = ss;
   __syncthreads();
   float tot = 0.f;
-  for (int w = 0; w < 8; ++w) tot += red[w];
+#pragma unroll
+  for (int w = 0; w < kNormThreads / 32; ++w) tot += red[w];
   const float r = rsqrtf(tot / static_cast<float>(D) + eps);
-  for (int e = threadIdx.x; e < D; e += 256) {
-    float y = 0.f;
-    for (int s = 0; s < k_splits; ++s) y += part[(static_cast<size_t>(s) * M + m) * D + e];
-    const float gv = g ? to_f32<TG>(g[e]) : 1.f;
-    const TH h = from_f32<TH>(y * r * gv);
-    ht[static_cast<size_t>(m) * D + e] = h;
-    if (ht_out) ht_out[static_cast<size_t>(m) * D + e] = h;
+  auto store = [&](int v, float4 t4) {
+    const int e = 4 * v;
+    const float g0 = g ? to_f32<TG>(g[e]) : 1.f, g1 = g ? to_f32<TG>(g[e + 1]) : 1.f;
+    const float g2 = g ? to_f32<TG>(g[e + 2]) : 1.f, g3 = g ? to_f32<TG>(g[e + 3]) : 1.f;
+    const TH h0 = from_f32<TH>(t4.x * r * g0), h1 = from_f32<TH>(t4.y * r * g1);
+    const TH h2 = from_f32<TH>(t4.z * r * g2), h3 = from_f32<TH>(t4.w * r * g3);
+    TH* d = ht + static_cast<size_t>(m) * D + e;
+    d[0] = h0;
+    d[1] = h1;
+    d[2] = h2;
+    d[3] = h3;
+    if (ht_out) {
+      TH* o = ht_out + static_cast<size_t>(m) * D + e;
+      o[0] = h0;
+      o[1] = h1;
+      o[2] = h2;
+      o[3] = h3;
+    }
+  };
+  if (in_regs) {
+#pragma unroll
+    for (int i = 0; i < kNormSlots; ++i) {
+      const int v = threadIdx.x + i * kNormThreads;
+      if (v < nv) store(v, y[i]);
+    }
+  } else {
+    for (int v = threadIdx.x; v < nv; v += kNormThreads) store(v, row_sum(v));
   }
 }
 
@@ -453,38 +540,51 @@ __global__ void __launch_bounds__(256) kv_store_f32_kernel(const float* __restri
 
 // ------------------------------------------------------------- planning -----
 
+// Fusion GEMM: 128-column units; a few new rows (M <= 256) take 256-row units
+// (the W_c tile of a unit is read once) split along K to about one unit per SM;
+// prefill-sized M takes 128-row units.  K/V GEMM: 128-row units of one head (enough units to
+// fill the SMs at M = 256).
 struct FusePlan {
-  int m_tiles, fuse_n_tiles, k_splits, kv_bn;
+  int fuse_mt, fuse_m_tiles, fuse_n_tiles, k_splits, kv_bn;
 };
 
 FusePlan plan(int M, int D, int Ntot) {
+  (void)Ntot;
   FusePlan f;
-  f.m_tiles = (M + kBM - 1) / kBM;
-  f.fuse_n_tiles = D / 256;
-  const int tiles = f.m_tiles * f.fuse_n_tiles;
+  f.fuse_mt = M <= 2 * kBM ? 2 : 1;
+  f.fuse_m_tiles = (M + f.fuse_mt * kBM - 1) / (f.fuse_mt * kBM);
+  f.fuse_n_tiles = D / 128;
+  const int tiles = f.fuse_m_tiles * f.fuse_n_tiles;
   f.k_splits = std::max(1, std::min(16, kSplitTarget / std::max(1, tiles)));
-  f.kv_bn = 256;  // two heads per tile; fewer, larger tiles beat a second wave at small M
+  f.kv_bn = 128;
   return f;
 }
 
-constexpr int kStagesBN256 = 4;
-constexpr int kStagesBN128 = 6;
-
-template <int BN, int STAGES>
+template <int BN, int STAGES, int MT>
 dflash_status launch_gemm(const TmapPack& am, const CUtensorMap& bm, const GemmArgs& a, cudaStream_t st,
                           const DeviceInfo& dev) {
-  const size_t smem = gemm_smem_bytes<BN, STAGES>();
+  const size_t smem = gemm_smem_bytes<BN, STAGES, MT>();
   if (smem > dev.max_smem_optin) return fail(DFLASH_ERR_UNSUPPORTED, "gemm_tc: shared memory");
   static int configured = -1;
   if (configured != dev.device) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, STAGES, MT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(gemm_tc_kernel)");
     configured = dev.device;
   }
   const int units = a.m_tiles * a.n_tiles * a.k_splits;
-  const int grid = std::min(units, dev.num_sms);
-  gemm_tc_kernel<BN, STAGES><<<grid, kGemmThreads, smem, st>>>(am, bm, a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(std::min(units, dev.num_sms)));
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.pdl ? 1 : 0;
+  cudaError_t le = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, STAGES, MT>, am, bm, a);
+  if (le != cudaSuccess) return cuda_fail(le, "gemm_tc_kernel launch");
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? DFLASH_OK : cuda_fail(e, "gemm_tc_kernel launch");
 }
@@ -520,7 +620,6 @@ dflash_status launch_fuse_context(int J, const void* const* taps, int dt_width, 
   WsCarver w(ws);
   int2* rowinfo = w.take<int2>(M);
   float2* rope_cs = w.take<float2>(static_cast<size_t>(M) * (HD / 2));
-  fuse_rowmap_kernel<<<M, 64, 0, st>>>(cu_new, c.seq_len, B, c.capacity, inv, rowinfo, rope_cs, dev.status);
 
   if (c.dtype == DFLASH_F32) {
     float* Y = w.take<float>(static_cast<size_t>(M) * D);
@@ -530,8 +629,9 @@ dflash_status launch_fuse_context(int J, const void* const* taps, int dt_width, 
     for (int j = 0; j < J; ++j) segs.a[j] = static_cast<const float*>(taps[j]);
     simt_gemm_f32_kernel<<<dim3((D + 63) / 64, (M + 63) / 64), 256, 0, st>>>(
         segs, dt_width, static_cast<const float*>(w_fuse), M, D, J * dt_width, Y);
-    fuse_rmsnorm_kernel<float, float><<<M, 256, 0, st>>>(Y, 1, M, D, static_cast<const float*>(g_fuse), eps, H,
-                                                         static_cast<float*>(h_t_out));
+    fuse_rownorm_kernel<float, float><<<M, kNormThreads, 0, st>>>(
+        Y, 1, M, D, static_cast<const float*>(g_fuse), eps, H, static_cast<float*>(h_t_out), cu_new, c.seq_len, B,
+        c.capacity, inv, rowinfo, rope_cs, dev.status);
     F32Segs hs{};
     hs.a[0] = H;
     simt_gemm_f32_kernel<<<dim3((Ntot + 63) / 64, (M + 63) / 64), 256, 0, st>>>(
@@ -545,6 +645,7 @@ dflash_status launch_fuse_context(int J, const void* const* taps, int dt_width, 
   }
 
   const FusePlan f = plan(M, D, Ntot);
+  if (D % 4 != 0) return fail(DFLASH_ERR_UNSUPPORTED, "fusion: d_model must be a multiple of 4");
   float* Ypart = w.take<float>(static_cast<size_t>(f.k_splits) * M * D);
   auto* H = w.take<__nv_bfloat16>(static_cast<size_t>(M) * D);
 
@@ -555,7 +656,7 @@ dflash_status launch_fuse_context(int J, const void* const* taps, int dt_width, 
     if (s) return s;
   }
   CUtensorMap bm;
-  dflash_status s = make_tmap_bf16_2d(&bm, w_fuse, static_cast<uint64_t>(D), static_cast<uint64_t>(J) * dt_width, 256, kBK);
+  dflash_status s = make_tmap_bf16_2d(&bm, w_fuse, static_cast<uint64_t>(D), static_cast<uint64_t>(J) * dt_width, 128, kBK);
   if (s) return s;
   GemmArgs a{};
   a.M = M;
@@ -563,18 +664,32 @@ dflash_status launch_fuse_context(int J, const void* const* taps, int dt_width, 
   a.num_kb = J * dt_width / kBK;
   a.kb_per_seg = dt_width / kBK;
   a.k_splits = std::min(f.k_splits, a.num_kb);
-  a.m_tiles = f.m_tiles;
+  a.m_tiles = f.fuse_m_tiles;
   a.n_tiles = f.fuse_n_tiles;
   a.epi = 0;
   a.out_f32 = Ypart;
   a.status = dev.status;
-  s = launch_gemm<256, kStagesBN256>(am, bm, a, st, dev);
+  s = f.fuse_mt == 2 ? launch_gemm<128, 4, 2>(am, bm, a, st, dev) : launch_gemm<128, 6, 1>(am, bm, a, st, dev);
   if (s) return s;
 
-  // 2. RMSNorm -> H_t (bf16)
-  fuse_rmsnorm_kernel<__nv_bfloat16, __nv_bfloat16><<<M, 256, 0, st>>>(
-      Ypart, a.k_splits, M, D, static_cast<const __nv_bfloat16*>(g_fuse), eps, H,
-      static_cast<__nv_bfloat16*>(h_t_out));
+  // 2. row map + split-K sum + RMSNorm -> H_t (bf16), a programmatic dependent
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(M));
+    cfg.blockDim = dim3(kNormThreads);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t le = cudaLaunchKernelEx(&cfg, fuse_rownorm_kernel<__nv_bfloat16, __nv_bfloat16>,
+                                        static_cast<const float*>(Ypart), a.k_splits, M, D,
+                                        static_cast<const __nv_bfloat16*>(g_fuse), eps, H,
+                                        static_cast<__nv_bfloat16*>(h_t_out), cu_new, c.seq_len, B, c.capacity, inv,
+                                        rowinfo, rope_cs, dev.status);
+    if (le != cudaSuccess) return cuda_fail(le, "fuse_rownorm_kernel launch");
+  }
 
   // 3. K/V GEMM with the cache epilogue
   TmapPack hm{};
@@ -589,9 +704,10 @@ dflash_status launch_fuse_context(int J, const void* const* taps, int dt_width, 
   k.num_kb = D / kBK;
   k.kb_per_seg = k.num_kb;
   k.k_splits = 1;
-  k.m_tiles = f.m_tiles;
+  k.m_tiles = (M + kBM - 1) / kBM;
   k.n_tiles = Ntot / f.kv_bn;
   k.epi = 1;
+  k.pdl = 1;
   k.cache_k = static_cast<__nv_bfloat16*>(c.k);
   k.cache_v = static_cast<__nv_bfloat16*>(c.v);
   k.L = L;
@@ -603,8 +719,7 @@ dflash_status launch_fuse_context(int J, const void* const* taps, int dt_width, 
   k.k_gain = static_cast<const __nv_bfloat16*>(k_gain);
   k.eps = eps;
   k.status = dev.status;
-  return f.kv_bn == 256 ? launch_gemm<256, kStagesBN256>(hm, wm, k, st, dev)
-                        : launch_gemm<128, kStagesBN128>(hm, wm, k, st, dev);
+  return f.kv_bn == 256 ? launch_gemm<256, 4, 1>(hm, wm, k, st, dev) : launch_gemm<128, 6, 1>(hm, wm, k, st, dev);
 }
 
 }  // namespace dflash
