@@ -189,7 +189,7 @@ class Cycle:
         self.cycle += 1
 
 
-LAUNCHES_PER_STEP = 4 + 5 * 3 + 4   # fusion 4, block attention 3 per layer, verify 4 (T > 0)
+LAUNCHES_PER_STEP = 3 + 5 * 3 + 2   # fusion 3, block attention 3 per layer, verification 2
 
 
 def run_gpu(args):
