@@ -165,24 +165,29 @@ class Cycle:
             + self.M * cfg.L * 2 * cfg.Hkv * cfg.d * 2
         self.fuse_flops = 2 * self.M * (cfg.J * cfg.d_target * cfg.D + cfg.D * cfg.L * 2 * cfg.Hkv * cfg.d)
 
-    def step(self, stream, ev=None, only="all"):
+    def inputs(self):
+        """The per-step inputs (what a serving loop would receive each cycle)."""
+        return {"taps": self.taps, "blocks": self.blocks, "lt": self.lt, "ld": self.ld, "x": self.x}
+
+    def step(self, stream, ev=None, only="all", inputs=None):
         dfl, c = self.dfl, self.cfg
+        inp = inputs if inputs is not None else self.inputs()
         if ev is not None:
             ev[0].record(stream)
         if only in ("all", "fuse"):
-            dfl.fuse_context(self.taps, self.cu, self.w.w_fuse, self.w.g_fuse, self.w.w_kv, self.w.k_gain,
+            dfl.fuse_context(inp["taps"], self.cu, self.w.w_fuse, self.w.g_fuse, self.w.w_kv, self.w.k_gain,
                              self.cache, workspace=self.ws_f, stream=stream)
         if ev is not None:
             ev[1].record(stream)
         if only in ("all", "attn"):
             for l in range(c.L):
-                q, kb, vb = self.blocks[l]
+                q, kb, vb = inp["blocks"][l]
                 dfl.block_attn(l, q, kb, vb, self.w.q_gain[l], self.w.k_gain[l], self.cache, out=self.outs[l],
                                workspace=self.ws_a, stream=stream)
         if ev is not None:
             ev[2].record(stream)
         if only in ("all", "verify"):
-            dfl.verify(self.lt, self.ld, self.x, self.T, 1234, self.cycle, accepted_len=self.acc,
+            dfl.verify(inp["lt"], inp["ld"], inp["x"], self.T, 1234, self.cycle, accepted_len=self.acc,
                        out_tokens=self.tok, workspace=self.ws_v, stream=stream)
         if ev is not None:
             ev[3].record(stream)
@@ -293,50 +298,77 @@ def run_gpu(args):
 
 def run_e2e(cyc, stream, args, dev):
     """Same cycle through the public API with the step's inputs in pinned host
-    memory: H2D copies of the new context rows, block projections, logits and
-    draft tokens, then the calls, then D2H of the accepted lengths and tokens."""
+    memory: every step copies its new context rows, block projections, logits
+    and draft tokens to the device, runs the calls and reads the accepted
+    lengths and tokens back.  As a serving loop would, the copies of step i+1
+    run on a second stream into a second set of device buffers while step i
+    computes (double buffering)."""
     host = {
         "taps": [t.cpu().pin_memory() for t in cyc.taps],
         "blocks": [[t.cpu().pin_memory() for t in b] for b in cyc.blocks],
         "lt": cyc.lt.cpu().pin_memory(), "ld": cyc.ld.cpu().pin_memory(), "x": cyc.x.cpu().pin_memory(),
     }
-    acc_h = torch.empty(cyc.cfg.B, dtype=torch.int32).pin_memory()
-    tok_h = torch.empty(cyc.cfg.B, cyc.cfg.bs, dtype=torch.int32).pin_memory()
+    res_h = [(torch.empty(cyc.cfg.B, dtype=torch.int32).pin_memory(),
+              torch.empty(cyc.cfg.B, cyc.cfg.bs, dtype=torch.int32).pin_memory()) for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host["taps"]) + \
         sum(t.numel() * t.element_size() for b in host["blocks"] for t in b) + \
         sum(host[k].numel() * host[k].element_size() for k in ("lt", "ld", "x"))
-    d2h = acc_h.numel() * 4 + tok_h.numel() * 4
+    d2h = res_h[0][0].numel() * 4 + res_h[0][1].numel() * 4
+    base = cyc.inputs()
+    sets = [base, {"taps": [t.clone() for t in base["taps"]], "blocks": [[t.clone() for t in b] for b in base["blocks"]],
+                   "lt": base["lt"].clone(), "ld": base["ld"].clone(), "x": base["x"].clone()}]
+    copy_stream = torch.cuda.Stream(device=dev)
+    uploaded = [torch.cuda.Event() for _ in range(2)]
+    released = [torch.cuda.Event() for _ in range(2)]
 
-    def step():
-        for d, h in zip(cyc.taps, host["taps"]):
-            d.copy_(h, non_blocking=True)
-        for db, hb in zip(cyc.blocks, host["blocks"]):
-            for d, h in zip(db, hb):
-                d.copy_(h, non_blocking=True)
-        cyc.lt.copy_(host["lt"], non_blocking=True)
-        cyc.ld.copy_(host["ld"], non_blocking=True)
-        cyc.x.copy_(host["x"], non_blocking=True)
-        cyc.step(stream)
-        acc_h.copy_(cyc.acc, non_blocking=True)
-        tok_h.copy_(cyc.tok, non_blocking=True)
+    def upload(i):
+        k = i % 2
+        d = sets[k]
+        with torch.cuda.stream(copy_stream):
+            if i >= 2:
+                copy_stream.wait_event(released[k])   # step i-2 is done with this set
+            for dt, ht in zip(d["taps"], host["taps"]):
+                dt.copy_(ht, non_blocking=True)
+            for db, hb in zip(d["blocks"], host["blocks"]):
+                for dt, ht in zip(db, hb):
+                    dt.copy_(ht, non_blocking=True)
+            for key in ("lt", "ld", "x"):
+                d[key].copy_(host[key], non_blocking=True)
+            uploaded[k].record(copy_stream)
 
-    with torch.cuda.stream(stream):
-        for _ in range(max(1, args.warmup)):
-            step()
-        torch.cuda.synchronize()
-        t0 = torch.cuda.Event(enable_timing=True)
-        t1 = torch.cuda.Event(enable_timing=True)
-        n = max(1, min(args.steps, 50))
-        t0.record(stream)
-        for _ in range(n):
-            step()
-        t1.record(stream)
-        torch.cuda.synchronize()
+    def compute(i):
+        k = i % 2
+        with torch.cuda.stream(stream):
+            stream.wait_event(uploaded[k])
+            cyc.step(stream, inputs=sets[k])
+            released[k].record(stream)
+            res_h[k][0].copy_(cyc.acc, non_blocking=True)
+            res_h[k][1].copy_(cyc.tok, non_blocking=True)
+
+    def run(n):
+        upload(0)
+        for i in range(n):
+            if i + 1 < n:
+                upload(i + 1)
+            compute(i)
+
+    run(max(1, args.warmup))
+    torch.cuda.synchronize()
+    n = max(1, min(args.steps, 50))
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(copy_stream)
+    stream.wait_event(t0)
+    run(n)
+    t1.record(stream)
+    torch.cuda.synchronize()
     el = t0.elapsed_time(t1) / 1e3
     el, _ = reduce_max_sum(el, 0.0, dev)
     _, world, _ = env_rank()
     return {"value": world * n / el, "unit": UNIT, "steps": n, "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h)}
+            "d2h_bytes_per_step": int(d2h),
+            "pipelining": "double-buffered: the host-to-device copies of step i+1 run on a second stream while "
+                          "step i computes; every step's copies and result read are inside the timed region"}
 
 
 # ------------------------------------------------------------ CPU oracle ----
