@@ -14,19 +14,22 @@
 //                  x = logit * log2(e)/T, or (max, first argmax) when T == 0.
 //   2. decide   -- (T == 0) one warp per sequence: the target argmax of every
 //                  row against the draft tokens.
-//   2. finish   -- (T > 0) one CTA per (sequence, chunk), launched as a
-//                  programmatic dependent of the stats pass.  Its first warp
-//                  merges the sequence's chunk partials into log-normalisers,
-//                  evaluates alpha_k = min(1, p(x)/q(x)) from two single-logit
-//                  loads per row, draws the Philox uniforms and finds the first
-//                  rejection n (every CTA of the sequence takes the same
-//                  decision).  The CTA then sums max(0, p - q) (the bonus row:
-//                  p) over its chunk of row n; the last CTA of the sequence to
-//                  finish (an atomic count) runs the inverse-CDF search for the
-//                  first index whose cumulative mass exceeds v * S.
+//   2. finish   -- (T > 0) one CTA per (sequence, two chunks), launched as a
+//                  programmatic dependent of the stats pass.  Before waiting
+//                  for it the CTA loads the draft tokens' target and draft
+//                  logits; then all warps merge the sequence's chunk partials
+//                  into log-normalisers and one warp evaluates
+//                  alpha_k = min(1, p(x)/q(x)), draws the Philox uniforms and
+//                  finds the first rejection n (every CTA of the sequence takes
+//                  the same decision).  The CTA sums max(0, p - q) (the bonus
+//                  row: p) over its chunks of row n; the last CTA of the
+//                  sequence to finish (an atomic count) runs the inverse-CDF
+//                  search for the first index whose cumulative mass exceeds
+//                  v * S.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <climits>
 
 #include "dflash_device.cuh"
@@ -39,6 +42,7 @@ constexpr int kThreads = 256;
 constexpr int kChunk = 16384;                 // logits per CTA chunk
 constexpr int kPerThread = kChunk / kThreads;  // 64 logits per thread
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kFinishChunks = 2;              // chunks per CTA of the finish kernel
 
 struct Decision {
   int n;            // accepted drafts; the correction/bonus comes from row n
@@ -244,10 +248,12 @@ __device__ __forceinline__ Decision decide_seq(const T* __restrict__ lt, const T
                                                int nchunk, float scale, const float2* __restrict__ part,
                                                uint32_t k0, uint32_t k1, uint32_t c_lo, uint32_t c_hi,
                                                int32_t* __restrict__ acc, int32_t* __restrict__ out,
-                                               unsigned* status, const float* s_lz = nullptr) {
+                                               unsigned* status, const float* s_lz = nullptr,
+                                               const float2* pre = nullptr) {
   const int lane = threadIdx.x % 32;
   int xk = -1;
   if (lane < bs - 1) xk = x[b * (bs - 1) + lane];
+  // pre (optional): lane k's target and draft logits of its token, loaded earlier
   float lzp = 0.f, lzq = 0.f;
   int amax = 0;
   if constexpr (GREEDY) {
@@ -274,8 +280,10 @@ __device__ __forceinline__ Decision decide_seq(const T* __restrict__ lt, const T
       } else if constexpr (GREEDY) {
         rejected = (amax != xk);
       } else {
-        const float lp = to_f32<T>(lt[static_cast<size_t>(b * bs + lane) * V + xk]) * scale - lzp;
-        const float lq = to_f32<T>(ld[static_cast<size_t>(b * (bs - 1) + lane) * V + xk]) * scale - lzq;
+        const float rt = pre ? pre->x : to_f32<T>(lt[static_cast<size_t>(b * bs + lane) * V + xk]);
+        const float rd = pre ? pre->y : to_f32<T>(ld[static_cast<size_t>(b * (bs - 1) + lane) * V + xk]);
+        const float lp = rt * scale - lzp;
+        const float lq = rd * scale - lzq;
         const float alpha = fminf(1.f, exp2f(lp - lq));
         rejected = !(uniform24(w.x) < alpha);
       }
@@ -334,8 +342,17 @@ __global__ void __launch_bounds__(kThreads) verify_finish_kernel(
     int nchunk, float scale, const float2* __restrict__ part, uint32_t k0, uint32_t k1, uint32_t c_lo,
     uint32_t c_hi, int32_t* __restrict__ acc, int32_t* __restrict__ out, float2* __restrict__ rpart,
     int* __restrict__ counters, unsigned* status) {
+  const int ncb = (nchunk + kFinishChunks - 1) / kFinishChunks;  // CTAs per sequence
+  const int b = blockIdx.x / ncb, cb = blockIdx.x % ncb;
+  // the draft tokens' logits do not depend on the stats pass: load them first
+  float2 pre = make_float2(0.f, 0.f);
+  if (threadIdx.x < bs - 1) {
+    const int xk = x[b * (bs - 1) + threadIdx.x];
+    if (xk >= 0 && xk < V)
+      pre = make_float2(to_f32<T>(lt[static_cast<size_t>(b * bs + threadIdx.x) * V + xk]),
+                        to_f32<T>(ld[static_cast<size_t>(b * (bs - 1) + threadIdx.x) * V + xk]));
+  }
   pdl_wait_primary();  // the stats pass's partials and cleared counters
-  const int b = blockIdx.x / nchunk, c = blockIdx.x % nchunk;
   __shared__ Decision s_dec;
   __shared__ int s_is_last;
   __shared__ float s_lz[32];
@@ -343,13 +360,13 @@ __global__ void __launch_bounds__(kThreads) verify_finish_kernel(
   __syncthreads();
   if (threadIdx.x < 32) {
     const Decision dw = decide_seq<T, false>(lt, ld, x, b, B, bs, V, nchunk, scale, part, k0, k1, c_lo, c_hi,
-                                             c == 0 ? acc : nullptr, c == 0 ? out : nullptr, status, s_lz);
+                                             cb == 0 ? acc : nullptr, cb == 0 ? out : nullptr, status, s_lz, &pre);
     if (threadIdx.x == 0) s_dec = dw;
   }
   __syncthreads();
   const Decision d = s_dec;
   const bool has_q = d.n < bs - 1;
-  {
+  for (int c = cb * kFinishChunks; c < min(nchunk, (cb + 1) * kFinishChunks); ++c) {
     // masses of max(0, p - q) and of p over this chunk of row n
     constexpr int NV = kPerThread / VEC;
     const T* prow = lt + static_cast<size_t>(b * bs + d.n) * V;
@@ -386,11 +403,14 @@ __global__ void __launch_bounds__(kThreads) verify_finish_kernel(
         a.y += red[w].y;
       }
       rpart[static_cast<size_t>(b) * nchunk + c] = a;
-      __threadfence();
-      s_is_last = atomicAdd(counters + b, 1) == nchunk - 1;
     }
     __syncthreads();
   }
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_is_last = atomicAdd(counters + b, 1) == ncb - 1;
+  }
+  __syncthreads();
   if (!s_is_last) return;
   __threadfence();
   // the last CTA of the sequence: inverse-CDF search over row n
@@ -539,7 +559,7 @@ dflash_status run(const T* lt, const T* ld, const int32_t* x, int B, int bs, int
   } else {
     verify_stats_kernel<T, VEC, false><<<g1, kThreads, 0, st>>>(lt, ld, B, bs, V, nchunk, scale, part, counters);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(nchunk) * static_cast<unsigned>(B));
+    cfg.gridDim = dim3(static_cast<unsigned>((nchunk + kFinishChunks - 1) / kFinishChunks) * static_cast<unsigned>(B));
     cfg.blockDim = dim3(kThreads);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
