@@ -254,6 +254,9 @@ def run_gpu(args):
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(cyc, stream, args, dev)
+    tensor_lines = None
+    if rank == 0 and not args.no_e2e:
+        tensor_lines = fusion_tensor_rooflines(dev, peaks()[1])
 
     if rank != 0:
         return
@@ -286,14 +289,57 @@ def run_gpu(args):
                              "achieved": cyc.fuse_bytes / (fuse_ms * 1e-3) / 1e9, "peak": hbm, "unit": "GB/s",
                              "frac": cyc.fuse_bytes / (fuse_ms * 1e-3) / 1e9 / hbm,
                              "tflops": cyc.fuse_flops / (fuse_ms * 1e-3) / 1e12}},
+        "peak_note": "HBM and bf16 peaks are the measured copy bandwidth and cuBLAS bf16 GEMM (burst) of this GPU",
         "gpu_launches": LAUNCHES_PER_STEP * args.steps,
         "clocks": clk,
     }
     if e2e is not None:
         line["e2e"] = e2e
+    if tensor_lines is not None:
+        line["rooflines"].update(tensor_lines)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, args.cpu_seconds, args.temperature)
     print(json.dumps(line), flush=True)
+
+
+def fusion_tensor_rooflines(dev, peak_tflops, iters=10):
+    """The fusion call on its tensor-bound shapes (the GEMMs' roofline): a 4 x 2048-row prefill chunk of the
+    long-context workload and the 128 x 16-row cycle of the high-batch bs = 16 workload.  Flops
+    2 M (J d_t D + D L 2 Hkv d) per call, CUDA events on the launching stream, 3 warm-up calls."""
+    import block_speculative_decoding_gb300 as dfl
+    from dataclasses import replace
+    out = {}
+    for name, B, rows, cap in (("fusion_prefill_4x2048", 4, 2048, 4096), ("fusion_cycle_128x16", 128, 16, 2064)):
+        cfg = replace(workloads.LONG_CONTEXT, B=B, S=cap - rows)
+        w = workloads.weights(cfg, dev)
+        M = B * rows
+        taps = workloads.taps(cfg, M, dev)
+        cu = workloads.cu_rows([rows] * B, dev)
+        k = torch.empty(cfg.L, B, cfg.Hkv, cap, cfg.d, dtype=torch.bfloat16, device=dev)
+        cache = dfl.KVCache(k, torch.empty_like(k), torch.zeros(B, dtype=torch.int32, device=dev))
+        ws = torch.empty(dfl.fuse_context_workspace_size(M, cfg.J, cfg.d_target, cfg.D, cfg.L, cfg.Hkv, dfl.BF16),
+                         dtype=torch.uint8, device=dev)
+        st = torch.cuda.Stream(device=dev)
+        call = lambda: dfl.fuse_context(taps, cu, w.w_fuse, w.g_fuse, w.w_kv, w.k_gain, cache,  # noqa: E731
+                                        workspace=ws, stream=st)
+        with torch.cuda.stream(st):
+            for _ in range(3):
+                call()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            for _ in range(iters):
+                call()
+            e1.record(st)
+            torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / iters
+        flops = 2 * M * (cfg.J * cfg.d_target * cfg.D + cfg.D * cfg.L * 2 * cfg.Hkv * cfg.d)
+        tf = flops / (ms * 1e-3) / 1e12
+        out[name] = {"bound": "tensor", "achieved": tf, "peak": peak_tflops, "unit": "TFLOP/s",
+                     "frac": tf / peak_tflops, "M": M, "ms_per_call": ms}
+        del taps, k, cache, ws
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_e2e(cyc, stream, args, dev):

@@ -540,12 +540,13 @@ __global__ void __launch_bounds__(256) kv_store_f32_kernel(const float* __restri
 
 // ------------------------------------------------------------- planning -----
 
-// Fusion GEMM: 128-column units; a few new rows (M <= 256) take 256-row units
-// (the W_c tile of a unit is read once) split along K to about one unit per SM;
-// prefill-sized M takes 128-row units.  K/V GEMM: 128-row units of one head (enough units to
-// fill the SMs at M = 256).
+// A few new rows (M <= 256, weight-bound): the fusion GEMM takes 256-row by
+// 128-column units (each W_c tile read once) split along K to about one unit
+// per SM, and the K/V GEMM 128 x 128 units of one head (enough units to fill
+// the SMs).  Larger M (tensor-bound): 128 x 256 units for both, the N = 256
+// MMA doing twice the work of N = 128 for 1.6x its time.
 struct FusePlan {
-  int fuse_mt, fuse_m_tiles, fuse_n_tiles, k_splits, kv_bn;
+  int fuse_mt, fuse_bn, fuse_m_tiles, fuse_n_tiles, k_splits, kv_bn;
 };
 
 FusePlan plan(int M, int D, int Ntot) {
@@ -553,10 +554,11 @@ FusePlan plan(int M, int D, int Ntot) {
   FusePlan f;
   f.fuse_mt = M <= 2 * kBM ? 2 : 1;
   f.fuse_m_tiles = (M + f.fuse_mt * kBM - 1) / (f.fuse_mt * kBM);
-  f.fuse_n_tiles = D / 128;
+  f.fuse_bn = M <= 2 * kBM ? 128 : 256;
+  f.fuse_n_tiles = D / f.fuse_bn;
   const int tiles = f.fuse_m_tiles * f.fuse_n_tiles;
   f.k_splits = std::max(1, std::min(16, kSplitTarget / std::max(1, tiles)));
-  f.kv_bn = 128;
+  f.kv_bn = M <= 2 * kBM ? 128 : 256;
   return f;
 }
 
@@ -656,7 +658,8 @@ dflash_status launch_fuse_context(int J, const void* const* taps, int dt_width, 
     if (s) return s;
   }
   CUtensorMap bm;
-  dflash_status s = make_tmap_bf16_2d(&bm, w_fuse, static_cast<uint64_t>(D), static_cast<uint64_t>(J) * dt_width, 128, kBK);
+  dflash_status s =
+      make_tmap_bf16_2d(&bm, w_fuse, static_cast<uint64_t>(D), static_cast<uint64_t>(J) * dt_width, f.fuse_bn, kBK);
   if (s) return s;
   GemmArgs a{};
   a.M = M;
@@ -669,7 +672,7 @@ dflash_status launch_fuse_context(int J, const void* const* taps, int dt_width, 
   a.epi = 0;
   a.out_f32 = Ypart;
   a.status = dev.status;
-  s = f.fuse_mt == 2 ? launch_gemm<128, 4, 2>(am, bm, a, st, dev) : launch_gemm<128, 6, 1>(am, bm, a, st, dev);
+  s = f.fuse_mt == 2 ? launch_gemm<128, 4, 2>(am, bm, a, st, dev) : launch_gemm<256, 4, 1>(am, bm, a, st, dev);
   if (s) return s;
 
   // 2. row map + split-K sum + RMSNorm -> H_t (bf16), a programmatic dependent
