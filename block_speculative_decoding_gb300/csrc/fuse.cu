@@ -56,6 +56,10 @@ struct TmapPack {
 
 struct GemmArgs {
   int M, N, num_kb, kb_per_seg, k_splits, m_tiles, n_tiles;
+  int stream_k;            // > 0: the number of shares (CTAs); CTA c takes the c-th near-equal share of the
+                           // (tile, K block) space
+  int dp_tiles;            // stream_k: leading tiles scheduled whole, a multiple of the share count
+  int* pieces;             // stream_k: [m_tiles * n_tiles] number of slots written for the tile
   int epi;                 // 0: fp32 partial store, 1: K/V cache epilogue
   int pdl;                 // launched as a programmatic dependent: A comes from the previous kernel
   float* out_f32;          // epi 0: [k_splits][M][N]
@@ -63,7 +67,7 @@ struct GemmArgs {
   __nv_bfloat16* cache_v;
   int L, Bc, Hkv, cap;
   const int2* rowinfo;     // [M] (sequence, position) or (-1, -1)
-  const float2* rope_cs;   // [M][64] (cos, sin)
+  const float2* rope_cs;   // [64][M] (cos, sin), element-major: a warp's rows read it coalesced
   const __nv_bfloat16* k_gain;  // [L][128] or null
   float eps;
   unsigned* status;
@@ -94,6 +98,82 @@ __device__ __forceinline__ void unit_coords(int u, const GemmArgs& p, int& m, in
   ks = u / (p.n_tiles * p.m_tiles);
   kb0 = static_cast<int>((static_cast<long>(ks) * p.num_kb) / p.k_splits);
   kb1 = static_cast<int>((static_cast<long>(ks + 1) * p.num_kb) / p.k_splits);
+}
+
+// The pieces of work of this CTA, in order.  Plain schedule: units
+// blockIdx.x, blockIdx.x + gridDim.x, ... (a unit: one tile over one K split,
+// its partial sum in slot = split index).  Stream-K schedule: the first
+// dp_tiles tiles (a whole number of waves) go round-robin as whole tiles;
+// the K blocks of the remaining tiles, laid end to end (tile-major, N tiles
+// fastest), are cut into gridDim.x near-equal, non-empty contiguous shares
+// [c tot / P, (c+1) tot / P), so K block x belongs to share ((x+1) P - 1) / tot.
+// A tile met by shares c0..c1 gets one partial sum per share, in slot c - c0;
+// the piece in slot 0 records the tile's slot count c1 - c0 + 1.  Keeping the
+// leading waves whole keeps the CTAs in step along K (operand tiles shared in
+// L2); only the tiles left over after the whole waves are balanced.
+__device__ __forceinline__ long share_of(long x, long tot, long P) { return ((x + 1) * P - 1) / tot; }
+
+struct Pieces {
+  long cur, end;  // plain: unit cursor and count; stream-K: cursor in the balanced K-block range
+  int dp_next;    // stream-K: next whole tile of this CTA
+  int count = 1;  // stream-K, slot 0: the tile's slot count
+  __device__ __forceinline__ explicit Pieces(const GemmArgs& p) {
+    dp_next = blockIdx.x;
+    if (p.stream_k) {
+      const long tot = (static_cast<long>(p.m_tiles) * p.n_tiles - p.dp_tiles) * p.num_kb;
+      cur = tot * blockIdx.x / gridDim.x;
+      end = tot * (blockIdx.x + 1) / gridDim.x;
+    } else {
+      cur = blockIdx.x;
+      end = static_cast<long>(p.m_tiles) * p.n_tiles * p.k_splits;
+    }
+  }
+  __device__ __forceinline__ bool next(const GemmArgs& p, int& m, int& n, int& kb0, int& kb1, int& slot) {
+    if (p.stream_k && dp_next < p.dp_tiles) {
+      n = dp_next % p.n_tiles;
+      m = dp_next / p.n_tiles;
+      kb0 = 0;
+      kb1 = p.num_kb;
+      slot = 0;
+      count = 1;
+      dp_next += gridDim.x;
+      return true;
+    }
+    if (cur >= end) return false;
+    if (p.stream_k) {
+      const long tr = cur / p.num_kb;  // tile index within the balanced range
+      const long t = p.dp_tiles + tr;
+      kb0 = static_cast<int>(cur - tr * p.num_kb);
+      kb1 = static_cast<int>(min(static_cast<long>(p.num_kb), kb0 + (end - cur)));
+      n = static_cast<int>(t % p.n_tiles);
+      m = static_cast<int>(t / p.n_tiles);
+      const long tot = (static_cast<long>(p.m_tiles) * p.n_tiles - p.dp_tiles) * p.num_kb;
+      const long c0 = share_of(tr * p.num_kb, tot, gridDim.x);
+      slot = static_cast<int>(blockIdx.x - c0);
+      if (slot == 0) count = static_cast<int>(share_of((tr + 1) * p.num_kb - 1, tot, gridDim.x) - c0 + 1);
+      cur += kb1 - kb0;
+    } else {
+      unit_coords(static_cast<int>(cur), p, m, n, kb0, kb1, slot);
+      cur += gridDim.x;
+    }
+    return true;
+  }
+};
+
+// Eight gains from element e of a head's [128] gain vector (ones without one),
+// one 16-byte load when the vector is 16-byte aligned.
+__device__ __forceinline__ void gain8(const __nv_bfloat16* kg, bool vec, int e, float (&g)[8]) {
+  if (kg == nullptr) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) g[i] = 1.f;
+  } else if (vec) {
+    const uint4 u = *reinterpret_cast<const uint4*>(kg + e);
+    g[0] = bf16_lo(u.x); g[1] = bf16_hi(u.x); g[2] = bf16_lo(u.y); g[3] = bf16_hi(u.y);
+    g[4] = bf16_lo(u.z); g[5] = bf16_hi(u.z); g[6] = bf16_lo(u.w); g[7] = bf16_hi(u.w);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) g[i] = __bfloat162float(kg[e + i]);
+  }
 }
 
 // Epilogue of one 128-column head of the K/V projection for this thread's row.
@@ -139,7 +219,9 @@ __device__ __forceinline__ void kv_head_epilogue(uint32_t taddr, int col0, int r
   }
   const float rinv = rsqrtf(ss * (1.0f / HD) + p.eps);
   const __nv_bfloat16* kg = p.k_gain ? p.k_gain + l * HD : nullptr;
-  const float2* cs = p.rope_cs + static_cast<size_t>(valid ? row : 0) * (HD / 2);
+  const bool kg_vec = kg && (reinterpret_cast<uintptr_t>(kg) & 15u) == 0;
+  const float2* cs = p.rope_cs + (valid ? row : 0);
+  const size_t cs_stride = static_cast<size_t>(p.M);
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
     const int e0 = half * 32;
@@ -149,21 +231,25 @@ __device__ __forceinline__ void kv_head_epilogue(uint32_t taddr, int col0, int r
     tmem_ld_wait();
     uint32_t o1[16], o2[16];
 #pragma unroll
-    for (int i = 0; i < 32; i += 2) {
-      float a[2], b[2];
+    for (int j8 = 0; j8 < 32; j8 += 8) {
+      float g1[8], g2[8];
+      gain8(kg, kg_vec, e0 + j8, g1);
+      gain8(kg, kg_vec, 64 + e0 + j8, g2);
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const int e = e0 + i + k;
-        const float g1 = kg ? __bfloat162float(kg[e]) : 1.f;
-        const float g2 = kg ? __bfloat162float(kg[e + 64]) : 1.f;
-        const float y1 = __uint_as_float(r[i + k]) * rinv * g1;
-        const float y2 = __uint_as_float(r2[i + k]) * rinv * g2;
-        const float2 c = valid ? cs[e] : make_float2(1.f, 0.f);
-        a[k] = y1 * c.x - y2 * c.y;
-        b[k] = y2 * c.x + y1 * c.y;
+      for (int i = 0; i < 8; i += 2) {
+        float a[2], b[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int j = j8 + i + k;
+          const float y1 = __uint_as_float(r[j]) * rinv * g1[i + k];
+          const float y2 = __uint_as_float(r2[j]) * rinv * g2[i + k];
+          const float2 c = valid ? cs[(e0 + j) * cs_stride] : make_float2(1.f, 0.f);
+          a[k] = y1 * c.x - y2 * c.y;
+          b[k] = y2 * c.x + y1 * c.y;
+        }
+        o1[(j8 + i) / 2] = pack_bf16x2(a[0], a[1]);
+        o2[(j8 + i) / 2] = pack_bf16x2(b[0], b[1]);
       }
-      o1[i / 2] = pack_bf16x2(a[0], a[1]);
-      o2[i / 2] = pack_bf16x2(b[0], b[1]);
     }
     if (valid) {
       uint4* d1 = reinterpret_cast<uint4*>(dst + e0);
@@ -218,7 +304,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
   tc_fence_after_sync();
   pdl_launch_dependents();
   const uint32_t tmem_base = *tmem_slot;
-  const int total = p.m_tiles * p.n_tiles * p.k_splits;
 
   if (warp == 0) {
     if (lane == 0) {  // ------------------------------ TMA producer
@@ -228,9 +313,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
       // The B operand (weights) does not depend on the previous kernel: as a
       // programmatic dependent, fill the ring's B halves first, then wait.
       int pre = 0;
-      if (p.pdl && blockIdx.x < total) {
-        int m, n, kb0, kb1, ks;
-        unit_coords(blockIdx.x, p, m, n, kb0, kb1, ks);
+      Pieces first(p);
+      int m, n, kb0, kb1, ks;
+      if (p.pdl && first.next(p, m, n, kb0, kb1, ks)) {
         for (; pre < STAGES && kb0 + pre < kb1; ++pre) {
           const uint32_t fb = full0 + 8 * pre;
           mbar_arrive_expect_tx(fb, STAGE);
@@ -241,11 +326,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-        int m, n, kb0, kb1, ks;
-        unit_coords(u, p, m, n, kb0, kb1, ks);
+      Pieces pcs(p);
+      for (bool head = true; ok && pcs.next(p, m, n, kb0, kb1, ks); head = false) {
         for (int kb = kb0; kb < kb1; ++kb) {
-          const bool b_done = u == static_cast<int>(blockIdx.x) && kb - kb0 < pre;
+          const bool b_done = head && kb - kb0 < pre;
           if (!b_done && !(ok = mbar_wait(empty0 + 8 * stage, phase ^ 1u, p.status))) break;
           const uint32_t fb = full0 + 8 * stage;
           if (!b_done) mbar_arrive_expect_tx(fb, STAGE);
@@ -269,9 +353,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-        int m, n, kb0, kb1, ks;
-        unit_coords(u, p, m, n, kb0, kb1, ks);
+      Pieces pcs(p);
+      int m, n, kb0, kb1, ks;
+      while (ok && pcs.next(p, m, n, kb0, kb1, ks)) {
         if (!(ok = mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1u, p.status))) break;
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
@@ -304,10 +388,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int u = blockIdx.x; u < total; u += gridDim.x) {
-      int m, n, kb0, kb1, ks;
-      unit_coords(u, p, m, n, kb0, kb1, ks);
+    Pieces pcs(p);
+    int m, n, kb0, kb1, ks;
+    while (pcs.next(p, m, n, kb0, kb1, ks)) {
       if (!mbar_wait(tfull0 + 8 * acc, acc_phase, p.status)) break;
+      if (p.stream_k && ks == 0 && warp == 2 && lane == 0) p.pieces[m * p.n_tiles + n] = pcs.count;
       tc_fence_after_sync();
 #pragma unroll 1
       for (int i = 0; i < MT; ++i) {
@@ -362,7 +447,8 @@ constexpr int kNormSlots = 4;  // float4 slots per thread
 
 template <typename TG, typename TH>
 __global__ void __launch_bounds__(kNormThreads) fuse_rownorm_kernel(
-    const float* __restrict__ part, int k_splits, int M, int D, const TG* __restrict__ g, float eps,
+    const float* __restrict__ part, int k_splits, const int* __restrict__ pieces, int tile_rows, int tile_cols,
+    int n_tiles, int M, int D, const TG* __restrict__ g, float eps,
     TH* __restrict__ ht, TH* __restrict__ ht_out, const int32_t* __restrict__ cu_new,
     const int32_t* __restrict__ seq_len, int B, int cap, InvFreq inv, int2* __restrict__ rowinfo,
     float2* __restrict__ rope_cs, unsigned* status) {
@@ -385,7 +471,7 @@ __global__ void __launch_bounds__(kNormThreads) fuse_rownorm_kernel(
       ang -= kTwoPi * rint(ang / kTwoPi);
       float sv, cv;
       sincosf(static_cast<float>(ang), &sv, &cv);
-      rope_cs[static_cast<size_t>(m) * (HD / 2) + threadIdx.x] = make_float2(cv, sv);
+      rope_cs[static_cast<size_t>(threadIdx.x) * M + m] = make_float2(cv, sv);
     } else {
       rowinfo[m] = valid ? make_int2(b, pos) : make_int2(-1, -1);
       if (!valid) raise_status(status, seq_ok ? DFLASH_DEV_CAPACITY : DFLASH_DEV_BAD_SEQLEN);
@@ -396,9 +482,12 @@ __global__ void __launch_bounds__(kNormThreads) fuse_rownorm_kernel(
   const int nv = D / 4;  // float4 slots of the row
   const float4* prow = reinterpret_cast<const float4*>(part + static_cast<size_t>(m) * D);
   const size_t split_stride = static_cast<size_t>(M) * D / 4;
+  // stream-K partials: a tile has as many slots as shares that met it
+  const int* prow_pieces = pieces ? pieces + (m / tile_rows) * n_tiles : nullptr;
   auto row_sum = [&](int v) {
     float4 t4 = prow[v];
-    for (int s = 1; s < k_splits; ++s) {
+    const int ns = prow_pieces ? prow_pieces[(4 * v) / tile_cols] : k_splits;
+    for (int s = 1; s < ns; ++s) {
       const float4 t = prow[s * split_stride + v];
       t4.x += t.x;
       t4.y += t.y;
@@ -531,7 +620,7 @@ __global__ void __launch_bounds__(256) kv_store_f32_kernel(const float* __restri
   x1 *= r * (kg ? kg[e0 + 1] : 1.f);
   y0 *= r * (kg ? kg[e0 + 64] : 1.f);
   y1 *= r * (kg ? kg[e0 + 65] : 1.f);
-  const float2 c0 = rope_cs[static_cast<size_t>(m) * 64 + e0], c1 = rope_cs[static_cast<size_t>(m) * 64 + e0 + 1];
+  const float2 c0 = rope_cs[static_cast<size_t>(e0) * M + m], c1 = rope_cs[static_cast<size_t>(e0 + 1) * M + m];
   dst[e0] = x0 * c0.x - y0 * c0.y;
   dst[e0 + 1] = x1 * c1.x - y1 * c1.y;
   dst[e0 + 64] = y0 * c0.x + x0 * c0.y;
@@ -544,20 +633,35 @@ __global__ void __launch_bounds__(256) kv_store_f32_kernel(const float* __restri
 // 128-column units (each W_c tile read once) split along K to about one unit
 // per SM, and the K/V GEMM 128 x 128 units of one head (enough units to fill
 // the SMs).  Larger M (tensor-bound): 128 x 256 units for both, the N = 256
-// MMA doing twice the work of N = 128 for 1.6x its time.
+// MMA doing twice the work of N = 128 for 1.6x its time.  When the fusion
+// GEMM's tiles do not fill whole waves of kSplitTarget CTAs, the whole waves
+// run tile by tile and the remaining tiles are balanced by stream-K over
+// kSplitTarget shares, with as many partial-sum slots as the most shares
+// meeting one tile.
 struct FusePlan {
-  int fuse_mt, fuse_bn, fuse_m_tiles, fuse_n_tiles, k_splits, kv_bn;
+  int fuse_mt, fuse_bn, fuse_m_tiles, fuse_n_tiles, k_splits, kv_bn, stream_k, shares, dp_tiles;
 };
 
-FusePlan plan(int M, int D, int Ntot) {
-  (void)Ntot;
+FusePlan plan(int M, int D, int num_kb) {
   FusePlan f;
   f.fuse_mt = M <= 2 * kBM ? 2 : 1;
   f.fuse_m_tiles = (M + f.fuse_mt * kBM - 1) / (f.fuse_mt * kBM);
   f.fuse_bn = M <= 2 * kBM ? 128 : 256;
   f.fuse_n_tiles = D / f.fuse_bn;
   const int tiles = f.fuse_m_tiles * f.fuse_n_tiles;
+  f.stream_k = f.fuse_mt == 1 && tiles % kSplitTarget != 0;
+  f.shares = 0;
+  f.dp_tiles = 0;
   f.k_splits = std::max(1, std::min(16, kSplitTarget / std::max(1, tiles)));
+  if (f.stream_k) {
+    f.dp_tiles = tiles / kSplitTarget * kSplitTarget;
+    const long tot = static_cast<long>(tiles - f.dp_tiles) * num_kb;
+    f.shares = static_cast<int>(std::min<long>(kSplitTarget, tot));  // every share non-empty
+    auto share = [&](long x) { return ((x + 1) * f.shares - 1) / tot; };
+    f.k_splits = 1;
+    for (long t = 0; t < tiles - f.dp_tiles; ++t)
+      f.k_splits = std::max(f.k_splits, static_cast<int>(share((t + 1) * num_kb - 1) - share(t * num_kb) + 1));
+  }
   f.kv_bn = M <= 2 * kBM ? 128 : 256;
   return f;
 }
@@ -576,7 +680,7 @@ dflash_status launch_gemm(const TmapPack& am, const CUtensorMap& bm, const GemmA
   }
   const int units = a.m_tiles * a.n_tiles * a.k_splits;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(std::min(units, dev.num_sms)));
+  cfg.gridDim = dim3(static_cast<unsigned>(a.stream_k ? a.stream_k : std::min(units, dev.num_sms)));
   cfg.blockDim = dim3(kGemmThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
@@ -594,15 +698,14 @@ dflash_status launch_gemm(const TmapPack& am, const CUtensorMap& bm, const GemmA
 }  // namespace
 
 size_t fuse_ws_bytes(int M, int J, int dt_width, int D, int L, int Hkv, dflash_dtype dt) {
-  (void)J;
-  (void)dt_width;
   const int Ntot = L * 2 * Hkv * HD;
   size_t s = align256(static_cast<size_t>(M) * sizeof(int2)) +
              align256(static_cast<size_t>(M) * (HD / 2) * sizeof(float2));
   if (dt == DFLASH_BF16) {
-    const FusePlan f = plan(M, D, Ntot);
+    const FusePlan f = plan(M, D, J * dt_width / kBK);
     s += align256(static_cast<size_t>(f.k_splits) * M * D * sizeof(float)) +
-         align256(static_cast<size_t>(M) * D * sizeof(__nv_bfloat16));
+         align256(static_cast<size_t>(M) * D * sizeof(__nv_bfloat16)) +
+         align256(static_cast<size_t>(f.fuse_m_tiles) * f.fuse_n_tiles * sizeof(int));
   } else {
     s += align256(static_cast<size_t>(M) * D * sizeof(float)) * 2 +
          align256(static_cast<size_t>(M) * Ntot * sizeof(float));
@@ -632,7 +735,7 @@ dflash_status launch_fuse_context(int J, const void* const* taps, int dt_width, 
     simt_gemm_f32_kernel<<<dim3((D + 63) / 64, (M + 63) / 64), 256, 0, st>>>(
         segs, dt_width, static_cast<const float*>(w_fuse), M, D, J * dt_width, Y);
     fuse_rownorm_kernel<float, float><<<M, kNormThreads, 0, st>>>(
-        Y, 1, M, D, static_cast<const float*>(g_fuse), eps, H, static_cast<float*>(h_t_out), cu_new, c.seq_len, B,
+        Y, 1, nullptr, kBM, D, 1, M, D, static_cast<const float*>(g_fuse), eps, H, static_cast<float*>(h_t_out), cu_new, c.seq_len, B,
         c.capacity, inv, rowinfo, rope_cs, dev.status);
     F32Segs hs{};
     hs.a[0] = H;
@@ -646,10 +749,11 @@ dflash_status launch_fuse_context(int J, const void* const* taps, int dt_width, 
     return e == cudaSuccess ? DFLASH_OK : cuda_fail(e, "fp32 fusion launch");
   }
 
-  const FusePlan f = plan(M, D, Ntot);
+  const FusePlan f = plan(M, D, J * dt_width / kBK);
   if (D % 4 != 0) return fail(DFLASH_ERR_UNSUPPORTED, "fusion: d_model must be a multiple of 4");
   float* Ypart = w.take<float>(static_cast<size_t>(f.k_splits) * M * D);
   auto* H = w.take<__nv_bfloat16>(static_cast<size_t>(M) * D);
+  int* tile_pieces = w.take<int>(static_cast<size_t>(f.fuse_m_tiles) * f.fuse_n_tiles);
 
   // 1. fusion GEMM: A = the J taps (one tensor map each), B = W_c [D][J*dt]
   TmapPack am{};
@@ -666,7 +770,10 @@ dflash_status launch_fuse_context(int J, const void* const* taps, int dt_width, 
   a.N = D;
   a.num_kb = J * dt_width / kBK;
   a.kb_per_seg = dt_width / kBK;
-  a.k_splits = std::min(f.k_splits, a.num_kb);
+  a.k_splits = f.stream_k ? f.k_splits : std::min(f.k_splits, a.num_kb);
+  a.stream_k = f.stream_k ? f.shares : 0;
+  a.dp_tiles = f.dp_tiles;
+  a.pieces = tile_pieces;
   a.m_tiles = f.fuse_m_tiles;
   a.n_tiles = f.fuse_n_tiles;
   a.epi = 0;
@@ -687,7 +794,9 @@ dflash_status launch_fuse_context(int J, const void* const* taps, int dt_width, 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cudaError_t le = cudaLaunchKernelEx(&cfg, fuse_rownorm_kernel<__nv_bfloat16, __nv_bfloat16>,
-                                        static_cast<const float*>(Ypart), a.k_splits, M, D,
+                                        static_cast<const float*>(Ypart), a.k_splits,
+                                        static_cast<const int*>(f.stream_k ? tile_pieces : nullptr), f.fuse_mt * kBM,
+                                        f.fuse_bn, f.fuse_n_tiles, M, D,
                                         static_cast<const __nv_bfloat16*>(g_fuse), eps, H,
                                         static_cast<__nv_bfloat16*>(h_t_out), cu_new, c.seq_len, B, c.capacity, inv,
                                         rowinfo, rope_cs, dev.status);

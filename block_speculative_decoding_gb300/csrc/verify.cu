@@ -43,6 +43,8 @@ constexpr int kChunk = 16384;                 // logits per CTA chunk
 constexpr int kPerThread = kChunk / kThreads;  // 64 logits per thread
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kFinishChunks = 2;              // chunks per CTA of the finish kernel
+constexpr int kSeg = 2048;                    // logits per residual-mass segment (one warp's share of a chunk)
+constexpr int kSegsPerChunk = kChunk / kSeg;
 
 struct Decision {
   int n;            // accepted drafts; the correction/bonus comes from row n
@@ -105,6 +107,20 @@ __device__ __forceinline__ void load_raw(const T* __restrict__ row, int e0, int 
   for (int i = 0; i < kPerThread / VEC; ++i) {
     const int e = e0 + (i * kThreads + threadIdx.x) * VEC;
     live[i] = e < e1;
+    if (live[i]) v[i] = __ldcs(reinterpret_cast<const VT*>(row + e));
+  }
+}
+
+// Raw vectors of lane `lane`'s 64 logits of one warp's contiguous segment
+// [s0, s1): vector i covers elements s0 + (i*32 + lane)*VEC ...
+template <typename T, int VEC>
+__device__ __forceinline__ void load_seg(const T* __restrict__ row, int s0, int s1, int lane,
+                                         typename Vec<T, VEC>::type (&v)[kPerThread / VEC], bool (&live)[kPerThread / VEC]) {
+  using VT = typename Vec<T, VEC>::type;
+#pragma unroll
+  for (int i = 0; i < kPerThread / VEC; ++i) {
+    const int e = s0 + (i * 32 + lane) * VEC;
+    live[i] = e < s1;
     if (live[i]) v[i] = __ldcs(reinterpret_cast<const VT*>(row + e));
   }
 }
@@ -315,9 +331,9 @@ __global__ void __launch_bounds__(128) verify_decide_kernel(
 // Residual weight of one logit pair (or of p alone for the bonus row).
 __device__ __forceinline__ float resid_weight(float xt, float xd, const Decision& d, bool has_q,
                                               float& pw) {
-  pw = exp2f(xt - d.lzp);
+  pw = ex2_approx(xt - d.lzp);
   if (!has_q) return pw;
-  const float qw = exp2f(xd - d.lzq);
+  const float qw = ex2_approx(xd - d.lzq);
   return fmaxf(0.f, pw - qw);
 }
 
@@ -337,7 +353,7 @@ __device__ __forceinline__ void row_normalisers(const float2* __restrict__ part,
 
 // Non-greedy verification after the stats pass; see the file comment.
 template <typename T, int VEC>
-__global__ void __launch_bounds__(kThreads) verify_finish_kernel(
+__global__ void __launch_bounds__(kThreads, 2) verify_finish_kernel(
     const T* __restrict__ lt, const T* __restrict__ ld, const int32_t* __restrict__ x, int B, int bs, int V,
     int nchunk, float scale, const float2* __restrict__ part, uint32_t k0, uint32_t k1, uint32_t c_lo,
     uint32_t c_hi, int32_t* __restrict__ acc, int32_t* __restrict__ out, float2* __restrict__ rpart,
@@ -366,15 +382,18 @@ __global__ void __launch_bounds__(kThreads) verify_finish_kernel(
   __syncthreads();
   const Decision d = s_dec;
   const bool has_q = d.n < bs - 1;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int nseg = nchunk * kSegsPerChunk;
+  const T* prow = lt + static_cast<size_t>(b * bs + d.n) * V;
+  const T* qrow = has_q ? ld + static_cast<size_t>(b * (bs - 1) + d.n) * V : nullptr;
   for (int c = cb * kFinishChunks; c < min(nchunk, (cb + 1) * kFinishChunks); ++c) {
-    // masses of max(0, p - q) and of p over this chunk of row n
+    // masses of max(0, p - q) and of p over this warp's segment of row n
     constexpr int NV = kPerThread / VEC;
-    const T* prow = lt + static_cast<size_t>(b * bs + d.n) * V;
-    const int e0 = c * kChunk, e1 = min(V, e0 + kChunk);
+    const int s0 = c * kChunk + warp * kSeg, s1 = min(V, s0 + kSeg);
     typename Vec<T, VEC>::type vt[NV], vq[NV];
     bool live[NV];
-    load_raw<T, VEC>(prow, e0, e1, vt, live);
-    if (has_q) load_raw<T, VEC>(ld + static_cast<size_t>(b * (bs - 1) + d.n) * V, e0, e1, vq, live);
+    load_seg<T, VEC>(prow, s0, s1, lane, vt, live);
+    if (has_q) load_seg<T, VEC>(qrow, s0, s1, lane, vq, live);
     float sr = 0.f, sp = 0.f;
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
@@ -393,19 +412,10 @@ __global__ void __launch_bounds__(kThreads) verify_finish_kernel(
     }
     sr = warp_sum(sr);
     sp = warp_sum(sp);
-    __shared__ float2 red[kThreads / 32];
-    if (threadIdx.x % 32 == 0) red[threadIdx.x / 32] = make_float2(sr, sp);
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      float2 a = red[0];
-      for (int w = 1; w < kThreads / 32; ++w) {
-        a.x += red[w].x;
-        a.y += red[w].y;
-      }
-      rpart[static_cast<size_t>(b) * nchunk + c] = a;
-    }
-    __syncthreads();
+    if (lane == 0 && s0 < V) rpart[static_cast<size_t>(b) * nseg + c * kSegsPerChunk + warp] = make_float2(sr, sp);
   }
+  if (lane == 0) __threadfence();  // this warp's masses before the CTA's count below
+  __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
     s_is_last = atomicAdd(counters + b, 1) == ncb - 1;
@@ -413,113 +423,130 @@ __global__ void __launch_bounds__(kThreads) verify_finish_kernel(
   __syncthreads();
   if (!s_is_last) return;
   __threadfence();
-  // the last CTA of the sequence: inverse-CDF search over row n
-  __shared__ int s_chunk;
+  // the last CTA of the sequence: inverse-CDF search over row n, first over
+  // the segment masses (one warp, vocabulary order), then inside the segment
+  __shared__ int s_seg;
   __shared__ int s_use_p;
   __shared__ float s_target;
-  __shared__ float s_scan[kThreads];
+  __shared__ float s_wsum[kThreads / 32];
   __shared__ int s_pick;
   __shared__ int s_last;
-  if (threadIdx.x == 0) {
-    const float2* rp = rpart + static_cast<size_t>(b) * nchunk;
-    float sr = 0.f;
-    for (int c = 0; c < nchunk; ++c) sr += __ldcg(&rp[c]).x;
-    const int use_p = !(sr > 0.f);
-    float S = 0.f;
-    for (int c = 0; c < nchunk; ++c) S += use_p ? __ldcg(&rp[c]).y : __ldcg(&rp[c]).x;
-    const float t = uniform24(d.vbits) * S;
-    float cum = 0.f;
-    int cs = -1;
-    float excl = 0.f;
-    int last_pos = 0;
-    for (int c = 0; c < nchunk; ++c) {
-      const float2 rc = __ldcg(&rp[c]);
-      const float w = use_p ? rc.y : rc.x;
-      if (w > 0.f) last_pos = c;
-      if (cs < 0 && cum + w > t) {
-        cs = c;
-        excl = cum;
+  const int nseg_live = (V + kSeg - 1) / kSeg;
+  if (warp == 0) {
+    const float2* rp = rpart + static_cast<size_t>(b) * nseg;
+    float sr = 0.f, sp = 0.f;
+    for (int g = lane; g < nseg_live; g += 32) {
+      const float2 v = __ldcg(rp + g);
+      sr += v.x;
+      sp += v.y;
+    }
+    sr = warp_sum(sr);
+    sp = warp_sum(sp);
+    const bool use_p = !(sr > 0.f);
+    const float t = uniform24(d.vbits) * (use_p ? sp : sr);
+    float before = 0.f;  // mass of the segments ahead of this group of 32
+    int cs = -1, last_pos = -1;
+    float excl_cs = 0.f, excl_last = 0.f;
+    for (int g0 = 0; g0 < nseg_live && cs < 0; g0 += 32) {
+      const int g = g0 + lane;
+      float w = 0.f;
+      if (g < nseg_live) {
+        const float2 v = __ldcg(rp + g);
+        w = use_p ? v.y : v.x;
       }
-      cum += w;
+      float inc = w;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float u = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += u;
+      }
+      const float ex = before + (inc - w);
+      const unsigned hit = __ballot_sync(0xffffffffu, w > 0.f && ex + w > t);
+      const unsigned pos = __ballot_sync(0xffffffffu, w > 0.f);
+      if (hit) {
+        const int l = __ffs(hit) - 1;
+        cs = g0 + l;
+        excl_cs = __shfl_sync(0xffffffffu, ex, l);
+      }
+      if (pos) {
+        const int l = 31 - __clz(pos);
+        last_pos = g0 + l;
+        excl_last = __shfl_sync(0xffffffffu, ex, l);
+      }
+      before += __shfl_sync(0xffffffffu, inc, 31);
     }
     if (cs < 0) {  // rounding left the threshold at the very end
-      cs = last_pos;
-      excl = 0.f;
-      for (int c = 0; c < cs; ++c) excl += use_p ? __ldcg(&rp[c]).y : __ldcg(&rp[c]).x;
+      cs = max(last_pos, 0);
+      excl_cs = last_pos >= 0 ? excl_last : 0.f;
     }
-    s_chunk = cs;
-    s_use_p = use_p;
-    s_target = fmaxf(0.f, t - excl);
-    s_pick = INT_MAX;
-    s_last = -1;
+    if (lane == 0) {
+      s_seg = cs;
+      s_use_p = use_p;
+      s_target = fmaxf(0.f, t - excl_cs);
+      s_pick = INT_MAX;
+      s_last = -1;
+    }
   }
   __syncthreads();
-  const int e0 = s_chunk * kChunk, e1 = min(V, e0 + kChunk);
   const bool use_p = s_use_p != 0;
   const float target = s_target;
-  const T* prow = lt + static_cast<size_t>(b * bs + d.n) * V;
-  const T* qrow = has_q ? ld + static_cast<size_t>(b * (bs - 1) + d.n) * V : nullptr;
-  // contiguous segment of 64 logits per thread, in vocabulary order
-  const int s0 = e0 + threadIdx.x * kPerThread;
-  const int s1 = min(e1, s0 + kPerThread);
-  float w[kPerThread];
+  const int seg0 = s_seg * kSeg;
+  // kSeg / kThreads = 8 consecutive logits per thread, in vocabulary order
+  constexpr int kEach = kSeg / kThreads;
+  const int q0 = seg0 + threadIdx.x * kEach;
+  float w[kEach];
   {
-    constexpr int NV = kPerThread / VEC;
-    using VT = typename Vec<T, VEC>::type;
-    VT vp[NV], vq[NV];
     const bool with_q = has_q && !use_p;
+    constexpr int NV = kEach / VEC;
+    using VT = typename Vec<T, VEC>::type;
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
-      if (s0 + i * VEC < s1) {
-        vp[i] = *reinterpret_cast<const VT*>(prow + s0 + i * VEC);
-        if (with_q) vq[i] = *reinterpret_cast<const VT*>(qrow + s0 + i * VEC);
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < NV; ++i) {
+      const int e = q0 + i * VEC;
       float fp[VEC], fq[VEC];
-      const bool in = s0 + i * VEC < s1;
+      const bool in = e < V;
       if (in) {
-        Vec<T, VEC>::unpack(vp[i], fp);
-        if (with_q) Vec<T, VEC>::unpack(vq[i], fq);
+        Vec<T, VEC>::unpack(*reinterpret_cast<const VT*>(prow + e), fp);
+        if (with_q) Vec<T, VEC>::unpack(*reinterpret_cast<const VT*>(qrow + e), fq);
       }
 #pragma unroll
       for (int j = 0; j < VEC; ++j) {
         float pw;
         w[i * VEC + j] = (!in || fp[j] == -INFINITY) ? 0.f
                          : with_q ? resid_weight(fp[j] * scale, fq[j] * scale, d, true, pw)
-                                  : exp2f(fp[j] * scale - d.lzp);
+                                  : ex2_approx(fp[j] * scale - d.lzp);
       }
     }
   }
-  float seg = 0.f;
+  float mine = 0.f;
   int last_pos = -1;
 #pragma unroll
-  for (int i = 0; i < kPerThread; ++i) {
-    if (w[i] > 0.f) last_pos = s0 + i;
-    seg += w[i];
+  for (int i = 0; i < kEach; ++i) {
+    if (w[i] > 0.f) last_pos = q0 + i;
+    mine += w[i];
   }
-  // inclusive scan of segment masses across the block (Hillis-Steele)
-  s_scan[threadIdx.x] = seg;
-  __syncthreads();
-  for (int o = 1; o < kThreads; o <<= 1) {
-    const float v = threadIdx.x >= o ? s_scan[threadIdx.x - o] : 0.f;
-    __syncthreads();
-    s_scan[threadIdx.x] += v;
-    __syncthreads();
+  // exclusive scan of the threads' masses: within the warp, then across warps
+  float inc = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float u = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += u;
   }
-  const float incl = s_scan[threadIdx.x];
-  const float excl = incl - seg;
+  if (lane == 31) s_wsum[warp] = inc;
   if (last_pos >= 0) atomicMax(&s_last, last_pos);
-  if (seg > 0.f && excl <= target && target < incl) {
+  __syncthreads();
+  float wbefore = 0.f;
+  for (int i = 0; i < warp; ++i) wbefore += s_wsum[i];
+  const float excl = wbefore + (inc - mine);
+  if (mine > 0.f && excl <= target && target < excl + mine) {
     float run = excl;
     int pick = -1;
-#pragma unroll 1
-    for (int i = 0; i < kPerThread; ++i) {
-      if (w[i] > 0.f) {
-        pick = s0 + i;  // last positive so far: fallback if rounding runs out
+    bool done = false;
+#pragma unroll
+    for (int i = 0; i < kEach; ++i) {
+      if (!done && w[i] > 0.f) {
+        pick = q0 + i;  // last positive so far: fallback if rounding runs out
         run += w[i];
-        if (run > target) break;
+        done = run > target;
       }
     }
     if (pick >= 0) atomicMin(&s_pick, pick);
@@ -527,7 +554,7 @@ __global__ void __launch_bounds__(kThreads) verify_finish_kernel(
   __syncthreads();
   if (threadIdx.x == 0) {
     int y = s_pick;
-    if (y == INT_MAX) y = s_last >= 0 ? s_last : e0;
+    if (y == INT_MAX) y = s_last >= 0 ? s_last : seg0;
     out[b * bs + d.n] = y;
   }
 }
@@ -547,7 +574,7 @@ dflash_status run(const T* lt, const T* ld, const int32_t* x, int B, int bs, int
   const int R = greedy ? B * bs : B * bs + B * (bs - 1);
   WsCarver w(ws);
   float2* part = w.take<float2>(static_cast<size_t>(2 * B * bs) * nchunk);
-  float2* rpart = w.take<float2>(static_cast<size_t>(B) * nchunk);
+  float2* rpart = w.take<float2>(static_cast<size_t>(B) * nchunk * kSegsPerChunk);
   int* counters = w.take<int>(B);
   const float scale = greedy ? 1.f : kLog2e / Temp;
   const uint32_t k0 = static_cast<uint32_t>(seed), k1 = static_cast<uint32_t>(seed >> 32);
@@ -581,7 +608,7 @@ dflash_status run(const T* lt, const T* ld, const int32_t* x, int B, int bs, int
 size_t verify_ws_bytes(int B, int bs, int V) {
   const size_t nchunk = (static_cast<size_t>(V) + kChunk - 1) / kChunk;
   return align256(2 * static_cast<size_t>(B) * bs * nchunk * sizeof(float2)) +
-         align256(static_cast<size_t>(B) * nchunk * sizeof(float2)) +
+         align256(static_cast<size_t>(B) * nchunk * kSegsPerChunk * sizeof(float2)) +
          align256(static_cast<size_t>(B) * sizeof(int)) + 256;
 }
 
