@@ -499,12 +499,39 @@ __global__ void __launch_bounds__(kNormThreads) fuse_rownorm_kernel(
   const bool in_regs = nv <= kNormThreads * kNormSlots;
   float4 y[kNormSlots];
   float ss = 0.f;
+  if (in_regs) {
+    // slots outermost, so the loads of a thread's float4 slots are independent
+    int ns[kNormSlots];
+    int ns_max = 0;
 #pragma unroll
-  for (int i = 0; i < kNormSlots; ++i) {
-    const int v = threadIdx.x + i * kNormThreads;
-    y[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (in_regs && v < nv) y[i] = row_sum(v);
-    ss += y[i].x * y[i].x + y[i].y * y[i].y + y[i].z * y[i].z + y[i].w * y[i].w;
+    for (int i = 0; i < kNormSlots; ++i) {
+      const int v = threadIdx.x + i * kNormThreads;
+      y[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      ns[i] = v < nv ? (prow_pieces ? prow_pieces[(4 * v) / tile_cols] : k_splits) : 0;
+      ns_max = max(ns_max, ns[i]);
+      if (v < nv) y[i] = prow[v];
+    }
+    for (int s0 = 1; s0 < ns_max; s0 += 2) {
+      float4 t[2][kNormSlots];
+#pragma unroll
+      for (int u = 0; u < 2; ++u)
+#pragma unroll
+        for (int i = 0; i < kNormSlots; ++i)
+          if (s0 + u < ns[i]) t[u][i] = prow[(s0 + u) * split_stride + threadIdx.x + i * kNormThreads];
+#pragma unroll
+      for (int u = 0; u < 2; ++u)
+#pragma unroll
+        for (int i = 0; i < kNormSlots; ++i)
+          if (s0 + u < ns[i]) {
+            y[i].x += t[u][i].x;
+            y[i].y += t[u][i].y;
+            y[i].z += t[u][i].z;
+            y[i].w += t[u][i].w;
+          }
+    }
+#pragma unroll
+    for (int i = 0; i < kNormSlots; ++i)
+      ss += y[i].x * y[i].x + y[i].y * y[i].y + y[i].z * y[i].z + y[i].w * y[i].w;
   }
   if (!in_regs) {
     for (int v = threadIdx.x; v < nv; v += kNormThreads) {

@@ -121,7 +121,7 @@ __device__ __forceinline__ void load_seg(const T* __restrict__ row, int s0, int 
   for (int i = 0; i < kPerThread / VEC; ++i) {
     const int e = s0 + (i * 32 + lane) * VEC;
     live[i] = e < s1;
-    if (live[i]) v[i] = __ldcs(reinterpret_cast<const VT*>(row + e));
+    if (live[i]) v[i] = __ldcg(reinterpret_cast<const VT*>(row + e));
   }
 }
 
