@@ -47,6 +47,7 @@ constexpr int kBoxBytes = kKeys * 64 * 2;       // 128 keys x 64 dims bf16 = 16 
 constexpr int kHalfBytes = 2 * kBoxBytes;       // K (or V) of one tile: 32 KB
 constexpr int kMaxBatch = 2048;
 constexpr double kTwoPi = 6.283185307179586476925286766559;
+constexpr double kInvTwoPi = 0.15915494309189533576888376337251;
 
 struct InvFreq {
   double v[HD / 2];
@@ -84,8 +85,10 @@ __host__ __device__ __forceinline__ int n_splits(int ncache, int chunk) {
 // --------------------------------------------------------------------------
 // prologue: q^ = RoPE(RMSNorm(q) * q_gain), k^_b = RoPE(RMSNorm(kb) * k_gain)
 // --------------------------------------------------------------------------
+constexpr int kPrologueThreads = 256;
+
 template <typename T>
-__global__ void __launch_bounds__(256) attn_prologue_kernel(
+__global__ void __launch_bounds__(kPrologueThreads) attn_prologue_kernel(
     const T* __restrict__ q, const T* __restrict__ kb, const T* __restrict__ qg,
     const T* __restrict__ kg, const int32_t* __restrict__ seq_len, int B, int bs, int Hq, int Hkv,
     int cap, float eps, InvFreq inv_freq, T* __restrict__ qh, T* __restrict__ kbh,
@@ -99,7 +102,7 @@ __global__ void __launch_bounds__(256) attn_prologue_kernel(
   __shared__ float s_cos[HD / 2], s_sin[HD / 2];
   if (threadIdx.x < HD / 2) {
     double ang = static_cast<double>(pos) * inv_freq.v[threadIdx.x];
-    ang -= kTwoPi * rint(ang / kTwoPi);
+    ang -= kTwoPi * rint(ang * kInvTwoPi);
     float sv, cv;
     sincosf(static_cast<float>(ang), &sv, &cv);
     s_cos[threadIdx.x] = cv;
@@ -108,28 +111,46 @@ __global__ void __launch_bounds__(256) attn_prologue_kernel(
   __syncthreads();
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int e0 = 2 * lane;  // this lane owns elements e0, e0+1 and e0+64, e0+65
-  for (int v = warp; v < Hq + Hkv; v += 8) {
-    const bool isq = v < Hq;
-    const T* src = isq ? q + ((static_cast<size_t>(b) * Hq + v) * bs + j) * HD
-                       : kb + ((static_cast<size_t>(b) * Hkv + (v - Hq)) * bs + j) * HD;
-    T* dst = isq ? qh + ((static_cast<size_t>(b) * Hq + v) * bs + j) * HD
-                 : kbh + ((static_cast<size_t>(b) * Hkv + (v - Hq)) * bs + j) * HD;
-    const T* gain = isq ? qg : kg;
-    float x0 = to_f32<T>(src[e0]), x1 = to_f32<T>(src[e0 + 1]);
-    float y0 = to_f32<T>(src[e0 + 64]), y1 = to_f32<T>(src[e0 + 65]);
-    const float ss = warp_sum(x0 * x0 + x1 * x1 + y0 * y0 + y1 * y1);
-    const float r = rsqrtf(ss * (1.0f / HD) + eps);
-    const float g0 = gain ? to_f32<T>(gain[e0]) : 1.f, g1 = gain ? to_f32<T>(gain[e0 + 1]) : 1.f;
-    const float g2 = gain ? to_f32<T>(gain[e0 + 64]) : 1.f, g3 = gain ? to_f32<T>(gain[e0 + 65]) : 1.f;
-    x0 *= r * g0;
-    x1 *= r * g1;
-    y0 *= r * g2;
-    y1 *= r * g3;
-    const float c0 = s_cos[e0], s0 = s_sin[e0], c1 = s_cos[e0 + 1], s1 = s_sin[e0 + 1];
-    dst[e0] = from_f32<T>(x0 * c0 - y0 * s0);
-    dst[e0 + 1] = from_f32<T>(x1 * c1 - y1 * s1);
-    dst[e0 + 64] = from_f32<T>(y0 * c0 + x0 * s0);
-    dst[e0 + 65] = from_f32<T>(y1 * c1 + x1 * s1);
+  constexpr int kWarps = kPrologueThreads / 32;
+  constexpr int kBatch = 5;  // head vectors a warp loads before working on them
+  for (int v0 = warp; v0 < Hq + Hkv; v0 += kWarps * kBatch) {
+    float x[kBatch][4];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int v = v0 + u * kWarps;
+      if (v < Hq + Hkv) {
+        const bool isq = v < Hq;
+        const T* src = isq ? q + ((static_cast<size_t>(b) * Hq + v) * bs + j) * HD
+                           : kb + ((static_cast<size_t>(b) * Hkv + (v - Hq)) * bs + j) * HD;
+        x[u][0] = to_f32<T>(src[e0]);
+        x[u][1] = to_f32<T>(src[e0 + 1]);
+        x[u][2] = to_f32<T>(src[e0 + 64]);
+        x[u][3] = to_f32<T>(src[e0 + 65]);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int v = v0 + u * kWarps;
+      if (v >= Hq + Hkv) break;
+      const bool isq = v < Hq;
+      T* dst = isq ? qh + ((static_cast<size_t>(b) * Hq + v) * bs + j) * HD
+                   : kbh + ((static_cast<size_t>(b) * Hkv + (v - Hq)) * bs + j) * HD;
+      const T* gain = isq ? qg : kg;
+      float x0 = x[u][0], x1 = x[u][1], y0 = x[u][2], y1 = x[u][3];
+      const float ss = warp_sum(x0 * x0 + x1 * x1 + y0 * y0 + y1 * y1);
+      const float r = rsqrtf(ss * (1.0f / HD) + eps);
+      const float g0 = gain ? to_f32<T>(gain[e0]) : 1.f, g1 = gain ? to_f32<T>(gain[e0 + 1]) : 1.f;
+      const float g2 = gain ? to_f32<T>(gain[e0 + 64]) : 1.f, g3 = gain ? to_f32<T>(gain[e0 + 65]) : 1.f;
+      x0 *= r * g0;
+      x1 *= r * g1;
+      y0 *= r * g2;
+      y1 *= r * g3;
+      const float c0 = s_cos[e0], s0 = s_sin[e0], c1 = s_cos[e0 + 1], s1 = s_sin[e0 + 1];
+      dst[e0] = from_f32<T>(x0 * c0 - y0 * s0);
+      dst[e0 + 1] = from_f32<T>(x1 * c1 - y1 * s1);
+      dst[e0 + 64] = from_f32<T>(y0 * c0 + x0 * s0);
+      dst[e0 + 65] = from_f32<T>(y1 * c1 + x1 * s1);
+    }
   }
 }
 
@@ -496,17 +517,26 @@ __global__ void __launch_bounds__(TcCfg<NC>::kThreads, 1) attn_tc_kernel(const _
     tmem_relinquish();
   }
   if (warp == C::kProdWarp) {  // per-sequence lengths and the prefix of full (non-last) splits
-    for (int b = lane; b < p.B; b += 32) s_n[b] = clamp_seq(p.seq_len[b], p.cap, p.status);
-    __syncwarp();
-    if (lane == 0) {
-      int acc = 0;
-      for (int b = 0; b < p.B; ++b) {
-        s_prefix[b] = acc;
-        const int first = p.window > 0 ? max(0, s_n[b] - p.window) : 0;
-        acc += (n_splits(s_n[b] - first, p.chunk) - 1) * p.Hkv;
+    int carry = 0;
+    for (int b0 = 0; b0 < p.B; b0 += 32) {  // a warp scan per 32 sequences
+      const int b = b0 + lane;
+      int cnt = 0;
+      if (b < p.B) {
+        const int n = clamp_seq(p.seq_len[b], p.cap, p.status);
+        s_n[b] = n;
+        const int first = p.window > 0 ? max(0, n - p.window) : 0;
+        cnt = (n_splits(n - first, p.chunk) - 1) * p.Hkv;
       }
-      s_prefix[p.B] = acc;
+      int inc = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += u;
+      }
+      if (b < p.B) s_prefix[b] = carry + inc - cnt;
+      carry += __shfl_sync(0xffffffffu, inc, 31);
     }
+    if (lane == 0) s_prefix[p.B] = carry;
   }
   tc_fence_before_sync();
   __syncthreads();
@@ -982,7 +1012,7 @@ dflash_status launch_block_attn(int layer, int B, int bs, int Hq, const void* q,
   if (c.dtype == DFLASH_F32) {
     float* qh = w.take<float>(static_cast<size_t>(B) * Hq * bs * HD);
     float* kbh = w.take<float>(static_cast<size_t>(B) * Hkv * bs * HD);
-    attn_prologue_kernel<float><<<B * bs, 256, 0, st>>>(
+    attn_prologue_kernel<float><<<B * bs, kPrologueThreads, 0, st>>>(
         static_cast<const float*>(q), static_cast<const float*>(kb), static_cast<const float*>(qg),
         static_cast<const float*>(kg), c.seq_len, B, bs, Hq, Hkv, c.capacity, eps, inv, qh, kbh, nullptr, 0,
         dev.status);
@@ -1032,7 +1062,7 @@ dflash_status launch_block_attn(int layer, int B, int bs, int Hq, const void* q,
   if (!s) s = make_tmap_bf16_2d(&maps.vb, vb, static_cast<uint64_t>(B) * Hkv * bs, HD, kBlockBoxRows, 64);
   if (s) return s;
 
-  attn_prologue_kernel<__nv_bfloat16><<<B * bs, 256, 0, st>>>(
+  attn_prologue_kernel<__nv_bfloat16><<<B * bs, kPrologueThreads, 0, st>>>(
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(kb),
       static_cast<const __nv_bfloat16*>(qg), static_cast<const __nv_bfloat16*>(kg), c.seq_len, B, bs, Hq, Hkv,
       c.capacity, eps, inv, qh, kbh, p.counters, 1 + B * Hkv, dev.status);

@@ -44,6 +44,7 @@ constexpr int kBK = 64;
 constexpr int kGemmThreads = 192;  // warp 0: TMA producer, warp 1: MMA issuer, warps 2-5: epilogue
 constexpr int kMaxSeg = 8;
 constexpr double kTwoPi = 6.283185307179586476925286766559;
+constexpr double kInvTwoPi = 0.15915494309189533576888376337251;
 constexpr int kSplitTarget = 152;  // work units aimed for when splitting K (one per SM)
 
 struct InvFreq {
@@ -468,7 +469,7 @@ __global__ void __launch_bounds__(kNormThreads) fuse_rownorm_kernel(
     const int pos = valid ? n + t : 0;
     if (threadIdx.x < HD / 2) {
       double ang = static_cast<double>(pos) * inv.v[threadIdx.x];
-      ang -= kTwoPi * rint(ang / kTwoPi);
+      ang -= kTwoPi * rint(ang * kInvTwoPi);
       float sv, cv;
       sincosf(static_cast<float>(ang), &sv, &cv);
       rope_cs[static_cast<size_t>(threadIdx.x) * M + m] = make_float2(cv, sv);
