@@ -270,9 +270,10 @@ struct TcLayout {
 };
 
 __host__ __device__ inline int tc_misc_bytes(int B, int nc) {
-  // tmem slot + item ring (64) | s_m [2][NC] | s_l [2][4][NC] | s_red [2 halves][2][4][32] |
-  // prefix [B+1], n [B]
-  return 64 + 2 * nc * 4 + 2 * 4 * nc * 4 + 2 * 2 * 4 * 32 * 4 + (2 * B + 1) * 4;
+  // tmem slot (64) | s_m [2][NC] | s_l [2][4][NC] | s_red [2 halves][2][4][32] |
+  // prefix [B+1], n [B] | decoded item ring [kItemRing]
+  return 64 + 2 * nc * 4 + 2 * 4 * nc * 4 + 2 * 2 * 4 * 32 * 4 + (2 * B + 1) * 4 +
+         kItemRing * static_cast<int>(sizeof(Item));
 }
 
 __host__ __device__ inline TcLayout tc_layout(int nc, int B, int smem_limit) {
@@ -393,14 +394,15 @@ struct Ring {
 };
 
 // Reads the next work item from the shared item ring (-1 = no more work).
-__device__ __forceinline__ int next_item(uint32_t it_full, uint32_t it_empty, const int* s_item, Ring& r,
-                                         unsigned* status) {
-  if (!mbar_wait(it_full + 8 * r.idx, r.phase, status)) return -1;
-  const int w = s_item[r.idx];
+// The next work item, decoded once by the producer (b < 0: the queue is empty).
+__device__ __forceinline__ bool next_item(uint32_t it_full, uint32_t it_empty, const Item* s_items, Ring& r,
+                                          unsigned* status, Item& it) {
+  if (!mbar_wait(it_full + 8 * r.idx, r.phase, status)) return false;
+  it = s_items[r.idx];
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbar_arrive(it_empty + 8 * r.idx);
   r.next(kItemRing);
-  return w;
+  return it.b >= 0;
 }
 
 // Sum over the warp's 32 lanes of each v[j] (N = 16 or 32 values); lane i
@@ -476,12 +478,12 @@ __global__ void __launch_bounds__(TcCfg<NC>::kThreads, 1) attn_tc_kernel(const _
   const uint32_t it_full = ml_empty + 16, it_empty = it_full + 8 * kItemRing;
   const uint32_t red_bar = it_empty + 8 * kItemRing;  // one per column half
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + lay.off_misc);
-  int* s_item = reinterpret_cast<int*>(tmem_slot + 8);                           // kItemRing entries
   float* s_m = reinterpret_cast<float*>(gbase + lay.off_misc + 64);               // [2][NC]
   float* s_l = s_m + 2 * NC;                                                       // [2][4][NC]
   float* s_red = s_l + 2 * 4 * NC;                                                 // [2 halves][2][4][32]
   int* s_prefix = reinterpret_cast<int*>(s_red + 2 * 2 * 4 * 32);
   int* s_n = s_prefix + (p.B + 1);
+  Item* s_items = reinterpret_cast<Item*>(s_n + p.B);                              // kItemRing entries
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
@@ -557,12 +559,14 @@ __global__ void __launch_bounds__(TcCfg<NC>::kThreads, 1) attn_tc_kernel(const _
       bool ok = true;
       while (ok) {
         const int w = atomicAdd(p.counters, 1);
+        Item it;
+        it.b = -1;
+        if (w < n_items) it = decode_item(w, s_prefix, s_n, p);
         if (!(ok = mbar_wait(it_empty + 8 * itr.idx, itr.phase ^ 1u, p.status))) break;
-        s_item[itr.idx] = w < n_items ? w : -1;
+        s_items[itr.idx] = it;  // decoded once here, read by every role
         mbar_arrive(it_full + 8 * itr.idx);
         itr.next(kItemRing);
         if (w >= n_items) break;
-        const Item it = decode_item(w, s_prefix, s_n, p);
         if (!(ok = mbar_wait(q_empty + 8 * q.idx, q.phase ^ 1u, p.status))) break;
         mbar_arrive_expect_tx(q_full + 8 * q.idx, 2 * C::kQBoxBytes);
         const int qrow = (it.b * p.Hq + it.g * p.G) * p.bs;
@@ -608,11 +612,10 @@ __global__ void __launch_bounds__(TcCfg<NC>::kThreads, 1) attn_tc_kernel(const _
       bool ok = true;
       while (ok) {
         if (!(ok = mbar_wait(it_full + 8 * itr.idx, itr.phase, p.status))) break;
-        const int w = s_item[itr.idx];
+        const Item it = s_items[itr.idx];
         mbar_arrive(it_empty + 8 * itr.idx);
         itr.next(kItemRing);
-        if (w < 0) break;
-        const Item it = decode_item(w, s_prefix, s_n, p);
+        if (it.b < 0) break;
         if (!(ok = mbar_wait(q_full + 8 * q.idx, q.phase, p.status))) break;
         const uint32_t qb = base + lay.off_q + q.idx * 2 * C::kQBoxBytes;
         for (int t = 0; t < it.nt && ok; ++t) {
@@ -643,11 +646,10 @@ __global__ void __launch_bounds__(TcCfg<NC>::kThreads, 1) attn_tc_kernel(const _
       bool ok = true;
       while (ok) {
         if (!(ok = mbar_wait(it_full + 8 * itr.idx, itr.phase, p.status))) break;
-        const int w = s_item[itr.idx];
+        const Item it = s_items[itr.idx];
         mbar_arrive(it_empty + 8 * itr.idx);
         itr.next(kItemRing);
-        if (w < 0) break;
-        const Item it = decode_item(w, s_prefix, s_n, p);
+        if (it.b < 0) break;
         const uint32_t od = tmem + C::kColO + 2 * NC * o.idx;
         for (int t = 0; t < it.nt && ok; ++t) {
           if (!(ok = mbar_wait(p_full + 8 * pr.idx, pr.phase, p.status))) break;
@@ -693,9 +695,8 @@ __global__ void __launch_bounds__(TcCfg<NC>::kThreads, 1) attn_tc_kernel(const _
     int pcnt[2] = {0, 0};
     bool ok = true;
     while (ok) {
-      const int w = next_item(it_full, it_empty, s_item, itr, p.status);
-      if (w < 0) break;
-      const Item it = decode_item(w, s_prefix, s_n, p);
+      Item it;
+      if (!next_item(it_full, it_empty, s_items, itr, p.status, it)) break;
       float m[CW], l[CW];
       float dmax = -INFINITY;  // largest score above m over the item's later tiles
       for (int t = 0; t < it.nt; ++t) {
@@ -821,9 +822,8 @@ __global__ void __launch_bounds__(TcCfg<NC>::kThreads, 1) attn_tc_kernel(const _
     Ring orr, mlr, itr;
     bool ok = true;
     while (ok) {
-      const int w = next_item(it_full, it_empty, s_item, itr, p.status);
-      if (w < 0) break;
-      const Item it = decode_item(w, s_prefix, s_n, p);
+      Item it;
+      if (!next_item(it_full, it_empty, s_items, itr, p.status, it)) break;
       if (!(ok = mbar_wait(o_full + 8 * orr.idx, orr.phase, p.status))) break;
       tc_fence_after_sync();
       float o[NC];  // O^T lane `dim`: the hi and lo column blocks added

@@ -155,3 +155,40 @@ def test_block_attn_bad_seq_len_is_flagged_not_faulted():
     ref = _oracle(q[:1], kb[:1], vb[:1], qg, kg, k[0, :1], v[0, :1], [100], 0, torch.bfloat16)
     assert rel_fro(out[:1], ref) <= TOL[torch.bfloat16]
     assert torch.isfinite(out.float()).all()
+
+
+def test_block_attn_split_count_does_not_change_the_result():
+    """One 3000-token sequence in a 65536-row cache: with the full cache the
+    keys are cut into 512-key splits (6 of them), with a 40000-key window
+    (longer than the sequence, so the same keys) into 384-key splits (8).  Both
+    outputs match the oracle and each other to a few bf16 ulps."""
+    seq = [3000]
+    cap = 65536
+    k, v, q, kb, vb, qg, kg = _inputs(1, 8, cap, torch.bfloat16, seed=91, layers=1)
+    cache = dfl.KVCache(k.to(DEV), v.to(DEV), torch.tensor(seq, dtype=torch.int32, device=DEV))
+    args = (q.to(DEV), kb.to(DEV), vb.to(DEV), qg.to(DEV), kg.to(DEV), cache)
+    out_full = dfl.block_attn(0, *args, window=0)
+    out_win = dfl.block_attn(0, *args, window=40000)
+    ref = _oracle(q, kb, vb, qg, kg, k[0], v[0], seq, 0, torch.bfloat16)
+    for out in (out_full, out_win):
+        assert rel_fro(out, ref) <= TOL[torch.bfloat16], (rel_fro(out, ref), max_abs(out, ref))
+    assert rel_fro(out_full, out_win.float().cpu().numpy()) <= 2e-3
+
+
+def test_block_attn_is_invariant_to_the_order_of_cached_rows():
+    """Permuting a sequence's cached (key, value) rows together leaves the
+    output unchanged up to summation order."""
+    seq = [900, 400]
+    cap = 1024
+    k, v, q, kb, vb, qg, kg = _inputs(2, 8, cap, torch.bfloat16, seed=93, layers=1)
+    perm = torch.from_numpy(np.random.default_rng(5).permutation(seq[0]))
+    kp, vp = k.clone(), v.clone()
+    kp[0, 0, :, :seq[0]] = k[0, 0][:, perm]
+    vp[0, 0, :, :seq[0]] = v[0, 0][:, perm]
+    sl = torch.tensor(seq, dtype=torch.int32, device=DEV)
+    a = dfl.block_attn(0, q.to(DEV), kb.to(DEV), vb.to(DEV), qg.to(DEV), kg.to(DEV),
+                       dfl.KVCache(k.to(DEV), v.to(DEV), sl))
+    b = dfl.block_attn(0, q.to(DEV), kb.to(DEV), vb.to(DEV), qg.to(DEV), kg.to(DEV),
+                       dfl.KVCache(kp.to(DEV), vp.to(DEV), sl))
+    assert rel_fro(a, b.float().cpu().numpy()) <= 2e-3
+    assert torch.equal(a[1], b[1])     # the other sequence is untouched bit for bit

@@ -197,3 +197,20 @@ def test_attention_is_non_causal_and_ignores_stale_cache():
     c4["cache_v"][0, :, :5] = 1e3
     np.testing.assert_array_equal(oracle.block_attn(**c4, window=4), oracle.block_attn(**c, window=4))
     assert np.abs(oracle.block_attn(**c4, window=5) - oracle.block_attn(**c, window=5)).max() > 1.0
+
+
+def test_attention_is_invariant_to_the_order_of_cached_rows():
+    """Softmax attention is a sum over keys: permuting the cached (key, value)
+    rows of a sequence together leaves the output unchanged; permuting the keys
+    alone (values left in place) does not."""
+    c = _attn_case(4)
+    base = oracle.block_attn(**c)
+    n = c["seq_len"][0]
+    perm = _perm(n, 11)
+    c2 = {k: v.copy() for k, v in c.items()}
+    c2["cache_k"][0, :, :n] = c["cache_k"][0][:, perm]
+    c2["cache_v"][0, :, :n] = c["cache_v"][0][:, perm]
+    np.testing.assert_allclose(oracle.block_attn(**c2), base, rtol=1e-12, atol=1e-12)
+    c3 = {k: v.copy() for k, v in c.items()}
+    c3["cache_k"][0, :, :n] = c["cache_k"][0][:, perm]
+    assert np.abs(oracle.block_attn(**c3)[0] - base[0]).max() > 1e-3
