@@ -65,7 +65,8 @@ struct AttnParams {
   const __nv_bfloat16* ck;   // this cache's K and V, [L, B, Hkv, cap, 128]
   const __nv_bfloat16* cv;
   float scale_log2;          // log2(e) / sqrt(128)
-  int* counters;             // [1 + B * Hkv]: work-queue counter, then one flag per (b, g)
+  int* counters;             // [1 + 2 B Hkv]: work-queue counter, a flag per (b, g), then per (b, g) the
+                             // count of epilogue warps (4 per split) that finished writing
                              // whose scores outgrew the running max (cleared by the prologue)
   unsigned* status;
 };
@@ -336,8 +337,11 @@ __device__ void attn_row_exact(const AttnParams& p, int b, int g, int row, int f
 // Per output row (one warp, 4 dims per lane): the log-sum-exp merge of the
 // split partials of a (sequence, KV head) with more than one split, or the
 // exact recomputation of a (sequence, KV head) the main kernel flagged.
+// Launched as a programmatic dependent of the main kernel but without waiting
+// for its whole grid: a warp starts on (b, g) as soon as the main kernel's
+// epilogue warps have written all of its splits (a counter per pair, four
+// arrivals per split), so the merges overlap the main kernel's last items.
 __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnParams p) {
-  pdl_wait_primary();
   const int gw = blockIdx.x * 8 + threadIdx.x / 32;   // global warp = (b, g, row)
   const int lane = threadIdx.x % 32;
   const int row = gw % p.rows;
@@ -346,15 +350,19 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnParams p) {
   const int b = bg / p.Hkv, g = bg % p.Hkv;
   const int n = min(max(p.seq_len[b], 0), p.cap);
   const int first = p.window > 0 ? max(0, n - p.window) : 0;
-  if (p.counters[1 + bg] != 0) {
+  const int nsplit = n_splits(n - first, p.chunk);
+  bool ready = true;
+  if (lane == 0) ready = wait_counter_at_least(p.counters + 1 + p.B * p.Hkv + bg, 4 * nsplit, p.status);
+  if (!__shfl_sync(0xffffffffu, ready ? 1 : 0, 0)) return;
+  if (__ldcg(p.counters + 1 + bg) != 0) {
     attn_row_exact(p, b, g, row, first, n);
     return;
   }
-  const int ns = n_splits(n - first, p.chunk);
+  const int ns = nsplit;
   if (ns <= 1) return;
   const size_t r0 = static_cast<size_t>(bg) * p.max_splits * p.rows + row;
   float M = -INFINITY;
-  for (int s = lane; s < ns; s += 32) M = fmaxf(M, p.mlpart[r0 + static_cast<size_t>(s) * p.rows].x);
+  for (int s = lane; s < ns; s += 32) M = fmaxf(M, __ldcg(p.mlpart + r0 + static_cast<size_t>(s) * p.rows).x);
   M = warp_max(M);
   const float Mu = M == -INFINITY ? 0.f : M;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -362,8 +370,8 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnParams p) {
 #pragma unroll 8
   for (int s = 0; s < ns; ++s) {
     const size_t r = r0 + static_cast<size_t>(s) * p.rows;
-    const float2 ml = p.mlpart[r];
-    const float4 o = reinterpret_cast<const float4*>(p.opart + r * HD)[lane];
+    const float2 ml = __ldcg(p.mlpart + r);  // written by other SMs during this kernel
+    const float4 o = __ldcg(reinterpret_cast<const float4*>(p.opart + r * HD) + lane);
     const float f = ml.y * exp2f(ml.x - Mu);
     den += f;
     acc.x += f * o.x;
@@ -872,8 +880,12 @@ __global__ void __launch_bounds__(TcCfg<NC>::kThreads, 1) attn_tc_kernel(const _
           }
         }
       }
+      __threadfence();  // this warp's output / partial before the pair's completion count
       __syncwarp();
-      if (lane == 0) mbar_arrive(ml_empty + 8 * mlr.idx);
+      if (lane == 0) {
+        mbar_arrive(ml_empty + 8 * mlr.idx);
+        atomicAdd(p.counters + 1 + p.B * p.Hkv + it.b * p.Hkv + it.g, 1);
+      }
       mlr.next(2);
     }
   }
@@ -995,7 +1007,7 @@ size_t attn_ws_bytes(int B, int bs, int Hq, int Hkv, int cap, int window, dflash
   if (dt == DFLASH_BF16)
     s += align256(static_cast<size_t>(B) * Hkv * max_splits * rows * HD * sizeof(float)) +
          align256(static_cast<size_t>(B) * Hkv * max_splits * rows * sizeof(float2)) +
-         align256((1 + static_cast<size_t>(B) * Hkv) * sizeof(int));
+         align256((1 + 2 * static_cast<size_t>(B) * Hkv) * sizeof(int));
   return s + 256;
 }
 
@@ -1046,7 +1058,7 @@ dflash_status launch_block_attn(int layer, int B, int bs, int Hq, const void* q,
   p.out = static_cast<__nv_bfloat16*>(out);
   p.opart = w.take<float>(static_cast<size_t>(B) * Hkv * p.max_splits * p.rows * HD);
   p.mlpart = w.take<float2>(static_cast<size_t>(B) * Hkv * p.max_splits * p.rows);
-  p.counters = w.take<int>(1 + static_cast<size_t>(B) * Hkv);
+  p.counters = w.take<int>(1 + 2 * static_cast<size_t>(B) * Hkv);
   p.ck = static_cast<const __nv_bfloat16*>(c.k);
   p.cv = static_cast<const __nv_bfloat16*>(c.v);
   p.scale_log2 = 1.4426950408889634f * scale;
@@ -1065,7 +1077,7 @@ dflash_status launch_block_attn(int layer, int B, int bs, int Hq, const void* q,
   attn_prologue_kernel<__nv_bfloat16><<<B * bs, kPrologueThreads, 0, st>>>(
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(kb),
       static_cast<const __nv_bfloat16*>(qg), static_cast<const __nv_bfloat16*>(kg), c.seq_len, B, bs, Hq, Hkv,
-      c.capacity, eps, inv, qh, kbh, p.counters, 1 + B * Hkv, dev.status);
+      c.capacity, eps, inv, qh, kbh, p.counters, 1 + 2 * B * Hkv, dev.status);
 
   const TcLayout lay = tc_layout(nc, B, static_cast<int>(dev.max_smem_optin));
   if (lay.nk < 1 || lay.nv < 1 || lay.bytes > static_cast<int>(dev.max_smem_optin))

@@ -32,6 +32,16 @@ __device__ __forceinline__ void raise_status(unsigned* status, unsigned bits) {
   if (status) atomicOr(status, bits);
 }
 
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Spin (bounded) until *counter >= target; false after kWaitLimitNs with
+// DFLASH_DEV_TIMEOUT raised.  Defined below kWaitLimitNs.
+__device__ __forceinline__ bool wait_counter_at_least(const int* counter, int target, unsigned* status);
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -84,6 +94,19 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 
 // Wait for the phase with the given parity to complete.  Bounded: after
 // kWaitLimitNs it raises DFLASH_DEV_TIMEOUT and returns false.
+__device__ __forceinline__ bool wait_counter_at_least(const int* counter, int target, unsigned* status) {
+  if (ld_acquire_gpu(counter) >= target) return true;
+  const unsigned long long t0 = global_timer_ns();
+  while (ld_acquire_gpu(counter) < target) {
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      raise_status(status, DFLASH_DEV_TIMEOUT);
+      return false;
+    }
+    __nanosleep(256);
+  }
+  return true;
+}
+
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* status) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();

@@ -101,6 +101,18 @@ __device__ __forceinline__ void unit_coords(int u, const GemmArgs& p, int& m, in
   kb1 = static_cast<int>((static_cast<long>(ks + 1) * p.num_kb) / p.k_splits);
 }
 
+// The i-th K block a unit of N tile n works on: the range [kb0, kb1) rotated by
+// a start spread over the N tiles, so the CTAs that share A blocks (the same
+// rows, other N tiles) do not all request the same block at the same time.
+// The sum is the same; only its rounding order differs.
+__device__ __forceinline__ int kb_at(int i, int kb0, int kb1, int n, const GemmArgs& p) {
+  const int nk = kb1 - kb0;
+  const int rot = static_cast<int>((static_cast<long>(n) * nk) / p.n_tiles);
+  int j = i + rot;
+  if (j >= nk) j -= nk;
+  return kb0 + j;
+}
+
 // The pieces of work of this CTA, in order.  Plain schedule: units
 // blockIdx.x, blockIdx.x + gridDim.x, ... (a unit: one tile over one K split,
 // its partial sum in slot = split index).  Stream-K schedule: the first
@@ -318,9 +330,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
       int m, n, kb0, kb1, ks;
       if (p.pdl && first.next(p, m, n, kb0, kb1, ks)) {
         for (; pre < STAGES && kb0 + pre < kb1; ++pre) {
+          const int kbp = kb_at(pre, kb0, kb1, n, p);
           const uint32_t fb = full0 + 8 * pre;
           mbar_arrive_expect_tx(fb, STAGE);
-          tma_load_2d(base + pre * STAGE + MT * A_BYTES, &bmap, fb, (kb0 + pre) * kBK, n * BN);
+          tma_load_2d(base + pre * STAGE + MT * A_BYTES, &bmap, fb, kbp * kBK, n * BN);
         }
       }
       pdl_wait_primary();
@@ -329,16 +342,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
       bool ok = true;
       Pieces pcs(p);
       for (bool head = true; ok && pcs.next(p, m, n, kb0, kb1, ks); head = false) {
-        for (int kb = kb0; kb < kb1; ++kb) {
-          const bool b_done = head && kb - kb0 < pre;
+        for (int i = 0; i < kb1 - kb0; ++i) {
+          const int kb = kb_at(i, kb0, kb1, n, p);
+          const bool b_done = head && i < pre;
           if (!b_done && !(ok = mbar_wait(empty0 + 8 * stage, phase ^ 1u, p.status))) break;
           const uint32_t fb = full0 + 8 * stage;
           if (!b_done) mbar_arrive_expect_tx(fb, STAGE);
           const uint32_t sa = base + stage * STAGE;
           const int seg = kb / p.kb_per_seg;
 #pragma unroll
-          for (int i = 0; i < MT; ++i)
-            tma_load_2d(sa + i * A_BYTES, &amaps.a[seg], fb, (kb - seg * p.kb_per_seg) * kBK, (m * MT + i) * kBM);
+          for (int mt = 0; mt < MT; ++mt)
+            tma_load_2d(sa + mt * A_BYTES, &amaps.a[seg], fb, (kb - seg * p.kb_per_seg) * kBK, (m * MT + mt) * kBM);
           if (!b_done) tma_load_2d(sa + MT * A_BYTES, &bmap, fb, kb * kBK, n * BN);
           if (++stage == STAGES) {
             stage = 0;
@@ -360,17 +374,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
         if (!(ok = mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1u, p.status))) break;
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
-        for (int kb = kb0; kb < kb1; ++kb) {
+        for (int i = 0; i < kb1 - kb0; ++i) {
           if (!(ok = mbar_wait(full0 + 8 * stage, phase, p.status))) break;
           tc_fence_after_sync();
           const uint32_t sa = base + stage * STAGE;
           const uint64_t bd = umma_desc_kmajor_sw128(sa + MT * A_BYTES);
 #pragma unroll
-          for (int i = 0; i < MT; ++i) {
-            const uint64_t ad = umma_desc_kmajor_sw128(sa + i * A_BYTES);
+          for (int mt = 0; mt < MT; ++mt) {
+            const uint64_t ad = umma_desc_kmajor_sw128(sa + mt * A_BYTES);
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k)
-              umma_bf16(d_tmem + i * BN, ad + 2 * k, bd + 2 * k, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
+              umma_bf16(d_tmem + mt * BN, ad + 2 * k, bd + 2 * k, IDESC, (i > 0 || k > 0) ? 1u : 0u);
           }
           umma_commit(empty0 + 8 * stage);
           if (++stage == STAGES) {
