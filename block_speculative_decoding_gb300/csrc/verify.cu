@@ -125,9 +125,17 @@ __device__ __forceinline__ void load_seg(const T* __restrict__ row, int s0, int 
   }
 }
 
+// Resident CTAs per SM of the stats pass: six for the bf16 sampling pass (40
+// registers, 48 KB of loads in flight per SM more than with four), four where
+// more live values would spill.
+template <typename T, int VEC, bool GREEDY>
+constexpr int stats_ctas_per_sm() {
+  return (sizeof(T) == 2 && VEC == 8 && !GREEDY) ? 6 : 4;
+}
+
 // The stats pass zeroes the per-sequence counters of the finish kernel.
 template <typename T, int VEC, bool GREEDY>
-__global__ void __launch_bounds__(kThreads, 4) verify_stats_kernel(const T* __restrict__ lt,
+__global__ void __launch_bounds__(kThreads, (stats_ctas_per_sm<T, VEC, GREEDY>())) verify_stats_kernel(const T* __restrict__ lt,
                                                                    const T* __restrict__ ld, int B,
                                                                    int bs, int V, int nchunk,
                                                                    float scale,
