@@ -95,6 +95,10 @@ __global__ void __launch_bounds__(kPrologueThreads) attn_prologue_kernel(
     int cap, float eps, InvFreq inv_freq, T* __restrict__ qh, T* __restrict__ kbh,
     int* __restrict__ counters, int n_counters, unsigned* status) {
   pdl_launch_dependents();
+  // Launched as a programmatic dependent of whatever precedes it in the stream
+  // (its CTAs become resident early): nothing is read or written before the
+  // preceding grid has completed.
+  pdl_wait_primary();
   if (blockIdx.x == 0 && counters)
     for (int i = threadIdx.x; i < n_counters; i += blockDim.x) counters[i] = 0;
   const int b = blockIdx.x / bs, j = blockIdx.x % bs;
@@ -342,6 +346,7 @@ __device__ void attn_row_exact(const AttnParams& p, int b, int g, int row, int f
 // epilogue warps have written all of its splits (a counter per pair, four
 // arrivals per split), so the merges overlap the main kernel's last items.
 __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnParams p) {
+  pdl_launch_dependents();  // a following call's first kernel may become resident; it waits for this grid
   const int gw = blockIdx.x * 8 + threadIdx.x / 32;   // global warp = (b, g, row)
   const int lane = threadIdx.x % 32;
   const int row = gw % p.rows;
@@ -1074,10 +1079,23 @@ dflash_status launch_block_attn(int layer, int B, int bs, int Hq, const void* q,
   if (!s) s = make_tmap_bf16_2d(&maps.vb, vb, static_cast<uint64_t>(B) * Hkv * bs, HD, kBlockBoxRows, 64);
   if (s) return s;
 
-  attn_prologue_kernel<__nv_bfloat16><<<B * bs, kPrologueThreads, 0, st>>>(
-      static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(kb),
-      static_cast<const __nv_bfloat16*>(qg), static_cast<const __nv_bfloat16*>(kg), c.seq_len, B, bs, Hq, Hkv,
-      c.capacity, eps, inv, qh, kbh, p.counters, 1 + 2 * B * Hkv, dev.status);
+  {
+    cudaLaunchConfig_t pc = {};
+    pc.gridDim = dim3(static_cast<unsigned>(B * bs));
+    pc.blockDim = dim3(kPrologueThreads);
+    pc.stream = st;
+    cudaLaunchAttribute pa[1];
+    pa[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pa[0].val.programmaticStreamSerializationAllowed = 1;
+    pc.attrs = pa;
+    pc.numAttrs = 1;
+    cudaError_t le = cudaLaunchKernelEx(&pc, attn_prologue_kernel<__nv_bfloat16>,
+                                        static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(kb),
+                                        static_cast<const __nv_bfloat16*>(qg), static_cast<const __nv_bfloat16*>(kg),
+                                        c.seq_len, B, bs, Hq, Hkv, c.capacity, eps, inv, qh, kbh, p.counters,
+                                        1 + 2 * B * Hkv, dev.status);
+    if (le != cudaSuccess) return cuda_fail(le, "attn_prologue_kernel launch");
+  }
 
   const TcLayout lay = tc_layout(nc, B, static_cast<int>(dev.max_smem_optin));
   if (lay.nk < 1 || lay.nv < 1 || lay.bytes > static_cast<int>(dev.max_smem_optin))

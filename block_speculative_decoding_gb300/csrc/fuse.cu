@@ -62,7 +62,8 @@ struct GemmArgs {
   int dp_tiles;            // stream_k: leading tiles scheduled whole, a multiple of the share count
   int* pieces;             // stream_k: [m_tiles * n_tiles] number of slots written for the tile
   int epi;                 // 0: fp32 partial store, 1: K/V cache epilogue
-  int pdl;                 // launched as a programmatic dependent: A comes from the previous kernel
+  int pdl;                 // launched as a programmatic dependent (waits for the preceding grid before any load)
+  int prefetch_b;          // the B operand (weights) may be loaded before that wait
   float* out_f32;          // epi 0: [k_splits][M][N]
   __nv_bfloat16* cache_k;  // epi 1
   __nv_bfloat16* cache_v;
@@ -328,7 +329,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
       int pre = 0;
       Pieces first(p);
       int m, n, kb0, kb1, ks;
-      if (p.pdl && first.next(p, m, n, kb0, kb1, ks)) {
+      if (p.prefetch_b && first.next(p, m, n, kb0, kb1, ks)) {
         for (; pre < STAGES && kb0 + pre < kb1; ++pre) {
           const int kbp = kb_at(pre, kb0, kb1, n, p);
           const uint32_t fb = full0 + 8 * pre;
@@ -819,6 +820,7 @@ dflash_status launch_fuse_context(int J, const void* const* taps, int dt_width, 
   a.m_tiles = f.fuse_m_tiles;
   a.n_tiles = f.fuse_n_tiles;
   a.epi = 0;
+  a.pdl = 1;  // its CTAs may start while the preceding kernel finishes; nothing is loaded before it has
   a.out_f32 = Ypart;
   a.status = dev.status;
   s = f.fuse_mt == 2 ? launch_gemm<128, 4, 2>(am, bm, a, st, dev) : launch_gemm<256, 4, 1>(am, bm, a, st, dev);
@@ -862,6 +864,7 @@ dflash_status launch_fuse_context(int J, const void* const* taps, int dt_width, 
   k.n_tiles = Ntot / f.kv_bn;
   k.epi = 1;
   k.pdl = 1;
+  k.prefetch_b = 1;
   k.cache_k = static_cast<__nv_bfloat16*>(c.k);
   k.cache_v = static_cast<__nv_bfloat16*>(c.v);
   k.L = L;

@@ -142,6 +142,9 @@ __global__ void __launch_bounds__(kThreads, (stats_ctas_per_sm<T, VEC, GREEDY>()
                                                                    float2* __restrict__ part,
                                                                    int* __restrict__ counters) {
   pdl_launch_dependents();
+  // launched as a programmatic dependent of the preceding kernel: nothing is
+  // read or written before that grid has completed
+  pdl_wait_primary();
   if (blockIdx.x == 0 && counters)
     for (int i = threadIdx.x; i < B; i += kThreads) counters[i] = 0;
   const int c = blockIdx.x % nchunk;
@@ -331,6 +334,7 @@ template <typename T>
 __global__ void __launch_bounds__(128) verify_decide_kernel(
     const T* __restrict__ lt, const int32_t* __restrict__ x, int B, int bs, int V, int nchunk,
     const float2* __restrict__ part, int32_t* __restrict__ acc, int32_t* __restrict__ out, unsigned* status) {
+  pdl_launch_dependents();
   const int b = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   if (b >= B) return;
   decide_seq<T, true>(lt, lt, x, b, B, bs, V, nchunk, 1.f, part, 0u, 0u, 0u, 0u, acc, out, status);
@@ -366,6 +370,7 @@ __global__ void __launch_bounds__(kThreads, 2) verify_finish_kernel(
     int nchunk, float scale, const float2* __restrict__ part, uint32_t k0, uint32_t k1, uint32_t c_lo,
     uint32_t c_hi, int32_t* __restrict__ acc, int32_t* __restrict__ out, float2* __restrict__ rpart,
     int* __restrict__ counters, unsigned* status) {
+  pdl_launch_dependents();  // a following call's first kernel may become resident; it waits for this grid
   const int ncb = (nchunk + kFinishChunks - 1) / kFinishChunks;  // CTAs per sequence
   const int b = blockIdx.x / ncb, cb = blockIdx.x % ncb;
   // the draft tokens' logits do not depend on the stats pass: load them first
@@ -588,18 +593,28 @@ dflash_status run(const T* lt, const T* ld, const int32_t* x, int B, int bs, int
   const uint32_t k0 = static_cast<uint32_t>(seed), k1 = static_cast<uint32_t>(seed >> 32);
   const uint32_t c0 = static_cast<uint32_t>(cycle), c1 = static_cast<uint32_t>(cycle >> 32);
   const unsigned g1 = static_cast<unsigned>(nchunk) * static_cast<unsigned>(R);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t sc = {};  // the stats pass, a programmatic dependent of the preceding kernel
+  sc.gridDim = dim3(g1);
+  sc.blockDim = dim3(kThreads);
+  sc.stream = st;
+  sc.attrs = attr;
+  sc.numAttrs = 1;
   if (greedy) {
-    verify_stats_kernel<T, VEC, true><<<g1, kThreads, 0, st>>>(lt, ld, B, bs, V, nchunk, scale, part, nullptr);
+    cudaError_t le = cudaLaunchKernelEx(&sc, verify_stats_kernel<T, VEC, true>, lt, ld, B, bs, V, nchunk, scale, part,
+                                        static_cast<int*>(nullptr));
+    if (le != cudaSuccess) return cuda_fail(le, "verify_stats_kernel launch");
     verify_decide_kernel<T><<<(B + 3) / 4, 128, 0, st>>>(lt, x, B, bs, V, nchunk, part, acc, out, dev.status);
   } else {
-    verify_stats_kernel<T, VEC, false><<<g1, kThreads, 0, st>>>(lt, ld, B, bs, V, nchunk, scale, part, counters);
+    cudaError_t le0 = cudaLaunchKernelEx(&sc, verify_stats_kernel<T, VEC, false>, lt, ld, B, bs, V, nchunk, scale, part,
+                                         counters);
+    if (le0 != cudaSuccess) return cuda_fail(le0, "verify_stats_kernel launch");
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>((nchunk + kFinishChunks - 1) / kFinishChunks) * static_cast<unsigned>(B));
     cfg.blockDim = dim3(kThreads);
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cudaError_t le = cudaLaunchKernelEx(&cfg, verify_finish_kernel<T, VEC>, lt, ld, x, B, bs, V, nchunk, scale,
