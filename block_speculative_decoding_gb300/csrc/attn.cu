@@ -94,11 +94,12 @@ __global__ void __launch_bounds__(kPrologueThreads) attn_prologue_kernel(
     const T* __restrict__ kg, const int32_t* __restrict__ seq_len, int B, int bs, int Hq, int Hkv,
     int cap, float eps, InvFreq inv_freq, T* __restrict__ qh, T* __restrict__ kbh,
     int* __restrict__ counters, int n_counters, unsigned* status) {
-  pdl_launch_dependents();
   // Launched as a programmatic dependent of whatever precedes it in the stream
   // (its CTAs become resident early): nothing is read or written before the
-  // preceding grid has completed.
+  // preceding grid has completed, and the main kernel (which reads sequence
+  // lengths before its own wait) is released only after that.
   pdl_wait_primary();
+  pdl_launch_dependents();
   if (blockIdx.x == 0 && counters)
     for (int i = threadIdx.x; i < n_counters; i += blockDim.x) counters[i] = 0;
   const int b = blockIdx.x / bs, j = blockIdx.x % bs;
@@ -556,7 +557,6 @@ __global__ void __launch_bounds__(TcCfg<NC>::kThreads, 1) attn_tc_kernel(const _
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
-  pdl_launch_dependents();  // the combine kernel may launch; it waits for this grid
   const uint32_t tmem = *tmem_slot;
   const int n_items = s_prefix[p.B] + p.B * p.Hkv;
 
@@ -567,6 +567,9 @@ __global__ void __launch_bounds__(TcCfg<NC>::kThreads, 1) attn_tc_kernel(const _
       tma_prefetch_desc(&maps.v);
       tma_prefetch_desc(&maps.q);
       pdl_wait_primary();  // the prologue's Q, block keys and cleared counter
+      // Release the combine kernel only now: it trusts the per-pair counters,
+      // which the prologue has cleared by this point.
+      pdl_launch_dependents();
       const uint64_t pol = l2_policy_evict_first();
       Ring kr, vr, q, itr;
       bool ok = true;

@@ -316,7 +316,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
-  pdl_launch_dependents();
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
@@ -338,6 +337,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
         }
       }
       pdl_wait_primary();
+      // The next kernel (the row norm) reads its inputs before its own wait:
+      // release it only once the grid this one depends on has completed.
+      pdl_launch_dependents();
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;

@@ -141,10 +141,12 @@ __global__ void __launch_bounds__(kThreads, (stats_ctas_per_sm<T, VEC, GREEDY>()
                                                                    float scale,
                                                                    float2* __restrict__ part,
                                                                    int* __restrict__ counters) {
-  pdl_launch_dependents();
   // launched as a programmatic dependent of the preceding kernel: nothing is
-  // read or written before that grid has completed
+  // read or written before that grid has completed, and the finish kernel
+  // (which loads the draft tokens' logits before its own wait) is released
+  // only after that
   pdl_wait_primary();
+  pdl_launch_dependents();
   if (blockIdx.x == 0 && counters)
     for (int i = threadIdx.x; i < B; i += kThreads) counters[i] = 0;
   const int c = blockIdx.x % nchunk;
