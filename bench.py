@@ -230,9 +230,11 @@ def run_gpu(args):
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    # the timed steps run back to back, nothing between the calls (an event
+    # between two kernels would stop the second from launching early)
     t0.record(stream)
     for i in range(args.steps):
-        cyc.step(stream, evs[i], only=args.only)
+        cyc.step(stream, only=args.only)
     t1.record(stream)
     torch.cuda.synchronize()
     if world > 1:
@@ -240,6 +242,11 @@ def run_gpu(args):
         dist.barrier()
     clk = clocks.stop()
     elapsed = t0.elapsed_time(t1) / 1e3
+    # per-call times (rooflines): a second pass of the same steps with events between the calls
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            cyc.step(stream, evs[i], only=args.only)
+    torch.cuda.synchronize()
     fuse_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     attn_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs) / cfg.L
     ver_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
@@ -281,7 +288,10 @@ def run_gpu(args):
                      "frac": attn_gbs / hbm, "peak_source": src,
                      "algorithmic_bytes_per_launch": cyc.attn_bytes_per_call,
                      "traffic": measured_traffic()},
-        "components_ms": {"fuse_context": fuse_ms, "block_attn_per_layer": attn_ms, "verify": ver_ms},
+        "components_ms": {"fuse_context": fuse_ms, "block_attn_per_layer": attn_ms, "verify": ver_ms,
+                          "timing": "a second pass of the same steps with CUDA events between the calls (the "
+                                    "events stop each call's first kernel from launching early, so these are "
+                                    "slightly longer than the calls take in the timed steps)"},
         "rooflines": {
             "verify": {"bound": "hbm", "achieved": cyc.verify_bytes / (ver_ms * 1e-3) / 1e9, "peak": hbm,
                        "unit": "GB/s", "frac": cyc.verify_bytes / (ver_ms * 1e-3) / 1e9 / hbm},
