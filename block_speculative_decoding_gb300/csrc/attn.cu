@@ -103,6 +103,34 @@ __global__ void __launch_bounds__(kPrologueThreads) attn_prologue_kernel(
   if (blockIdx.x == 0 && counters)
     for (int i = threadIdx.x; i < n_counters; i += blockDim.x) counters[i] = 0;
   const int b = blockIdx.x / bs, j = blockIdx.x % bs;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int e0 = 2 * lane;  // this lane owns elements e0, e0+1 and e0+64, e0+65
+  constexpr int kWarps = kPrologueThreads / 32;
+  constexpr int kBatch = 5;  // head vectors a warp loads before working on them
+  // a batch of a warp's head vectors and their gains, loaded together
+  float x[kBatch][4], gn[kBatch][4];
+  auto load_batch = [&](int v0) {
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int v = v0 + u * kWarps;
+      if (v < Hq + Hkv) {
+        const bool isq = v < Hq;
+        const T* src = isq ? q + ((static_cast<size_t>(b) * Hq + v) * bs + j) * HD
+                           : kb + ((static_cast<size_t>(b) * Hkv + (v - Hq)) * bs + j) * HD;
+        const T* gain = isq ? qg : kg;
+        x[u][0] = to_f32<T>(src[e0]);
+        x[u][1] = to_f32<T>(src[e0 + 1]);
+        x[u][2] = to_f32<T>(src[e0 + 64]);
+        x[u][3] = to_f32<T>(src[e0 + 65]);
+        gn[u][0] = gain ? to_f32<T>(gain[e0]) : 1.f;
+        gn[u][1] = gain ? to_f32<T>(gain[e0 + 1]) : 1.f;
+        gn[u][2] = gain ? to_f32<T>(gain[e0 + 64]) : 1.f;
+        gn[u][3] = gain ? to_f32<T>(gain[e0 + 65]) : 1.f;
+      }
+    }
+  };
+  // the first batch does not depend on the position: load it before the angles
+  load_batch(warp);
   const int n = clamp_seq(seq_len[b], cap, status);
   const int pos = n + j;
   __shared__ float s_cos[HD / 2], s_sin[HD / 2];
@@ -115,25 +143,9 @@ __global__ void __launch_bounds__(kPrologueThreads) attn_prologue_kernel(
     s_sin[threadIdx.x] = sv;
   }
   __syncthreads();
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int e0 = 2 * lane;  // this lane owns elements e0, e0+1 and e0+64, e0+65
-  constexpr int kWarps = kPrologueThreads / 32;
-  constexpr int kBatch = 5;  // head vectors a warp loads before working on them
+  const float c0 = s_cos[e0], s0 = s_sin[e0], c1 = s_cos[e0 + 1], s1 = s_sin[e0 + 1];
   for (int v0 = warp; v0 < Hq + Hkv; v0 += kWarps * kBatch) {
-    float x[kBatch][4];
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int v = v0 + u * kWarps;
-      if (v < Hq + Hkv) {
-        const bool isq = v < Hq;
-        const T* src = isq ? q + ((static_cast<size_t>(b) * Hq + v) * bs + j) * HD
-                           : kb + ((static_cast<size_t>(b) * Hkv + (v - Hq)) * bs + j) * HD;
-        x[u][0] = to_f32<T>(src[e0]);
-        x[u][1] = to_f32<T>(src[e0 + 1]);
-        x[u][2] = to_f32<T>(src[e0 + 64]);
-        x[u][3] = to_f32<T>(src[e0 + 65]);
-      }
-    }
+    if (v0 != warp) load_batch(v0);
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
       const int v = v0 + u * kWarps;
@@ -141,17 +153,13 @@ __global__ void __launch_bounds__(kPrologueThreads) attn_prologue_kernel(
       const bool isq = v < Hq;
       T* dst = isq ? qh + ((static_cast<size_t>(b) * Hq + v) * bs + j) * HD
                    : kbh + ((static_cast<size_t>(b) * Hkv + (v - Hq)) * bs + j) * HD;
-      const T* gain = isq ? qg : kg;
       float x0 = x[u][0], x1 = x[u][1], y0 = x[u][2], y1 = x[u][3];
       const float ss = warp_sum(x0 * x0 + x1 * x1 + y0 * y0 + y1 * y1);
       const float r = rsqrtf(ss * (1.0f / HD) + eps);
-      const float g0 = gain ? to_f32<T>(gain[e0]) : 1.f, g1 = gain ? to_f32<T>(gain[e0 + 1]) : 1.f;
-      const float g2 = gain ? to_f32<T>(gain[e0 + 64]) : 1.f, g3 = gain ? to_f32<T>(gain[e0 + 65]) : 1.f;
-      x0 *= r * g0;
-      x1 *= r * g1;
-      y0 *= r * g2;
-      y1 *= r * g3;
-      const float c0 = s_cos[e0], s0 = s_sin[e0], c1 = s_cos[e0 + 1], s1 = s_sin[e0 + 1];
+      x0 *= r * gn[u][0];
+      x1 *= r * gn[u][1];
+      y0 *= r * gn[u][2];
+      y1 *= r * gn[u][3];
       dst[e0] = from_f32<T>(x0 * c0 - y0 * s0);
       dst[e0 + 1] = from_f32<T>(x1 * c1 - y1 * s1);
       dst[e0 + 64] = from_f32<T>(y0 * c0 + x0 * s0);
