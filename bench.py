@@ -264,6 +264,7 @@ def run_gpu(args):
     tensor_lines = None
     if rank == 0 and not args.no_e2e:
         tensor_lines = fusion_tensor_rooflines(dev, peaks()[1])
+        tensor_lines.update(window_attention_roofline(cyc, dev, peaks()[0]))
 
     if rank != 0:
         return
@@ -310,6 +311,47 @@ def run_gpu(args):
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, args.cpu_seconds, args.temperature)
     print(json.dumps(line), flush=True)
+
+
+def window_attention_roofline(cyc, dev, peak_gbs, W=1024, iters=20):
+    """Block attention of the batched workload over the drafter's sliding
+    window kept as a ring cache of W rows (every sequence is longer than W, so
+    each attends to exactly W cached keys): five layer calls back to back,
+    CUDA events on the launching stream, 3 warm-up rounds; algorithmic bytes
+    B * W * 4096 per layer call."""
+    import block_speculative_decoding_gb300 as dfl
+    from dataclasses import replace
+    cfg = replace(cyc.cfg, S=W, S_min=None)
+    k, v = workloads.cache(replace(cfg, bs=0, fuse_rows_per_seq=0), dev)
+    ring = dfl.KVCache(k[..., :W, :].contiguous(), v[..., :W, :].contiguous(), cyc.seq.clone(), ring=True)
+    del k, v
+    ws = torch.empty(dfl.block_attn_workspace_size(cfg.B, cfg.bs, cfg.Hq, cfg.Hkv, W, 0, dfl.BF16),
+                     dtype=torch.uint8, device=dev)
+    st = torch.cuda.Stream(device=dev)
+
+    def layers():
+        for l in range(cfg.L):
+            q, kb, vb = cyc.blocks[l]
+            dfl.block_attn(l, q, kb, vb, cyc.w.q_gain[l], cyc.w.k_gain[l], ring, out=cyc.outs[l], workspace=ws,
+                           stream=st)
+    with torch.cuda.stream(st):
+        for _ in range(3):
+            layers()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for _ in range(iters):
+            layers()
+        e1.record(st)
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / (iters * cfg.L)
+    gbs = cfg.B * W * cfg.Hkv * cfg.d * 2 * 2 / (ms * 1e-3) / 1e9
+    del ring, ws
+    torch.cuda.empty_cache()
+    return {"block_attn_ring_window_%d" % W: {"bound": "hbm", "achieved": gbs, "peak": peak_gbs, "unit": "GB/s",
+                                             "frac": gbs / peak_gbs, "ms_per_layer_call": ms,
+                                             "note": "ring cache of %d rows per (layer, sequence, KV head); every "
+                                                     "sequence longer than the window" % W}}
 
 
 def fusion_tensor_rooflines(dev, peak_tflops, iters=10):

@@ -43,6 +43,7 @@ class _KVCacheDesc(ctypes.Structure):
         ("num_layers", ctypes.c_int), ("batch", ctypes.c_int), ("num_kv_heads", ctypes.c_int),
         ("head_dim", ctypes.c_int), ("capacity", ctypes.c_int), ("dtype", ctypes.c_int),
         ("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("seq_len", ctypes.c_void_p),
+        ("ring", ctypes.c_int),
     ]
 
 
@@ -127,17 +128,22 @@ def _workspace(nbytes, device, ws):
 
 @dataclass
 class KVCache:
-    """Caller-owned draft cache: k, v [L, B, Hkv, cap, 128], seq_len int32 [B]."""
+    """Caller-owned draft cache: k, v [L, B, Hkv, cap, 128], seq_len int32 [B].
+
+    ring=True makes it the drafter's sliding window: position p lives in row
+    p % cap, seq_len may exceed cap, attention sees the latest min(seq_len,
+    cap) positions (block_attn's window must then be 0)."""
     k: torch.Tensor
     v: torch.Tensor
     seq_len: torch.Tensor
+    ring: bool = False
 
     def desc(self) -> _KVCacheDesc:
         L, B, H, cap, d = self.k.shape
         if self.seq_len.dtype != torch.int32:
             raise TypeError("seq_len must be int32")
         return _KVCacheDesc(L, B, H, d, cap, _dt(self.k), self.k.data_ptr(), self.v.data_ptr(),
-                            self.seq_len.data_ptr())
+                            self.seq_len.data_ptr(), int(bool(self.ring)))
 
 
 def version() -> int:

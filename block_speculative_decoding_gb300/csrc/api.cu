@@ -133,6 +133,7 @@ static dflash_status check_cache(const dflash_kv_cache* c) {
   if (c->head_dim != 128) return fail(DFLASH_ERR_UNSUPPORTED, "head_dim must be 128");
   if (c->dtype != DFLASH_F32 && c->dtype != DFLASH_BF16) return fail(DFLASH_ERR_UNSUPPORTED, "cache dtype");
   if (!aligned16(c->k) || !aligned16(c->v)) return fail(DFLASH_ERR_INVALID_ARGUMENT, "cache k/v must be 16-byte aligned");
+  if (c->ring != 0 && c->ring != 1) return fail(DFLASH_ERR_INVALID_ARGUMENT, "cache ring must be 0 or 1");
   const double rows = double(c->num_layers) * c->batch * c->num_kv_heads * c->capacity;
   if (rows >= 2147483647.0) return fail(DFLASH_ERR_UNSUPPORTED, "cache has 2^31 or more rows");
   return DFLASH_OK;
@@ -150,7 +151,7 @@ static dflash_status check_ws(void* ws, size_t have, size_t need) {
 
 extern "C" {
 
-int dflash_version(void) { return (1 << 16) | 0; }
+int dflash_version(void) { return (1 << 16) | 1; }
 
 const char* dflash_last_error_string(void) { return t_last_error.c_str(); }
 
@@ -241,6 +242,8 @@ dflash_status dflash_block_attn(int layer, int batch, int block_size, int num_q_
   if ((num_q_heads / hkv) * block_size > 64)
     return fail(DFLASH_ERR_UNSUPPORTED, "(num_q_heads/num_kv_heads) * block_size must be <= 64");
   if (window < 0) return fail(DFLASH_ERR_INVALID_ARGUMENT, "window < 0");
+  if (cache->ring && window != 0)
+    return fail(DFLASH_ERR_UNSUPPORTED, "a ring cache is its own window: window must be 0");
   if (!q || !kb || !vb || !out) return fail(DFLASH_ERR_INVALID_ARGUMENT, "NULL q/kb/vb/out");
   if (!aligned16(q) || !aligned16(kb) || !aligned16(vb) || !aligned16(out))
     return fail(DFLASH_ERR_INVALID_ARGUMENT, "q/kb/vb/out must be 16-byte aligned");

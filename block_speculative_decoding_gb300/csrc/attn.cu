@@ -54,7 +54,7 @@ struct InvFreq {
 };
 
 struct AttnParams {
-  int B, bs, G, Hkv, Hq, cap, layer, window, chunk, max_splits, rows;
+  int B, bs, G, Hkv, Hq, cap, ring, layer, window, chunk, max_splits, rows;
   const int32_t* seq_len;
   const __nv_bfloat16* qh;   // [B, Hq, bs, 128]   prologue output
   const __nv_bfloat16* kbh;  // [B, Hkv, bs, 128]  prologue output
@@ -65,11 +65,18 @@ struct AttnParams {
   const __nv_bfloat16* ck;   // this cache's K and V, [L, B, Hkv, cap, 128]
   const __nv_bfloat16* cv;
   float scale_log2;          // log2(e) / sqrt(128)
-  int* counters;             // [1 + 2 B Hkv]: work-queue counter, a flag per (b, g), then per (b, g) the
-                             // count of epilogue warps (4 per split) that finished writing
-                             // whose scores outgrew the running max (cleared by the prologue)
+  int* counters;             // [1 + 2 B Hkv], cleared by the prologue: the work-queue counter, per (b, g)
+                             // a flag (scores outgrew the running max), then per (b, g) the count of
+                             // epilogue warps (4 per split) that finished writing
   unsigned* status;
 };
+
+// Cached rows a sequence attends to: its length, clamped to the capacity; a
+// ring cache (sliding window) holds the latest min(n, cap) positions.
+__device__ __forceinline__ int cached_rows(int n, int cap, int ring, unsigned* status) {
+  if (n < 0 || (!ring && n > cap)) raise_status(status, DFLASH_DEV_BAD_SEQLEN);
+  return min(max(n, 0), cap);
+}
 
 __device__ __forceinline__ int clamp_seq(int n, int cap, unsigned* status) {
   if (n < 0 || n > cap) {
@@ -92,7 +99,7 @@ template <typename T>
 __global__ void __launch_bounds__(kPrologueThreads) attn_prologue_kernel(
     const T* __restrict__ q, const T* __restrict__ kb, const T* __restrict__ qg,
     const T* __restrict__ kg, const int32_t* __restrict__ seq_len, int B, int bs, int Hq, int Hkv,
-    int cap, float eps, InvFreq inv_freq, T* __restrict__ qh, T* __restrict__ kbh,
+    int cap, int ring, float eps, InvFreq inv_freq, T* __restrict__ qh, T* __restrict__ kbh,
     int* __restrict__ counters, int n_counters, unsigned* status) {
   // Launched as a programmatic dependent of whatever precedes it in the stream
   // (its CTAs become resident early): nothing is read or written before the
@@ -131,7 +138,9 @@ __global__ void __launch_bounds__(kPrologueThreads) attn_prologue_kernel(
   };
   // the first batch does not depend on the position: load it before the angles
   load_batch(warp);
-  const int n = clamp_seq(seq_len[b], cap, status);
+  // the block's positions follow the sequence: seq_len (a ring cache's
+  // length may exceed its capacity) plus j
+  const int n = ring ? max(seq_len[b], 0) : clamp_seq(seq_len[b], cap, status);
   const int pos = n + j;
   __shared__ float s_cos[HD / 2], s_sin[HD / 2];
   if (threadIdx.x < HD / 2) {
@@ -546,7 +555,7 @@ __global__ void __launch_bounds__(TcCfg<NC>::kThreads, 1) attn_tc_kernel(const _
       const int b = b0 + lane;
       int cnt = 0;
       if (b < p.B) {
-        const int n = clamp_seq(p.seq_len[b], p.cap, p.status);
+        const int n = cached_rows(p.seq_len[b], p.cap, p.ring, p.status);
         s_n[b] = n;
         const int first = p.window > 0 ? max(0, n - p.window) : 0;
         cnt = (n_splits(n - first, p.chunk) - 1) * p.Hkv;
@@ -1002,10 +1011,15 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const float* __restrict__
 // Keys per split: aims at ~1200 work items for a full cache (about eight per
 // SM).  Longer splits amortise each split's partial output (written, then
 // merged by the combine kernel) and its pipeline ramp; enough items remain for
-// the dynamic queue to balance the SMs.
+// the dynamic queue to balance the SMs.  A split is at least ~1024 keys (a
+// work item costs about as much as a few tiles on top of its keys) unless
+// that would leave fewer items than the 152 SMs of a GB300.
 int pick_chunk(int B, int Hkv, int cap, int window) {
   const long keys = window > 0 ? std::min(window, cap) : cap;
-  long c = (static_cast<long>(B) * Hkv * keys) / 1200;
+  const long total = static_cast<long>(B) * Hkv * keys;
+  long c = total / 1200;
+  const long lo = std::min<long>(1024, std::max<long>(256, total / 152));
+  c = std::max(c, lo);
   c = (c + kKeys - 1) / kKeys * kKeys;
   return static_cast<int>(std::min<long>(4096, std::max<long>(256, c)));
 }
@@ -1042,7 +1056,7 @@ dflash_status launch_block_attn(int layer, int B, int bs, int Hq, const void* q,
     float* kbh = w.take<float>(static_cast<size_t>(B) * Hkv * bs * HD);
     attn_prologue_kernel<float><<<B * bs, kPrologueThreads, 0, st>>>(
         static_cast<const float*>(q), static_cast<const float*>(kb), static_cast<const float*>(qg),
-        static_cast<const float*>(kg), c.seq_len, B, bs, Hq, Hkv, c.capacity, eps, inv, qh, kbh, nullptr, 0,
+        static_cast<const float*>(kg), c.seq_len, B, bs, Hq, Hkv, c.capacity, c.ring, eps, inv, qh, kbh, nullptr, 0,
         dev.status);
     attn_f32_kernel<<<B * Hq, 128, 0, st>>>(qh, kbh, static_cast<const float*>(vb),
                                             static_cast<const float*>(c.k), static_cast<const float*>(c.v),
@@ -1059,6 +1073,7 @@ dflash_status launch_block_attn(int layer, int B, int bs, int Hq, const void* q,
   p.Hkv = Hkv;
   p.Hq = Hq;
   p.cap = c.capacity;
+  p.ring = c.ring;
   p.layer = layer;
   p.window = window;
   p.chunk = pick_chunk(B, Hkv, c.capacity, window);
@@ -1103,7 +1118,7 @@ dflash_status launch_block_attn(int layer, int B, int bs, int Hq, const void* q,
     cudaError_t le = cudaLaunchKernelEx(&pc, attn_prologue_kernel<__nv_bfloat16>,
                                         static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(kb),
                                         static_cast<const __nv_bfloat16*>(qg), static_cast<const __nv_bfloat16*>(kg),
-                                        c.seq_len, B, bs, Hq, Hkv, c.capacity, eps, inv, qh, kbh, p.counters,
+                                        c.seq_len, B, bs, Hq, Hkv, c.capacity, c.ring, eps, inv, qh, kbh, p.counters,
                                         1 + 2 * B * Hkv, dev.status);
     if (le != cudaSuccess) return cuda_fail(le, "attn_prologue_kernel launch");
   }

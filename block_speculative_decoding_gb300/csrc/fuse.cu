@@ -68,7 +68,7 @@ struct GemmArgs {
   __nv_bfloat16* cache_k;  // epi 1
   __nv_bfloat16* cache_v;
   int L, Bc, Hkv, cap;
-  const int2* rowinfo;     // [M] (sequence, position) or (-1, -1)
+  const int2* rowinfo;     // [M] (sequence, cache row) or (-1, -1)
   const float2* rope_cs;   // [64][M] (cos, sin), element-major: a warp's rows read it coalesced
   const __nv_bfloat16* k_gain;  // [L][128] or null
   float eps;
@@ -468,7 +468,7 @@ __global__ void __launch_bounds__(kNormThreads) fuse_rownorm_kernel(
     const float* __restrict__ part, int k_splits, const int* __restrict__ pieces, int tile_rows, int tile_cols,
     int n_tiles, int M, int D, const TG* __restrict__ g, float eps,
     TH* __restrict__ ht, TH* __restrict__ ht_out, const int32_t* __restrict__ cu_new,
-    const int32_t* __restrict__ seq_len, int B, int cap, InvFreq inv, int2* __restrict__ rowinfo,
+    const int32_t* __restrict__ seq_len, int B, int cap, int ring, InvFreq inv, int2* __restrict__ rowinfo,
     float2* __restrict__ rope_cs, unsigned* status) {
   const int m = blockIdx.x;
   if (threadIdx.x <= HD / 2) {
@@ -481,9 +481,11 @@ __global__ void __launch_bounds__(kNormThreads) fuse_rownorm_kernel(
     const int t = m - cu_new[b];
     const int nnew = cu_new[b + 1] - cu_new[b];
     const int n = seq_len[b];
-    const bool seq_ok = n >= 0 && n <= cap;
-    const bool valid = seq_ok && n + nnew <= cap && t >= 0 && t < nnew;
-    const int pos = valid ? n + t : 0;
+    // linear cache: position p is row p (n + nnew <= cap); ring cache: row
+    // p % cap, at most cap new rows per sequence and call
+    const bool seq_ok = n >= 0 && (ring || n <= cap);
+    const bool valid = seq_ok && (ring ? nnew <= cap : n + nnew <= cap) && t >= 0 && t < nnew;
+    const int pos = valid ? n + t : 0;  // the RoPE position is always the absolute one
     if (threadIdx.x < HD / 2) {
       double ang = static_cast<double>(pos) * inv.v[threadIdx.x];
       ang -= kTwoPi * rint(ang * kInvTwoPi);
@@ -491,7 +493,7 @@ __global__ void __launch_bounds__(kNormThreads) fuse_rownorm_kernel(
       sincosf(static_cast<float>(ang), &sv, &cv);
       rope_cs[static_cast<size_t>(threadIdx.x) * M + m] = make_float2(cv, sv);
     } else {
-      rowinfo[m] = valid ? make_int2(b, pos) : make_int2(-1, -1);
+      rowinfo[m] = valid ? make_int2(b, ring ? pos % cap : pos) : make_int2(-1, -1);  // (sequence, cache row)
       if (!valid) raise_status(status, seq_ok ? DFLASH_DEV_CAPACITY : DFLASH_DEV_BAD_SEQLEN);
     }
   }
@@ -781,7 +783,7 @@ dflash_status launch_fuse_context(int J, const void* const* taps, int dt_width, 
         segs, dt_width, static_cast<const float*>(w_fuse), M, D, J * dt_width, Y);
     fuse_rownorm_kernel<float, float><<<M, kNormThreads, 0, st>>>(
         Y, 1, nullptr, kBM, D, 1, M, D, static_cast<const float*>(g_fuse), eps, H, static_cast<float*>(h_t_out), cu_new, c.seq_len, B,
-        c.capacity, inv, rowinfo, rope_cs, dev.status);
+        c.capacity, c.ring, inv, rowinfo, rope_cs, dev.status);
     F32Segs hs{};
     hs.a[0] = H;
     simt_gemm_f32_kernel<<<dim3((Ntot + 63) / 64, (M + 63) / 64), 256, 0, st>>>(
@@ -844,8 +846,8 @@ dflash_status launch_fuse_context(int J, const void* const* taps, int dt_width, 
                                         static_cast<const int*>(f.stream_k ? tile_pieces : nullptr), f.fuse_mt * kBM,
                                         f.fuse_bn, f.fuse_n_tiles, M, D,
                                         static_cast<const __nv_bfloat16*>(g_fuse), eps, H,
-                                        static_cast<__nv_bfloat16*>(h_t_out), cu_new, c.seq_len, B, c.capacity, inv,
-                                        rowinfo, rope_cs, dev.status);
+                                        static_cast<__nv_bfloat16*>(h_t_out), cu_new, c.seq_len, B, c.capacity,
+                                        c.ring, inv, rowinfo, rope_cs, dev.status);
     if (le != cudaSuccess) return cuda_fail(le, "fuse_rownorm_kernel launch");
   }
 

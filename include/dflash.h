@@ -80,6 +80,12 @@ enum {
  *             read it and never advance it: after dflash_fuse_context the
  *             caller adds n_new[b] (rolling back a rejected proposal = not
  *             advancing; block K/V are never written to the cache).
+ *   ring    : 0: position p is row p (seq_len <= capacity).  1: the cache is
+ *             the draft's sliding window (E4B page, the released drafter's
+ *             1024-token window): position p is row p % capacity, seq_len may
+ *             exceed capacity, and attention sees the latest
+ *             min(seq_len, capacity) positions (block_attn's window must be 0).
+ *             A fusion call may add at most capacity rows per sequence.
  */
 typedef struct {
   int num_layers;
@@ -91,6 +97,7 @@ typedef struct {
   void* k;
   void* v;
   const int32_t* seq_len;
+  int ring;        /* 0: linear cache, 1: ring buffer of capacity rows (sliding window) */
 } dflash_kv_cache;
 
 /* ---------------------------------------------------------------------------

@@ -49,16 +49,16 @@ def test_workspace_queries(L):
     assert dfl.block_attn_workspace_size(32, 8, 32, 8, 8256, 0, dfl.BF16) > 0
     assert dfl.block_attn_workspace_size(0, 8, 32, 8, 8256, 0, dfl.BF16) == 0
     assert dfl.fuse_context_workspace_size(256, 5, 2560, 2560, 5, 8, dfl.BF16) >= 256 * 2560 * 2
-    assert dfl.version() == (1 << 16)
+    assert dfl.version() == (1 << 16) | 1
 
 
 def _cache(**kw):
     import block_speculative_decoding_gb300 as dfl
     d = dict(num_layers=5, batch=2, num_kv_heads=8, head_dim=128, capacity=64, dtype=dfl.BF16,
-             k=16, v=16, seq_len=16)
+             k=16, v=16, seq_len=16, ring=0)
     d.update(kw)
     return dfl._KVCacheDesc(d["num_layers"], d["batch"], d["num_kv_heads"], d["head_dim"], d["capacity"],
-                            d["dtype"], d["k"], d["v"], d["seq_len"])
+                            d["dtype"], d["k"], d["v"], d["seq_len"], d["ring"])
 
 
 def test_host_validation_rejects_bad_arguments_before_any_launch(L):
@@ -84,6 +84,11 @@ def test_host_validation_rejects_bad_arguments_before_any_launch(L):
     assert lib.dflash_block_attn(5, 2, 8, 32, P(16), P(16), P(16), None, None, 1e6, 1e-6, ctypes.byref(c), 0, P(16), P(256), 1 << 30, None) == 1
     assert lib.dflash_block_attn(0, 2, 8, 32, P(16), P(16), P(16), None, None, 1e6, 1e-6, None, 0, P(16), P(256), 1 << 30, None) == 1
     assert lib.dflash_block_attn(0, 2, 8, 32, P(17), P(16), P(16), None, None, 1e6, 1e-6, ctypes.byref(c), 0, P(16), P(256), 1 << 30, None) == 1
+    # a ring cache is its own window; the ring flag is 0 or 1
+    r = _cache(ring=1)
+    assert lib.dflash_block_attn(0, 2, 8, 32, P(16), P(16), P(16), None, None, 1e6, 1e-6, ctypes.byref(r), 5, P(16), P(256), 1 << 30, None) == 2
+    r = _cache(ring=2)
+    assert lib.dflash_block_attn(0, 2, 8, 32, P(16), P(16), P(16), None, None, 1e6, 1e-6, ctypes.byref(r), 0, P(16), P(256), 1 << 30, None) == 1
     # fusion: tap count, widths, capacity visible on the host
     taps = (ctypes.c_void_p * 5)(16, 16, 16, 16, 16)
     assert lib.dflash_fuse_context(0, taps, 2560, P(16), 2, 8, P(16), None, 2560, P(16), None, 1e6, 1e-6, ctypes.byref(c), None, P(256), 1 << 30, None) == 2

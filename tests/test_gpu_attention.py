@@ -158,21 +158,21 @@ def test_block_attn_bad_seq_len_is_flagged_not_faulted():
 
 
 def test_block_attn_split_count_does_not_change_the_result():
-    """One 3000-token sequence in a 65536-row cache: with the full cache the
-    keys are cut into 512-key splits (6 of them), with a 40000-key window
-    (longer than the sequence, so the same keys) into 384-key splits (8).  Both
-    outputs match the oracle and each other to a few bf16 ulps."""
-    seq = [3000]
-    cap = 65536
-    k, v, q, kb, vb, qg, kg = _inputs(1, 8, cap, torch.bfloat16, seed=91, layers=1)
-    cache = dfl.KVCache(k.to(DEV), v.to(DEV), torch.tensor(seq, dtype=torch.int32, device=DEV))
-    args = (q.to(DEV), kb.to(DEV), vb.to(DEV), qg.to(DEV), kg.to(DEV), cache)
-    out_full = dfl.block_attn(0, *args, window=0)
-    out_win = dfl.block_attn(0, *args, window=40000)
-    ref = _oracle(q, kb, vb, qg, kg, k[0], v[0], seq, 0, torch.bfloat16)
-    for out in (out_full, out_win):
-        assert rel_fro(out, ref) <= TOL[torch.bfloat16], (rel_fro(out, ref), max_abs(out, ref))
-    assert rel_fro(out_full, out_win.float().cpu().numpy()) <= 2e-3
+    """The same 3000-token sequence attended alone (batch 1: 256-key splits,
+    12 of them) and as the first of a batch of four (896-key splits, 4 of
+    them): both outputs match the oracle and each other to a few bf16 ulps."""
+    seq = [3000, 100, 2000, 4000]
+    cap = 4096
+    k, v, q, kb, vb, qg, kg = _inputs(4, 8, cap, torch.bfloat16, seed=91, layers=1)
+    outs = []
+    for B in (1, 4):
+        cache = dfl.KVCache(k[:, :B].contiguous().to(DEV), v[:, :B].contiguous().to(DEV),
+                            torch.tensor(seq[:B], dtype=torch.int32, device=DEV))
+        outs.append(dfl.block_attn(0, q[:B].to(DEV), kb[:B].to(DEV), vb[:B].to(DEV), qg.to(DEV), kg.to(DEV), cache))
+    ref = _oracle(q[:1], kb[:1], vb[:1], qg, kg, k[0, :1], v[0, :1], seq[:1], 0, torch.bfloat16)
+    for out in outs:
+        assert rel_fro(out[:1], ref) <= TOL[torch.bfloat16], (rel_fro(out[:1], ref), max_abs(out[:1], ref))
+    assert rel_fro(outs[0], outs[1][:1].float().cpu().numpy()) <= 2e-3
 
 
 def test_block_attn_is_invariant_to_the_order_of_cached_rows():
