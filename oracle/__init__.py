@@ -27,6 +27,10 @@ from .dflash_oracle import (  # noqa: F401
     block_attn,
     verify,
     VerifyResult,
+    draft_head,
+    draft_race_uniforms,
+    draft_sample,
+    DRAFT_TIE_EPS,
     draft_param_count,
     kv_cache_payload_bytes,
     fusion_weight_bytes,

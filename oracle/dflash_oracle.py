@@ -422,6 +422,82 @@ def verify(target_logits, draft_logits, draft_tokens, temperature, seed, cycle, 
 
 
 # --------------------------------------------------------------------------
+# step 4: the drafter's head -- final RMSNorm, LM head, draft sampling
+#         ([E4B] "The released serving cycle": the drafter proposes the block's
+#         tokens from its final hidden states through the LM head; "The
+#         parameter count exposes the real cost": the head is V x D)
+# --------------------------------------------------------------------------
+
+DRAFT_TAG = 0x80000000  # top bit of the fourth counter word: draft sampling
+
+
+def draft_head(x, g_final, w_head, eps=1e-6, bf16=False):
+    """Draft logits of the proposal rows.
+
+    x [R, D] final hidden states, g_final [D], w_head [V, D] (row v = token v):
+    logits = RMSNorm(x) * g_final @ w_head^T.  bf16: the normalised rows are
+    stored as bfloat16 before the product and the logits are rounded to
+    bfloat16 (the kernel's storage points).
+    """
+    h = rms_norm(np.asarray(x, dtype=F64), np.asarray(g_final, dtype=F64), eps)
+    if bf16:
+        h = round_to_bf16(h)
+    z = h @ np.asarray(w_head, dtype=F64).T
+    return round_to_bf16(z) if bf16 else z
+
+
+def draft_race_uniforms(seed, cycle, b, k, V):
+    """U(0,1] for every vocabulary index y of proposal row k of sequence b.
+
+    One Philox-4x32-10 block per 4 consecutive indices: counter =
+    (y >> 2, (b << 5) | k, cycle_lo, cycle_hi | DRAFT_TAG), key = (seed_lo,
+    seed_hi); index y takes word y & 3; U = ((w >> 8) + 1) * 2^-24.  The tag
+    bit keeps these counters apart from the verification's (k, b, cycle_lo,
+    cycle_hi) for cycles below 2^63 (reading taken: the pages give no
+    random-number convention).
+    """
+    seed, cycle = int(seed), int(cycle)
+    nb = (V + 3) // 4
+    w = philox4x32_10((np.arange(nb, dtype=np.uint64), (int(b) << 5) | int(k), cycle & 0xFFFFFFFF,
+                       ((cycle >> 32) & 0x7FFFFFFF) | DRAFT_TAG),
+                      (seed & 0xFFFFFFFF, (seed >> 32) & 0xFFFFFFFF))
+    words = np.stack([np.asarray(x, dtype=np.uint64) for x in w], axis=1).reshape(-1)[:V]
+    return ((words >> np.uint64(8)) + np.uint64(1)).astype(F64) * (2.0 ** -24)
+
+
+DRAFT_TIE_EPS = 1e-4
+
+
+def draft_sample(logits, temperature, seed, cycle, seq_ids=None):
+    """Draft tokens from the proposal rows' logits [B, R, V].
+
+    T > 0: the exponential race -- y* = argmax_y q(y) / E_y with E_y = -ln U_y,
+    i.e. argmax_y logits[y] / T - ln(-ln U_y), a draw from softmax(logits / T)
+    (no normalisation needed).  T == 0: argmax of the logits.  Ties go to the
+    lowest index.  Returns (tokens [B, R] int64, near_tie [B, R] bool): a row is
+    flagged when its two largest keys are within DRAFT_TIE_EPS.
+    """
+    z = np.asarray(logits, dtype=F64)
+    B, R, V = z.shape
+    ids = np.arange(B) if seq_ids is None else np.asarray(seq_ids, dtype=np.int64)
+    T = float(temperature)
+    tok = np.zeros((B, R), dtype=np.int64)
+    near = np.zeros((B, R), dtype=bool)
+    for b in range(B):
+        for k in range(R):
+            key = z[b, k].copy()
+            if T > 0.0:
+                u = draft_race_uniforms(seed, cycle, ids[b], k, V)
+                key = key / T - np.log(-np.log(u))
+            y = int(np.argmax(key))  # first maximum = lowest index
+            tok[b, k] = y
+            if V > 1:
+                top2 = np.partition(key, V - 2)[V - 2:]
+                near[b, k] = (top2[1] - top2[0]) < DRAFT_TIE_EPS
+    return tok, near
+
+
+# --------------------------------------------------------------------------
 # size arithmetic printed by the pages ([E4B] "The parameter count exposes the
 # real cost", "Cache and latency have separate break-even points"; [DF2] 4.1)
 # --------------------------------------------------------------------------

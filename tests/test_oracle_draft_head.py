@@ -1,0 +1,77 @@
+"""Pins for the oracle's drafter head: final RMSNorm + LM head, and the
+exponential-race draft sampler.
+
+Each test checks a closed form, an invariant, a constructed case or a
+distribution, not the oracle's own formula retyped.
+"""
+import numpy as np
+import pytest
+from scipy import stats
+
+import oracle
+
+
+def test_draft_head_matches_loops_and_the_norm_closed_form():
+    rng = np.random.default_rng(0)
+    R, D, V = 3, 8, 11
+    x = rng.normal(size=(R, D)) * 3.0
+    g = 1 + 0.1 * rng.normal(size=D)
+    w = rng.normal(size=(V, D))
+    z = oracle.draft_head(x, g, w, eps=1e-6)
+    for r in range(R):
+        ms = sum(v * v for v in x[r]) / D
+        h = [x[r][i] / np.sqrt(ms + 1e-6) * g[i] for i in range(D)]
+        for t in range(V):
+            assert abs(z[r, t] - sum(h[i] * w[t, i] for i in range(D))) < 1e-10
+    # constant gain c: every normalised row has root-mean-square |c|; with the
+    # identity as head the logits are that row
+    c = -1.7
+    zi = oracle.draft_head(x, np.full(D, c), np.eye(D), eps=0.0)
+    np.testing.assert_allclose(np.sqrt((zi ** 2).mean(axis=1)), abs(c), rtol=1e-12)
+    # bf16 storage points: the logits are bfloat16 values
+    zb = oracle.draft_head(x, g, w, bf16=True)
+    np.testing.assert_array_equal(zb, oracle.round_to_bf16(zb))
+
+
+def test_greedy_draft_is_the_first_argmax():
+    z = np.zeros((1, 2, 7))
+    z[0, 0, [2, 5]] = 3.0           # tie: lowest index
+    z[0, 1, 6] = 1.0
+    tok, near = oracle.draft_sample(z, 0.0, seed=1, cycle=0)
+    assert tok.tolist() == [[2, 6]]
+    assert near.tolist() == [[True, False]]
+
+
+def test_temperature_scales_the_logits():
+    z = np.random.default_rng(2).normal(size=(2, 3, 50)) * 4
+    for T in (0.3, 1.0, 2.5):
+        a, _ = oracle.draft_sample(z, T, seed=9, cycle=4)
+        b, _ = oracle.draft_sample(z / T, 1.0, seed=9, cycle=4)
+        np.testing.assert_array_equal(a, b)
+
+
+def test_race_uniforms_are_in_the_open_unit_interval_and_distinct_per_row():
+    u = oracle.draft_race_uniforms(seed=5, cycle=11, b=3, k=2, V=4096)
+    assert u.min() > 0.0 and u.max() <= 1.0
+    assert abs(u.mean() - 0.5) < 0.02 and abs(u.var() - 1 / 12) < 0.01
+    v = oracle.draft_race_uniforms(seed=5, cycle=11, b=3, k=1, V=4096)
+    w = oracle.draft_race_uniforms(seed=5, cycle=12, b=3, k=2, V=4096)
+    assert not np.array_equal(u, v) and not np.array_equal(u, w)
+    # a prefix of the vocabulary draws the same uniforms as the whole row
+    np.testing.assert_array_equal(oracle.draft_race_uniforms(5, 11, 3, 2, 10), u[:10])
+
+
+def test_race_draws_follow_the_softmax():
+    """Many cycles of one row: the empirical distribution of the drawn token
+    is softmax(logits / T) (chi-square)."""
+    V, T, N = 6, 0.7, 6000
+    z = np.array([0.3, -1.0, 1.2, 0.0, 2.0, -0.4])
+    p = np.exp(z / T - (z / T).max())
+    p /= p.sum()
+    counts = np.zeros(V)
+    zz = np.broadcast_to(z, (1, 1, V))
+    for c in range(N):
+        tok, _ = oracle.draft_sample(zz, T, seed=77, cycle=c)
+        counts[tok[0, 0]] += 1
+    chi2 = ((counts - N * p) ** 2 / (N * p)).sum()
+    assert stats.chi2.sf(chi2, V - 1) > 1e-3, (counts, N * p)
