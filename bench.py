@@ -265,6 +265,7 @@ def run_gpu(args):
     if rank == 0 and not args.no_e2e:
         tensor_lines = fusion_tensor_rooflines(dev, peaks()[1])
         tensor_lines.update(window_attention_roofline(cyc, dev, peaks()[0]))
+        tensor_lines.update(draft_head_roofline(cyc, dev, peaks()[0]))
 
     if rank != 0:
         return
@@ -352,6 +353,46 @@ def window_attention_roofline(cyc, dev, peak_gbs, W=1024, iters=20):
                                              "frac": gbs / peak_gbs, "ms_per_layer_call": ms,
                                              "note": "ring cache of %d rows per (layer, sequence, KV head); every "
                                                      "sequence longer than the window" % W}}
+
+
+def draft_head_roofline(cyc, dev, peak_gbs, iters=10):
+    """The drafter's head on the batched workload's proposal rows: B x (bs - 1)
+    rows, D = 2560, V = 262144 (final RMSNorm, LM head, draft race at T).
+    Algorithmic bytes: the head's weights V * D * 2 read once, the logits
+    M * V * 2 written, the rows M * D * 2 read; CUDA events on the launching
+    stream, 3 warm-up calls."""
+    import block_speculative_decoding_gb300 as dfl
+    cfg = cyc.cfg
+    R = cfg.bs - 1
+    M = cfg.B * R
+    g = workloads.generator(cfg.seed * 1000 + 21, dev)
+    x = (torch.randn(M, cfg.D, generator=g, device=dev) * 2.0).to(torch.bfloat16)
+    gain = (1 + 0.1 * torch.randn(cfg.D, generator=g, device=dev)).to(torch.bfloat16)
+    w = (torch.randn(cfg.V, cfg.D, generator=g, device=dev) * 0.05).to(torch.bfloat16)
+    logits = torch.empty(M, cfg.V, dtype=torch.bfloat16, device=dev)
+    tok = torch.empty(M, dtype=torch.int32, device=dev)
+    ws = torch.empty(dfl.draft_head_workspace_size(cfg.B, R, cfg.D, cfg.V), dtype=torch.uint8, device=dev)
+    st = torch.cuda.Stream(device=dev)
+    call = lambda c: dfl.draft_head(x, gain, w, R, cyc.T, 1234, c, logits=logits, tokens=tok,  # noqa: E731
+                                    workspace=ws, stream=st)
+    with torch.cuda.stream(st):
+        for c in range(3):
+            call(c)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for c in range(iters):
+            call(c)
+        e1.record(st)
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / iters
+    nbytes = cfg.V * cfg.D * 2 + M * cfg.V * 2 + M * cfg.D * 2
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    del x, w, logits, ws
+    torch.cuda.empty_cache()
+    return {"draft_head": {"bound": "hbm", "achieved": gbs, "peak": peak_gbs, "unit": "GB/s", "frac": gbs / peak_gbs,
+                           "ms_per_call": ms, "rows": M, "vocab": cfg.V, "temperature": cyc.T,
+                           "tflops": 2.0 * M * cfg.V * cfg.D / (ms * 1e-3) / 1e12}}
 
 
 def fusion_tensor_rooflines(dev, peak_tflops, iters=10):

@@ -19,8 +19,8 @@ from dataclasses import dataclass
 import torch
 
 __all__ = [
-    "KVCache", "DFlashError", "lib", "fuse_context", "block_attn", "verify",
-    "fuse_context_workspace_size", "block_attn_workspace_size", "verify_workspace_size",
+    "KVCache", "DFlashError", "lib", "fuse_context", "block_attn", "verify", "draft_head",
+    "fuse_context_workspace_size", "block_attn_workspace_size", "verify_workspace_size", "draft_head_workspace_size",
     "philox4x32_10", "read_device_status", "version", "LIB_PATH",
     "DEV_CAPACITY", "DEV_BAD_TOKEN", "DEV_BAD_SEQLEN", "DEV_TIMEOUT",
 ]
@@ -76,6 +76,10 @@ def lib():
     L.dflash_verify_workspace_size.restype = sz
     L.dflash_verify.argtypes = [vp, vp, i32, vp, i32, i32, i32, f32, u64, u64, vp, vp, vp, sz, vp]
     L.dflash_verify.restype = i32
+    L.dflash_draft_head_workspace_size.argtypes = [i32] * 4
+    L.dflash_draft_head_workspace_size.restype = sz
+    L.dflash_draft_head.argtypes = [vp, i32, i32, i32, vp, f32, vp, i32, f32, u64, u64, vp, vp, vp, sz, vp]
+    L.dflash_draft_head.restype = i32
     L.dflash_verify_noalloc_max_scratch.argtypes = []
     L.dflash_verify_noalloc_max_scratch.restype = sz
     L.dflash_verify_noalloc.argtypes = [vp, vp, i32, vp, i32, i32, i32, f32, u64, u64, vp, vp, vp]
@@ -215,6 +219,34 @@ def verify(target_logits, draft_logits, draft_tokens, temperature, seed, cycle, 
                                float(temperature), int(seed), int(cycle), _ptr(accepted_len),
                                _ptr(out_tokens), _ptr(ws), nbytes, _stream(stream)))
     return accepted_len, out_tokens
+
+
+def draft_head_workspace_size(batch, rows_per_seq, d_model, vocab):
+    return lib().dflash_draft_head_workspace_size(batch, rows_per_seq, d_model, vocab)
+
+
+def draft_head(x, g_final, w_head, rows_per_seq, temperature, seed, cycle, eps=1e-6, logits=None, tokens=None,
+               workspace=None, stream=None):
+    """The drafter's head: final RMSNorm, LM head, draft sampling.
+
+    x [B * rows_per_seq, D] bf16 (row b * rows_per_seq + k), w_head [V, D] bf16;
+    returns (logits [B * rows_per_seq, V] bf16, tokens [B * rows_per_seq] int32)."""
+    M, D = x.shape
+    V = w_head.shape[0]
+    if M % rows_per_seq:
+        raise ValueError("rows must be a multiple of rows_per_seq")
+    B = M // rows_per_seq
+    dev = x.device
+    if logits is None:
+        logits = torch.empty(M, V, dtype=torch.bfloat16, device=dev)
+    if tokens is None:
+        tokens = torch.empty(M, dtype=torch.int32, device=dev)
+    nbytes = draft_head_workspace_size(B, rows_per_seq, D, V)
+    ws = _workspace(nbytes, dev, workspace)
+    _check(lib().dflash_draft_head(_ptr(x), B, rows_per_seq, D, _ptr(g_final), float(eps), _ptr(w_head), V,
+                                   float(temperature), int(seed), int(cycle), _ptr(logits), _ptr(tokens),
+                                   _ptr(ws), nbytes, _stream(stream)))
+    return logits, tokens
 
 
 def philox4x32_10(ctr: torch.Tensor, key0: int, key1: int, stream=None) -> torch.Tensor:

@@ -259,6 +259,40 @@ dflash_status dflash_block_attn(int layer, int batch, int block_size, int num_q_
                            static_cast<cudaStream_t>(stream), dev);
 }
 
+// ----------------------------------------------------------- draft head ----
+
+size_t dflash_draft_head_workspace_size(int batch, int rows_per_seq, int d_model, int vocab) {
+  if (batch < 1 || rows_per_seq < 1 || d_model < 1 || vocab < 1) return 0;
+  return head_ws_bytes(batch * rows_per_seq, d_model, vocab);
+}
+
+dflash_status dflash_draft_head(const void* x, int batch, int rows_per_seq, int d_model, const void* g_final,
+                                float eps, const void* w_head, int vocab, float temperature, uint64_t seed,
+                                uint64_t cycle, void* logits_out, int32_t* tokens_out, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  if (batch < 0 || rows_per_seq < 1 || rows_per_seq > 31 || d_model < 1 || vocab < 1)
+    return fail(DFLASH_ERR_INVALID_ARGUMENT, "need batch >= 0, 1 <= rows_per_seq <= 31, d_model, vocab >= 1");
+  if (batch == 0) return DFLASH_OK;
+  if (d_model % 64 || vocab % 128)
+    return fail(DFLASH_ERR_UNSUPPORTED, "draft head needs d_model % 64 == 0 and vocab % 128 == 0");
+  if (double(batch) * rows_per_seq >= 65536.0 * 1024.0)
+    return fail(DFLASH_ERR_UNSUPPORTED, "draft head: too many rows");
+  if (!(temperature >= 0.0f)) return fail(DFLASH_ERR_INVALID_ARGUMENT, "temperature must be >= 0");
+  if (!(eps >= 0.0f)) return fail(DFLASH_ERR_INVALID_ARGUMENT, "eps must be >= 0");
+  if (!x || !w_head || !logits_out || !tokens_out)
+    return fail(DFLASH_ERR_INVALID_ARGUMENT, "NULL x/w_head/logits_out/tokens_out");
+  if (!aligned16(x) || !aligned16(w_head) || !aligned16(logits_out) || (g_final && !aligned16(g_final)))
+    return fail(DFLASH_ERR_INVALID_ARGUMENT, "x, w_head, g_final and logits_out must be 16-byte aligned");
+  const size_t need = head_ws_bytes(batch * rows_per_seq, d_model, vocab);
+  dflash_status s = check_ws(workspace, workspace_bytes, need);
+  if (s) return s;
+  DeviceInfo dev;
+  s = device_info(&dev);
+  if (s) return s;
+  return launch_draft_head(x, batch, rows_per_seq, d_model, g_final, eps, w_head, vocab, temperature, seed, cycle,
+                           logits_out, tokens_out, workspace, static_cast<cudaStream_t>(stream), dev);
+}
+
 // --------------------------------------------------------- fuse context ----
 
 size_t dflash_fuse_context_workspace_size(int total_new, int num_taps, int d_target, int d_model,

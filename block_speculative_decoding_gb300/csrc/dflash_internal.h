@@ -61,6 +61,12 @@ dflash_status launch_block_attn(int layer, int B, int bs, int Hq, const void* q,
                                 float eps, const dflash_kv_cache& c, int window, void* out, void* ws,
                                 cudaStream_t st, const DeviceInfo& dev);
 
+// --- drafter head ------------------------------------------------------------
+size_t head_ws_bytes(int M, int D, int V);
+dflash_status launch_draft_head(const void* x, int B, int rows_per_seq, int D, const void* g_final, float eps,
+                                const void* w_head, int V, float T, uint64_t seed, uint64_t cycle, void* logits,
+                                int32_t* tokens, void* ws, cudaStream_t st, const DeviceInfo& dev);
+
 // --- context fusion ----------------------------------------------------------
 size_t fuse_ws_bytes(int M, int J, int dt_width, int D, int L, int Hkv, dflash_dtype dt);
 dflash_status launch_fuse_context(int J, const void* const* taps, int dt_width, const int32_t* cu_new,

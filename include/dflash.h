@@ -239,6 +239,37 @@ DFLASH_API dflash_status dflash_verify_noalloc(const void* target_logits, const 
 DFLASH_API dflash_status dflash_philox4x32_10(const uint32_t* ctr, uint32_t key0, uint32_t key1,
                                    uint32_t* out, int n, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * 4. The drafter's head: final RMSNorm, LM head and draft sampling.
+ *    E4B page "The released serving cycle" (the drafter proposes the block's
+ *    tokens from its final hidden states through its LM head) and "The
+ *    parameter count exposes the real cost" (the V x D head).
+ *
+ *  x            : [batch * rows_per_seq, d_model] bf16 final hidden states of
+ *                 the proposal rows, row b * rows_per_seq + k = sequence b,
+ *                 proposal k (the block's rows 1 .. bs-1: rows_per_seq = bs-1)
+ *  g_final      : [d_model] final RMSNorm gain (NULL = ones); eps its epsilon
+ *  w_head       : [vocab, d_model] bf16, row v = token v
+ *  temperature  : > 0: token = argmax_y logits[y]/T - ln(-ln U_y), a draw from
+ *                 softmax(logits/T) (the exponential race); U_y from
+ *                 Philox-4x32-10 with key (seed_lo, seed_hi) and counter
+ *                 (y >> 2, (b << 5) | k, cycle_lo, cycle_hi | 2^31), word y & 3,
+ *                 U = ((w >> 8) + 1) * 2^-24 (cycle < 2^63).  == 0: argmax.
+ *                 Ties go to the lowest index.
+ *  logits_out   : [batch * rows_per_seq, vocab] bf16 (the draft logits that
+ *                 dflash_verify takes)
+ *  tokens_out   : device int32 [batch * rows_per_seq], the draft tokens
+ * Constraints: bf16 only; d_model % 64 == 0; vocab % 128 == 0;
+ *              1 <= rows_per_seq <= 31; x, w_head, logits 16-byte aligned.
+ * ------------------------------------------------------------------------- */
+DFLASH_API size_t dflash_draft_head_workspace_size(int batch, int rows_per_seq, int d_model, int vocab);
+
+DFLASH_API dflash_status dflash_draft_head(const void* x, int batch, int rows_per_seq, int d_model,
+                                const void* g_final, float eps, const void* w_head, int vocab,
+                                float temperature, uint64_t seed, uint64_t cycle,
+                                void* logits_out, int32_t* tokens_out,
+                                void* workspace, size_t workspace_bytes, void* stream);
+
 /* Synchronises `stream`, returns the device status word (DFLASH_DEV_* bits)
  * in *flags and clears it on the current device. */
 DFLASH_API dflash_status dflash_read_device_status(uint32_t* flags, void* stream);

@@ -468,18 +468,21 @@ def draft_race_uniforms(seed, cycle, b, k, V):
 DRAFT_TIE_EPS = 1e-4
 
 
-def draft_sample(logits, temperature, seed, cycle, seq_ids=None):
+def draft_sample(logits, temperature, seed, cycle, seq_ids=None, row_ids=None):
     """Draft tokens from the proposal rows' logits [B, R, V].
 
     T > 0: the exponential race -- y* = argmax_y q(y) / E_y with E_y = -ln U_y,
     i.e. argmax_y logits[y] / T - ln(-ln U_y), a draw from softmax(logits / T)
     (no normalisation needed).  T == 0: argmax of the logits.  Ties go to the
     lowest index.  Returns (tokens [B, R] int64, near_tie [B, R] bool): a row is
-    flagged when its two largest keys are within DRAFT_TIE_EPS.
+    flagged when its two largest keys are within DRAFT_TIE_EPS.  seq_ids [B] and
+    row_ids [R] (default 0 .. B-1, 0 .. R-1) are the sequence and proposal-row
+    numbers used in the random-number counter, so that a subset can be checked.
     """
     z = np.asarray(logits, dtype=F64)
     B, R, V = z.shape
     ids = np.arange(B) if seq_ids is None else np.asarray(seq_ids, dtype=np.int64)
+    kid = np.arange(R) if row_ids is None else np.asarray(row_ids, dtype=np.int64)
     T = float(temperature)
     tok = np.zeros((B, R), dtype=np.int64)
     near = np.zeros((B, R), dtype=bool)
@@ -487,7 +490,7 @@ def draft_sample(logits, temperature, seed, cycle, seq_ids=None):
         for k in range(R):
             key = z[b, k].copy()
             if T > 0.0:
-                u = draft_race_uniforms(seed, cycle, ids[b], k, V)
+                u = draft_race_uniforms(seed, cycle, ids[b], kid[k], V)
                 key = key / T - np.log(-np.log(u))
             y = int(np.argmax(key))  # first maximum = lowest index
             tok[b, k] = y

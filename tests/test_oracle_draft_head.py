@@ -75,3 +75,10 @@ def test_race_draws_follow_the_softmax():
         counts[tok[0, 0]] += 1
     chi2 = ((counts - N * p) ** 2 / (N * p)).sum()
     assert stats.chi2.sf(chi2, V - 1) > 1e-3, (counts, N * p)
+
+
+def test_a_subset_of_rows_draws_what_the_whole_batch_draws():
+    z = np.random.default_rng(4).normal(size=(3, 4, 40))
+    full, _ = oracle.draft_sample(z, 0.9, seed=3, cycle=8)
+    part, _ = oracle.draft_sample(z[2:3, 1:3], 0.9, seed=3, cycle=8, seq_ids=[2], row_ids=[1, 2])
+    np.testing.assert_array_equal(part, full[2:3, 1:3])
