@@ -28,6 +28,8 @@ from .dflash_oracle import (  # noqa: F401
     verify,
     VerifyResult,
     draft_head,
+    draft_layer_tail,
+    silu,
     draft_race_uniforms,
     draft_sample,
     DRAFT_TIE_EPS,

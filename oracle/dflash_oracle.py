@@ -428,6 +428,38 @@ def verify(target_logits, draft_logits, draft_tokens, temperature, seed, cycle, 
 #         parameter count exposes the real cost": the head is V x D)
 # --------------------------------------------------------------------------
 
+def silu(z):
+    """z * sigmoid(z)."""
+    z = np.asarray(z, dtype=F64)
+    return z / (1.0 + np.exp(-z))
+
+
+def draft_layer_tail(x, o, w_o, g_post, w_gate, w_up, w_down, eps=1e-6, bf16=False):
+    """The rest of one draft layer after its attention (Qwen3-style layer,
+    [E4B] "The parameter count exposes the real cost": q/k/v/o projections, a
+    gated MLP of intermediate size I, two RMSNorms per layer).
+
+    x [M, D] residual stream of the block rows (row b * bs + j), o [B, Hq, bs,
+    hd] the attention output, w_o [D, Hq*hd], g_post [D], w_gate / w_up [I, D],
+    w_down [D, I]:
+      x1 = x + o_flat w_o^T          (o_flat row b*bs + j = o[b, :, j, :] flattened)
+      h  = RMSNorm(x1) * g_post
+      a  = silu(h w_gate^T) * (h w_up^T)
+      x2 = x1 + a w_down^T
+    Returns (x1, x2).  bf16: x1, h, a and x2 are stored as bfloat16.
+    """
+    rnd = round_to_bf16 if bf16 else (lambda v: v)
+    x = np.asarray(x, dtype=F64)
+    o = np.asarray(o, dtype=F64)
+    B, Hq, bs, hd = o.shape
+    o_flat = o.transpose(0, 2, 1, 3).reshape(B * bs, Hq * hd)
+    x1 = rnd(x + o_flat @ np.asarray(w_o, dtype=F64).T)
+    h = rnd(rms_norm(x1, np.asarray(g_post, dtype=F64), eps))
+    a = rnd(silu(h @ np.asarray(w_gate, dtype=F64).T) * (h @ np.asarray(w_up, dtype=F64).T))
+    x2 = rnd(x1 + a @ np.asarray(w_down, dtype=F64).T)
+    return x1, x2
+
+
 DRAFT_TAG = 0x80000000  # top bit of the fourth counter word: draft sampling
 
 

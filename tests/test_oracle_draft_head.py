@@ -82,3 +82,47 @@ def test_a_subset_of_rows_draws_what_the_whole_batch_draws():
     full, _ = oracle.draft_sample(z, 0.9, seed=3, cycle=8)
     part, _ = oracle.draft_sample(z[2:3, 1:3], 0.9, seed=3, cycle=8, seq_ids=[2], row_ids=[1, 2])
     np.testing.assert_array_equal(part, full[2:3, 1:3])
+
+
+def _tail_case(seed, B=2, Hq=4, bs=3, hd=4, D=8, I=6):
+    rng = np.random.default_rng(seed)
+    return dict(x=rng.normal(size=(B * bs, D)), o=rng.normal(size=(B, Hq, bs, hd)),
+                w_o=rng.normal(size=(D, Hq * hd)) * 0.3, g_post=1 + 0.1 * rng.normal(size=D),
+                w_gate=rng.normal(size=(I, D)), w_up=rng.normal(size=(I, D)), w_down=rng.normal(size=(D, I)) * 0.3)
+
+
+def test_layer_tail_matches_loops():
+    c = _tail_case(0)
+    x1, x2 = oracle.draft_layer_tail(**c)
+    B, Hq, bs, hd = c["o"].shape
+    D, I = c["w_o"].shape[0], c["w_gate"].shape[0]
+    for b in range(B):
+        for j in range(bs):
+            r = b * bs + j
+            ox = [c["o"][b, h, j, e] for h in range(Hq) for e in range(hd)]   # head-major flattening
+            y1 = [c["x"][r, i] + sum(ox[t] * c["w_o"][i, t] for t in range(Hq * hd)) for i in range(D)]
+            assert np.allclose(x1[r], y1, atol=1e-12)
+            ms = sum(v * v for v in y1) / D
+            h = [y1[i] / np.sqrt(ms + 1e-6) * c["g_post"][i] for i in range(D)]
+            a = []
+            for u in range(I):
+                g = sum(h[i] * c["w_gate"][u, i] for i in range(D))
+                up = sum(h[i] * c["w_up"][u, i] for i in range(D))
+                a.append(g / (1 + np.exp(-g)) * up)
+            y2 = [y1[i] + sum(a[u] * c["w_down"][i, u] for u in range(I)) for i in range(D)]
+            assert np.allclose(x2[r], y2, atol=1e-10)
+
+
+def test_layer_tail_special_cases():
+    c = _tail_case(1)
+    # a zero output projection leaves the residual stream; a zero gate zeroes the MLP (silu(0) = 0)
+    z = dict(c, w_o=np.zeros_like(c["w_o"]), w_gate=np.zeros_like(c["w_gate"]))
+    x1, x2 = oracle.draft_layer_tail(**z)
+    np.testing.assert_array_equal(x1, c["x"])
+    np.testing.assert_array_equal(x2, c["x"])
+    # silu: closed values and the limit z * sigmoid(z) -> z
+    np.testing.assert_allclose(oracle.silu([0.0, 1.0, -1.0, 40.0]),
+                               [0.0, 1 / (1 + np.exp(-1)), -1 / (1 + np.e), 40.0], rtol=1e-12)
+    # bf16 storage points
+    x1b, x2b = oracle.draft_layer_tail(**c, bf16=True)
+    np.testing.assert_array_equal(x2b, oracle.round_to_bf16(x2b))
