@@ -19,7 +19,8 @@ from dataclasses import dataclass
 import torch
 
 __all__ = [
-    "KVCache", "DFlashError", "lib", "fuse_context", "block_attn", "verify", "draft_head",
+    "KVCache", "DFlashError", "lib", "fuse_context", "block_attn", "verify", "draft_head", "draft_layer_tail",
+    "interleave_gate_up", "draft_layer_tail_workspace_size",
     "fuse_context_workspace_size", "block_attn_workspace_size", "verify_workspace_size", "draft_head_workspace_size",
     "philox4x32_10", "read_device_status", "version", "LIB_PATH",
     "DEV_CAPACITY", "DEV_BAD_TOKEN", "DEV_BAD_SEQLEN", "DEV_TIMEOUT",
@@ -80,6 +81,10 @@ def lib():
     L.dflash_draft_head_workspace_size.restype = sz
     L.dflash_draft_head.argtypes = [vp, i32, i32, i32, vp, f32, vp, i32, f32, u64, u64, vp, vp, vp, sz, vp]
     L.dflash_draft_head.restype = i32
+    L.dflash_draft_layer_tail_workspace_size.argtypes = [i32] * 5
+    L.dflash_draft_layer_tail_workspace_size.restype = sz
+    L.dflash_draft_layer_tail.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, f32, vp, sz, vp]
+    L.dflash_draft_layer_tail.restype = i32
     L.dflash_verify_noalloc_max_scratch.argtypes = []
     L.dflash_verify_noalloc_max_scratch.restype = sz
     L.dflash_verify_noalloc.argtypes = [vp, vp, i32, vp, i32, i32, i32, f32, u64, u64, vp, vp, vp]
@@ -219,6 +224,29 @@ def verify(target_logits, draft_logits, draft_tokens, temperature, seed, cycle, 
                                float(temperature), int(seed), int(cycle), _ptr(accepted_len),
                                _ptr(out_tokens), _ptr(ws), nbytes, _stream(stream)))
     return accepted_len, out_tokens
+
+
+def interleave_gate_up(w_gate, w_up):
+    """[2I, D] rows in the layer tail's order: 64 gate rows, then the same 64 up rows."""
+    I, D = w_gate.shape
+    return torch.stack([w_gate.view(I // 64, 64, D), w_up.view(I // 64, 64, D)], dim=1).reshape(2 * I, D)
+
+
+def draft_layer_tail_workspace_size(batch, block_size, num_q_heads, d_model, mlp_dim):
+    return lib().dflash_draft_layer_tail_workspace_size(batch, block_size, num_q_heads, d_model, mlp_dim)
+
+
+def draft_layer_tail(x, attn_out, w_o, g_post, w_gate_up, w_down, eps=1e-6, workspace=None, stream=None):
+    """x [B * bs, D] (updated in place to x2), attn_out [B, Hq, bs, 128], w_gate_up from interleave_gate_up."""
+    B, Hq, bs, _ = attn_out.shape
+    D = x.shape[1]
+    I = w_down.shape[1]
+    nbytes = draft_layer_tail_workspace_size(B, bs, Hq, D, I)
+    ws = _workspace(nbytes, x.device, workspace)
+    _check(lib().dflash_draft_layer_tail(_ptr(x), _ptr(attn_out), B, bs, Hq, D, I, _ptr(w_o), _ptr(g_post),
+                                         _ptr(w_gate_up), _ptr(w_down), float(eps), _ptr(ws), nbytes,
+                                         _stream(stream)))
+    return x
 
 
 def draft_head_workspace_size(batch, rows_per_seq, d_model, vocab):

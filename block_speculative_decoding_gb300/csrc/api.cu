@@ -102,6 +102,26 @@ dflash_status make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t row
   return DFLASH_OK;
 }
 
+// A [d3][d2][d1][128] bf16 tensor (d0 = 128 elements innermost) read in boxes of
+// 64 x b1 x 1 x b3 elements, 128-byte swizzle: the rows of a box are (d3, d1)
+// pairs of 128 bytes, as a 2D box of b1 * b3 rows.
+dflash_status make_tmap_bf16_4d(CUtensorMap* map, const void* base, uint64_t d1, uint64_t d2, uint64_t d3,
+                                uint32_t b1, uint32_t b3) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(DFLASH_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  if (reinterpret_cast<uintptr_t>(base) & 15) return fail(DFLASH_ERR_INVALID_ARGUMENT, "TMA tensor base must be 16-byte aligned");
+  cuuint64_t dims[4] = {128, d1, d2, d3};
+  cuuint64_t strides[3] = {128 * 2, d1 * 128 * 2, d2 * d1 * 128 * 2};
+  cuuint32_t box[4] = {64, b1, 1, b3};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(DFLASH_ERR_CUDA, "cuTensorMapEncodeTiled (4D) failed with CUresult " + std::to_string(r));
+  return DFLASH_OK;
+}
+
 // --- philox diagnostic kernel -------------------------------------------------
 
 __global__ void philox_kernel(const uint4* ctr, uint32_t k0, uint32_t k1, uint4* out, int n) {
@@ -257,6 +277,40 @@ dflash_status dflash_block_attn(int layer, int batch, int block_size, int num_q_
   return launch_block_attn(layer, batch, block_size, num_q_heads, q, kb, vb, q_gain, k_gain,
                            rope_theta, eps, *cache, window, out, workspace,
                            static_cast<cudaStream_t>(stream), dev);
+}
+
+// ------------------------------------------------------ draft layer tail ----
+
+size_t dflash_draft_layer_tail_workspace_size(int batch, int block_size, int num_q_heads, int d_model,
+                                              int mlp_dim) {
+  if (batch < 1 || block_size < 1 || num_q_heads < 1 || d_model < 1 || mlp_dim < 1) return 0;
+  return tail_ws_bytes(batch * block_size, d_model, num_q_heads, mlp_dim);
+}
+
+dflash_status dflash_draft_layer_tail(void* x, const void* attn_out, int batch, int block_size, int num_q_heads,
+                                      int d_model, int mlp_dim, const void* w_o, const void* g_post,
+                                      const void* w_gate_up, const void* w_down, float eps, void* workspace,
+                                      size_t workspace_bytes, void* stream) {
+  if (batch < 0 || block_size < 1 || num_q_heads < 1 || d_model < 1 || mlp_dim < 1)
+    return fail(DFLASH_ERR_INVALID_ARGUMENT, "need batch >= 0 and positive sizes");
+  if (batch == 0) return DFLASH_OK;
+  if (d_model % 128 || d_model > 4096 || mlp_dim % 64 || 128 % block_size)
+    return fail(DFLASH_ERR_UNSUPPORTED,
+                "layer tail needs d_model % 128 == 0 (<= 4096), mlp_dim % 64 == 0, 128 % block_size == 0");
+  if (!(eps >= 0.0f)) return fail(DFLASH_ERR_INVALID_ARGUMENT, "eps must be >= 0");
+  if (!x || !attn_out || !w_o || !w_gate_up || !w_down)
+    return fail(DFLASH_ERR_INVALID_ARGUMENT, "NULL x/attn_out/w_o/w_gate_up/w_down");
+  if (!aligned16(x) || !aligned16(attn_out) || !aligned16(w_o) || !aligned16(w_gate_up) || !aligned16(w_down) ||
+      (g_post && !aligned16(g_post)))
+    return fail(DFLASH_ERR_INVALID_ARGUMENT, "pointers must be 16-byte aligned");
+  const size_t need = tail_ws_bytes(batch * block_size, d_model, num_q_heads, mlp_dim);
+  dflash_status s = check_ws(workspace, workspace_bytes, need);
+  if (s) return s;
+  DeviceInfo dev;
+  s = device_info(&dev);
+  if (s) return s;
+  return launch_layer_tail(x, attn_out, batch, block_size, num_q_heads, d_model, mlp_dim, w_o, g_post, w_gate_up,
+                           w_down, eps, workspace, static_cast<cudaStream_t>(stream), dev);
 }
 
 // ----------------------------------------------------------- draft head ----

@@ -31,6 +31,8 @@ dflash_status device_info(DeviceInfo* out);
 // the 128-byte swizzle (box_cols * 2 must be 128).  Out-of-range rows read 0.
 dflash_status make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                                 uint32_t box_rows, uint32_t box_cols);
+dflash_status make_tmap_bf16_4d(CUtensorMap* map, const void* base, uint64_t d1, uint64_t d2, uint64_t d3,
+                                uint32_t b1, uint32_t b3);
 
 // Workspace carving: 256-byte aligned sub-buffers.
 struct WsCarver {
@@ -66,6 +68,12 @@ size_t head_ws_bytes(int M, int D, int V);
 dflash_status launch_draft_head(const void* x, int B, int rows_per_seq, int D, const void* g_final, float eps,
                                 const void* w_head, int V, float T, uint64_t seed, uint64_t cycle, void* logits,
                                 int32_t* tokens, void* ws, cudaStream_t st, const DeviceInfo& dev);
+
+// --- draft layer remainder ---------------------------------------------------
+size_t tail_ws_bytes(int M, int D, int Hq, int I);
+dflash_status launch_layer_tail(void* x, const void* attn_out, int B, int bs, int Hq, int D, int I, const void* w_o,
+                                const void* g_post, const void* w_gate_up, const void* w_down, float eps, void* ws,
+                                cudaStream_t st, const DeviceInfo& dev);
 
 // --- context fusion ----------------------------------------------------------
 size_t fuse_ws_bytes(int M, int J, int dt_width, int D, int L, int Hkv, dflash_dtype dt);

@@ -37,7 +37,11 @@ struct GemmArgs {
                            // (tile, K block) space
   int dp_tiles;            // stream_k: leading tiles scheduled whole, a multiple of the share count
   int* pieces;             // stream_k: [m_tiles * n_tiles] number of slots written for the tile
-  int epi;                 // 0: fp32 partial store, 1: K/V cache epilogue, 2: drafter logits + draft race
+  int epi;                 // 0: fp32 partial store, 1: K/V cache epilogue, 2: drafter logits + draft race,
+                           // 3: SwiGLU (columns 64t.. of a 128-column unit gate, the next 64 up)
+  int a4d_bs;              // > 0: A is an attention output [B][Hq][a4d_bs][128] read through a 4D map
+                           // (row b * bs + j, K index h * 128 + e); 0: A is a row-major 2D tensor
+  __nv_bfloat16* act;      // epi 3: [M][N / 2] bf16
   int pdl;                 // launched as a programmatic dependent (waits for the preceding grid before any load)
   int prefetch_b;          // the B operand (weights) may be loaded before that wait
   float* out_f32;          // epi 0: [k_splits][M][N]
@@ -228,6 +232,41 @@ __device__ __forceinline__ void head_epilogue(uint32_t taddr, int col0, int row,
   if (live) p.race[static_cast<size_t>(row) * p.n_tiles + n_tile] = make_float2(best, __int_as_float(best_col));
 }
 
+// SwiGLU of this thread's row: in every 128 columns of the unit, the first 64
+// are gate values and the next 64 the up values of the same 64 outputs
+// (the weight rows are interleaved that way); out = silu(gate) * up, bf16.
+template <int BN>
+__device__ __forceinline__ void swiglu_epilogue(uint32_t taddr, int n_tile, int row, const GemmArgs& p) {
+  // every lane takes part in the tensor-memory loads (warp-collective); only
+  // the rows of the problem store
+  const bool live = row < p.M;
+  const int I = p.N / 2;
+#pragma unroll 1
+  for (int blk = 0; blk < BN / 128; ++blk) {
+    __nv_bfloat16* dst = p.act + static_cast<size_t>(live ? row : 0) * I + (n_tile * BN + blk * 128) / 2;
+#pragma unroll 1
+    for (int c = 0; c < 2; ++c) {
+      uint32_t g[32], u[32];
+      tmem_ld_32cols(taddr + blk * 128 + c * 32, g);
+      tmem_ld_32cols(taddr + blk * 128 + 64 + c * 32, u);
+      tmem_ld_wait();
+      uint32_t o[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float g0 = __uint_as_float(g[2 * j]), g1 = __uint_as_float(g[2 * j + 1]);
+        const float a0 = g0 / (1.0f + __expf(-g0)) * __uint_as_float(u[2 * j]);
+        const float a1 = g1 / (1.0f + __expf(-g1)) * __uint_as_float(u[2 * j + 1]);
+        o[j] = pack_bf16x2(a0, a1);
+      }
+      if (live) {
+        uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) d4[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+      }
+    }
+  }
+}
+
 // Epilogue of one 128-column head of the K/V projection for this thread's row.
 __device__ __forceinline__ void kv_head_epilogue(uint32_t taddr, int col0, int row, const GemmArgs& p) {
   const int hidx = col0 / HD;
@@ -392,8 +431,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
           const uint32_t sa = base + stage * STAGE;
           const int seg = kb / p.kb_per_seg;
 #pragma unroll
-          for (int mt = 0; mt < MT; ++mt)
-            tma_load_2d(sa + mt * A_BYTES, &amaps.a[seg], fb, (kb - seg * p.kb_per_seg) * kBK, (m * MT + mt) * kBM);
+          for (int mt = 0; mt < MT; ++mt) {
+            if (p.a4d_bs > 0)  // K block kb = (head kb / 2, dims (kb % 2) * 64 ..), rows = (sequence, block row)
+              tma_load_4d(sa + mt * A_BYTES, &amaps.a[0], fb, (kb & 1) * 64, 0, kb >> 1,
+                          (m * MT + mt) * kBM / p.a4d_bs);
+            else
+              tma_load_2d(sa + mt * A_BYTES, &amaps.a[seg], fb, (kb - seg * p.kb_per_seg) * kBK, (m * MT + mt) * kBM);
+          }
           if (!b_done) tma_load_2d(sa + MT * A_BYTES, &bmap, fb, kb * kBK, n * BN);
           if (++stage == STAGES) {
             stage = 0;
@@ -472,8 +516,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
         } else if (p.epi == 1) {
 #pragma unroll 1
           for (int hh = 0; hh < BN / HD; ++hh) kv_head_epilogue(taddr + hh * HD, n * BN + hh * HD, row, p);
-        } else {
+        } else if (p.epi == 2) {
           head_epilogue<BN>(taddr, n * BN, row, n, p);
+        } else {
+          swiglu_epilogue<BN>(taddr, n, row, p);
         }
       }
       tc_fence_before_sync();

@@ -1,0 +1,231 @@
+// The rest of a draft layer after its attention: output projection and
+// residual, post-attention RMSNorm, SwiGLU MLP and residual.
+//
+// Pages: "Nemotron 3.5 Bolt E4B: Block-Parallel Speculation with DFlash",
+// section "The parameter count exposes the real cost" (a Qwen3-style layer:
+// q/k/v/o projections, a gated MLP, two RMSNorms; the MLP's intermediate size
+// 5120 closes the printed parameter count) and "The released serving cycle"
+// (the drafter runs its layers over the block).
+//
+// Five launches chained as programmatic dependents (M = B * bs block rows):
+//   1. gemm_tc   Y = o W_o^T, split K; the attention output [B][Hq][bs][128]
+//                is read through a 4D tensor map (rows (b, j), K = (h, e)),
+//                never copied -> fp32 partial slots
+//   2. resnorm   x1 = bf16(x + sum of the slots), written back to x;
+//                h = bf16(RMSNorm(x1) * g_post)
+//   3. gemm_tc   act = bf16(silu(h W_gate^T) * (h W_up^T)): the weight rows are
+//                interleaved in 64-row blocks, so each 128-column unit holds
+//                the gate and up values of the same 64 outputs (epilogue 3)
+//   4. gemm_tc   Y = act W_down^T, split K -> slots
+//   5. resnorm   x2 = bf16(x1 + sum of the slots) -> x
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "dflash_device.cuh"
+#include "dflash_internal.h"
+#include "gemm_tc.cuh"
+
+namespace dflash {
+namespace {
+
+constexpr int kResThreads = 256;
+constexpr int kResSlots = 4;  // float4 slots per thread: rows up to 4096 wide
+
+// One CTA per row m: x1 = bf16(x + sum_s part[s]) (written to x); with g_mode,
+// h = bf16(x1 * rsqrt(mean(x1^2) + eps) * g), g == nullptr meaning ones.
+__global__ void __launch_bounds__(kResThreads) resnorm_kernel(const float* __restrict__ part, int k_splits, int M,
+                                                             int D, __nv_bfloat16* __restrict__ x, int g_mode,
+                                                             const __nv_bfloat16* __restrict__ g, float eps,
+                                                             __nv_bfloat16* __restrict__ h) {
+  pdl_wait_primary();
+  pdl_launch_dependents();
+  const int m = blockIdx.x;
+  const int nv = D / 4;
+  const float4* pr = reinterpret_cast<const float4*>(part + static_cast<size_t>(m) * D);
+  const size_t stride = static_cast<size_t>(M) * D / 4;
+  uint2* xr = reinterpret_cast<uint2*>(x + static_cast<size_t>(m) * D);
+  float4 y[kResSlots];
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < kResSlots; ++i) {
+    const int v = threadIdx.x + i * kResThreads;
+    y[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (v < nv) {
+      float4 t = pr[v];
+      for (int s = 1; s < k_splits; ++s) {
+        const float4 u = pr[s * stride + v];
+        t.x += u.x;
+        t.y += u.y;
+        t.z += u.z;
+        t.w += u.w;
+      }
+      const uint2 xv = xr[v];
+      const uint32_t lo = pack_bf16x2(bf16_lo(xv.x) + t.x, bf16_hi(xv.x) + t.y);
+      const uint32_t hi = pack_bf16x2(bf16_lo(xv.y) + t.z, bf16_hi(xv.y) + t.w);
+      xr[v] = make_uint2(lo, hi);
+      y[i] = make_float4(bf16_lo(lo), bf16_hi(lo), bf16_lo(hi), bf16_hi(hi));  // the stored x1
+      ss += y[i].x * y[i].x + y[i].y * y[i].y + y[i].z * y[i].z + y[i].w * y[i].w;
+    }
+  }
+  if (!g_mode) return;
+  ss = warp_sum(ss);
+  __shared__ float red[kResThreads / 32];
+  if (threadIdx.x % 32 == 0) red[threadIdx.x / 32] = ss;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < kResThreads / 32; ++w) tot += red[w];
+  const float r = rsqrtf(tot / static_cast<float>(D) + eps);
+  uint2* hr = reinterpret_cast<uint2*>(h + static_cast<size_t>(m) * D);
+#pragma unroll
+  for (int i = 0; i < kResSlots; ++i) {
+    const int v = threadIdx.x + i * kResThreads;
+    if (v >= nv) continue;
+    float g4[4] = {1.f, 1.f, 1.f, 1.f};
+    if (g) {
+      const uint2 gv = reinterpret_cast<const uint2*>(g)[v];
+      g4[0] = bf16_lo(gv.x);
+      g4[1] = bf16_hi(gv.x);
+      g4[2] = bf16_lo(gv.y);
+      g4[3] = bf16_hi(gv.y);
+    }
+    hr[v] = make_uint2(pack_bf16x2(y[i].x * r * g4[0], y[i].y * r * g4[1]),
+                       pack_bf16x2(y[i].z * r * g4[2], y[i].w * r * g4[3]));
+  }
+}
+
+struct TailPlan {
+  int mt, m_tiles, ks_o, ks_down;
+};
+
+TailPlan tail_plan(int M, int D, int Kq, int I) {
+  TailPlan t;
+  t.mt = M <= 2 * kBM ? 2 : 1;
+  t.m_tiles = (M + t.mt * kBM - 1) / (t.mt * kBM);
+  const int tiles = t.m_tiles * (D / 128);
+  const int ks = std::max(1, std::min(16, kSplitTarget / std::max(1, tiles)));
+  t.ks_o = std::min(ks, Kq / kBK);
+  t.ks_down = std::min(ks, I / kBK);
+  return t;
+}
+
+dflash_status launch_resnorm(const float* part, int k_splits, int M, int D, __nv_bfloat16* x, int g_mode,
+                             const __nv_bfloat16* g, float eps, __nv_bfloat16* h, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(M));
+  cfg.blockDim = dim3(kResThreads);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, resnorm_kernel, part, k_splits, M, D, x, g_mode, g, eps, h);
+  return e == cudaSuccess ? DFLASH_OK : cuda_fail(e, "resnorm_kernel launch");
+}
+
+template <int MT>
+dflash_status run_gemm(const TmapPack& am, const CUtensorMap& bm, const GemmArgs& a, cudaStream_t st,
+                       const DeviceInfo& dev) {
+  return MT == 2 ? launch_gemm<128, 4, 2>(am, bm, a, st, dev) : launch_gemm<128, 6, 1>(am, bm, a, st, dev);
+}
+
+}  // namespace
+
+size_t tail_ws_bytes(int M, int D, int Hq, int I) {
+  const TailPlan t = tail_plan(M, D, Hq * 128, I);
+  return align256(static_cast<size_t>(std::max(t.ks_o, t.ks_down)) * M * D * sizeof(float)) +
+         align256(static_cast<size_t>(M) * D * sizeof(__nv_bfloat16)) +
+         align256(static_cast<size_t>(M) * I * sizeof(__nv_bfloat16)) + 256;
+}
+
+dflash_status launch_layer_tail(void* x, const void* attn_out, int B, int bs, int Hq, int D, int I, const void* w_o,
+                                const void* g_post, const void* w_gate_up, const void* w_down, float eps, void* ws,
+                                cudaStream_t st, const DeviceInfo& dev) {
+  const int M = B * bs, Kq = Hq * 128;
+  const TailPlan t = tail_plan(M, D, Kq, I);
+  WsCarver w(ws);
+  float* part = w.take<float>(static_cast<size_t>(std::max(t.ks_o, t.ks_down)) * M * D);
+  auto* h = w.take<__nv_bfloat16>(static_cast<size_t>(M) * D);
+  auto* act = w.take<__nv_bfloat16>(static_cast<size_t>(M) * I);
+  auto* xb = static_cast<__nv_bfloat16*>(x);
+
+  // 1. output projection, A through a 4D map of the attention output
+  TmapPack am{};
+  dflash_status s = make_tmap_bf16_4d(&am.a[0], attn_out, static_cast<uint64_t>(bs), static_cast<uint64_t>(Hq),
+                                      static_cast<uint64_t>(B), static_cast<uint32_t>(bs),
+                                      static_cast<uint32_t>(kBM / bs));
+  if (s) return s;
+  CUtensorMap bm;
+  s = make_tmap_bf16_2d(&bm, w_o, static_cast<uint64_t>(D), Kq, 128, kBK);
+  if (s) return s;
+  GemmArgs a{};
+  a.M = M;
+  a.N = D;
+  a.num_kb = Kq / kBK;
+  a.kb_per_seg = a.num_kb;
+  a.k_splits = t.ks_o;
+  a.m_tiles = t.m_tiles;
+  a.n_tiles = D / 128;
+  a.epi = 0;
+  a.a4d_bs = bs;
+  a.pdl = 1;  // nothing is loaded before the preceding grid (the attention) has completed
+  a.out_f32 = part;
+  a.status = dev.status;
+  s = t.mt == 2 ? run_gemm<2>(am, bm, a, st, dev) : run_gemm<1>(am, bm, a, st, dev);
+  if (s) return s;
+  // 2. residual + post-attention norm
+  s = launch_resnorm(part, t.ks_o, M, D, xb, 1, static_cast<const __nv_bfloat16*>(g_post), eps, h, st);
+  if (s) return s;
+  // 3. gate/up with SwiGLU
+  TmapPack hm{};
+  s = make_tmap_bf16_2d(&hm.a[0], h, static_cast<uint64_t>(M), D, kBM, kBK);
+  if (s) return s;
+  CUtensorMap gm;
+  s = make_tmap_bf16_2d(&gm, w_gate_up, static_cast<uint64_t>(2) * I, D, 128, kBK);
+  if (s) return s;
+  GemmArgs gu{};
+  gu.M = M;
+  gu.N = 2 * I;
+  gu.num_kb = D / kBK;
+  gu.kb_per_seg = gu.num_kb;
+  gu.k_splits = 1;
+  gu.m_tiles = t.m_tiles;
+  gu.n_tiles = 2 * I / 128;
+  gu.epi = 3;
+  gu.pdl = 1;
+  gu.prefetch_b = 1;
+  gu.act = act;
+  gu.status = dev.status;
+  s = t.mt == 2 ? run_gemm<2>(hm, gm, gu, st, dev) : run_gemm<1>(hm, gm, gu, st, dev);
+  if (s) return s;
+  // 4. down projection
+  TmapPack xm{};
+  s = make_tmap_bf16_2d(&xm.a[0], act, static_cast<uint64_t>(M), I, kBM, kBK);
+  if (s) return s;
+  CUtensorMap dm;
+  s = make_tmap_bf16_2d(&dm, w_down, static_cast<uint64_t>(D), I, 128, kBK);
+  if (s) return s;
+  GemmArgs dn{};
+  dn.M = M;
+  dn.N = D;
+  dn.num_kb = I / kBK;
+  dn.kb_per_seg = dn.num_kb;
+  dn.k_splits = t.ks_down;
+  dn.m_tiles = t.m_tiles;
+  dn.n_tiles = D / 128;
+  dn.epi = 0;
+  dn.pdl = 1;
+  dn.prefetch_b = 1;
+  dn.out_f32 = part;
+  dn.status = dev.status;
+  s = t.mt == 2 ? run_gemm<2>(xm, dm, dn, st, dev) : run_gemm<1>(xm, dm, dn, st, dev);
+  if (s) return s;
+  // 5. residual
+  return launch_resnorm(part, t.ks_down, M, D, xb, 0, nullptr, eps, nullptr, st);
+}
+
+}  // namespace dflash

@@ -240,6 +240,34 @@ DFLASH_API dflash_status dflash_philox4x32_10(const uint32_t* ctr, uint32_t key0
                                    uint32_t* out, int n, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * 5. The rest of a draft layer after its attention (E4B page "The parameter
+ *    count exposes the real cost": a Qwen3-style layer, gated MLP of
+ *    intermediate size 5120):
+ *      x1 = x + o W_o^T;  h = RMSNorm(x1) * g_post;
+ *      x2 = x1 + (silu(h W_gate^T) * (h W_up^T)) W_down^T
+ *
+ *  x          : [batch * block_size, d_model] bf16 residual stream of the
+ *               block rows (row b * block_size + j); overwritten with x2
+ *  attn_out   : [batch, num_q_heads, block_size, 128] bf16 (dflash_block_attn's out)
+ *  w_o        : [d_model, num_q_heads * 128]
+ *  g_post     : [d_model] post-attention RMSNorm gain (NULL = ones)
+ *  w_gate_up  : [2 * mlp_dim, d_model], gate and up rows interleaved in blocks of
+ *               64: rows 128t .. 128t+63 = gate rows 64t .. 64t+63, rows
+ *               128t+64 .. 128t+127 = up rows 64t .. 64t+63
+ *  w_down     : [d_model, mlp_dim]
+ * bf16 storage points: x1, the normalised rows, the SwiGLU activations, x2.
+ * Constraints: bf16; d_model % 128 == 0 and <= 4096; mlp_dim % 64 == 0;
+ *              128 % block_size == 0; all pointers 16-byte aligned.
+ * ------------------------------------------------------------------------- */
+DFLASH_API size_t dflash_draft_layer_tail_workspace_size(int batch, int block_size, int num_q_heads, int d_model,
+                                              int mlp_dim);
+
+DFLASH_API dflash_status dflash_draft_layer_tail(void* x, const void* attn_out, int batch, int block_size,
+                                      int num_q_heads, int d_model, int mlp_dim, const void* w_o,
+                                      const void* g_post, const void* w_gate_up, const void* w_down, float eps,
+                                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * 4. The drafter's head: final RMSNorm, LM head and draft sampling.
  *    E4B page "The released serving cycle" (the drafter proposes the block's
  *    tokens from its final hidden states through its LM head) and "The
