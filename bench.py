@@ -266,6 +266,7 @@ def run_gpu(args):
         tensor_lines = fusion_tensor_rooflines(dev, peaks()[1])
         tensor_lines.update(window_attention_roofline(cyc, dev, peaks()[0]))
         tensor_lines.update(draft_head_roofline(cyc, dev, peaks()[0]))
+        tensor_lines.update(layer_tail_roofline(cyc, dev, peaks()[0], peaks()[1]))
 
     if rank != 0:
         return
@@ -393,6 +394,46 @@ def draft_head_roofline(cyc, dev, peak_gbs, iters=10):
     return {"draft_head": {"bound": "hbm", "achieved": gbs, "peak": peak_gbs, "unit": "GB/s", "frac": gbs / peak_gbs,
                            "ms_per_call": ms, "rows": M, "vocab": cfg.V, "temperature": cyc.T,
                            "tflops": 2.0 * M * cfg.V * cfg.D / (ms * 1e-3) / 1e12}}
+
+
+def layer_tail_roofline(cyc, dev, peak_gbs, peak_tflops, iters=20):
+    """The rest of one draft layer on the batched workload's block rows: M = B x bs
+    rows, 32 heads of 128, D = 2560, MLP width I = 5120 (output projection +
+    residual, post-attention RMSNorm, SwiGLU MLP + residual).  Algorithmic bytes:
+    the weights (D Hq 128 + 3 I D) x 2 read once, the attention output M Hq 128 x 2
+    read, the residual rows M D x 2 read and written; flops 2 M (Hq 128 D + 3 I D).
+    CUDA events on the launching stream, 3 warm-up calls."""
+    import block_speculative_decoding_gb300 as dfl
+    cfg = cyc.cfg
+    M, D, I, Kq = cfg.B * cfg.bs, cfg.D, cfg.mlp_dim, cfg.Hq * cfg.d
+    g = workloads.generator(cfg.seed * 1000 + 23, dev)
+    r = lambda *s, std=1.0: (torch.randn(*s, generator=g, device=dev) * std).to(torch.bfloat16)  # noqa: E731
+    x, o = r(M, D, std=2.0), r(cfg.B, cfg.Hq, cfg.bs, cfg.d)
+    w_o, w_gu, w_dn = r(D, Kq, std=0.02), r(2 * I, D, std=0.05), r(D, I, std=0.02)
+    g_post = (1 + 0.1 * torch.randn(D, generator=g, device=dev)).to(torch.bfloat16)
+    ws = torch.empty(dfl.draft_layer_tail_workspace_size(cfg.B, cfg.bs, cfg.Hq, D, I), dtype=torch.uint8, device=dev)
+    st = torch.cuda.Stream(device=dev)
+    call = lambda: dfl.draft_layer_tail(x, o, w_o, g_post, w_gu, w_dn, workspace=ws, stream=st)  # noqa: E731
+    with torch.cuda.stream(st):
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for _ in range(iters):
+            call()
+        e1.record(st)
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / iters
+    nbytes = (D * Kq + 3 * I * D) * 2 + M * Kq * 2 + 2 * M * D * 2
+    flops = 2.0 * M * (Kq * D + 3 * I * D)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    tf = flops / (ms * 1e-3) / 1e12
+    del x, o, w_o, w_gu, w_dn, ws
+    torch.cuda.empty_cache()
+    return {"draft_layer_tail": {"bound": "hbm", "achieved": gbs, "peak": peak_gbs, "unit": "GB/s",
+                                 "frac": gbs / peak_gbs, "ms_per_call": ms, "rows": M, "mlp_dim": I,
+                                 "tflops": tf, "tensor_frac": tf / peak_tflops}}
 
 
 def fusion_tensor_rooflines(dev, peak_tflops, iters=10):

@@ -344,6 +344,22 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Bidirectional proxy fence between the generic and the async proxy, all
+// state spaces (generic accesses before it are ordered with async-proxy
+// accesses after it, such as bulk copies).
+__device__ __forceinline__ void fence_proxy_async_all() {
+  asm volatile("fence.proxy.async;" ::: "memory");
+}
+
+// Bulk copy without a tensor map: `bytes` (a multiple of 16; both addresses
+// 16-byte aligned) from global to this CTA's shared memory, completing on the
+// mbarrier's transaction count.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
 // Programmatic dependent launch: let the next kernel in the stream start /
 // wait for the previous kernel's completion and memory.
 __device__ __forceinline__ void pdl_launch_dependents() {

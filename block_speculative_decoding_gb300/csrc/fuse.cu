@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(kNormThreads) fuse_rownorm_kernel(
     int n_tiles, int M, int D, const TG* __restrict__ g, float eps,
     TH* __restrict__ ht, TH* __restrict__ ht_out, const int32_t* __restrict__ cu_new,
     const int32_t* __restrict__ seq_len, int B, int cap, int ring, InvFreq inv, int2* __restrict__ rowinfo,
-    float2* __restrict__ rope_cs, unsigned* status) {
+    float2* __restrict__ rope_cs, int* __restrict__ zero_flags, int n_zero, unsigned* status) {
   const int m = blockIdx.x;
   if (threadIdx.x <= HD / 2) {
     int lo = 0, hi = B - 1;
@@ -92,6 +92,9 @@ __global__ void __launch_bounds__(kNormThreads) fuse_rownorm_kernel(
   }
   pdl_launch_dependents();
   pdl_wait_primary();  // the partials of the fusion GEMM
+  // the fixup flags of the K/V GEMM that follows (every earlier grid has completed)
+  if (m == 0)
+    for (int i = threadIdx.x; i < n_zero; i += kNormThreads) zero_flags[i] = 0;
   const int nv = D / 4;  // float4 slots of the row
   const float4* prow = reinterpret_cast<const float4*>(part + static_cast<size_t>(m) * D);
   const size_t split_stride = static_cast<size_t>(M) * D / 4;
@@ -280,9 +283,10 @@ __global__ void __launch_bounds__(256) kv_store_f32_kernel(const float* __restri
 // meeting one tile.
 struct FusePlan {
   int fuse_mt, fuse_bn, fuse_m_tiles, fuse_n_tiles, k_splits, kv_bn, stream_k, shares, dp_tiles;
+  int kv_mt, kv_m_tiles, kv_n_tiles, kv_shares;  // K/V GEMM: stream-K with fixup over kv_shares CTAs
 };
 
-FusePlan plan(int M, int D, int num_kb) {
+FusePlan plan(int M, int D, int num_kb, int n_kv) {
   FusePlan f;
   f.fuse_mt = M <= 2 * kBM ? 2 : 1;
   f.fuse_m_tiles = (M + f.fuse_mt * kBM - 1) / (f.fuse_mt * kBM);
@@ -303,6 +307,10 @@ FusePlan plan(int M, int D, int num_kb) {
       f.k_splits = std::max(f.k_splits, static_cast<int>(share((t + 1) * num_kb - 1) - share(t * num_kb) + 1));
   }
   f.kv_bn = M <= 2 * kBM ? 128 : 256;
+  f.kv_mt = M <= 2 * kBM ? 2 : 1;
+  f.kv_m_tiles = (M + f.kv_mt * kBM - 1) / (f.kv_mt * kBM);
+  f.kv_n_tiles = n_kv / f.kv_bn;
+  f.kv_shares = fixup_shares(f.kv_m_tiles * f.kv_n_tiles, D / kBK);
   return f;
 }
 
@@ -314,8 +322,9 @@ size_t fuse_ws_bytes(int M, int J, int dt_width, int D, int L, int Hkv, dflash_d
   size_t s = align256(static_cast<size_t>(M) * sizeof(int2)) +
              align256(static_cast<size_t>(M) * (HD / 2) * sizeof(float2));
   if (dt == DFLASH_BF16) {
-    const FusePlan f = plan(M, D, J * dt_width / kBK);
-    s += align256(static_cast<size_t>(f.k_splits) * M * D * sizeof(float)) +
+    const FusePlan f = plan(M, D, J * dt_width / kBK, Ntot);
+    s += (f.kv_mt == 2 ? fixup_ws_bytes<128, 2>(f.kv_shares) : fixup_ws_bytes<256, 1>(f.kv_shares)) +
+         align256(static_cast<size_t>(f.k_splits) * M * D * sizeof(float)) +
          align256(static_cast<size_t>(M) * D * sizeof(__nv_bfloat16)) +
          align256(static_cast<size_t>(f.fuse_m_tiles) * f.fuse_n_tiles * sizeof(int));
   } else {
@@ -348,7 +357,7 @@ dflash_status launch_fuse_context(int J, const void* const* taps, int dt_width, 
         segs, dt_width, static_cast<const float*>(w_fuse), M, D, J * dt_width, Y);
     fuse_rownorm_kernel<float, float><<<M, kNormThreads, 0, st>>>(
         Y, 1, nullptr, kBM, D, 1, M, D, static_cast<const float*>(g_fuse), eps, H, static_cast<float*>(h_t_out), cu_new, c.seq_len, B,
-        c.capacity, c.ring, inv, rowinfo, rope_cs, dev.status);
+        c.capacity, c.ring, inv, rowinfo, rope_cs, nullptr, 0, dev.status);
     F32Segs hs{};
     hs.a[0] = H;
     simt_gemm_f32_kernel<<<dim3((Ntot + 63) / 64, (M + 63) / 64), 256, 0, st>>>(
@@ -361,11 +370,13 @@ dflash_status launch_fuse_context(int J, const void* const* taps, int dt_width, 
     return e == cudaSuccess ? DFLASH_OK : cuda_fail(e, "fp32 fusion launch");
   }
 
-  const FusePlan f = plan(M, D, J * dt_width / kBK);
+  const FusePlan f = plan(M, D, J * dt_width / kBK, Ntot);
   if (D % 4 != 0) return fail(DFLASH_ERR_UNSUPPORTED, "fusion: d_model must be a multiple of 4");
   float* Ypart = w.take<float>(static_cast<size_t>(f.k_splits) * M * D);
   auto* H = w.take<__nv_bfloat16>(static_cast<size_t>(M) * D);
   int* tile_pieces = w.take<int>(static_cast<size_t>(f.fuse_m_tiles) * f.fuse_n_tiles);
+  GemmArgs k{};
+  if (f.kv_mt == 2) fixup_take<128, 2>(w, f.kv_shares, k); else fixup_take<256, 1>(w, f.kv_shares, k);
 
   // 1. fusion GEMM: A = the J taps (one tensor map each), B = W_c [D][J*dt]
   TmapPack am{};
@@ -389,7 +400,8 @@ dflash_status launch_fuse_context(int J, const void* const* taps, int dt_width, 
   a.m_tiles = f.fuse_m_tiles;
   a.n_tiles = f.fuse_n_tiles;
   a.epi = 0;
-  a.pdl = 1;  // its CTAs may start while the preceding kernel finishes; nothing is loaded before it has
+  a.pdl = 1;  // its CTAs may start while the preceding kernel finishes; the taps are loaded after it has,
+  a.prefetch_b = 1;  // the weights (which no kernel of the chain writes) before
   a.out_f32 = Ypart;
   a.status = dev.status;
   s = f.fuse_mt == 2 ? launch_gemm<128, 4, 2>(am, bm, a, st, dev) : launch_gemm<256, 4, 1>(am, bm, a, st, dev);
@@ -412,7 +424,7 @@ dflash_status launch_fuse_context(int J, const void* const* taps, int dt_width, 
                                         f.fuse_bn, f.fuse_n_tiles, M, D,
                                         static_cast<const __nv_bfloat16*>(g_fuse), eps, H,
                                         static_cast<__nv_bfloat16*>(h_t_out), cu_new, c.seq_len, B, c.capacity,
-                                        c.ring, inv, rowinfo, rope_cs, dev.status);
+                                        c.ring, inv, rowinfo, rope_cs, k.fix_flag, f.kv_shares, dev.status);
     if (le != cudaSuccess) return cuda_fail(le, "fuse_rownorm_kernel launch");
   }
 
@@ -423,14 +435,12 @@ dflash_status launch_fuse_context(int J, const void* const* taps, int dt_width, 
   CUtensorMap wm;
   s = make_tmap_bf16_2d(&wm, w_kv, static_cast<uint64_t>(Ntot), D, f.kv_bn, kBK);
   if (s) return s;
-  GemmArgs k{};
   k.M = M;
   k.N = Ntot;
   k.num_kb = D / kBK;
   k.kb_per_seg = k.num_kb;
-  k.k_splits = 1;
-  k.m_tiles = (M + kBM - 1) / kBM;
-  k.n_tiles = Ntot / f.kv_bn;
+  k.m_tiles = f.kv_m_tiles;
+  k.n_tiles = f.kv_n_tiles;
   k.epi = 1;
   k.pdl = 1;
   k.prefetch_b = 1;
@@ -445,7 +455,7 @@ dflash_status launch_fuse_context(int J, const void* const* taps, int dt_width, 
   k.k_gain = static_cast<const __nv_bfloat16*>(k_gain);
   k.eps = eps;
   k.status = dev.status;
-  return f.kv_bn == 256 ? launch_gemm<256, 4, 1>(hm, wm, k, st, dev) : launch_gemm<128, 6, 1>(hm, wm, k, st, dev);
+  return f.kv_mt == 2 ? launch_gemm<128, 4, 2>(hm, wm, k, st, dev) : launch_gemm<256, 4, 1>(hm, wm, k, st, dev);
 }
 
 }  // namespace dflash

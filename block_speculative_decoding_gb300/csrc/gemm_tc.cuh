@@ -2,8 +2,10 @@
 // head: a TMA producer warp, one MMA-issuing thread, four epilogue warps;
 // operands staged by TMA in a shared-memory ring (128-byte swizzle, K-major),
 // accumulators in tensor memory (double-buffered when they fit), plain or
-// stream-K schedules, and three epilogues (fp32 partial sums, the K/V cache
-// rows of the fusion, the drafter's logits with the draft race).
+// stream-K schedules (the partial sums of a tile either left in slots for the
+// next kernel or added in by the share that holds the tile's first K block),
+// and four epilogues (fp32 sums, the K/V cache rows of the fusion, the
+// drafter's logits with the draft race, SwiGLU).
 #pragma once
 
 #include <cuda.h>
@@ -26,6 +28,11 @@ constexpr int kBK = 64;
 constexpr int kGemmThreads = 192;  // warp 0: TMA producer, warp 1: MMA issuer, warps 2-5: epilogue
 constexpr int kMaxSeg = 8;
 constexpr int kSplitTarget = 152;  // work units aimed for when splitting K (one per SM)
+constexpr int kStgRow = 36;        // fp32 staging row of an epilogue warp: 32 columns + 4 of padding
+constexpr int kStgBytes = 32 * kStgRow * 4;
+constexpr int kBarBytes = 512;     // mbarriers and the tensor-memory address
+constexpr int kFixGroupF4 = 4 * 8 * kBM;         // float4 of one partial sum over a 128-column group
+constexpr int kFixGroupBytes = kFixGroupF4 * 16;  // 64 KB
 
 struct TmapPack {
   CUtensorMap a[kMaxSeg];
@@ -36,7 +43,12 @@ struct GemmArgs {
   int stream_k;            // > 0: the number of shares (CTAs); CTA c takes the c-th near-equal share of the
                            // (tile, K block) space
   int dp_tiles;            // stream_k: leading tiles scheduled whole, a multiple of the share count
-  int* pieces;             // stream_k: [m_tiles * n_tiles] number of slots written for the tile
+  int* pieces;             // stream_k without fixup: [m_tiles * n_tiles] number of slots written for the tile
+  int fixup;               // stream_k: a share that holds a tile's first K block adds the other shares'
+                           // partial sums before the epilogue (which then sees the whole sum)
+  float4* fix_part;        // fixup: [shares][MT * BN * 32] float4, the partial sum of a share's first piece
+                           // in the accumulator's own order (column chunk, 4-column group, row)
+  int* fix_flag;           // fixup: [shares], zero at launch; 4 once the share's partial sum is stored
   int epi;                 // 0: fp32 partial store, 1: K/V cache epilogue, 2: drafter logits + draft race,
                            // 3: SwiGLU (columns 64t.. of a 128-column unit gate, the next 64 up)
   int a4d_bs;              // > 0: A is an attention output [B][Hq][a4d_bs][128] read through a 4D map
@@ -76,7 +88,66 @@ __host__ __device__ constexpr int num_acc() {
 
 template <int BN, int STAGES, int MT>
 constexpr size_t gemm_smem_bytes() {
-  return 1024 + static_cast<size_t>(STAGES) * stage_bytes<BN, MT>() + 8 * (2 * STAGES + 4) + 16;
+  static_assert(8 * (2 * STAGES + 5) + 16 <= kBarBytes, "mbarrier block");
+  return 1024 + static_cast<size_t>(STAGES) * stage_bytes<BN, MT>() + kBarBytes + 4 * kStgBytes;
+}
+
+template <int BN, int MT>
+__host__ __device__ constexpr int fix_part_float4() {
+  return MT * BN * kBM / 4;
+}
+
+// Where the epilogue reads this thread's row of a unit: tensor memory, plus
+// (fixup) the partial sums of nfix later shares of the same tile.  A partial
+// sum is stored as float4 [column chunk of 32][group of 4 columns][row of the
+// 128-row block], so the 32 rows of a warp read and write 512 contiguous bytes.
+struct AccSrc {
+  uint32_t taddr;        // tensor memory of the 128-column group (lane quarter and accumulator applied)
+  const float4* fix;     // the first later share's partial sum (this thread's row applied), in global
+                         // memory or staged in shared memory
+  int nfix;
+  int fix_stride;        // float4 between two shares' partial sums
+  int col_base;          // column of the group in the layout fix points into
+  bool smem;             // fix points into shared memory
+};
+
+// Adds the later shares' partial sums of columns col .. col + 31 (col a
+// multiple of 32) of this thread's row to r.
+__device__ __forceinline__ void acc_add32(const AccSrc& s, int col, uint32_t (&r)[32]) {
+  const float4* src = s.fix + static_cast<size_t>((s.col_base + col) >> 5) * 8 * kBM;
+  for (int k = 0; k < s.nfix; ++k, src += s.fix_stride) {
+    float4 v[8];
+    if (s.smem) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = src[j * kBM];
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = __ldcg(src + j * kBM);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      r[4 * j] = __float_as_uint(__uint_as_float(r[4 * j]) + v[j].x);
+      r[4 * j + 1] = __float_as_uint(__uint_as_float(r[4 * j + 1]) + v[j].y);
+      r[4 * j + 2] = __float_as_uint(__uint_as_float(r[4 * j + 2]) + v[j].z);
+      r[4 * j + 3] = __float_as_uint(__uint_as_float(r[4 * j + 3]) + v[j].w);
+    }
+  }
+}
+
+// 32 accumulator columns from col (a multiple of 32) of this thread's row.
+__device__ __forceinline__ void acc_ld32(const AccSrc& s, int col, uint32_t (&r)[32]) {
+  tmem_ld_32cols(s.taddr + col, r);
+  tmem_ld_wait();
+  acc_add32(s, col, r);
+}
+
+// Two 32-column blocks, both tensor-memory loads in flight before one wait.
+__device__ __forceinline__ void acc_ld32x2(const AccSrc& s, int ca, uint32_t (&ra)[32], int cb, uint32_t (&rb)[32]) {
+  tmem_ld_32cols(s.taddr + ca, ra);
+  tmem_ld_32cols(s.taddr + cb, rb);
+  tmem_ld_wait();
+  acc_add32(s, ca, ra);
+  acc_add32(s, cb, rb);
 }
 
 __device__ __forceinline__ void unit_coords(int u, const GemmArgs& p, int& m, int& n, int& kb0, int& kb1,
@@ -232,43 +303,71 @@ __device__ __forceinline__ void head_epilogue(uint32_t taddr, int col0, int row,
   if (live) p.race[static_cast<size_t>(row) * p.n_tiles + n_tile] = make_float2(best, __int_as_float(best_col));
 }
 
-// SwiGLU of this thread's row: in every 128 columns of the unit, the first 64
-// are gate values and the next 64 the up values of the same 64 outputs
-// (the weight rows are interleaved that way); out = silu(gate) * up, bf16.
-template <int BN>
-__device__ __forceinline__ void swiglu_epilogue(uint32_t taddr, int n_tile, int row, const GemmArgs& p) {
+// SwiGLU of this thread's row over one 128-column group from column col0 (a
+// multiple of 128): the first 64 columns are gate values and the next 64 the
+// up values of the same 64 outputs (the weight rows are interleaved that way);
+// out = silu(gate) * up, bf16, to act[row][col0 / 2 ..].
+__device__ __forceinline__ void swiglu_group(const AccSrc& src, int col0, int row, const GemmArgs& p) {
   // every lane takes part in the tensor-memory loads (warp-collective); only
   // the rows of the problem store
   const bool live = row < p.M;
   const int I = p.N / 2;
+  __nv_bfloat16* dst = p.act + static_cast<size_t>(live ? row : 0) * I + col0 / 2;
 #pragma unroll 1
-  for (int blk = 0; blk < BN / 128; ++blk) {
-    __nv_bfloat16* dst = p.act + static_cast<size_t>(live ? row : 0) * I + (n_tile * BN + blk * 128) / 2;
+  for (int c = 0; c < 2; ++c) {
+    uint32_t g[32], u[32];
+    acc_ld32x2(src, c * 32, g, 64 + c * 32, u);
+    uint32_t o[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      // silu(g) = g / (1 + e^-g) with the approximate divide (relative error
+      // a few units in the last place, far below the bf16 rounding); it gives
+      // 0 once e^-g exceeds 2^126, the limit of silu there
+      const float g0 = __uint_as_float(g[2 * j]), g1 = __uint_as_float(g[2 * j + 1]);
+      const float a0 = __fdividef(g0, 1.0f + __expf(-g0)) * __uint_as_float(u[2 * j]);
+      const float a1 = __fdividef(g1, 1.0f + __expf(-g1)) * __uint_as_float(u[2 * j + 1]);
+      o[j] = pack_bf16x2(a0, a1);
+    }
+    if (live) {
+      uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) d4[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+    }
+  }
+}
+
+// fp32 sums of one 128-column group from column col0 into out_f32 slot ks,
+// staged through this warp's shared-memory rows so that each store instruction
+// writes four whole 128-byte row segments; row0 is the warp's first row.
+__device__ __forceinline__ void f32_group(const AccSrc& src, float* stg, int ks, int row0, int col0, int lane,
+                                          const GemmArgs& p) {
+  float* dst = p.out_f32 + static_cast<size_t>(ks) * p.M * p.N + col0 + (lane & 7) * 4;
 #pragma unroll 1
-    for (int c = 0; c < 2; ++c) {
-      uint32_t g[32], u[32];
-      tmem_ld_32cols(taddr + blk * 128 + c * 32, g);
-      tmem_ld_32cols(taddr + blk * 128 + 64 + c * 32, u);
-      tmem_ld_wait();
-      uint32_t o[16];
+  for (int c2 = 0; c2 < 4; c2 += 2) {
+    uint32_t r[2][32];
+    acc_ld32x2(src, c2 * 32, r[0], c2 * 32 + 32, r[1]);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const float g0 = __uint_as_float(g[2 * j]), g1 = __uint_as_float(g[2 * j + 1]);
-        const float a0 = g0 / (1.0f + __expf(-g0)) * __uint_as_float(u[2 * j]);
-        const float a1 = g1 / (1.0f + __expf(-g1)) * __uint_as_float(u[2 * j + 1]);
-        o[j] = pack_bf16x2(a0, a1);
-      }
-      if (live) {
-        uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+    for (int h = 0; h < 2; ++h) {
+      __syncwarp();
 #pragma unroll
-        for (int j = 0; j < 4; ++j) d4[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+      for (int j = 0; j < 8; ++j)
+        *reinterpret_cast<float4*>(stg + lane * kStgRow + 4 * j) =
+            make_float4(__uint_as_float(r[h][4 * j]), __uint_as_float(r[h][4 * j + 1]),
+                        __uint_as_float(r[h][4 * j + 2]), __uint_as_float(r[h][4 * j + 3]));
+      __syncwarp();
+#pragma unroll
+      for (int it = 0; it < 8; ++it) {
+        const int rl = it * 4 + (lane >> 3);
+        const float4 v = *reinterpret_cast<const float4*>(stg + rl * kStgRow + (lane & 7) * 4);
+        if (row0 + rl < p.M)
+          *reinterpret_cast<float4*>(dst + static_cast<size_t>(row0 + rl) * p.N + (c2 + h) * 32) = v;
       }
     }
   }
 }
 
 // Epilogue of one 128-column head of the K/V projection for this thread's row.
-__device__ __forceinline__ void kv_head_epilogue(uint32_t taddr, int col0, int row, const GemmArgs& p) {
+__device__ __forceinline__ void kv_head_epilogue(const AccSrc& src, int hcol, int col0, int row, const GemmArgs& p) {
   const int hidx = col0 / HD;
   const int l = hidx / (2 * p.Hkv);
   const int s = (hidx / p.Hkv) % 2;
@@ -281,10 +380,9 @@ __device__ __forceinline__ void kv_head_epilogue(uint32_t taddr, int col0, int r
                         (valid ? ri.y : 0)) * HD;
   uint32_t r[32];
   if (s == 1) {
-#pragma unroll
+#pragma unroll 1
     for (int c = 0; c < 4; ++c) {
-      tmem_ld_32cols(taddr + c * 32, r);
-      tmem_ld_wait();
+      acc_ld32(src, hcol + c * 32, r);
       if (valid) {
         uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
@@ -297,29 +395,35 @@ __device__ __forceinline__ void kv_head_epilogue(uint32_t taddr, int col0, int r
     }
     return;
   }
-  float ss = 0.f;
+  const float2* cs = p.rope_cs + (valid ? row : 0);
+  const size_t cs_stride = static_cast<size_t>(p.M);
+  // the rotation angles of the first half are requested before the
+  // accumulator is read, so their global-memory latency overlaps it
+  float2 csh[32];
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    tmem_ld_32cols(taddr + c * 32, r);
-    tmem_ld_wait();
+  for (int j = 0; j < 32; ++j) csh[j] = valid ? __ldg(cs + j * cs_stride) : make_float2(1.f, 0.f);
+  float ss = 0.f;
+  uint32_t r2[32];
+#pragma unroll 1
+  for (int c = 0; c < 4; c += 2) {
+    acc_ld32x2(src, hcol + c * 32, r, hcol + c * 32 + 32, r2);
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-      const float v = __uint_as_float(r[i]);
-      ss += v * v;
+      const float v = __uint_as_float(r[i]), v2 = __uint_as_float(r2[i]);
+      ss += v * v + v2 * v2;
     }
   }
   const float rinv = rsqrtf(ss * (1.0f / HD) + p.eps);
   const __nv_bfloat16* kg = p.k_gain ? p.k_gain + l * HD : nullptr;
   const bool kg_vec = kg && (reinterpret_cast<uintptr_t>(kg) & 15u) == 0;
-  const float2* cs = p.rope_cs + (valid ? row : 0);
-  const size_t cs_stride = static_cast<size_t>(p.M);
-#pragma unroll
+#pragma unroll 1
   for (int half = 0; half < 2; ++half) {
     const int e0 = half * 32;
-    uint32_t r2[32];
-    tmem_ld_32cols(taddr + e0, r);
-    tmem_ld_32cols(taddr + 64 + e0, r2);
-    tmem_ld_wait();
+    if (half == 1) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) csh[j] = valid ? __ldg(cs + (32 + j) * cs_stride) : make_float2(1.f, 0.f);
+    }
+    acc_ld32x2(src, hcol + e0, r, hcol + 64 + e0, r2);
     uint32_t o1[16], o2[16];
 #pragma unroll
     for (int j8 = 0; j8 < 32; j8 += 8) {
@@ -334,7 +438,7 @@ __device__ __forceinline__ void kv_head_epilogue(uint32_t taddr, int col0, int r
           const int j = j8 + i + k;
           const float y1 = __uint_as_float(r[j]) * rinv * g1[i + k];
           const float y2 = __uint_as_float(r2[j]) * rinv * g2[i + k];
-          const float2 c = valid ? cs[(e0 + j) * cs_stride] : make_float2(1.f, 0.f);
+          const float2 c = csh[j];
           a[k] = y1 * c.x - y2 * c.y;
           b[k] = y2 * c.x + y1 * c.y;
         }
@@ -368,11 +472,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + STAGES * STAGE);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  float* stg_all = reinterpret_cast<float*>(gbase + STAGES * STAGE + kBarBytes);
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = full0 + 8 * STAGES;
   const uint32_t tfull0 = empty0 + 8 * STAGES;
   const uint32_t tempty0 = tfull0 + 16;
+  const uint32_t fixbar = tempty0 + 16;  // staged partial sums of a fixup
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
@@ -384,6 +490,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
       mbar_init(tfull0 + 8 * a, 1);
       mbar_init(tempty0 + 8 * a, 4);
     }
+    mbar_init(fixbar, 1);
     mbar_fence_init();
   }
   if (warp == 1) {
@@ -490,36 +597,95 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
     uint32_t acc_phase = 0;
     Pieces pcs(p);
     int m, n, kb0, kb1, ks;
+    float* stg = stg_all + q * (32 * kStgRow);
+    constexpr int FIX = fix_part_float4<BN, MT>();
+    const int rowl = q * 32 + lane;  // row within a 128-row block
+    uint32_t fphase = 0;             // parity of the staged-partials barrier
     while (pcs.next(p, m, n, kb0, kb1, ks)) {
       if (!mbar_wait(tfull0 + 8 * acc, acc_phase, p.status)) break;
-      if (p.stream_k && ks == 0 && warp == 2 && lane == 0) p.pieces[m * p.n_tiles + n] = pcs.count;
+      if (p.stream_k && !p.fixup && ks == 0 && warp == 2 && lane == 0) p.pieces[m * p.n_tiles + n] = pcs.count;
       tc_fence_after_sync();
+      const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * ACC_COLS;
+      if (p.fixup && ks > 0) {
+        // a later share of the tile: store the partial sum, then raise this share's flag
+        float4* dst = p.fix_part + static_cast<size_t>(blockIdx.x) * FIX + rowl;
 #pragma unroll 1
-      for (int i = 0; i < MT; ++i) {
-        const int row = (m * MT + i) * kBM + q * 32 + lane;
-        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * ACC_COLS + i * BN;
-        if (p.epi == 0) {
-          float* dst = p.out_f32 + (static_cast<size_t>(ks) * p.M + row) * p.N + n * BN;
-#pragma unroll 1
-          for (int c = 0; c < BN / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld_32cols(taddr + c * 32, r);
-            tmem_ld_wait();
-            if (row < p.M) {
-              float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+        for (int cc = 0; cc < MT * BN / 32; ++cc) {
+          uint32_t r[32];
+          tmem_ld_32cols(tacc + cc * 32, r);
+          tmem_ld_wait();
 #pragma unroll
-              for (int j = 0; j < 8; ++j)
-                d4[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                    __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-            }
-          }
-        } else if (p.epi == 1) {
+          for (int j = 0; j < 8; ++j)
+            __stcg(dst + (cc * 8 + j) * kBM, make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                                         __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3])));
+        }
+        __syncwarp();
+        if (lane == 0) {
+          __threadfence();
+          atomicAdd(p.fix_flag + blockIdx.x, 1);
+        }
+      } else {
+        // the tile's first share adds the later shares' partial sums (shares
+        // blockIdx.x + 1 ..).  This is the share's last piece, so once its
+        // accumulator is complete the operand ring is idle: up to three
+        // partial sums are staged there, one 128-column group at a time, by
+        // bulk copies; more are read from global memory as they are used.
+        const int nfix = (p.fixup && pcs.count > 1) ? pcs.count - 1 : 0;
+        const bool staged = nfix > 0 && nfix * kFixGroupBytes <= STAGES * STAGE;
+        if (nfix > 0 && !staged) {
+          if (lane == 0)
+            for (int k = 1; k <= nfix; ++k)
+              if (!wait_counter_at_least(p.fix_flag + blockIdx.x + k, 4, p.status)) break;
+          __syncwarp();
+        }
+        bool first_group = true;
 #pragma unroll 1
-          for (int hh = 0; hh < BN / HD; ++hh) kv_head_epilogue(taddr + hh * HD, n * BN + hh * HD, row, p);
-        } else if (p.epi == 2) {
-          head_epilogue<BN>(taddr, n * BN, row, n, p);
-        } else {
-          swiglu_epilogue<BN>(taddr, n, row, p);
+        for (int i = 0; i < MT; ++i) {
+          const int row = (m * MT + i) * kBM + rowl;
+          if (p.epi == 2) {
+            head_epilogue<BN>(tacc + i * BN, n * BN, row, n, p);
+            continue;
+          }
+#pragma unroll 1
+          for (int grp = 0; grp < BN / 128; ++grp) {
+            AccSrc src;
+            src.taddr = tacc + i * BN + grp * 128;
+            src.nfix = nfix;
+            if (staged) {
+              named_barrier_sync(1, 128);  // the previous group's staged sums have been read
+              if (warp == 2 && lane == 0) {
+                if (first_group)
+                  for (int k = 1; k <= nfix; ++k)
+                    if (!wait_counter_at_least(p.fix_flag + blockIdx.x + k, 4, p.status)) break;
+                fence_proxy_async_all();
+                mbar_arrive_expect_tx(fixbar, nfix * kFixGroupBytes);
+                for (int k = 0; k < nfix; ++k)
+                  bulk_load(base + k * kFixGroupBytes,
+                            p.fix_part + static_cast<size_t>(blockIdx.x + 1 + k) * FIX +
+                                static_cast<size_t>(i * (BN / 128) + grp) * kFixGroupF4,
+                            kFixGroupBytes, fixbar);
+              }
+              mbar_wait(fixbar, fphase, p.status);
+              fphase ^= 1u;
+              src.fix = reinterpret_cast<const float4*>(gbase) + rowl;
+              src.fix_stride = kFixGroupF4;
+              src.col_base = 0;
+              src.smem = true;
+            } else {
+              src.fix = p.fix_part + static_cast<size_t>(blockIdx.x + 1) * FIX + rowl;
+              src.fix_stride = FIX;
+              src.col_base = i * BN + grp * 128;
+              src.smem = false;
+            }
+            first_group = false;
+            const int col0 = n * BN + grp * 128;
+            if (p.epi == 0)
+              f32_group(src, stg, ks, row - lane, col0, lane, p);
+            else if (p.epi == 1)
+              kv_head_epilogue(src, 0, col0, row, p);
+            else
+              swiglu_group(src, col0, row, p);
+          }
         }
       }
       tc_fence_before_sync();
@@ -537,6 +703,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
     tc_fence_after_sync();
     tmem_dealloc(tmem_base, NACC * ACC_COLS);
   }
+}
+
+// Stream-K with fixup over all of a GEMM's tiles: as many shares as SMs
+// (every share non-empty); each share's partial-sum area and its flag.
+inline int fixup_shares(int tiles, int num_kb) {
+  return static_cast<int>(std::min<long>(kSplitTarget, static_cast<long>(tiles) * num_kb));
+}
+
+template <int BN, int MT>
+size_t fixup_ws_bytes(int shares) {
+  return align256(static_cast<size_t>(shares) * fix_part_float4<BN, MT>() * sizeof(float4)) +
+         align256(static_cast<size_t>(shares) * sizeof(int));
+}
+
+template <int BN, int MT>
+void fixup_take(WsCarver& w, int shares, GemmArgs& a) {
+  a.fix_part = w.take<float4>(static_cast<size_t>(shares) * fix_part_float4<BN, MT>());
+  a.fix_flag = w.take<int>(static_cast<size_t>(shares));
+  a.fixup = 1;
+  a.stream_k = shares;
+  a.dp_tiles = 0;
+  a.k_splits = 1;
 }
 
 template <int BN, int STAGES, int MT>

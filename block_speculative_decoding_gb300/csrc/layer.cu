@@ -15,7 +15,9 @@
 //                h = bf16(RMSNorm(x1) * g_post)
 //   3. gemm_tc   act = bf16(silu(h W_gate^T) * (h W_up^T)): the weight rows are
 //                interleaved in 64-row blocks, so each 128-column unit holds
-//                the gate and up values of the same 64 outputs (epilogue 3)
+//                the gate and up values of the same 64 outputs (epilogue 3);
+//                stream-K over all SMs, the tile's first share adding the
+//                others' partial sums before the SwiGLU
 //   4. gemm_tc   Y = act W_down^T, split K -> slots
 //   5. resnorm   x2 = bf16(x1 + sum of the slots) -> x
 #include <cuda.h>
@@ -32,17 +34,24 @@ namespace dflash {
 namespace {
 
 constexpr int kResThreads = 256;
-constexpr int kResSlots = 4;  // float4 slots per thread: rows up to 4096 wide
+constexpr int kResSlots = 4;      // float4 slots per thread: rows up to 4096 wide
+constexpr int kMaxKSplits = 16;   // partial sums per output (split-K slots)
 
 // One CTA per row m: x1 = bf16(x + sum_s part[s]) (written to x); with g_mode,
-// h = bf16(x1 * rsqrt(mean(x1^2) + eps) * g), g == nullptr meaning ones.
+// h = bf16(x1 * rsqrt(mean(x1^2) + eps) * g), g == nullptr meaning ones.  The
+// slots of one float4 are loaded together before any add, so each thread keeps
+// all of its loads in flight.
 __global__ void __launch_bounds__(kResThreads) resnorm_kernel(const float* __restrict__ part, int k_splits, int M,
                                                              int D, __nv_bfloat16* __restrict__ x, int g_mode,
                                                              const __nv_bfloat16* __restrict__ g, float eps,
-                                                             __nv_bfloat16* __restrict__ h) {
+                                                             __nv_bfloat16* __restrict__ h, int* __restrict__ zero_flags,
+                                                             int n_zero) {
   pdl_wait_primary();
   pdl_launch_dependents();
   const int m = blockIdx.x;
+  // the fixup flags of the GEMM that follows (every earlier grid has completed)
+  if (m == 0)
+    for (int i = threadIdx.x; i < n_zero; i += kResThreads) zero_flags[i] = 0;
   const int nv = D / 4;
   const float4* pr = reinterpret_cast<const float4*>(part + static_cast<size_t>(m) * D);
   const size_t stride = static_cast<size_t>(M) * D / 4;
@@ -54,15 +63,21 @@ __global__ void __launch_bounds__(kResThreads) resnorm_kernel(const float* __res
     const int v = threadIdx.x + i * kResThreads;
     y[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (v < nv) {
-      float4 t = pr[v];
-      for (int s = 1; s < k_splits; ++s) {
-        const float4 u = pr[s * stride + v];
-        t.x += u.x;
-        t.y += u.y;
-        t.z += u.z;
-        t.w += u.w;
-      }
+      float4 u[kMaxKSplits];
+#pragma unroll
+      for (int s = 0; s < kMaxKSplits; ++s)
+        if (s < k_splits) u[s] = __ldcg(pr + s * stride + v);
       const uint2 xv = xr[v];
+      float4 t = u[0];
+#pragma unroll
+      for (int s = 1; s < kMaxKSplits; ++s) {
+        if (s < k_splits) {
+          t.x += u[s].x;
+          t.y += u[s].y;
+          t.z += u[s].z;
+          t.w += u[s].w;
+        }
+      }
       const uint32_t lo = pack_bf16x2(bf16_lo(xv.x) + t.x, bf16_hi(xv.x) + t.y);
       const uint32_t hi = pack_bf16x2(bf16_lo(xv.y) + t.z, bf16_hi(xv.y) + t.w);
       xr[v] = make_uint2(lo, hi);
@@ -98,7 +113,7 @@ __global__ void __launch_bounds__(kResThreads) resnorm_kernel(const float* __res
 }
 
 struct TailPlan {
-  int mt, m_tiles, ks_o, ks_down;
+  int mt, m_tiles, ks_o, ks_down, gu_shares;  // gate/up: stream-K with fixup over gu_shares CTAs
 };
 
 TailPlan tail_plan(int M, int D, int Kq, int I) {
@@ -106,14 +121,16 @@ TailPlan tail_plan(int M, int D, int Kq, int I) {
   t.mt = M <= 2 * kBM ? 2 : 1;
   t.m_tiles = (M + t.mt * kBM - 1) / (t.mt * kBM);
   const int tiles = t.m_tiles * (D / 128);
-  const int ks = std::max(1, std::min(16, kSplitTarget / std::max(1, tiles)));
+  const int ks = std::max(1, std::min(kMaxKSplits, kSplitTarget / std::max(1, tiles)));
   t.ks_o = std::min(ks, Kq / kBK);
   t.ks_down = std::min(ks, I / kBK);
+  t.gu_shares = fixup_shares(t.m_tiles * (2 * I / 128), D / kBK);
   return t;
 }
 
 dflash_status launch_resnorm(const float* part, int k_splits, int M, int D, __nv_bfloat16* x, int g_mode,
-                             const __nv_bfloat16* g, float eps, __nv_bfloat16* h, cudaStream_t st) {
+                             const __nv_bfloat16* g, float eps, __nv_bfloat16* h, int* zero_flags, int n_zero,
+                             cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(M));
   cfg.blockDim = dim3(kResThreads);
@@ -123,7 +140,8 @@ dflash_status launch_resnorm(const float* part, int k_splits, int M, int D, __nv
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, resnorm_kernel, part, k_splits, M, D, x, g_mode, g, eps, h);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, resnorm_kernel, part, k_splits, M, D, x, g_mode, g, eps, h, zero_flags,
+                                     n_zero);
   return e == cudaSuccess ? DFLASH_OK : cuda_fail(e, "resnorm_kernel launch");
 }
 
@@ -137,7 +155,8 @@ dflash_status run_gemm(const TmapPack& am, const CUtensorMap& bm, const GemmArgs
 
 size_t tail_ws_bytes(int M, int D, int Hq, int I) {
   const TailPlan t = tail_plan(M, D, Hq * 128, I);
-  return align256(static_cast<size_t>(std::max(t.ks_o, t.ks_down)) * M * D * sizeof(float)) +
+  return (t.mt == 2 ? fixup_ws_bytes<128, 2>(t.gu_shares) : fixup_ws_bytes<128, 1>(t.gu_shares)) +
+         align256(static_cast<size_t>(std::max(t.ks_o, t.ks_down)) * M * D * sizeof(float)) +
          align256(static_cast<size_t>(M) * D * sizeof(__nv_bfloat16)) +
          align256(static_cast<size_t>(M) * I * sizeof(__nv_bfloat16)) + 256;
 }
@@ -152,6 +171,8 @@ dflash_status launch_layer_tail(void* x, const void* attn_out, int B, int bs, in
   auto* h = w.take<__nv_bfloat16>(static_cast<size_t>(M) * D);
   auto* act = w.take<__nv_bfloat16>(static_cast<size_t>(M) * I);
   auto* xb = static_cast<__nv_bfloat16*>(x);
+  GemmArgs gu{};
+  if (t.mt == 2) fixup_take<128, 2>(w, t.gu_shares, gu); else fixup_take<128, 1>(w, t.gu_shares, gu);
 
   // 1. output projection, A through a 4D map of the attention output
   TmapPack am{};
@@ -172,13 +193,15 @@ dflash_status launch_layer_tail(void* x, const void* attn_out, int B, int bs, in
   a.n_tiles = D / 128;
   a.epi = 0;
   a.a4d_bs = bs;
-  a.pdl = 1;  // nothing is loaded before the preceding grid (the attention) has completed
+  a.pdl = 1;  // the attention output is loaded only once the preceding grid has completed;
+  a.prefetch_b = 1;  // the weights, which no kernel of the chain writes, before that
   a.out_f32 = part;
   a.status = dev.status;
   s = t.mt == 2 ? run_gemm<2>(am, bm, a, st, dev) : run_gemm<1>(am, bm, a, st, dev);
   if (s) return s;
   // 2. residual + post-attention norm
-  s = launch_resnorm(part, t.ks_o, M, D, xb, 1, static_cast<const __nv_bfloat16*>(g_post), eps, h, st);
+  s = launch_resnorm(part, t.ks_o, M, D, xb, 1, static_cast<const __nv_bfloat16*>(g_post), eps, h, gu.fix_flag,
+                     t.gu_shares, st);
   if (s) return s;
   // 3. gate/up with SwiGLU
   TmapPack hm{};
@@ -187,12 +210,10 @@ dflash_status launch_layer_tail(void* x, const void* attn_out, int B, int bs, in
   CUtensorMap gm;
   s = make_tmap_bf16_2d(&gm, w_gate_up, static_cast<uint64_t>(2) * I, D, 128, kBK);
   if (s) return s;
-  GemmArgs gu{};
   gu.M = M;
   gu.N = 2 * I;
   gu.num_kb = D / kBK;
   gu.kb_per_seg = gu.num_kb;
-  gu.k_splits = 1;
   gu.m_tiles = t.m_tiles;
   gu.n_tiles = 2 * I / 128;
   gu.epi = 3;
@@ -225,7 +246,7 @@ dflash_status launch_layer_tail(void* x, const void* attn_out, int B, int bs, in
   s = t.mt == 2 ? run_gemm<2>(xm, dm, dn, st, dev) : run_gemm<1>(xm, dm, dn, st, dev);
   if (s) return s;
   // 5. residual
-  return launch_resnorm(part, t.ks_down, M, D, xb, 0, nullptr, eps, nullptr, st);
+  return launch_resnorm(part, t.ks_down, M, D, xb, 0, nullptr, eps, nullptr, nullptr, 0, st);
 }
 
 }  // namespace dflash

@@ -43,6 +43,7 @@ class CycleConfig:
     Hkv: int = 8
     d: int = 128
     D: int = 2560
+    mlp_dim: int = 5120         # drafter layer MLP width
     J: int = 5
     d_target: int = 2560
     V: int = 262144
