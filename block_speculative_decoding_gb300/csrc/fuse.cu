@@ -27,6 +27,7 @@
 // fp32 path: the same steps as plain SIMT kernels (parity path).
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -53,16 +54,18 @@ struct InvFreq {
 //     gain g, stored as TH (workspace copy for the K/V GEMM) and optionally as
 //     the caller's copy.  Each thread keeps its float4 slots of the row in
 //     registers (rows up to 4096 wide), so the partials are read once.
-constexpr int kNormThreads = 256;
-constexpr int kNormSlots = 4;  // float4 slots per thread
+constexpr int kNormThreads = 256;     // fp32 path
+constexpr int kNormMaxThreads = 512;
+constexpr int kNormSlots = 2;        // float4 slots per thread (in registers up to 2 x the block)
+constexpr int kNormBatch = 8;        // split-K slots requested together
 
 template <typename TG, typename TH>
-__global__ void __launch_bounds__(kNormThreads) fuse_rownorm_kernel(
+__global__ void __launch_bounds__(kNormMaxThreads) fuse_rownorm_kernel(
     const float* __restrict__ part, int k_splits, const int* __restrict__ pieces, int tile_rows, int tile_cols,
     int n_tiles, int M, int D, const TG* __restrict__ g, float eps,
     TH* __restrict__ ht, TH* __restrict__ ht_out, const int32_t* __restrict__ cu_new,
     const int32_t* __restrict__ seq_len, int B, int cap, int ring, InvFreq inv, int2* __restrict__ rowinfo,
-    float2* __restrict__ rope_cs, int* __restrict__ zero_flags, int n_zero, unsigned* status) {
+    void* __restrict__ rope_cs, int* __restrict__ zero_flags, int n_zero, unsigned* status) {
   const int m = blockIdx.x;
   if (threadIdx.x <= HD / 2) {
     int lo = 0, hi = B - 1;
@@ -84,7 +87,14 @@ __global__ void __launch_bounds__(kNormThreads) fuse_rownorm_kernel(
       ang -= kTwoPi * rint(ang * kInvTwoPi);
       float sv, cv;
       sincosf(static_cast<float>(ang), &sv, &cv);
-      rope_cs[static_cast<size_t>(threadIdx.x) * M + m] = make_float2(cv, sv);
+      // fp32 rows keep fp32 angles; for bf16 rows the (cos, sin) pairs are held
+      // as fp16 (relative error 2^-11, a quarter of the bf16 rounding of the
+      // stored key), so that a K head's 64 pairs fit one register load each
+      const size_t ci = static_cast<size_t>(threadIdx.x) * M + m;
+      if (sizeof(TH) == 4)
+        static_cast<float2*>(rope_cs)[ci] = make_float2(cv, sv);
+      else
+        static_cast<__half2*>(rope_cs)[ci] = __floats2half2_rn(cv, sv);
     } else {
       rowinfo[m] = valid ? make_int2(b, ring ? pos % cap : pos) : make_int2(-1, -1);  // (sequence, cache row)
       if (!valid) raise_status(status, seq_ok ? DFLASH_DEV_CAPACITY : DFLASH_DEV_BAD_SEQLEN);
@@ -94,7 +104,7 @@ __global__ void __launch_bounds__(kNormThreads) fuse_rownorm_kernel(
   pdl_wait_primary();  // the partials of the fusion GEMM
   // the fixup flags of the K/V GEMM that follows (every earlier grid has completed)
   if (m == 0)
-    for (int i = threadIdx.x; i < n_zero; i += kNormThreads) zero_flags[i] = 0;
+    for (int i = threadIdx.x; i < n_zero; i += static_cast<int>(blockDim.x)) zero_flags[i] = 0;
   const int nv = D / 4;  // float4 slots of the row
   const float4* prow = reinterpret_cast<const float4*>(part + static_cast<size_t>(m) * D);
   const size_t split_stride = static_cast<size_t>(M) * D / 4;
@@ -112,7 +122,8 @@ __global__ void __launch_bounds__(kNormThreads) fuse_rownorm_kernel(
     }
     return t4;
   };
-  const bool in_regs = nv <= kNormThreads * kNormSlots;
+  const int nthr = blockDim.x;
+  const bool in_regs = nv <= nthr * kNormSlots;
   float4 y[kNormSlots];
   float ss = 0.f;
   if (in_regs) {
@@ -121,21 +132,21 @@ __global__ void __launch_bounds__(kNormThreads) fuse_rownorm_kernel(
     int ns_max = 0;
 #pragma unroll
     for (int i = 0; i < kNormSlots; ++i) {
-      const int v = threadIdx.x + i * kNormThreads;
+      const int v = threadIdx.x + i * nthr;
       y[i] = make_float4(0.f, 0.f, 0.f, 0.f);
       ns[i] = v < nv ? (prow_pieces ? prow_pieces[(4 * v) / tile_cols] : k_splits) : 0;
       ns_max = max(ns_max, ns[i]);
       if (v < nv) y[i] = prow[v];
     }
-    for (int s0 = 1; s0 < ns_max; s0 += 2) {
-      float4 t[2][kNormSlots];
+    for (int s0 = 1; s0 < ns_max; s0 += kNormBatch) {
+      float4 t[kNormBatch][kNormSlots];
 #pragma unroll
-      for (int u = 0; u < 2; ++u)
+      for (int u = 0; u < kNormBatch; ++u)
 #pragma unroll
         for (int i = 0; i < kNormSlots; ++i)
-          if (s0 + u < ns[i]) t[u][i] = prow[(s0 + u) * split_stride + threadIdx.x + i * kNormThreads];
+          if (s0 + u < ns[i]) t[u][i] = __ldcg(prow + (s0 + u) * split_stride + threadIdx.x + i * nthr);
 #pragma unroll
-      for (int u = 0; u < 2; ++u)
+      for (int u = 0; u < kNormBatch; ++u)
 #pragma unroll
         for (int i = 0; i < kNormSlots; ++i)
           if (s0 + u < ns[i]) {
@@ -150,18 +161,17 @@ __global__ void __launch_bounds__(kNormThreads) fuse_rownorm_kernel(
       ss += y[i].x * y[i].x + y[i].y * y[i].y + y[i].z * y[i].z + y[i].w * y[i].w;
   }
   if (!in_regs) {
-    for (int v = threadIdx.x; v < nv; v += kNormThreads) {
+    for (int v = threadIdx.x; v < nv; v += nthr) {
       const float4 t4 = row_sum(v);
       ss += t4.x * t4.x + t4.y * t4.y + t4.z * t4.z + t4.w * t4.w;
     }
   }
   ss = warp_sum(ss);
-  __shared__ float red[kNormThreads / 32];
+  __shared__ float red[kNormMaxThreads / 32];
   if (threadIdx.x % 32 == 0) red[threadIdx.x / 32] = ss;
   __syncthreads();
   float tot = 0.f;
-#pragma unroll
-  for (int w = 0; w < kNormThreads / 32; ++w) tot += red[w];
+  for (int w = 0; w < nthr / 32; ++w) tot += red[w];
   const float r = rsqrtf(tot / static_cast<float>(D) + eps);
   auto store = [&](int v, float4 t4) {
     const int e = 4 * v;
@@ -185,11 +195,11 @@ __global__ void __launch_bounds__(kNormThreads) fuse_rownorm_kernel(
   if (in_regs) {
 #pragma unroll
     for (int i = 0; i < kNormSlots; ++i) {
-      const int v = threadIdx.x + i * kNormThreads;
+      const int v = threadIdx.x + i * nthr;
       if (v < nv) store(v, y[i]);
     }
   } else {
-    for (int v = threadIdx.x; v < nv; v += kNormThreads) store(v, row_sum(v));
+    for (int v = threadIdx.x; v < nv; v += nthr) store(v, row_sum(v));
   }
 }
 
@@ -270,6 +280,92 @@ __global__ void __launch_bounds__(256) kv_store_f32_kernel(const float* __restri
   dst[e0 + 65] = y1 * c1.x + x1 * c1.y;
 }
 
+// bf16 cache, few rows: the K/V GEMM leaves stream-K partial sums in slots and
+// this kernel finishes them, one warp per (row, head of the K/V projection):
+// the sum of the tile's slots, then for keys the per-head RMSNorm * k_gain and
+// RoPE, and the bf16 store into the cache.  Lane i holds elements 2i, 2i + 1
+// and their RoPE partners 2i + 64, 2i + 65; a warp's slot loads and stores are
+// 256 contiguous bytes.  Every load of a warp is issued before any is used:
+// the first kMaxKvSlots slots are read whatever the tile's slot count (the
+// unused ones are masked out), so the warp waits for memory once; many warps
+// per SM overlap those waits, which the GEMM's four epilogue warps cannot.
+constexpr int kMaxKvSlots = 4;
+
+__global__ void __launch_bounds__(256) kv_epilogue_kernel(
+    const float* __restrict__ part, int slots, const int* __restrict__ pieces, int tile_rows, int n_tiles, int M,
+    int L, int Hkv, int Bc, int cap, const int2* __restrict__ rowinfo, const __half2* __restrict__ rope_cs,
+    const __nv_bfloat16* __restrict__ k_gain, float eps, __nv_bfloat16* __restrict__ cache_k,
+    __nv_bfloat16* __restrict__ cache_v) {
+  pdl_wait_primary();  // the partial sums of the K/V GEMM
+  pdl_launch_dependents();
+  const int heads = L * 2 * Hkv;
+  const long wid = (static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
+  const int lane = threadIdx.x % 32;
+  if (wid >= static_cast<long>(M) * heads) return;
+  const int m = static_cast<int>(wid / heads), hidx = static_cast<int>(wid % heads);
+  const int l = hidx / (2 * Hkv), s = (hidx / Hkv) % 2, h = hidx % Hkv;
+  const size_t N = static_cast<size_t>(heads) * HD;
+  const size_t slot = static_cast<size_t>(M) * N;
+  const float* src = part + static_cast<size_t>(m) * N + static_cast<size_t>(hidx) * HD;
+  const int e0 = 2 * lane;
+  // every load up front
+  const int2 ri = rowinfo[m];
+  const int ns = pieces[(m / tile_rows) * n_tiles + hidx];  // 128-column tiles: tile n = head
+  float2 u[kMaxKvSlots], v[kMaxKvSlots];
+#pragma unroll
+  for (int k = 0; k < kMaxKvSlots; ++k) {
+    u[k] = make_float2(0.f, 0.f);
+    v[k] = make_float2(0.f, 0.f);
+    if (k < slots) {
+      u[k] = __ldcg(reinterpret_cast<const float2*>(src + k * slot + e0));
+      v[k] = __ldcg(reinterpret_cast<const float2*>(src + k * slot + e0 + 64));
+    }
+  }
+  __half2 cs0 = __floats2half2_rn(1.f, 0.f), cs1 = cs0;
+  float g0 = 1.f, g1 = 1.f, g2 = 1.f, g3 = 1.f;  // element loads: the gain vector may be 2-byte aligned
+  if (s == 0) {
+    cs0 = rope_cs[static_cast<size_t>(e0) * M + m];
+    cs1 = rope_cs[static_cast<size_t>(e0 + 1) * M + m];
+    if (k_gain) {
+      const __nv_bfloat16* kg = k_gain + l * HD;
+      g0 = __bfloat162float(kg[e0]);
+      g1 = __bfloat162float(kg[e0 + 1]);
+      g2 = __bfloat162float(kg[e0 + 64]);
+      g3 = __bfloat162float(kg[e0 + 65]);
+    }
+  }
+  float2 a = make_float2(0.f, 0.f), b = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int k = 0; k < kMaxKvSlots; ++k)
+    if (k < ns) {
+      a.x += u[k].x;
+      a.y += u[k].y;
+      b.x += v[k].x;
+      b.y += v[k].y;
+    }
+  for (int k = kMaxKvSlots; k < ns; ++k) {  // more slots than kept in registers
+    const float2 x = __ldcg(reinterpret_cast<const float2*>(src + k * slot + e0));
+    const float2 y = __ldcg(reinterpret_cast<const float2*>(src + k * slot + e0 + 64));
+    a.x += x.x;
+    a.y += x.y;
+    b.x += y.x;
+    b.y += y.y;
+  }
+  if (s == 0) {
+    const float ss = warp_sum(a.x * a.x + a.y * a.y + b.x * b.x + b.y * b.y);
+    const float r = rsqrtf(ss * (1.0f / HD) + eps);
+    const float x0 = a.x * r * g0, x1 = a.y * r * g1, y0 = b.x * r * g2, y1 = b.y * r * g3;
+    const float2 c0 = __half22float2(cs0), c1 = __half22float2(cs1);
+    a = make_float2(x0 * c0.x - y0 * c0.y, x1 * c1.x - y1 * c1.y);
+    b = make_float2(y0 * c0.x + x0 * c0.y, y1 * c1.x + x1 * c1.y);
+  }
+  if (ri.x < 0) return;  // row flagged by the row map: nothing is stored
+  __nv_bfloat16* dst =
+      (s == 0 ? cache_k : cache_v) + (((static_cast<size_t>(l) * Bc + ri.x) * Hkv + h) * cap + ri.y) * HD;
+  reinterpret_cast<uint32_t*>(dst)[lane] = pack_bf16x2(a.x, a.y);
+  reinterpret_cast<uint32_t*>(dst + 64)[lane] = pack_bf16x2(b.x, b.y);
+}
+
 // ------------------------------------------------------------- planning -----
 
 // A few new rows (M <= 256, weight-bound): the fusion GEMM takes 256-row by
@@ -283,8 +379,21 @@ __global__ void __launch_bounds__(256) kv_store_f32_kernel(const float* __restri
 // meeting one tile.
 struct FusePlan {
   int fuse_mt, fuse_bn, fuse_m_tiles, fuse_n_tiles, k_splits, kv_bn, stream_k, shares, dp_tiles;
-  int kv_mt, kv_m_tiles, kv_n_tiles, kv_shares;  // K/V GEMM: stream-K with fixup over kv_shares CTAs
+  int kv_mt, kv_m_tiles, kv_n_tiles, kv_shares;  // K/V GEMM: stream-K over kv_shares CTAs
+  int kv_split;  // M <= 256: partial sums left in kv_slots slots, finished by kv_epilogue_kernel;
+  int kv_slots;  // otherwise the GEMM's own epilogue finishes them (fixup)
 };
+
+// The most stream-K shares that meet one tile when `tiles` tiles of num_kb K
+// blocks are cut into `shares` near-equal shares.
+int sk_max_count(long tiles, long num_kb, long shares) {
+  const long tot = tiles * num_kb;
+  auto share = [&](long x) { return ((x + 1) * shares - 1) / tot; };
+  int c = 1;
+  for (long t = 0; t < tiles; ++t)
+    c = std::max(c, static_cast<int>(share((t + 1) * num_kb - 1) - share(t * num_kb) + 1));
+  return c;
+}
 
 FusePlan plan(int M, int D, int num_kb, int n_kv) {
   FusePlan f;
@@ -311,6 +420,8 @@ FusePlan plan(int M, int D, int num_kb, int n_kv) {
   f.kv_m_tiles = (M + f.kv_mt * kBM - 1) / (f.kv_mt * kBM);
   f.kv_n_tiles = n_kv / f.kv_bn;
   f.kv_shares = fixup_shares(f.kv_m_tiles * f.kv_n_tiles, D / kBK);
+  f.kv_split = M <= 2 * kBM;
+  f.kv_slots = sk_max_count(static_cast<long>(f.kv_m_tiles) * f.kv_n_tiles, D / kBK, f.kv_shares);
   return f;
 }
 
@@ -323,7 +434,9 @@ size_t fuse_ws_bytes(int M, int J, int dt_width, int D, int L, int Hkv, dflash_d
              align256(static_cast<size_t>(M) * (HD / 2) * sizeof(float2));
   if (dt == DFLASH_BF16) {
     const FusePlan f = plan(M, D, J * dt_width / kBK, Ntot);
-    s += (f.kv_mt == 2 ? fixup_ws_bytes<128, 2>(f.kv_shares) : fixup_ws_bytes<256, 1>(f.kv_shares)) +
+    s += (f.kv_split ? align256(static_cast<size_t>(f.kv_slots) * M * Ntot * sizeof(float)) +
+                           align256(static_cast<size_t>(f.kv_m_tiles) * f.kv_n_tiles * sizeof(int))
+                     : fixup_ws_bytes<256, 1>(f.kv_shares)) +
          align256(static_cast<size_t>(f.k_splits) * M * D * sizeof(float)) +
          align256(static_cast<size_t>(M) * D * sizeof(__nv_bfloat16)) +
          align256(static_cast<size_t>(f.fuse_m_tiles) * f.fuse_n_tiles * sizeof(int));
@@ -364,19 +477,31 @@ dflash_status launch_fuse_context(int J, const void* const* taps, int dt_width, 
         hs, D, static_cast<const float*>(w_kv), M, Ntot, D, KV);
     const long warps = static_cast<long>(M) * L * 2 * Hkv;
     kv_store_f32_kernel<<<static_cast<unsigned>((warps * 32 + 255) / 256), 256, 0, st>>>(
-        KV, M, L, Hkv, c.batch, c.capacity, rowinfo, rope_cs, static_cast<const float*>(k_gain), eps,
+        KV, M, L, Hkv, c.batch, c.capacity, rowinfo, const_cast<const float2*>(rope_cs), static_cast<const float*>(k_gain), eps,
         static_cast<float*>(c.k), static_cast<float*>(c.v));
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? DFLASH_OK : cuda_fail(e, "fp32 fusion launch");
   }
 
   const FusePlan f = plan(M, D, J * dt_width / kBK, Ntot);
+  if (L * HD > 4 * 32 * kStgRow)  // the K/V epilogue keeps every layer's K gains in shared memory
+    return fail(DFLASH_ERR_UNSUPPORTED, "fusion: at most 36 draft layers");
   if (D % 4 != 0) return fail(DFLASH_ERR_UNSUPPORTED, "fusion: d_model must be a multiple of 4");
   float* Ypart = w.take<float>(static_cast<size_t>(f.k_splits) * M * D);
   auto* H = w.take<__nv_bfloat16>(static_cast<size_t>(M) * D);
   int* tile_pieces = w.take<int>(static_cast<size_t>(f.fuse_m_tiles) * f.fuse_n_tiles);
   GemmArgs k{};
-  if (f.kv_mt == 2) fixup_take<128, 2>(w, f.kv_shares, k); else fixup_take<256, 1>(w, f.kv_shares, k);
+  float* KVpart = nullptr;
+  if (f.kv_split) {
+    KVpart = w.take<float>(static_cast<size_t>(f.kv_slots) * M * Ntot);
+    k.pieces = w.take<int>(static_cast<size_t>(f.kv_m_tiles) * f.kv_n_tiles);
+    k.stream_k = f.kv_shares;
+    k.dp_tiles = 0;
+    k.k_splits = f.kv_slots;
+    k.out_f32 = KVpart;
+  } else {
+    fixup_take<256, 1>(w, f.kv_shares, k);
+  }
 
   // 1. fusion GEMM: A = the J taps (one tensor map each), B = W_c [D][J*dt]
   TmapPack am{};
@@ -411,7 +536,10 @@ dflash_status launch_fuse_context(int J, const void* const* taps, int dt_width, 
   {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(M));
-    cfg.blockDim = dim3(kNormThreads);
+    // one or two float4 of the row per thread; at least 65 threads (the
+    // RoPE angles and the row map)
+    cfg.blockDim = dim3(static_cast<unsigned>(
+        std::min(kNormMaxThreads, std::max(96, ((D / 4 + kNormSlots - 1) / kNormSlots + 31) / 32 * 32))));
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -424,7 +552,8 @@ dflash_status launch_fuse_context(int J, const void* const* taps, int dt_width, 
                                         f.fuse_bn, f.fuse_n_tiles, M, D,
                                         static_cast<const __nv_bfloat16*>(g_fuse), eps, H,
                                         static_cast<__nv_bfloat16*>(h_t_out), cu_new, c.seq_len, B, c.capacity,
-                                        c.ring, inv, rowinfo, rope_cs, k.fix_flag, f.kv_shares, dev.status);
+                                        c.ring, inv, rowinfo, rope_cs, k.fix_flag, f.kv_split ? 0 : f.kv_shares,
+                                        dev.status);
     if (le != cudaSuccess) return cuda_fail(le, "fuse_rownorm_kernel launch");
   }
 
@@ -441,7 +570,7 @@ dflash_status launch_fuse_context(int J, const void* const* taps, int dt_width, 
   k.kb_per_seg = k.num_kb;
   k.m_tiles = f.kv_m_tiles;
   k.n_tiles = f.kv_n_tiles;
-  k.epi = 1;
+  k.epi = f.kv_split ? 0 : 1;
   k.pdl = 1;
   k.prefetch_b = 1;
   k.cache_k = static_cast<__nv_bfloat16*>(c.k);
@@ -451,11 +580,31 @@ dflash_status launch_fuse_context(int J, const void* const* taps, int dt_width, 
   k.Hkv = Hkv;
   k.cap = c.capacity;
   k.rowinfo = rowinfo;
-  k.rope_cs = rope_cs;
+  k.rope_cs = reinterpret_cast<const __half2*>(rope_cs);
   k.k_gain = static_cast<const __nv_bfloat16*>(k_gain);
   k.eps = eps;
   k.status = dev.status;
-  return f.kv_mt == 2 ? launch_gemm<128, 4, 2>(hm, wm, k, st, dev) : launch_gemm<256, 4, 1>(hm, wm, k, st, dev);
+  if (!f.kv_split) return launch_gemm<256, 4, 1>(hm, wm, k, st, dev);
+  s = launch_gemm<128, 4, 2>(hm, wm, k, st, dev);
+  if (s) return s;
+
+  // 4. the K/V epilogue over the partial sums, a programmatic dependent
+  cudaLaunchConfig_t cfg = {};
+  const long warps = static_cast<long>(M) * L * 2 * Hkv;
+  cfg.gridDim = dim3(static_cast<unsigned>((warps * 32 + 255) / 256));
+  cfg.blockDim = dim3(256);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t le = cudaLaunchKernelEx(&cfg, kv_epilogue_kernel, static_cast<const float*>(KVpart), f.kv_slots,
+                                      static_cast<const int*>(k.pieces), f.kv_mt * kBM, f.kv_n_tiles, M, L, Hkv,
+                                      c.batch, c.capacity, static_cast<const int2*>(rowinfo),
+                                      reinterpret_cast<const __half2*>(rope_cs), static_cast<const __nv_bfloat16*>(k_gain),
+                                      eps, static_cast<__nv_bfloat16*>(c.k), static_cast<__nv_bfloat16*>(c.v));
+  return le == cudaSuccess ? DFLASH_OK : cuda_fail(le, "kv_epilogue_kernel launch");
 }
 
 }  // namespace dflash

@@ -10,6 +10,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -61,7 +62,7 @@ struct GemmArgs {
   __nv_bfloat16* cache_v;
   int L, Bc, Hkv, cap;
   const int2* rowinfo;     // [M] (sequence, cache row) or (-1, -1)
-  const float2* rope_cs;   // [64][M] (cos, sin), element-major: a warp's rows read it coalesced
+  const __half2* rope_cs;  // [64][M] (cos, sin) in fp16, element-major: a warp's rows read it coalesced
   const __nv_bfloat16* k_gain;  // [L][128] or null
   float eps;
   // epi 2 (drafter head): rows are (sequence b, proposal row k) with k < rows_per_seq
@@ -231,19 +232,17 @@ struct Pieces {
   }
 };
 
-// Eight gains from element e of a head's [128] gain vector (ones without one),
-// one 16-byte load when the vector is 16-byte aligned.
-__device__ __forceinline__ void gain8(const __nv_bfloat16* kg, bool vec, int e, float (&g)[8]) {
+// Eight gains from element e of a head's [128] gain vector, held as fp32 in
+// shared memory (nullptr: ones).
+__device__ __forceinline__ void gain8(const float* kg, int e, float (&g)[8]) {
   if (kg == nullptr) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) g[i] = 1.f;
-  } else if (vec) {
-    const uint4 u = *reinterpret_cast<const uint4*>(kg + e);
-    g[0] = bf16_lo(u.x); g[1] = bf16_hi(u.x); g[2] = bf16_lo(u.y); g[3] = bf16_hi(u.y);
-    g[4] = bf16_lo(u.z); g[5] = bf16_hi(u.z); g[6] = bf16_lo(u.w); g[7] = bf16_hi(u.w);
   } else {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) g[i] = __bfloat162float(kg[e + i]);
+    const float4 a = *reinterpret_cast<const float4*>(kg + e);
+    const float4 b = *reinterpret_cast<const float4*>(kg + e + 4);
+    g[0] = a.x; g[1] = a.y; g[2] = a.z; g[3] = a.w;
+    g[4] = b.x; g[5] = b.y; g[6] = b.z; g[7] = b.w;
   }
 }
 
@@ -367,7 +366,8 @@ __device__ __forceinline__ void f32_group(const AccSrc& src, float* stg, int ks,
 }
 
 // Epilogue of one 128-column head of the K/V projection for this thread's row.
-__device__ __forceinline__ void kv_head_epilogue(const AccSrc& src, int hcol, int col0, int row, const GemmArgs& p) {
+__device__ __forceinline__ void kv_head_epilogue(const AccSrc& src, int hcol, int col0, int row, const float* kgain,
+                                                 const GemmArgs& p) {
   const int hidx = col0 / HD;
   const int l = hidx / (2 * p.Hkv);
   const int s = (hidx / p.Hkv) % 2;
@@ -380,28 +380,33 @@ __device__ __forceinline__ void kv_head_epilogue(const AccSrc& src, int hcol, in
                         (valid ? ri.y : 0)) * HD;
   uint32_t r[32];
   if (s == 1) {
+    uint32_t rv[2][32];
 #pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
-      acc_ld32(src, hcol + c * 32, r);
+    for (int c = 0; c < 4; c += 2) {
+      acc_ld32x2(src, hcol + c * 32, rv[0], hcol + c * 32 + 32, rv[1]);
       if (valid) {
-        uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          d4[i] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * i]), __uint_as_float(r[8 * i + 1])),
-                             pack_bf16x2(__uint_as_float(r[8 * i + 2]), __uint_as_float(r[8 * i + 3])),
-                             pack_bf16x2(__uint_as_float(r[8 * i + 4]), __uint_as_float(r[8 * i + 5])),
-                             pack_bf16x2(__uint_as_float(r[8 * i + 6]), __uint_as_float(r[8 * i + 7])));
+        for (int h2 = 0; h2 < 2; ++h2) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + (c + h2) * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            d4[i] = make_uint4(pack_bf16x2(__uint_as_float(rv[h2][8 * i]), __uint_as_float(rv[h2][8 * i + 1])),
+                               pack_bf16x2(__uint_as_float(rv[h2][8 * i + 2]), __uint_as_float(rv[h2][8 * i + 3])),
+                               pack_bf16x2(__uint_as_float(rv[h2][8 * i + 4]), __uint_as_float(rv[h2][8 * i + 5])),
+                               pack_bf16x2(__uint_as_float(rv[h2][8 * i + 6]), __uint_as_float(rv[h2][8 * i + 7])));
+        }
       }
     }
     return;
   }
-  const float2* cs = p.rope_cs + (valid ? row : 0);
+  // all 64 rotation pairs of the row are requested before the accumulator is
+  // read (unconditionally: rows past the end read row 0 and store nothing),
+  // so their global-memory latency overlaps it
+  const __half2* cs = p.rope_cs + (row < p.M ? row : 0);
   const size_t cs_stride = static_cast<size_t>(p.M);
-  // the rotation angles of the first half are requested before the
-  // accumulator is read, so their global-memory latency overlaps it
-  float2 csh[32];
+  __half2 csh[64];
 #pragma unroll
-  for (int j = 0; j < 32; ++j) csh[j] = valid ? __ldg(cs + j * cs_stride) : make_float2(1.f, 0.f);
+  for (int j = 0; j < 64; ++j) csh[j] = __ldg(cs + j * cs_stride);
   float ss = 0.f;
   uint32_t r2[32];
 #pragma unroll 1
@@ -414,22 +419,17 @@ __device__ __forceinline__ void kv_head_epilogue(const AccSrc& src, int hcol, in
     }
   }
   const float rinv = rsqrtf(ss * (1.0f / HD) + p.eps);
-  const __nv_bfloat16* kg = p.k_gain ? p.k_gain + l * HD : nullptr;
-  const bool kg_vec = kg && (reinterpret_cast<uintptr_t>(kg) & 15u) == 0;
-#pragma unroll 1
+  const float* kg = kgain ? kgain + l * HD : nullptr;
+#pragma unroll
   for (int half = 0; half < 2; ++half) {
     const int e0 = half * 32;
-    if (half == 1) {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) csh[j] = valid ? __ldg(cs + (32 + j) * cs_stride) : make_float2(1.f, 0.f);
-    }
     acc_ld32x2(src, hcol + e0, r, hcol + 64 + e0, r2);
     uint32_t o1[16], o2[16];
 #pragma unroll
     for (int j8 = 0; j8 < 32; j8 += 8) {
       float g1[8], g2[8];
-      gain8(kg, kg_vec, e0 + j8, g1);
-      gain8(kg, kg_vec, 64 + e0 + j8, g2);
+      gain8(kg, e0 + j8, g1);
+      gain8(kg, 64 + e0 + j8, g2);
 #pragma unroll
       for (int i = 0; i < 8; i += 2) {
         float a[2], b[2];
@@ -438,7 +438,7 @@ __device__ __forceinline__ void kv_head_epilogue(const AccSrc& src, int hcol, in
           const int j = j8 + i + k;
           const float y1 = __uint_as_float(r[j]) * rinv * g1[i + k];
           const float y2 = __uint_as_float(r2[j]) * rinv * g2[i + k];
-          const float2 c = csh[j];
+          const float2 c = __half22float2(csh[e0 + j]);
           a[k] = y1 * c.x - y2 * c.y;
           b[k] = y2 * c.x + y1 * c.y;
         }
@@ -599,6 +599,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
     int m, n, kb0, kb1, ks;
     float* stg = stg_all + q * (32 * kStgRow);
     constexpr int FIX = fix_part_float4<BN, MT>();
+    // K/V epilogue: every layer's K gains, as fp32, in the staging area (which
+    // only the fp32 epilogue uses otherwise)
+    const float* kgain = nullptr;
+    if (p.epi == 1 && p.k_gain != nullptr && p.L * HD <= 4 * 32 * kStgRow) {
+      for (int i = threadIdx.x - 64; i < p.L * HD; i += 128) stg_all[i] = __bfloat162float(p.k_gain[i]);
+      named_barrier_sync(1, 128);
+      kgain = stg_all;
+    }
     const int rowl = q * 32 + lane;  // row within a 128-row block
     uint32_t fphase = 0;             // parity of the staged-partials barrier
     while (pcs.next(p, m, n, kb0, kb1, ks)) {
@@ -682,7 +690,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
             if (p.epi == 0)
               f32_group(src, stg, ks, row - lane, col0, lane, p);
             else if (p.epi == 1)
-              kv_head_epilogue(src, 0, col0, row, p);
+              kv_head_epilogue(src, 0, col0, row, kgain, p);
             else
               swiglu_group(src, col0, row, p);
           }

@@ -33,53 +33,69 @@
 namespace dflash {
 namespace {
 
-constexpr int kResThreads = 256;
-constexpr int kResSlots = 4;      // float4 slots per thread: rows up to 4096 wide
+constexpr int kResMaxThreads = 512;
+constexpr int kResSlots = 2;      // float4 of the row per thread: rows up to 4096 wide
 constexpr int kMaxKSplits = 16;   // partial sums per output (split-K slots)
+constexpr int kResBatch = 8;      // slots loaded together
 
 // One CTA per row m: x1 = bf16(x + sum_s part[s]) (written to x); with g_mode,
-// h = bf16(x1 * rsqrt(mean(x1^2) + eps) * g), g == nullptr meaning ones.  The
-// slots of one float4 are loaded together before any add, so each thread keeps
-// all of its loads in flight.
-__global__ void __launch_bounds__(kResThreads) resnorm_kernel(const float* __restrict__ part, int k_splits, int M,
-                                                             int D, __nv_bfloat16* __restrict__ x, int g_mode,
-                                                             const __nv_bfloat16* __restrict__ g, float eps,
-                                                             __nv_bfloat16* __restrict__ h, int* __restrict__ zero_flags,
-                                                             int n_zero) {
+// h = bf16(x1 * rsqrt(mean(x1^2) + eps) * g), g == nullptr meaning ones.
+// Each thread owns kResSlots float4 of the row and requests up to kResBatch
+// slots of each before adding any, so its loads are in flight together.
+__global__ void __launch_bounds__(kResMaxThreads) resnorm_kernel(const float* __restrict__ part, int k_splits, int M,
+                                                                int D, __nv_bfloat16* __restrict__ x, int g_mode,
+                                                                const __nv_bfloat16* __restrict__ g, float eps,
+                                                                __nv_bfloat16* __restrict__ h,
+                                                                int* __restrict__ zero_flags, int n_zero) {
   pdl_wait_primary();
   pdl_launch_dependents();
   const int m = blockIdx.x;
+  const int nthr = blockDim.x;
   // the fixup flags of the GEMM that follows (every earlier grid has completed)
   if (m == 0)
-    for (int i = threadIdx.x; i < n_zero; i += kResThreads) zero_flags[i] = 0;
+    for (int i = threadIdx.x; i < n_zero; i += nthr) zero_flags[i] = 0;
   const int nv = D / 4;
   const float4* pr = reinterpret_cast<const float4*>(part + static_cast<size_t>(m) * D);
   const size_t stride = static_cast<size_t>(M) * D / 4;
   uint2* xr = reinterpret_cast<uint2*>(x + static_cast<size_t>(m) * D);
+  float4 t[kResSlots];
+  uint2 xv[kResSlots];
+#pragma unroll
+  for (int i = 0; i < kResSlots; ++i) {
+    const int v = threadIdx.x + i * nthr;
+    t[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    xv[i] = make_uint2(0u, 0u);
+    if (v < nv) xv[i] = xr[v];
+  }
+  for (int s0 = 0; s0 < k_splits; s0 += kResBatch) {
+    float4 u[kResSlots][kResBatch];
+#pragma unroll
+    for (int i = 0; i < kResSlots; ++i)
+#pragma unroll
+      for (int b = 0; b < kResBatch; ++b) {
+        const int v = threadIdx.x + i * nthr;
+        u[i][b] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (v < nv && s0 + b < k_splits) u[i][b] = __ldcg(pr + (s0 + b) * stride + v);
+      }
+#pragma unroll
+    for (int i = 0; i < kResSlots; ++i)
+#pragma unroll
+      for (int b = 0; b < kResBatch; ++b) {
+        t[i].x += u[i][b].x;
+        t[i].y += u[i][b].y;
+        t[i].z += u[i][b].z;
+        t[i].w += u[i][b].w;
+      }
+  }
   float4 y[kResSlots];
   float ss = 0.f;
 #pragma unroll
   for (int i = 0; i < kResSlots; ++i) {
-    const int v = threadIdx.x + i * kResThreads;
+    const int v = threadIdx.x + i * nthr;
     y[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (v < nv) {
-      float4 u[kMaxKSplits];
-#pragma unroll
-      for (int s = 0; s < kMaxKSplits; ++s)
-        if (s < k_splits) u[s] = __ldcg(pr + s * stride + v);
-      const uint2 xv = xr[v];
-      float4 t = u[0];
-#pragma unroll
-      for (int s = 1; s < kMaxKSplits; ++s) {
-        if (s < k_splits) {
-          t.x += u[s].x;
-          t.y += u[s].y;
-          t.z += u[s].z;
-          t.w += u[s].w;
-        }
-      }
-      const uint32_t lo = pack_bf16x2(bf16_lo(xv.x) + t.x, bf16_hi(xv.x) + t.y);
-      const uint32_t hi = pack_bf16x2(bf16_lo(xv.y) + t.z, bf16_hi(xv.y) + t.w);
+      const uint32_t lo = pack_bf16x2(bf16_lo(xv[i].x) + t[i].x, bf16_hi(xv[i].x) + t[i].y);
+      const uint32_t hi = pack_bf16x2(bf16_lo(xv[i].y) + t[i].z, bf16_hi(xv[i].y) + t[i].w);
       xr[v] = make_uint2(lo, hi);
       y[i] = make_float4(bf16_lo(lo), bf16_hi(lo), bf16_lo(hi), bf16_hi(hi));  // the stored x1
       ss += y[i].x * y[i].x + y[i].y * y[i].y + y[i].z * y[i].z + y[i].w * y[i].w;
@@ -87,17 +103,16 @@ __global__ void __launch_bounds__(kResThreads) resnorm_kernel(const float* __res
   }
   if (!g_mode) return;
   ss = warp_sum(ss);
-  __shared__ float red[kResThreads / 32];
+  __shared__ float red[kResMaxThreads / 32];
   if (threadIdx.x % 32 == 0) red[threadIdx.x / 32] = ss;
   __syncthreads();
   float tot = 0.f;
-#pragma unroll
-  for (int w = 0; w < kResThreads / 32; ++w) tot += red[w];
+  for (int w = 0; w < nthr / 32; ++w) tot += red[w];
   const float r = rsqrtf(tot / static_cast<float>(D) + eps);
   uint2* hr = reinterpret_cast<uint2*>(h + static_cast<size_t>(m) * D);
 #pragma unroll
   for (int i = 0; i < kResSlots; ++i) {
-    const int v = threadIdx.x + i * kResThreads;
+    const int v = threadIdx.x + i * nthr;
     if (v >= nv) continue;
     float g4[4] = {1.f, 1.f, 1.f, 1.f};
     if (g) {
@@ -133,7 +148,8 @@ dflash_status launch_resnorm(const float* part, int k_splits, int M, int D, __nv
                              cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(M));
-  cfg.blockDim = dim3(kResThreads);
+  const int nv = D / 4;
+  cfg.blockDim = dim3(static_cast<unsigned>(std::min(kResMaxThreads, ((nv + kResSlots - 1) / kResSlots + 31) / 32 * 32)));
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
