@@ -384,16 +384,6 @@ struct FusePlan {
   int kv_slots;  // otherwise the GEMM's own epilogue finishes them (fixup)
 };
 
-// The most stream-K shares that meet one tile when `tiles` tiles of num_kb K
-// blocks are cut into `shares` near-equal shares.
-int sk_max_count(long tiles, long num_kb, long shares) {
-  const long tot = tiles * num_kb;
-  auto share = [&](long x) { return ((x + 1) * shares - 1) / tot; };
-  int c = 1;
-  for (long t = 0; t < tiles; ++t)
-    c = std::max(c, static_cast<int>(share((t + 1) * num_kb - 1) - share(t * num_kb) + 1));
-  return c;
-}
 
 FusePlan plan(int M, int D, int num_kb, int n_kv) {
   FusePlan f;

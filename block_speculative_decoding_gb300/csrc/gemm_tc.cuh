@@ -713,6 +713,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
   }
 }
 
+// The most stream-K shares that meet one tile when `tiles` tiles of num_kb K
+// blocks are cut into `shares` near-equal shares (the slots a tile needs).
+inline int sk_max_count(long tiles, long num_kb, long shares) {
+  const long tot = tiles * num_kb;
+  auto share = [&](long x) { return ((x + 1) * shares - 1) / tot; };
+  int c = 1;
+  for (long t = 0; t < tiles; ++t)
+    c = std::max(c, static_cast<int>(share((t + 1) * num_kb - 1) - share(t * num_kb) + 1));
+  return c;
+}
+
 // Stream-K with fixup over all of a GEMM's tiles: as many shares as SMs
 // (every share non-empty); each share's partial-sum area and its flag.
 inline int fixup_shares(int tiles, int num_kb) {

@@ -7,19 +7,21 @@
 // 5120 closes the printed parameter count) and "The released serving cycle"
 // (the drafter runs its layers over the block).
 //
-// Five launches chained as programmatic dependents (M = B * bs block rows):
+// Six launches chained as programmatic dependents (M = B * bs block rows):
 //   1. gemm_tc   Y = o W_o^T, split K; the attention output [B][Hq][bs][128]
 //                is read through a 4D tensor map (rows (b, j), K = (h, e)),
 //                never copied -> fp32 partial slots
 //   2. resnorm   x1 = bf16(x + sum of the slots), written back to x;
 //                h = bf16(RMSNorm(x1) * g_post)
-//   3. gemm_tc   act = bf16(silu(h W_gate^T) * (h W_up^T)): the weight rows are
-//                interleaved in 64-row blocks, so each 128-column unit holds
-//                the gate and up values of the same 64 outputs (epilogue 3);
-//                stream-K over all SMs, the tile's first share adding the
-//                others' partial sums before the SwiGLU
-//   4. gemm_tc   Y = act W_down^T, split K -> slots
-//   5. resnorm   x2 = bf16(x1 + sum of the slots) -> x
+//   3. gemm_tc   [gate | up] = h [W_gate | W_up]^T, stream-K over all SMs ->
+//                fp32 slots; the weight rows are interleaved in 64-row blocks,
+//                so each 128-column tile holds the gate and up values of the
+//                same 64 outputs
+//   4. swiglu    act = bf16(silu(gate) * up) from the slots, one thread per
+//                four outputs (the GEMM's four epilogue warps per SM cannot
+//                hide the latency of this work; a full grid can)
+//   5. gemm_tc   Y = act W_down^T, split K -> slots
+//   6. resnorm   x2 = bf16(x1 + sum of the slots) -> x
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -127,8 +129,60 @@ __global__ void __launch_bounds__(kResMaxThreads) resnorm_kernel(const float* __
   }
 }
 
+// act[m][j] = bf16(silu(gate) * up) from the gate/up GEMM's stream-K partial
+// sums: in 128-column tile t of the GEMM output, columns 0..63 are the gate
+// values and 64..127 the up values of outputs 64 t .. 64 t + 63.  One thread
+// per four outputs; the first kMaxGuSlots slots of both halves are requested
+// together whatever the tile's slot count (unused ones are masked out).
+constexpr int kMaxGuSlots = 4;
+
+__global__ void __launch_bounds__(256) swiglu_kernel(const float* __restrict__ part, int slots,
+                                                     const int* __restrict__ pieces, int tile_rows, int n_tiles,
+                                                     int M, int I, __nv_bfloat16* __restrict__ act) {
+  pdl_wait_primary();  // the partial sums of the gate/up GEMM
+  pdl_launch_dependents();
+  const long t = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int q4 = I / 4;
+  if (t >= static_cast<long>(M) * q4) return;
+  const int m = static_cast<int>(t / q4), j = static_cast<int>(t % q4) * 4;
+  const int tile = j / 64;
+  const size_t N = static_cast<size_t>(2) * I;
+  const size_t slot = static_cast<size_t>(M) * N;
+  const float* g = part + static_cast<size_t>(m) * N + static_cast<size_t>(tile) * 128 + (j % 64);
+  const int ns = pieces[(m / tile_rows) * n_tiles + tile];
+  float4 gu[kMaxGuSlots], uu[kMaxGuSlots];
+#pragma unroll
+  for (int k = 0; k < kMaxGuSlots; ++k) {
+    gu[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    uu[k] = gu[k];
+    if (k < slots) {
+      gu[k] = __ldcg(reinterpret_cast<const float4*>(g + k * slot));
+      uu[k] = __ldcg(reinterpret_cast<const float4*>(g + k * slot + 64));
+    }
+  }
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+#pragma unroll
+  for (int k = 0; k < kMaxGuSlots; ++k)
+    if (k < ns) {
+      a.x += gu[k].x; a.y += gu[k].y; a.z += gu[k].z; a.w += gu[k].w;
+      b.x += uu[k].x; b.y += uu[k].y; b.z += uu[k].z; b.w += uu[k].w;
+    }
+  for (int k = kMaxGuSlots; k < ns; ++k) {  // more slots than kept in registers
+    const float4 x = __ldcg(reinterpret_cast<const float4*>(g + k * slot));
+    const float4 y = __ldcg(reinterpret_cast<const float4*>(g + k * slot + 64));
+    a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
+    b.x += y.x; b.y += y.y; b.z += y.z; b.w += y.w;
+  }
+  // silu(g) = g / (1 + e^-g) with the approximate divide (relative error a
+  // few units in the last place); it gives 0 once e^-g exceeds 2^126
+  auto silu = [](float x) { return __fdividef(x, 1.0f + __expf(-x)); };
+  reinterpret_cast<uint2*>(act + static_cast<size_t>(m) * I + j)[0] =
+      make_uint2(pack_bf16x2(silu(a.x) * b.x, silu(a.y) * b.y), pack_bf16x2(silu(a.z) * b.z, silu(a.w) * b.w));
+}
+
 struct TailPlan {
-  int mt, m_tiles, ks_o, ks_down, gu_shares;  // gate/up: stream-K with fixup over gu_shares CTAs
+  int mt, m_tiles, ks_o, ks_down;
+  int gu_shares, gu_slots;  // gate/up: stream-K over gu_shares CTAs into gu_slots slots
 };
 
 TailPlan tail_plan(int M, int D, int Kq, int I) {
@@ -140,6 +194,7 @@ TailPlan tail_plan(int M, int D, int Kq, int I) {
   t.ks_o = std::min(ks, Kq / kBK);
   t.ks_down = std::min(ks, I / kBK);
   t.gu_shares = fixup_shares(t.m_tiles * (2 * I / 128), D / kBK);
+  t.gu_slots = sk_max_count(static_cast<long>(t.m_tiles) * (2 * I / 128), D / kBK, t.gu_shares);
   return t;
 }
 
@@ -169,10 +224,18 @@ dflash_status run_gemm(const TmapPack& am, const CUtensorMap& bm, const GemmArgs
 
 }  // namespace
 
+// fp32 partial sums: the output projection's and the down projection's split-K
+// slots, and the gate/up GEMM's stream-K slots, share one buffer (each set is
+// read before the next GEMM's epilogue writes, the launches being chained).
+size_t tail_part_floats(const TailPlan& t, int M, int D, int I) {
+  return std::max(static_cast<size_t>(std::max(t.ks_o, t.ks_down)) * M * D,
+                  static_cast<size_t>(t.gu_slots) * M * 2 * I);
+}
+
 size_t tail_ws_bytes(int M, int D, int Hq, int I) {
   const TailPlan t = tail_plan(M, D, Hq * 128, I);
-  return (t.mt == 2 ? fixup_ws_bytes<128, 2>(t.gu_shares) : fixup_ws_bytes<128, 1>(t.gu_shares)) +
-         align256(static_cast<size_t>(std::max(t.ks_o, t.ks_down)) * M * D * sizeof(float)) +
+  return align256(tail_part_floats(t, M, D, I) * sizeof(float)) +
+         align256(static_cast<size_t>(t.m_tiles) * (2 * I / 128) * sizeof(int)) +
          align256(static_cast<size_t>(M) * D * sizeof(__nv_bfloat16)) +
          align256(static_cast<size_t>(M) * I * sizeof(__nv_bfloat16)) + 256;
 }
@@ -183,12 +246,11 @@ dflash_status launch_layer_tail(void* x, const void* attn_out, int B, int bs, in
   const int M = B * bs, Kq = Hq * 128;
   const TailPlan t = tail_plan(M, D, Kq, I);
   WsCarver w(ws);
-  float* part = w.take<float>(static_cast<size_t>(std::max(t.ks_o, t.ks_down)) * M * D);
+  float* part = w.take<float>(tail_part_floats(t, M, D, I));
+  int* gu_pieces = w.take<int>(static_cast<size_t>(t.m_tiles) * (2 * I / 128));
   auto* h = w.take<__nv_bfloat16>(static_cast<size_t>(M) * D);
   auto* act = w.take<__nv_bfloat16>(static_cast<size_t>(M) * I);
   auto* xb = static_cast<__nv_bfloat16*>(x);
-  GemmArgs gu{};
-  if (t.mt == 2) fixup_take<128, 2>(w, t.gu_shares, gu); else fixup_take<128, 1>(w, t.gu_shares, gu);
 
   // 1. output projection, A through a 4D map of the attention output
   TmapPack am{};
@@ -216,8 +278,7 @@ dflash_status launch_layer_tail(void* x, const void* attn_out, int B, int bs, in
   s = t.mt == 2 ? run_gemm<2>(am, bm, a, st, dev) : run_gemm<1>(am, bm, a, st, dev);
   if (s) return s;
   // 2. residual + post-attention norm
-  s = launch_resnorm(part, t.ks_o, M, D, xb, 1, static_cast<const __nv_bfloat16*>(g_post), eps, h, gu.fix_flag,
-                     t.gu_shares, st);
+  s = launch_resnorm(part, t.ks_o, M, D, xb, 1, static_cast<const __nv_bfloat16*>(g_post), eps, h, nullptr, 0, st);
   if (s) return s;
   // 3. gate/up with SwiGLU
   TmapPack hm{};
@@ -226,19 +287,39 @@ dflash_status launch_layer_tail(void* x, const void* attn_out, int B, int bs, in
   CUtensorMap gm;
   s = make_tmap_bf16_2d(&gm, w_gate_up, static_cast<uint64_t>(2) * I, D, 128, kBK);
   if (s) return s;
+  GemmArgs gu{};
   gu.M = M;
   gu.N = 2 * I;
   gu.num_kb = D / kBK;
   gu.kb_per_seg = gu.num_kb;
   gu.m_tiles = t.m_tiles;
   gu.n_tiles = 2 * I / 128;
-  gu.epi = 3;
+  gu.epi = 0;
+  gu.stream_k = t.gu_shares;
+  gu.dp_tiles = 0;
+  gu.k_splits = t.gu_slots;
+  gu.pieces = gu_pieces;
+  gu.out_f32 = part;
   gu.pdl = 1;
   gu.prefetch_b = 1;
-  gu.act = act;
   gu.status = dev.status;
   s = t.mt == 2 ? run_gemm<2>(hm, gm, gu, st, dev) : run_gemm<1>(hm, gm, gu, st, dev);
   if (s) return s;
+  {  // the SwiGLU over the gate/up partial sums
+    cudaLaunchConfig_t cfg = {};
+    const long threads = static_cast<long>(M) * (I / 4);
+    cfg.gridDim = dim3(static_cast<unsigned>((threads + 255) / 256));
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, swiglu_kernel, static_cast<const float*>(part), t.gu_slots,
+                                       static_cast<const int*>(gu_pieces), t.mt * kBM, 2 * I / 128, M, I, act);
+    if (e != cudaSuccess) return cuda_fail(e, "swiglu_kernel launch");
+  }
   // 4. down projection
   TmapPack xm{};
   s = make_tmap_bf16_2d(&xm.a[0], act, static_cast<uint64_t>(M), I, kBM, kBK);
