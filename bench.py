@@ -194,7 +194,11 @@ class Cycle:
         self.cycle += 1
 
 
-LAUNCHES_PER_STEP = 3 + 5 * 3 + 2   # fusion 3, block attention 3 per layer, verification 2
+def launches_per_step(M: int, layers: int) -> int:
+    """The library's kernel launches in one step: fusion 4 for up to 256 new rows (fusion GEMM, row
+    norm, K/V GEMM, K/V epilogue) else 3 (the K/V epilogue fused into the GEMM), block attention 3 per
+    layer (prologue, main, combine), verification 2 (stats, finish)."""
+    return (4 if M <= 256 else 3) + 3 * layers + 2
 
 
 def run_gpu(args):
@@ -303,7 +307,7 @@ def run_gpu(args):
                              "frac": cyc.fuse_bytes / (fuse_ms * 1e-3) / 1e9 / hbm,
                              "tflops": cyc.fuse_flops / (fuse_ms * 1e-3) / 1e12}},
         "peak_note": "HBM and bf16 peaks are the measured copy bandwidth and cuBLAS bf16 GEMM (burst) of this GPU",
-        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "gpu_launches": launches_per_step(cyc.M, cfg.L) * args.steps,
         "clocks": clk,
     }
     if e2e is not None:
@@ -711,6 +715,21 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_profile(args):
+    """One roofline measurement (3 warm-up calls, then the timed calls) of a call
+    outside the cycle, on the batched workload's shapes, for ncu launch lists."""
+    from types import SimpleNamespace
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    cyc = SimpleNamespace(cfg=workloads.BATCHED, T=args.temperature)
+    hbm, tfl, _ = peaks()
+    if args.profile == "layer_tail":
+        line = layer_tail_roofline(cyc, dev, hbm, tfl)
+    else:
+        line = draft_head_roofline(cyc, dev, hbm)
+    print(json.dumps({"profiling_run": True, "profile": args.profile, **line}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -725,7 +744,12 @@ def main():
                     help="profiling runs: time one component of the cycle only")
     ap.add_argument("--batch", type=int, default=None, help="profiling runs: smaller batch")
     ap.add_argument("--layers", type=int, default=None, help="profiling runs: fewer draft layers")
+    ap.add_argument("--profile", default=None, choices=["layer_tail", "draft_head"],
+                    help="profiling runs: only this call's roofline measurement on the batched workload")
     args = ap.parse_args()
+    if args.profile:
+        run_profile(args)
+        return
     if args.warmup < 3 and args.impl == "dflash":
         args.warmup = 3
     if args.impl == "reference":
