@@ -44,7 +44,8 @@ class _KVCacheDesc(ctypes.Structure):
         ("num_layers", ctypes.c_int), ("batch", ctypes.c_int), ("num_kv_heads", ctypes.c_int),
         ("head_dim", ctypes.c_int), ("capacity", ctypes.c_int), ("dtype", ctypes.c_int),
         ("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("seq_len", ctypes.c_void_p),
-        ("ring", ctypes.c_int),
+        ("ring", ctypes.c_int), ("block_table", ctypes.c_void_p), ("page_size", ctypes.c_int),
+        ("num_pages", ctypes.c_int), ("max_pages", ctypes.c_int),
     ]
 
 
@@ -141,18 +142,31 @@ class KVCache:
 
     ring=True makes it the drafter's sliding window: position p lives in row
     p % cap, seq_len may exceed cap, attention sees the latest min(seq_len,
-    cap) positions (block_attn's window must then be 0)."""
+    cap) positions (block_attn's window must then be 0).
+
+    block_table (int32 [B, max_pages]) makes it paged: k, v are then
+    [L, num_pages, Hkv, page_size, 128] and position p of sequence b lives in
+    page block_table[b, p // page_size], row p % page_size (page_size a
+    multiple of 128, bf16, window 0)."""
     k: torch.Tensor
     v: torch.Tensor
     seq_len: torch.Tensor
     ring: bool = False
+    block_table: torch.Tensor | None = None
 
     def desc(self) -> _KVCacheDesc:
-        L, B, H, cap, d = self.k.shape
         if self.seq_len.dtype != torch.int32:
             raise TypeError("seq_len must be int32")
-        return _KVCacheDesc(L, B, H, d, cap, _dt(self.k), self.k.data_ptr(), self.v.data_ptr(),
-                            self.seq_len.data_ptr(), int(bool(self.ring)))
+        if self.block_table is None:
+            L, B, H, cap, d = self.k.shape
+            return _KVCacheDesc(L, B, H, d, cap, _dt(self.k), self.k.data_ptr(), self.v.data_ptr(),
+                                self.seq_len.data_ptr(), int(bool(self.ring)), None, 0, 0, 0)
+        if self.block_table.dtype != torch.int32 or self.block_table.dim() != 2:
+            raise TypeError("block_table must be int32 [batch, max_pages]")
+        L, NP, H, P, d = self.k.shape
+        B, MP = self.block_table.shape
+        return _KVCacheDesc(L, B, H, d, MP * P, _dt(self.k), self.k.data_ptr(), self.v.data_ptr(),
+                            self.seq_len.data_ptr(), int(bool(self.ring)), self.block_table.data_ptr(), P, NP, MP)
 
 
 def version() -> int:
@@ -179,14 +193,14 @@ def fuse_context(taps, cu_new, w_fuse, g_fuse, w_kv, k_gain, cache: KVCache, rop
     J = len(taps)
     M, d_t = taps[0].shape
     D = w_fuse.shape[0]
-    L, B, Hkv = cache.k.shape[:3]
+    desc = cache.desc()
+    L, B, Hkv = desc.num_layers, desc.batch, desc.num_kv_heads
     dt = _dt(taps[0])
     nbytes = fuse_context_workspace_size(M, J, d_t, D, L, Hkv, dt)
     ws = _workspace(nbytes, taps[0].device, workspace)
     arr = (ctypes.c_void_p * J)(*[t.data_ptr() for t in taps])
     for t in taps:
         _ptr(t)
-    desc = cache.desc()
     _check(lib().dflash_fuse_context(J, arr, d_t, _ptr(cu_new), B, M, _ptr(w_fuse), _ptr(g_fuse), D,
                                      _ptr(w_kv), _ptr(k_gain), rope_theta, eps, ctypes.byref(desc),
                                      _ptr(h_t_out), _ptr(ws), nbytes, _stream(stream)))

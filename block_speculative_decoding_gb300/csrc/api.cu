@@ -154,6 +154,19 @@ static dflash_status check_cache(const dflash_kv_cache* c) {
   if (c->dtype != DFLASH_F32 && c->dtype != DFLASH_BF16) return fail(DFLASH_ERR_UNSUPPORTED, "cache dtype");
   if (!aligned16(c->k) || !aligned16(c->v)) return fail(DFLASH_ERR_INVALID_ARGUMENT, "cache k/v must be 16-byte aligned");
   if (c->ring != 0 && c->ring != 1) return fail(DFLASH_ERR_INVALID_ARGUMENT, "cache ring must be 0 or 1");
+  if (c->block_table) {  // paged layout
+    if (c->dtype != DFLASH_BF16) return fail(DFLASH_ERR_UNSUPPORTED, "a paged cache must be bf16");
+    if (c->ring) return fail(DFLASH_ERR_UNSUPPORTED, "a paged cache cannot be a ring");
+    if (c->page_size < 128 || c->page_size % 128 != 0)
+      return fail(DFLASH_ERR_UNSUPPORTED, "page_size must be a positive multiple of 128");
+    if (c->num_pages < 1 || c->max_pages < 1)
+      return fail(DFLASH_ERR_INVALID_ARGUMENT, "num_pages and max_pages must be positive");
+    if (static_cast<long long>(c->max_pages) * c->page_size != c->capacity)
+      return fail(DFLASH_ERR_INVALID_ARGUMENT, "capacity must equal max_pages * page_size");
+    const double prow = double(c->num_layers) * c->num_pages * c->num_kv_heads * c->page_size;
+    if (prow >= 2147483647.0) return fail(DFLASH_ERR_UNSUPPORTED, "cache has 2^31 or more rows");
+    return DFLASH_OK;
+  }
   const double rows = double(c->num_layers) * c->batch * c->num_kv_heads * c->capacity;
   if (rows >= 2147483647.0) return fail(DFLASH_ERR_UNSUPPORTED, "cache has 2^31 or more rows");
   return DFLASH_OK;
@@ -171,7 +184,7 @@ static dflash_status check_ws(void* ws, size_t have, size_t need) {
 
 extern "C" {
 
-int dflash_version(void) { return (1 << 16) | 1; }
+int dflash_version(void) { return (1 << 16) | 2; }
 
 const char* dflash_last_error_string(void) { return t_last_error.c_str(); }
 
@@ -264,6 +277,8 @@ dflash_status dflash_block_attn(int layer, int batch, int block_size, int num_q_
   if (window < 0) return fail(DFLASH_ERR_INVALID_ARGUMENT, "window < 0");
   if (cache->ring && window != 0)
     return fail(DFLASH_ERR_UNSUPPORTED, "a ring cache is its own window: window must be 0");
+  if (cache->block_table && window != 0)
+    return fail(DFLASH_ERR_UNSUPPORTED, "a paged cache takes window 0 (key tiles start on page boundaries)");
   if (!q || !kb || !vb || !out) return fail(DFLASH_ERR_INVALID_ARGUMENT, "NULL q/kb/vb/out");
   if (!aligned16(q) || !aligned16(kb) || !aligned16(vb) || !aligned16(out))
     return fail(DFLASH_ERR_INVALID_ARGUMENT, "q/kb/vb/out must be 16-byte aligned");

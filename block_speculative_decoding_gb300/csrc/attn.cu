@@ -62,8 +62,10 @@ struct AttnParams {
   __nv_bfloat16* out;        // [B, Hq, bs, 128]
   float* opart;              // [B, Hkv, max_splits, rows, 128] normalised partial outputs
   float2* mlpart;            // [B, Hkv, max_splits, rows]      (max, sum) in log2 units
-  const __nv_bfloat16* ck;   // this cache's K and V, [L, B, Hkv, cap, 128]
+  const __nv_bfloat16* ck;   // this cache's K and V, [L, B, Hkv, cap, 128] (paged: [L, num_pages, Hkv, page_size, 128])
   const __nv_bfloat16* cv;
+  const int32_t* table;      // paged layout: [B, max_pages] block table; nullptr: linear or ring
+  int max_pages, page_size, num_pages;
   float scale_log2;          // log2(e) / sqrt(128)
   int* counters;             // [1 + 2 B Hkv], cleared by the prologue: the work-queue counter, per (b, g)
                              // a flag (scores outgrew the running max), then per (b, g) the count of
@@ -316,6 +318,13 @@ __host__ __device__ inline TcLayout tc_layout(int nc, int B, int smem_limit) {
   return L;
 }
 
+// Row of the cache's [rows][128] view that holds position pos of (sequence b,
+// KV head g) in this layer; page: the block-table entry of pos (paged only).
+__device__ __forceinline__ long cache_row(const AttnParams& p, int b, int g, int pos, int page) {
+  if (p.table) return ((static_cast<long>(p.layer) * p.num_pages + page) * p.Hkv + g) * p.page_size + pos % p.page_size;
+  return ((static_cast<long>(p.layer) * p.B + b) * p.Hkv + g) * p.cap + pos;
+}
+
 // One output row computed key by key (4 dims per lane, exact running max):
 // the fallback for a (sequence, KV head) whose scores outgrew the running max
 // of the tensor-core kernel.
@@ -323,17 +332,27 @@ __device__ void attn_row_exact(const AttnParams& p, int b, int g, int row, int f
   const int lane = threadIdx.x % 32;
   const int h = g * p.G + row / p.bs, j = row % p.bs;
   const float4 q = bf16x4_to_f32(p.qh + ((static_cast<size_t>(b) * p.Hq + h) * p.bs + j) * HD + 4 * lane);
-  const size_t cbase = ((static_cast<size_t>(p.layer) * p.B + b) * p.Hkv + g) * p.cap;
   const size_t bbase = (static_cast<size_t>(b) * p.Hkv + g) * p.bs;
   float m = -INFINITY, l = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int t = first; t < n + p.bs; ++t) {
     const bool blk = t >= n;
-    const __nv_bfloat16* kr = blk ? p.kbh + (bbase + (t - n)) * HD : p.ck + (cbase + t) * HD;
-    const __nv_bfloat16* vr = blk ? p.vb + (bbase + (t - n)) * HD : p.cv + (cbase + t) * HD;
-    const float4 k = bf16x4_to_f32(kr + 4 * lane);
+    long crow = 0;
+    bool zero = false;  // a paged position whose block-table entry is outside the pool reads zeros
+    if (!blk) {
+      int page = 0;
+      if (p.table) {
+        page = p.table[static_cast<size_t>(b) * p.max_pages + t / p.page_size];
+        zero = page < 0 || page >= p.num_pages;
+        if (zero) raise_status(p.status, DFLASH_DEV_BAD_SEQLEN);
+      }
+      crow = zero ? 0 : cache_row(p, b, g, t, page);
+    }
+    const __nv_bfloat16* kr = blk ? p.kbh + (bbase + (t - n)) * HD : p.ck + crow * HD;
+    const __nv_bfloat16* vr = blk ? p.vb + (bbase + (t - n)) * HD : p.cv + crow * HD;
+    const float4 k = zero ? make_float4(0.f, 0.f, 0.f, 0.f) : bf16x4_to_f32(kr + 4 * lane);
     const float s = warp_sum(q.x * k.x + q.y * k.y + q.z * k.z + q.w * k.w) * p.scale_log2;
-    const float4 v = bf16x4_to_f32(vr + 4 * lane);
+    const float4 v = zero ? make_float4(0.f, 0.f, 0.f, 0.f) : bf16x4_to_f32(vr + 4 * lane);
     if (s > m) {
       const float f = exp2f(m - s);
       l *= f;
@@ -607,12 +626,31 @@ __global__ void __launch_bounds__(TcCfg<NC>::kThreads, 1) attn_tc_kernel(const _
         tma_load_2d(qdst, &maps.q, q_full + 8 * q.idx, 0, qrow);
         tma_load_2d(qdst + C::kQBoxBytes, &maps.q, q_full + 8 * q.idx, 64, qrow);
         q.next(2);
-        const int rowbase = ((p.layer * p.B + it.b) * p.Hkv + it.g) * p.cap;
         const int brow = (it.b * p.Hkv + it.g) * p.bs;
+        // paged: the block-table entry of the next tile is requested one tile
+        // ahead, so its latency hides behind this tile's ring waits (a key
+        // tile never crosses a page: pages are multiples of 128 rows and tiles
+        // start at multiples of 128).  An entry outside the pool gives a row
+        // outside the tensor map, which TMA fills with zeros.
+        const int32_t* trow = p.table ? p.table + static_cast<size_t>(it.b) * p.max_pages : nullptr;
+        int page = (trow && it.ntiles > 0) ? __ldg(trow + it.kstart / p.page_size) : 0;
         for (int t = 0; t < it.nt && ok; ++t) {
           const bool blk = t >= it.ntiles;
           const uint32_t bytes = blk ? 2 * kBlockBoxRows * 128 : kHalfBytes;
-          const int y = rowbase + it.kstart + t * kKeys;
+          const int pos = it.kstart + t * kKeys;
+          int next_page = page;
+          if (trow && t + 1 < it.ntiles && (pos + kKeys) / p.page_size != pos / p.page_size)
+            next_page = __ldg(trow + (pos + kKeys) / p.page_size);
+          int y = 0;
+          if (!blk) {
+            if (trow && (page < 0 || page >= p.num_pages)) {
+              raise_status(p.status, DFLASH_DEV_BAD_SEQLEN);
+              y = -kKeys;  // wholly outside the map: the tile reads zeros
+            } else {
+              y = static_cast<int>(cache_row(p, it.b, it.g, pos, page));
+            }
+          }
+          page = next_page;
           if (!(ok = mbar_wait(k_empty + 8 * kr.idx, kr.phase ^ 1u, p.status))) break;
           const uint32_t kdst = base + lay.off_k + kr.idx * kHalfBytes;
           mbar_arrive_expect_tx(k_full + 8 * kr.idx, bytes);
@@ -1092,12 +1130,17 @@ dflash_status launch_block_attn(int layer, int B, int bs, int Hq, const void* q,
   p.counters = w.take<int>(1 + 2 * static_cast<size_t>(B) * Hkv);
   p.ck = static_cast<const __nv_bfloat16*>(c.k);
   p.cv = static_cast<const __nv_bfloat16*>(c.v);
+  p.table = c.block_table;
+  p.max_pages = c.max_pages;
+  p.page_size = c.page_size;
+  p.num_pages = c.num_pages;
   p.scale_log2 = 1.4426950408889634f * scale;
   p.status = dev.status;
 
   const int nc = p.rows > 32 ? 64 : 32;   // query rows padded to the MMA's N
   AttnMaps maps;
-  const uint64_t rows = static_cast<uint64_t>(c.num_layers) * c.batch * Hkv * c.capacity;
+  const uint64_t rows = c.block_table ? static_cast<uint64_t>(c.num_layers) * c.num_pages * Hkv * c.page_size
+                                      : static_cast<uint64_t>(c.num_layers) * c.batch * Hkv * c.capacity;
   dflash_status s = make_tmap_bf16_2d(&maps.k, c.k, rows, HD, kKeys, 64);
   if (!s) s = make_tmap_bf16_2d(&maps.v, c.v, rows, HD, kKeys, 64);
   if (!s) s = make_tmap_bf16_2d(&maps.q, qh, static_cast<uint64_t>(B) * Hq * bs, HD, nc, 64);

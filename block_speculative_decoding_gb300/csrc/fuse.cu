@@ -65,7 +65,8 @@ __global__ void __launch_bounds__(kNormMaxThreads) fuse_rownorm_kernel(
     int n_tiles, int M, int D, const TG* __restrict__ g, float eps,
     TH* __restrict__ ht, TH* __restrict__ ht_out, const int32_t* __restrict__ cu_new,
     const int32_t* __restrict__ seq_len, int B, int cap, int ring, InvFreq inv, int2* __restrict__ rowinfo,
-    void* __restrict__ rope_cs, int* __restrict__ zero_flags, int n_zero, unsigned* status) {
+    void* __restrict__ rope_cs, int* __restrict__ zero_flags, int n_zero, const int32_t* __restrict__ table,
+    int max_pages, int page_size, int num_pages, unsigned* status) {
   const int m = blockIdx.x;
   if (threadIdx.x <= HD / 2) {
     int lo = 0, hi = B - 1;
@@ -96,8 +97,21 @@ __global__ void __launch_bounds__(kNormMaxThreads) fuse_rownorm_kernel(
       else
         static_cast<__half2*>(rope_cs)[ci] = __floats2half2_rn(cv, sv);
     } else {
-      rowinfo[m] = valid ? make_int2(b, ring ? pos % cap : pos) : make_int2(-1, -1);  // (sequence, cache row)
-      if (!valid) raise_status(status, seq_ok ? DFLASH_DEV_CAPACITY : DFLASH_DEV_BAD_SEQLEN);
+      // (cache slab, row): linear (sequence, position), ring (sequence, position
+      // mod capacity), paged (page of the position, position mod page size)
+      int2 ri = make_int2(-1, -1);
+      if (!valid) {
+        raise_status(status, seq_ok ? DFLASH_DEV_CAPACITY : DFLASH_DEV_BAD_SEQLEN);
+      } else if (table) {
+        const int pg = table[static_cast<size_t>(b) * max_pages + pos / page_size];
+        if (pg >= 0 && pg < num_pages)
+          ri = make_int2(pg, pos % page_size);
+        else
+          raise_status(status, DFLASH_DEV_BAD_SEQLEN);
+      } else {
+        ri = make_int2(b, ring ? pos % cap : pos);
+      }
+      rowinfo[m] = ri;
     }
   }
   pdl_launch_dependents();
@@ -460,7 +474,7 @@ dflash_status launch_fuse_context(int J, const void* const* taps, int dt_width, 
         segs, dt_width, static_cast<const float*>(w_fuse), M, D, J * dt_width, Y);
     fuse_rownorm_kernel<float, float><<<M, kNormThreads, 0, st>>>(
         Y, 1, nullptr, kBM, D, 1, M, D, static_cast<const float*>(g_fuse), eps, H, static_cast<float*>(h_t_out), cu_new, c.seq_len, B,
-        c.capacity, c.ring, inv, rowinfo, rope_cs, nullptr, 0, dev.status);
+        c.capacity, c.ring, inv, rowinfo, rope_cs, nullptr, 0, nullptr, 0, 0, 0, dev.status);
     F32Segs hs{};
     hs.a[0] = H;
     simt_gemm_f32_kernel<<<dim3((Ntot + 63) / 64, (M + 63) / 64), 256, 0, st>>>(
@@ -543,7 +557,7 @@ dflash_status launch_fuse_context(int J, const void* const* taps, int dt_width, 
                                         static_cast<const __nv_bfloat16*>(g_fuse), eps, H,
                                         static_cast<__nv_bfloat16*>(h_t_out), cu_new, c.seq_len, B, c.capacity,
                                         c.ring, inv, rowinfo, rope_cs, k.fix_flag, f.kv_split ? 0 : f.kv_shares,
-                                        dev.status);
+                                        c.block_table, c.max_pages, c.page_size, c.num_pages, dev.status);
     if (le != cudaSuccess) return cuda_fail(le, "fuse_rownorm_kernel launch");
   }
 
@@ -566,9 +580,13 @@ dflash_status launch_fuse_context(int J, const void* const* taps, int dt_width, 
   k.cache_k = static_cast<__nv_bfloat16*>(c.k);
   k.cache_v = static_cast<__nv_bfloat16*>(c.v);
   k.L = L;
-  k.Bc = c.batch;
+  // a cache slab per (layer, x, head) of R rows: x = sequence and R = capacity
+  // (linear, ring) or x = page and R = page size (paged)
+  const int slabs = c.block_table ? c.num_pages : c.batch;
+  const int slab_rows = c.block_table ? c.page_size : c.capacity;
+  k.Bc = slabs;
   k.Hkv = Hkv;
-  k.cap = c.capacity;
+  k.cap = slab_rows;
   k.rowinfo = rowinfo;
   k.rope_cs = reinterpret_cast<const __half2*>(rope_cs);
   k.k_gain = static_cast<const __nv_bfloat16*>(k_gain);
@@ -591,7 +609,7 @@ dflash_status launch_fuse_context(int J, const void* const* taps, int dt_width, 
   cfg.numAttrs = 1;
   cudaError_t le = cudaLaunchKernelEx(&cfg, kv_epilogue_kernel, static_cast<const float*>(KVpart), f.kv_slots,
                                       static_cast<const int*>(k.pieces), f.kv_mt * kBM, f.kv_n_tiles, M, L, Hkv,
-                                      c.batch, c.capacity, static_cast<const int2*>(rowinfo),
+                                      slabs, slab_rows, static_cast<const int2*>(rowinfo),
                                       reinterpret_cast<const __half2*>(rope_cs), static_cast<const __nv_bfloat16*>(k_gain),
                                       eps, static_cast<__nv_bfloat16*>(c.k), static_cast<__nv_bfloat16*>(c.v));
   return le == cudaSuccess ? DFLASH_OK : cuda_fail(le, "kv_epilogue_kernel launch");

@@ -68,13 +68,17 @@ enum { DFLASH_F32 = 0, DFLASH_BF16 = 1 };
 enum {
   DFLASH_DEV_CAPACITY = 1u << 0,   /* fuse_context: seq_len[b]+n_new[b] > capacity; rows skipped */
   DFLASH_DEV_BAD_TOKEN = 1u << 1,  /* verify: draft token outside [0, V); treated as rejected   */
-  DFLASH_DEV_BAD_SEQLEN = 1u << 2, /* seq_len[b] < 0 or > capacity; sequence skipped          */
+  DFLASH_DEV_BAD_SEQLEN = 1u << 2, /* seq_len[b] < 0 or > capacity, or (paged) a block-table
+                                      entry a new row needs outside [0, num_pages); row skipped */
   DFLASH_DEV_TIMEOUT = 1u << 3     /* a bounded wait inside a kernel gave up (never expected) */
 };
 
 /*
  * Draft KV cache, one per draft model (all layers).  Caller-owned.
- *   k, v    : [num_layers][batch][num_kv_heads][capacity][head_dim], dtype.
+ *   k, v    : linear: [num_layers][batch][num_kv_heads][capacity][head_dim];
+ *             paged: [num_layers][num_pages][num_kv_heads][page_size][head_dim]
+ *             (a page is page_size consecutive positions of one sequence, for
+ *             every KV head and both K and V of the layer); dtype.
  *             K rows hold keys already RMS-normalised and rotated.
  *   seq_len : device int32 [batch], cached positions per sequence.  The calls
  *             read it and never advance it: after dflash_fuse_context the
@@ -86,6 +90,16 @@ enum {
  *             exceed capacity, and attention sees the latest
  *             min(seq_len, capacity) positions (block_attn's window must be 0).
  *             A fusion call may add at most capacity rows per sequence.
+ *   block_table : NULL for the linear layout.  Paged layout (the ragged
+ *             serving shape: sequences take pages from a shared pool as they
+ *             grow): device int32 [batch][max_pages]; position p of sequence b
+ *             lives in page block_table[b * max_pages + p / page_size], row
+ *             p % page_size.  capacity must equal max_pages * page_size;
+ *             page_size a multiple of 128 (one attention key tile never
+ *             crosses a page); bf16 only; ring must be 0; block_attn's window
+ *             must be 0.  Entries past a sequence's length are never read; a
+ *             needed entry outside [0, num_pages) raises DFLASH_DEV_BAD_SEQLEN
+ *             and the fusion skips the row (attention reads zeros there).
  */
 typedef struct {
   int num_layers;
@@ -98,6 +112,10 @@ typedef struct {
   void* v;
   const int32_t* seq_len;
   int ring;        /* 0: linear cache, 1: ring buffer of capacity rows (sliding window) */
+  const int32_t* block_table;  /* NULL: linear layout; else the paged layout's [batch][max_pages] */
+  int page_size;   /* paged: positions per page (multiple of 128) */
+  int num_pages;   /* paged: pages in the pool (the k/v arrays' second dimension) */
+  int max_pages;   /* paged: block-table entries per sequence */
 } dflash_kv_cache;
 
 /* ---------------------------------------------------------------------------

@@ -36,4 +36,5 @@ from .dflash_oracle import (  # noqa: F401
     draft_param_count,
     kv_cache_payload_bytes,
     fusion_weight_bytes,
+    gather_pages,
 )

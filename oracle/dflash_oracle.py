@@ -561,3 +561,27 @@ def kv_cache_payload_bytes(num_layers, num_kv_heads, positions, head_dim, bytes_
 def fusion_weight_bytes(d_model, num_taps, bytes_per_elem):
     """Bytes of W_c in R^{D x J*D} ([DF2] 4.1 memory-overhead example)."""
     return d_model * num_taps * d_model * bytes_per_elem
+
+
+def gather_pages(pool, block_table, page_size):
+    """Linear cache view [L][B][Hkv][max_pages * page_size][d] of a paged pool.
+
+    [E4B] "Cache and latency have separate break-even points" counts the
+    per-sequence cache payload before paging; [DF2] 7.2 has the serving stack
+    keep the draft cache in paged memory.  Neither fixes a layout; this one is
+    the library's: pool [L][num_pages][Hkv][page_size][d], and position p of
+    sequence b is row p % page_size of page block_table[b, p // page_size].
+    Entries outside [0, num_pages) give zero rows.
+    """
+    pool = np.asarray(pool)
+    table = np.asarray(block_table)
+    L, NP, H, P, d = pool.shape
+    assert P == page_size
+    B, MP = table.shape
+    out = np.zeros((L, B, H, MP * P, d), dtype=pool.dtype)
+    for b in range(B):
+        for j in range(MP):
+            pg = int(table[b, j])
+            if 0 <= pg < NP:
+                out[:, b, :, j * P:(j + 1) * P, :] = pool[:, pg]
+    return out

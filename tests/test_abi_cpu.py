@@ -49,20 +49,22 @@ def test_workspace_queries(L):
     assert dfl.block_attn_workspace_size(32, 8, 32, 8, 8256, 0, dfl.BF16) > 0
     assert dfl.block_attn_workspace_size(0, 8, 32, 8, 8256, 0, dfl.BF16) == 0
     assert dfl.fuse_context_workspace_size(256, 5, 2560, 2560, 5, 8, dfl.BF16) >= 256 * 2560 * 2
-    assert dfl.version() == (1 << 16) | 1
+    assert dfl.version() == (1 << 16) | 2
 
 
 def _cache(**kw):
     import block_speculative_decoding_gb300 as dfl
     d = dict(num_layers=5, batch=2, num_kv_heads=8, head_dim=128, capacity=64, dtype=dfl.BF16,
-             k=16, v=16, seq_len=16, ring=0)
+             k=16, v=16, seq_len=16, ring=0, block_table=None, page_size=0, num_pages=0, max_pages=0)
     d.update(kw)
     return dfl._KVCacheDesc(d["num_layers"], d["batch"], d["num_kv_heads"], d["head_dim"], d["capacity"],
-                            d["dtype"], d["k"], d["v"], d["seq_len"], d["ring"])
+                            d["dtype"], d["k"], d["v"], d["seq_len"], d["ring"], d["block_table"], d["page_size"],
+                            d["num_pages"], d["max_pages"])
 
 
 def test_host_validation_rejects_bad_arguments_before_any_launch(L):
     lib, _ = L
+    import block_speculative_decoding_gb300 as dfl
     P = ctypes.c_void_p
     # verify: block size out of range, negative temperature, NULL outputs
     assert lib.dflash_verify(P(16), P(16), 1, P(16), 2, 0, 100, 1.0, 0, 0, P(16), P(16), P(256), 1 << 20, None) == 1
@@ -89,6 +91,15 @@ def test_host_validation_rejects_bad_arguments_before_any_launch(L):
     assert lib.dflash_block_attn(0, 2, 8, 32, P(16), P(16), P(16), None, None, 1e6, 1e-6, ctypes.byref(r), 5, P(16), P(256), 1 << 30, None) == 2
     r = _cache(ring=2)
     assert lib.dflash_block_attn(0, 2, 8, 32, P(16), P(16), P(16), None, None, 1e6, 1e-6, ctypes.byref(r), 0, P(16), P(256), 1 << 30, None) == 1
+    # paged layout: page size a multiple of 128, capacity = max_pages * page_size, bf16 only, no ring,
+    # window 0
+    pg = dict(block_table=16, page_size=128, num_pages=4, max_pages=2, capacity=256)
+    ok = _cache(**pg)
+    for bad, code in ((dict(pg, page_size=64, capacity=128), 2), (dict(pg, capacity=255), 1),
+                      (dict(pg, num_pages=0), 1), (dict(pg, ring=1), 2), (dict(pg, dtype=dfl.F32), 2)):
+        b = _cache(**bad)
+        assert lib.dflash_block_attn(0, 2, 8, 32, P(16), P(16), P(16), None, None, 1e6, 1e-6, ctypes.byref(b), 0, P(16), P(256), 1 << 30, None) == code, bad
+    assert lib.dflash_block_attn(0, 2, 8, 32, P(16), P(16), P(16), None, None, 1e6, 1e-6, ctypes.byref(ok), 64, P(16), P(256), 1 << 30, None) == 2
     # fusion: tap count, widths, capacity visible on the host
     taps = (ctypes.c_void_p * 5)(16, 16, 16, 16, 16)
     assert lib.dflash_fuse_context(0, taps, 2560, P(16), 2, 8, P(16), None, 2560, P(16), None, 1e6, 1e-6, ctypes.byref(c), None, P(256), 1 << 30, None) == 2
