@@ -269,6 +269,7 @@ def run_gpu(args):
     if rank == 0 and not args.no_e2e:
         tensor_lines = fusion_tensor_rooflines(dev, peaks()[1])
         tensor_lines.update(window_attention_roofline(cyc, dev, peaks()[0]))
+        tensor_lines.update(paged_attention_roofline(cyc, dev, peaks()[0]))
         tensor_lines.update(draft_head_roofline(cyc, dev, peaks()[0]))
         tensor_lines.update(layer_tail_roofline(cyc, dev, peaks()[0], peaks()[1]))
 
@@ -358,6 +359,56 @@ def window_attention_roofline(cyc, dev, peak_gbs, W=1024, iters=20):
                                              "frac": gbs / peak_gbs, "ms_per_layer_call": ms,
                                              "note": "ring cache of %d rows per (layer, sequence, KV head); every "
                                                      "sequence longer than the window" % W}}
+
+
+def paged_attention_roofline(cyc, dev, peak_gbs, P=128, iters=20):
+    """Block attention of the batched workload over the same cache contents in
+    a paged pool: 128-row pages, a random permutation of the pool as the block
+    table; five layer calls back to back, CUDA events on the launching stream,
+    3 warm-up rounds; algorithmic bytes as for the linear cache (every cached
+    key and value read once)."""
+    import block_speculative_decoding_gb300 as dfl
+    cfg = cyc.cfg
+    L, B, H, cap, d = cyc.k.shape
+    MP = -(-cap // P)
+    g = torch.Generator().manual_seed(cfg.seed * 1000 + 25)
+    perm = torch.randperm(B * MP, generator=g).to(dev)
+
+    def pool_of(lin):
+        x = torch.nn.functional.pad(lin, (0, 0, 0, MP * P - cap))
+        x = x.view(L, B, H, MP, P, d).permute(0, 1, 3, 2, 4, 5).reshape(L, B * MP, H, P, d)
+        out = torch.empty_like(x)
+        out[:, perm] = x
+        return out
+    pages = dfl.KVCache(pool_of(cyc.k), pool_of(cyc.v), cyc.seq.clone(),
+                        block_table=perm.view(B, MP).to(torch.int32).contiguous())
+    ws = torch.empty(dfl.block_attn_workspace_size(B, cfg.bs, cfg.Hq, H, MP * P, 0, dfl.BF16),
+                     dtype=torch.uint8, device=dev)
+    st = torch.cuda.Stream(device=dev)
+
+    def layers():
+        for l in range(cfg.L):
+            q, kb, vb = cyc.blocks[l]
+            dfl.block_attn(l, q, kb, vb, cyc.w.q_gain[l], cyc.w.k_gain[l], pages, out=cyc.outs[l], workspace=ws,
+                           stream=st)
+    with torch.cuda.stream(st):
+        for _ in range(3):
+            layers()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for _ in range(iters):
+            layers()
+        e1.record(st)
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / (iters * cfg.L)
+    gbs = cyc.attn_bytes_per_call / (ms * 1e-3) / 1e9
+    del pages, ws
+    torch.cuda.empty_cache()
+    return {"block_attn_paged_%d" % P: {"bound": "hbm", "achieved": gbs, "peak": peak_gbs, "unit": "GB/s",
+                                        "frac": gbs / peak_gbs, "ms_per_layer_call": ms,
+                                        "note": "the batched cache in %d-row pages of a shared pool, block table = "
+                                                "a random permutation of the pool" % P}}
 
 
 def draft_head_roofline(cyc, dev, peak_gbs, iters=10):

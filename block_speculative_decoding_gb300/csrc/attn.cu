@@ -421,6 +421,11 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnParams p) {
     acc.z += f * o.z;
     acc.w += f * o.w;
   }
+  // this row's split outputs (512 bytes each) are read by this warp only: drop
+  // them from L2 rather than let the next layer's stream write them back
+  __syncwarp();
+  for (int i = lane; i < 4 * ns; i += 32)
+    discard_l2_line(p.opart + (r0 + static_cast<size_t>(i / 4) * p.rows) * HD + (i % 4) * 32);
   const float inv = den > 0.f ? 1.f / den : 0.f;
   const size_t out_row = (static_cast<size_t>(b) * p.Hq + g * p.G) * p.bs + row;
   reinterpret_cast<uint2*>(p.out + out_row * HD)[lane] =

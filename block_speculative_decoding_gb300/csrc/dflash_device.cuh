@@ -351,6 +351,14 @@ __device__ __forceinline__ void fence_proxy_async_all() {
   asm volatile("fence.proxy.async;" ::: "memory");
 }
 
+// Drop a 128-byte line (128-byte aligned) from L2 without writing it back:
+// for scratch that has been read for the last time (its contents become
+// undefined), so dead partial sums cost no DRAM write-back.  Only the reader
+// that owns the line calls it, after its loads of the line have returned.
+__device__ __forceinline__ void discard_l2_line(const void* p) {
+  asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
 // Bulk copy without a tensor map: `bytes` (a multiple of 16; both addresses
 // 16-byte aligned) from global to this CTA's shared memory, completing on the
 // mbarrier's transaction count.

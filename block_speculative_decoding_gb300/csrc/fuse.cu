@@ -187,6 +187,15 @@ __global__ void __launch_bounds__(kNormMaxThreads) fuse_rownorm_kernel(
   float tot = 0.f;
   for (int w = 0; w < nthr / 32; ++w) tot += red[w];
   const float r = rsqrtf(tot / static_cast<float>(D) + eps);
+  if (in_regs && sizeof(TH) == 2 && D % 32 == 0) {  // whole, aligned 128-byte lines per row
+    // every thread's slot loads have returned (the barrier above): the row's
+    // slot lines are read by this CTA only, drop them from L2 rather than let
+    // them be written back
+    const int lines = D / 32;  // 128-byte lines of one slot row
+    const float* pr = part + static_cast<size_t>(m) * D;
+    for (int i = threadIdx.x; i < k_splits * lines; i += nthr)
+      discard_l2_line(pr + (i / lines) * split_stride * 4 + (i % lines) * 32);
+  }
   auto store = [&](int v, float4 t4) {
     const int e = 4 * v;
     const float g0 = g ? to_f32<TG>(g[e]) : 1.f, g1 = g ? to_f32<TG>(g[e + 1]) : 1.f;
@@ -365,6 +374,11 @@ __global__ void __launch_bounds__(256) kv_epilogue_kernel(
     b.x += y.x;
     b.y += y.y;
   }
+  // the slots' lines of this (row, head) are read by this warp only: drop them
+  // from L2 (4 lines of 128 bytes per slot) rather than let them be written back
+  __syncwarp();
+  const int nread = max(ns, min(slots, kMaxKvSlots));
+  for (int i = lane; i < 4 * nread; i += 32) discard_l2_line(src + (i / 4) * slot + (i % 4) * 32);
   if (s == 0) {
     const float ss = warp_sum(a.x * a.x + a.y * a.y + b.x * b.x + b.y * b.y);
     const float r = rsqrtf(ss * (1.0f / HD) + eps);

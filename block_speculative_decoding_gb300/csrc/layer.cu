@@ -89,6 +89,18 @@ __global__ void __launch_bounds__(kResMaxThreads) resnorm_kernel(const float* __
         t[i].w += u[i][b].w;
       }
   }
+  // the row's slot lines are read by this CTA only (a 128-byte line by eight
+  // consecutive threads of one warp): drop them from L2 once the warp has them
+  if (D % 32 == 0) {
+    __syncwarp();
+    if (threadIdx.x % 8 == 0)
+#pragma unroll
+      for (int i = 0; i < kResSlots; ++i) {
+        const int v = threadIdx.x + i * nthr;
+        if (v < nv)
+          for (int s = 0; s < k_splits; ++s) discard_l2_line(pr + s * stride + v);
+      }
+  }
   float4 y[kResSlots];
   float ss = 0.f;
 #pragma unroll
@@ -172,6 +184,18 @@ __global__ void __launch_bounds__(256) swiglu_kernel(const float* __restrict__ p
     const float4 y = __ldcg(reinterpret_cast<const float4*>(g + k * slot + 64));
     a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
     b.x += y.x; b.y += y.y; b.z += y.z; b.w += y.w;
+  }
+  // the gate and up lines (eight threads of this warp each) are read for the
+  // last time: a whole warp drops them from L2 rather than let them be written back
+  if (((t | 31) < static_cast<long>(M) * q4)) {
+    __syncwarp();
+    if (j % 32 == 0) {
+      const int nread = max(ns, min(slots, kMaxGuSlots));
+      for (int k = 0; k < nread; ++k) {
+        discard_l2_line(g + k * slot);
+        discard_l2_line(g + k * slot + 64);
+      }
+    }
   }
   // silu(g) = g / (1 + e^-g) with the approximate divide (relative error a
   // few units in the last place); it gives 0 once e^-g exceeds 2^126
