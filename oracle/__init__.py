@@ -37,4 +37,7 @@ from .dflash_oracle import (  # noqa: F401
     kv_cache_payload_bytes,
     fusion_weight_bytes,
     gather_pages,
+    block_conv,
+    draft_topm,
+    path_score,
 )

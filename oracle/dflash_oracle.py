@@ -585,3 +585,70 @@ def gather_pages(pool, block_table, page_size):
             if 0 <= pg < NP:
                 out[:, b, :, j * P:(j + 1) * P, :] = pool[:, pg]
     return out
+
+
+# DFlash2 variants  ([DF2] 5 "DFlash2 innovations": local depthwise
+# convolutions and the candidate path selector)
+
+def block_conv(h, w, bias, block_size, residual=False):
+    """[DF2] 5.1: ConvOutput_t = sum_{j=0}^{k-1} W_conv,j (.) H_{t-j} + b_conv,
+    a depthwise (per-channel) 1D convolution along the block positions.
+
+    h [B * block_size, D]: the block rows of B sequences, sequence-major; w
+    [k, D]; bias [D] or None.  Readings: positions before a block's first row
+    contribute zero (the sum stays within one sequence's block and only looks
+    back); with residual the output is h + ConvOutput (the convolution as a
+    sub-layer on the residual stream between attention and the MLP).
+    """
+    h = np.asarray(h, dtype=np.float64)
+    w = np.asarray(w, dtype=np.float64)
+    R, D = h.shape
+    k = w.shape[0]
+    out = np.zeros_like(h)
+    for r in range(R):
+        t = r % block_size
+        acc = np.zeros(D) if bias is None else np.asarray(bias, dtype=np.float64).copy()
+        for j in range(k):
+            if t - j >= 0:
+                acc = acc + w[j] * h[r - j]
+        out[r] = acc
+    return h + out if residual else out
+
+
+def draft_topm(logits, m, temperature, lam):
+    """[DF2] 5.2: the draft head's top-m candidates per block position and the
+    path score S(path) = sum_j log P_draft(x_j^(m_j)) + lam * Entropy(P_draft(x_j)).
+
+    logits [B, R, V] (R draft positions per sequence), P_draft = softmax(l / T),
+    T > 0.  Per row: the m candidates by logit (descending, ties to the lower
+    index; dividing by T > 0 keeps the order), their log-probabilities, and the
+    entropy -sum p ln p.  The score is a sum of per-position terms and the
+    entropy term does not depend on the choice, so the best path takes every
+    position's first candidate; its score is returned per sequence.
+    Returns (idx [B, R, m] int64, logp [B, R, m], entropy [B, R], best [B]).
+    """
+    l = np.asarray(logits, dtype=np.float64)
+    B, R, V = l.shape
+    s = l / temperature
+    mx = s.max(axis=-1, keepdims=True)
+    logz = mx[..., 0] + np.log(np.exp(s - mx).sum(axis=-1))
+    logp_all = s - logz[..., None]
+    p = np.exp(logp_all)
+    ent = -(p * logp_all).sum(axis=-1)
+    idx = np.zeros((B, R, m), dtype=np.int64)
+    for b in range(B):
+        for r in range(R):
+            order = sorted(range(V), key=lambda y: (-l[b, r, y], y))   # descending, lower index first
+            idx[b, r] = order[:m]
+    logp = np.take_along_axis(logp_all, idx, axis=-1)
+    best = logp[..., 0].sum(axis=-1) + lam * ent.sum(axis=-1)
+    return idx, logp, ent, best
+
+
+def path_score(logp, entropy, choice, lam):
+    """S of one path ([DF2] 5.2): choice [B, R] picks candidate choice[b, r] of
+    each position from logp [B, R, m]; entropy [B, R]."""
+    logp = np.asarray(logp, dtype=np.float64)
+    ch = np.asarray(choice)
+    sel = np.take_along_axis(logp, ch[..., None], axis=-1)[..., 0]
+    return sel.sum(axis=-1) + lam * np.asarray(entropy, dtype=np.float64).sum(axis=-1)
