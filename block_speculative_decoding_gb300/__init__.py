@@ -86,6 +86,12 @@ def lib():
     L.dflash_draft_layer_tail_workspace_size.restype = sz
     L.dflash_draft_layer_tail.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, f32, vp, sz, vp]
     L.dflash_draft_layer_tail.restype = i32
+    L.dflash_block_conv.argtypes = [vp, i32, i32, i32, i32, vp, vp, i32, vp, vp]
+    L.dflash_block_conv.restype = i32
+    L.dflash_draft_topm_workspace_size.argtypes = [i32] * 4
+    L.dflash_draft_topm_workspace_size.restype = sz
+    L.dflash_draft_topm.argtypes = [vp, i32, i32, i32, i32, f32, f32, vp, vp, vp, vp, vp, sz, vp]
+    L.dflash_draft_topm.restype = i32
     L.dflash_verify_noalloc_max_scratch.argtypes = []
     L.dflash_verify_noalloc_max_scratch.restype = sz
     L.dflash_verify_noalloc.argtypes = [vp, vp, i32, vp, i32, i32, i32, f32, u64, u64, vp, vp, vp]
@@ -244,6 +250,40 @@ def interleave_gate_up(w_gate, w_up):
     """[2I, D] rows in the layer tail's order: 64 gate rows, then the same 64 up rows."""
     I, D = w_gate.shape
     return torch.stack([w_gate.view(I // 64, 64, D), w_up.view(I // 64, 64, D)], dim=1).reshape(2 * I, D)
+
+
+def block_conv(h, w, bias, block_size, residual=False, out=None, stream=None):
+    """DFlash2 local depthwise convolution along each sequence's block rows:
+    out_t = sum_j w[j] * h_{t-j} + bias (+ h_t with residual).  h [B * bs, D]
+    bf16, w [k, D] bf16, bias [D] or None; out may be h (in place)."""
+    R, D = h.shape
+    if R % block_size:
+        raise ValueError("rows must be a multiple of block_size")
+    if out is None:
+        out = torch.empty_like(h)
+    _check(lib().dflash_block_conv(_ptr(h), R // block_size, block_size, D, w.shape[0], _ptr(w), _ptr(bias),
+                                   int(bool(residual)), _ptr(out), _stream(stream)))
+    return out
+
+
+def draft_topm_workspace_size(batch, rows_per_seq, vocab, m):
+    return lib().dflash_draft_topm_workspace_size(batch, rows_per_seq, vocab, m)
+
+
+def draft_topm(logits, m, temperature, lam, workspace=None, stream=None):
+    """DFlash2 candidate path selector inputs for draft logits [B, R, V] bf16:
+    returns (idx [B, R, m] int32, logp [B, R, m], entropy [B, R], path_score [B])."""
+    B, R, V = logits.shape
+    dev = logits.device
+    idx = torch.empty(B, R, m, dtype=torch.int32, device=dev)
+    logp = torch.empty(B, R, m, dtype=torch.float32, device=dev)
+    ent = torch.empty(B, R, dtype=torch.float32, device=dev)
+    score = torch.empty(B, dtype=torch.float32, device=dev)
+    nbytes = draft_topm_workspace_size(B, R, V, m)
+    ws = _workspace(nbytes, dev, workspace)
+    _check(lib().dflash_draft_topm(_ptr(logits), B, R, V, m, float(temperature), float(lam), _ptr(idx), _ptr(logp),
+                                   _ptr(ent), _ptr(score), _ptr(ws), nbytes, _stream(stream)))
+    return idx, logp, ent, score
 
 
 def draft_layer_tail_workspace_size(batch, block_size, num_q_heads, d_model, mlp_dim):

@@ -184,7 +184,7 @@ static dflash_status check_ws(void* ws, size_t have, size_t need) {
 
 extern "C" {
 
-int dflash_version(void) { return (1 << 16) | 2; }
+int dflash_version(void) { return (1 << 16) | 3; }
 
 const char* dflash_last_error_string(void) { return t_last_error.c_str(); }
 
@@ -360,6 +360,56 @@ dflash_status dflash_draft_head(const void* x, int batch, int rows_per_seq, int 
   if (s) return s;
   return launch_draft_head(x, batch, rows_per_seq, d_model, g_final, eps, w_head, vocab, temperature, seed, cycle,
                            logits_out, tokens_out, workspace, static_cast<cudaStream_t>(stream), dev);
+}
+
+// ------------------------------------------------------- DFlash2 variants ----
+
+dflash_status dflash_block_conv(const void* h, int batch, int block_size, int d_model, int kernel, const void* w,
+                                const void* bias, int residual, void* out, void* stream) {
+  if (batch < 0 || block_size < 1 || block_size > 16 || d_model < 1 || kernel < 1 || kernel > 8)
+    return fail(DFLASH_ERR_INVALID_ARGUMENT, "need batch >= 0, 1 <= block_size <= 16, d_model >= 1, 1 <= kernel <= 8");
+  if (residual != 0 && residual != 1) return fail(DFLASH_ERR_INVALID_ARGUMENT, "residual must be 0 or 1");
+  if (batch == 0) return DFLASH_OK;
+  if (d_model % 4) return fail(DFLASH_ERR_UNSUPPORTED, "block_conv needs d_model % 4 == 0");
+  if (!h || !w || !out) return fail(DFLASH_ERR_INVALID_ARGUMENT, "NULL h/w/out");
+  auto a8 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 7) == 0; };
+  if (!a8(h) || !a8(w) || !a8(out) || (bias && !a8(bias)))
+    return fail(DFLASH_ERR_INVALID_ARGUMENT, "h, w, bias and out must be 8-byte aligned");
+  if (double(batch) * (d_model / 4) >= 2147483647.0) return fail(DFLASH_ERR_UNSUPPORTED, "block_conv: too large");
+  DeviceInfo dev;
+  dflash_status s = device_info(&dev);
+  if (s) return s;
+  return launch_block_conv(h, batch, block_size, d_model, kernel, w, bias, residual, out,
+                           static_cast<cudaStream_t>(stream));
+}
+
+size_t dflash_draft_topm_workspace_size(int batch, int rows_per_seq, int vocab, int m) {
+  if (batch < 1 || rows_per_seq < 1 || vocab < 1 || m < 1) return 0;
+  return topm_ws_bytes(batch, rows_per_seq, vocab, m);
+}
+
+dflash_status dflash_draft_topm(const void* logits, int batch, int rows_per_seq, int vocab, int m, float temperature,
+                                float lambda, int32_t* idx_out, float* logp_out, float* entropy_out,
+                                float* path_score_out, void* workspace, size_t workspace_bytes, void* stream) {
+  if (batch < 0 || rows_per_seq < 1 || rows_per_seq > 16 || vocab < 1 || m < 1)
+    return fail(DFLASH_ERR_INVALID_ARGUMENT, "need batch >= 0, 1 <= rows_per_seq <= 16, vocab >= 1, m >= 1");
+  if (m > topm_max_m() || m > vocab) return fail(DFLASH_ERR_UNSUPPORTED, "draft_topm: m <= 8 and m <= vocab");
+  if (!(temperature > 0.0f)) return fail(DFLASH_ERR_INVALID_ARGUMENT, "draft_topm: temperature must be > 0");
+  if (batch == 0) return DFLASH_OK;
+  if (vocab % 8 || vocab > 32 * 16384)
+    return fail(DFLASH_ERR_UNSUPPORTED, "draft_topm needs vocab % 8 == 0 and vocab <= 524288");
+  if (double(batch) * rows_per_seq * ((vocab + 16383) / 16384) >= 2147483647.0)
+    return fail(DFLASH_ERR_UNSUPPORTED, "draft_topm: too many rows");
+  if (!logits || !idx_out || !logp_out || !entropy_out || !path_score_out)
+    return fail(DFLASH_ERR_INVALID_ARGUMENT, "NULL logits or output");
+  if (!aligned16(logits)) return fail(DFLASH_ERR_INVALID_ARGUMENT, "logits must be 16-byte aligned");
+  dflash_status s = check_ws(workspace, workspace_bytes, topm_ws_bytes(batch, rows_per_seq, vocab, m));
+  if (s) return s;
+  DeviceInfo dev;
+  s = device_info(&dev);
+  if (s) return s;
+  return launch_draft_topm(logits, batch, rows_per_seq, vocab, m, temperature, lambda, idx_out, logp_out,
+                           entropy_out, path_score_out, workspace, static_cast<cudaStream_t>(stream));
 }
 
 // --------------------------------------------------------- fuse context ----

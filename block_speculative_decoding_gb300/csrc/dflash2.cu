@@ -1,0 +1,388 @@
+// DFlash2 variants: the local depthwise convolution along the draft block and
+// the candidate path selector's per-position statistics.
+//
+// Page: "DFlash & DFlash2: Block-Diffusion LLM-Speedup", section 5 (DFlash2
+// innovations): 5.1 depthwise 1D convolutions of kernel width k in {3, 5}
+// between the drafter's attention and feed-forward sub-layers,
+// ConvOutput_t = sum_j W_conv,j (.) H_{t-j} + b_conv; 5.2 the draft head's
+// top-m candidates per block position and the path score
+// S = sum_j log P_draft(x_j^(m_j)) + lambda * Entropy(P_draft(x_j)).
+//
+// Kernels:
+//   block_conv_kernel  one thread per (sequence, 4 channels): the block's rows
+//                      of those channels in registers, the causal depthwise
+//                      sum, bf16 out (in place allowed).
+//   topm_chunk_kernel  one CTA per (row, 16384-logit chunk): the chunk's
+//                      (max, sum e^(s-max), sum e^(s-max) (s-max)) of s = l / T
+//                      and its m best logits (ties to the lower index).
+//   topm_merge_kernel  one CTA per sequence, one warp per row: the row's
+//                      log-normaliser and entropy from the chunk triples, its
+//                      m best candidates from the chunks' candidates, their
+//                      log-probabilities, and the sequence's best-path score.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cfloat>
+#include <climits>
+
+#include "dflash_device.cuh"
+#include "dflash_internal.h"
+
+namespace dflash {
+namespace {
+
+constexpr int kConvMaxBlock = 16;
+constexpr int kConvMaxK = 8;
+
+// h, out [B * bs, D] bf16 (sequence-major rows, out may be h); w [k, D] bf16;
+// bias [D] bf16 or null.  out_t = sum_{j < k, j <= t} w_j * h_{t-j} + b
+// (+ h_t if residual), t the row's position in its block.  One thread per
+// (sequence, 4 channels).
+__global__ void __launch_bounds__(256) block_conv_kernel(const __nv_bfloat16* h, int B, int bs, int D, int k,
+                                                         const __nv_bfloat16* __restrict__ w,
+                                                         const __nv_bfloat16* __restrict__ bias, int residual,
+                                                         __nv_bfloat16* out) {
+  const int groups = D / 4;
+  const long t = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= static_cast<long>(B) * groups) return;
+  const int b = static_cast<int>(t / groups), c0 = static_cast<int>(t % groups) * 4;
+  float x[kConvMaxBlock][4];
+#pragma unroll
+  for (int r = 0; r < kConvMaxBlock; ++r) {
+    if (r >= bs) continue;
+    const uint2 v = *reinterpret_cast<const uint2*>(h + (static_cast<size_t>(b) * bs + r) * D + c0);
+    x[r][0] = bf16_lo(v.x);
+    x[r][1] = bf16_hi(v.x);
+    x[r][2] = bf16_lo(v.y);
+    x[r][3] = bf16_hi(v.y);
+  }
+  float wk[kConvMaxK][4];
+#pragma unroll
+  for (int j = 0; j < kConvMaxK; ++j) {
+    if (j >= k) continue;
+    const uint2 v = *reinterpret_cast<const uint2*>(w + static_cast<size_t>(j) * D + c0);
+    wk[j][0] = bf16_lo(v.x);
+    wk[j][1] = bf16_hi(v.x);
+    wk[j][2] = bf16_lo(v.y);
+    wk[j][3] = bf16_hi(v.y);
+  }
+  float bv[4] = {0.f, 0.f, 0.f, 0.f};
+  if (bias) {
+    const uint2 v = *reinterpret_cast<const uint2*>(bias + c0);
+    bv[0] = bf16_lo(v.x);
+    bv[1] = bf16_hi(v.x);
+    bv[2] = bf16_lo(v.y);
+    bv[3] = bf16_hi(v.y);
+  }
+  // every input row is in registers before the first store, so out may be h
+#pragma unroll
+  for (int r = 0; r < kConvMaxBlock; ++r) {
+    if (r >= bs) continue;
+    float acc[4] = {bv[0], bv[1], bv[2], bv[3]};
+#pragma unroll
+    for (int j = 0; j < kConvMaxK; ++j) {
+      if (j >= k || j > r) continue;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[i] = fmaf(wk[j][i], x[r - j][i], acc[i]);
+    }
+    if (residual) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[i] += x[r][i];
+    }
+    *reinterpret_cast<uint2*>(out + (static_cast<size_t>(b) * bs + r) * D + c0) =
+        make_uint2(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]));
+  }
+}
+
+constexpr int kTopmThreads = 256;
+constexpr int kTopmChunk = 16384;                       // logits per chunk CTA
+constexpr int kTopmVecs = kTopmChunk / (kTopmThreads * 8);  // 8 vectors of 8 bf16 per thread
+constexpr int kMaxM = 8;
+
+// (value, index) order of the candidates: larger logit first, then lower index.
+__device__ __forceinline__ bool better(float v1, int i1, float v2, int i2) {
+  return v1 > v2 || (v1 == v2 && i1 < i2);
+}
+
+// Warp-wide best (value, index); every lane gets it.
+__device__ __forceinline__ void warp_best(float& v, int& i) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, i, o);
+    if (better(ov, oi, v, i)) {
+      v = ov;
+      i = oi;
+    }
+  }
+}
+
+// One CTA per (row, chunk).  stats[row][c] = (max s, sum e^(s - max),
+// sum e^(s - max) (s - max), 0) over the chunk's finite logits, s = l * inv_t;
+// cand[row][c][r] = (logit bits, index) of the chunk's r-th best logit.
+__global__ void __launch_bounds__(kTopmThreads) topm_chunk_kernel(const __nv_bfloat16* __restrict__ logits, int V,
+                                                                 int nchunk, float inv_t, int m,
+                                                                 float4* __restrict__ stats, int2* __restrict__ cand) {
+  const int row = blockIdx.x / nchunk, c = blockIdx.x % nchunk;
+  const __nv_bfloat16* lr = logits + static_cast<size_t>(row) * V;
+  const int e0 = c * kTopmChunk;
+  const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
+  uint4 raw[kTopmVecs];
+#pragma unroll
+  for (int i = 0; i < kTopmVecs; ++i) {
+    const int e = e0 + (i * kTopmThreads + tid) * 8;
+    raw[i] = e < V ? __ldcs(reinterpret_cast<const uint4*>(lr + e)) : make_uint4(0xFF80FF80u, 0xFF80FF80u,
+                                                                                0xFF80FF80u, 0xFF80FF80u);
+  }
+  // this thread's m best, sorted (best first), and its maximum
+  float lv[kMaxM];
+  int li[kMaxM];
+#pragma unroll
+  for (int r = 0; r < kMaxM; ++r) {
+    lv[r] = -INFINITY;
+    li[r] = INT_MAX;
+  }
+  float mx = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < kTopmVecs; ++i) {
+    const uint32_t u[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float v = (j & 1) ? bf16_hi(u[j / 2]) : bf16_lo(u[j / 2]);
+      const int idx = e0 + (i * kTopmThreads + tid) * 8 + j;
+      mx = fmaxf(mx, v);
+      if (idx < V && better(v, idx, lv[kMaxM - 1], li[kMaxM - 1])) {
+        // insert, keeping the list sorted (the first m entries are used)
+        float cv = v;
+        int ci = idx;
+#pragma unroll
+        for (int r = 0; r < kMaxM; ++r) {
+          if (better(cv, ci, lv[r], li[r])) {
+            const float tv = lv[r];
+            const int ti = li[r];
+            lv[r] = cv;
+            li[r] = ci;
+            cv = tv;
+            ci = ti;
+          }
+        }
+      }
+    }
+  }
+  __shared__ float s_red[kTopmThreads / 32][2];
+  __shared__ float s_bv[kTopmThreads / 32];
+  __shared__ int s_bi[kTopmThreads / 32];
+  __shared__ int s_wi;
+  // the chunk's maximum of s = l * inv_t (inv_t > 0 keeps the order)
+  float wm = warp_max(mx);
+  if (lane == 0) s_red[warp][0] = wm;
+  __syncthreads();
+  float M = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < kTopmThreads / 32; ++w) M = fmaxf(M, s_red[w][0]);
+  const float Ms = M * inv_t;
+  float S = 0.f, W = 0.f;
+  if (M != -INFINITY) {
+#pragma unroll
+    for (int i = 0; i < kTopmVecs; ++i) {
+      const uint32_t u[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float v = (j & 1) ? bf16_hi(u[j / 2]) : bf16_lo(u[j / 2]);
+        if (v == -INFINITY) continue;  // zero probability (also the padding past V)
+        const float d = v * inv_t - Ms;
+        const float e = __expf(d);
+        S += e;
+        W = fmaf(e, d, W);
+      }
+    }
+  }
+  S = warp_sum(S);
+  W = warp_sum(W);
+  __syncthreads();  // every thread has read s_red[.][0]
+  if (lane == 0) {
+    s_red[warp][0] = S;
+    s_red[warp][1] = W;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float St = 0.f, Wt = 0.f;
+    for (int w = 0; w < kTopmThreads / 32; ++w) {
+      St += s_red[w][0];
+      Wt += s_red[w][1];
+    }
+    stats[static_cast<size_t>(row) * nchunk + c] = make_float4(Ms, St, Wt, 0.f);
+  }
+  // the chunk's m best: m rounds over the threads' list heads
+  int2* cout = cand + (static_cast<size_t>(row) * nchunk + c) * m;
+  for (int r = 0; r < m; ++r) {
+    float bv = lv[0];
+    int bi = li[0];
+    warp_best(bv, bi);
+    if (lane == 0) {
+      s_bv[warp] = bv;
+      s_bi[warp] = bi;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      float v = lane < kTopmThreads / 32 ? s_bv[lane] : -INFINITY;
+      int i = lane < kTopmThreads / 32 ? s_bi[lane] : INT_MAX;
+      warp_best(v, i);
+      if (lane == 0) {
+        s_wi = i;
+        cout[r] = make_int2(__float_as_int(v), i);
+      }
+    }
+    __syncthreads();
+    if (li[0] == s_wi && s_wi != INT_MAX) {  // this thread's head won: pop it
+#pragma unroll
+      for (int q = 0; q < kMaxM - 1; ++q) {
+        lv[q] = lv[q + 1];
+        li[q] = li[q + 1];
+      }
+      lv[kMaxM - 1] = -INFINITY;
+      li[kMaxM - 1] = INT_MAX;
+    }
+  }
+}
+
+// One CTA per sequence, one warp per draft row r < R: the row's
+// log-normaliser logZ = max + ln S and entropy ln S - W / S from the chunk
+// triples, its m best candidates from the chunks' candidates with
+// logp = l * inv_t - logZ, and the sequence's best-path score
+// sum_r (logp of the first candidate) + lambda * sum_r entropy.
+__global__ void __launch_bounds__(512) topm_merge_kernel(const float4* __restrict__ stats,
+                                                        const int2* __restrict__ cand, int R, int nchunk, int m,
+                                                        float inv_t, float lambda, int32_t* __restrict__ idx_out,
+                                                        float* __restrict__ logp_out, float* __restrict__ ent_out,
+                                                        float* __restrict__ score_out) {
+  pdl_wait_primary();
+  pdl_launch_dependents();
+  const int b = blockIdx.x, warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  __shared__ float s_part[16];
+  if (warp < R) {
+    const int row = b * R + warp;
+    // log-normaliser and entropy: rescale every chunk's sums to the row maximum
+    float M = -INFINITY;
+    for (int c = lane; c < nchunk; c += 32) M = fmaxf(M, stats[static_cast<size_t>(row) * nchunk + c].x);
+    M = warp_max(M);
+    float S = 0.f, W = 0.f;
+    if (M != -INFINITY) {
+      for (int c = lane; c < nchunk; c += 32) {
+        const float4 t = stats[static_cast<size_t>(row) * nchunk + c];
+        if (t.x == -INFINITY) continue;
+        const float f = __expf(t.x - M);
+        S = fmaf(f, t.y, S);
+        W = fmaf(f, t.z + (t.x - M) * t.y, W);
+      }
+    }
+    S = warp_sum(S);
+    W = warp_sum(W);
+    const float logz = M + logf(S);
+    const float ent = S > 0.f ? logf(S) - W / S : 0.f;
+    // the m best of the nchunk * m chunk candidates (each lane holds up to
+    // kMaxCand of them), m rounds of a warp arg-best with exclusion
+    constexpr int kMaxCand = 8;  // nchunk * m <= 256
+    float cv[kMaxCand];
+    int ci[kMaxCand];
+    const int ncand = nchunk * m;
+#pragma unroll
+    for (int q = 0; q < kMaxCand; ++q) {
+      const int k = lane + 32 * q;
+      cv[q] = -INFINITY;
+      ci[q] = INT_MAX;
+      if (k < ncand) {
+        const int2 e = cand[static_cast<size_t>(row) * ncand + k];
+        if (e.y != INT_MAX) {
+          cv[q] = __int_as_float(e.x);
+          ci[q] = e.y;
+        }
+      }
+    }
+    float first = 0.f;
+    for (int r = 0; r < m; ++r) {
+      float bv = -INFINITY;
+      int bi = INT_MAX;
+#pragma unroll
+      for (int q = 0; q < kMaxCand; ++q)
+        if (better(cv[q], ci[q], bv, bi)) {
+          bv = cv[q];
+          bi = ci[q];
+        }
+      warp_best(bv, bi);
+#pragma unroll
+      for (int q = 0; q < kMaxCand; ++q)
+        if (ci[q] == bi) {
+          cv[q] = -INFINITY;
+          ci[q] = INT_MAX;
+        }
+      const float lp = bi == INT_MAX ? -INFINITY : bv * inv_t - logz;
+      if (r == 0) first = lp;
+      if (lane == 0) {
+        idx_out[static_cast<size_t>(row) * m + r] = bi == INT_MAX ? -1 : bi;
+        logp_out[static_cast<size_t>(row) * m + r] = lp;
+      }
+    }
+    if (lane == 0) {
+      ent_out[row] = ent;
+      s_part[warp] = first + lambda * ent;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float sc = 0.f;
+    for (int r = 0; r < R; ++r) sc += s_part[r];
+    score_out[b] = sc;
+  }
+}
+
+}  // namespace
+
+dflash_status launch_block_conv(const void* h, int B, int bs, int D, int k, const void* w, const void* bias,
+                                int residual, void* out, cudaStream_t st) {
+  const long threads = static_cast<long>(B) * (D / 4);
+  block_conv_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(h), B, bs, D, k, static_cast<const __nv_bfloat16*>(w),
+      static_cast<const __nv_bfloat16*>(bias), residual, static_cast<__nv_bfloat16*>(out));
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? DFLASH_OK : cuda_fail(e, "block_conv_kernel launch");
+}
+
+size_t topm_ws_bytes(int B, int R, int V, int m) {
+  const size_t rows = static_cast<size_t>(B) * R;
+  const size_t nchunk = (static_cast<size_t>(V) + kTopmChunk - 1) / kTopmChunk;
+  return align256(rows * nchunk * sizeof(float4)) + align256(rows * nchunk * m * sizeof(int2)) + 256;
+}
+
+int topm_max_m() { return kMaxM; }
+int topm_max_chunks_times_m() { return 32 * 8; }
+
+dflash_status launch_draft_topm(const void* logits, int B, int R, int V, int m, float T, float lambda,
+                                int32_t* idx, float* logp, float* ent, float* score, void* ws, cudaStream_t st) {
+  const int nchunk = (V + kTopmChunk - 1) / kTopmChunk;
+  WsCarver w(ws);
+  float4* stats = w.take<float4>(static_cast<size_t>(B) * R * nchunk);
+  int2* cand = w.take<int2>(static_cast<size_t>(B) * R * nchunk * m);
+  const float inv_t = 1.0f / T;
+  topm_chunk_kernel<<<static_cast<unsigned>(static_cast<long>(B) * R * nchunk), kTopmThreads, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(logits), V, nchunk, inv_t, m, stats, cand);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "topm_chunk_kernel launch");
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(B));
+  cfg.blockDim = dim3(static_cast<unsigned>(32 * R));
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, topm_merge_kernel, static_cast<const float4*>(stats), static_cast<const int2*>(cand),
+                         R, nchunk, m, inv_t, lambda, idx, logp, ent, score);
+  return e == cudaSuccess ? DFLASH_OK : cuda_fail(e, "topm_merge_kernel launch");
+}
+
+}  // namespace dflash
+

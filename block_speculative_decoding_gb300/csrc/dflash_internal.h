@@ -75,6 +75,14 @@ dflash_status launch_layer_tail(void* x, const void* attn_out, int B, int bs, in
                                 const void* g_post, const void* w_gate_up, const void* w_down, float eps, void* ws,
                                 cudaStream_t st, const DeviceInfo& dev);
 
+// --- DFlash2 variants ----------------------------------------------------------
+dflash_status launch_block_conv(const void* h, int B, int bs, int D, int k, const void* w, const void* bias,
+                                int residual, void* out, cudaStream_t st);
+size_t topm_ws_bytes(int B, int R, int V, int m);
+int topm_max_m();
+dflash_status launch_draft_topm(const void* logits, int B, int R, int V, int m, float T, float lambda,
+                                int32_t* idx, float* logp, float* ent, float* score, void* ws, cudaStream_t st);
+
 // --- context fusion ----------------------------------------------------------
 size_t fuse_ws_bytes(int M, int J, int dt_width, int D, int L, int Hkv, dflash_dtype dt);
 dflash_status launch_fuse_context(int J, const void* const* taps, int dt_width, const int32_t* cu_new,

@@ -258,6 +258,45 @@ DFLASH_API dflash_status dflash_philox4x32_10(const uint32_t* ctr, uint32_t key0
                                    uint32_t* out, int n, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * 6. DFlash2 variants (DFlash & DFlash2 page, section 5).
+ *
+ * dflash_block_conv -- 5.1, the local depthwise 1D convolution along the
+ *    block:  out_t = sum_{j=0}^{k-1} w_j (.) h_{t-j} + bias  (+ h_t if residual)
+ *  h, out       : [batch * block_size, d_model] bf16, row b * block_size + t;
+ *                 out may be h (in place).  Positions before a block's first
+ *                 row contribute zero: the sum never crosses sequences.
+ *  w            : [kernel, d_model] bf16 (per-channel taps, tap j on h_{t-j});
+ *                 bias [d_model] bf16 or NULL.  kernel 1..8 (the pages use 3, 5).
+ *  residual     : 1 adds h_t (the convolution as a sub-layer on the residual
+ *                 stream between attention and the MLP), 0 the plain formula.
+ *  Constraints: 1 <= block_size <= 16, d_model % 4 == 0, 8-byte aligned pointers.
+ *
+ * dflash_draft_topm -- 5.2, the candidate path selector's inputs: per draft
+ *    position (row) of logits [batch, rows_per_seq, vocab] bf16, with
+ *    P = softmax(logits / temperature), temperature > 0:
+ *  idx_out      : [batch, rows_per_seq, m] int32, the m largest logits of the
+ *                 row, larger first, ties to the lower index
+ *  logp_out     : [batch, rows_per_seq, m] float, ln P of those candidates
+ *  entropy_out  : [batch, rows_per_seq] float, -sum P ln P
+ *  path_score_out: [batch] float, S = sum_j ln P(x_j^(m_j)) + lambda *
+ *                 sum_j Entropy(P(x_j)) of the best path.  S is a sum of
+ *                 per-position terms and the entropy term does not depend on
+ *                 the choice, so the best path takes every position's first
+ *                 candidate (a tree of candidates is idx_out itself).
+ *  Constraints: 1 <= m <= 8, m <= vocab, 1 <= rows_per_seq <= 16,
+ *               vocab % 8 == 0 and <= 524288, logits 16-byte aligned.
+ * ------------------------------------------------------------------------- */
+DFLASH_API dflash_status dflash_block_conv(const void* h, int batch, int block_size, int d_model, int kernel,
+                                           const void* w, const void* bias, int residual, void* out, void* stream);
+
+DFLASH_API size_t dflash_draft_topm_workspace_size(int batch, int rows_per_seq, int vocab, int m);
+
+DFLASH_API dflash_status dflash_draft_topm(const void* logits, int batch, int rows_per_seq, int vocab, int m,
+                                           float temperature, float lambda, int32_t* idx_out, float* logp_out,
+                                           float* entropy_out, float* path_score_out, void* workspace,
+                                           size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * 5. The rest of a draft layer after its attention (E4B page "The parameter
  *    count exposes the real cost": a Qwen3-style layer, gated MLP of
  *    intermediate size 5120):

@@ -634,7 +634,8 @@ def draft_topm(logits, m, temperature, lam):
     logz = mx[..., 0] + np.log(np.exp(s - mx).sum(axis=-1))
     logp_all = s - logz[..., None]
     p = np.exp(logp_all)
-    ent = -(p * logp_all).sum(axis=-1)
+    plogp = np.where(p > 0, p * np.where(p > 0, logp_all, 0.0), 0.0)   # 0 ln 0 = 0 (tokens of zero probability)
+    ent = -plogp.sum(axis=-1)
     idx = np.zeros((B, R, m), dtype=np.int64)
     for b in range(B):
         for r in range(R):

@@ -28,7 +28,7 @@ def test_header_declares_the_three_calls():
     syms = declared_symbols()
     for s in ("dflash_fuse_context", "dflash_block_attn", "dflash_verify"):
         assert s in syms
-    assert len(syms) == 16
+    assert len(syms) == 19
 
 
 def test_library_exports_every_declared_symbol(L):
@@ -49,7 +49,7 @@ def test_workspace_queries(L):
     assert dfl.block_attn_workspace_size(32, 8, 32, 8, 8256, 0, dfl.BF16) > 0
     assert dfl.block_attn_workspace_size(0, 8, 32, 8, 8256, 0, dfl.BF16) == 0
     assert dfl.fuse_context_workspace_size(256, 5, 2560, 2560, 5, 8, dfl.BF16) >= 256 * 2560 * 2
-    assert dfl.version() == (1 << 16) | 2
+    assert dfl.version() == (1 << 16) | 3
 
 
 def _cache(**kw):

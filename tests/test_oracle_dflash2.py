@@ -104,3 +104,12 @@ def test_best_path_by_enumerating_every_path():
     for b in range(B):
         for r in range(R):
             assert set(idx[b, r]) == set(np.argsort(-l[b, r], kind="stable")[:m])
+
+
+def test_topm_zero_probability_tokens():
+    """-inf logits have probability 0: they add nothing to the entropy (0 ln 0 = 0) and come last."""
+    l = np.zeros((1, 1, 8))
+    l[0, 0, :4] = -np.inf
+    idx, logp, ent, _ = oracle.draft_topm(l, 5, 1.0, 0.0)
+    np.testing.assert_allclose(ent[0, 0], np.log(4), rtol=1e-14)
+    assert list(idx[0, 0]) == [4, 5, 6, 7, 0] and logp[0, 0, 4] == -np.inf
