@@ -271,6 +271,7 @@ def run_gpu(args):
         tensor_lines.update(window_attention_roofline(cyc, dev, peaks()[0]))
         tensor_lines.update(paged_attention_roofline(cyc, dev, peaks()[0]))
         tensor_lines.update(draft_head_roofline(cyc, dev, peaks()[0]))
+        tensor_lines.update(dflash2_roofline(cyc, dev, peaks()[0]))
         tensor_lines.update(layer_tail_roofline(cyc, dev, peaks()[0], peaks()[1]))
 
     if rank != 0:
@@ -409,6 +410,46 @@ def paged_attention_roofline(cyc, dev, peak_gbs, P=128, iters=20):
                                         "frac": gbs / peak_gbs, "ms_per_layer_call": ms,
                                         "note": "the batched cache in %d-row pages of a shared pool, block table = "
                                                 "a random permutation of the pool" % P}}
+
+
+def dflash2_roofline(cyc, dev, peak_gbs, m=8, lam=0.2, iters=20):
+    """The DFlash2 candidate pass on the batched workload's draft logits: B x
+    (bs - 1) rows of V = 262144 bf16, top-8 candidates, entropies and the
+    best-path score per sequence.  Algorithmic bytes: every logit read once,
+    B (bs - 1) V 2.  Beside it, the depthwise block convolution (k = 5) of the
+    B x bs block rows of width D.  CUDA events on the launching stream, 3
+    warm-up calls."""
+    import block_speculative_decoding_gb300 as dfl
+    cfg = cyc.cfg
+    R = cfg.bs - 1
+    g = workloads.generator(cfg.seed * 1000 + 27, dev)
+    logits = (cfg.logit_std * torch.randn(cfg.B, R, cfg.V, generator=g, device=dev)).to(torch.bfloat16)
+    ws = torch.empty(dfl.draft_topm_workspace_size(cfg.B, R, cfg.V, m), dtype=torch.uint8, device=dev)
+    h = torch.randn(cfg.B * cfg.bs, cfg.D, generator=g, device=dev).to(torch.bfloat16)
+    wc = (0.3 * torch.randn(5, cfg.D, generator=g, device=dev)).to(torch.bfloat16)
+    st = torch.cuda.Stream(device=dev)
+
+    def timed(fn):
+        with torch.cuda.stream(st):
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            for _ in range(iters):
+                fn()
+            e1.record(st)
+            torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / iters
+    ms = timed(lambda: dfl.draft_topm(logits, m, cyc.T if cyc.T > 0 else 1.0, lam, workspace=ws, stream=st))
+    conv_ms = timed(lambda: dfl.block_conv(h, wc, None, cfg.bs, residual=True, out=h, stream=st))
+    nbytes = cfg.B * R * cfg.V * 2
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    del logits, ws, h
+    torch.cuda.empty_cache()
+    return {"dflash2_topm": {"bound": "hbm", "achieved": gbs, "peak": peak_gbs, "unit": "GB/s", "frac": gbs / peak_gbs,
+                             "ms_per_call": ms, "rows": cfg.B * R, "vocab": cfg.V, "m": m,
+                             "block_conv_k5_ms_per_call": conv_ms}}
 
 
 def draft_head_roofline(cyc, dev, peak_gbs, iters=10):
@@ -776,6 +817,8 @@ def run_profile(args):
     hbm, tfl, _ = peaks()
     if args.profile == "layer_tail":
         line = layer_tail_roofline(cyc, dev, hbm, tfl)
+    elif args.profile == "dflash2":
+        line = dflash2_roofline(cyc, dev, hbm)
     else:
         line = draft_head_roofline(cyc, dev, hbm)
     print(json.dumps({"profiling_run": True, "profile": args.profile, **line}), flush=True)
@@ -795,7 +838,7 @@ def main():
                     help="profiling runs: time one component of the cycle only")
     ap.add_argument("--batch", type=int, default=None, help="profiling runs: smaller batch")
     ap.add_argument("--layers", type=int, default=None, help="profiling runs: fewer draft layers")
-    ap.add_argument("--profile", default=None, choices=["layer_tail", "draft_head"],
+    ap.add_argument("--profile", default=None, choices=["layer_tail", "draft_head", "dflash2"],
                     help="profiling runs: only this call's roofline measurement on the batched workload")
     args = ap.parse_args()
     if args.profile:

@@ -100,6 +100,7 @@ constexpr int kTopmThreads = 256;
 constexpr int kTopmChunk = 16384;                       // logits per chunk CTA
 constexpr int kTopmVecs = kTopmChunk / (kTopmThreads * 8);  // 8 vectors of 8 bf16 per thread
 constexpr int kMaxM = 8;
+constexpr int kTopmBuf = 128;                            // compacted candidates per warp
 
 // (value, index) order of the candidates: larger logit first, then lower index.
 __device__ __forceinline__ bool better(float v1, int i1, float v2, int i2) {
@@ -122,7 +123,7 @@ __device__ __forceinline__ void warp_best(float& v, int& i) {
 // One CTA per (row, chunk).  stats[row][c] = (max s, sum e^(s - max),
 // sum e^(s - max) (s - max), 0) over the chunk's finite logits, s = l * inv_t;
 // cand[row][c][r] = (logit bits, index) of the chunk's r-th best logit.
-__global__ void __launch_bounds__(kTopmThreads) topm_chunk_kernel(const __nv_bfloat16* __restrict__ logits, int V,
+__global__ void __launch_bounds__(kTopmThreads, 2) topm_chunk_kernel(const __nv_bfloat16* __restrict__ logits, int V,
                                                                  int nchunk, float inv_t, int m,
                                                                  float4* __restrict__ stats, int2* __restrict__ cand) {
   const int row = blockIdx.x / nchunk, c = blockIdx.x % nchunk;
@@ -136,45 +137,126 @@ __global__ void __launch_bounds__(kTopmThreads) topm_chunk_kernel(const __nv_bfl
     raw[i] = e < V ? __ldcs(reinterpret_cast<const uint4*>(lr + e)) : make_uint4(0xFF80FF80u, 0xFF80FF80u,
                                                                                 0xFF80FF80u, 0xFF80FF80u);
   }
-  // this thread's m best, sorted (best first), and its maximum
-  float lv[kMaxM];
-  int li[kMaxM];
-#pragma unroll
-  for (int r = 0; r < kMaxM; ++r) {
-    lv[r] = -INFINITY;
-    li[r] = INT_MAX;
-  }
-  float mx = -INFINITY;
+  // per vector, the largest of its 8 logits (packed bf16 maxima); this lane's
+  // best key (value, lowest index with it) from the first vector holding it
+  float vmax[kTopmVecs];
+  float mv = -INFINITY;
 #pragma unroll
   for (int i = 0; i < kTopmVecs; ++i) {
+    const __nv_bfloat162 a = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&raw[i].x),
+                                     *reinterpret_cast<const __nv_bfloat162*>(&raw[i].y));
+    const __nv_bfloat162 c2 = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&raw[i].z),
+                                      *reinterpret_cast<const __nv_bfloat162*>(&raw[i].w));
+    const __nv_bfloat162 d2 = __hmax2(a, c2);
+    vmax[i] = fmaxf(__low2float(d2), __high2float(d2));
+    mv = fmaxf(mv, vmax[i]);
+  }
+  int mi = INT_MAX;
+#pragma unroll
+  for (int i = 0; i < kTopmVecs; ++i) {
+    if (mi == INT_MAX && vmax[i] == mv) {
+      const uint32_t u[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+      const int e = e0 + (i * kTopmThreads + tid) * 8;
+#pragma unroll
+      for (int j = 7; j >= 0; --j)
+        if (((j & 1) ? bf16_hi(u[j / 2]) : bf16_lo(u[j / 2])) == mv) mi = e + j;
+    }
+  }
+  if (mv == -INFINITY) {  // all of the lane's logits are -inf: its key is its lowest index (none past V)
+    const int first = e0 + tid * 8;
+    mi = first < V ? first : INT_MAX;
+  }
+  const float mx = mv;
+  // the warp's threshold tau: the m-th best of the 32 lane keys.  At least m
+  // of the warp's elements have a key >= tau (in the total order of
+  // better(): larger logit, then lower index), so its m best are among them.
+  float tv = -INFINITY;
+  int ti = INT_MAX;
+  {
+    bool taken = false;
+    for (int r = 0; r < m; ++r) {
+      float bv = taken ? -INFINITY : mv;
+      int bi = taken ? INT_MAX : mi;
+      warp_best(bv, bi);
+      if (!taken && bi == mi) taken = true;
+      tv = bv;
+      ti = bi;
+    }
+  }
+  // the warp's keys >= tau, compacted into shared memory (ballot order); few
+  // pass: an all-equal row passes (m - 1) * 8 + 1 of them
+  __shared__ int2 s_buf[kTopmThreads / 32][kTopmBuf];
+  __shared__ int2 s_wcand[kTopmThreads / 32][kMaxM];
+  int cnt = 0;
+#pragma unroll
+  for (int i = 0; i < kTopmVecs; ++i) {
+    // a vector none of whose logits reaches tau in value is skipped by the warp
+    if (!__any_sync(0xffffffffu, vmax[i] >= tv)) continue;
     const uint32_t u[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const float v = (j & 1) ? bf16_hi(u[j / 2]) : bf16_lo(u[j / 2]);
       const int idx = e0 + (i * kTopmThreads + tid) * 8 + j;
-      mx = fmaxf(mx, v);
-      if (idx < V && better(v, idx, lv[kMaxM - 1], li[kMaxM - 1])) {
-        // insert, keeping the list sorted (the first m entries are used)
-        float cv = v;
-        int ci = idx;
-#pragma unroll
-        for (int r = 0; r < kMaxM; ++r) {
-          if (better(cv, ci, lv[r], li[r])) {
-            const float tv = lv[r];
-            const int ti = li[r];
-            lv[r] = cv;
-            li[r] = ci;
-            cv = tv;
-            ci = ti;
-          }
-        }
+      const bool pass = idx < V && !better(tv, ti, v, idx);
+      const unsigned bal = __ballot_sync(0xffffffffu, pass);
+      if (bal) {
+        const int pos = cnt + __popc(bal & ((1u << lane) - 1u));
+        if (pass && pos < kTopmBuf) s_buf[warp][pos] = make_int2(__float_as_int(v), idx);
+        cnt += __popc(bal);
       }
     }
   }
+  __syncwarp();
+  // the warp's m best: m rounds over the buffer, or (overflow) over the registers
+  if (cnt <= kTopmBuf) {
+    for (int r = 0; r < m; ++r) {
+      float bv = -INFINITY;
+      int bi = INT_MAX, bk = -1;
+      for (int k = lane; k < cnt; k += 32) {
+        const int2 e = s_buf[warp][k];
+        if (better(__int_as_float(e.x), e.y, bv, bi)) {
+          bv = __int_as_float(e.x);
+          bi = e.y;
+          bk = k;
+        }
+      }
+      float wv = bv;
+      int wi = bi;
+      warp_best(wv, wi);
+      if (bk >= 0 && bi == wi) s_buf[warp][bk] = make_int2(__float_as_int(-INFINITY), INT_MAX);
+      if (lane == 0) s_wcand[warp][r] = make_int2(__float_as_int(wv), wi);
+      __syncwarp();
+    }
+  } else {
+    float pv = INFINITY;  // the previous round's winner: this round takes the best key after it
+    int pi = -1;
+    for (int r = 0; r < m; ++r) {
+      float bv = -INFINITY;
+      int bi = INT_MAX;
+      // (rare) re-read the lane's vectors rather than keep them live in registers
+#pragma unroll 1
+      for (int i = 0; i < kTopmVecs; ++i) {
+        const int e = e0 + (i * kTopmThreads + tid) * 8;
+        if (e >= V) continue;
+        const uint4 q = __ldg(reinterpret_cast<const uint4*>(lr + e));
+        const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float v = (j & 1) ? bf16_hi(u[j / 2]) : bf16_lo(u[j / 2]);
+          const int idx = e + j;
+          if (better(pv, pi, v, idx) && better(v, idx, bv, bi)) {
+            bv = v;
+            bi = idx;
+          }
+        }
+      }
+      warp_best(bv, bi);
+      if (lane == 0) s_wcand[warp][r] = make_int2(__float_as_int(bv), bi);
+      pv = bv;
+      pi = bi;
+    }
+  }
   __shared__ float s_red[kTopmThreads / 32][2];
-  __shared__ float s_bv[kTopmThreads / 32];
-  __shared__ int s_bi[kTopmThreads / 32];
-  __shared__ int s_wi;
   // the chunk's maximum of s = l * inv_t (inv_t > 0 keeps the order)
   float wm = warp_max(mx);
   if (lane == 0) s_red[warp][0] = wm;
@@ -215,35 +297,28 @@ __global__ void __launch_bounds__(kTopmThreads) topm_chunk_kernel(const __nv_bfl
     }
     stats[static_cast<size_t>(row) * nchunk + c] = make_float4(Ms, St, Wt, 0.f);
   }
-  // the chunk's m best: m rounds over the threads' list heads
-  int2* cout = cand + (static_cast<size_t>(row) * nchunk + c) * m;
-  for (int r = 0; r < m; ++r) {
-    float bv = lv[0];
-    int bi = li[0];
-    warp_best(bv, bi);
-    if (lane == 0) {
-      s_bv[warp] = bv;
-      s_bi[warp] = bi;
-    }
-    __syncthreads();
-    if (warp == 0) {
-      float v = lane < kTopmThreads / 32 ? s_bv[lane] : -INFINITY;
-      int i = lane < kTopmThreads / 32 ? s_bi[lane] : INT_MAX;
-      warp_best(v, i);
-      if (lane == 0) {
-        s_wi = i;
-        cout[r] = make_int2(__float_as_int(v), i);
+  // the chunk's m best from the warps' m best each (warp 0, m rounds)
+  __syncthreads();
+  if (warp == 0) {
+    int2* cout = cand + (static_cast<size_t>(row) * nchunk + c) * m;
+    constexpr int kW = kTopmThreads / 32;
+    for (int r = 0; r < m; ++r) {
+      float bv = -INFINITY;
+      int bi = INT_MAX, bk = -1;
+      for (int k = lane; k < kW * m; k += 32) {
+        const int2 e = s_wcand[k / m][k % m];
+        if (better(__int_as_float(e.x), e.y, bv, bi)) {
+          bv = __int_as_float(e.x);
+          bi = e.y;
+          bk = k;
+        }
       }
-    }
-    __syncthreads();
-    if (li[0] == s_wi && s_wi != INT_MAX) {  // this thread's head won: pop it
-#pragma unroll
-      for (int q = 0; q < kMaxM - 1; ++q) {
-        lv[q] = lv[q + 1];
-        li[q] = li[q + 1];
-      }
-      lv[kMaxM - 1] = -INFINITY;
-      li[kMaxM - 1] = INT_MAX;
+      float wv = bv;
+      int wi = bi;
+      warp_best(wv, wi);
+      if (bk >= 0 && bi == wi) s_wcand[bk / m][bk % m] = make_int2(__float_as_int(-INFINITY), INT_MAX);
+      if (lane == 0) cout[r] = make_int2(__float_as_int(wv), wi);
+      __syncwarp();
     }
   }
 }

@@ -98,3 +98,18 @@ def test_draft_topm_batched_shape_sampled():
     g = torch.Generator(device=DEV).manual_seed(21)
     logits = (3.0 * torch.randn(32, 7, 262144, generator=g, device=DEV)).to(torch.bfloat16)
     _check_topm(logits, 8, 1.0, 0.2, rows=torch.tensor([3, 30], device=DEV))
+
+
+def test_draft_topm_rows_with_fewer_finite_logits_than_m():
+    """Fewer than m finite logits: the -inf logits follow them, lowest index first."""
+    V, m = 16384 + 8, 8
+    logits = torch.full((1, 2, V), float("-inf"), dtype=torch.bfloat16, device=DEV)
+    logits[0, 0, 100] = 1.0
+    logits[0, 0, 7000] = 2.0
+    logits[0, 0, 16390] = 2.0
+    idx, logp, ent, score = dfl.draft_topm(logits, m, 1.0, 0.0)
+    torch.cuda.synchronize()
+    ri, rl, re, rs = oracle.draft_topm(np64(logits), m, 1.0, 0.0)
+    np.testing.assert_array_equal(idx[0, 0].cpu().numpy(), ri[0, 0])
+    np.testing.assert_allclose(logp[0, 0, :3].cpu().numpy(), rl[0, 0, :3], rtol=1e-5)
+    assert torch.all(torch.isinf(logp[0, 0, 3:]))
