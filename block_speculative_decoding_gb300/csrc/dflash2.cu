@@ -12,7 +12,7 @@
 //   block_conv_kernel  one thread per (sequence, 4 channels): the block's rows
 //                      of those channels in registers, the causal depthwise
 //                      sum, bf16 out (in place allowed).
-//   topm_chunk_kernel  one CTA per (row, 16384-logit chunk): the chunk's
+//   topm_chunk_kernel  one CTA per (row, 32768-logit chunk): the chunk's
 //                      (max, sum e^(s-max), sum e^(s-max) (s-max)) of s = l / T
 //                      and its m best logits (ties to the lower index).
 //   topm_merge_kernel  one CTA per sequence, one warp per row: the row's
@@ -97,8 +97,8 @@ __global__ void __launch_bounds__(256) block_conv_kernel(const __nv_bfloat16* h,
 }
 
 constexpr int kTopmThreads = 256;
-constexpr int kTopmChunk = 16384;                       // logits per chunk CTA
-constexpr int kTopmVecs = kTopmChunk / (kTopmThreads * 8);  // 8 vectors of 8 bf16 per thread
+constexpr int kTopmChunk = 32768;                       // logits per chunk CTA
+constexpr int kTopmVecs = kTopmChunk / (kTopmThreads * 8);  // 16 vectors of 8 bf16 per thread
 constexpr int kMaxM = 8;
 constexpr int kTopmBuf = 128;                            // compacted candidates per warp
 
@@ -116,6 +116,27 @@ __device__ __forceinline__ void warp_best(float& v, int& i) {
     if (better(ov, oi, v, i)) {
       v = ov;
       i = oi;
+    }
+  }
+}
+
+// Bitonic sort of the warp's 32 keys, best first (lane 0 ends with the best):
+// in every compare-exchange the lower lane of a best-first run keeps the
+// better key, of a worst-first run the worse one.
+__device__ __forceinline__ void warp_sort_best_first(float& v, int& i, int lane) {
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, v, j);
+      const int oi = __shfl_xor_sync(0xffffffffu, i, j);
+      const bool best_first = (lane & k) == 0 || k == 32;
+      const bool lower = (lane & j) == 0;
+      const bool take = (lower == best_first) ? better(ov, oi, v, i) : better(v, i, ov, oi);
+      if (take) {
+        v = ov;
+        i = oi;
+      }
     }
   }
 }
@@ -170,45 +191,49 @@ __global__ void __launch_bounds__(kTopmThreads, 2) topm_chunk_kernel(const __nv_
   // the warp's threshold tau: the m-th best of the 32 lane keys.  At least m
   // of the warp's elements have a key >= tau (in the total order of
   // better(): larger logit, then lower index), so its m best are among them.
-  float tv = -INFINITY;
-  int ti = INT_MAX;
-  {
-    bool taken = false;
-    for (int r = 0; r < m; ++r) {
-      float bv = taken ? -INFINITY : mv;
-      int bi = taken ? INT_MAX : mi;
-      warp_best(bv, bi);
-      if (!taken && bi == mi) taken = true;
-      tv = bv;
-      ti = bi;
-    }
-  }
-  // the warp's keys >= tau, compacted into shared memory (ballot order); few
-  // pass: an all-equal row passes (m - 1) * 8 + 1 of them
+  float tv = mv;
+  int ti = mi;
+  warp_sort_best_first(tv, ti, lane);
+  tv = __shfl_sync(0xffffffffu, tv, m - 1);
+  ti = __shfl_sync(0xffffffffu, ti, m - 1);
+  // the warp's keys >= tau, appended to shared memory by the lanes holding
+  // them (only vectors whose maximum reaches tau are looked into); few pass:
+  // an all-equal row passes (m - 1) * 8 + 1 of them
   __shared__ int2 s_buf[kTopmThreads / 32][kTopmBuf];
   __shared__ int2 s_wcand[kTopmThreads / 32][kMaxM];
-  int cnt = 0;
+  __shared__ int s_cnt[kTopmThreads / 32];
+  if (lane == 0) s_cnt[warp] = 0;
+  __syncwarp();
 #pragma unroll
   for (int i = 0; i < kTopmVecs; ++i) {
-    // a vector none of whose logits reaches tau in value is skipped by the warp
-    if (!__any_sync(0xffffffffu, vmax[i] >= tv)) continue;
-    const uint32_t u[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+    if (vmax[i] >= tv) {
+      const uint32_t u[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float v = (j & 1) ? bf16_hi(u[j / 2]) : bf16_lo(u[j / 2]);
-      const int idx = e0 + (i * kTopmThreads + tid) * 8 + j;
-      const bool pass = idx < V && !better(tv, ti, v, idx);
-      const unsigned bal = __ballot_sync(0xffffffffu, pass);
-      if (bal) {
-        const int pos = cnt + __popc(bal & ((1u << lane) - 1u));
-        if (pass && pos < kTopmBuf) s_buf[warp][pos] = make_int2(__float_as_int(v), idx);
-        cnt += __popc(bal);
+      for (int j = 0; j < 8; ++j) {
+        const float v = (j & 1) ? bf16_hi(u[j / 2]) : bf16_lo(u[j / 2]);
+        const int idx = e0 + (i * kTopmThreads + tid) * 8 + j;
+        if (idx < V && !better(tv, ti, v, idx)) {
+          const int pos = atomicAdd(&s_cnt[warp], 1);
+          if (pos < kTopmBuf) s_buf[warp][pos] = make_int2(__float_as_int(v), idx);
+        }
       }
     }
   }
   __syncwarp();
-  // the warp's m best: m rounds over the buffer, or (overflow) over the registers
-  if (cnt <= kTopmBuf) {
+  const int cnt = s_cnt[warp];
+  // the warp's m best: one sort when they fit a warp, else m rounds over the
+  // buffer, else (overflow) over the registers
+  if (cnt <= 32) {
+    float bv = -INFINITY;
+    int bi = INT_MAX;
+    if (lane < cnt) {
+      const int2 e = s_buf[warp][lane];
+      bv = __int_as_float(e.x);
+      bi = e.y;
+    }
+    warp_sort_best_first(bv, bi, lane);
+    if (lane < m) s_wcand[warp][lane] = make_int2(__float_as_int(bv), bi);
+  } else if (cnt <= kTopmBuf) {
     for (int r = 0; r < m; ++r) {
       float bv = -INFINITY;
       int bi = INT_MAX, bk = -1;
@@ -297,29 +322,38 @@ __global__ void __launch_bounds__(kTopmThreads, 2) topm_chunk_kernel(const __nv_
     }
     stats[static_cast<size_t>(row) * nchunk + c] = make_float4(Ms, St, Wt, 0.f);
   }
-  // the chunk's m best from the warps' m best each (warp 0, m rounds)
+  // the chunk's m best from the warps' m best each: warp 0 sorts warps 0-3's
+  // and warps 4-7's candidates (32 each), and a bitonic merge of the first
+  // list with the reversed second keeps the 32 best in order
   __syncthreads();
   if (warp == 0) {
-    int2* cout = cand + (static_cast<size_t>(row) * nchunk + c) * m;
     constexpr int kW = kTopmThreads / 32;
-    for (int r = 0; r < m; ++r) {
-      float bv = -INFINITY;
-      int bi = INT_MAX, bk = -1;
-      for (int k = lane; k < kW * m; k += 32) {
-        const int2 e = s_wcand[k / m][k % m];
-        if (better(__int_as_float(e.x), e.y, bv, bi)) {
-          bv = __int_as_float(e.x);
-          bi = e.y;
-          bk = k;
-        }
-      }
-      float wv = bv;
-      int wi = bi;
-      warp_best(wv, wi);
-      if (bk >= 0 && bi == wi) s_wcand[bk / m][bk % m] = make_int2(__float_as_int(-INFINITY), INT_MAX);
-      if (lane == 0) cout[r] = make_int2(__float_as_int(wv), wi);
-      __syncwarp();
+    static_assert(kW == 8 && kMaxM == 8, "two lists of four warps' eight candidates");
+    const int w_a = lane / kMaxM, r_a = lane % kMaxM;
+    int2 ea = r_a < m ? s_wcand[w_a][r_a] : make_int2(__float_as_int(-INFINITY), INT_MAX);
+    int2 eb = r_a < m ? s_wcand[w_a + 4][r_a] : make_int2(__float_as_int(-INFINITY), INT_MAX);
+    float av = __int_as_float(ea.x), bvv = __int_as_float(eb.x);
+    int ai = ea.y, bii = eb.y;
+    warp_sort_best_first(av, ai, lane);
+    warp_sort_best_first(bvv, bii, lane);
+    // lane l pairs a[l] with b[31 - l]: the better of each pair forms a bitonic sequence of the 32 best
+    const float rv = __shfl_sync(0xffffffffu, bvv, 31 - lane);
+    const int ri = __shfl_sync(0xffffffffu, bii, 31 - lane);
+    if (better(rv, ri, av, ai)) {
+      av = rv;
+      ai = ri;
     }
+#pragma unroll
+    for (int j = 16; j > 0; j >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, av, j);
+      const int oi = __shfl_xor_sync(0xffffffffu, ai, j);
+      const bool lower = (lane & j) == 0;
+      if (lower ? better(ov, oi, av, ai) : better(av, ai, ov, oi)) {
+        av = ov;
+        ai = oi;
+      }
+    }
+    if (lane < m) cand[(static_cast<size_t>(row) * nchunk + c) * m + lane] = make_int2(__float_as_int(av), ai);
   }
 }
 
