@@ -100,6 +100,20 @@ def test_host_validation_rejects_bad_arguments_before_any_launch(L):
         b = _cache(**bad)
         assert lib.dflash_block_attn(0, 2, 8, 32, P(16), P(16), P(16), None, None, 1e6, 1e-6, ctypes.byref(b), 0, P(16), P(256), 1 << 30, None) == code, bad
     assert lib.dflash_block_attn(0, 2, 8, 32, P(16), P(16), P(16), None, None, 1e6, 1e-6, ctypes.byref(ok), 64, P(16), P(256), 1 << 30, None) == 2
+    # DFlash2: block convolution sizes and flags; top-m m, temperature, vocabulary and workspace
+    assert lib.dflash_block_conv(P(16), 2, 17, 256, 3, P(16), None, 0, P(16), None) == 1
+    assert lib.dflash_block_conv(P(16), 2, 8, 256, 9, P(16), None, 0, P(16), None) == 1
+    assert lib.dflash_block_conv(P(16), 2, 8, 256, 3, P(16), None, 2, P(16), None) == 1
+    assert lib.dflash_block_conv(P(16), 2, 8, 258, 3, P(16), None, 0, P(16), None) == 2
+    assert lib.dflash_block_conv(P(16), 2, 8, 256, 3, P(12), None, 0, P(16), None) == 1
+    assert lib.dflash_block_conv(None, 0, 8, 256, 3, None, None, 0, None, None) == 0
+    assert lib.dflash_draft_topm(P(16), 2, 7, 4096, 9, 1.0, 0.1, P(16), P(16), P(16), P(16), P(256), 1 << 20, None) == 2
+    assert lib.dflash_draft_topm(P(16), 2, 7, 4096, 8, 0.0, 0.1, P(16), P(16), P(16), P(16), P(256), 1 << 20, None) == 1
+    assert lib.dflash_draft_topm(P(16), 2, 7, 4100, 8, 1.0, 0.1, P(16), P(16), P(16), P(16), P(256), 1 << 20, None) == 2
+    assert lib.dflash_draft_topm(P(16), 2, 17, 4096, 8, 1.0, 0.1, P(16), P(16), P(16), P(16), P(256), 1 << 20, None) == 1
+    assert lib.dflash_draft_topm(P(16), 2, 7, 4096, 8, 1.0, 0.1, P(16), P(16), P(16), P(16), P(256), 8, None) == 5
+    assert lib.dflash_draft_topm(P(8), 2, 7, 4096, 8, 1.0, 0.1, P(16), P(16), P(16), P(16), P(256), 1 << 20, None) == 1
+    assert lib.dflash_draft_topm_workspace_size(2, 7, 4096, 8) > 0
     # fusion: tap count, widths, capacity visible on the host
     taps = (ctypes.c_void_p * 5)(16, 16, 16, 16, 16)
     assert lib.dflash_fuse_context(0, taps, 2560, P(16), 2, 8, P(16), None, 2560, P(16), None, 1e6, 1e-6, ctypes.byref(c), None, P(256), 1 << 30, None) == 2
