@@ -101,6 +101,7 @@ constexpr int kTopmChunk = 32768;                       // logits per chunk CTA
 constexpr int kTopmVecs = kTopmChunk / (kTopmThreads * 8);  // 16 vectors of 8 bf16 per thread
 constexpr int kMaxM = 8;
 constexpr int kTopmBuf = 128;                            // compacted candidates per warp
+constexpr int kTopmVecCap = 32;                          // staged 8-logit vectors per warp
 
 // (value, index) order of the candidates: larger logit first, then lower index.
 __device__ __forceinline__ bool better(float v1, int i1, float v2, int i2) {
@@ -202,19 +203,55 @@ __global__ void __launch_bounds__(kTopmThreads, 2) topm_chunk_kernel(const __nv_
   __shared__ int2 s_buf[kTopmThreads / 32][kTopmBuf];
   __shared__ int2 s_wcand[kTopmThreads / 32][kMaxM];
   __shared__ int s_cnt[kTopmThreads / 32];
-  if (lane == 0) s_cnt[warp] = 0;
+  __shared__ uint4 s_vec[kTopmThreads / 32][kTopmVecCap];
+  __shared__ int s_vbase[kTopmThreads / 32][kTopmVecCap];
+  __shared__ int s_vcnt[kTopmThreads / 32];
+  if (lane == 0) {
+    s_cnt[warp] = 0;
+    s_vcnt[warp] = 0;
+  }
   __syncwarp();
+  // stage the vectors whose maximum reaches tau (few), then test them with
+  // eight lanes per vector, four vectors per step
 #pragma unroll
   for (int i = 0; i < kTopmVecs; ++i) {
     if (vmax[i] >= tv) {
-      const uint32_t u[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float v = (j & 1) ? bf16_hi(u[j / 2]) : bf16_lo(u[j / 2]);
-        const int idx = e0 + (i * kTopmThreads + tid) * 8 + j;
+      const int k = atomicAdd(&s_vcnt[warp], 1);
+      if (k < kTopmVecCap) {
+        s_vec[warp][k] = raw[i];
+        s_vbase[warp][k] = e0 + (i * kTopmThreads + tid) * 8;
+      }
+    }
+  }
+  __syncwarp();
+  const int nvec = s_vcnt[warp];
+  if (nvec <= kTopmVecCap) {
+    for (int k0 = 0; k0 < nvec; k0 += 4) {
+      const int k = k0 + lane / 8, j = lane % 8;
+      if (k < nvec) {
+        const uint4 q = s_vec[warp][k];
+        const uint32_t w2 = j < 2 ? q.x : j < 4 ? q.y : j < 6 ? q.z : q.w;
+        const float v = (j & 1) ? bf16_hi(w2) : bf16_lo(w2);
+        const int idx = s_vbase[warp][k] + j;
         if (idx < V && !better(tv, ti, v, idx)) {
           const int pos = atomicAdd(&s_cnt[warp], 1);
           if (pos < kTopmBuf) s_buf[warp][pos] = make_int2(__float_as_int(v), idx);
+        }
+      }
+    }
+  } else {  // many vectors reach tau: every lane tests its own
+#pragma unroll
+    for (int i = 0; i < kTopmVecs; ++i) {
+      if (vmax[i] >= tv) {
+        const uint32_t u[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float v = (j & 1) ? bf16_hi(u[j / 2]) : bf16_lo(u[j / 2]);
+          const int idx = e0 + (i * kTopmThreads + tid) * 8 + j;
+          if (idx < V && !better(tv, ti, v, idx)) {
+            const int pos = atomicAdd(&s_cnt[warp], 1);
+            if (pos < kTopmBuf) s_buf[warp][pos] = make_int2(__float_as_int(v), idx);
+          }
         }
       }
     }
@@ -292,19 +329,23 @@ __global__ void __launch_bounds__(kTopmThreads, 2) topm_chunk_kernel(const __nv_
   const float Ms = M * inv_t;
   float S = 0.f, W = 0.f;
   if (M != -INFINITY) {
+    // in base 2 and without branches: d2 = (s - max) log2(e), clamped so that a
+    // -inf logit (zero probability, also the padding past V) adds e = 0 and
+    // e * d2 = 0; W is converted back to natural units below
+    const float k2 = inv_t * 1.4426950408889634f, m2 = Ms * 1.4426950408889634f;
 #pragma unroll
     for (int i = 0; i < kTopmVecs; ++i) {
       const uint32_t u[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const float v = (j & 1) ? bf16_hi(u[j / 2]) : bf16_lo(u[j / 2]);
-        if (v == -INFINITY) continue;  // zero probability (also the padding past V)
-        const float d = v * inv_t - Ms;
-        const float e = __expf(d);
+        const float d2 = fmaxf(fmaf(v, k2, -m2), -1.0e30f);
+        const float e = ex2_approx(d2);
         S += e;
-        W = fmaf(e, d, W);
+        W = fmaf(e, d2, W);
       }
     }
+    W *= 0.6931471805599453f;
   }
   S = warp_sum(S);
   W = warp_sum(W);
