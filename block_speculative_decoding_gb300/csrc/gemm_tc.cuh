@@ -1,11 +1,12 @@
-// The warp-specialised tcgen05 GEMM shared by the fusion and the drafter's
-// head: a TMA producer warp, one MMA-issuing thread, four epilogue warps;
+// The warp-specialised tcgen05 GEMM shared by the fusion, the drafter's
+// head and the draft-layer remainder: a TMA producer warp, one MMA-issuing
+// thread, four epilogue warps;
 // operands staged by TMA in a shared-memory ring (128-byte swizzle, K-major),
 // accumulators in tensor memory (double-buffered when they fit), plain or
 // stream-K schedules (the partial sums of a tile either left in slots for the
 // next kernel or added in by the share that holds the tile's first K block),
-// and four epilogues (fp32 sums, the K/V cache rows of the fusion, the
-// drafter's logits with the draft race, SwiGLU).
+// and three epilogues (fp32 sums, the K/V cache rows of the fusion, the
+// drafter's logits with the draft race).
 #pragma once
 
 #include <cuda.h>
@@ -50,11 +51,9 @@ struct GemmArgs {
   float4* fix_part;        // fixup: [shares][MT * BN * 32] float4, the partial sum of a share's first piece
                            // in the accumulator's own order (column chunk, 4-column group, row)
   int* fix_flag;           // fixup: [shares], zero at launch; 4 once the share's partial sum is stored
-  int epi;                 // 0: fp32 partial store, 1: K/V cache epilogue, 2: drafter logits + draft race,
-                           // 3: SwiGLU (columns 64t.. of a 128-column unit gate, the next 64 up)
+  int epi;                 // 0: fp32 partial store, 1: K/V cache epilogue, 2: drafter logits + draft race
   int a4d_bs;              // > 0: A is an attention output [B][Hq][a4d_bs][128] read through a 4D map
                            // (row b * bs + j, K index h * 128 + e); 0: A is a row-major 2D tensor
-  __nv_bfloat16* act;      // epi 3: [M][N / 2] bf16
   int pdl;                 // launched as a programmatic dependent (waits for the preceding grid before any load)
   int prefetch_b;          // the B operand (weights) may be loaded before that wait
   float* out_f32;          // epi 0: [k_splits][M][N]
@@ -300,39 +299,6 @@ __device__ __forceinline__ void head_epilogue(uint32_t taddr, int col0, int row,
     }
   }
   if (live) p.race[static_cast<size_t>(row) * p.n_tiles + n_tile] = make_float2(best, __int_as_float(best_col));
-}
-
-// SwiGLU of this thread's row over one 128-column group from column col0 (a
-// multiple of 128): the first 64 columns are gate values and the next 64 the
-// up values of the same 64 outputs (the weight rows are interleaved that way);
-// out = silu(gate) * up, bf16, to act[row][col0 / 2 ..].
-__device__ __forceinline__ void swiglu_group(const AccSrc& src, int col0, int row, const GemmArgs& p) {
-  // every lane takes part in the tensor-memory loads (warp-collective); only
-  // the rows of the problem store
-  const bool live = row < p.M;
-  const int I = p.N / 2;
-  __nv_bfloat16* dst = p.act + static_cast<size_t>(live ? row : 0) * I + col0 / 2;
-#pragma unroll 1
-  for (int c = 0; c < 2; ++c) {
-    uint32_t g[32], u[32];
-    acc_ld32x2(src, c * 32, g, 64 + c * 32, u);
-    uint32_t o[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      // silu(g) = g / (1 + e^-g) with the approximate divide (relative error
-      // a few units in the last place, far below the bf16 rounding); it gives
-      // 0 once e^-g exceeds 2^126, the limit of silu there
-      const float g0 = __uint_as_float(g[2 * j]), g1 = __uint_as_float(g[2 * j + 1]);
-      const float a0 = __fdividef(g0, 1.0f + __expf(-g0)) * __uint_as_float(u[2 * j]);
-      const float a1 = __fdividef(g1, 1.0f + __expf(-g1)) * __uint_as_float(u[2 * j + 1]);
-      o[j] = pack_bf16x2(a0, a1);
-    }
-    if (live) {
-      uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) d4[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
-    }
-  }
 }
 
 // fp32 sums of one 128-column group from column col0 into out_f32 slot ks,
@@ -689,10 +655,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
             const int col0 = n * BN + grp * 128;
             if (p.epi == 0)
               f32_group(src, stg, ks, row - lane, col0, lane, p);
-            else if (p.epi == 1)
-              kv_head_epilogue(src, 0, col0, row, kgain, p);
             else
-              swiglu_group(src, col0, row, p);
+              kv_head_epilogue(src, 0, col0, row, kgain, p);
           }
         }
       }
