@@ -12,7 +12,7 @@
 //   block_conv_kernel  one thread per (sequence, 4 channels): the block's rows
 //                      of those channels in registers, the causal depthwise
 //                      sum, bf16 out (in place allowed).
-//   topm_chunk_kernel  one CTA per (row, 32768-logit chunk): the chunk's
+//   topm_chunk_kernel  one CTA per (row, 16384-logit chunk; four per SM): the chunk's
 //                      (max, sum e^(s-max), sum e^(s-max) (s-max)) of s = l / T
 //                      and its m best logits (ties to the lower index).
 //   topm_merge_kernel  one CTA per sequence, one warp per row: the row's
@@ -97,8 +97,8 @@ __global__ void __launch_bounds__(256) block_conv_kernel(const __nv_bfloat16* h,
 }
 
 constexpr int kTopmThreads = 256;
-constexpr int kTopmChunk = 32768;                       // logits per chunk CTA
-constexpr int kTopmVecs = kTopmChunk / (kTopmThreads * 8);  // 16 vectors of 8 bf16 per thread
+constexpr int kTopmChunk = 16384;                       // logits per chunk CTA
+constexpr int kTopmVecs = kTopmChunk / (kTopmThreads * 8);  // 8 vectors of 8 bf16 per thread
 constexpr int kMaxM = 8;
 constexpr int kTopmBuf = 128;                            // compacted candidates per warp
 constexpr int kTopmVecCap = 32;                          // staged 8-logit vectors per warp
@@ -145,7 +145,7 @@ __device__ __forceinline__ void warp_sort_best_first(float& v, int& i, int lane)
 // One CTA per (row, chunk).  stats[row][c] = (max s, sum e^(s - max),
 // sum e^(s - max) (s - max), 0) over the chunk's finite logits, s = l * inv_t;
 // cand[row][c][r] = (logit bits, index) of the chunk's r-th best logit.
-__global__ void __launch_bounds__(kTopmThreads, 2) topm_chunk_kernel(const __nv_bfloat16* __restrict__ logits, int V,
+__global__ void __launch_bounds__(kTopmThreads, 4) topm_chunk_kernel(const __nv_bfloat16* __restrict__ logits, int V,
                                                                  int nchunk, float inv_t, int m,
                                                                  float4* __restrict__ stats, int2* __restrict__ cand) {
   const int row = blockIdx.x / nchunk, c = blockIdx.x % nchunk;
