@@ -468,7 +468,7 @@ __global__ void __launch_bounds__(512) topm_merge_kernel(const float4* __restric
           cv[q] = -INFINITY;
           ci[q] = INT_MAX;
         }
-      const float lp = bi == INT_MAX ? -INFINITY : bv * inv_t - logz;
+      const float lp = (bi == INT_MAX || logz == -INFINITY) ? -INFINITY : bv * inv_t - logz;  // -inf row: no mass
       if (r == 0) first = lp;
       if (lane == 0) {
         idx_out[static_cast<size_t>(row) * m + r] = bi == INT_MAX ? -1 : bi;

@@ -631,8 +631,11 @@ def draft_topm(logits, m, temperature, lam):
     B, R, V = l.shape
     s = l / temperature
     mx = s.max(axis=-1, keepdims=True)
-    logz = mx[..., 0] + np.log(np.exp(s - mx).sum(axis=-1))
-    logp_all = s - logz[..., None]
+    empty = ~np.isfinite(mx[..., 0])     # a row of -inf logits carries no probability mass
+    mxs = np.where(np.isfinite(mx), mx, 0.0)
+    with np.errstate(divide="ignore"):   # ln 0 of an empty row is replaced just below
+        logz = np.where(empty, -np.inf, mxs[..., 0] + np.log(np.exp(s - mxs).sum(axis=-1)))
+    logp_all = np.where(empty[..., None], -np.inf, s - np.where(empty, 0.0, logz)[..., None])
     p = np.exp(logp_all)
     plogp = np.where(p > 0, p * np.where(p > 0, logp_all, 0.0), 0.0)   # 0 ln 0 = 0 (tokens of zero probability)
     ent = -plogp.sum(axis=-1)

@@ -113,3 +113,6 @@ def test_draft_topm_rows_with_fewer_finite_logits_than_m():
     np.testing.assert_array_equal(idx[0, 0].cpu().numpy(), ri[0, 0])
     np.testing.assert_allclose(logp[0, 0, :3].cpu().numpy(), rl[0, 0, :3], rtol=1e-5)
     assert torch.all(torch.isinf(logp[0, 0, 3:]))
+    # the all -inf row: indices in order, ln P = -inf, entropy 0 (as the oracle)
+    np.testing.assert_array_equal(idx[0, 1].cpu().numpy(), ri[0, 1])
+    assert torch.all(torch.isneginf(logp[0, 1])) and ent[0, 1].item() == 0.0

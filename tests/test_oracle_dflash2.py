@@ -113,3 +113,12 @@ def test_topm_zero_probability_tokens():
     idx, logp, ent, _ = oracle.draft_topm(l, 5, 1.0, 0.0)
     np.testing.assert_allclose(ent[0, 0], np.log(4), rtol=1e-14)
     assert list(idx[0, 0]) == [4, 5, 6, 7, 0] and logp[0, 0, 4] == -np.inf
+
+
+def test_topm_row_of_only_minus_inf():
+    """A row without probability mass: ln P = -inf for its candidates, entropy 0, no NaN."""
+    l = np.full((1, 2, 6), -np.inf)
+    l[0, 0, 2] = 1.0
+    idx, logp, ent, best = oracle.draft_topm(l, 3, 1.0, 0.5)
+    assert list(idx[0, 1]) == [0, 1, 2] and np.all(logp[0, 1] == -np.inf) and ent[0, 1] == 0.0
+    assert logp[0, 0, 0] == 0.0 and not np.isnan(best).any()
