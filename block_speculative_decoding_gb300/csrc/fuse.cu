@@ -8,7 +8,7 @@
 // multiplication); "DFlash & DFlash2: Block-Diffusion LLM-Speedup" 4.1
 // (H_t = RMSNorm(W_c [H^(l1); ...; H^(l5)]), K_i = W_i^K H_t, V_i = W_i^V H_t).
 //
-// bf16 path, three launches chained as programmatic dependents:
+// bf16 path, launches chained as programmatic dependents:
 //   1. gemm_tc (fusion)  Y = [taps] W_c^T on tcgen05 tensor cores: a unit is
 //      MT x 128 rows by 128 columns of Y over a range of K blocks; TMA loads
 //      128x64 A tiles (taken from the tap that owns the K block -- the concat is
@@ -20,10 +20,14 @@
 //   2. rownorm           row -> (sequence, cache position) and its RoPE table
 //      (before waiting for the GEMM), then H_t = bf16(sum_splits(Y) *
 //      rsqrt(mean(Y^2) + eps) * g)
-//   3. gemm_tc (K/V)     [K|V] = H_t W_kv^T, one head (128 columns) per unit, with
-//      a fused epilogue: a K head is RMS-normalised (gain k_gain[l]) and rotated
-//      at its cache position, a V head copied, both stored as bf16 cache rows.
-//      Its producer loads the first W_kv tiles before waiting for H_t.
+//   3. gemm_tc (K/V)     [K|V] = H_t W_kv^T; its producer loads the first W_kv
+//      tiles before waiting for H_t.  Few rows (M <= 256): 256 x 128 units (one
+//      head), stream-K over all SMs into fp32 slots, and
+//   4. kv_epilogue       one warp per (row, head): the slot sum; a K head is
+//      RMS-normalised (gain k_gain[l]) and rotated at its cache position, a V
+//      head copied, both stored as bf16 cache rows.
+//      More rows: 128 x 256 units (two heads) with that epilogue fused into the
+//      GEMM (stream-K with the in-kernel fixup for tiles past whole waves).
 // fp32 path: the same steps as plain SIMT kernels (parity path).
 #include <cuda.h>
 #include <cuda_bf16.h>
