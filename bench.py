@@ -302,6 +302,13 @@ def run_gpu(args):
                                     "events stop each call's first kernel from launching early, so these are "
                                     "slightly longer than the calls take in the timed steps)"},
         "rooflines": {
+            "attention_plus_verify": {
+                "bound": "hbm", "peak": hbm, "unit": "GB/s",
+                "achieved": (cfg.L * cyc.attn_bytes_per_call + cyc.verify_bytes) / ((cfg.L * attn_ms + ver_ms) * 1e-3) / 1e9,
+                "frac": (cfg.L * cyc.attn_bytes_per_call + cyc.verify_bytes) / ((cfg.L * attn_ms + ver_ms) * 1e-3) / 1e9
+                        / hbm,
+                "note": "the cycle's five block-attention calls and its verification together: their algorithmic "
+                        "bytes over their summed component times"},
             "verify": {"bound": "hbm", "achieved": cyc.verify_bytes / (ver_ms * 1e-3) / 1e9, "peak": hbm,
                        "unit": "GB/s", "frac": cyc.verify_bytes / (ver_ms * 1e-3) / 1e9 / hbm},
             "fuse_context": {"bound": "hbm (M=%d: weight-bound)" % cyc.M,
