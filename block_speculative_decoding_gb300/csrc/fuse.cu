@@ -72,13 +72,25 @@ __global__ void __launch_bounds__(kNormMaxThreads) fuse_rownorm_kernel(
     void* __restrict__ rope_cs, int* __restrict__ zero_flags, int n_zero, const int32_t* __restrict__ table,
     int max_pages, int page_size, int num_pages, unsigned* status) {
   const int m = blockIdx.x;
-  if (threadIdx.x <= HD / 2) {
-    int lo = 0, hi = B - 1;
-    while (lo < hi) {  // largest b with cu_new[b] <= m
-      const int mid = (lo + hi + 1) >> 1;
-      if (cu_new[mid] <= m) lo = mid; else hi = mid - 1;
+  // the row's sequence: the largest b with cu_new[b] <= m (cu_new is
+  // non-decreasing), found by warp 0 with 32 probes per step, so a 2048-row
+  // batch takes two dependent loads, not eleven; the invariant cu_new[lo] <= m
+  // keeps lane 0's probe true
+  __shared__ int s_b;
+  if (threadIdx.x < 32) {
+    int lo = 0, hi = B;
+    while (hi - lo > 1) {
+      const int step = (hi - lo + 31) / 32;
+      const int idx = lo + static_cast<int>(threadIdx.x) * step;
+      const unsigned bal = __ballot_sync(0xffffffffu, idx < hi && cu_new[idx] <= m);
+      lo += (31 - __clz(bal)) * step;
+      hi = min(hi, lo + step);
     }
-    const int b = lo;
+    if (threadIdx.x == 0) s_b = lo;
+  }
+  __syncthreads();
+  if (threadIdx.x <= HD / 2) {
+    const int b = s_b;
     const int t = m - cu_new[b];
     const int nnew = cu_new[b + 1] - cu_new[b];
     const int n = seq_len[b];
