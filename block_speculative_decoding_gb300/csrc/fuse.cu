@@ -73,9 +73,9 @@ __global__ void __launch_bounds__(kNormMaxThreads) fuse_rownorm_kernel(
     int max_pages, int page_size, int num_pages, unsigned* status) {
   const int m = blockIdx.x;
   // the row's sequence: the largest b with cu_new[b] <= m (cu_new is
-  // non-decreasing), found by warp 0 with 32 probes per step, so a 2048-row
-  // batch takes two dependent loads, not eleven; the invariant cu_new[lo] <= m
-  // keeps lane 0's probe true
+  // non-decreasing), found by warp 0 with 32 probes per step, so 128
+  // sequences take two dependent loads, not seven; the invariant
+  // cu_new[lo] <= m keeps lane 0's probe true
   __shared__ int s_b;
   if (threadIdx.x < 32) {
     int lo = 0, hi = B;
