@@ -55,7 +55,7 @@ typedef int dflash_status;
 enum {
   DFLASH_OK = 0,
   DFLASH_ERR_INVALID_ARGUMENT = 1, /* null pointer, negative size, bad alignment  */
-  DFLASH_ERR_UNSUPPORTED = 2,      /* a shape or dtype this build does not handle */
+  DFLASH_ERR_UNSUPPORTED = 2,      /* a shape or dtype the library does not handle */
   DFLASH_ERR_CAPACITY = 3,         /* host-visible size exceeds the cache capacity */
   DFLASH_ERR_CUDA = 4,             /* a CUDA call failed: dflash_last_error_string */
   DFLASH_ERR_WORKSPACE = 5         /* workspace NULL, misaligned or too small     */
