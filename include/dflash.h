@@ -92,7 +92,10 @@ enum {
  *             A fusion call may add at most capacity rows per sequence.
  *   block_table : NULL for the linear layout.  Paged layout (the ragged
  *             serving shape: sequences take pages from a shared pool as they
- *             grow): device int32 [batch][max_pages]; position p of sequence b
+ *             grow; E4B page "Cache and latency have separate break-even
+ *             points" counts the cache payload before paging, DFlash2 page 7.2
+ *             keeps the draft cache in a paged memory manager; neither fixes a
+ *             layout, this one is the library's): device int32 [batch][max_pages]; position p of sequence b
  *             lives in page block_table[b * max_pages + p / page_size], row
  *             p % page_size.  capacity must equal max_pages * page_size;
  *             page_size a multiple of 128 (one attention key tile never
