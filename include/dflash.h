@@ -15,6 +15,10 @@
  *      acceptance, a correction drawn from the normalised max(0, p - q)
  *      residual, or argmax matching under greedy decoding (E4B page, "Why exact
  *      verification preserves the target"; DFlash2 page, 4.4).
+ * Beyond the cycle: the drafter's head and sampling (section 4), the rest of a
+ * draft layer (section 5) and the DFlash2 variants (section 6).  The cache
+ * descriptor takes a linear, ring (sliding window) or paged (block table)
+ * layout.
  *
  * Conventions for every call
  *  - All tensor pointers are DEVICE pointers (cudaMalloc'd, or any memory the
@@ -26,7 +30,8 @@
  *  - Every argument is validated on the host before any launch; on a non-zero
  *    status nothing has been enqueued and nothing is written.
  *  - Conditions only the device can see (a sequence whose seq_len + n_new
- *    exceeds the cache capacity, a draft token outside [0, V)) never fault:
+ *    exceeds the cache capacity, a draft token outside [0, V), a paged
+ *    block-table entry outside the pool) never fault:
  *    the kernel skips the affected writes and raises a bit in the library's
  *    device status word, read with dflash_read_device_status().
  *  - Tensors are dense, row-major, in the stated shape.  One dtype per call:
