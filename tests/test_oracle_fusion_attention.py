@@ -214,3 +214,89 @@ def test_attention_is_invariant_to_the_order_of_cached_rows():
     c3 = {k: v.copy() for k, v in c.items()}
     c3["cache_k"][0, :, :n] = c["cache_k"][0][:, perm]
     assert np.abs(oracle.block_attn(**c3)[0] - base[0]).max() > 1e-3
+
+
+@pytest.mark.parametrize("gain0", [0.5, 1.5, 3.0])
+def test_attention_closed_form_pins_scale_and_block_positions(gain0):
+    """A case whose output is written out by hand, without the oracle's own
+    formula.  Every query head vector is c_h * e_0, so the per-head RMSNorm
+    leaves c_h / sqrt(c_h^2 / d + eps) * gain[0] in element 0 and zeros
+    elsewhere; element pair (0, d/2) has inverse frequency theta^0 = 1, so RoPE
+    turns it by exactly the row's position in radians.  Two cached keys (the
+    cache holds keys already normalised and rotated) lie in that same pair at
+    angles phi_1 = n (where block row 0 sits when rows start at seq_len = n)
+    and phi_2 = 0 (where it would sit if rows started at 0), with lengths a_1,
+    a_2.  The block keys are zero, so RMSNorm keeps them zero and they score 0.
+    Score of key i for block row j: s_i = qn * a_i * cos(n + j - phi_i) / sqrt(d).
+    Output: (sum_i e^{s_i} v_i + sum_j' vb_j') / (sum_i e^{s_i} + bs).
+    An oracle without the 1/sqrt(d) scale, with 1/d, or with block row j at
+    position j fails this test."""
+    import math
+    d, bs, n, eps, theta = 128, 3, 2, 1e-6, 1e6
+    rng = np.random.default_rng(31)
+    c = [1000.0, -1000.0, 250.0, 4000.0]          # one per query head (GQA 4:1 onto one KV head)
+    q = np.zeros((1, 4, bs, d))
+    for h in range(4):
+        q[0, h, :, 0] = c[h]
+    q_gain = 1.0 + 0.1 * rng.normal(size=d)
+    q_gain[0] = gain0
+    k_gain = 1.0 + 0.1 * rng.normal(size=d)
+    a = [4.0, 3.0]
+    phi = [float(n), 0.0]
+    cache_k = np.zeros((1, 1, 4, d))
+    cache_v = rng.normal(size=(1, 1, 4, d))
+    for i in range(2):
+        cache_k[0, 0, i, 0] = a[i] * math.cos(phi[i])
+        cache_k[0, 0, i, d // 2] = a[i] * math.sin(phi[i])
+    cache_k[0, 0, 2:] = 50.0                       # rows at and past seq_len: never read
+    kb = np.zeros((1, 1, bs, d))
+    vb = rng.normal(size=(1, 1, bs, d))
+    o = oracle.block_attn(q, kb, vb, q_gain, k_gain, cache_k, cache_v, np.array([n]), theta=theta, eps=eps)
+    for h in range(4):
+        qn = c[h] / math.sqrt(c[h] ** 2 / d + eps) * gain0
+        for j in range(bs):
+            s = [qn * a[i] * math.cos(n + j - phi[i]) / math.sqrt(d) for i in range(2)]
+            w = [math.exp(x) for x in s]
+            num = w[0] * cache_v[0, 0, 0] + w[1] * cache_v[0, 0, 1] + vb[0, 0].sum(axis=0)
+            np.testing.assert_allclose(o[0, h, j], num / (w[0] + w[1] + bs), rtol=1e-12, atol=1e-14)
+
+
+def test_attention_brute_force_loops():
+    """Scalar loops over the definition for a few (sequence, head, row)
+    outputs: per-head RMSNorm with the gain, RoPE as a complex rotation of the
+    pair (e, e + d/2) by pos * theta^(-2e/d), scores q.k / sqrt(d) over the
+    window's cached keys followed by the block's keys, an explicit exp / sum
+    softmax, and the weighted sum of the values."""
+    import cmath
+    import math
+    d, theta, eps = 16, 1e4, 1e-6
+    c = _attn_case(7, d=d, cap=20, seq_len=(9, 3))
+
+    def norm_rot(x, gain, pos):
+        r = math.sqrt(sum(t * t for t in x) / d + eps)
+        y = [x[e] / r * gain[e] for e in range(d)]
+        out = [0.0] * d
+        for e in range(d // 2):
+            z = complex(y[e], y[e + d // 2]) * cmath.exp(1j * pos * theta ** (-2.0 * e / d))
+            out[e], out[e + d // 2] = z.real, z.imag
+        return out
+
+    for window in (0, 4):
+        o = oracle.block_attn(**c, theta=theta, eps=eps, window=window)
+        for b, h, j in [(0, 0, 0), (0, 5, 3), (1, 7, 2), (1, 2, 1)]:
+            n = int(c["seq_len"][b])
+            g = h // 4
+            qv = norm_rot(list(c["q"][b, h, j]), c["q_gain"], n + j)
+            keys, vals = [], []
+            for t in range(max(0, n - window) if window else 0, n):
+                keys.append(list(c["cache_k"][b, g, t]))
+                vals.append(list(c["cache_v"][b, g, t]))
+            for jj in range(4):
+                keys.append(norm_rot(list(c["kb"][b, g, jj]), c["k_gain"], n + jj))
+                vals.append(list(c["vb"][b, g, jj]))
+            s = [sum(qv[e] * k[e] for e in range(d)) / math.sqrt(d) for k in keys]
+            mx = max(s)
+            w = [math.exp(x - mx) for x in s]
+            tot = sum(w)
+            ref = [sum(w[i] * vals[i][e] for i in range(len(w))) / tot for e in range(d)]
+            np.testing.assert_allclose(o[b, h, j], ref, rtol=1e-12, atol=1e-13)
