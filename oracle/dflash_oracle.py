@@ -334,8 +334,10 @@ def _log_softmax(l):
 def _categorical_draw(weights, v):
     """Inverse-CDF draw per row: first index y with cumsum(w)[y] > v * sum(w).
 
-    Returns (index, near_tie) where near_tie flags rows whose threshold lies
-    within BOUNDARY_EPS of either edge of the chosen bin.
+    Returns (index, near_tie) where near_tie flags rows whose uniform v lies
+    within BOUNDARY_EPS of either edge of the chosen bin, the edges taken on
+    the uniform's own scale: cumulative mass divided by the total, the values
+    of v at which the draw would change.
     """
     C = np.cumsum(weights, axis=-1)
     S = C[:, -1]
@@ -344,7 +346,7 @@ def _categorical_draw(weights, v):
     rows = np.arange(weights.shape[0])
     upper = C[rows, y]
     lower = np.where(y > 0, C[rows, np.maximum(y - 1, 0)], 0.0)
-    tie = ((t - lower) < BOUNDARY_EPS) | ((upper - t) < BOUNDARY_EPS)
+    tie = ((t - lower) < BOUNDARY_EPS * S) | ((upper - t) < BOUNDARY_EPS * S)
     return y, tie
 
 

@@ -1,6 +1,7 @@
 """GPU parity of the DFlash2 variants (dflash_block_conv, dflash_draft_topm) against the oracle.
 
-block_conv: bf16 output within the relative Frobenius bound of the oracle;
+block_conv: bf16 output within the relative Frobenius bound and the per-row
+bound (each D-wide row) of the oracle;
 identity and one-step-shift kernels reproduce / shift the input bit for bit;
 in place equals out of place.  draft_topm: the candidate indices equal the
 oracle's exactly (the order is taken on the exact bf16 logits, ties to the
@@ -13,7 +14,7 @@ import torch
 
 import block_speculative_decoding_gb300 as dfl
 import oracle
-from helpers import TOL, max_abs, np64, rel_fro
+from helpers import assert_close, np64
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -36,7 +37,7 @@ def test_block_conv_matches_oracle(bs, k, with_bias, residual):
     torch.cuda.synchronize()
     ref = oracle.round_to_bf16(oracle.block_conv(np64(h), np64(w), np64(b) if b is not None else None, bs,
                                                  residual=residual))
-    assert rel_fro(out, ref) <= TOL[torch.bfloat16], (rel_fro(out, ref), max_abs(out, ref))
+    assert_close(out, ref, torch.bfloat16, row=h.shape[1], what="conv")
     # in place gives the same bytes
     hd = h.to(DEV).clone()
     dfl.block_conv(hd, w.to(DEV), b.to(DEV) if b is not None else None, bs, residual=residual, out=hd)

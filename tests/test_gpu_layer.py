@@ -2,7 +2,7 @@
 
 The updated residual stream x2 must match the oracle's (bf16 storage of x1, the
 normalised rows, the SwiGLU activations and x2) within the relative Frobenius
-bound, on small cases with several tiles and split-K slots and on sampled
+bound and the per-row bound (each D-wide row), on small cases with several tiles and split-K slots and on sampled
 sequences of the batched workload's shapes (D = 2560, 32 heads, I = 5120).
 """
 import numpy as np
@@ -11,7 +11,7 @@ import torch
 
 import block_speculative_decoding_gb300 as dfl
 import oracle
-from helpers import TOL, max_abs, np64, rel_fro
+from helpers import assert_close, np64
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -39,7 +39,7 @@ def test_layer_tail_small(bs):
     x2 = _run(c)
     _, ref = oracle.draft_layer_tail(*[np64(c[k]) for k in ("x", "o", "w_o", "g_post", "w_gate", "w_up", "w_down")],
                                      bf16=True)
-    assert rel_fro(x2, ref) <= TOL[torch.bfloat16], (rel_fro(x2, ref), max_abs(x2, ref))
+    assert_close(x2, ref, torch.bfloat16, row=c["x"].shape[1], what="x2")
 
 
 def test_layer_tail_zero_projections_leave_the_stream():
@@ -64,4 +64,4 @@ def test_layer_tail_batched_shape_sampled():
     _, ref = oracle.draft_layer_tail(np64(c["x"][torch.as_tensor(rows, device=DEV)]), np64(c["o"][sel]),
                                      *[np64(c[k]) for k in ("w_o", "g_post", "w_gate", "w_up", "w_down")], bf16=True)
     got = x2[torch.as_tensor(rows, device=DEV)]
-    assert rel_fro(got, ref) <= TOL[torch.bfloat16], (rel_fro(got, ref), max_abs(got, ref))
+    assert_close(got, ref, torch.bfloat16, row=D, what="x2")

@@ -71,6 +71,30 @@ def test_categorical_draw_bins():
     assert y.tolist() == [0, 1, 2, 3]
 
 
+def test_boundary_band_is_on_the_uniforms_scale():
+    """A draw is a boundary case when its uniform lies within 1e-6 of a value
+    at which the drawn index would change: a bin edge C_y / S of the
+    normalised cumulative mass.  With total mass S = 0.25 the edge of
+    [0.125, 0.125] sits at v = 0.5: v = 0.5 - 5e-7 is flagged, v = 0.5 - 2e-6
+    is not (its distance in unnormalised mass, 5e-7, is not the criterion),
+    and with S = 1 the same two uniforms behave the same way."""
+    from oracle.dflash_oracle import _categorical_draw
+    for S in (0.25, 1.0):
+        w = np.array([[S / 2, S / 2]] * 4)
+        y, tie = _categorical_draw(w, np.array([0.5 - 5e-7, 0.5 - 2e-6, 0.5 + 5e-7, 0.5 + 2e-6]))
+        assert y.tolist() == [0, 0, 1, 1]
+        assert tie.tolist() == [True, False, True, False], S
+    # the acceptance decision: |u - alpha| < 1e-6 flags the sequence
+    lt = np.log(np.array([[[0.5, 0.5], [0.5, 0.5]]]))
+    ld = np.log(np.array([[[0.25, 0.75]]]))               # alpha = min(1, 0.5 / 0.75) = 2/3 for token 1
+    for seed in range(200):
+        u = oracle.verify_uniforms(seed, 0, 0, np.array([0]))[0][0]
+        r = oracle.verify(lt, ld, np.array([[1]]), 1.0, seed, 0)
+        assert r.accepted_len[0] == (1 if u < 2.0 / 3.0 else 0)
+        if abs(u - 2.0 / 3.0) >= 1e-6 and r.accepted_len[0] == 1:
+            assert not r.near_tie[0]       # accepted, bonus draw from p = [0.5, 0.5]: edge at v = 0.5
+
+
 def _mc_case(seed, B, bs, V, sharp=1.5):
     rng = np.random.default_rng(seed)
     lt1 = rng.normal(0, sharp, size=(bs, V))

@@ -3,11 +3,11 @@
 Callers inside a CUDA graph capture, or with an allocator that forbids late
 allocation, cannot hand dflash_verify a fresh workspace; this entry point uses
 the library's static device scratch instead.  Its results must equal
-dflash_verify's (both are deterministic) on two calls in a row, which also
-shows that what the first call leaves in the shared scratch does not leak into
-the second.  Runs last (file name) and also passes alone in a fresh process.
+dflash_verify's (both are deterministic) on two calls in a row, and after a
+larger call whose leftovers in the shared scratch have other strides.  Runs last (file name) and also passes alone in a fresh process.
 """
 import ctypes
+from dataclasses import replace
 
 import pytest
 import torch
@@ -42,6 +42,23 @@ def test_noalloc_verify_matches_workspace_verify_twice(T):
         acc, out = _noalloc(lt, ld, x, T, 99, cycle)
         torch.cuda.synchronize()
         assert torch.equal(acc, ref_acc) and torch.equal(out, ref_out)
+
+
+@pytest.mark.parametrize("T", [1.0, 0.0])
+def test_noalloc_verify_after_a_larger_call(T):
+    """A large call (128 sequences, V = 262144) leaves its partial sums all
+    over the shared scratch; a following smaller call with other strides
+    (5 sequences, block 16, V = 40000) must still equal dflash_verify with a
+    fresh workspace, and so must a third, larger call again."""
+    big = workloads.high_batch(8, 1.0)
+    small = replace(workloads.high_batch(16, 1.0), B=5, V=40000, seed=77)
+    for cfg, cycle in ((big, 3), (small, 4), (workloads.BATCHED, 5)):
+        lt, ld = workloads.logits(cfg, DEV)
+        x = workloads.draft_tokens(ld, T, seed=cycle)
+        acc, out = _noalloc(lt, ld, x, T, 123, cycle)
+        ref_acc, ref_out = dfl.verify(lt, ld, x, T, 123, cycle)
+        torch.cuda.synchronize()
+        assert torch.equal(acc, ref_acc) and torch.equal(out, ref_out), cfg.name
 
 
 def test_noalloc_verify_rejects_oversized_problems():
