@@ -226,26 +226,44 @@ def run_gpu(args):
     tokens_per_cycle = float((cyc.acc.cpu() + 1).sum())
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+
+    def timed_region():
+        """Exactly `steps` cycles bracketed by a barrier and a device
+        synchronisation on both sides; seconds on the stream's clock."""
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        # the timed steps run back to back, nothing between the calls (an event
+        # between two kernels would stop the second from launching early)
+        t0.record(stream)
+        for i in range(args.steps):
+            cyc.step(stream, only=args.only)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        return t0.elapsed_time(t1) / 1e3
+
     clocks = ClockSampler(local)
     time.sleep(0.3)
-    if world > 1:
+    # the timed region runs `repeats` times back to back (enough for about two
+    # seconds of load unless given), so that the clock sampler sees the GPU
+    # under load; the median region is reported
+    regions = [timed_region()]
+    repeats = args.repeats if args.repeats > 0 else int(min(500, max(5, np.ceil(2.0 / max(regions[0], 1e-4)))))
+    if world > 1:      # every rank runs the same number of regions (each one ends in a barrier)
         import torch.distributed as dist
-        dist.barrier()
-    torch.cuda.synchronize()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    # the timed steps run back to back, nothing between the calls (an event
-    # between two kernels would stop the second from launching early)
-    t0.record(stream)
-    for i in range(args.steps):
-        cyc.step(stream, only=args.only)
-    t1.record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
+        r = torch.tensor([repeats], dtype=torch.int64, device=dev)
+        dist.all_reduce(r, op=dist.ReduceOp.MAX)
+        repeats = int(r.item())
+    for _ in range(repeats - 1):
+        regions.append(timed_region())
     clk = clocks.stop()
-    elapsed = t0.elapsed_time(t1) / 1e3
+    elapsed = float(np.median(regions))
     # per-call times (rooflines): a second pass of the same steps with events between the calls
     with torch.cuda.stream(stream):
         for i in range(args.steps):
@@ -282,6 +300,9 @@ def run_gpu(args):
     line = {
         "metric": METRIC, "value": cycles / elapsed_max, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": elapsed_max * 1e3 / args.steps, "higher_is_better": True,
+        "repeats": {"count": repeats, "reported": "median",
+                    "ms_per_step_min": min(regions) * 1e3 / args.steps,
+                    "ms_per_step_max": max(regions) * 1e3 / args.steps},
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": "batched: B=32, cached context uniform in [1024, 8192] (ragged), 5 draft layers, "
                                "GQA 32/8, head 128, D=2560, block 8, V=262144, T=%g; per step: fusion of 8 new rows "
@@ -656,53 +677,66 @@ def run_e2e(cyc, stream, args, dev):
 
 # ------------------------------------------------------------ CPU oracle ----
 
-def blas_threads():
-    try:
-        from threadpoolctl import threadpool_info
-        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
-        if n:
-            return max(n)
-    except Exception:
-        pass
-    return os.cpu_count()
+def oracle_verify_batch(cfg, T):
+    """(target logits [B, bs, V], draft logits [B, bs-1, V], both float32
+    holding bf16 values; draft tokens [B, bs-1]) from the seeded generators."""
+    lt, ld = workloads.logits(cfg, "cpu")
+    x = workloads.draft_tokens(ld, T, seed=cfg.seed + 7)
+    return lt.float().numpy(), ld.float().numpy(), x.numpy()
+
+
+def oracle_verify_rows(cfg, T, seqs, batch=None):
+    """Per sequence b: (target logits [1, bs, V], draft logits [1, bs-1, V],
+    draft tokens [1, bs-1]), sliced from the batch's (drawn if not given)."""
+    lt, ld, x = batch if batch is not None else oracle_verify_batch(cfg, T)
+    return {b: (lt[b:b + 1], ld[b:b + 1], x[b:b + 1]) for b in seqs}
+
+
+def oracle_weights(cfg):
+    """The seeded weights as float64 arrays."""
+    f = lambda t: t.detach().to("cpu", torch.float64).numpy()  # noqa: E731
+    w = workloads.weights(cfg, "cpu")
+    return {"w_fuse": f(w.w_fuse), "g_fuse": f(w.g_fuse), "w_kv": f(w.w_kv), "k_gain": f(w.k_gain),
+            "q_gain": f(w.q_gain)}
+
+
+def oracle_cache(cfg):
+    """(k, v) [L, 1, Hkv, max seq_len, d] float32 holding bf16 N(0, 1) values."""
+    g = workloads.generator(cfg.seed * 1000 + 3, "cpu")
+    n = int(workloads.seq_lens(cfg).max())
+    shape = (cfg.L, 1, cfg.Hkv, n, cfg.d)
+    return (torch.randn(shape, generator=g).to(torch.bfloat16).float().numpy(),
+            torch.randn(shape, generator=g).to(torch.bfloat16).float().numpy())
 
 
 class OracleSample:
     """Host (float64) copies of the workload for a few sampled sequences.
 
-    Weights, taps, block projections, logits and draft tokens are the same
-    seeded tensors the GPU arm uses; each sampled sequence's cached K/V (its
-    own seq_len rows per layer and head, synthetic N(0,1) in bf16 values) is
-    drawn up front from a generator seeded by the sequence index."""
+    Weights, taps and block projections are the same seeded tensors the GPU
+    arm uses; logits and draft tokens come from the seeded batch generators
+    (`oracle_verify_rows`).  The cached K/V (synthetic N(0, 1) in bf16 values,
+    as float32) is one array of the longest sequence's length per layer and
+    head (`oracle_cache`); sequence b reads its first seq_len[b] rows."""
 
-    def __init__(self, cfg, T, seqs):
+    def __init__(self, cfg, T, seqs, verify_rows=None, kv=None, weights=None):
         f = lambda t: t.detach().to("cpu", torch.float64).numpy()  # noqa: E731
         self.cfg, self.T, self.seqs = cfg, T, list(seqs)
-        w = workloads.weights(cfg, "cpu")
-        self.w = {"w_fuse": f(w.w_fuse), "g_fuse": f(w.g_fuse), "w_kv": f(w.w_kv), "k_gain": f(w.k_gain),
-                  "q_gain": f(w.q_gain)}
+        self.w = weights if weights is not None else oracle_weights(cfg)
         self.seq = workloads.seq_lens(cfg).numpy().astype(np.int64)
         taps = workloads.taps(cfg, cfg.B * cfg.bs, "cpu")
         self.taps = {b: [f(t[b * cfg.bs:(b + 1) * cfg.bs]) for t in taps] for b in self.seqs}
         blocks = [workloads.block(cfg, "cpu", layer=l) for l in range(cfg.L)]
         self.blocks = {b: [[f(t[b:b + 1]) for t in blocks[l]] for l in range(cfg.L)] for b in self.seqs}
-        lt, ld = workloads.logits(cfg, "cpu")
-        x = workloads.draft_tokens(ld, T, seed=cfg.seed + 7)
-        self.lt = {b: f(lt[b:b + 1]) for b in self.seqs}
-        self.ld = {b: f(ld[b:b + 1]) for b in self.seqs}
-        self.x = {b: x[b:b + 1].numpy() for b in self.seqs}
-        # cached K/V of the sampled sequences: float32 holding bf16 values (the oracle
-        # widens what it reads to float64)
-        self._kv = {}
-        for b in self.seqs:
-            g = workloads.generator(cfg.seed * 1000 + 3 + b, "cpu")
-            n = int(self.seq[b])
-            k = torch.randn(cfg.L, 1, cfg.Hkv, n, cfg.d, generator=g).to(torch.bfloat16).float().numpy()
-            v = torch.randn(cfg.L, 1, cfg.Hkv, n, cfg.d, generator=g).to(torch.bfloat16).float().numpy()
-            self._kv[b] = (k, v)
+        rows = verify_rows if verify_rows is not None else oracle_verify_rows(cfg, T, self.seqs)
+        self.lt = {b: rows[b][0].astype(np.float64) for b in self.seqs}
+        self.ld = {b: rows[b][1].astype(np.float64) for b in self.seqs}
+        self.x = {b: rows[b][2] for b in self.seqs}
+        self._kv = kv if kv is not None else oracle_cache(cfg)
 
     def kv(self, b):
-        return self._kv[b]
+        k, v = self._kv
+        n = int(self.seq[b])
+        return k[:, :, :, :n], v[:, :, :, :n]
 
     # the three parts of one sequence's cycle, as the oracle computes them
     def fuse(self, b):
@@ -737,79 +771,174 @@ class OracleSample:
         self.verify(b)
 
 
-def cpu_baseline(cfg, seconds, T):
-    """Oracle cycles/s on the host: whole cycles of sampled sequences, repeated
-    until `seconds` have passed, scaled to the B-sequence batch."""
-    sample = OracleSample(cfg, T, range(8))
-    t0 = time.perf_counter()
-    done = 0
+def _oracle_worker(conn, T, seqs, paths):
+    """A host worker for the oracle timings: single-threaded (its BLAS thread
+    count is fixed to 1 by the environment it was spawned with), holding the
+    inputs of its own sequences.  Commands: ("cycle",) runs one cycle of each
+    of its sequences and answers the seconds taken; ("budget", s) runs cycles
+    over its sequences until s seconds have passed and answers (count, seconds,
+    summed context); ("stop",) ends it."""
+    torch.set_num_threads(1)
+    rows = oracle_verify_rows(workloads.BATCHED, T, seqs,
+                              batch=tuple(np.load(paths[n], mmap_mode="r") for n in ("lt", "ld", "x")))
+    kv = tuple(np.load(paths[n], mmap_mode="r") for n in ("k", "v"))
+    weights = {n: np.load(paths[n], mmap_mode="r") for n in ("w_fuse", "g_fuse", "w_kv", "k_gain", "q_gain")}
+    sample = OracleSample(workloads.BATCHED, T, seqs, verify_rows=rows, kv=kv, weights=weights)
+    conn.send("ready")
     while True:
-        sample.cycle(sample.seqs[done % len(sample.seqs)])
-        done += 1
-        if time.perf_counter() - t0 > seconds:
-            break
-    el = time.perf_counter() - t0
-    ctx = float(np.mean([sample.seq[sample.seqs[i % len(sample.seqs)]] for i in range(done)]))
-    per_cycle = el * cfg.B / done
-    return {"value": 1.0 / per_cycle, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
-            "sample": "%d full single-sequence cycles (fusion of its 8 rows, 5 layers of block attention, "
-                      "verification) over sequences 0-7 (mean context %.0f vs %.0f for the batch), %.1f s, "
-                      "scaled x%d to the batch" % (done, ctx, float(sample.seq.mean()), el, cfg.B)}
+        cmd = conn.recv()
+        if cmd[0] == "cycle":
+            t0 = time.perf_counter()
+            for b in sample.seqs:
+                sample.cycle(b)
+            conn.send(time.perf_counter() - t0)
+        elif cmd[0] == "budget":
+            t0 = time.perf_counter()
+            done, ctx = 0, 0
+            while done == 0 or time.perf_counter() - t0 < cmd[1]:
+                b = sample.seqs[done % len(sample.seqs)]
+                sample.cycle(b)
+                ctx += int(sample.seq[b])
+                done += 1
+            conn.send((done, time.perf_counter() - t0, ctx))
+        else:
+            conn.close()
+            return
+
+
+class OraclePool:
+    """Spawned host processes that split the batch's sequences between them
+    (sequence-parallel: the sequences of a cycle are independent), one thread
+    each.  Spawned, not forked, so it is safe after CUDA has been used."""
+
+    def __init__(self, T, n_workers, seqs_of, inputs):
+        import multiprocessing as mp
+        paths = inputs.paths
+        ctx = mp.get_context("spawn")
+        keep = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+        for k in keep:
+            os.environ[k] = "1"          # inherited by the spawned workers before they import numpy
+        try:
+            self.conns, self.procs = [], []
+            for i in range(n_workers):
+                a, b = ctx.Pipe()
+                mine = seqs_of(i)
+                pr = ctx.Process(target=_oracle_worker, args=(b, T, mine, paths), daemon=True)
+                pr.start()
+                self.conns.append(a)
+                self.procs.append(pr)
+        finally:
+            for k, v in keep.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
+        for c in self.conns:
+            assert c.recv() == "ready"
+
+    def ask(self, cmd):
+        for c in self.conns:
+            c.send(cmd)
+        return [c.recv() for c in self.conns]
+
+    def close(self):
+        for c in self.conns:
+            c.send(("stop",))
+        for pr in self.procs:
+            pr.join(timeout=30)
+
+
+class OracleInputs:
+    """The oracle workers' shared inputs -- the verification logits and draft
+    tokens, the weights and the synthetic cache -- drawn once and saved to
+    files that every worker maps (one copy in the page cache instead of one
+    per process, and nothing large to send to a starting process)."""
+
+    def __init__(self, cfg, T):
+        self.dir = tempfile.mkdtemp(prefix="dflash_oracle_")
+        arrays = dict(oracle_weights(cfg))
+        arrays["k"], arrays["v"] = oracle_cache(cfg)
+        arrays["lt"], arrays["ld"], arrays["x"] = oracle_verify_batch(cfg, T)
+        self.paths = {}
+        for n, a in arrays.items():
+            self.paths[n] = os.path.join(self.dir, n + ".npy")
+            np.save(self.paths[n], a)
+
+    def close(self):
+        for pth in self.paths.values():
+            os.unlink(pth)
+        os.rmdir(self.dir)
+
+
+def host_cores():
+    return max(1, os.cpu_count() or 1)
+
+
+def cpu_baseline(cfg, seconds, T):
+    """Oracle cycles/s on the host, two ways, each over about `seconds`:
+    one thread running whole single-sequence cycles of sequences 0-7, and
+    every host core with the batch's sequences split between single-threaded
+    processes (sequence-parallel).  Both are scaled to the B-sequence batch;
+    `value` is the all-cores figure."""
+    inputs = OracleInputs(cfg, T)
+    one = OraclePool(T, 1, lambda i: list(range(8)), inputs)
+    done1, el1, ctx1 = one.ask(("budget", seconds / 2))[0]
+    one.close()
+    n = min(host_cores(), cfg.B)
+    pool = OraclePool(T, n, lambda i: list(range(i, cfg.B, n)), inputs)
+    res = pool.ask(("budget", seconds / 2))
+    pool.close()
+    inputs.close()
+    done_n = sum(r[0] for r in res)
+    el_n = max(r[1] for r in res)
+    ctx_n = sum(r[2] for r in res)
+    mean_ctx = float(workloads.seq_lens(cfg).float().mean())
+    v1 = done1 / el1 / cfg.B
+    vn = done_n / el_n / cfg.B
+    return {"value": vn, "unit": UNIT, "cores": n, "kind": "oracle",
+            "single_thread_value": v1,
+            "sample": "whole single-sequence cycles (fusion of its 8 rows, 5 layers of block attention, "
+                      "verification) scaled to the %d-sequence batch.  One thread: %d cycles over sequences 0-7 "
+                      "(mean context %.0f vs %.0f for the batch) in %.1f s -> %.4f cycles/s.  All %d cores: the "
+                      "batch's sequences split over %d single-threaded processes (sequence-parallel), %d cycles "
+                      "(mean context %.0f) in %.1f s -> %.4f cycles/s"
+                      % (cfg.B, done1, ctx1 / done1, mean_ctx, el1, v1, n, n, done_n, ctx_n / done_n, el_n, vn)}
 
 
 def run_reference(args):
-    """The oracle as the reference arm.  Each step is one unit of a sampled
-    sequence's cycle, rotating over fusion (one sequence), block attention
-    (one layer, one KV head with its query group) and verification (one
-    sequence); the batch cycle time is estimated as
-    B * (t_fuse + L * Hkv * t_attn_head + t_verify) from the units' means."""
+    """The oracle as the reference arm: each step is one whole cycle of the
+    batch (fusion, five layers of block attention and verification for all
+    B sequences), computed by single-threaded host processes that split the
+    sequences between them, one per core (rank 0 only)."""
     rank, world, _ = env_rank()
     if rank != 0:
         return
     cfg = workloads.BATCHED
-    sample = OracleSample(cfg, args.temperature, range(8))
-    kinds = ("fuse", "attn", "verify")
-
-    def unit(i):
-        b = sample.seqs[(i // 3) % len(sample.seqs)]
-        kind = kinds[i % 3]
-        if kind == "fuse":
-            sample.fuse(b)
-        elif kind == "attn":
-            j = i // 3
-            sample.attn(b, j % cfg.L, (j // cfg.L) % cfg.Hkv)
-        else:
-            sample.verify(b)
-        return kind
-
-    for i in range(args.warmup):
-        unit(i)
-    times = {k: [] for k in kinds}
+    steps = args.steps if args.steps is not None else 5
+    n = min(host_cores(), cfg.B)
+    inputs = OracleInputs(cfg, args.temperature)
+    pool = OraclePool(args.temperature, n, lambda i: list(range(i, cfg.B, n)), inputs)
+    for _ in range(args.warmup):
+        pool.ask(("cycle",))
     t0 = time.perf_counter()
-    for i in range(args.steps):
+    per = []
+    for _ in range(steps):
         ts = time.perf_counter()
-        k = unit(i)
-        times[k].append(time.perf_counter() - ts)
-    i = args.steps
-    while any(not v for v in times.values()):     # fewer than 3 steps: finish one unit of each kind
-        ts = time.perf_counter()
-        k = unit(i)
-        times[k].append(time.perf_counter() - ts)
-        i += 1
+        pool.ask(("cycle",))
+        per.append(time.perf_counter() - ts)
     el = time.perf_counter() - t0
-    m = {k: statistics.mean(v) for k, v in times.items()}
-    cycle_s = cfg.B * (m["fuse"] + cfg.L * cfg.Hkv * m["attn"] + m["verify"])
-    value = 1.0 / cycle_s
-    sample_txt = ("%d oracle units (rotating: one sequence's fusion, one layer x KV head of block attention, "
-                  "one sequence's verification) over sequences 0-7, %.1f s; batch cycle = B x (fuse + L x Hkv x "
-                  "attn + verify) = %.2f s" % (i, el, cycle_s))
+    pool.close()
+    inputs.close()
+    value = steps / el
+    sample_txt = ("%d whole batch cycles (B=%d sequences: fusion of 8 rows each, 5 layers of block attention, "
+                  "verification), the sequences split over %d single-threaded processes, %.1f s"
+                  % (steps, cfg.B, n, el))
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el * 1e3 / max(args.steps, 1),
+            "steps": steps, "warmup": args.warmup, "ms_per_step": el * 1e3 / steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": "batched: B=32, ragged context [1024, 8192], 5 layers, block 8, V=262144, T=%g"
                        % args.temperature},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
-                             "sample": sample_txt},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": n, "kind": "oracle", "sample": sample_txt},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -834,7 +963,11 @@ def run_profile(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: 1000 GPU cycles per repeat; 5 batch cycles for the reference arm)")
+    ap.add_argument("--repeats", type=int, default=0,
+                    help="timed regions of --steps steps each (default: enough for about 2 s of load); the "
+                         "median is reported")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="dflash", choices=["dflash", "reference"])
     ap.add_argument("--temperature", type=float, default=1.0)
@@ -853,6 +986,8 @@ def main():
         return
     if args.warmup < 3 and args.impl == "dflash":
         args.warmup = 3
+    if args.impl == "dflash" and args.steps is None:
+        args.steps = 1000
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -22,7 +22,7 @@ __all__ = [
     "KVCache", "DFlashError", "lib", "fuse_context", "block_attn", "verify", "draft_head", "draft_layer_tail",
     "interleave_gate_up", "draft_layer_tail_workspace_size",
     "fuse_context_workspace_size", "block_attn_workspace_size", "verify_workspace_size", "draft_head_workspace_size",
-    "philox4x32_10", "read_device_status", "version", "LIB_PATH",
+    "philox4x32_10", "read_device_status", "debug_block_attn_wait_timeout", "version", "LIB_PATH",
     "DEV_CAPACITY", "DEV_BAD_TOKEN", "DEV_BAD_SEQLEN", "DEV_TIMEOUT",
 ]
 
@@ -96,6 +96,8 @@ def lib():
     L.dflash_verify_noalloc_max_scratch.restype = sz
     L.dflash_verify_noalloc.argtypes = [vp, vp, i32, vp, i32, i32, i32, f32, u64, u64, vp, vp, vp]
     L.dflash_verify_noalloc.restype = i32
+    L.dflash_debug_block_attn_wait_timeout.argtypes = [i32, i32, i32, P(_KVCacheDesc), vp, vp, sz, u32, vp]
+    L.dflash_debug_block_attn_wait_timeout.restype = i32
     L.dflash_philox4x32_10.argtypes = [vp, u32, u32, vp, i32, vp]
     L.dflash_philox4x32_10.restype = i32
     L.dflash_read_device_status.argtypes = [P(u32), vp]
@@ -226,6 +228,19 @@ def block_attn(layer, q, kb, vb, q_gain, k_gain, cache: KVCache, window=0, rope_
                                    _ptr(k_gain), rope_theta, eps, ctypes.byref(desc), window, _ptr(out),
                                    _ptr(ws), nbytes, _stream(stream)))
     return out
+
+
+def debug_block_attn_wait_timeout(cache: KVCache, block_size, num_q_heads, limit_us, out, workspace=None,
+                                  stream=None):
+    """Test hook: the block attention's split-merge kernel alone, over counters
+    nothing increments, with its bounded wait cut to limit_us; every wait runs
+    out and raises DEV_TIMEOUT (see include/dflash.h)."""
+    desc = cache.desc()
+    nbytes = block_attn_workspace_size(desc.batch, block_size, num_q_heads, desc.num_kv_heads, desc.capacity, 0,
+                                       desc.dtype)
+    ws = _workspace(nbytes, out.device, workspace)
+    _check(lib().dflash_debug_block_attn_wait_timeout(desc.batch, block_size, num_q_heads, ctypes.byref(desc),
+                                                      _ptr(out), _ptr(ws), nbytes, int(limit_us), _stream(stream)))
 
 
 def verify(target_logits, draft_logits, draft_tokens, temperature, seed, cycle, accepted_len=None,

@@ -294,6 +294,31 @@ dflash_status dflash_block_attn(int layer, int batch, int block_size, int num_q_
                            static_cast<cudaStream_t>(stream), dev);
 }
 
+dflash_status dflash_debug_block_attn_wait_timeout(int batch, int block_size, int num_q_heads,
+                                                  const dflash_kv_cache* cache, void* out, void* workspace,
+                                                  size_t workspace_bytes, unsigned limit_us, void* stream) {
+  dflash_status s = check_cache(cache);
+  if (s) return s;
+  if (cache->dtype != DFLASH_BF16) return fail(DFLASH_ERR_UNSUPPORTED, "the wait probe runs the bf16 path");
+  if (batch != cache->batch) return fail(DFLASH_ERR_INVALID_ARGUMENT, "batch must equal cache->batch");
+  if (block_size < 1 || block_size > 16) return fail(DFLASH_ERR_UNSUPPORTED, "block_size must be 1..16");
+  const int hkv = cache->num_kv_heads;
+  if (num_q_heads < 1 || num_q_heads % hkv) return fail(DFLASH_ERR_INVALID_ARGUMENT, "num_q_heads % num_kv_heads != 0");
+  if ((num_q_heads / hkv) * block_size > 64)
+    return fail(DFLASH_ERR_UNSUPPORTED, "(num_q_heads/num_kv_heads) * block_size must be <= 64");
+  if (!out || !aligned16(out)) return fail(DFLASH_ERR_INVALID_ARGUMENT, "out must be 16-byte aligned");
+  if (limit_us < 1 || limit_us > 100000) return fail(DFLASH_ERR_INVALID_ARGUMENT, "limit_us must be 1..100000");
+  const size_t need = attn_ws_bytes(batch, block_size, num_q_heads, hkv, cache->capacity, 0, DFLASH_BF16);
+  s = check_ws(workspace, workspace_bytes, need);
+  if (s) return s;
+  DeviceInfo dev;
+  s = device_info(&dev);
+  if (s) return s;
+  return launch_attn_wait_timeout_probe(batch, block_size, num_q_heads, *cache, out, workspace,
+                                        static_cast<unsigned long long>(limit_us) * 1000ull,
+                                        static_cast<cudaStream_t>(stream), dev);
+}
+
 // ------------------------------------------------------ draft layer tail ----
 
 size_t dflash_draft_layer_tail_workspace_size(int batch, int block_size, int num_q_heads, int d_model,

@@ -8,25 +8,31 @@
 // block); "DFlash & DFlash2: Block-Diffusion LLM-Speedup" 4.1 (K_i, V_i are the
 // injected context rows followed by the block rows).
 //
-// Kernels:
+// Kernels (three launches per call, each a programmatic dependent of the one
+// before it):
 //   prologue -- per (sequence, block row): RMSNorm * gain and RoPE of every
 //               query head and block key, rounded to the storage dtype; also
-//               clears the work-queue counter of the main kernel.
+//               clears the work-queue counter and the per-pair counters.
 //   main     -- split-KV, memory-bound: a persistent grid (one CTA per SM)
 //               takes work items (sequence, KV head, key split) from an atomic
-//               queue; splits of one (sequence, KV head) are near-equal.  A
-//               producer warp streams 64-key K/V tiles of the cache (and, for
-//               the last split, the block's own keys) with TMA (128-byte
-//               swizzle) through a ring of up to six stages.  Q is loaded twice,
-//               as MMA rows 0.. and 64.. (two lane quarters); one thread issues
-//               S = Q K^T and another O += P V with tcgen05.mma; softmax warps
-//               own one query row per thread and per copy, each copy taking
-//               one half of every tile's keys, and write P (bf16 hi + lo) to
-//               tensor memory.  Epilogue warps merge the two copies (log-sum-
-//               exp) and write the output row, or a normalised fp32 partial
-//               and its (max, sum) when the item is one of several splits.
+//               queue; the producer warp decodes each item once and hands it
+//               to the other roles through shared memory.  The products are
+//               taken transposed: the 128 keys of a tile fill the tensor
+//               core's M and the G * bs query rows of the pair (padded to
+//               NC = 32 or 64) its N.  The producer streams 128-key K and V
+//               tiles of the cache (and, for the last split, the block's own
+//               keys) with TMA (128-byte swizzle) through K and V rings sized
+//               to the shared memory (two K and three V stages at 227 KB); one thread issues S^T = K Q^T into tensor
+//               memory, eight softmax warps (one key per thread) write
+//               P^T = 2^(S^T scale - m) to shared memory as bf16 hi + lo parts,
+//               another thread issues O^T += V^T [P_hi^T P_lo^T], and four
+//               epilogue warps add the hi and lo columns and write the output
+//               row, or a normalised fp32 partial and its (max, sum) when the
+//               item is one of several splits.  The running max of each row is
+//               fixed per item from its first tile.
 //   combine  -- one warp per output row merges the splits' partials
-//               (log-sum-exp); launched as a programmatic dependent of main.
+//               (log-sum-exp) as soon as its pair's splits are written, and
+//               recomputes exactly any pair whose scores outgrew the max.
 // fp32 storage uses a plain SIMT kernel (parity path for the tiny fp32 case).
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -71,6 +77,7 @@ struct AttnParams {
                              // a flag (scores outgrew the running max), then per (b, g) the count of
                              // epilogue warps (4 per split) that finished writing
   unsigned* status;
+  unsigned long long wait_limit_ns;  // the combine kernel's bounded wait for a pair's splits
 };
 
 // Cached rows a sequence attends to: its length, clamped to the capacity; a
@@ -394,7 +401,8 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnParams p) {
   const int first = p.window > 0 ? max(0, n - p.window) : 0;
   const int nsplit = n_splits(n - first, p.chunk);
   bool ready = true;
-  if (lane == 0) ready = wait_counter_at_least(p.counters + 1 + p.B * p.Hkv + bg, 4 * nsplit, p.status);
+  if (lane == 0)
+    ready = wait_counter_at_least(p.counters + 1 + p.B * p.Hkv + bg, 4 * nsplit, p.status, p.wait_limit_ns);
   if (!__shfl_sync(0xffffffffu, ready ? 1 : 0, 0)) return;
   if (__ldcg(p.counters + 1 + bg) != 0) {
     attn_row_exact(p, b, g, row, first, n);
@@ -1141,6 +1149,7 @@ dflash_status launch_block_attn(int layer, int B, int bs, int Hq, const void* q,
   p.num_pages = c.num_pages;
   p.scale_log2 = 1.4426950408889634f * scale;
   p.status = dev.status;
+  p.wait_limit_ns = kWaitLimitNs;
 
   const int nc = p.rows > 32 ? 64 : 32;   // query rows padded to the MMA's N
   AttnMaps maps;
@@ -1186,23 +1195,15 @@ dflash_status launch_block_attn(int layer, int B, int bs, int Hq, const void* q,
   cfg.numAttrs = 1;
   cudaError_t le;
   if (nc == 32) {
-    static int configured = -1;
-    if (configured != dev.device) {
-      le = cudaFuncSetAttribute(attn_tc_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(dev.max_smem_optin));
-      if (le != cudaSuccess) return cuda_fail(le, "cudaFuncSetAttribute(attn_tc_kernel)");
-      configured = dev.device;
-    }
+    dflash_status ss = smem_limit_once<attn_tc_kernel<32>>(dev.device, static_cast<int>(dev.max_smem_optin),
+                                                           "cudaFuncSetAttribute(attn_tc_kernel)");
+    if (ss) return ss;
     cfg.blockDim = dim3(TcCfg<32>::kThreads);
     le = cudaLaunchKernelEx(&cfg, attn_tc_kernel<32>, maps, p, lay);
   } else {
-    static int configured = -1;
-    if (configured != dev.device) {
-      le = cudaFuncSetAttribute(attn_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(dev.max_smem_optin));
-      if (le != cudaSuccess) return cuda_fail(le, "cudaFuncSetAttribute(attn_tc_kernel)");
-      configured = dev.device;
-    }
+    dflash_status ss = smem_limit_once<attn_tc_kernel<64>>(dev.device, static_cast<int>(dev.max_smem_optin),
+                                                           "cudaFuncSetAttribute(attn_tc_kernel)");
+    if (ss) return ss;
     cfg.blockDim = dim3(TcCfg<64>::kThreads);
     le = cudaLaunchKernelEx(&cfg, attn_tc_kernel<64>, maps, p, lay);
   }
@@ -1218,6 +1219,44 @@ dflash_status launch_block_attn(int layer, int B, int bs, int Hq, const void* q,
   }
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? DFLASH_OK : cuda_fail(e, "block attention launch");
+}
+
+// Test hook for the bounded waits: the combine kernel alone, over per-pair
+// counters cleared here and incremented by nothing (no main kernel runs), with
+// its wait cut to limit_ns.  Each warp gives up after limit_ns, raises
+// DFLASH_DEV_TIMEOUT and returns without touching the output; only the
+// sequence lengths and the counters are read.
+dflash_status launch_attn_wait_timeout_probe(int B, int bs, int Hq, const dflash_kv_cache& c, void* out, void* ws,
+                                             unsigned long long limit_ns, cudaStream_t st, const DeviceInfo& dev) {
+  const int Hkv = c.num_kv_heads;
+  AttnParams p{};
+  p.B = B;
+  p.bs = bs;
+  p.G = Hq / Hkv;
+  p.Hkv = Hkv;
+  p.Hq = Hq;
+  p.cap = c.capacity;
+  p.ring = c.ring;
+  p.window = 0;
+  p.chunk = pick_chunk(B, Hkv, c.capacity, 0);
+  p.max_splits = n_splits(c.capacity, p.chunk);
+  p.rows = p.G * bs;
+  p.seq_len = c.seq_len;
+  WsCarver w(ws);
+  w.take<__nv_bfloat16>(static_cast<size_t>(B) * Hq * bs * HD);
+  w.take<__nv_bfloat16>(static_cast<size_t>(B) * Hkv * bs * HD);
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.opart = w.take<float>(static_cast<size_t>(B) * Hkv * p.max_splits * p.rows * HD);
+  p.mlpart = w.take<float2>(static_cast<size_t>(B) * Hkv * p.max_splits * p.rows);
+  p.counters = w.take<int>(1 + 2 * static_cast<size_t>(B) * Hkv);
+  p.status = dev.status;
+  p.wait_limit_ns = limit_ns;
+  cudaError_t e = cudaMemsetAsync(p.counters, 0, (1 + 2 * static_cast<size_t>(B) * Hkv) * sizeof(int), st);
+  if (e != cudaSuccess) return cuda_fail(e, "clear counters");
+  const long warps = static_cast<long>(B) * Hkv * p.rows;
+  attn_combine_kernel<<<static_cast<unsigned>((warps + 7) / 8), 256, 0, st>>>(p);
+  e = cudaGetLastError();
+  return e == cudaSuccess ? DFLASH_OK : cuda_fail(e, "attn_combine_kernel launch");
 }
 
 }  // namespace dflash

@@ -38,9 +38,10 @@ __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
   return v;
 }
 
-// Spin (bounded) until *counter >= target; false after kWaitLimitNs with
-// DFLASH_DEV_TIMEOUT raised.  Defined below kWaitLimitNs.
-__device__ __forceinline__ bool wait_counter_at_least(const int* counter, int target, unsigned* status);
+// Spin (bounded) until *counter >= target; false after limit_ns (default
+// kWaitLimitNs) with DFLASH_DEV_TIMEOUT raised.
+__device__ __forceinline__ bool wait_counter_at_least(const int* counter, int target, unsigned* status,
+                                                      unsigned long long limit_ns = kWaitLimitNs);
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -94,11 +95,12 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 
 // Wait for the phase with the given parity to complete.  Bounded: after
 // kWaitLimitNs it raises DFLASH_DEV_TIMEOUT and returns false.
-__device__ __forceinline__ bool wait_counter_at_least(const int* counter, int target, unsigned* status) {
+__device__ __forceinline__ bool wait_counter_at_least(const int* counter, int target, unsigned* status,
+                                                      unsigned long long limit_ns) {
   if (ld_acquire_gpu(counter) >= target) return true;
   const unsigned long long t0 = global_timer_ns();
   while (ld_acquire_gpu(counter) < target) {
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
+    if (global_timer_ns() - t0 > limit_ns) {
       raise_status(status, DFLASH_DEV_TIMEOUT);
       return false;
     }

@@ -6,6 +6,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <string>
 
 #include "../../include/dflash.h"
@@ -25,6 +26,26 @@ struct DeviceInfo {
   unsigned* status = nullptr;  // address of the library's device status word
 };
 dflash_status device_info(DeviceInfo* out);
+
+// --- kernel attributes ---------------------------------------------------------
+constexpr int kAttrMaxDevices = 64;
+
+// Raises Kernel's dynamic shared-memory limit to at least `bytes` on `device`
+// (the current device), once per kernel, device and process.  Safe to call
+// from several host threads: each device has its own atomic record, and two
+// threads racing on a first call both set the same (idempotent) attribute.
+template <auto Kernel>
+dflash_status smem_limit_once(int device, int bytes, const char* what) {
+  static std::atomic<int> done[kAttrMaxDevices];
+  if (device < 0 || device >= kAttrMaxDevices) return fail(DFLASH_ERR_UNSUPPORTED, "device index out of range");
+  if (done[device].load(std::memory_order_acquire) >= bytes) return DFLASH_OK;
+  const cudaError_t e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return cuda_fail(e, what);
+  int cur = done[device].load(std::memory_order_relaxed);
+  while (cur < bytes && !done[device].compare_exchange_weak(cur, bytes, std::memory_order_release)) {
+  }
+  return DFLASH_OK;
+}
 
 // --- TMA descriptors --------------------------------------------------------
 // 2D row-major bf16 tensor [rows][cols] with a (box_cols x box_rows) box and
@@ -62,6 +83,9 @@ dflash_status launch_block_attn(int layer, int B, int bs, int Hq, const void* q,
                                 const void* vb, const void* qg, const void* kg, float theta,
                                 float eps, const dflash_kv_cache& c, int window, void* out, void* ws,
                                 cudaStream_t st, const DeviceInfo& dev);
+
+dflash_status launch_attn_wait_timeout_probe(int B, int bs, int Hq, const dflash_kv_cache& c, void* out, void* ws,
+                                             unsigned long long limit_ns, cudaStream_t st, const DeviceInfo& dev);
 
 // --- drafter head ------------------------------------------------------------
 size_t head_ws_bytes(int M, int D, int V);

@@ -715,13 +715,9 @@ dflash_status launch_gemm(const TmapPack& am, const CUtensorMap& bm, const GemmA
                           const DeviceInfo& dev) {
   const size_t smem = gemm_smem_bytes<BN, STAGES, MT>();
   if (smem > dev.max_smem_optin) return fail(DFLASH_ERR_UNSUPPORTED, "gemm_tc: shared memory");
-  static int configured = -1;
-  if (configured != dev.device) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, STAGES, MT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(gemm_tc_kernel)");
-    configured = dev.device;
-  }
+  dflash_status ss = smem_limit_once<gemm_tc_kernel<BN, STAGES, MT>>(dev.device, static_cast<int>(smem),
+                                                                      "cudaFuncSetAttribute(gemm_tc_kernel)");
+  if (ss) return ss;
   const int units = a.m_tiles * a.n_tiles * a.k_splits;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(a.stream_k ? a.stream_k : std::min(units, dev.num_sms)));

@@ -39,6 +39,16 @@
  *  - Reading of positions (the pages do not fix them): cached context row t of
  *    a sequence sits at cache position t; block row j sits at seq_len[b] + j.
  *  - RoPE pairs element e with e + d/2 and turns it by pos * theta^(-2e/d).
+ *  - Weight orientation: every weight is stored with its input (K) dimension
+ *    contiguous.  W_c is taken as the DFlash2 page writes it (4.1), D rows of
+ *    J * d_t, so Y = concat(taps) W_c^T; W_kv and the drafter's projections
+ *    are [outputs][inputs] (the nn.Linear layout).  A [J * d_t, D] listing of
+ *    W_c is this matrix transposed.
+ *  - RoPE theta and the RMSNorm eps are plain float arguments of each call
+ *    (1e6 and 1e-6 in the pages' drafter configuration), not a struct.
+ *  - Status 5 is a workspace error (NULL, misaligned or too small); there is
+ *    no debug-only status: conditions only the device sees are reported
+ *    through the device status word in every build.
  */
 #ifndef DFLASH_H_
 #define DFLASH_H_
@@ -259,6 +269,20 @@ DFLASH_API dflash_status dflash_verify_noalloc(const void* target_logits, const 
 /* ---------------------------------------------------------------------------
  * Diagnostics.
  * ------------------------------------------------------------------------- */
+
+/* Test hook for the bounded waits inside the kernels (no counterpart in the
+ * pages).  Runs only the last kernel of dflash_block_attn -- the one that
+ * merges the key splits of each (sequence, KV head) once their writers have
+ * counted in -- over counters that it clears and that nothing increments, with
+ * its wait cut to limit_us microseconds (1..100000).  Every wait runs out:
+ * the kernel raises DFLASH_DEV_TIMEOUT in the device status word, leaves `out`
+ * untouched and returns, so the stream stays usable.  Arguments and workspace
+ * as dflash_block_attn with window 0; bf16 caches only.  It reads the
+ * sequence lengths and writes only the workspace's counters. */
+DFLASH_API dflash_status dflash_debug_block_attn_wait_timeout(int batch, int block_size, int num_q_heads,
+                                                             const dflash_kv_cache* cache, void* out,
+                                                             void* workspace, size_t workspace_bytes,
+                                                             unsigned limit_us, void* stream);
 
 /* Philox-4x32-10 (Salmon et al., SC'11) on n device counters: ctr [n][4],
  * key [2] (host values), out [n][4].  The generator verification draws from. */

@@ -28,7 +28,7 @@ def test_header_declares_the_three_calls():
     syms = declared_symbols()
     for s in ("dflash_fuse_context", "dflash_block_attn", "dflash_verify"):
         assert s in syms
-    assert len(syms) == 19
+    assert len(syms) == 20
 
 
 def test_library_exports_every_declared_symbol(L):
@@ -100,6 +100,12 @@ def test_host_validation_rejects_bad_arguments_before_any_launch(L):
         b = _cache(**bad)
         assert lib.dflash_block_attn(0, 2, 8, 32, P(16), P(16), P(16), None, None, 1e6, 1e-6, ctypes.byref(b), 0, P(16), P(256), 1 << 30, None) == code, bad
     assert lib.dflash_block_attn(0, 2, 8, 32, P(16), P(16), P(16), None, None, 1e6, 1e-6, ctypes.byref(ok), 64, P(16), P(256), 1 << 30, None) == 2
+    # the bounded-wait probe: bf16 only, a limit of 1 .. 100000 us
+    assert lib.dflash_debug_block_attn_wait_timeout(2, 8, 32, ctypes.byref(c), P(16), P(256), 1 << 30, 0, None) == 1
+    assert lib.dflash_debug_block_attn_wait_timeout(2, 8, 32, ctypes.byref(c), P(16), P(256), 1 << 30, 200000, None) == 1
+    f = _cache(dtype=dfl.F32)
+    assert lib.dflash_debug_block_attn_wait_timeout(2, 8, 32, ctypes.byref(f), P(16), P(256), 1 << 30, 100, None) == 2
+    assert lib.dflash_debug_block_attn_wait_timeout(2, 8, 32, ctypes.byref(c), P(16), P(256), 8, 100, None) == 5
     # DFlash2: block convolution sizes and flags; top-m m, temperature, vocabulary and workspace
     assert lib.dflash_block_conv(P(16), 2, 17, 256, 3, P(16), None, 0, P(16), None) == 1
     assert lib.dflash_block_conv(P(16), 2, 8, 256, 9, P(16), None, 0, P(16), None) == 1

@@ -20,6 +20,8 @@ def test_reference_arm_prints_one_contract_line():
                 "scaling", "dtype", "data", "config"):
         assert key in d, key
     assert d["value"] > 0 and d["higher_is_better"] is True and d["steps"] == 3
+    # a step is one whole batch cycle: the step time and the cycle rate agree
+    assert abs(d["ms_per_step"] * d["value"] / 1e3 - 1.0) < 1e-6
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
