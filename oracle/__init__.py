@@ -28,6 +28,7 @@ from .dflash_oracle import (  # noqa: F401
     verify,
     VerifyResult,
     draft_head,
+    draft_layer_qkv,
     draft_layer_tail,
     silu,
     draft_race_uniforms,

@@ -436,6 +436,37 @@ def silu(z):
     return z / (1.0 + np.exp(-z))
 
 
+def draft_layer_qkv(x, g_in, w_qkv, batch, num_q_heads, num_kv_heads, head_dim=128, eps=1e-6, bf16=False):
+    """The start of one draft layer: its input RMSNorm and the block rows' q, k
+    and v projections (Qwen3-style layer, [E4B] "The parameter count exposes
+    the real cost": q/k/v/o projections and two RMSNorms per layer).
+
+    x [M, D] residual stream of the block rows (row b * bs + j, M = batch * bs),
+    g_in [D] the input norm's gain, w_qkv [(Hq + 2 Hkv) * hd, D] whose output
+    rows are the Hq query heads, then the Hkv key heads, then the Hkv value
+    heads, head h's element e at row h * hd + e:
+      h   = RMSNorm(x) * g_in
+      y   = h w_qkv^T
+      q[b, h, j, e]  = y[b*bs + j, h*hd + e]
+      kb[b, g, j, e] = y[b*bs + j, (Hq + g)*hd + e]
+      vb[b, g, j, e] = y[b*bs + j, (Hq + Hkv + g)*hd + e]
+    The per-head Q/K norms and RoPE belong to the block attention.  Returns
+    (q [B, Hq, bs, hd], kb [B, Hkv, bs, hd], vb [B, Hkv, bs, hd]).  bf16: the
+    normalised rows and the three outputs are stored as bfloat16.
+    """
+    rnd = round_to_bf16 if bf16 else (lambda v: v)
+    x = np.asarray(x, dtype=F64)
+    M = x.shape[0]
+    bs = M // batch
+    h = rnd(rms_norm(x, np.asarray(g_in, dtype=F64), eps))
+    y = h @ np.asarray(w_qkv, dtype=F64).T
+    heads = y.reshape(batch, bs, num_q_heads + 2 * num_kv_heads, head_dim).transpose(0, 2, 1, 3)
+    q = rnd(heads[:, :num_q_heads])
+    kb = rnd(heads[:, num_q_heads:num_q_heads + num_kv_heads])
+    vb = rnd(heads[:, num_q_heads + num_kv_heads:])
+    return q, kb, vb
+
+
 def draft_layer_tail(x, o, w_o, g_post, w_gate, w_up, w_down, eps=1e-6, bf16=False):
     """The rest of one draft layer after its attention (Qwen3-style layer,
     [E4B] "The parameter count exposes the real cost": q/k/v/o projections, a

@@ -126,3 +126,52 @@ def test_layer_tail_special_cases():
     # bf16 storage points
     x1b, x2b = oracle.draft_layer_tail(**c, bf16=True)
     np.testing.assert_array_equal(x2b, oracle.round_to_bf16(x2b))
+
+
+def test_layer_qkv_matches_loops():
+    """The input norm and the q/k/v projections, element by element: row
+    b * bs + j of x, query head h at output row h * hd + e of w_qkv, key head g
+    at (Hq + g) * hd + e, value head g at (Hq + Hkv + g) * hd + e."""
+    rng = np.random.default_rng(21)
+    B, bs, D, Hq, Hkv, hd = 2, 3, 8, 4, 2, 4
+    x = rng.normal(size=(B * bs, D)) * 2.0
+    g = 1 + 0.1 * rng.normal(size=D)
+    w = rng.normal(size=((Hq + 2 * Hkv) * hd, D))
+    q, kb, vb = oracle.draft_layer_qkv(x, g, w, B, Hq, Hkv, head_dim=hd, eps=1e-6)
+    assert q.shape == (B, Hq, bs, hd) and kb.shape == (B, Hkv, bs, hd) and vb.shape == (B, Hkv, bs, hd)
+    for b in range(B):
+        for j in range(bs):
+            row = x[b * bs + j]
+            r = (sum(v * v for v in row) / D + 1e-6) ** 0.5
+            h = [row[i] / r * g[i] for i in range(D)]
+            dot = lambda o: sum(h[i] * w[o, i] for i in range(D))  # noqa: E731
+            for e in range(hd):
+                for hh in range(Hq):
+                    assert abs(q[b, hh, j, e] - dot(hh * hd + e)) < 1e-10
+                for gg in range(Hkv):
+                    assert abs(kb[b, gg, j, e] - dot((Hq + gg) * hd + e)) < 1e-10
+                    assert abs(vb[b, gg, j, e] - dot((Hq + Hkv + gg) * hd + e)) < 1e-10
+
+
+def test_layer_qkv_selection_weights_place_each_head():
+    """A weight whose output row o reads input column pi(o) (a selection
+    matrix) puts the normalised row's column pi(o) at o's head position: this
+    catches a transposed layout or a wrong head order; zero weights give zero
+    heads; bf16 outputs are bfloat16 values."""
+    rng = np.random.default_rng(22)
+    B, bs, D, Hq, Hkv, hd = 2, 4, 16, 4, 2, 8
+    N = (Hq + 2 * Hkv) * hd
+    x = rng.normal(size=(B * bs, D))
+    pi = rng.integers(0, D, size=N)
+    w = np.zeros((N, D))
+    w[np.arange(N), pi] = 1.0
+    q, kb, vb = oracle.draft_layer_qkv(x, np.ones(D), w, B, Hq, Hkv, head_dim=hd, eps=0.0)
+    hn = x / np.sqrt(np.mean(x * x, axis=1, keepdims=True))
+    full = np.concatenate([q, kb, vb], axis=1)        # [B, Hq + 2 Hkv, bs, hd]
+    for o in range(N):
+        np.testing.assert_allclose(full[:, o // hd, :, o % hd], hn[:, pi[o]].reshape(B, bs), rtol=1e-12)
+    z = oracle.draft_layer_qkv(x, np.ones(D), np.zeros((N, D)), B, Hq, Hkv, head_dim=hd)
+    assert all(np.all(t == 0) for t in z)
+    qb, _, _ = oracle.draft_layer_qkv(x, 1 + 0.1 * rng.normal(size=D), rng.normal(size=(N, D)), B, Hq, Hkv,
+                                      head_dim=hd, bf16=True)
+    np.testing.assert_array_equal(qb, oracle.round_to_bf16(qb))
