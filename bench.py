@@ -291,6 +291,7 @@ def run_gpu(args):
         tensor_lines.update(draft_head_roofline(cyc, dev, peaks()[0]))
         tensor_lines.update(dflash2_roofline(cyc, dev, peaks()[0]))
         tensor_lines.update(layer_tail_roofline(cyc, dev, peaks()[0], peaks()[1]))
+        tensor_lines.update(full_drafter_cycle(cyc, dev, peaks()[0]))
 
     if rank != 0:
         return
@@ -518,6 +519,85 @@ def draft_head_roofline(cyc, dev, peak_gbs, iters=10):
     return {"draft_head": {"bound": "hbm", "achieved": gbs, "peak": peak_gbs, "unit": "GB/s", "frac": gbs / peak_gbs,
                            "ms_per_call": ms, "rows": M, "vocab": cfg.V, "temperature": cyc.T,
                            "tflops": 2.0 * M * cfg.V * cfg.D / (ms * 1e-3) / 1e12}}
+
+
+def full_drafter_cycle(cyc, dev, peak_gbs, iters=20):
+    """One whole draft-and-verify cycle with the drafter's own forward on the
+    batched workload, beside the headline cycle: context fusion of 8 new rows
+    per sequence; five layers of input norm + q/k/v projections, block
+    attention over the cache and the layer remainder (D = 2560, 32/8 heads,
+    MLP 5120); the head (final norm, LM head over V = 262144, draft race) on
+    the 7 mask rows of each sequence; verification of the head's own draft
+    tokens and logits against the target logits.  Synthetic weights; the
+    block's input rows are copied in fresh each cycle.  Algorithmic bytes:
+    every weight read once, the cache rows attended, the logits written by
+    the head and read by verification, the target logits read.  Steps run back
+    to back; CUDA events around them; 3 warm-up cycles."""
+    import block_speculative_decoding_gb300 as dfl
+    cfg = cyc.cfg
+    M, D, I, Hq, Hkv, V, R = cfg.B * cfg.bs, cfg.D, cfg.mlp_dim, cfg.Hq, cfg.Hkv, cfg.V, cfg.bs - 1
+    g = workloads.generator(cfg.seed * 1000 + 31, dev)
+    r = lambda *s, std=0.02: (torch.randn(*s, generator=g, device=dev) * std).to(torch.bfloat16)  # noqa: E731
+    gain = lambda *s: (1 + 0.1 * torch.randn(*s, generator=g, device=dev)).to(torch.bfloat16)  # noqa: E731
+    g_in, w_qkv = gain(cfg.L, D), r(cfg.L, (Hq + 2 * Hkv) * 128, D)
+    w_o, g_post, w_gu, w_dn = r(cfg.L, D, Hq * 128), gain(cfg.L, D), r(cfg.L, 2 * I, D), r(cfg.L, D, I)
+    g_final, w_head = gain(D), r(V, D, std=0.05)
+    x0 = r(M, D, std=1.0)
+    x = torch.empty_like(x0)
+    mask_rows = torch.tensor([b * cfg.bs + j for b in range(cfg.B) for j in range(1, cfg.bs)], device=dev)
+    xh = torch.empty(cfg.B * R, D, dtype=torch.bfloat16, device=dev)
+    q, kb, vb = (torch.empty(cfg.B, h, cfg.bs, 128, dtype=torch.bfloat16, device=dev) for h in (Hq, Hkv, Hkv))
+    o = torch.empty_like(q)
+    logits = torch.empty(cfg.B * R, V, dtype=torch.bfloat16, device=dev)
+    tok = torch.empty(cfg.B * R, dtype=torch.int32, device=dev)
+    ws = lambda n: torch.empty(n, dtype=torch.uint8, device=dev)  # noqa: E731
+    ws_q = ws(dfl.draft_layer_qkv_workspace_size(cfg.B, cfg.bs, Hq, Hkv, D))
+    ws_t = ws(dfl.draft_layer_tail_workspace_size(cfg.B, cfg.bs, Hq, D, I))
+    ws_h = ws(dfl.draft_head_workspace_size(cfg.B, R, D, V))
+    st = torch.cuda.Stream(device=dev)
+
+    def step(c):
+        dfl.fuse_context(cyc.taps, cyc.cu, cyc.w.w_fuse, cyc.w.g_fuse, cyc.w.w_kv, cyc.w.k_gain, cyc.cache,
+                         workspace=cyc.ws_f, stream=st)
+        x.copy_(x0)                                   # the block's input rows of this cycle
+        for l in range(cfg.L):
+            dfl.draft_layer_qkv(x, g_in[l], w_qkv[l], cfg.B, Hq, Hkv, q=q, kb=kb, vb=vb, workspace=ws_q, stream=st)
+            dfl.block_attn(l, q, kb, vb, cyc.w.q_gain[l], cyc.w.k_gain[l], cyc.cache, out=o, workspace=cyc.ws_a,
+                           stream=st)
+            dfl.draft_layer_tail(x, o, w_o[l], g_post[l], w_gu[l], w_dn[l], workspace=ws_t, stream=st)
+        torch.index_select(x, 0, mask_rows, out=xh)   # the 7 mask rows of each sequence
+        dfl.draft_head(xh, g_final, w_head, R, cyc.T, 1234, c, logits=logits, tokens=tok, workspace=ws_h, stream=st)
+        dfl.verify(cyc.lt, logits.view(cfg.B, R, V), tok.view(cfg.B, R), cyc.T, 1234, c, accepted_len=cyc.acc,
+                   out_tokens=cyc.tok, workspace=cyc.ws_v, stream=st)
+
+    with torch.cuda.stream(st):
+        for c in range(3):
+            step(c)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for c in range(iters):
+            step(c)
+        e1.record(st)
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / iters
+    tokens = float((cyc.acc.cpu() + 1).sum())
+    weights = (cyc.w.w_fuse.numel() + cyc.w.w_kv.numel() + w_qkv.numel() + w_o.numel() + w_gu.numel() +
+               w_dn.numel() + w_head.numel()) * 2
+    nbytes = weights + cfg.L * cyc.attn_bytes_per_call + 2 * cfg.B * R * V * 2 + cfg.B * cfg.bs * V * 2
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    launches = (4 + 3 * cfg.L + 2) + cfg.L * 3 + cfg.L * 6 + 3
+    del w_qkv, w_o, w_gu, w_dn, w_head, logits, ws_q, ws_t, ws_h
+    torch.cuda.empty_cache()
+    return {"full_drafter_cycle": {
+        "bound": "hbm", "achieved": gbs, "peak": peak_gbs, "unit": "GB/s", "frac": gbs / peak_gbs,
+        "ms_per_cycle": ms, "cycles_per_sec": 1e3 / ms, "tokens_per_sec": tokens * 1e3 / ms,
+        "algorithmic_bytes": nbytes, "gpu_launches_per_cycle": launches,
+        "note": "fusion + 5 x (q/k/v + block attention + layer remainder) + head (7 mask rows per sequence, "
+                "V=262144) + verification of the head's own draft; synthetic weights, so the acceptance (and "
+                "tokens_per_sec) is that of a random drafter against synthetic target logits; the mask rows are "
+                "gathered with torch.index_select (1.1 MB) and the block's input rows copied in with torch each "
+                "cycle"}}
 
 
 def layer_tail_roofline(cyc, dev, peak_gbs, peak_tflops, iters=20):

@@ -20,7 +20,7 @@ import torch
 
 __all__ = [
     "KVCache", "DFlashError", "lib", "fuse_context", "block_attn", "verify", "draft_head", "draft_layer_tail",
-    "interleave_gate_up", "draft_layer_tail_workspace_size",
+    "interleave_gate_up", "draft_layer_tail_workspace_size", "draft_layer_qkv", "draft_layer_qkv_workspace_size",
     "fuse_context_workspace_size", "block_attn_workspace_size", "verify_workspace_size", "draft_head_workspace_size",
     "philox4x32_10", "read_device_status", "debug_block_attn_wait_timeout", "version", "LIB_PATH",
     "DEV_CAPACITY", "DEV_BAD_TOKEN", "DEV_BAD_SEQLEN", "DEV_TIMEOUT",
@@ -82,6 +82,10 @@ def lib():
     L.dflash_draft_head_workspace_size.restype = sz
     L.dflash_draft_head.argtypes = [vp, i32, i32, i32, vp, f32, vp, i32, f32, u64, u64, vp, vp, vp, sz, vp]
     L.dflash_draft_head.restype = i32
+    L.dflash_draft_layer_qkv_workspace_size.argtypes = [i32] * 5
+    L.dflash_draft_layer_qkv_workspace_size.restype = sz
+    L.dflash_draft_layer_qkv.argtypes = [vp, i32, i32, i32, i32, i32, vp, f32, vp, vp, vp, vp, vp, sz, vp]
+    L.dflash_draft_layer_qkv.restype = i32
     L.dflash_draft_layer_tail_workspace_size.argtypes = [i32] * 5
     L.dflash_draft_layer_tail_workspace_size.restype = sz
     L.dflash_draft_layer_tail.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, f32, vp, sz, vp]
@@ -259,6 +263,30 @@ def verify(target_logits, draft_logits, draft_tokens, temperature, seed, cycle, 
                                float(temperature), int(seed), int(cycle), _ptr(accepted_len),
                                _ptr(out_tokens), _ptr(ws), nbytes, _stream(stream)))
     return accepted_len, out_tokens
+
+
+def draft_layer_qkv_workspace_size(B, bs, Hq, Hkv, D):
+    return lib().dflash_draft_layer_qkv_workspace_size(B, bs, Hq, Hkv, D)
+
+
+def draft_layer_qkv(x, g_in, w_qkv, batch, num_q_heads, num_kv_heads, eps=1e-6, q=None, kb=None, vb=None,
+                    workspace=None, stream=None):
+    """Input RMSNorm and q/k/v projections of the block rows x [B*bs, D];
+    returns (q [B, Hq, bs, 128], kb [B, Hkv, bs, 128], vb [B, Hkv, bs, 128])."""
+    M, D = x.shape
+    bs = M // batch
+    dev = x.device
+    if q is None:
+        q = torch.empty(batch, num_q_heads, bs, 128, dtype=x.dtype, device=dev)
+    if kb is None:
+        kb = torch.empty(batch, num_kv_heads, bs, 128, dtype=x.dtype, device=dev)
+    if vb is None:
+        vb = torch.empty(batch, num_kv_heads, bs, 128, dtype=x.dtype, device=dev)
+    nbytes = draft_layer_qkv_workspace_size(batch, bs, num_q_heads, num_kv_heads, D)
+    ws = _workspace(nbytes, dev, workspace)
+    _check(lib().dflash_draft_layer_qkv(_ptr(x), batch, bs, num_q_heads, num_kv_heads, D, _ptr(g_in), eps,
+                                        _ptr(w_qkv), _ptr(q), _ptr(kb), _ptr(vb), _ptr(ws), nbytes, _stream(stream)))
+    return q, kb, vb
 
 
 def interleave_gate_up(w_gate, w_up):

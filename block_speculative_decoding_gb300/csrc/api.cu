@@ -319,6 +319,37 @@ dflash_status dflash_debug_block_attn_wait_timeout(int batch, int block_size, in
                                         static_cast<cudaStream_t>(stream), dev);
 }
 
+// ------------------------------------------------------- draft layer qkv ----
+
+size_t dflash_draft_layer_qkv_workspace_size(int batch, int block_size, int num_q_heads, int num_kv_heads,
+                                             int d_model) {
+  if (batch < 1 || block_size < 1 || num_q_heads < 1 || num_kv_heads < 1 || d_model < 1) return 0;
+  return qkv_ws_bytes(batch * block_size, d_model, num_q_heads, num_kv_heads);
+}
+
+dflash_status dflash_draft_layer_qkv(const void* x, int batch, int block_size, int num_q_heads, int num_kv_heads,
+                                     int d_model, const void* g_in, float eps, const void* w_qkv, void* q, void* kb,
+                                     void* vb, void* workspace, size_t workspace_bytes, void* stream) {
+  if (batch < 0 || block_size < 1 || num_q_heads < 1 || num_kv_heads < 1 || d_model < 1)
+    return fail(DFLASH_ERR_INVALID_ARGUMENT, "need batch >= 0 and positive sizes");
+  if (batch == 0) return DFLASH_OK;
+  if (d_model % 128 || d_model > 4096)
+    return fail(DFLASH_ERR_UNSUPPORTED, "layer q/k/v needs d_model % 128 == 0 and d_model <= 4096");
+  if (!(eps >= 0.0f)) return fail(DFLASH_ERR_INVALID_ARGUMENT, "eps must be >= 0");
+  if (!x || !w_qkv || !q || !kb || !vb) return fail(DFLASH_ERR_INVALID_ARGUMENT, "NULL x/w_qkv/q/kb/vb");
+  if (!aligned16(x) || !aligned16(w_qkv) || !aligned16(q) || !aligned16(kb) || !aligned16(vb) ||
+      (g_in && !aligned16(g_in)))
+    return fail(DFLASH_ERR_INVALID_ARGUMENT, "pointers must be 16-byte aligned");
+  const size_t need = qkv_ws_bytes(batch * block_size, d_model, num_q_heads, num_kv_heads);
+  dflash_status s = check_ws(workspace, workspace_bytes, need);
+  if (s) return s;
+  DeviceInfo dev;
+  s = device_info(&dev);
+  if (s) return s;
+  return launch_layer_qkv(x, batch, block_size, d_model, num_q_heads, num_kv_heads, g_in, eps, w_qkv, q, kb, vb,
+                          workspace, static_cast<cudaStream_t>(stream), dev);
+}
+
 // ------------------------------------------------------ draft layer tail ----
 
 size_t dflash_draft_layer_tail_workspace_size(int batch, int block_size, int num_q_heads, int d_model,

@@ -99,6 +99,11 @@ dflash_status launch_layer_tail(void* x, const void* attn_out, int B, int bs, in
                                 const void* g_post, const void* w_gate_up, const void* w_down, float eps, void* ws,
                                 cudaStream_t st, const DeviceInfo& dev);
 
+size_t qkv_ws_bytes(int M, int D, int Hq, int Hkv);
+dflash_status launch_layer_qkv(const void* x, int B, int bs, int D, int Hq, int Hkv, const void* g_in, float eps,
+                               const void* w_qkv, void* q, void* kb, void* vb, void* ws, cudaStream_t st,
+                               const DeviceInfo& dev);
+
 // --- DFlash2 variants ----------------------------------------------------------
 dflash_status launch_block_conv(const void* h, int B, int bs, int D, int k, const void* w, const void* bias,
                                 int residual, void* out, cudaStream_t st);

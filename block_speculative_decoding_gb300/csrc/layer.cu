@@ -1,4 +1,5 @@
-// The rest of a draft layer after its attention: output projection and
+// A draft layer around its attention: before it, the input RMSNorm and the
+// block rows' q/k/v projections; after it, the output projection and
 // residual, post-attention RMSNorm, SwiGLU MLP and residual.
 //
 // Pages: "Nemotron 3.5 Bolt E4B: Block-Parallel Speculation with DFlash",
@@ -22,6 +23,13 @@
 //                hide the latency of this work; a full grid can)
 //   5. gemm_tc   Y = act W_down^T, split K -> slots
 //   6. resnorm   x2 = bf16(x1 + sum of the slots) -> x
+//
+// The q/k/v projections, three launches:
+//   1. resnorm   h = bf16(RMSNorm(x) * g_in) (no slots; x left as it is)
+//   2. gemm_tc   [q | k | v] = h W_qkv^T, stream-K over all SMs -> fp32 slots;
+//                a 128-column tile is one head
+//   3. qkv_scatter  the sum of each tile's slots, rounded to bf16 and stored
+//                in the block attention's [B][heads][bs][128] layouts
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -40,12 +48,13 @@ constexpr int kResSlots = 2;      // float4 of the row per thread: rows up to 40
 constexpr int kMaxKSplits = 16;   // partial sums per output (split-K slots)
 constexpr int kResBatch = 8;      // slots loaded together
 
-// One CTA per row m: x1 = bf16(x + sum_s part[s]) (written to x); with g_mode,
+// One CTA per row m: x1 = bf16(x + sum_s part[s]) (written to x if write_x); with g_mode,
 // h = bf16(x1 * rsqrt(mean(x1^2) + eps) * g), g == nullptr meaning ones.
 // Each thread owns kResSlots float4 of the row and requests up to kResBatch
 // slots of each before adding any, so its loads are in flight together.
 __global__ void __launch_bounds__(kResMaxThreads) resnorm_kernel(const float* __restrict__ part, int k_splits, int M,
-                                                                int D, __nv_bfloat16* __restrict__ x, int g_mode,
+                                                                int D, __nv_bfloat16* __restrict__ x, int write_x,
+                                                                int g_mode,
                                                                 const __nv_bfloat16* __restrict__ g, float eps,
                                                                 __nv_bfloat16* __restrict__ h,
                                                                 int* __restrict__ zero_flags, int n_zero) {
@@ -110,7 +119,7 @@ __global__ void __launch_bounds__(kResMaxThreads) resnorm_kernel(const float* __
     if (v < nv) {
       const uint32_t lo = pack_bf16x2(bf16_lo(xv[i].x) + t[i].x, bf16_hi(xv[i].x) + t[i].y);
       const uint32_t hi = pack_bf16x2(bf16_lo(xv[i].y) + t[i].z, bf16_hi(xv[i].y) + t[i].w);
-      xr[v] = make_uint2(lo, hi);
+      if (write_x) xr[v] = make_uint2(lo, hi);
       y[i] = make_float4(bf16_lo(lo), bf16_hi(lo), bf16_lo(hi), bf16_hi(hi));  // the stored x1
       ss += y[i].x * y[i].x + y[i].y * y[i].y + y[i].z * y[i].z + y[i].w * y[i].w;
     }
@@ -204,6 +213,67 @@ __global__ void __launch_bounds__(256) swiglu_kernel(const float* __restrict__ p
       make_uint2(pack_bf16x2(silu(a.x) * b.x, silu(a.y) * b.y), pack_bf16x2(silu(a.z) * b.z, silu(a.w) * b.w));
 }
 
+// q/k/v of the block rows from the projection's stream-K partial sums: one
+// thread per four consecutive outputs of a row (a warp covers one 128-wide
+// head row, 256 contiguous bytes stored); 128-column tile t of the GEMM output
+// is head t: query heads first, then key heads, then value heads.  The first
+// kMaxQkvSlots slots are requested together whatever the tile's slot count
+// (unused ones are masked out), then the lines are dropped from L2.
+constexpr int kMaxQkvSlots = 4;
+
+__global__ void __launch_bounds__(256) qkv_scatter_kernel(const float* __restrict__ part, int slots,
+                                                          const int* __restrict__ pieces, int tile_rows, int M,
+                                                          int bs, int Hq, int Hkv, __nv_bfloat16* __restrict__ q,
+                                                          __nv_bfloat16* __restrict__ kb,
+                                                          __nv_bfloat16* __restrict__ vb) {
+  pdl_wait_primary();  // the partial sums of the projection
+  pdl_launch_dependents();
+  const int heads = Hq + 2 * Hkv;
+  const int q4 = heads * 32;  // four outputs per thread
+  const long t = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= static_cast<long>(M) * q4) return;
+  const int m = static_cast<int>(t / q4), c = static_cast<int>(t % q4) * 4;
+  const int head = c / 128, e = c % 128;
+  const size_t N = static_cast<size_t>(heads) * 128;
+  const size_t slot = static_cast<size_t>(M) * N;
+  const float* src = part + static_cast<size_t>(m) * N + c;
+  const int ns = pieces[(m / tile_rows) * heads + head];
+  float4 u[kMaxQkvSlots];
+#pragma unroll
+  for (int k = 0; k < kMaxQkvSlots; ++k) {
+    u[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (k < slots) u[k] = __ldcg(reinterpret_cast<const float4*>(src + k * slot));
+  }
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int k = 0; k < kMaxQkvSlots; ++k)
+    if (k < ns) {
+      a.x += u[k].x; a.y += u[k].y; a.z += u[k].z; a.w += u[k].w;
+    }
+  for (int k = kMaxQkvSlots; k < ns; ++k) {  // more slots than kept in registers
+    const float4 x = __ldcg(reinterpret_cast<const float4*>(src + k * slot));
+    a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
+  }
+  // a 128-byte line of a slot is read by eight consecutive threads of this
+  // warp, for the last time: the first of them drops it from L2
+  if ((t | 31) < static_cast<long>(M) * q4) {
+    __syncwarp();
+    if (e % 32 == 0) {
+      const int nread = max(ns, min(slots, kMaxQkvSlots));
+      for (int k = 0; k < nread; ++k) discard_l2_line(src + k * slot);
+    }
+  }
+  const int b = m / bs, j = m % bs;
+  __nv_bfloat16* dst;
+  if (head < Hq)
+    dst = q + ((static_cast<size_t>(b) * Hq + head) * bs + j) * 128;
+  else if (head < Hq + Hkv)
+    dst = kb + ((static_cast<size_t>(b) * Hkv + (head - Hq)) * bs + j) * 128;
+  else
+    dst = vb + ((static_cast<size_t>(b) * Hkv + (head - Hq - Hkv)) * bs + j) * 128;
+  reinterpret_cast<uint2*>(dst + e)[0] = make_uint2(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w));
+}
+
 struct TailPlan {
   int mt, m_tiles, ks_o, ks_down;
   int gu_shares, gu_slots;  // gate/up: stream-K over gu_shares CTAs into gu_slots slots
@@ -222,7 +292,7 @@ TailPlan tail_plan(int M, int D, int Kq, int I) {
   return t;
 }
 
-dflash_status launch_resnorm(const float* part, int k_splits, int M, int D, __nv_bfloat16* x, int g_mode,
+dflash_status launch_resnorm(const float* part, int k_splits, int M, int D, __nv_bfloat16* x, int write_x, int g_mode,
                              const __nv_bfloat16* g, float eps, __nv_bfloat16* h, int* zero_flags, int n_zero,
                              cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
@@ -235,8 +305,8 @@ dflash_status launch_resnorm(const float* part, int k_splits, int M, int D, __nv
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, resnorm_kernel, part, k_splits, M, D, x, g_mode, g, eps, h, zero_flags,
-                                     n_zero);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, resnorm_kernel, part, k_splits, M, D, x, write_x, g_mode, g, eps, h,
+                                     zero_flags, n_zero);
   return e == cudaSuccess ? DFLASH_OK : cuda_fail(e, "resnorm_kernel launch");
 }
 
@@ -302,7 +372,7 @@ dflash_status launch_layer_tail(void* x, const void* attn_out, int B, int bs, in
   s = t.mt == 2 ? run_gemm<2>(am, bm, a, st, dev) : run_gemm<1>(am, bm, a, st, dev);
   if (s) return s;
   // 2. residual + post-attention norm
-  s = launch_resnorm(part, t.ks_o, M, D, xb, 1, static_cast<const __nv_bfloat16*>(g_post), eps, h, nullptr, 0, st);
+  s = launch_resnorm(part, t.ks_o, M, D, xb, 1, 1, static_cast<const __nv_bfloat16*>(g_post), eps, h, nullptr, 0, st);
   if (s) return s;
   // 3. gate/up with SwiGLU
   TmapPack hm{};
@@ -367,7 +437,85 @@ dflash_status launch_layer_tail(void* x, const void* attn_out, int B, int bs, in
   s = t.mt == 2 ? run_gemm<2>(xm, dm, dn, st, dev) : run_gemm<1>(xm, dm, dn, st, dev);
   if (s) return s;
   // 5. residual
-  return launch_resnorm(part, t.ks_down, M, D, xb, 0, nullptr, eps, nullptr, nullptr, 0, st);
+  return launch_resnorm(part, t.ks_down, M, D, xb, 1, 0, nullptr, eps, nullptr, nullptr, 0, st);
+}
+
+struct QkvPlan {
+  int mt, m_tiles, heads, shares, slots;
+};
+
+QkvPlan qkv_plan(int M, int D, int Hq, int Hkv) {
+  QkvPlan p;
+  p.mt = M <= 2 * kBM ? 2 : 1;
+  p.m_tiles = (M + p.mt * kBM - 1) / (p.mt * kBM);
+  p.heads = Hq + 2 * Hkv;
+  p.shares = fixup_shares(p.m_tiles * p.heads, D / kBK);
+  p.slots = sk_max_count(static_cast<long>(p.m_tiles) * p.heads, D / kBK, p.shares);
+  return p;
+}
+
+size_t qkv_ws_bytes(int M, int D, int Hq, int Hkv) {
+  const QkvPlan p = qkv_plan(M, D, Hq, Hkv);
+  return align256(static_cast<size_t>(p.slots) * M * p.heads * 128 * sizeof(float)) +
+         align256(static_cast<size_t>(p.m_tiles) * p.heads * sizeof(int)) +
+         align256(static_cast<size_t>(M) * D * sizeof(__nv_bfloat16)) + 256;
+}
+
+dflash_status launch_layer_qkv(const void* x, int B, int bs, int D, int Hq, int Hkv, const void* g_in, float eps,
+                               const void* w_qkv, void* q, void* kb, void* vb, void* ws, cudaStream_t st,
+                               const DeviceInfo& dev) {
+  const int M = B * bs;
+  const QkvPlan pl = qkv_plan(M, D, Hq, Hkv);
+  const int N = pl.heads * 128;
+  WsCarver w(ws);
+  float* part = w.take<float>(static_cast<size_t>(pl.slots) * M * N);
+  int* pieces = w.take<int>(static_cast<size_t>(pl.m_tiles) * pl.heads);
+  auto* h = w.take<__nv_bfloat16>(static_cast<size_t>(M) * D);
+  // 1. input norm: h = bf16(RMSNorm(x) * g_in); x is only read
+  dflash_status s = launch_resnorm(nullptr, 0, M, D, const_cast<__nv_bfloat16*>(static_cast<const __nv_bfloat16*>(x)),
+                                   0, 1, static_cast<const __nv_bfloat16*>(g_in), eps, h, nullptr, 0, st);
+  if (s) return s;
+  // 2. the projections, stream-K into slots
+  TmapPack hm{};
+  s = make_tmap_bf16_2d(&hm.a[0], h, static_cast<uint64_t>(M), D, kBM, kBK);
+  if (s) return s;
+  CUtensorMap wm;
+  s = make_tmap_bf16_2d(&wm, w_qkv, static_cast<uint64_t>(N), D, 128, kBK);
+  if (s) return s;
+  GemmArgs a{};
+  a.M = M;
+  a.N = N;
+  a.num_kb = D / kBK;
+  a.kb_per_seg = a.num_kb;
+  a.m_tiles = pl.m_tiles;
+  a.n_tiles = pl.heads;
+  a.epi = 0;
+  a.stream_k = pl.shares;
+  a.dp_tiles = 0;
+  a.k_splits = pl.slots;
+  a.pieces = pieces;
+  a.out_f32 = part;
+  a.pdl = 1;
+  a.prefetch_b = 1;  // the weights, which no kernel of the chain writes, before the wait
+  a.status = dev.status;
+  s = pl.mt == 2 ? run_gemm<2>(hm, wm, a, st, dev) : run_gemm<1>(hm, wm, a, st, dev);
+  if (s) return s;
+  // 3. the heads into the block attention's layouts
+  cudaLaunchConfig_t cfg = {};
+  const long threads = static_cast<long>(M) * pl.heads * 32;
+  cfg.gridDim = dim3(static_cast<unsigned>((threads + 255) / 256));
+  cfg.blockDim = dim3(256);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, qkv_scatter_kernel, static_cast<const float*>(part), pl.slots,
+                                     static_cast<const int*>(pieces), pl.mt * kBM, M, bs, Hq, Hkv,
+                                     static_cast<__nv_bfloat16*>(q), static_cast<__nv_bfloat16*>(kb),
+                                     static_cast<__nv_bfloat16*>(vb));
+  return e == cudaSuccess ? DFLASH_OK : cuda_fail(e, "qkv_scatter_kernel launch");
 }
 
 }  // namespace dflash

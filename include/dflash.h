@@ -329,6 +329,35 @@ DFLASH_API dflash_status dflash_draft_topm(const void* logits, int batch, int ro
                                            size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * 5a. The start of a draft layer, before its attention (E4B page "The
+ *    parameter count exposes the real cost": a Qwen3-style layer with q/k/v/o
+ *    projections and two RMSNorms; "The released serving cycle": the drafter
+ *    runs its layers over the block):
+ *      h = RMSNorm(x) * g_in;  [q | k | v] = h W_qkv^T
+ *
+ *  x          : [batch * block_size, d_model] bf16 residual stream of the
+ *               block rows (row b * block_size + j); only read
+ *  g_in       : [d_model] the layer's input RMSNorm gain (NULL = ones)
+ *  w_qkv      : [(num_q_heads + 2 * num_kv_heads) * 128, d_model] bf16: output
+ *               rows h * 128 + e are query head h, then key heads, then value
+ *               heads (element e of head g at row (num_q_heads + g) * 128 + e
+ *               for keys, (num_q_heads + num_kv_heads + g) * 128 + e for values)
+ *  q          : [batch, num_q_heads, block_size, 128] bf16 (dflash_block_attn's q)
+ *  kb, vb     : [batch, num_kv_heads, block_size, 128] bf16 (its kb and vb)
+ * The per-head Q/K RMSNorm and RoPE are dflash_block_attn's.  bf16 storage
+ * points: the normalised rows and the three outputs.
+ * Constraints: bf16; d_model % 128 == 0 and <= 4096; all pointers 16-byte
+ *              aligned; workspace of dflash_draft_layer_qkv_workspace_size().
+ * ------------------------------------------------------------------------- */
+DFLASH_API size_t dflash_draft_layer_qkv_workspace_size(int batch, int block_size, int num_q_heads,
+                                                       int num_kv_heads, int d_model);
+
+DFLASH_API dflash_status dflash_draft_layer_qkv(const void* x, int batch, int block_size, int num_q_heads,
+                                                int num_kv_heads, int d_model, const void* g_in, float eps,
+                                                const void* w_qkv, void* q, void* kb, void* vb, void* workspace,
+                                                size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * 5. The rest of a draft layer after its attention (E4B page "The parameter
  *    count exposes the real cost": a Qwen3-style layer, gated MLP of
  *    intermediate size 5120):

@@ -556,7 +556,8 @@ def draft_sample(logits, temperature, seed, cycle, seq_ids=None, row_ids=None):
             key = z[b, k].copy()
             if T > 0.0:
                 u = draft_race_uniforms(seed, cycle, ids[b], kid[k], V)
-                key = key / T - np.log(-np.log(u))
+                with np.errstate(divide="ignore"):  # U = 1: E = 0 and the key is +inf (that index wins)
+                    key = key / T - np.log(-np.log(u))
             y = int(np.argmax(key))  # first maximum = lowest index
             tok[b, k] = y
             if V > 1:

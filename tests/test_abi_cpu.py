@@ -28,7 +28,7 @@ def test_header_declares_the_three_calls():
     syms = declared_symbols()
     for s in ("dflash_fuse_context", "dflash_block_attn", "dflash_verify"):
         assert s in syms
-    assert len(syms) == 20
+    assert len(syms) == 22
 
 
 def test_library_exports_every_declared_symbol(L):
@@ -100,6 +100,14 @@ def test_host_validation_rejects_bad_arguments_before_any_launch(L):
         b = _cache(**bad)
         assert lib.dflash_block_attn(0, 2, 8, 32, P(16), P(16), P(16), None, None, 1e6, 1e-6, ctypes.byref(b), 0, P(16), P(256), 1 << 30, None) == code, bad
     assert lib.dflash_block_attn(0, 2, 8, 32, P(16), P(16), P(16), None, None, 1e6, 1e-6, ctypes.byref(ok), 64, P(16), P(256), 1 << 30, None) == 2
+    # layer q/k/v: d_model multiple of 128 and <= 4096, alignment, workspace; empty batch is a no-op
+    assert lib.dflash_draft_layer_qkv(P(16), 2, 8, 32, 8, 2500, None, 1e-6, P(16), P(16), P(16), P(16), P(256), 1 << 30, None) == 2
+    assert lib.dflash_draft_layer_qkv(P(16), 2, 8, 32, 8, 8192, None, 1e-6, P(16), P(16), P(16), P(16), P(256), 1 << 30, None) == 2
+    assert lib.dflash_draft_layer_qkv(P(16), 2, 8, 32, 8, 2560, None, 1e-6, P(16), P(8), P(16), P(16), P(256), 1 << 30, None) == 1
+    assert lib.dflash_draft_layer_qkv(P(16), 2, 8, 32, 8, 2560, None, 1e-6, P(16), P(16), P(16), P(16), P(256), 8, None) == 5
+    assert lib.dflash_draft_layer_qkv(P(16), 2, 8, 32, 8, 2560, None, -1.0, P(16), P(16), P(16), P(16), P(256), 1 << 30, None) == 1
+    assert lib.dflash_draft_layer_qkv(None, 0, 8, 32, 8, 2560, None, 1e-6, None, None, None, None, None, 0, None) == 0
+    assert lib.dflash_draft_layer_qkv_workspace_size(32, 8, 32, 8, 2560) > 256 * 2560 * 2
     # the bounded-wait probe: bf16 only, a limit of 1 .. 100000 us
     assert lib.dflash_debug_block_attn_wait_timeout(2, 8, 32, ctypes.byref(c), P(16), P(256), 1 << 30, 0, None) == 1
     assert lib.dflash_debug_block_attn_wait_timeout(2, 8, 32, ctypes.byref(c), P(16), P(256), 1 << 30, 200000, None) == 1

@@ -1,4 +1,9 @@
-"""GPU parity of dflash_draft_layer_tail against the oracle.
+"""GPU parity of dflash_draft_layer_qkv and dflash_draft_layer_tail against the oracle.
+
+dflash_draft_layer_qkv: q, kb and vb (the input norm and the projections,
+bf16 storage of the normalised rows and of the outputs) within the relative
+bounds of the oracle's, for block sizes 4, 8, 16 on small shapes, the batched
+workload's shape (every row) and a 2048-row high-batch shape (sampled rows).
 
 The updated residual stream x2 must match the oracle's (bf16 storage of x1, the
 normalised rows, the SwiGLU activations and x2) within the relative Frobenius
@@ -65,3 +70,51 @@ def test_layer_tail_batched_shape_sampled():
                                      *[np64(c[k]) for k in ("w_o", "g_post", "w_gate", "w_up", "w_down")], bf16=True)
     got = x2[torch.as_tensor(rows, device=DEV)]
     assert_close(got, ref, torch.bfloat16, row=D, what="x2")
+
+
+def _qkv_case(B, bs, Hq, Hkv, D, seed, device="cpu"):
+    g = torch.Generator(device=device).manual_seed(seed)
+    x = (torch.randn(B * bs, D, generator=g, device=device) * 2.0).to(torch.bfloat16)
+    gain = (1 + 0.1 * torch.randn(D, generator=g, device=device)).to(torch.bfloat16)
+    w = (torch.randn((Hq + 2 * Hkv) * 128, D, generator=g, device=device) * 0.02).to(torch.bfloat16)
+    return x, gain, w
+
+
+def _check_qkv(x, gain, w, B, Hq, Hkv, seqs=None):
+    q, kb, vb = dfl.draft_layer_qkv(x, gain, w, B, Hq, Hkv)
+    torch.cuda.synchronize()
+    bs = x.shape[0] // B
+    seqs = np.arange(B) if seqs is None else np.asarray(seqs)
+    rows = (seqs[:, None] * bs + np.arange(bs)[None, :]).reshape(-1)
+    xs = x[torch.as_tensor(rows, device=x.device)]
+    rq, rk, rv = oracle.draft_layer_qkv(np64(xs), np64(gain), np64(w), len(seqs), Hq, Hkv, bf16=True)
+    sel = torch.as_tensor(seqs, device=x.device)
+    for got, ref, what in ((q[sel], rq, "q"), (kb[sel], rk, "kb"), (vb[sel], rv, "vb")):
+        assert_close(got, ref, torch.bfloat16, row=128, what=what)
+    return q, kb, vb
+
+
+@pytest.mark.parametrize("bs", [4, 8, 16])
+def test_layer_qkv_small(bs):
+    x, gain, w = _qkv_case(B=5, bs=bs, Hq=4, Hkv=2, D=256, seed=bs + 40)
+    _check_qkv(x.to(DEV), gain.to(DEV), w.to(DEV), 5, 4, 2)
+
+
+def test_layer_qkv_null_gain_means_ones():
+    x, gain, w = _qkv_case(B=3, bs=8, Hq=4, Hkv=2, D=256, seed=44)
+    q, kb, vb = dfl.draft_layer_qkv(x.to(DEV), None, w.to(DEV), 3, 4, 2)
+    q1, kb1, vb1 = dfl.draft_layer_qkv(x.to(DEV), torch.ones(256, dtype=torch.bfloat16, device=DEV), w.to(DEV), 3, 4, 2)
+    assert torch.equal(q, q1) and torch.equal(kb, kb1) and torch.equal(vb, vb1)
+
+
+def test_layer_qkv_batched_shape():
+    """B = 32 sequences x 8 block rows, D = 2560, 32 query and 8 KV heads (the
+    batched workload's drafter layer): every row checked."""
+    x, gain, w = _qkv_case(32, 8, 32, 8, 2560, seed=45, device=DEV)
+    _check_qkv(x, gain, w, 32, 32, 8)
+
+
+def test_layer_qkv_high_batch_shape_sampled():
+    """B = 128 x 16 block rows (2048 rows, 128-row units): sampled sequences."""
+    x, gain, w = _qkv_case(128, 16, 32, 8, 2560, seed=46, device=DEV)
+    _check_qkv(x, gain, w, 128, 32, 8, seqs=[0, 9, 64, 127])
