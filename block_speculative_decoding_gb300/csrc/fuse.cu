@@ -61,7 +61,7 @@ struct InvFreq {
 constexpr int kNormThreads = 256;     // fp32 path
 constexpr int kNormMaxThreads = 512;
 constexpr int kNormSlots = 2;        // float4 slots per thread (in registers up to 2 x the block)
-constexpr int kNormBatch = 8;        // split-K slots requested together
+constexpr int kNormBatch = 4;        // split-K slots requested together (more costs occupancy at large M)
 
 template <typename TG, typename TH>
 __global__ void __launch_bounds__(kNormMaxThreads) fuse_rownorm_kernel(
@@ -156,9 +156,9 @@ __global__ void __launch_bounds__(kNormMaxThreads) fuse_rownorm_kernel(
   const bool in_regs = nv <= nthr * kNormSlots;
   float4 y[kNormSlots];
   float ss = 0.f;
+  int ns[kNormSlots] = {};
   if (in_regs) {
     // slots outermost, so the loads of a thread's float4 slots are independent
-    int ns[kNormSlots];
     int ns_max = 0;
 #pragma unroll
     for (int i = 0; i < kNormSlots; ++i) {
@@ -206,11 +206,16 @@ __global__ void __launch_bounds__(kNormMaxThreads) fuse_rownorm_kernel(
   if (in_regs && sizeof(TH) == 2 && D % 32 == 0) {  // whole, aligned 128-byte lines per row
     // every thread's slot loads have returned (the barrier above): the row's
     // slot lines are read by this CTA only, drop them from L2 rather than let
-    // them be written back
-    const int lines = D / 32;  // 128-byte lines of one slot row
-    const float* pr = part + static_cast<size_t>(m) * D;
-    for (int i = threadIdx.x; i < k_splits * lines; i += nthr)
-      discard_l2_line(pr + (i / lines) * split_stride * 4 + (i % lines) * 32);
+    // them be written back.  A 128-byte line is eight float4 of eight
+    // consecutive threads of one warp; the first of them drops it, for the
+    // slots its tile has (stream-K tiles past the whole waves have many, the
+    // others one).
+#pragma unroll
+    for (int i = 0; i < kNormSlots; ++i) {
+      const int v = threadIdx.x + i * nthr;
+      if (v < nv && (v & 7) == 0)
+        for (int sl = 0; sl < ns[i]; ++sl) discard_l2_line(prow + sl * split_stride + v);
+    }
   }
   auto store = [&](int v, float4 t4) {
     const int e = 4 * v;
@@ -219,16 +224,22 @@ __global__ void __launch_bounds__(kNormMaxThreads) fuse_rownorm_kernel(
     const TH h0 = from_f32<TH>(t4.x * r * g0), h1 = from_f32<TH>(t4.y * r * g1);
     const TH h2 = from_f32<TH>(t4.z * r * g2), h3 = from_f32<TH>(t4.w * r * g3);
     TH* d = ht + static_cast<size_t>(m) * D + e;
-    d[0] = h0;
-    d[1] = h1;
-    d[2] = h2;
-    d[3] = h3;
-    if (ht_out) {
-      TH* o = ht_out + static_cast<size_t>(m) * D + e;
-      o[0] = h0;
-      o[1] = h1;
-      o[2] = h2;
-      o[3] = h3;
+    TH* o = ht_out ? ht_out + static_cast<size_t>(m) * D + e : nullptr;
+    if constexpr (sizeof(TH) == 2) {  // one 8-byte store per four values (e is a multiple of 4)
+      const uint2 pk = make_uint2(pack_bf16x2(to_f32<TH>(h0), to_f32<TH>(h1)), pack_bf16x2(to_f32<TH>(h2), to_f32<TH>(h3)));
+      *reinterpret_cast<uint2*>(d) = pk;
+      if (o) *reinterpret_cast<uint2*>(o) = pk;
+    } else {
+      d[0] = h0;
+      d[1] = h1;
+      d[2] = h2;
+      d[3] = h3;
+      if (o) {
+        o[0] = h0;
+        o[1] = h1;
+        o[2] = h2;
+        o[3] = h3;
+      }
     }
   };
   if (in_regs) {
