@@ -10,13 +10,15 @@
 //
 // bf16 path, launches chained as programmatic dependents:
 //   1. gemm_tc (fusion)  Y = [taps] W_c^T on tcgen05 tensor cores: a unit is
-//      MT x 128 rows by 128 columns of Y over a range of K blocks; TMA loads
+//      MT x 128 rows by BN columns of Y over a range of K blocks; TMA loads
 //      128x64 A tiles (taken from the tap that owns the K block -- the concat is
-//      never materialised) and the 128x64 W_c tile into a ring, one thread
-//      issues tcgen05.mma (M=128, N=128, K=16) into MT accumulators in tensor
-//      memory, four epilogue warps drain them.  A few new rows (M <= 256) take
-//      MT = 2, so each W_c tile is read once, and split K over ~one unit per
-//      SM; the fp32 partial sums stay in the workspace.
+//      never materialised) and the BNx64 W_c tile into a ring, one thread
+//      issues tcgen05.mma (M=128, N=BN, K=16) into MT accumulators in tensor
+//      memory, four epilogue warps drain them.  A few new rows (M <= 256):
+//      256 x 128 units, so each W_c tile is read once, split K over ~one unit
+//      per SM.  Up to ~3840 rows: 256 x 256 units, stream-K over the SMs;
+//      more rows: 128 x 256 units.  The fp32 partial sums stay in the
+//      workspace.
 //   2. rownorm           row -> (sequence, cache position) and its RoPE table
 //      (before waiting for the GEMM), then H_t = bf16(sum_splits(Y) *
 //      rsqrt(mean(Y^2) + eps) * g)
@@ -442,12 +444,16 @@ struct FusePlan {
 
 FusePlan plan(int M, int D, int num_kb, int n_kv) {
   FusePlan f;
-  f.fuse_mt = M <= 2 * kBM ? 2 : 1;
-  f.fuse_m_tiles = (M + f.fuse_mt * kBM - 1) / (f.fuse_mt * kBM);
   f.fuse_bn = M <= 2 * kBM ? 128 : 256;
   f.fuse_n_tiles = D / f.fuse_bn;
+  // 256-row units read each activation tile half as often; they fill all of
+  // tensor memory (no second accumulator to overlap an epilogue with the next
+  // unit), so they are taken only while every CTA has at most about one unit
+  const int m256 = (M + 2 * kBM - 1) / (2 * kBM);
+  f.fuse_mt = (M <= 2 * kBM || m256 * f.fuse_n_tiles <= kSplitTarget) ? 2 : 1;
+  f.fuse_m_tiles = (M + f.fuse_mt * kBM - 1) / (f.fuse_mt * kBM);
   const int tiles = f.fuse_m_tiles * f.fuse_n_tiles;
-  f.stream_k = f.fuse_mt == 1 && tiles % kSplitTarget != 0;
+  f.stream_k = M > 2 * kBM && tiles % kSplitTarget != 0;
   f.shares = 0;
   f.dp_tiles = 0;
   f.k_splits = std::max(1, std::min(16, kSplitTarget / std::max(1, tiles)));
@@ -574,7 +580,9 @@ dflash_status launch_fuse_context(int J, const void* const* taps, int dt_width, 
   a.prefetch_b = 1;  // the weights (which no kernel of the chain writes) before
   a.out_f32 = Ypart;
   a.status = dev.status;
-  s = f.fuse_mt == 2 ? launch_gemm<128, 4, 2>(am, bm, a, st, dev) : launch_gemm<256, 4, 1>(am, bm, a, st, dev);
+  s = f.fuse_bn == 128  ? launch_gemm<128, 4, 2>(am, bm, a, st, dev)
+      : f.fuse_mt == 2 ? launch_gemm<256, 3, 2>(am, bm, a, st, dev)
+                       : launch_gemm<256, 4, 1>(am, bm, a, st, dev);
   if (s) return s;
 
   // 2. row map + split-K sum + RMSNorm -> H_t (bf16), a programmatic dependent
