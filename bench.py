@@ -1029,9 +1029,13 @@ def run_profile(args):
     from types import SimpleNamespace
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
+    from __graft_entry__ import build
+    build()
     cyc = SimpleNamespace(cfg=workloads.BATCHED, T=args.temperature)
     hbm, tfl, _ = peaks()
-    if args.profile == "layer_tail":
+    if args.profile == "fusion_tensor":
+        line = fusion_tensor_rooflines(dev, tfl)
+    elif args.profile == "layer_tail":
         line = layer_tail_roofline(cyc, dev, hbm, tfl)
     elif args.profile == "dflash2":
         line = dflash2_roofline(cyc, dev, hbm)
@@ -1058,7 +1062,7 @@ def main():
                     help="profiling runs: time one component of the cycle only")
     ap.add_argument("--batch", type=int, default=None, help="profiling runs: smaller batch")
     ap.add_argument("--layers", type=int, default=None, help="profiling runs: fewer draft layers")
-    ap.add_argument("--profile", default=None, choices=["layer_tail", "draft_head", "dflash2"],
+    ap.add_argument("--profile", default=None, choices=["layer_tail", "draft_head", "dflash2", "fusion_tensor"],
                     help="profiling runs: only this call's roofline measurement on the batched workload")
     args = ap.parse_args()
     if args.profile:
