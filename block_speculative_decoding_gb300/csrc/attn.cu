@@ -116,6 +116,11 @@ __global__ void __launch_bounds__(kPrologueThreads) attn_prologue_kernel(
   // lengths before its own wait) is released only after that.
   pdl_wait_primary();
   pdl_launch_dependents();
+  q = pdl_fresh(q);
+  kb = pdl_fresh(kb);
+  qg = pdl_fresh(qg);
+  kg = pdl_fresh(kg);
+  seq_len = pdl_fresh(seq_len);
   if (blockIdx.x == 0 && counters)
     for (int i = threadIdx.x; i < n_counters; i += blockDim.x) counters[i] = 0;
   const int b = blockIdx.x / bs, j = blockIdx.x % bs;

@@ -410,6 +410,8 @@ __global__ void __launch_bounds__(512) topm_merge_kernel(const float4* __restric
                                                         float* __restrict__ score_out) {
   pdl_wait_primary();
   pdl_launch_dependents();
+  stats = pdl_fresh(stats);
+  cand = pdl_fresh(cand);
   const int b = blockIdx.x, warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   __shared__ float s_part[16];
   if (warp < R) {

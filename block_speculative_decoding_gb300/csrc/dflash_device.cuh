@@ -379,6 +379,17 @@ __device__ __forceinline__ void pdl_wait_primary() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// A pointer to memory that an earlier grid writes, passed through an empty asm
+// after pdl_wait_primary(): loads through the result depend on that asm and
+// cannot be scheduled before the wait.  Needed for const __restrict__ kernel
+// parameters, whose loads the compiler may otherwise treat as reading memory
+// that nothing changes during the kernel and move above the wait.
+template <typename T>
+__device__ __forceinline__ T* pdl_fresh(T* p) {
+  asm volatile("" : "+l"(p)::"memory");
+  return p;
+}
+
 // ---------------------------------------------------------------------------
 // warp-level mma.sync (bf16, m16n8k16) and ldmatrix
 // ---------------------------------------------------------------------------

@@ -134,6 +134,7 @@ __global__ void __launch_bounds__(kNormMaxThreads) fuse_rownorm_kernel(
   }
   pdl_launch_dependents();
   pdl_wait_primary();  // the partials of the fusion GEMM
+  pieces = pdl_fresh(pieces);
   // the fixup flags of the K/V GEMM that follows (every earlier grid has completed)
   if (m == 0)
     for (int i = threadIdx.x; i < n_zero; i += static_cast<int>(blockDim.x)) zero_flags[i] = 0;
@@ -350,6 +351,7 @@ __global__ void __launch_bounds__(256) kv_epilogue_kernel(
     __nv_bfloat16* __restrict__ cache_v) {
   pdl_wait_primary();  // the partial sums of the K/V GEMM
   pdl_launch_dependents();
+  pieces = pdl_fresh(pieces);
   const int heads = L * 2 * Hkv;
   const long wid = (static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
   const int lane = threadIdx.x % 32;

@@ -37,6 +37,8 @@ __global__ void __launch_bounds__(kHeadNormThreads) head_norm_kernel(const __nv_
                                                                     __nv_bfloat16* __restrict__ h) {
   pdl_wait_primary();  // a programmatic dependent of the preceding kernel: nothing is read before it completed
   pdl_launch_dependents();
+  x = pdl_fresh(x);
+  g = pdl_fresh(g);
   const int m = blockIdx.x;
   const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<size_t>(m) * D);
   const int nv = D / 8;
@@ -78,6 +80,7 @@ __global__ void __launch_bounds__(256) race_reduce_kernel(const float2* __restri
                                                           int32_t* __restrict__ tokens) {
   pdl_wait_primary();
   pdl_launch_dependents();
+  race = pdl_fresh(race);
   const int row = blockIdx.x * 8 + threadIdx.x / 32, lane = threadIdx.x % 32;
   if (row >= M) return;
   float best = -INFINITY;

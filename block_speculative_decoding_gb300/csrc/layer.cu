@@ -162,6 +162,7 @@ __global__ void __launch_bounds__(256) swiglu_kernel(const float* __restrict__ p
                                                      int M, int I, __nv_bfloat16* __restrict__ act) {
   pdl_wait_primary();  // the partial sums of the gate/up GEMM
   pdl_launch_dependents();
+  pieces = pdl_fresh(pieces);
   const long t = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int q4 = I / 4;
   if (t >= static_cast<long>(M) * q4) return;
@@ -228,6 +229,7 @@ __global__ void __launch_bounds__(256) qkv_scatter_kernel(const float* __restric
                                                           __nv_bfloat16* __restrict__ vb) {
   pdl_wait_primary();  // the partial sums of the projection
   pdl_launch_dependents();
+  pieces = pdl_fresh(pieces);
   const int heads = Hq + 2 * Hkv;
   const int q4 = heads * 32;  // four outputs per thread
   const long t = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x;

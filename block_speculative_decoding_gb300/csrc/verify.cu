@@ -42,7 +42,8 @@ constexpr int kThreads = 256;
 constexpr int kChunk = 16384;                 // logits per CTA chunk
 constexpr int kPerThread = kChunk / kThreads;  // 64 logits per thread
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kFinishChunks = 2;              // chunks per CTA of the finish kernel
+constexpr int kFinishChunks = 1;              // chunks per CTA of the finish kernel
+constexpr int kResidParts = 2;                // passes per warp over its residual segment
 constexpr int kSeg = 2048;                    // logits per residual-mass segment (one warp's share of a chunk)
 constexpr int kSegsPerChunk = kChunk / kSeg;
 
@@ -111,14 +112,15 @@ __device__ __forceinline__ void load_raw(const T* __restrict__ row, int e0, int 
   }
 }
 
-// Raw vectors of lane `lane`'s 64 logits of one warp's contiguous segment
-// [s0, s1): vector i covers elements s0 + (i*32 + lane)*VEC ...
-template <typename T, int VEC>
+// Raw vectors of lane `lane`'s N * VEC logits of one warp's contiguous span
+// starting at s0 (in-range below s1): vector i covers elements
+// s0 + (i*32 + lane)*VEC ...
+template <typename T, int VEC, int N>
 __device__ __forceinline__ void load_seg(const T* __restrict__ row, int s0, int s1, int lane,
-                                         typename Vec<T, VEC>::type (&v)[kPerThread / VEC], bool (&live)[kPerThread / VEC]) {
+                                         typename Vec<T, VEC>::type (&v)[N], bool (&live)[N]) {
   using VT = typename Vec<T, VEC>::type;
 #pragma unroll
-  for (int i = 0; i < kPerThread / VEC; ++i) {
+  for (int i = 0; i < N; ++i) {
     const int e = s0 + (i * 32 + lane) * VEC;
     live[i] = e < s1;
     if (live[i]) v[i] = __ldcg(reinterpret_cast<const VT*>(row + e));
@@ -278,11 +280,12 @@ __device__ __forceinline__ Decision decide_seq(const T* __restrict__ lt, const T
                                                uint32_t k0, uint32_t k1, uint32_t c_lo, uint32_t c_hi,
                                                int32_t* __restrict__ acc, int32_t* __restrict__ out,
                                                unsigned* status, const float* s_lz = nullptr,
-                                               const float2* pre = nullptr) {
+                                               const float2* pre = nullptr, const uint2* words = nullptr) {
   const int lane = threadIdx.x % 32;
   int xk = -1;
   if (lane < bs - 1) xk = x[b * (bs - 1) + lane];
-  // pre (optional): lane k's target and draft logits of its token, loaded earlier
+  // pre, words (optional): lane k's target and draft logits of its token and its
+  // two Philox words (acceptance, draw), computed earlier
   float lzp = 0.f, lzq = 0.f;
   int amax = 0;
   if constexpr (GREEDY) {
@@ -300,7 +303,14 @@ __device__ __forceinline__ Decision decide_seq(const T* __restrict__ lt, const T
   uint32_t vbits = 0;
   if (lane < bs) {
     uint4 w = make_uint4(0u, 0u, 0u, 0u);
-    if constexpr (!GREEDY) w = philox4x32_10(make_uint4(lane, b, c_lo, c_hi), k0, k1);
+    if constexpr (!GREEDY) {
+      if (words) {
+        w.x = words->x;
+        w.y = words->y;
+      } else {
+        w = philox4x32_10(make_uint4(lane, b, c_lo, c_hi), k0, k1);
+      }
+    }
     vbits = w.y;
     if (lane < bs - 1) {
       if (xk < 0 || xk >= V) {
@@ -365,9 +375,16 @@ __device__ __forceinline__ void row_normalisers(const float2* __restrict__ part,
   }
 }
 
+// Resident CTAs per SM of the finish kernel: four for 16-byte bf16 loads (64
+// registers), two where the wider live values would spill.
+template <typename T, int VEC>
+constexpr int finish_ctas_per_sm() {
+  return (sizeof(T) == 2 && VEC == 8) ? 4 : 2;
+}
+
 // Non-greedy verification after the stats pass; see the file comment.
 template <typename T, int VEC>
-__global__ void __launch_bounds__(kThreads, 2) verify_finish_kernel(
+__global__ void __launch_bounds__(kThreads, (finish_ctas_per_sm<T, VEC>())) verify_finish_kernel(
     const T* __restrict__ lt, const T* __restrict__ ld, const int32_t* __restrict__ x, int B, int bs, int V,
     int nchunk, float scale, const float2* __restrict__ part, uint32_t k0, uint32_t k1, uint32_t c_lo,
     uint32_t c_hi, int32_t* __restrict__ acc, int32_t* __restrict__ out, float2* __restrict__ rpart,
@@ -375,15 +392,22 @@ __global__ void __launch_bounds__(kThreads, 2) verify_finish_kernel(
   pdl_launch_dependents();  // a following call's first kernel may become resident; it waits for this grid
   const int ncb = (nchunk + kFinishChunks - 1) / kFinishChunks;  // CTAs per sequence
   const int b = blockIdx.x / ncb, cb = blockIdx.x % ncb;
-  // the draft tokens' logits do not depend on the stats pass: load them first
+  // the draft tokens' logits and the Philox words do not depend on the stats
+  // pass: fetch and draw them first
   float2 pre = make_float2(0.f, 0.f);
+  uint2 words = make_uint2(0u, 0u);
   if (threadIdx.x < bs - 1) {
     const int xk = x[b * (bs - 1) + threadIdx.x];
     if (xk >= 0 && xk < V)
       pre = make_float2(to_f32<T>(lt[static_cast<size_t>(b * bs + threadIdx.x) * V + xk]),
                         to_f32<T>(ld[static_cast<size_t>(b * (bs - 1) + threadIdx.x) * V + xk]));
   }
+  if (threadIdx.x < bs) {
+    const uint4 w = philox4x32_10(make_uint4(threadIdx.x, b, c_lo, c_hi), k0, k1);
+    words = make_uint2(w.x, w.y);
+  }
   pdl_wait_primary();  // the stats pass's partials and cleared counters
+  part = pdl_fresh(part);
   __shared__ Decision s_dec;
   __shared__ int s_is_last;
   __shared__ float s_lz[32];
@@ -391,7 +415,8 @@ __global__ void __launch_bounds__(kThreads, 2) verify_finish_kernel(
   __syncthreads();
   if (threadIdx.x < 32) {
     const Decision dw = decide_seq<T, false>(lt, ld, x, b, B, bs, V, nchunk, scale, part, k0, k1, c_lo, c_hi,
-                                             cb == 0 ? acc : nullptr, cb == 0 ? out : nullptr, status, s_lz, &pre);
+                                             cb == 0 ? acc : nullptr, cb == 0 ? out : nullptr, status, s_lz, &pre,
+                                             &words);
     if (threadIdx.x == 0) s_dec = dw;
   }
   __syncthreads();
@@ -402,27 +427,33 @@ __global__ void __launch_bounds__(kThreads, 2) verify_finish_kernel(
   const T* prow = lt + static_cast<size_t>(b * bs + d.n) * V;
   const T* qrow = has_q ? ld + static_cast<size_t>(b * (bs - 1) + d.n) * V : nullptr;
   for (int c = cb * kFinishChunks; c < min(nchunk, (cb + 1) * kFinishChunks); ++c) {
-    // masses of max(0, p - q) and of p over this warp's segment of row n
-    constexpr int NV = kPerThread / VEC;
+    // masses of max(0, p - q) and of p over this warp's segment of row n, in
+    // kResidParts passes: fewer live registers, so that four CTAs fit on an
+    // SM and the whole grid is resident at once
+    constexpr int NP = kPerThread / VEC / kResidParts;
     const int s0 = c * kChunk + warp * kSeg, s1 = min(V, s0 + kSeg);
-    typename Vec<T, VEC>::type vt[NV], vq[NV];
-    bool live[NV];
-    load_seg<T, VEC>(prow, s0, s1, lane, vt, live);
-    if (has_q) load_seg<T, VEC>(qrow, s0, s1, lane, vq, live);
     float sr = 0.f, sp = 0.f;
+#pragma unroll 1
+    for (int h = 0; h < kResidParts; ++h) {
+      typename Vec<T, VEC>::type vt[NP], vq[NP];
+      bool live[NP];
+      const int h0 = s0 + h * NP * 32 * VEC;
+      load_seg<T, VEC, NP>(prow, h0, s1, lane, vt, live);
+      if (has_q) load_seg<T, VEC, NP>(qrow, h0, s1, lane, vq, live);
 #pragma unroll
-    for (int i = 0; i < NV; ++i) {
-      if (!live[i]) continue;
-      float ft[VEC], fq[VEC];
-      Vec<T, VEC>::unpack(vt[i], ft);
-      if (has_q) Vec<T, VEC>::unpack(vq[i], fq);
+      for (int i = 0; i < NP; ++i) {
+        if (!live[i]) continue;
+        float ft[VEC], fq[VEC];
+        Vec<T, VEC>::unpack(vt[i], ft);
+        if (has_q) Vec<T, VEC>::unpack(vq[i], fq);
 #pragma unroll
-      for (int j = 0; j < VEC; ++j) {
-        if (ft[j] == -INFINITY) continue;  // a -inf logit: zero mass
-        float pw;
-        const float r = resid_weight(ft[j] * scale, has_q ? fq[j] * scale : 0.f, d, has_q, pw);
-        sr += r;
-        sp += pw;
+        for (int j = 0; j < VEC; ++j) {
+          if (ft[j] == -INFINITY) continue;  // a -inf logit: zero mass
+          float pw;
+          const float r = resid_weight(ft[j] * scale, has_q ? fq[j] * scale : 0.f, d, has_q, pw);
+          sr += r;
+          sp += pw;
+        }
       }
     }
     sr = warp_sum(sr);
@@ -449,11 +480,28 @@ __global__ void __launch_bounds__(kThreads, 2) verify_finish_kernel(
   const int nseg_live = (V + kSeg - 1) / kSeg;
   if (warp == 0) {
     const float2* rp = rpart + static_cast<size_t>(b) * nseg;
+    // Up to kKeep masses per lane stay in registers between the total and the
+    // scan (V up to 32 * kKeep * kSeg); longer rows read them again.
+    constexpr int kKeep = 8;
+    const bool kept = nseg_live <= 32 * kKeep;
+    float kr[kKeep], kp[kKeep];
     float sr = 0.f, sp = 0.f;
-    for (int g = lane; g < nseg_live; g += 32) {
-      const float2 v = __ldcg(rp + g);
-      sr += v.x;
-      sp += v.y;
+    if (kept) {
+#pragma unroll
+      for (int i = 0; i < kKeep; ++i) {
+        const int g = lane + 32 * i;
+        const float2 v = g < nseg_live ? __ldcg(rp + g) : make_float2(0.f, 0.f);
+        kr[i] = v.x;
+        kp[i] = v.y;
+        sr += v.x;
+        sp += v.y;
+      }
+    } else {
+      for (int g = lane; g < nseg_live; g += 32) {
+        const float2 v = __ldcg(rp + g);
+        sr += v.x;
+        sp += v.y;
+      }
     }
     sr = warp_sum(sr);
     sp = warp_sum(sp);
@@ -462,13 +510,8 @@ __global__ void __launch_bounds__(kThreads, 2) verify_finish_kernel(
     float before = 0.f;  // mass of the segments ahead of this group of 32
     int cs = -1, last_pos = -1;
     float excl_cs = 0.f, excl_last = 0.f;
-    for (int g0 = 0; g0 < nseg_live && cs < 0; g0 += 32) {
-      const int g = g0 + lane;
-      float w = 0.f;
-      if (g < nseg_live) {
-        const float2 v = __ldcg(rp + g);
-        w = use_p ? v.y : v.x;
-      }
+    // one group of 32 segments (lane: segment g0 + lane, mass w), in vocabulary order
+    auto group = [&](int g0, float w) {
       float inc = w;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -489,6 +532,21 @@ __global__ void __launch_bounds__(kThreads, 2) verify_finish_kernel(
         excl_last = __shfl_sync(0xffffffffu, ex, l);
       }
       before += __shfl_sync(0xffffffffu, inc, 31);
+    };
+    if (kept) {
+#pragma unroll
+      for (int i = 0; i < kKeep; ++i)
+        if (32 * i < nseg_live && cs < 0) group(32 * i, use_p ? kp[i] : kr[i]);
+    } else {
+      for (int g0 = 0; g0 < nseg_live && cs < 0; g0 += 32) {
+        const int g = g0 + lane;
+        float w = 0.f;
+        if (g < nseg_live) {
+          const float2 v = __ldcg(rp + g);
+          w = use_p ? v.y : v.x;
+        }
+        group(g0, w);
+      }
     }
     if (cs < 0) {  // rounding left the threshold at the very end
       cs = max(last_pos, 0);
