@@ -280,12 +280,13 @@ __device__ __forceinline__ Decision decide_seq(const T* __restrict__ lt, const T
                                                uint32_t k0, uint32_t k1, uint32_t c_lo, uint32_t c_hi,
                                                int32_t* __restrict__ acc, int32_t* __restrict__ out,
                                                unsigned* status, const float* s_lz = nullptr,
-                                               const float2* pre = nullptr, const uint2* words = nullptr) {
+                                               const float2* pre = nullptr, const uint2* words = nullptr,
+                                               const int* xk_pre = nullptr) {
   const int lane = threadIdx.x % 32;
   int xk = -1;
-  if (lane < bs - 1) xk = x[b * (bs - 1) + lane];
-  // pre, words (optional): lane k's target and draft logits of its token and its
-  // two Philox words (acceptance, draw), computed earlier
+  if (lane < bs - 1) xk = xk_pre ? *xk_pre : x[b * (bs - 1) + lane];
+  // pre, words, xk_pre (optional): lane k's target and draft logits of its
+  // token, its two Philox words (acceptance, draw) and its token, obtained earlier
   float lzp = 0.f, lzq = 0.f;
   int amax = 0;
   if constexpr (GREEDY) {
@@ -396,8 +397,9 @@ __global__ void __launch_bounds__(kThreads, (finish_ctas_per_sm<T, VEC>())) veri
   // pass: fetch and draw them first
   float2 pre = make_float2(0.f, 0.f);
   uint2 words = make_uint2(0u, 0u);
+  int xk = -1;
   if (threadIdx.x < bs - 1) {
-    const int xk = x[b * (bs - 1) + threadIdx.x];
+    xk = x[b * (bs - 1) + threadIdx.x];
     if (xk >= 0 && xk < V)
       pre = make_float2(to_f32<T>(lt[static_cast<size_t>(b * bs + threadIdx.x) * V + xk]),
                         to_f32<T>(ld[static_cast<size_t>(b * (bs - 1) + threadIdx.x) * V + xk]));
@@ -416,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, (finish_ctas_per_sm<T, VEC>())) veri
   if (threadIdx.x < 32) {
     const Decision dw = decide_seq<T, false>(lt, ld, x, b, B, bs, V, nchunk, scale, part, k0, k1, c_lo, c_hi,
                                              cb == 0 ? acc : nullptr, cb == 0 ? out : nullptr, status, s_lz, &pre,
-                                             &words);
+                                             &words, &xk);
     if (threadIdx.x == 0) s_dec = dw;
   }
   __syncthreads();
