@@ -111,8 +111,9 @@ def _full_size(cfg, layer, sample):
     w = workloads.weights(cfg, DEV)
     q, kb, vb = workloads.block(cfg, DEV, layer=layer)
     cache = dfl.KVCache(k, v, seq)
+    dfl.read_device_status()
     out = dfl.block_attn(0, q, kb, vb, w.q_gain[layer], w.k_gain[layer], cache)
-    torch.cuda.synchronize()
+    assert dfl.read_device_status() == 0  # no bounded wait gave up, no bad length
     sel = torch.tensor(sample)
     seq_c = seq.cpu()[sel]
     nmax = int(seq_c.max())
