@@ -71,7 +71,8 @@ __global__ void __launch_bounds__(kNormMaxThreads) fuse_rownorm_kernel(
     int n_tiles, int M, int D, const TG* __restrict__ g, float eps,
     TH* __restrict__ ht, TH* __restrict__ ht_out, const int32_t* __restrict__ cu_new,
     const int32_t* __restrict__ seq_len, int B, int cap, int ring, InvFreq inv, int2* __restrict__ rowinfo,
-    void* __restrict__ rope_cs, int* __restrict__ zero_flags, int n_zero, const int32_t* __restrict__ table,
+    void* __restrict__ rope_cs, int rope_row_major, int* __restrict__ zero_flags, int n_zero,
+    const int32_t* __restrict__ table,
     int max_pages, int page_size, int num_pages, unsigned* status) {
   const int m = blockIdx.x;
   // the row's sequence: the largest b with cu_new[b] <= m (cu_new is
@@ -109,7 +110,10 @@ __global__ void __launch_bounds__(kNormMaxThreads) fuse_rownorm_kernel(
       // fp32 rows keep fp32 angles; for bf16 rows the (cos, sin) pairs are held
       // as fp16 (relative error 2^-11, a quarter of the bf16 rounding of the
       // stored key), so that a K head's 64 pairs fit one register load each
-      const size_t ci = static_cast<size_t>(threadIdx.x) * M + m;
+      // element-major [64][M] for the GEMM's fused epilogue (a warp's lanes are
+      // rows); row-major [M][64] for kv_epilogue_kernel (a warp is one row)
+      const size_t ci = rope_row_major ? static_cast<size_t>(m) * (HD / 2) + threadIdx.x
+                                       : static_cast<size_t>(threadIdx.x) * M + m;
       if (sizeof(TH) == 4)
         static_cast<float2*>(rope_cs)[ci] = make_float2(cv, sv);
       else
@@ -378,8 +382,10 @@ __global__ void __launch_bounds__(256) kv_epilogue_kernel(
   __half2 cs0 = __floats2half2_rn(1.f, 0.f), cs1 = cs0;
   float g0 = 1.f, g1 = 1.f, g2 = 1.f, g3 = 1.f;  // element loads: the gain vector may be 2-byte aligned
   if (s == 0) {
-    cs0 = rope_cs[static_cast<size_t>(e0) * M + m];
-    cs1 = rope_cs[static_cast<size_t>(e0 + 1) * M + m];
+    // the row's (cos, sin) pairs, row-major: one 8-byte load of frequencies e0, e0 + 1
+    const uint2 cs = *reinterpret_cast<const uint2*>(rope_cs + static_cast<size_t>(m) * (HD / 2) + e0);
+    cs0 = *reinterpret_cast<const __half2*>(&cs.x);
+    cs1 = *reinterpret_cast<const __half2*>(&cs.y);
     if (k_gain) {
       const __nv_bfloat16* kg = k_gain + l * HD;
       g0 = __bfloat162float(kg[e0]);
@@ -523,7 +529,7 @@ dflash_status launch_fuse_context(int J, const void* const* taps, int dt_width, 
         segs, dt_width, static_cast<const float*>(w_fuse), M, D, J * dt_width, Y);
     fuse_rownorm_kernel<float, float><<<M, kNormThreads, 0, st>>>(
         Y, 1, nullptr, kBM, D, 1, M, D, static_cast<const float*>(g_fuse), eps, H, static_cast<float*>(h_t_out), cu_new, c.seq_len, B,
-        c.capacity, c.ring, inv, rowinfo, rope_cs, nullptr, 0, nullptr, 0, 0, 0, dev.status);
+        c.capacity, c.ring, inv, rowinfo, rope_cs, 0, nullptr, 0, nullptr, 0, 0, 0, dev.status);
     F32Segs hs{};
     hs.a[0] = H;
     simt_gemm_f32_kernel<<<dim3((Ntot + 63) / 64, (M + 63) / 64), 256, 0, st>>>(
@@ -607,7 +613,8 @@ dflash_status launch_fuse_context(int J, const void* const* taps, int dt_width, 
                                         f.fuse_bn, f.fuse_n_tiles, M, D,
                                         static_cast<const __nv_bfloat16*>(g_fuse), eps, H,
                                         static_cast<__nv_bfloat16*>(h_t_out), cu_new, c.seq_len, B, c.capacity,
-                                        c.ring, inv, rowinfo, rope_cs, k.fix_flag, f.kv_split ? 0 : f.kv_shares,
+                                        c.ring, inv, rowinfo, rope_cs, f.kv_split ? 1 : 0, k.fix_flag,
+                                        f.kv_split ? 0 : f.kv_shares,
                                         c.block_table, c.max_pages, c.page_size, c.num_pages, dev.status);
     if (le != cudaSuccess) return cuda_fail(le, "fuse_rownorm_kernel launch");
   }
