@@ -364,14 +364,41 @@ __device__ __forceinline__ float resid_weight(float xt, float xd, const Decision
 
 // log2 normaliser of every row of sequence b (target rows 0..bs-1, then the
 // draft rows), from the chunk partials: the warps of the block take the rows in
-// turn, each loading all its partials before merging them.
+// turn.  With at most 32 chunks a row (lane c: chunk c), a warp issues the loads
+// of all its rows before merging any.
 __device__ __forceinline__ void row_normalisers(const float2* __restrict__ part, int b, int B, int bs, int nchunk,
                                                 float* s_lz) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  constexpr int kWarps = kThreads / 32;
   const int nrows = 2 * bs - 1;
-  for (int r = warp; r < nrows; r += kThreads / 32) {
-    const size_t prow = r < bs ? static_cast<size_t>(b * bs + r) : static_cast<size_t>(B * bs + b * (bs - 1) + r - bs);
-    const float2 st = merge_row<false>(part + prow * nchunk, nchunk);
+  auto part_row = [&](int r) {
+    return r < bs ? static_cast<size_t>(b * bs + r) : static_cast<size_t>(B * bs + b * (bs - 1) + r - bs);
+  };
+  if (nchunk <= 32) {
+    constexpr int kRows = (2 * 32 - 1 + kWarps - 1) / kWarps;  // rows per warp for blocks of up to 32
+    float2 v[kRows];
+#pragma unroll
+    for (int i = 0; i < kRows; ++i) {
+      const int r = warp + kWarps * i;
+      v[i] = (r < nrows && lane < nchunk) ? part[part_row(r) * nchunk + lane] : make_float2(-INFINITY, 0.f);
+    }
+#pragma unroll
+    for (int i = 0; i < kRows; ++i) {
+      const int r = warp + kWarps * i;
+      if (r >= nrows) break;
+      float m = v[i].x, sum = v[i].y;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+        const float s2 = __shfl_xor_sync(0xffffffffu, sum, o);
+        lse_merge(m, sum, m2, s2);
+      }
+      if (lane == 0) s_lz[r] = m + log2f(sum);
+    }
+    return;
+  }
+  for (int r = warp; r < nrows; r += kWarps) {
+    const float2 st = merge_row<false>(part + part_row(r) * nchunk, nchunk);
     if (lane == 0) s_lz[r] = st.x + log2f(st.y);
   }
 }
@@ -462,15 +489,13 @@ __global__ void __launch_bounds__(kThreads, (finish_ctas_per_sm<T, VEC>())) veri
     sp = warp_sum(sp);
     if (lane == 0 && s0 < V) rpart[static_cast<size_t>(b) * nseg + c * kSegsPerChunk + warp] = make_float2(sr, sp);
   }
-  if (lane == 0) __threadfence();  // this warp's masses before the CTA's count below
+  if (lane == 0) __threadfence();  // this warp's masses, visible before the CTA's count below
   __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    s_is_last = atomicAdd(counters + b, 1) == ncb - 1;
-  }
+  // The count is an acquire-release add: the last CTA's thread 0 then sees
+  // every other CTA's masses, and the barrier passes that on to its threads.
+  if (threadIdx.x == 0) s_is_last = atom_add_acq_rel_gpu(counters + b, 1) == ncb - 1;
   __syncthreads();
   if (!s_is_last) return;
-  __threadfence();
   // the last CTA of the sequence: inverse-CDF search over row n, first over
   // the segment masses (one warp, vocabulary order), then inside the segment
   __shared__ int s_seg;
