@@ -382,18 +382,19 @@ __device__ __forceinline__ void row_normalisers(const float2* __restrict__ part,
       const int r = warp + kWarps * i;
       v[i] = (r < nrows && lane < nchunk) ? part[part_row(r) * nchunk + lane] : make_float2(-INFINITY, 0.f);
     }
+    // per row: the largest chunk maximum first (a max tree), then the chunk
+    // sums rescaled to it, one exponential per lane (an add tree)
 #pragma unroll
     for (int i = 0; i < kRows; ++i) {
       const int r = warp + kWarps * i;
       if (r >= nrows) break;
-      float m = v[i].x, sum = v[i].y;
+      float M = v[i].x;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-        const float s2 = __shfl_xor_sync(0xffffffffu, sum, o);
-        lse_merge(m, sum, m2, s2);
-      }
-      if (lane == 0) s_lz[r] = m + log2f(sum);
+      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      float sum = (v[i].x == -INFINITY) ? 0.f : v[i].y * exp2f(v[i].x - M);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      if (lane == 0) s_lz[r] = M + log2f(sum);
     }
     return;
   }
