@@ -508,64 +508,89 @@ __global__ void __launch_bounds__(kThreads, (finish_ctas_per_sm<T, VEC>())) veri
   const int nseg_live = (V + kSeg - 1) / kSeg;
   if (warp == 0) {
     const float2* rp = rpart + static_cast<size_t>(b) * nseg;
-    // Up to kKeep masses per lane stay in registers between the total and the
-    // scan (V up to 32 * kKeep * kSeg); longer rows read them again.
-    constexpr int kKeep = 8;
-    const bool kept = nseg_live <= 32 * kKeep;
-    float kr[kKeep], kp[kKeep];
-    float sr = 0.f, sp = 0.f;
-    if (kept) {
+    int cs = -1;
+    float excl_cs = 0.f, t = 0.f;
+    bool use_p = false;
+    constexpr int kKeep = 8;  // segment masses per lane held in registers (V up to 32 * kKeep * kSeg)
+    if (nseg_live <= 32 * kKeep) {
+      // lane l holds the k contiguous segments l*k .. l*k + k - 1: one warp
+      // scan of the lane totals finds the lane, a scan of its k masses the segment
+      const int k = (nseg_live + 31) / 32;
+      float wr[kKeep], wp[kKeep];
+      float lr = 0.f, lp = 0.f;
 #pragma unroll
-      for (int i = 0; i < kKeep; ++i) {
-        const int g = lane + 32 * i;
-        const float2 v = g < nseg_live ? __ldcg(rp + g) : make_float2(0.f, 0.f);
-        kr[i] = v.x;
-        kp[i] = v.y;
-        sr += v.x;
-        sp += v.y;
+      for (int j = 0; j < kKeep; ++j) {
+        const int g = lane * k + j;
+        const float2 v = (j < k && g < nseg_live) ? __ldcg(rp + g) : make_float2(0.f, 0.f);
+        wr[j] = v.x;
+        wp[j] = v.y;
+        lr += v.x;
+        lp += v.y;
       }
-    } else {
+      float ir = lr, ip = lp;  // inclusive scans of the lane totals
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float ur = __shfl_up_sync(0xffffffffu, ir, o);
+        const float up = __shfl_up_sync(0xffffffffu, ip, o);
+        if (lane >= o) {
+          ir += ur;
+          ip += up;
+        }
+      }
+      use_p = !(__shfl_sync(0xffffffffu, ir, 31) > 0.f);
+      t = uniform24(d.vbits) * __shfl_sync(0xffffffffu, use_p ? ip : ir, 31);
+      const float L = use_p ? lp : lr;
+      const float ex = (use_p ? ip : ir) - L;  // mass of the lanes ahead
+      const unsigned hit = __ballot_sync(0xffffffffu, L > 0.f && ex + L > t);
+      const unsigned pos = __ballot_sync(0xffffffffu, L > 0.f);
+      // the first lane whose segments reach t; if rounding left t past the
+      // end, the last lane holding mass (and in it its last positive segment)
+      const int lsel = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : -1);
+      int pick = -1;
+      float excl = 0.f;
+      if (lane == lsel) {
+        float run = ex, ex_last = 0.f;
+        int last = -1;
+#pragma unroll
+        for (int j = 0; j < kKeep; ++j) {
+          const float w = use_p ? wp[j] : wr[j];
+          if (j < k && w > 0.f) {
+            if (pick < 0 && hit && run + w > t) {
+              pick = j;
+              excl = run;
+            }
+            last = j;
+            ex_last = run;
+          }
+          run += w;
+        }
+        if (pick < 0) {
+          pick = last;
+          excl = ex_last;
+        }
+      }
+      if (lsel >= 0) {
+        pick = __shfl_sync(0xffffffffu, pick, lsel);
+        excl = __shfl_sync(0xffffffffu, excl, lsel);
+        cs = lsel * k + max(pick, 0);
+        excl_cs = pick >= 0 ? excl : 0.f;
+      } else {
+        cs = 0;
+      }
+    } else {  // longer rows: groups of 32 segments in turn, read again for the scan
+      float sr = 0.f, sp = 0.f;
       for (int g = lane; g < nseg_live; g += 32) {
         const float2 v = __ldcg(rp + g);
         sr += v.x;
         sp += v.y;
       }
-    }
-    sr = warp_sum(sr);
-    sp = warp_sum(sp);
-    const bool use_p = !(sr > 0.f);
-    const float t = uniform24(d.vbits) * (use_p ? sp : sr);
-    float before = 0.f;  // mass of the segments ahead of this group of 32
-    int cs = -1, last_pos = -1;
-    float excl_cs = 0.f, excl_last = 0.f;
-    // one group of 32 segments (lane: segment g0 + lane, mass w), in vocabulary order
-    auto group = [&](int g0, float w) {
-      float inc = w;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float u = __shfl_up_sync(0xffffffffu, inc, o);
-        if (lane >= o) inc += u;
-      }
-      const float ex = before + (inc - w);
-      const unsigned hit = __ballot_sync(0xffffffffu, w > 0.f && ex + w > t);
-      const unsigned pos = __ballot_sync(0xffffffffu, w > 0.f);
-      if (hit) {
-        const int l = __ffs(hit) - 1;
-        cs = g0 + l;
-        excl_cs = __shfl_sync(0xffffffffu, ex, l);
-      }
-      if (pos) {
-        const int l = 31 - __clz(pos);
-        last_pos = g0 + l;
-        excl_last = __shfl_sync(0xffffffffu, ex, l);
-      }
-      before += __shfl_sync(0xffffffffu, inc, 31);
-    };
-    if (kept) {
-#pragma unroll
-      for (int i = 0; i < kKeep; ++i)
-        if (32 * i < nseg_live && cs < 0) group(32 * i, use_p ? kp[i] : kr[i]);
-    } else {
+      sr = warp_sum(sr);
+      sp = warp_sum(sp);
+      use_p = !(sr > 0.f);
+      t = uniform24(d.vbits) * (use_p ? sp : sr);
+      float before = 0.f;  // mass of the segments ahead of this group of 32
+      int last_pos = -1;
+      float excl_last = 0.f;
       for (int g0 = 0; g0 < nseg_live && cs < 0; g0 += 32) {
         const int g = g0 + lane;
         float w = 0.f;
@@ -573,12 +598,31 @@ __global__ void __launch_bounds__(kThreads, (finish_ctas_per_sm<T, VEC>())) veri
           const float2 v = __ldcg(rp + g);
           w = use_p ? v.y : v.x;
         }
-        group(g0, w);
+        float inc = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float u = __shfl_up_sync(0xffffffffu, inc, o);
+          if (lane >= o) inc += u;
+        }
+        const float ex = before + (inc - w);
+        const unsigned hit = __ballot_sync(0xffffffffu, w > 0.f && ex + w > t);
+        const unsigned pos = __ballot_sync(0xffffffffu, w > 0.f);
+        if (hit) {
+          const int l = __ffs(hit) - 1;
+          cs = g0 + l;
+          excl_cs = __shfl_sync(0xffffffffu, ex, l);
+        }
+        if (pos) {
+          const int l = 31 - __clz(pos);
+          last_pos = g0 + l;
+          excl_last = __shfl_sync(0xffffffffu, ex, l);
+        }
+        before += __shfl_sync(0xffffffffu, inc, 31);
       }
-    }
-    if (cs < 0) {  // rounding left the threshold at the very end
-      cs = max(last_pos, 0);
-      excl_cs = last_pos >= 0 ? excl_last : 0.f;
+      if (cs < 0) {  // rounding left the threshold at the very end
+        cs = max(last_pos, 0);
+        excl_cs = last_pos >= 0 ? excl_last : 0.f;
+      }
     }
     if (lane == 0) {
       s_seg = cs;
