@@ -14,18 +14,19 @@
 //                  x = logit * log2(e)/T, or (max, first argmax) when T == 0.
 //   2. decide   -- (T == 0) one warp per sequence: the target argmax of every
 //                  row against the draft tokens.
-//   2. finish   -- (T > 0) one CTA per (sequence, two chunks), launched as a
-//                  programmatic dependent of the stats pass.  Before waiting
-//                  for it the CTA loads the draft tokens' target and draft
-//                  logits; then all warps merge the sequence's chunk partials
-//                  into log-normalisers and one warp evaluates
-//                  alpha_k = min(1, p(x)/q(x)), draws the Philox uniforms and
-//                  finds the first rejection n (every CTA of the sequence takes
-//                  the same decision).  The CTA sums max(0, p - q) (the bonus
-//                  row: p) over its chunks of row n; the last CTA of the
-//                  sequence to finish (an atomic count) runs the inverse-CDF
-//                  search for the first index whose cumulative mass exceeds
-//                  v * S.
+//   2. finish   -- (T > 0) one CTA per (sequence, chunk), launched as a
+//                  programmatic dependent of the stats pass; four fit on an
+//                  SM, so the whole grid is resident at once.  Before waiting
+//                  for the stats pass the CTA loads the draft tokens and their
+//                  target and draft logits and draws the Philox words; then
+//                  its warps merge the sequence's chunk partials into
+//                  log-normalisers and one warp evaluates
+//                  alpha_k = min(1, p(x)/q(x)) and finds the first rejection n
+//                  (every CTA of the sequence takes the same decision).  The
+//                  CTA sums max(0, p - q) (the bonus row: p) over its chunk of
+//                  row n; the last CTA of the sequence to finish (an atomic
+//                  count) runs the inverse-CDF search for the first index
+//                  whose cumulative mass exceeds v * S.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
