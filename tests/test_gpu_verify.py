@@ -79,6 +79,18 @@ def test_verify_small_grid(dtype, V, bs, T):
     run_and_compare(lt, ld, x, T, seed=1234 + bs, cycle=V)
 
 
+@pytest.mark.parametrize("V", [600000, 600001])
+@pytest.mark.parametrize("T", [1.0, 0.0])
+def test_verify_rows_longer_than_the_register_paths(V, T):
+    """Rows of more than 32 stats chunks and 256 residual segments: the
+    normalisers merge through the looped path and the draw scans its segment
+    masses 32 at a time; V = 600001 also takes the scalar (unvectorised) loads."""
+    B, bs = 3, 4
+    lt, ld = _mk_logits(B, bs, V, torch.bfloat16, seed=V % 1000 + 3)
+    x = _greedy_tokens(lt, seed=5) if T == 0.0 else workloads.draft_tokens(ld, T, seed=9)
+    run_and_compare(lt, ld, x, T, seed=77, cycle=2)
+
+
 def test_verify_identical_rows_accept_everything():
     B, bs, V = 16, 8, 50000
     lt, _ = _mk_logits(B, bs, V, torch.bfloat16, seed=3)
