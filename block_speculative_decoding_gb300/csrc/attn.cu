@@ -1064,16 +1064,17 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const float* __restrict__
 }
 
 
-// Keys per split: aims at ~1200 work items for a full cache (about eight per
-// SM).  Longer splits amortise each split's partial output (written, then
-// merged by the combine kernel) and its pipeline ramp; enough items remain for
-// the dynamic queue to balance the SMs.  A split is at least ~1024 keys (a
+// Keys per split: aims at ~800 work items for a full cache (about five per
+// SM; a cache filled to about half its capacity then gives about three).
+// Longer splits amortise each split's partial output (written, then merged by
+// the combine kernel) and its pipeline ramp; enough items remain for the
+// dynamic queue to balance the SMs.  A split is at least ~1024 keys (a
 // work item costs about as much as a few tiles on top of its keys) unless
 // that would leave fewer items than the 152 SMs of a GB300.
 int pick_chunk(int B, int Hkv, int cap, int window) {
   const long keys = window > 0 ? std::min(window, cap) : cap;
   const long total = static_cast<long>(B) * Hkv * keys;
-  long c = total / 1200;
+  long c = total / 800;
   const long lo = std::min<long>(1024, std::max<long>(256, total / 152));
   c = std::max(c, lo);
   c = (c + kKeys - 1) / kKeys * kKeys;
