@@ -52,11 +52,9 @@ constexpr int kKeys = 128;                      // keys per tile (the tensor cor
 constexpr int kBoxBytes = kKeys * 64 * 2;       // 128 keys x 64 dims bf16 = 16 KB (one TMA box)
 constexpr int kHalfBytes = 2 * kBoxBytes;       // K (or V) of one tile: 32 KB
 constexpr int kMaxBatch = 2048;
-constexpr double kTwoPi = 6.283185307179586476925286766559;
-constexpr double kInvTwoPi = 0.15915494309189533576888376337251;
 
 struct InvFreq {
-  double v[HD / 2];
+  unsigned long long v[HD / 2];  // round(2^64 inv_freq[e] / 2 pi): turns per position, 64-bit fraction
 };
 
 struct AttnParams {
@@ -104,6 +102,30 @@ __host__ __device__ __forceinline__ int n_splits(int ncache, int chunk) {
 // --------------------------------------------------------------------------
 constexpr int kPrologueThreads = 256;
 
+// Elements (e, e + 1) of a head vector, e even: one 4-byte (bf16) or 8-byte
+// (fp32) access, aligned because the rows are 16-byte aligned.
+template <typename T>
+__device__ __forceinline__ float2 load_pair(const T* p);
+template <>
+__device__ __forceinline__ float2 load_pair<float>(const float* p) {
+  return *reinterpret_cast<const float2*>(p);
+}
+template <>
+__device__ __forceinline__ float2 load_pair<__nv_bfloat16>(const __nv_bfloat16* p) {
+  const uint32_t u = *reinterpret_cast<const uint32_t*>(p);
+  return make_float2(bf16_lo(u), bf16_hi(u));
+}
+template <typename T>
+__device__ __forceinline__ void store_pair(T* p, float a, float b);
+template <>
+__device__ __forceinline__ void store_pair<float>(float* p, float a, float b) {
+  *reinterpret_cast<float2*>(p) = make_float2(a, b);
+}
+template <>
+__device__ __forceinline__ void store_pair<__nv_bfloat16>(__nv_bfloat16* p, float a, float b) {
+  *reinterpret_cast<uint32_t*>(p) = pack_bf16x2(a, b);
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kPrologueThreads) attn_prologue_kernel(
     const T* __restrict__ q, const T* __restrict__ kb, const T* __restrict__ qg,
@@ -121,32 +143,32 @@ __global__ void __launch_bounds__(kPrologueThreads) attn_prologue_kernel(
   qg = pdl_fresh(qg);
   kg = pdl_fresh(kg);
   seq_len = pdl_fresh(seq_len);
+  const int b = blockIdx.x / bs, j = blockIdx.x % bs;
+  // the sequence length first: the angles that depend on it are this
+  // kernel's longest chain, so its load is not queued behind the others
+  const int n_in = seq_len[b];
   if (blockIdx.x == 0 && counters)
     for (int i = threadIdx.x; i < n_counters; i += blockDim.x) counters[i] = 0;
-  const int b = blockIdx.x / bs, j = blockIdx.x % bs;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int e0 = 2 * lane;  // this lane owns elements e0, e0+1 and e0+64, e0+65
   constexpr int kWarps = kPrologueThreads / 32;
   constexpr int kBatch = 5;  // head vectors a warp loads before working on them
-  // a batch of a warp's head vectors and their gains, loaded together
-  float x[kBatch][4], gn[kBatch][4];
+  // this lane's elements of the two gains, shared by all head vectors
+  const float gq0 = qg ? to_f32<T>(qg[e0]) : 1.f, gq1 = qg ? to_f32<T>(qg[e0 + 1]) : 1.f;
+  const float gq2 = qg ? to_f32<T>(qg[e0 + 64]) : 1.f, gq3 = qg ? to_f32<T>(qg[e0 + 65]) : 1.f;
+  const float gk0 = kg ? to_f32<T>(kg[e0]) : 1.f, gk1 = kg ? to_f32<T>(kg[e0 + 1]) : 1.f;
+  const float gk2 = kg ? to_f32<T>(kg[e0 + 64]) : 1.f, gk3 = kg ? to_f32<T>(kg[e0 + 65]) : 1.f;
+  // a batch of a warp's head vectors, two pair loads per vector
+  float2 xa[kBatch], xb[kBatch];
   auto load_batch = [&](int v0) {
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
       const int v = v0 + u * kWarps;
       if (v < Hq + Hkv) {
-        const bool isq = v < Hq;
-        const T* src = isq ? q + ((static_cast<size_t>(b) * Hq + v) * bs + j) * HD
-                           : kb + ((static_cast<size_t>(b) * Hkv + (v - Hq)) * bs + j) * HD;
-        const T* gain = isq ? qg : kg;
-        x[u][0] = to_f32<T>(src[e0]);
-        x[u][1] = to_f32<T>(src[e0 + 1]);
-        x[u][2] = to_f32<T>(src[e0 + 64]);
-        x[u][3] = to_f32<T>(src[e0 + 65]);
-        gn[u][0] = gain ? to_f32<T>(gain[e0]) : 1.f;
-        gn[u][1] = gain ? to_f32<T>(gain[e0 + 1]) : 1.f;
-        gn[u][2] = gain ? to_f32<T>(gain[e0 + 64]) : 1.f;
-        gn[u][3] = gain ? to_f32<T>(gain[e0 + 65]) : 1.f;
+        const T* src = v < Hq ? q + ((static_cast<size_t>(b) * Hq + v) * bs + j) * HD
+                              : kb + ((static_cast<size_t>(b) * Hkv + (v - Hq)) * bs + j) * HD;
+        xa[u] = load_pair<T>(src + e0);
+        xb[u] = load_pair<T>(src + e0 + 64);
       }
     }
   };
@@ -154,14 +176,16 @@ __global__ void __launch_bounds__(kPrologueThreads) attn_prologue_kernel(
   load_batch(warp);
   // the block's positions follow the sequence: seq_len (a ring cache's
   // length may exceed its capacity) plus j
-  const int n = ring ? max(seq_len[b], 0) : clamp_seq(seq_len[b], cap, status);
+  const int n = ring ? max(n_in, 0) : clamp_seq(n_in, cap, status);
   const int pos = n + j;
   __shared__ float s_cos[HD / 2], s_sin[HD / 2];
   if (threadIdx.x < HD / 2) {
-    double ang = static_cast<double>(pos) * inv_freq.v[threadIdx.x];
-    ang -= kTwoPi * rint(ang * kInvTwoPi);
+    // pos * inv_freq / 2 pi mod 1 turn, as a 64-bit fraction (exact to 2^-34
+    // turn for any position below 2^31); its top 32 bits as a signed turn in
+    // [-1/2, 1/2) give the angle for sin / cos of pi * [-1, 1)
+    const unsigned long long t = static_cast<unsigned long long>(pos) * inv_freq.v[threadIdx.x];
     float sv, cv;
-    sincosf(static_cast<float>(ang), &sv, &cv);
+    sincospif(static_cast<float>(static_cast<int>(t >> 32)) * 0x1p-31f, &sv, &cv);
     s_cos[threadIdx.x] = cv;
     s_sin[threadIdx.x] = sv;
   }
@@ -176,17 +200,15 @@ __global__ void __launch_bounds__(kPrologueThreads) attn_prologue_kernel(
       const bool isq = v < Hq;
       T* dst = isq ? qh + ((static_cast<size_t>(b) * Hq + v) * bs + j) * HD
                    : kbh + ((static_cast<size_t>(b) * Hkv + (v - Hq)) * bs + j) * HD;
-      float x0 = x[u][0], x1 = x[u][1], y0 = x[u][2], y1 = x[u][3];
+      float x0 = xa[u].x, x1 = xa[u].y, y0 = xb[u].x, y1 = xb[u].y;
       const float ss = warp_sum(x0 * x0 + x1 * x1 + y0 * y0 + y1 * y1);
       const float r = rsqrtf(ss * (1.0f / HD) + eps);
-      x0 *= r * gn[u][0];
-      x1 *= r * gn[u][1];
-      y0 *= r * gn[u][2];
-      y1 *= r * gn[u][3];
-      dst[e0] = from_f32<T>(x0 * c0 - y0 * s0);
-      dst[e0 + 1] = from_f32<T>(x1 * c1 - y1 * s1);
-      dst[e0 + 64] = from_f32<T>(y0 * c0 + x0 * s0);
-      dst[e0 + 65] = from_f32<T>(y1 * c1 + x1 * s1);
+      x0 *= r * (isq ? gq0 : gk0);
+      x1 *= r * (isq ? gq1 : gk1);
+      y0 *= r * (isq ? gq2 : gk2);
+      y1 *= r * (isq ? gq3 : gk3);
+      store_pair<T>(dst + e0, x0 * c0 - y0 * s0, x1 * c1 - y1 * s1);
+      store_pair<T>(dst + e0 + 64, y0 * c0 + x0 * s0, y1 * c1 + x1 * s1);
     }
   }
 }
@@ -1105,7 +1127,10 @@ dflash_status launch_block_attn(int layer, int B, int bs, int Hq, const void* q,
   const int Hkv = c.num_kv_heads;
   const int G = Hq / Hkv;
   InvFreq inv;
-  for (int e = 0; e < HD / 2; ++e) inv.v[e] = std::pow(static_cast<double>(theta), -2.0 * e / HD);
+  for (int e = 0; e < HD / 2; ++e) {
+    const long double f = std::pow(static_cast<double>(theta), -2.0 * e / HD);  // inverse frequency, as the fp64 one
+    inv.v[e] = static_cast<unsigned long long>(std::llroundl(f * 0x1p64L / (2.0L * 3.14159265358979323846264338327950288L)) );
+  }
   WsCarver w(ws);
   const float scale = 1.0f / std::sqrt(static_cast<float>(HD));
   if (c.dtype == DFLASH_F32) {
