@@ -197,7 +197,7 @@ class Cycle:
 def launches_per_step(M: int, layers: int) -> int:
     """The library's kernel launches in one step: fusion 4 for up to 256 new rows (fusion GEMM, row
     norm, K/V GEMM, K/V epilogue) else 3 (the K/V epilogue fused into the GEMM), block attention 3 per
-    layer (prologue, main, combine), verification 2 (stats, finish)."""
+    layer (counter clear, main, combine), verification 2 (stats, finish)."""
     return (4 if M <= 256 else 3) + 3 * layers + 2
 
 
@@ -327,7 +327,7 @@ def run_gpu(args):
                        (cfg.L * cyc.attn_bytes_per_call + cyc.verify_bytes + cyc.fuse_bytes) / 1e9)},
         "tokens_per_sec": tokens_all / elapsed_max,
         "mean_tokens_per_cycle": tokens_per_cycle / cfg.B,
-        "roofline": {"kernel": "block attention (prologue + split-KV main + combine), per layer call",
+        "roofline": {"kernel": "block attention (counter clear + split-KV main with in-kernel Q/K norm and RoPE + combine), per layer call",
                      "bound": "hbm", "achieved": attn_gbs, "peak": hbm, "unit": "GB/s",
                      "frac": attn_gbs / hbm, "peak_source": src,
                      "algorithmic_bytes_per_launch": cyc.attn_bytes_per_call,

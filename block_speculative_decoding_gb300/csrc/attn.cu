@@ -10,20 +10,26 @@
 //
 // Kernels (three launches per call, each a programmatic dependent of the one
 // before it):
-//   prologue -- per (sequence, block row): RMSNorm * gain and RoPE of every
-//               query head and block key, rounded to the storage dtype; also
-//               clears the work-queue counter and the per-pair counters.
+//   clear    -- one CTA: waits for the preceding grid, releases the main
+//               kernel, and clears the work-queue counter and the per-pair
+//               counters.
 //   main     -- split-KV, memory-bound: a persistent grid (one CTA per SM)
-//               takes work items (sequence, KV head, key split) from an atomic
-//               queue; the producer warp decodes each item once and hands it
-//               to the other roles through shared memory.  The products are
+//               takes work items (sequence, KV head, key split), the first one
+//               per CTA by its index (so it starts while the counters are
+//               being cleared) and the rest from an atomic queue; the producer
+//               warp decodes each item once and hands it to the other roles
+//               through shared memory.  The producer loads the pair's raw query
+//               rows (and the block's raw keys) into shared memory, where the
+//               epilogue warps apply RMSNorm * gain and RoPE in place, one item
+//               ahead of their epilogue work.  The products are
 //               taken transposed: the 128 keys of a tile fill the tensor
 //               core's M and the G * bs query rows of the pair (padded to
 //               NC = 32 or 64) its N.  The producer streams 128-key K and V
 //               tiles of the cache (and, for the last split, the block's own
-//               keys) with TMA (128-byte swizzle) through K and V rings sized
-//               to the shared memory (two K and three V stages at 227 KB); one thread issues S^T = K Q^T into tensor
-//               memory, eight softmax warps (one key per thread) write
+//               values; its keys sit in their own buffer) with TMA (128-byte
+//               swizzle) through K and V rings sized to the shared memory (two
+//               K and three V stages at 227 KB); one thread issues
+//               S^T = K Q^T into tensor memory, eight softmax warps (one key per thread) write
 //               P^T = 2^(S^T scale - m) to shared memory as bf16 hi + lo parts,
 //               another thread issues O^T += V^T [P_hi^T P_lo^T], and four
 //               epilogue warps add the hi and lo columns and write the output
@@ -60,8 +66,10 @@ struct InvFreq {
 struct AttnParams {
   int B, bs, G, Hkv, Hq, cap, ring, layer, window, chunk, max_splits, rows;
   const int32_t* seq_len;
-  const __nv_bfloat16* qh;   // [B, Hq, bs, 128]   prologue output
-  const __nv_bfloat16* kbh;  // [B, Hkv, bs, 128]  prologue output
+  const __nv_bfloat16* q;    // [B, Hq, bs, 128]   block queries (input, before norm and RoPE)
+  const __nv_bfloat16* kb;   // [B, Hkv, bs, 128]  block keys (input, before norm and RoPE)
+  const __nv_bfloat16* qg;   // [128] query-norm gain (nullptr = ones)
+  const __nv_bfloat16* kg;   // [128] key-norm gain (nullptr = ones)
   const __nv_bfloat16* vb;   // [B, Hkv, bs, 128]  block values (input)
   __nv_bfloat16* out;        // [B, Hq, bs, 128]
   float* opart;              // [B, Hkv, max_splits, rows, 128] normalised partial outputs
@@ -71,11 +79,13 @@ struct AttnParams {
   const int32_t* table;      // paged layout: [B, max_pages] block table; nullptr: linear or ring
   int max_pages, page_size, num_pages;
   float scale_log2;          // log2(e) / sqrt(128)
-  int* counters;             // [1 + 2 B Hkv], cleared by the prologue: the work-queue counter, per (b, g)
+  int* counters;             // [1 + 2 B Hkv], cleared before the main kernel: the work-queue counter, per (b, g)
                              // a flag (scores outgrew the running max), then per (b, g) the count of
                              // epilogue warps (4 per split) that finished writing
   unsigned* status;
   unsigned long long wait_limit_ns;  // the combine kernel's bounded wait for a pair's splits
+  float eps;                         // RMSNorm epsilon of the query and key norms
+  InvFreq inv;                       // RoPE frequencies as fixed-point turns per position
 };
 
 // Cached rows a sequence attends to: its length, clamped to the capacity; a
@@ -97,33 +107,34 @@ __host__ __device__ __forceinline__ int n_splits(int ncache, int chunk) {
   return ncache <= 0 ? 1 : (ncache + chunk - 1) / chunk;
 }
 
+// sin and cos of the RoPE angle at position pos of the frequency whose turns
+// per position are f (a 64-bit fraction): pos * f mod 2^64 is the angle in
+// turns, exact to 2^-34 turn for any position below 2^31; its top 32 bits, as
+// a signed turn in [-1/2, 1/2), give sin / cos of pi * [-1, 1).
+__device__ __forceinline__ void rope_sincos(int pos, unsigned long long f, float* sv, float* cv) {
+  const unsigned long long t = static_cast<unsigned long long>(pos) * f;
+  sincospif(static_cast<float>(static_cast<int>(t >> 32)) * 0x1p-31f, sv, cv);
+}
+
 // --------------------------------------------------------------------------
-// prologue: q^ = RoPE(RMSNorm(q) * q_gain), k^_b = RoPE(RMSNorm(kb) * k_gain)
+// fp32 prologue: q^ = RoPE(RMSNorm(q) * q_gain), k^_b = RoPE(RMSNorm(kb) * k_gain)
+// into the workspace (the bf16 path does this inside the main kernel)
 // --------------------------------------------------------------------------
 constexpr int kPrologueThreads = 256;
 
-// Elements (e, e + 1) of a head vector, e even: one 4-byte (bf16) or 8-byte
-// (fp32) access, aligned because the rows are 16-byte aligned.
+// Elements (e, e + 1) of an fp32 head vector, e even: one 8-byte access,
+// aligned because the rows are 16-byte aligned.
 template <typename T>
 __device__ __forceinline__ float2 load_pair(const T* p);
 template <>
 __device__ __forceinline__ float2 load_pair<float>(const float* p) {
   return *reinterpret_cast<const float2*>(p);
 }
-template <>
-__device__ __forceinline__ float2 load_pair<__nv_bfloat16>(const __nv_bfloat16* p) {
-  const uint32_t u = *reinterpret_cast<const uint32_t*>(p);
-  return make_float2(bf16_lo(u), bf16_hi(u));
-}
 template <typename T>
 __device__ __forceinline__ void store_pair(T* p, float a, float b);
 template <>
 __device__ __forceinline__ void store_pair<float>(float* p, float a, float b) {
   *reinterpret_cast<float2*>(p) = make_float2(a, b);
-}
-template <>
-__device__ __forceinline__ void store_pair<__nv_bfloat16>(__nv_bfloat16* p, float a, float b) {
-  *reinterpret_cast<uint32_t*>(p) = pack_bf16x2(a, b);
 }
 
 template <typename T>
@@ -180,12 +191,8 @@ __global__ void __launch_bounds__(kPrologueThreads) attn_prologue_kernel(
   const int pos = n + j;
   __shared__ float s_cos[HD / 2], s_sin[HD / 2];
   if (threadIdx.x < HD / 2) {
-    // pos * inv_freq / 2 pi mod 1 turn, as a 64-bit fraction (exact to 2^-34
-    // turn for any position below 2^31); its top 32 bits as a signed turn in
-    // [-1/2, 1/2) give the angle for sin / cos of pi * [-1, 1)
-    const unsigned long long t = static_cast<unsigned long long>(pos) * inv_freq.v[threadIdx.x];
     float sv, cv;
-    sincospif(static_cast<float>(static_cast<int>(t >> 32)) * 0x1p-31f, &sv, &cv);
+    rope_sincos(pos, inv_freq.v[threadIdx.x], &sv, &cv);
     s_cos[threadIdx.x] = cv;
     s_sin[threadIdx.x] = sv;
   }
@@ -298,7 +305,8 @@ constexpr int kMaxRing = 4;       // K and V ring stages (each)
 constexpr int kSBufs = 4;         // S^T buffers in tensor memory
 constexpr int kItemRing = 4;
 constexpr int kBlockBoxRows = 16; // block keys per TMA box (bs <= 16)
-constexpr int kNumBars = 4 * kMaxRing + 2 * 2 + 2 * kSBufs + 4 * 2 + 2 * 2 + 2 * kItemRing + 2;
+constexpr int kBlkBoxBytes = kBlockBoxRows * 128;  // one 64-dim box of the block keys
+constexpr int kNumBars = 4 * kMaxRing + 2 * 2 + 2 * kSBufs + 4 * 2 + 2 * 2 + 2 * kItemRing + 2 + 2;
 constexpr float kOverflowLog2 = 64.0f;  // largest score above the running max, in log2 units
 
 template <int NC>
@@ -325,20 +333,25 @@ struct TcCfg {
 
 struct TcLayout {
   int nk, nv;
-  int off_q, off_p, off_k, off_v, off_bar, off_misc, bytes;
+  int off_q, off_kb, off_p, off_k, off_v, off_bar, off_misc, bytes;
 };
 
 __host__ __device__ inline int tc_misc_bytes(int B, int nc) {
-  // tmem slot (64) | s_m [2][NC] | s_l [2][4][NC] | s_red [2 halves][2][4][32] |
+  // tmem slot (64) | RoPE turns per position [64] (u64) | gains [2][128] (bf16) |
+  // s_m [2][NC] | s_l [2][4][NC] | s_red [2 halves][2][4][32] |
   // prefix [B+1], n [B] | decoded item ring [kItemRing]
-  return 64 + 2 * nc * 4 + 2 * 4 * nc * 4 + 2 * 2 * 4 * 32 * 4 + (2 * B + 1) * 4 +
+  return 64 + 512 + 512 + 2 * nc * 4 + 2 * 4 * nc * 4 + 2 * 2 * 4 * 32 * 4 + (2 * B + 1) * 4 +
          kItemRing * static_cast<int>(sizeof(Item));
 }
 
 __host__ __device__ inline TcLayout tc_layout(int nc, int B, int smem_limit) {
   TcLayout L;
   L.off_q = 0;                           // 2 buffers x 2 boxes of NC rows
-  L.off_p = 4 * nc * 128;                // 2 buffers of P^T (hi and lo)
+  // 2 buffers x 2 boxes of the block keys.  The block tile's S product reads
+  // 128 rows from a box; the 112 past its 16 lie in the next buffers and the
+  // P region (masked keys: their scores are never used).
+  L.off_kb = 4 * nc * 128;
+  L.off_p = L.off_kb + 4 * kBlkBoxBytes;  // 2 buffers of P^T (hi and lo)
   L.off_k = L.off_p + 2 * kKeys * 2 * nc * 2;
   const int fixed = 1024 + L.off_k + 8 * kNumBars + tc_misc_bytes(B, nc);
   int total = (smem_limit - fixed) / kHalfBytes;
@@ -359,13 +372,46 @@ __device__ __forceinline__ long cache_row(const AttnParams& p, int b, int g, int
   return ((static_cast<long>(p.layer) * p.B + b) * p.Hkv + g) * p.cap + pos;
 }
 
+// This lane's four elements (4 lane .. 4 lane + 3) of RoPE(RMSNorm(x) * gain)
+// at position pos, rounded to bf16 as the tensor-core path stores them; the
+// rotation partner of element e < 64 is e + 64, held by lane ^ 16.
+__device__ float4 norm_rope_lanes(const __nv_bfloat16* x, const __nv_bfloat16* gain, float eps, int pos,
+                                  const InvFreq& inv) {
+  const int lane = threadIdx.x % 32;
+  float v[4];
+  {
+    const float4 t = bf16x4_to_f32(x + 4 * lane);
+    v[0] = t.x, v[1] = t.y, v[2] = t.z, v[3] = t.w;
+  }
+  const float ss = warp_sum(v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3]);
+  const float rn = rsqrtf(ss * (1.0f / HD) + eps);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) v[i] *= rn * (gain ? __bfloat162float(gain[4 * lane + i]) : 1.f);
+  float out[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float w = __shfl_xor_sync(0xffffffffu, v[i], 16);
+    float sv, cv;
+    rope_sincos(pos, inv.v[(4 * lane + i) & 63], &sv, &cv);
+    // first half: x cos - y sin; second half: y cos + x sin (x = element e, y = e + 64)
+    out[i] = lane < 16 ? v[i] * cv - w * sv : v[i] * cv + w * sv;
+    out[i] = __bfloat162float(__float2bfloat16_rn(out[i]));
+  }
+  return make_float4(out[0], out[1], out[2], out[3]);
+}
+
 // One output row computed key by key (4 dims per lane, exact running max):
 // the fallback for a (sequence, KV head) whose scores outgrew the running max
-// of the tensor-core kernel.
+// of the tensor-core kernel.  The query and the block keys are normalised and
+// rotated here from the inputs, as the main kernel does in shared memory.
 __device__ void attn_row_exact(const AttnParams& p, int b, int g, int row, int first, int n) {
   const int lane = threadIdx.x % 32;
   const int h = g * p.G + row / p.bs, j = row % p.bs;
-  const float4 q = bf16x4_to_f32(p.qh + ((static_cast<size_t>(b) * p.Hq + h) * p.bs + j) * HD + 4 * lane);
+  // the block's positions follow the sequence: its length (a ring cache's
+  // may exceed the capacity), else the cached rows
+  const int pos0 = p.ring ? max(p.seq_len[b], 0) : n;
+  const float4 q = norm_rope_lanes(p.q + ((static_cast<size_t>(b) * p.Hq + h) * p.bs + j) * HD, p.qg, p.eps,
+                                   pos0 + j, p.inv);
   const size_t bbase = (static_cast<size_t>(b) * p.Hkv + g) * p.bs;
   float m = -INFINITY, l = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -382,9 +428,10 @@ __device__ void attn_row_exact(const AttnParams& p, int b, int g, int row, int f
       }
       crow = zero ? 0 : cache_row(p, b, g, t, page);
     }
-    const __nv_bfloat16* kr = blk ? p.kbh + (bbase + (t - n)) * HD : p.ck + crow * HD;
     const __nv_bfloat16* vr = blk ? p.vb + (bbase + (t - n)) * HD : p.cv + crow * HD;
-    const float4 k = zero ? make_float4(0.f, 0.f, 0.f, 0.f) : bf16x4_to_f32(kr + 4 * lane);
+    const float4 k = blk    ? norm_rope_lanes(p.kb + (bbase + (t - n)) * HD, p.kg, p.eps, pos0 + (t - n), p.inv)
+                     : zero ? make_float4(0.f, 0.f, 0.f, 0.f)
+                            : bf16x4_to_f32(p.ck + crow * HD + 4 * lane);
     const float s = warp_sum(q.x * k.x + q.y * k.y + q.z * k.z + q.w * k.w) * p.scale_log2;
     const float4 v = zero ? make_float4(0.f, 0.f, 0.f, 0.f) : bf16x4_to_f32(vr + 4 * lane);
     if (s > m) {
@@ -409,6 +456,28 @@ __device__ void attn_row_exact(const AttnParams& p, int b, int g, int row, int f
       make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
 }
 
+// Clears the main kernel's counters.  Launched as a programmatic dependent of
+// whatever precedes it in the stream, it waits for that grid (which may have
+// written the block's queries, keys or the sequence lengths) and only then
+// releases the main kernel, whose first work items need none of the counters;
+// the main kernel's threads wait for this grid before they touch them.  It
+// also asks L2 for the block's raw query and key rows (a few MB), which every
+// work item loads just before it needs them.
+constexpr uint32_t kPrefetchChunk = 4096;
+__global__ void __launch_bounds__(1024) attn_clear_kernel(int* __restrict__ counters, int n,
+                                                          const uint8_t* __restrict__ q, size_t q_bytes,
+                                                          const uint8_t* __restrict__ kb, size_t kb_bytes) {
+  pdl_wait_primary();
+  pdl_launch_dependents();
+  for (size_t off = static_cast<size_t>(threadIdx.x) * kPrefetchChunk; off < q_bytes;
+       off += static_cast<size_t>(blockDim.x) * kPrefetchChunk)
+    prefetch_l2_bulk(q + off, static_cast<uint32_t>(q_bytes - off < kPrefetchChunk ? q_bytes - off : kPrefetchChunk));
+  for (size_t off = static_cast<size_t>(threadIdx.x) * kPrefetchChunk; off < kb_bytes;
+       off += static_cast<size_t>(blockDim.x) * kPrefetchChunk)
+    prefetch_l2_bulk(kb + off, static_cast<uint32_t>(kb_bytes - off < kPrefetchChunk ? kb_bytes - off : kPrefetchChunk));
+  for (int i = threadIdx.x; i < n; i += blockDim.x) counters[i] = 0;
+}
+
 // Per output row (one warp, 4 dims per lane): the log-sum-exp merge of the
 // split partials of a (sequence, KV head) with more than one split, or the
 // exact recomputation of a (sequence, KV head) the main kernel flagged.
@@ -416,7 +485,8 @@ __device__ void attn_row_exact(const AttnParams& p, int b, int g, int row, int f
 // for its whole grid: a warp starts on (b, g) as soon as the main kernel's
 // epilogue warps have written all of its splits (a counter per pair, four
 // arrivals per split), so the merges overlap the main kernel's last items.
-__global__ void __launch_bounds__(256) attn_combine_kernel(const AttnParams p) {
+// Five CTAs per SM: the exact path's registers (rare) do not cost the merges' occupancy.
+__global__ void __launch_bounds__(256, 5) attn_combine_kernel(const __grid_constant__ AttnParams p) {
   pdl_launch_dependents();  // a following call's first kernel may become resident; it waits for this grid
   const int gw = blockIdx.x * 8 + threadIdx.x / 32;   // global warp = (b, g, row)
   const int lane = threadIdx.x % 32;
@@ -541,16 +611,79 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&d)[N]) {
   for (int j = 0; j < N; ++j) d[j] = __uint_as_float(r[j]);
 }
 
+// RMSNorm * gain and RoPE of one row of head vectors held in shared memory as
+// two K-major boxes with the 128-byte swizzle (elements 0..63 and 64..127,
+// box_stride bytes apart; row r at r * 128, its 16-byte chunk c at chunk
+// c ^ (r & 7)), rewritten in place as bf16.  Sixteen consecutive lanes share
+// the row: lane part k owns elements 4k .. 4k+3 and their rotation partners
+// 64+4k .. 64+4k+3.  cv, sv: the part's four cos and sin at the row's
+// position; g: its gains (elements, then partners) as bf16 pairs.  Every lane
+// of the warp calls it; only active lanes store.
+__device__ __forceinline__ void norm_rope_row_smem(uint32_t box0, uint32_t box_stride, int r, int k,
+                                                   const float (&cv)[4], const float (&sv)[4], const uint2 gx,
+                                                   const uint2 gy, float eps, bool active) {
+  const uint32_t a = box0 + static_cast<uint32_t>(r) * 128u + 16u * static_cast<uint32_t>((k >> 1) ^ (r & 7)) +
+                     8u * static_cast<uint32_t>(k & 1);
+  const uint2 xr = ld_shared_v2(a), yr = ld_shared_v2(a + box_stride);
+  const float x[4] = {bf16_lo(xr.x), bf16_hi(xr.x), bf16_lo(xr.y), bf16_hi(xr.y)};
+  const float y[4] = {bf16_lo(yr.x), bf16_hi(yr.x), bf16_lo(yr.y), bf16_hi(yr.y)};
+  const float g0[4] = {bf16_lo(gx.x), bf16_hi(gx.x), bf16_lo(gx.y), bf16_hi(gx.y)};
+  const float g1[4] = {bf16_lo(gy.x), bf16_hi(gy.x), bf16_lo(gy.y), bf16_hi(gy.y)};
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) ss = fmaf(y[i], y[i], fmaf(x[i], x[i], ss));
+#pragma unroll
+  for (int o = 1; o < 16; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  const float rn = rsqrtf(ss * (1.0f / HD) + eps);
+  float ox[4], oy[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float xs = x[i] * (rn * g0[i]);
+    const float ys = y[i] * (rn * g1[i]);
+    ox[i] = xs * cv[i] - ys * sv[i];
+    oy[i] = ys * cv[i] + xs * sv[i];
+  }
+  if (active) {
+    st_shared_v2(a, make_uint2(pack_bf16x2(ox[0], ox[1]), pack_bf16x2(ox[2], ox[3])));
+    st_shared_v2(a + box_stride, make_uint2(pack_bf16x2(oy[0], oy[1]), pack_bf16x2(oy[2], oy[3])));
+  }
+}
+
+// One work item's query rows (row h * bs + j of the pair: query head h of the
+// KV head at block position j) and, when with_keys, the block's keys (row j),
+// normalised and rotated in place by 128 threads: thread t takes positions
+// j = t / 16 (+ 8, ...) and part k = t % 16, so the sin and cos of a
+// (position, frequency) serve all G heads and the key at that position.
+__device__ __forceinline__ void prep_item_rows(uint32_t qbox0, uint32_t qbox_stride, bool with_keys, uint32_t kbox0,
+                                               int G, int bs,
+                                               int pos0, const unsigned long long* inv, const uint2 (&gq)[2],
+                                               const uint2 (&gk)[2], float eps, int t) {
+  const int k = t & 15;
+  for (int jb = 0; jb < bs; jb += 8) {  // uniform over the 128 threads
+    const int j = jb + (t >> 4);
+    const bool active = j < bs;
+    float cv[4], sv[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) rope_sincos(pos0 + j, inv[4 * k + i], &sv[i], &cv[i]);
+    for (int h = 0; h < G; ++h)
+      norm_rope_row_smem(qbox0, qbox_stride, active ? h * bs + j : 0, k, cv, sv, gq[0], gq[1], eps, active);
+    if (with_keys) norm_rope_row_smem(kbox0, kBlkBoxBytes, active ? j : 0, k, cv, sv, gk[0], gk[1], eps, active);
+  }
+}
+
 // Roles (c = NC/2 query rows per softmax warp):
 //   warps 0 .. 7       softmax: warp w owns key (lane) 32*(w%4) + lane of every
 //                      tile and query rows c*(w/4) .. +c-1
-//   warps 8 .. 11      epilogue: O^T lanes (dims) of lane quarter w%4
-//   warp 12            TMA producer (work queue, Q, K ring, V ring)
+//   warps 8 .. 11      epilogue: O^T lanes (dims) of lane quarter w%4; before
+//                      that, one item ahead, RMSNorm * gain and RoPE of the
+//                      item's query rows (and block keys) in shared memory
+//   warp 12            TMA producer (work queue, raw Q and block keys, K ring, V ring)
 //   warp 13            S^T = K Q^T issuer; allocates tensor memory
 //   warp 14            O^T += V^T P^T issuer
 template <int NC>
 __global__ void __launch_bounds__(TcCfg<NC>::kThreads, 1) attn_tc_kernel(const __grid_constant__ AttnMaps maps,
-                                                                         const AttnParams p, const TcLayout lay) {
+                                                                         const __grid_constant__ AttnParams p,
+                                                                         const TcLayout lay) {
   using C = TcCfg<NC>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -567,8 +700,11 @@ __global__ void __launch_bounds__(TcCfg<NC>::kThreads, 1) attn_tc_kernel(const _
   const uint32_t ml_full = o_free + 16, ml_empty = ml_full + 16;
   const uint32_t it_full = ml_empty + 16, it_empty = it_full + 8 * kItemRing;
   const uint32_t red_bar = it_empty + 8 * kItemRing;  // one per column half
+  const uint32_t qraw_full = red_bar + 16;             // per Q buffer: the raw rows landed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + lay.off_misc);
-  float* s_m = reinterpret_cast<float*>(gbase + lay.off_misc + 64);               // [2][NC]
+  unsigned long long* s_inv = reinterpret_cast<unsigned long long*>(gbase + lay.off_misc + 64);  // [64]
+  __nv_bfloat16* s_gain = reinterpret_cast<__nv_bfloat16*>(gbase + lay.off_misc + 576);          // [2][128]
+  float* s_m = reinterpret_cast<float*>(gbase + lay.off_misc + 1088);             // [2][NC]
   float* s_l = s_m + 2 * NC;                                                       // [2][4][NC]
   float* s_red = s_l + 2 * 4 * NC;                                                 // [2 halves][2][4][32]
   int* s_prefix = reinterpret_cast<int*>(s_red + 2 * 2 * 4 * 32);
@@ -588,8 +724,9 @@ __global__ void __launch_bounds__(TcCfg<NC>::kThreads, 1) attn_tc_kernel(const _
       mbar_init(s_empty + 8 * s, C::kSoftWarps);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(q_full + 8 * i, 1);
+      mbar_init(q_full + 8 * i, 4);   // the four epilogue warps, after normalising and rotating in place
       mbar_init(q_empty + 8 * i, 1);
+      mbar_init(qraw_full + 8 * i, 1);
       mbar_init(p_full + 8 * i, C::kSoftWarps);
       mbar_init(p_empty + 8 * i, 1);
       mbar_init(o_full + 8 * i, 1);
@@ -607,6 +744,12 @@ __global__ void __launch_bounds__(TcCfg<NC>::kThreads, 1) attn_tc_kernel(const _
   if (warp == C::kSWarp) {
     tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
     tmem_relinquish();
+  }
+  if (warp >= C::kEpiWarp0 && warp < C::kEpiWarp0 + 4) {  // the norm gains and RoPE frequencies
+    const int et = threadIdx.x - 32 * C::kEpiWarp0;
+    s_gain[et] = p.qg ? p.qg[et] : __float2bfloat16_rn(1.f);
+    s_gain[HD + et] = p.kg ? p.kg[et] : __float2bfloat16_rn(1.f);
+    if (et < HD / 2) s_inv[et] = p.inv.v[et];
   }
   if (warp == C::kProdWarp) {  // per-sequence lengths and the prefix of full (non-last) splits
     int carry = 0;
@@ -642,15 +785,24 @@ __global__ void __launch_bounds__(TcCfg<NC>::kThreads, 1) attn_tc_kernel(const _
       tma_prefetch_desc(&maps.k);
       tma_prefetch_desc(&maps.v);
       tma_prefetch_desc(&maps.q);
-      pdl_wait_primary();  // the prologue's Q, block keys and cleared counter
-      // Release the combine kernel only now: it trusts the per-pair counters,
-      // which the prologue has cleared by this point.
-      pdl_launch_dependents();
       const uint64_t pol = l2_policy_evict_first();
       Ring kr, vr, q, itr;
       bool ok = true;
+      // The first work item of each CTA is its own index: it needs no queue,
+      // so it starts before the counters are known to be cleared.
+      int w = static_cast<int>(blockIdx.x);
+      bool waited = false;
       while (ok) {
-        const int w = atomicAdd(p.counters, 1);
+        if (w < 0) {
+          if (!waited) {
+            pdl_wait_primary();  // the cleared counters
+            // Release the combine kernel only now: it trusts the per-pair
+            // counters, cleared by the preceding grid.
+            pdl_launch_dependents();
+            waited = true;
+          }
+          w = static_cast<int>(gridDim.x) + atomicAdd(p.counters, 1);
+        }
         Item it;
         it.b = -1;
         if (w < n_items) it = decode_item(w, s_prefix, s_n, p);
@@ -659,14 +811,22 @@ __global__ void __launch_bounds__(TcCfg<NC>::kThreads, 1) attn_tc_kernel(const _
         mbar_arrive(it_full + 8 * itr.idx);
         itr.next(kItemRing);
         if (w >= n_items) break;
+        w = -1;
+        // the pair's raw query rows (and, for the last split, the block's raw
+        // keys): the epilogue warps normalise and rotate them in place
         if (!(ok = mbar_wait(q_empty + 8 * q.idx, q.phase ^ 1u, p.status))) break;
-        mbar_arrive_expect_tx(q_full + 8 * q.idx, 2 * C::kQBoxBytes);
         const int qrow = (it.b * p.Hq + it.g * p.G) * p.bs;
-        const uint32_t qdst = base + lay.off_q + q.idx * 2 * C::kQBoxBytes;
-        tma_load_2d(qdst, &maps.q, q_full + 8 * q.idx, 0, qrow);
-        tma_load_2d(qdst + C::kQBoxBytes, &maps.q, q_full + 8 * q.idx, 64, qrow);
-        q.next(2);
         const int brow = (it.b * p.Hkv + it.g) * p.bs;
+        const uint32_t qdst = base + lay.off_q + q.idx * 2 * C::kQBoxBytes;
+        const uint32_t kbdst = base + lay.off_kb + q.idx * 2 * kBlkBoxBytes;
+        mbar_arrive_expect_tx(qraw_full + 8 * q.idx, 2 * C::kQBoxBytes + (it.last ? 2 * kBlkBoxBytes : 0));
+        tma_load_2d(qdst, &maps.q, qraw_full + 8 * q.idx, 0, qrow);
+        tma_load_2d(qdst + C::kQBoxBytes, &maps.q, qraw_full + 8 * q.idx, 64, qrow);
+        if (it.last) {
+          tma_load_2d(kbdst, &maps.kb, qraw_full + 8 * q.idx, 0, brow);
+          tma_load_2d(kbdst + kBlkBoxBytes, &maps.kb, qraw_full + 8 * q.idx, 64, brow);
+        }
+        q.next(2);
         // paged: the block-table entry of the next tile is requested one tile
         // ahead, so its latency hides behind this tile's ring waits (a key
         // tile never crosses a page: pages are multiples of 128 rows and tiles
@@ -691,17 +851,14 @@ __global__ void __launch_bounds__(TcCfg<NC>::kThreads, 1) attn_tc_kernel(const _
             }
           }
           page = next_page;
-          if (!(ok = mbar_wait(k_empty + 8 * kr.idx, kr.phase ^ 1u, p.status))) break;
-          const uint32_t kdst = base + lay.off_k + kr.idx * kHalfBytes;
-          mbar_arrive_expect_tx(k_full + 8 * kr.idx, bytes);
-          if (!blk) {
+          if (!blk) {  // the block's keys are not in the ring: the S product reads them from their own buffer
+            if (!(ok = mbar_wait(k_empty + 8 * kr.idx, kr.phase ^ 1u, p.status))) break;
+            const uint32_t kdst = base + lay.off_k + kr.idx * kHalfBytes;
+            mbar_arrive_expect_tx(k_full + 8 * kr.idx, bytes);
             tma_load_2d_hint(kdst, &maps.k, k_full + 8 * kr.idx, 0, y, pol);
             tma_load_2d_hint(kdst + kBoxBytes, &maps.k, k_full + 8 * kr.idx, 64, y, pol);
-          } else {
-            tma_load_2d(kdst, &maps.kb, k_full + 8 * kr.idx, 0, brow);
-            tma_load_2d(kdst + kBoxBytes, &maps.kb, k_full + 8 * kr.idx, 64, brow);
+            kr.next(NK);
           }
-          kr.next(NK);
           if (!(ok = mbar_wait(v_empty + 8 * vr.idx, vr.phase ^ 1u, p.status))) break;
           const uint32_t vdst = base + lay.off_v + vr.idx * kHalfBytes;
           mbar_arrive_expect_tx(v_full + 8 * vr.idx, bytes);
@@ -730,20 +887,24 @@ __global__ void __launch_bounds__(TcCfg<NC>::kThreads, 1) attn_tc_kernel(const _
         if (!(ok = mbar_wait(q_full + 8 * q.idx, q.phase, p.status))) break;
         const uint32_t qb = base + lay.off_q + q.idx * 2 * C::kQBoxBytes;
         for (int t = 0; t < it.nt && ok; ++t) {
-          if (!(ok = mbar_wait(k_full + 8 * kr.idx, kr.phase, p.status))) break;
+          const bool blk = t >= it.ntiles;  // the block's keys: their own buffer, ready with Q
+          if (!blk && !(ok = mbar_wait(k_full + 8 * kr.idx, kr.phase, p.status))) break;
           if (!(ok = mbar_wait(s_empty + 8 * sq.idx, sq.phase ^ 1u, p.status))) break;
           tc_fence_after_sync();
-          const uint32_t kb = base + lay.off_k + kr.idx * kHalfBytes;
+          const uint32_t kb = blk ? base + lay.off_kb + q.idx * 2 * kBlkBoxBytes : base + lay.off_k + kr.idx * kHalfBytes;
+          const uint32_t kbox = blk ? kBlkBoxBytes : kBoxBytes;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t ad = umma_desc_kmajor_sw128(kb + (kk >> 2) * kBoxBytes) + 2 * (kk & 3);
+            const uint64_t ad = umma_desc_kmajor_sw128(kb + (kk >> 2) * kbox) + 2 * (kk & 3);
             const uint64_t bd = umma_desc_kmajor_sw128(qb + (kk >> 2) * C::kQBoxBytes) + 2 * (kk & 3);
             umma_bf16(tmem + C::kColS + NC * sq.idx, ad, bd, C::kIdescS, kk > 0 ? 1u : 0u);
           }
           umma_commit(s_full + 8 * sq.idx);
-          umma_commit(k_empty + 8 * kr.idx);
+          if (!blk) {
+            umma_commit(k_empty + 8 * kr.idx);
+            kr.next(NK);
+          }
           sq.next(kSBufs);
-          kr.next(NK);
         }
         if (!ok) break;
         umma_commit(q_empty + 8 * q.idx);
@@ -909,7 +1070,10 @@ __global__ void __launch_bounds__(TcCfg<NC>::kThreads, 1) attn_tc_kernel(const _
       if (!ok) break;
       // a score beyond 2^64 above the running max: the combine kernel redoes
       // this (sequence, KV head) exactly
-      if (__any_sync(0xffffffffu, dmax > kOverflowLog2) && lane == 0) atomicOr(p.counters + 1 + it.b * p.Hkv + it.g, 1);
+      if (__any_sync(0xffffffffu, dmax > kOverflowLog2) && lane == 0) {
+        pdl_wait_primary();  // the cleared flags (the first work item may run ahead of the clearing)
+        atomicOr(p.counters + 1 + it.b * p.Hkv + it.g, 1);
+      }
       // row sums over this warp's keys -> the epilogue; the quarter-0 warps also
       // hand over the running max
       if (!(ok = mbar_wait(ml_empty + 8 * mlr.idx, mlr.phase ^ 1u, p.status))) break;
@@ -927,69 +1091,103 @@ __global__ void __launch_bounds__(TcCfg<NC>::kThreads, 1) attn_tc_kernel(const _
     }
   } else {
     // ------------------------------------------------ epilogue
+    // One item ahead of its epilogue, each work item's query rows (and, for a
+    // last split, the block's keys), loaded raw by the producer, get their
+    // RMSNorm * gain and RoPE in place in shared memory: Q of item i is made
+    // before the epilogue of item i - 1.
     const int qd = warp & 3;
     const int dim = 32 * qd + lane;
     const uint32_t tl = tmem + (static_cast<uint32_t>(32 * qd) << 16);
-    Ring orr, mlr, itr;
-    bool ok = true;
+    const int et = threadIdx.x - 32 * C::kEpiWarp0;  // 0 .. 127
+    // this thread's gains for its part of every head vector (elements 4k .. 4k+3, partners 64+4k ..)
+    const int gpart = 4 * (et & 15);
+    const uint2 gq[2] = {*reinterpret_cast<const uint2*>(s_gain + gpart),
+                         *reinterpret_cast<const uint2*>(s_gain + 64 + gpart)};
+    const uint2 gk[2] = {*reinterpret_cast<const uint2*>(s_gain + HD + gpart),
+                         *reinterpret_cast<const uint2*>(s_gain + HD + 64 + gpart)};
+    Ring orr, mlr, itr, qq;
+    bool ok = true, waited = false, have_prev = false;
+    Item prev;
     while (ok) {
       Item it;
-      if (!next_item(it_full, it_empty, s_items, itr, p.status, it)) break;
-      if (!(ok = mbar_wait(o_full + 8 * orr.idx, orr.phase, p.status))) break;
-      tc_fence_after_sync();
-      float o[NC];  // O^T lane `dim`: the hi and lo column blocks added
-#pragma unroll
-      for (int c = 0; c < NC / 32; ++c) {
-        uint32_t rh[32], rl[32];
-        tmem_ld_32cols(tl + C::kColO + 2 * NC * orr.idx + 32 * c, rh);
-        tmem_ld_32cols(tl + C::kColO + 2 * NC * orr.idx + NC + 32 * c, rl);
-        tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) o[32 * c + j] = __uint_as_float(rh[j]) + __uint_as_float(rl[j]);
+      const bool got = next_item(it_full, it_empty, s_items, itr, p.status, it);
+      if (got) {
+        if (!(ok = mbar_wait(qraw_full + 8 * qq.idx, qq.phase, p.status))) break;
+        const int n_in = p.seq_len[it.b];
+        // the block's positions follow the sequence: its length (a ring
+        // cache's may exceed the capacity), else the cached rows
+        const int pos0 = p.ring ? max(n_in, 0) : min(max(n_in, 0), p.cap);
+        prep_item_rows(base + lay.off_q + qq.idx * 2 * C::kQBoxBytes, C::kQBoxBytes, it.last,
+                       base + lay.off_kb + qq.idx * 2 * kBlkBoxBytes, p.G, p.bs, pos0, s_inv, gq, gk, p.eps, et);
+        fence_proxy_async_smem();  // the rows, for the tensor core's reads
+        __syncwarp();
+        if (lane == 0) mbar_arrive(q_full + 8 * qq.idx);
+        qq.next(2);
       }
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(o_free + 8 * orr.idx);
-      orr.next(2);
-      if (!(ok = mbar_wait(ml_full + 8 * mlr.idx, mlr.phase, p.status))) break;
-      // lane i: the sum and its reciprocal for rows i and 32 + i
-      const float* lrow = s_l + mlr.idx * 4 * NC;
-      float den[NC / 32], inv[NC / 32];
+      if (have_prev) {
+        if (!(ok = mbar_wait(o_full + 8 * orr.idx, orr.phase, p.status))) break;
+        tc_fence_after_sync();
+        float o[NC];  // O^T lane `dim`: the hi and lo column blocks added
 #pragma unroll
-      for (int c = 0; c < NC / 32; ++c) {
-        const int r = 32 * c + lane;
-        den[c] = lrow[r] + lrow[NC + r] + lrow[2 * NC + r] + lrow[3 * NC + r];
-        inv[c] = r < p.rows ? 1.f / den[c] : 0.f;
-      }
-      if (it.nsplit == 1) {
-        const size_t row0 = (static_cast<size_t>(it.b) * p.Hq + it.g * p.G) * p.bs;
+        for (int c = 0; c < NC / 32; ++c) {
+          uint32_t rh[32], rl[32];
+          tmem_ld_32cols(tl + C::kColO + 2 * NC * orr.idx + 32 * c, rh);
+          tmem_ld_32cols(tl + C::kColO + 2 * NC * orr.idx + NC + 32 * c, rl);
+          tmem_ld_wait();
 #pragma unroll
-        for (int r = 0; r < NC; ++r) {
-          const float iv = __shfl_sync(0xffffffffu, inv[r / 32], r % 32);
-          if (r < p.rows) p.out[(row0 + r) * HD + dim] = __float2bfloat16_rn(o[r] * iv);
+          for (int j = 0; j < 32; ++j) o[32 * c + j] = __uint_as_float(rh[j]) + __uint_as_float(rl[j]);
         }
-      } else {
-        const size_t r0 = ((static_cast<size_t>(it.b) * p.Hkv + it.g) * p.max_splits + it.s) * p.rows;
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(o_free + 8 * orr.idx);
+        orr.next(2);
+        if (!(ok = mbar_wait(ml_full + 8 * mlr.idx, mlr.phase, p.status))) break;
+        // lane i: the sum and its reciprocal for rows i and 32 + i
+        const float* lrow = s_l + mlr.idx * 4 * NC;
+        float den[NC / 32], inv[NC / 32];
 #pragma unroll
-        for (int r = 0; r < NC; ++r) {
-          const float iv = __shfl_sync(0xffffffffu, inv[r / 32], r % 32);
-          if (r < p.rows) p.opart[(r0 + r) * HD + dim] = o[r] * iv;
+        for (int c = 0; c < NC / 32; ++c) {
+          const int r = 32 * c + lane;
+          den[c] = lrow[r] + lrow[NC + r] + lrow[2 * NC + r] + lrow[3 * NC + r];
+          inv[c] = r < p.rows ? 1.f / den[c] : 0.f;
         }
-        if (qd == 0) {
+        if (prev.nsplit == 1) {
+          const size_t row0 = (static_cast<size_t>(prev.b) * p.Hq + prev.g * p.G) * p.bs;
 #pragma unroll
-          for (int c = 0; c < NC / 32; ++c) {
-            const int r = 32 * c + lane;
-            if (r < p.rows) p.mlpart[r0 + r] = make_float2(s_m[mlr.idx * NC + r], den[c]);
+          for (int r = 0; r < NC; ++r) {
+            const float iv = __shfl_sync(0xffffffffu, inv[r / 32], r % 32);
+            if (r < p.rows) p.out[(row0 + r) * HD + dim] = __float2bfloat16_rn(o[r] * iv);
+          }
+        } else {
+          const size_t r0 = ((static_cast<size_t>(prev.b) * p.Hkv + prev.g) * p.max_splits + prev.s) * p.rows;
+#pragma unroll
+          for (int r = 0; r < NC; ++r) {
+            const float iv = __shfl_sync(0xffffffffu, inv[r / 32], r % 32);
+            if (r < p.rows) p.opart[(r0 + r) * HD + dim] = o[r] * iv;
+          }
+          if (qd == 0) {
+#pragma unroll
+            for (int c = 0; c < NC / 32; ++c) {
+              const int r = 32 * c + lane;
+              if (r < p.rows) p.mlpart[r0 + r] = make_float2(s_m[mlr.idx * NC + r], den[c]);
+            }
           }
         }
+        __threadfence();  // this warp's output / partial before the pair's completion count
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(ml_empty + 8 * mlr.idx);
+          if (!waited) {
+            pdl_wait_primary();  // the cleared pair counts (the first item may run ahead of the clearing)
+            waited = true;
+          }
+          atomicAdd(p.counters + 1 + p.B * p.Hkv + prev.b * p.Hkv + prev.g, 1);
+        }
+        mlr.next(2);
       }
-      __threadfence();  // this warp's output / partial before the pair's completion count
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(ml_empty + 8 * mlr.idx);
-        atomicAdd(p.counters + 1 + p.B * p.Hkv + it.b * p.Hkv + it.g, 1);
-      }
-      mlr.next(2);
+      if (!got) break;
+      prev = it;
+      have_prev = true;
     }
   }
   tc_fence_before_sync();
@@ -1111,9 +1309,10 @@ size_t attn_ws_bytes(int B, int bs, int Hq, int Hkv, int cap, int window, dflash
   const int chunk = pick_chunk(B, Hkv, cap, window);
   const int keys = window > 0 ? std::min(window, cap) : cap;
   const int max_splits = n_splits(keys, chunk);
-  size_t s = align256(static_cast<size_t>(B) * Hq * bs * HD * esz) +
-             align256(static_cast<size_t>(B) * Hkv * bs * HD * esz);
-  if (dt == DFLASH_BF16)
+  size_t s = 0;
+  if (dt != DFLASH_BF16)  // the fp32 prologue's q^ and k^_b (the bf16 path makes them in shared memory)
+    s += align256(static_cast<size_t>(B) * Hq * bs * HD * esz) + align256(static_cast<size_t>(B) * Hkv * bs * HD * esz);
+  else
     s += align256(static_cast<size_t>(B) * Hkv * max_splits * rows * HD * sizeof(float)) +
          align256(static_cast<size_t>(B) * Hkv * max_splits * rows * sizeof(float2)) +
          align256((1 + 2 * static_cast<size_t>(B) * Hkv) * sizeof(int));
@@ -1163,10 +1362,12 @@ dflash_status launch_block_attn(int layer, int B, int bs, int Hq, const void* q,
   p.max_splits = n_splits(keys, p.chunk);
   p.rows = G * bs;
   p.seq_len = c.seq_len;
-  auto* qh = w.take<__nv_bfloat16>(static_cast<size_t>(B) * Hq * bs * HD);
-  auto* kbh = w.take<__nv_bfloat16>(static_cast<size_t>(B) * Hkv * bs * HD);
-  p.qh = qh;
-  p.kbh = kbh;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.kb = static_cast<const __nv_bfloat16*>(kb);
+  p.qg = static_cast<const __nv_bfloat16*>(qg);
+  p.kg = static_cast<const __nv_bfloat16*>(kg);
+  p.eps = eps;
+  p.inv = inv;
   p.vb = static_cast<const __nv_bfloat16*>(vb);
   p.out = static_cast<__nv_bfloat16*>(out);
   p.opart = w.take<float>(static_cast<size_t>(B) * Hkv * p.max_splits * p.rows * HD);
@@ -1188,27 +1389,25 @@ dflash_status launch_block_attn(int layer, int B, int bs, int Hq, const void* q,
                                       : static_cast<uint64_t>(c.num_layers) * c.batch * Hkv * c.capacity;
   dflash_status s = make_tmap_bf16_2d(&maps.k, c.k, rows, HD, kKeys, 64);
   if (!s) s = make_tmap_bf16_2d(&maps.v, c.v, rows, HD, kKeys, 64);
-  if (!s) s = make_tmap_bf16_2d(&maps.q, qh, static_cast<uint64_t>(B) * Hq * bs, HD, nc, 64);
-  if (!s) s = make_tmap_bf16_2d(&maps.kb, kbh, static_cast<uint64_t>(B) * Hkv * bs, HD, kBlockBoxRows, 64);
+  if (!s) s = make_tmap_bf16_2d(&maps.q, q, static_cast<uint64_t>(B) * Hq * bs, HD, nc, 64);
+  if (!s) s = make_tmap_bf16_2d(&maps.kb, kb, static_cast<uint64_t>(B) * Hkv * bs, HD, kBlockBoxRows, 64);
   if (!s) s = make_tmap_bf16_2d(&maps.vb, vb, static_cast<uint64_t>(B) * Hkv * bs, HD, kBlockBoxRows, 64);
   if (s) return s;
 
-  {
+  {  // one CTA clears the counters; the main kernel's first items run meanwhile
     cudaLaunchConfig_t pc = {};
-    pc.gridDim = dim3(static_cast<unsigned>(B * bs));
-    pc.blockDim = dim3(kPrologueThreads);
+    pc.gridDim = dim3(1);
+    pc.blockDim = dim3(1024);
     pc.stream = st;
     cudaLaunchAttribute pa[1];
     pa[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pa[0].val.programmaticStreamSerializationAllowed = 1;
     pc.attrs = pa;
     pc.numAttrs = 1;
-    cudaError_t le = cudaLaunchKernelEx(&pc, attn_prologue_kernel<__nv_bfloat16>,
-                                        static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(kb),
-                                        static_cast<const __nv_bfloat16*>(qg), static_cast<const __nv_bfloat16*>(kg),
-                                        c.seq_len, B, bs, Hq, Hkv, c.capacity, c.ring, eps, inv, qh, kbh, p.counters,
-                                        1 + 2 * B * Hkv, dev.status);
-    if (le != cudaSuccess) return cuda_fail(le, "attn_prologue_kernel launch");
+    cudaError_t le = cudaLaunchKernelEx(&pc, attn_clear_kernel, p.counters, 1 + 2 * B * Hkv,
+                                        static_cast<const uint8_t*>(q), static_cast<size_t>(B) * Hq * bs * HD * 2,
+                                        static_cast<const uint8_t*>(kb), static_cast<size_t>(B) * Hkv * bs * HD * 2);
+    if (le != cudaSuccess) return cuda_fail(le, "attn_clear_kernel launch");
   }
 
   const TcLayout lay = tc_layout(nc, B, static_cast<int>(dev.max_smem_optin));
@@ -1274,8 +1473,6 @@ dflash_status launch_attn_wait_timeout_probe(int B, int bs, int Hq, const dflash
   p.rows = p.G * bs;
   p.seq_len = c.seq_len;
   WsCarver w(ws);
-  w.take<__nv_bfloat16>(static_cast<size_t>(B) * Hq * bs * HD);
-  w.take<__nv_bfloat16>(static_cast<size_t>(B) * Hkv * bs * HD);
   p.out = static_cast<__nv_bfloat16*>(out);
   p.opart = w.take<float>(static_cast<size_t>(B) * Hkv * p.max_splits * p.rows * HD);
   p.mlpart = w.take<float2>(static_cast<size_t>(B) * Hkv * p.max_splits * p.rows);
