@@ -85,6 +85,21 @@ def test_block_attn_scores_far_above_the_first_tile_stay_exact():
     assert_close(out, ref, torch.bfloat16, row=128, what="out")
 
 
+@pytest.mark.parametrize("Hq,Hkv,bs", [(4, 4, 16), (8, 8, 1), (12, 4, 5), (16, 2, 3), (32, 2, 4)])
+def test_block_attn_head_groupings(Hq, Hkv, bs):
+    """Query heads per KV head G = 1, 3, 8 and 16 (32 and 64 query rows per
+    pair): the main kernel normalises and rotates each block position's G
+    query rows and its block key together; an empty cache, a ragged length
+    and several tiles."""
+    seq = [0, 130, 700]
+    cap = 768
+    k, v, q, kb, vb, qg, kg = _inputs(3, bs, cap, torch.bfloat16, seed=Hq * 31 + Hkv * 7 + bs, Hq=Hq, Hkv=Hkv)
+    cache = dfl.KVCache(k.to(DEV), v.to(DEV), torch.tensor(seq, dtype=torch.int32, device=DEV))
+    out = dfl.block_attn(1, q.to(DEV), kb.to(DEV), vb.to(DEV), qg.to(DEV), kg.to(DEV), cache)
+    ref = _oracle(q, kb, vb, qg, kg, k[1], v[1], seq, 0, torch.bfloat16)
+    assert_close(out, ref, torch.bfloat16, row=128, what="out")
+
+
 def test_block_attn_fp32_tiny_case():
     cfg = workloads.TINY_FP32
     k, v, q, kb, vb, qg, kg = _inputs(2, cfg.bs, 128, torch.float32, seed=1, layers=1)

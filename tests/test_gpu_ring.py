@@ -71,6 +71,35 @@ def test_block_attn_over_a_ring_equals_the_window_of_a_linear_cache(bs):
     assert dfl.read_device_status() == 0
 
 
+def test_ring_scores_far_above_the_first_tile_take_the_exact_path():
+    """A key scoring far above its item's first tile, in a ring whose
+    sequences are longer than the ring: the combine kernel redoes the pair key
+    by key, with the block at positions seq_len + j (past the ring's
+    capacity), and both the ring and the linear window match the oracle."""
+    W = 256
+    steps = [[150, 90, 256], [150, 200, 1], [150, 5, 256], [150, 256, 0], [120, 0, 3]]
+    cfg, w, lin, ring = _filled_caches(W, steps, seed=41)
+    n = lin.seq_len.cpu().tolist()
+    assert n[0] > W
+    p = n[0] - 1                    # latest position: the second key tile of both layouts
+    assert p % W >= 128 and p >= n[0] - 128
+    g = torch.Generator().manual_seed(42)
+    big = (200.0 * torch.randn(128, generator=g)).to(torch.bfloat16).to(DEV)
+    lin.k[1, 0, 5, p] = big
+    ring.k[1, 0, 5, p % W] = big
+    q, kb, vb = workloads.block(cfg, DEV, layer=1)
+    dfl.read_device_status()
+    out_lin = dfl.block_attn(1, q, kb, vb, w.q_gain[1], w.k_gain[1], lin, window=W)
+    out_ring = dfl.block_attn(1, q, kb, vb, w.q_gain[1], w.k_gain[1], ring)
+    assert dfl.read_device_status() == 0
+    seq = lin.seq_len.cpu().numpy()
+    ref = oracle.block_attn(np64(q), np64(kb), np64(vb), np64(w.q_gain[1]), np64(w.k_gain[1]), np64(lin.k[1]),
+                            np64(lin.v[1]), seq, window=W, bf16=True)
+    for out in (out_lin, out_ring):
+        assert torch.isfinite(out.float()).all()
+        assert_close(out, ref, torch.bfloat16, row=128, what="out")
+
+
 def test_ring_fusion_of_more_rows_than_the_ring_is_flagged_and_skipped():
     """One call may add at most W rows to a sequence of a W-row ring; more is
     flagged on the device and that sequence's rows are skipped (the host only
