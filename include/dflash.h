@@ -184,6 +184,8 @@ DFLASH_API dflash_status dflash_fuse_context(int num_taps, const void* const* ta
  *  batch, block_size, num_q_heads : B, bs (1..16), Hq (Hq % Hkv == 0,
  *                 Hq/Hkv * bs <= 64)
  *  q            : [B, Hq, bs, 128]    kb, vb : [B, Hkv, bs, 128]
+ *                 (q, kb, vb and out 16-byte aligned: the rows are loaded
+ *                 and stored in bulk; else status 1 and nothing enqueued)
  *  q_gain, k_gain: [128] this layer's norm gains (NULL = ones)
  *  window       : 0 = the whole cached context, else the latest `window`
  *                 cached positions
@@ -192,6 +194,8 @@ DFLASH_API dflash_status dflash_fuse_context(int num_taps, const void* const* ta
  *                 keys = cache[layer][b][h/(Hq/Hkv)][lo..seq_len[b]) ++
  *                 RoPE(RMSNorm(kb) * k_gain).
  * bf16 rounding points: q^ and the block keys (before the products) and out.
+ * The workspace holds the split partials and the call's counters (cleared by
+ * the call itself): two calls in flight at once need two workspaces.
  * ------------------------------------------------------------------------- */
 DFLASH_API size_t dflash_block_attn_workspace_size(int batch, int block_size, int num_q_heads,
                                         int num_kv_heads, int capacity, int window,
