@@ -261,7 +261,8 @@ __host__ __device__ __forceinline__ int split_start(int s, int nsplit, int ncach
 // split, then the last split of every (b, g), which also carries the block
 // keys.  The splits of a sequence are near-equal, so the dynamic queue keeps
 // the tail short.
-__device__ __forceinline__ Item decode_item(int w, const int* s_full_prefix, const int* s_n, const AttnParams& p) {
+__device__ __forceinline__ Item decode_item(int w, const int* s_full_prefix, const int* s_n, const int* s_multi,
+                                            const AttnParams& p) {
   Item it;
   const int F = s_full_prefix[p.B];
   int b, g, s;
@@ -277,8 +278,20 @@ __device__ __forceinline__ Item decode_item(int w, const int* s_full_prefix, con
     g = r / nfull;
     s = r % nfull;
   } else {
-    b = (w - F) / p.Hkv;
-    g = (w - F) % p.Hkv;
+    // last splits: those of sequences with several splits first (their merges
+    // can then finish before the queue's end), then the one-split sequences
+    const int M = s_multi[p.B];
+    const int wl = w - F;
+    const bool multi = wl < M * p.Hkv;
+    const int idx = multi ? wl / p.Hkv : (wl - M * p.Hkv) / p.Hkv;
+    g = wl % p.Hkv;
+    int lo = 0, hi = p.B - 1;
+    while (lo < hi) {  // largest b whose count of earlier multi (or one-split) sequences is <= idx
+      const int mid = (lo + hi + 1) >> 1;
+      const int before = multi ? s_multi[mid] : mid - s_multi[mid];
+      if (before <= idx) lo = mid; else hi = mid - 1;
+    }
+    b = lo;
     s = -1;
   }
   const int n = s_n[b];
@@ -340,7 +353,7 @@ __host__ __device__ inline int tc_misc_bytes(int B, int nc) {
   // tmem slot (64) | RoPE turns per position [64] (u64) | gains [2][128] (bf16) |
   // s_m [2][NC] | s_l [2][4][NC] | s_red [2 halves][2][4][32] |
   // prefix [B+1], n [B] | decoded item ring [kItemRing]
-  return 64 + 512 + 512 + 2 * nc * 4 + 2 * 4 * nc * 4 + 2 * 2 * 4 * 32 * 4 + (2 * B + 1) * 4 +
+  return 64 + 512 + 512 + 2 * nc * 4 + 2 * 4 * nc * 4 + 2 * 2 * 4 * 32 * 4 + (3 * B + 2) * 4 +
          kItemRing * static_cast<int>(sizeof(Item));
 }
 
@@ -709,7 +722,8 @@ __global__ void __launch_bounds__(TcCfg<NC>::kThreads, 1) attn_tc_kernel(const _
   float* s_red = s_l + 2 * 4 * NC;                                                 // [2 halves][2][4][32]
   int* s_prefix = reinterpret_cast<int*>(s_red + 2 * 2 * 4 * 32);
   int* s_n = s_prefix + (p.B + 1);
-  Item* s_items = reinterpret_cast<Item*>(s_n + p.B);                              // kItemRing entries
+  int* s_multi = s_n + p.B;                                                        // [B+1]
+  Item* s_items = reinterpret_cast<Item*>(s_multi + p.B + 1);                              // kItemRing entries
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
@@ -752,7 +766,7 @@ __global__ void __launch_bounds__(TcCfg<NC>::kThreads, 1) attn_tc_kernel(const _
     if (et < HD / 2) s_inv[et] = p.inv.v[et];
   }
   if (warp == C::kProdWarp) {  // per-sequence lengths and the prefix of full (non-last) splits
-    int carry = 0;
+    int carry = 0, mcarry = 0;
     for (int b0 = 0; b0 < p.B; b0 += 32) {  // a warp scan per 32 sequences
       const int b = b0 + lane;
       int cnt = 0;
@@ -762,16 +776,24 @@ __global__ void __launch_bounds__(TcCfg<NC>::kThreads, 1) attn_tc_kernel(const _
         const int first = p.window > 0 ? max(0, n - p.window) : 0;
         cnt = (n_splits(n - first, p.chunk) - 1) * p.Hkv;
       }
+      const unsigned mb = __ballot_sync(0xffffffffu, cnt > 0);  // sequences of several splits
       int inc = cnt;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int u = __shfl_up_sync(0xffffffffu, inc, o);
         if (lane >= o) inc += u;
       }
-      if (b < p.B) s_prefix[b] = carry + inc - cnt;
+      if (b < p.B) {
+        s_prefix[b] = carry + inc - cnt;
+        s_multi[b] = mcarry + __popc(mb & ((1u << lane) - 1u));
+      }
       carry += __shfl_sync(0xffffffffu, inc, 31);
+      mcarry += __popc(mb);
     }
-    if (lane == 0) s_prefix[p.B] = carry;
+    if (lane == 0) {
+      s_prefix[p.B] = carry;
+      s_multi[p.B] = mcarry;
+    }
   }
   tc_fence_before_sync();
   __syncthreads();
@@ -805,7 +827,7 @@ __global__ void __launch_bounds__(TcCfg<NC>::kThreads, 1) attn_tc_kernel(const _
         }
         Item it;
         it.b = -1;
-        if (w < n_items) it = decode_item(w, s_prefix, s_n, p);
+        if (w < n_items) it = decode_item(w, s_prefix, s_n, s_multi, p);
         if (!(ok = mbar_wait(it_empty + 8 * itr.idx, itr.phase ^ 1u, p.status))) break;
         s_items[itr.idx] = it;  // decoded once here, read by every role
         mbar_arrive(it_full + 8 * itr.idx);
